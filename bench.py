@@ -1,0 +1,427 @@
+"""Benchmark of one EAGLE-2 draft-tree verification step on GB300.
+
+A step is the whole hot path over one batch of synthetic inputs that are
+already resident in HBM: D x et_tree_expand, et_tree_rerank,
+et_tree_mask_posids, et_tree_attention, et_verify_accept.  Steps are replayed
+from CUDA graphs over R rotating input sets whose combined footprint is
+larger than L2, so every step reads its logits and KV from HBM.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+instead (the only other implementation of this path), on a bounded sample.
+
+Multi-GPU: each rank is an independent replica on its own GPU with its own
+sequences (the step has no exchange), so scaling is weak and there is no
+collective in the data path; a barrier and a max-over-ranks of the timed
+region are the only communication.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 1024 * 1024
+DEFAULT_WORKLOAD = "llama2-7b"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1900.0)), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes
+# ---------------------------------------------------------------------------
+def attention_bytes(wl, prefix_lens):
+    """Bytes one et_tree_attention launch must move: KV prefix + tree K/V + Q + O."""
+    el = 2 if wl.dtype == "bf16" else 4
+    kv = sum(2 * wl.Hkv * int(L) * wl.d * el for L in prefix_lens)
+    B = len(prefix_lens)
+    tree = 2 * B * wl.N * wl.Hkv * wl.d * el
+    qo = 2 * B * wl.N * wl.Hq * wl.d * el
+    return kv + tree + qo
+
+
+def step_bytes(wl, cfg, prefix_lens, expanded_rows):
+    """Bytes a step reads from its inputs: expanded draft rows, the N target rows and the attention bytes."""
+    B = len(prefix_lens)
+    return B * (expanded_rows + wl.N) * wl.V * 4 + attention_bytes(wl, prefix_lens)
+
+
+# ---------------------------------------------------------------------------
+# clocks sampling (nvidia-smi during the timed region)
+# ---------------------------------------------------------------------------
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = open(os.devnull if not os.path.isdir(os.path.join(ROOT, "gpurun_out")) else
+                            os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv"), "w+")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+            if self.out:
+                self.out.write("\n".join(self.lines) + "\n")
+        if self.out:
+            self.out.close()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample
+# ---------------------------------------------------------------------------
+ORACLE_SNIPPET = r"""
+import json, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+import oracle as O
+from speculative_decoding_eagle_gb300 import workloads as W
+wl = W.WORKLOADS[{name!r}].with_(B=1)
+cfg = O.TreeCfg(B=1, V=wl.V, depth=wl.depth, topk=wl.topk, m=wl.m, n=wl.n, temperature=wl.temperature)
+C = O.num_candidates(cfg)
+budget = {budget}
+done, spent, parts = 0, 0.0, {{}}
+b = 0
+while spent < budget and done < {max_steps}:
+    target, draft, rmap = W.logit_tables(wl, C, batch=range(b, b + 1))
+    L = int(W.prefix_lengths(wl, b + 1)[b])
+    x = W.qkv(wl, b, L)
+    u = W.uniforms(wl, b)[None]
+    root = W.root_tokens(wl, b + 1)[b:b + 1]
+    t0 = time.perf_counter()
+    tree = O.build_tree(cfg, draft, rmap, root)
+    t1 = time.perf_counter()
+    mask, pos = O.mask_posids(tree.flat_parent, tree.flat_depth, np.array([L]))
+    q = W.as_float(wl, x["q"])[None].astype(np.float64)
+    kp = [W.as_float(wl, x["k_prefix"]).astype(np.float64)]
+    vp = [W.as_float(wl, x["v_prefix"]).astype(np.float64)]
+    kt = W.as_float(wl, x["k_tree"])[None].astype(np.float64)
+    vt = W.as_float(wl, x["v_tree"])[None].astype(np.float64)
+    t2 = time.perf_counter()
+    O.tree_attention(q, kp, vp, kt, vt, mask, wl.d ** -0.5)
+    t3 = time.perf_counter()
+    mode = O.GREEDY if "greedy" in wl.accept else O.STOCH_POINT
+    O.verify_accept(cfg, mode, tree.flat_tok, tree.flat_parent, tree.flat_node, target, rmap, uniforms=u)
+    t4 = time.perf_counter()
+    spent += (t1 - t0) + (t3 - t2) + (t4 - t3) + (t2 - t1)
+    for k, v in (("tree", t1 - t0), ("mask_conv", t2 - t1), ("attention", t3 - t2), ("accept", t4 - t3)):
+        parts[k] = parts.get(k, 0.0) + v
+    done += 1
+    b += 1
+print(json.dumps({{"steps": done, "seconds": spent, "parts": parts}}))
+"""
+
+
+def oracle_baseline(name, budget_s=12.0, max_steps=40):
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[k] = "1"
+    code = ORACLE_SNIPPET.format(root=ROOT, name=name, budget=budget_s, max_steps=max_steps)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError("oracle baseline failed:\n" + r.stderr[-2000:])
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": d["steps"] / d["seconds"], "unit": "steps/s", "cores": 1, "kind": "oracle",
+            "sample": f"{d['steps']} full steps of the {name} workload (batch 1, fresh seeded inputs each), "
+                      f"fp64 numpy, 1 BLAS thread; input generation untimed",
+            "seconds": round(d["seconds"], 3), "parts_s": {k: round(v, 3) for k, v in d["parts"].items()}}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from speculative_decoding_eagle_gb300 import binding as E
+    from speculative_decoding_eagle_gb300 import build_lib
+    from speculative_decoding_eagle_gb300 import step as S
+    from speculative_decoding_eagle_gb300 import workloads as W
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if rank == 0 or world == 1:
+        build_lib.build()
+    if world > 1:
+        dist.barrier()
+    E.load()
+    wl = W.WORKLOADS[args.workload]
+    if args.batch:
+        wl = wl.with_(B=args.batch)
+    mode = None if args.mode == "auto" else {"greedy": E.ET_ACCEPT_GREEDY, "stoch": E.ET_ACCEPT_STOCH_POINT,
+                                              "draftq": E.ET_ACCEPT_STOCH_DRAFTQ}[args.mode]
+    st = S.VerifyStep(wl, mode=mode, num_splits=args.splits)
+    cfg = st.cfg
+    prefix = W.prefix_lengths(wl, cfg.B)
+    expanded = sum(E.et_layer_expanded(cfg, l) for l in range(cfg.depth))
+    per_step = step_bytes(wl, cfg, prefix, expanded)
+    R = args.sets or max(2, int(np.ceil(2 * L2_BYTES / per_step)) + 1)
+    # rank r's sequences are disjoint from every other rank's (weak scaling)
+    sets = []
+    for r in range(R):
+        b0 = (rank * R + r) * cfg.B
+        sets.append(S.to_device(wl, S.host_inputs(wl, st.C, cfg.B, b0=b0)))
+    st.prepare(sets[0])
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.Stream()
+    # eager warm-up on a side stream, then one graph per input set
+    with torch.cuda.stream(stream):
+        for r in range(R):
+            st.run(sets[r], stream=stream)
+    stream.synchronize()
+    graphs = []
+    if not args.eager:
+        for r in range(R):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                st.run(sets[r], stream=stream)
+            graphs.append(g)
+    torch.cuda.synchronize()
+
+    def one_step(i):
+        if graphs:
+            graphs[i % R].replay()
+        else:
+            with torch.cuda.stream(stream):
+                st.run(sets[i % R], stream=stream)
+
+    for i in range(args.warmup):
+        one_step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream()
+    with Clocks(local) as clk:
+        t_wall = time.perf_counter()
+        ev0.record(cur)
+        for i in range(args.steps):
+            one_step(i)
+        ev1.record(cur)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    step_ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        t = torch.tensor([step_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    steps_per_s = world * 1000.0 / step_ms
+
+    # ---- attention alone: a graph of K launches over the rotating sets ----
+    K = max(8, min(200, args.steps))
+    ga = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for r in range(R):
+            st.attention(sets[r], stream=stream)
+    stream.synchronize()
+    with torch.cuda.graph(ga, stream=stream):
+        for i in range(K):
+            st.attention(sets[i % R], stream=stream)
+    ga.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    ga.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    attn_us = e0.elapsed_time(e1) * 1000.0 / K
+    attn_b = attention_bytes(wl, prefix)
+    hbm_peak, bf16_peak, peak_src = _peaks()
+    achieved = attn_b / (attn_us * 1e-6) / 1e9
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = run_e2e(args, st, sets, wl, stream)
+
+    launches = st.launches() * args.steps
+    out = {
+        "metric": "tree-verify steps/s (1 GB300, batch 1) with tree-attention HBM GB/s",
+        "value": round(steps_per_s, 2), "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 attention (fp32 accumulate), fp32 logits" if wl.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded Zipf target logits, noisy draft logits, N(0,1) Q/K/V)",
+        "config": {"workload": wl.name, "batch": cfg.B, "V": wl.V, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+                   "prefix": int(prefix.max()), "depth": wl.depth, "topk": wl.topk, "m": wl.m, "n": wl.n,
+                   "accept": {0: "greedy", 1: "stoch_point", 2: "stoch_draftq"}[st.mode],
+                   "attention_splits": E.et_tree_attention_splits(st.shape),
+                   "l2": f"inputs larger than L2: {R} rotating input sets, {per_step / 1e6:.1f} MB read per step",
+                   "cuda_graphs": bool(graphs), "parallelism": f"replicas x{world}"},
+        "tree_attention": {"us_per_launch": round(attn_us, 3), "GBps": round(achieved, 1),
+                           "pct_of_8TBps": round(100 * achieved / 8000.0, 2), "bytes": attn_b},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": args.traffic,
+                     "peak_source": peak_src, "kernel": "et_tree_attention"},
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        try:
+            out["cpu_baseline"] = oracle_baseline(wl.name)
+        except Exception as ex:  # report, never hide
+            out["cpu_baseline"] = {"error": str(ex)[:300]}
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_e2e(args, st, sets, wl, stream):
+    """Steps through the public API with the inputs in pinned host memory:
+    H2D of every input, the step, D2H of accept_len/path/tokens."""
+    import torch
+    names = ("draft", "target", "row_of_node", "root_tok", "prefix_len", "kv_row0", "q", "k_prefix", "v_prefix",
+             "k_tree", "v_tree", "uniforms")
+    R = min(len(sets), 2)
+    host = [{n: getattr(sets[r], n).cpu().pin_memory() for n in names} for r in range(R)]
+    dev = sets[0]
+    outs = [st.accept_len, st.path, st.tokens]
+    host_out = [t.cpu().pin_memory() for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host[0].values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    K = max(3, min(20, args.steps))
+
+    def one(i):
+        with torch.cuda.stream(stream):
+            for n in names:
+                getattr(dev, n).copy_(host[i % R][n], non_blocking=True)
+            st.run(dev, stream=stream)
+            for d, hh in zip(outs, host_out):
+                hh.copy_(d, non_blocking=True)
+        stream.synchronize()
+
+    for i in range(2):
+        one(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        one(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    ms = max(e0.elapsed_time(e1), wall * 1000.0) / K
+    return {"value": round(1000.0 / ms, 2), "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 4), "steps": K}
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    from speculative_decoding_eagle_gb300 import workloads as W
+    wl = W.WORKLOADS[args.workload]
+    times = []
+    base = None
+    for i in range(args.warmup + args.steps):
+        r = oracle_baseline(wl.name, budget_s=max(1.0, 20.0 / max(1, args.steps + args.warmup)), max_steps=2)
+        if i >= args.warmup:
+            times.append(1.0 / r["value"])
+            base = r
+    v = len(times) / sum(times)
+    out = {"impl": "reference", "metric": "tree-verify steps/s (1 GB300, batch 1) with tree-attention HBM GB/s",
+           "value": round(v, 4), "unit": "steps/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(1000.0 / v, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "f64", "data": "synthetic (seeded)", "config": {"workload": wl.name, "batch": 1},
+           "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": base["sample"] if base else "",
+                            "value": round(v, 4)},
+           "e2e": {"value": round(v, 4), "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--batch", type=int, default=0)
+    ap.add_argument("--mode", default="auto", choices=["auto", "greedy", "stoch", "draftq"])
+    ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--sets", type=int, default=0)
+    ap.add_argument("--eager", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes per attention launch from an ncu capture of the same kernel")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,266 @@
+/*
+ * eagle_tree.h -- C ABI of the GB300 (sm_103a) EAGLE-2 draft-tree
+ * verification step.
+ *
+ * One verification step, as the EAGLE-2 article (sbmmt.com, "Up to 5x
+ * lossless acceleration: EAGLE-2 lets an RTX 3060 generate faster than an
+ * A100") describes it, is:
+ *
+ *   for layer = 0 .. depth-1:  et_tree_expand      (expansion phase)
+ *   et_tree_rerank                                  (reranking phase, flatten)
+ *   et_tree_mask_posids                             (attention mask, positions)
+ *   et_tree_attention  (inside each target layer)   (ancestor-masked attention)
+ *   et_verify_accept                                (lossless acceptance)
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer argument that names a tensor is a DEVICE pointer unless the
+ *   comment says "host".  The caller owns every buffer; the library allocates
+ *   nothing, keeps no pointer after a call returns, and never synchronises.
+ * - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t; 0
+ *   is the legacy default stream).  They do no host<->device copies, so they
+ *   can be captured in a CUDA graph.
+ * - Shapes and limits are checked on the host before any launch; a bad
+ *   argument returns ET_ERR_INVALID_ARG / ET_ERR_UNSUPPORTED and launches
+ *   nothing.  A failed launch returns ET_ERR_CUDA (cudaGetLastError is
+ *   consumed).
+ * - Problems only the device can see (non-finite logits, an index outside
+ *   its table) are OR-ed as ET_DEV_* bits into `dev_status` (a device int32,
+ *   nullable).  Kernels never trap.
+ * - Workspaces: calls that take `ws` need `ws_bytes` >= the matching
+ *   *_workspace_size() and a 256-byte aligned `ws` that was zero-filled once
+ *   before its first use (et_workspace_init does that).  Each call leaves
+ *   the counters it uses at zero again.  One workspace must not be used by
+ *   two calls that can run at the same time (e.g. on two streams).
+ * - Layout names: B sequences, V vocabulary, D depth, k top-k, m frontier,
+ *   n kept nodes, N = n + 1 flat rows (row 0 = the root), C candidates
+ *   (et_num_candidates), Hq/Hkv query/KV heads, d head dim, W = ceil(N/64).
+ */
+#ifndef EAGLE_TREE_H
+#define EAGLE_TREE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                       /* = cudaStream_t's pointee */
+typedef struct CUstream_st *et_stream_t;
+
+#define ET_ABI_VERSION 1
+
+typedef enum {
+    ET_OK = 0,
+    ET_ERR_INVALID_ARG = 1,   /* null pointer, shape out of range, misalignment */
+    ET_ERR_UNSUPPORTED = 2,   /* valid but not built (e.g. head dim other than 64/128) */
+    ET_ERR_WORKSPACE = 3,     /* ws null, misaligned or smaller than required */
+    ET_ERR_CUDA = 4,          /* a CUDA launch or runtime call failed */
+    ET_ERR_TIMEOUT = 5        /* a bounded device wait gave up (reported through dev_status) */
+} et_status;
+
+/* bits OR-ed into *dev_status by kernels */
+#define ET_DEV_NONFINITE   1  /* NaN (counted as -inf) or +inf (counted as FLT_MAX) in logits */
+#define ET_DEV_BAD_INDEX   2  /* a node / row / token index outside its table; the entry is skipped */
+#define ET_DEV_DISCONNECTED 4 /* rerank found a kept node whose parent is not kept (cannot happen
+                                 for keys produced by et_tree_expand) */
+#define ET_DEV_TIMEOUT     8  /* a bounded wait inside a kernel gave up */
+
+/* Tree shape.  Limits: 1 <= topk <= 32, 1 <= m <= 32, 1 <= depth <= 16,
+ * topk <= V, 1 <= n <= C, n + 1 <= 128, C <= 4096, temperature > 0. */
+typedef struct {
+    int32_t B;            /* sequences in the batch */
+    int32_t V;            /* vocabulary size */
+    int32_t depth;        /* D: number of expansion layers */
+    int32_t topk;         /* k: children per expanded node */
+    int32_t m;            /* frontier width: nodes expanded per layer after the first */
+    int32_t n;            /* nodes kept by the rerank */
+    float temperature;    /* T of the target/draft distributions in stochastic acceptance */
+} et_tree_cfg;
+
+/*
+ * Device-side tree state (struct of caller-owned device pointers).
+ *
+ * Candidate ids are layer-major: layer-1 ids are 0..k-1 in top-k rank order;
+ * the children of layer L+1 follow all ids of layer L and are numbered
+ * base + slot*k + rank, slot being the parent's frontier slot (frontier
+ * slots hold ascending ids).  Hence a parent's id is always smaller than its
+ * children's and id order is depth order.
+ */
+typedef struct {
+    /* candidates, [B, C] each (row stride C) */
+    int32_t *cand_tok;      /* token id */
+    int32_t *cand_parent;   /* parent candidate id, -1 = the root */
+    float   *cand_lp;       /* fp32 log-prob of the token in the parent's draft row */
+    int64_t *cand_key;      /* path value: sum of rint(lp * 2^32) over the path, saturating at
+                               -(2^52-1); ranks nodes exactly like the product of confidences */
+    int32_t *frontier;      /* [B, m]: ids expanded by the next layer, ascending, -1 padded */
+    /* flattened kept tree, [B, N] each (row stride N); row 0 is the root */
+    const int32_t *root_tok;/* [B] input: token of each root (nullable: flat_tok[:,0] = -1) */
+    int32_t *flat_node;     /* candidate id of each row, -1 for the root */
+    int32_t *flat_tok;      /* token of each row */
+    int32_t *flat_parent;   /* flat row of the parent (< own row), -1 for the root */
+    int32_t *flat_depth;    /* depth, root = 0 */
+} et_tree;
+
+typedef enum { ET_BF16 = 0, ET_F32 = 1 } et_dtype;
+
+typedef enum {
+    ET_ACCEPT_GREEDY = 0,       /* argmax match along the tree */
+    ET_ACCEPT_STOCH_POINT = 1,  /* point-mass proposals: accept child x w.p. p(x)/(1-R) */
+    ET_ACCEPT_STOCH_DRAFTQ = 2  /* draft-q proposals: min(1, r(x)/q(x)), residual update */
+} et_accept_mode;
+
+/* Attention problem shape (host struct). */
+typedef struct {
+    int32_t B, N, Hq, Hkv, d; /* Hq % Hkv == 0, 128 % (Hq/Hkv) == 0, d in {64, 128}, N <= 128 */
+    et_dtype dtype;           /* of q, k/v prefix, k/v tree and out */
+    float scale;              /* score scale, usually 1/sqrt(d) */
+    int32_t max_prefix;       /* host upper bound of prefix_len[b] (sizes the grid) */
+    int64_t kv_rows;          /* d-element rows in each of k_prefix / v_prefix (bounds check) */
+    int64_t kv_head_stride;   /* rows between heads of one sequence's prefix; 0 = prefix_len[b] */
+    int32_t num_splits;       /* KV splits per (sequence, head, row tile); 0 = library heuristic */
+} et_attn_shape;
+
+/* ---- geometry helpers (host, no device work) ---- */
+
+/* C = k + sum_{l=2..D} min(m, width_{l-1}) * k, or -1 if cfg breaks a limit. */
+int32_t et_num_candidates(const et_tree_cfg *cfg);
+/* Nodes expanded by `layer` (1 for layer 0, else min(m, width of layer)), -1 if out of range. */
+int32_t et_layer_expanded(const et_tree_cfg *cfg, int32_t layer);
+/* First candidate id of `layer` (>= 1), -1 if out of range. */
+int32_t et_layer_base(const et_tree_cfg *cfg, int32_t layer);
+/* Workspace bytes for et_tree_expand and et_verify_accept with this cfg. */
+size_t et_tree_workspace_size(const et_tree_cfg *cfg);
+/* Workspace bytes for et_tree_attention with this shape (0 if no split merge is needed). */
+size_t et_tree_attention_workspace_size(const et_attn_shape *shape);
+/* Splits the attention call will use for this shape. */
+int32_t et_tree_attention_splits(const et_attn_shape *shape);
+/* Zero-fill a workspace on `stream` (cudaMemsetAsync). */
+et_status et_workspace_init(void *ws, size_t ws_bytes, et_stream_t stream);
+const char *et_status_string(et_status s);
+int32_t et_abi_version(void);
+
+/*
+ * et_tree_expand -- one layer of the expansion phase (EAGLE-2 article,
+ * expansion phase; node value = product of confidences along the path).
+ *
+ * Expanded nodes: the root at layer 0, else tree->frontier[b, 0..m_l) written
+ * by the previous layer (m_l = et_layer_expanded(cfg, layer)).  For each,
+ * over its fp32 draft-logit row z (length V):
+ *   lp = log-softmax(z) (fp32, NaN counted as -inf);
+ *   children = the k largest logits (ties: lower token id), ids
+ *     et_layer_base(cfg, layer+1) + slot*k + rank;
+ *   key(child) = key(parent) + rint(lp(child) * 2^32) (key(root) = 0).
+ * If layer + 1 < D, the frontier of layer + 1 is then the top-m_{l+1} new
+ * nodes by (key desc, id asc), written in ascending id order.
+ *
+ * logits      fp32 table; row r starts at logits + r * row_stride.
+ * row_stride  elements between rows (>= V).  With 16-byte aligned `logits`
+ *             and row_stride % 4 == 0 the rows are read with 128-bit loads.
+ * row_of_node nullable int32 [B, C + 1]: table row of each node (index 0 =
+ *             the root, 1 + id = candidate id).  Null: rows are in expansion
+ *             order, row = b * m_l + slot (what a draft model writes).
+ * ws          et_tree_workspace_size(cfg) bytes (see conventions).
+ */
+et_status et_tree_expand(const et_tree_cfg *cfg, int32_t layer,
+                         const float *logits, int64_t row_stride, const int32_t *row_of_node,
+                         et_tree *tree, int32_t *dev_status,
+                         void *ws, size_t ws_bytes, et_stream_t stream);
+
+/*
+ * et_tree_rerank -- reranking phase (EAGLE-2 article): keep the n candidates
+ * with the largest (key desc, id asc) -- equal values keep the shallower
+ * node, so the kept tree is connected -- and flatten them: row 0 is the
+ * root, rows 1..n the kept ids ascending.  Writes tree->flat_*.
+ * One CTA per sequence (segmented radix select over C 64-bit keys).
+ */
+et_status et_tree_rerank(const et_tree_cfg *cfg, et_tree *tree, int32_t *dev_status,
+                         et_stream_t stream);
+
+/*
+ * et_tree_mask_posids -- attention mask and position ids of the flattened
+ * tree (EAGLE-2 article, attention-mask example and position encoding).
+ *
+ * mask   uint64 [B, N, W]: bit j of word w of row i (LSB first) is set iff
+ *        flat row 64w + j is row i or one of its ancestors; bits >= N clear.
+ * posids int32 [B, N]: prefix_len[b] + flat_depth[b, i].
+ * prefix_len int32 [B]: tokens already in each sequence's KV cache.
+ */
+et_status et_tree_mask_posids(const et_tree_cfg *cfg, const et_tree *tree,
+                              const int32_t *prefix_len, uint64_t *mask, int32_t *posids,
+                              et_stream_t stream);
+
+/*
+ * et_tree_attention -- attention of the N flattened draft rows over the KV
+ * prefix plus their in-tree ancestors (EAGLE-2 article: each token sees only
+ * its ancestors; EAGLE blog 1.1: one target forward verifies the draft).
+ *
+ *   out[b,i,h] = sum_j softmax_j(scale * q[b,i,h] . k_j) v_j,
+ *   j over prefix tokens 0..prefix_len[b]-1 of KV head g = h / (Hq/Hkv) and
+ *   tree rows t with mask bit (b,i,t).
+ *
+ * q, out        [B, N, Hq, d]  (bf16 or fp32 per shape->dtype)
+ * k/v_prefix    prefix row of (b, g, j) = kv_row0[b] + g * S_b + j, S_b =
+ *               shape->kv_head_stride or prefix_len[b]; rows of d elements.
+ * kv_row0       int64 [B] first row of each sequence's prefix.
+ * prefix_len    int32 [B], each in [0, max_prefix].
+ * k/v_tree      [B, N, Hkv, d]: the tree rows' own keys/values (already
+ *               rotated, like q and the prefix).
+ * mask          uint64 [B, N, W] from et_tree_mask_posids.
+ * lse           nullable fp32 [B, Hq, N]: natural-log log-sum-exp of the
+ *               scaled scores of each row.
+ * ws            et_tree_attention_workspace_size(shape) bytes (may be 0/null
+ *               when that size is 0).
+ * Accumulation is fp32; P is rounded to the input dtype before P.V.
+ */
+et_status et_tree_attention(const et_attn_shape *shape,
+                            const void *q, const void *k_prefix, const void *v_prefix,
+                            const int64_t *kv_row0, const int32_t *prefix_len,
+                            const void *k_tree, const void *v_tree, const uint64_t *mask,
+                            void *out, float *lse, int32_t *dev_status,
+                            void *ws, size_t ws_bytes, et_stream_t stream);
+
+/*
+ * et_verify_accept -- lossless acceptance walk (EAGLE blog 1.2: lossless in
+ * greedy and non-greedy decoding; the non-greedy rule is the speculative
+ * sampling the blog cites in 1.1).
+ *
+ * From row 0, children are tried in ascending flat row:
+ *  GREEDY: a child is accepted iff its token is the argmax (lowest id on
+ *    ties) of the current row's target logits; the bonus token is that
+ *    argmax at the row where the walk stops.
+ *  STOCH_POINT: p = softmax(target / T); child x is accepted iff
+ *    uniforms[b, child] < p(x) / (1 - R), R = p-mass of siblings rejected
+ *    so far at this row; bonus = smallest token t whose cumulative residual
+ *    mass (rejected tokens removed, ascending token id) exceeds
+ *    uniforms[b, 0] * (remaining mass).
+ *  STOCH_DRAFTQ: q = softmax(draft row of the current node / T); accept iff
+ *    uniforms[b, child] < min(1, r(x) / q(x)), r starting at p and becoming
+ *    norm(max(r - q, 0)) after each rejection (kept if that mass is 0);
+ *    bonus drawn from the final r the same way.
+ *
+ * target_logits fp32 rows, stride target_stride; target_row_of_node
+ *               nullable int32 [B, C+1] (index 1 + node, 0 = root); null:
+ *               row = b * N + flat row (the target forward's output order).
+ * draft_logits  (DRAFTQ only) same convention with draft_row_of_node.
+ * uniforms      fp32 [B, N] in [0, 1) (stochastic modes; nullable for GREEDY).
+ * accept_len    int32 [B]: accepted draft tokens (0..D).
+ * path          int32 [B, D+1]: flat rows of the accepted path, root first, -1 padded.
+ * tokens        int32 [B, D+1]: accepted draft tokens then the bonus token, -1 padded.
+ * ws            et_tree_workspace_size(cfg) bytes (see conventions).
+ */
+et_status et_verify_accept(const et_tree_cfg *cfg, et_accept_mode mode, const et_tree *tree,
+                           const float *target_logits, int64_t target_stride,
+                           const int32_t *target_row_of_node,
+                           const float *draft_logits, int64_t draft_stride,
+                           const int32_t *draft_row_of_node,
+                           const float *uniforms,
+                           int32_t *accept_len, int32_t *path, int32_t *tokens,
+                           int32_t *dev_status, void *ws, size_t ws_bytes, et_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EAGLE_TREE_H */

@@ -1,0 +1,216 @@
+// Shared helpers of the sm_103a EAGLE-2 tree kernels: limits, the node-id
+// geometry, fixed-point path keys, 64-bit rank keys and block reductions.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <float.h>
+#include <math.h>
+
+#include "eagle_tree.h"
+
+namespace et {
+
+constexpr int kMaxTopk = 32;
+constexpr int kMaxM = 32;
+constexpr int kMaxDepth = 16;
+constexpr int kMaxN = 128;
+constexpr int kMaxC = 4096;
+constexpr int kMaxV = 262144;
+constexpr int kIdBits = 12;                      // C <= 4096
+constexpr long long kKeyMin = -((1LL << 52) - 1);  // saturation of path keys (-2^20 nats)
+
+// Layer widths and id bases of the dynamic tree (EAGLE-2 article, expansion
+// phase): layer 1 has k nodes; layer l+1 has min(m, width_l) * k.
+struct Geometry {
+  int C;
+  int depth;
+  int width[kMaxDepth + 1];    // width[0] = 1 (root)
+  int base[kMaxDepth + 2];     // first id of layer l (l >= 1); base[D+1] = C
+  int expanded[kMaxDepth];     // nodes expanded at layer l
+};
+
+inline bool make_geometry(const et_tree_cfg *cfg, Geometry *g) {
+  if (!cfg) return false;
+  if (cfg->B < 1 || cfg->depth < 1 || cfg->depth > kMaxDepth || cfg->topk < 1 ||
+      cfg->topk > kMaxTopk || cfg->m < 1 || cfg->m > kMaxM || cfg->V < cfg->topk ||
+      cfg->V > kMaxV || !(cfg->temperature > 0.f) || cfg->n < 1 || cfg->n + 1 > kMaxN)
+    return false;
+  g->depth = cfg->depth;
+  g->width[0] = 1;
+  g->width[1] = cfg->topk;
+  long long C = cfg->topk;
+  for (int l = 2; l <= cfg->depth; ++l) {
+    int e = g->width[l - 1] < cfg->m ? g->width[l - 1] : cfg->m;
+    g->width[l] = e * cfg->topk;
+    C += g->width[l];
+    if (C > kMaxC) return false;
+  }
+  g->C = (int)C;
+  g->base[1] = 0;
+  for (int l = 1; l <= cfg->depth; ++l) g->base[l + 1] = g->base[l] + g->width[l];
+  g->base[0] = -1;
+  g->expanded[0] = 1;
+  for (int l = 1; l < cfg->depth; ++l) g->expanded[l] = g->width[l] < cfg->m ? g->width[l] : cfg->m;
+  if (cfg->n > g->C) return false;
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+// NaN counts as -inf, +inf as FLT_MAX; reports either through *flag.
+__device__ __forceinline__ float sanitize_logit(float z, int &flag) {
+  if (z != z) { flag = 1; return -INFINITY; }
+  if (z == INFINITY) { flag = 1; return FLT_MAX; }
+  return z;
+}
+
+// (z desc, id asc): is (za, ia) ranked before (zb, ib)?
+__device__ __forceinline__ bool ranks_before(float za, int ia, float zb, int ib) {
+  return za > zb || (za == zb && ia < ib);
+}
+
+// Fixed-point image of an fp32 log-prob: rint(lp * 2^32), saturating.  The
+// product lp * 2^32 is exact in fp32 (a power-of-two scale).
+__device__ __forceinline__ long long fixed_key(float lp) {
+  if (!(lp > -4.0e15f / 4294967296.0f)) return kKeyMin;  // -inf, NaN, or beyond the range
+  long long k = __float2ll_rn(lp * 4294967296.0f);
+  return k < kKeyMin ? kKeyMin : k;
+}
+
+__device__ __forceinline__ long long add_keys(long long a, long long b) {
+  long long s = a + b;
+  return s < kKeyMin ? kKeyMin : s;
+}
+
+// Unique 64-bit rank key: ascending order == (key desc, id asc).
+__device__ __forceinline__ unsigned long long rank_key(long long key, int id) {
+  if (key > 0) key = 0;
+  if (key < kKeyMin) key = kKeyMin;
+  return ((unsigned long long)(-key) << kIdBits) | (unsigned long long)id;
+}
+
+__device__ __forceinline__ void flag_status(int32_t *dev_status, int bits) {
+  if (dev_status && bits) atomicOr(dev_status, bits);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = w < v ? w : v;
+  }
+  return v;
+}
+// warp-wide best (z desc, id asc); every lane gets the winner
+__device__ __forceinline__ void warp_best(float &z, int &id) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float z2 = __shfl_xor_sync(0xffffffffu, z, o);
+    int i2 = __shfl_xor_sync(0xffffffffu, id, o);
+    if (ranks_before(z2, i2, z, id)) { z = z2; id = i2; }
+  }
+}
+
+// Block reductions; `red` must hold >= 32 elements; all threads get the result.
+template <int NT>
+__device__ __forceinline__ float block_max(float v, float *red) {
+  v = warp_max(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  v = l < NT / 32 ? red[l] : -INFINITY;
+  return warp_max(v);
+}
+template <int NT>
+__device__ __forceinline__ float block_sum(float v, float *red) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  v = l < NT / 32 ? red[l] : 0.f;
+  return warp_sum(v);
+}
+template <int NT>
+__device__ __forceinline__ double block_sum_d(double v, double *red) {
+  v = warp_sum_d(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  v = l < NT / 32 ? red[l] : 0.0;
+  return warp_sum_d(v);
+}
+template <int NT>
+__device__ __forceinline__ unsigned long long block_min_u64(unsigned long long v, unsigned long long *red) {
+  v = warp_min_u64(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  v = l < NT / 32 ? red[l] : ~0ull;
+  return warp_min_u64(v);
+}
+template <int NT>
+__device__ __forceinline__ void block_best(float &z, int &id, float *redz, int *redi) {
+  warp_best(z, id);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) { redz[w] = z; redi[w] = id; }
+  __syncthreads();
+  if (l < NT / 32) { z = redz[l]; id = redi[l]; } else { z = -INFINITY; id = 0x7fffffff; }
+  warp_best(z, id);
+}
+
+// "Last block to arrive" handshake: every thread of the block has written its
+// part; returns true in exactly one block per counter round and re-arms the
+// counter for the next call.  No block ever waits on another.
+__device__ __forceinline__ bool arrive_last(unsigned int *counter, unsigned int expected, int *smem_flag) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned int prev = atomicAdd(counter, 1u);
+    int last = (prev == expected - 1);
+    if (last) *counter = 0u;  // all arrivals of this round are in
+    *smem_flag = last;
+  }
+  __syncthreads();
+  const bool last = *smem_flag != 0;
+  if (last) __threadfence();
+  return last;
+}
+
+template <typename T>
+__device__ __forceinline__ T ld_cg(const T *p) { return __ldcg(p); }
+
+}  // namespace et
+
+// host-side helpers shared by the entry points
+#define ET_RETURN_IF(cond, code) \
+  do {                           \
+    if (cond) return (code);     \
+  } while (0)
+
+static inline et_status et_launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? ET_OK : ET_ERR_CUDA;
+}
+static inline bool et_aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }

@@ -1,0 +1,570 @@
+// Dynamic draft tree on sm_103a: expansion (log-softmax + top-k + path value
+// + top-m frontier), rerank (top-n + flatten) and the ancestor mask /
+// position ids.  Follows the EAGLE-2 article on sbmmt.com ("Up to 5x lossless
+// acceleration: EAGLE-2 lets an RTX 3060 generate faster than an A100"):
+// expansion phase, reranking phase, attention-mask example and the
+// position-encoding sentence.
+#include "et_common.cuh"
+
+namespace et {
+
+// ---------------------------------------------------------------------------
+// expand
+// ---------------------------------------------------------------------------
+constexpr int kExpThreads = 256;
+constexpr int kExpVec = 2;                               // float4 loads per thread
+constexpr int kExpChunk = kExpThreads * 4 * kExpVec;     // logits per block
+
+struct ExpandArgs {
+  const float *logits;
+  long long row_stride;
+  const int32_t *row_of_node;
+  int vec4;
+  int B, V, k, m, C, layer, m_l, base_next, m_next, nchunk;
+  et_tree tree;
+  int32_t *dev_status;
+  float *part;             // [B*m_l][nchunk][2 + 2k]
+  unsigned int *row_cnt;   // [B*m_l]
+  unsigned int *seq_cnt;   // [B]
+};
+
+// Loads this block's slice of a logit row (128-bit loads when aligned);
+// out-of-row slots get -inf with id INT_MAX so they rank after every token.
+template <int NV>
+__device__ __forceinline__ void load_chunk(const float *zrow, int V, int c0, int vec4, float (&v)[4 * NV],
+                                           int &flag) {
+#pragma unroll
+  for (int u = 0; u < NV; ++u) {
+    const int e0 = c0 + (u * kExpThreads + threadIdx.x) * 4;
+    if (zrow && vec4 && e0 + 3 < V) {
+      float4 f = __ldcs(reinterpret_cast<const float4 *>(zrow + e0));
+      v[4 * u + 0] = f.x; v[4 * u + 1] = f.y; v[4 * u + 2] = f.z; v[4 * u + 3] = f.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[4 * u + j] = (zrow && e0 + j < V) ? __ldcs(zrow + e0 + j) : -INFINITY;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (e0 + j < V) v[4 * u + j] = sanitize_logit(v[4 * u + j], flag);
+  }
+}
+
+__device__ __forceinline__ int chunk_id(int c0, int j, int V) {
+  const int e = c0 + ((j >> 2) * kExpThreads + threadIdx.x) * 4 + (j & 3);
+  return e < V ? e : 0x7fffffff;
+}
+
+__global__ void __launch_bounds__(kExpThreads) k_expand(ExpandArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  float *mz = reinterpret_cast<float *>(smem_raw);              // [nchunk*k]
+  int *mi = reinterpret_cast<int *>(mz + a.nchunk * a.k);       // [nchunk*k]
+  __shared__ float redz[32];
+  __shared__ int redi[32];
+  __shared__ float wz[kExpThreads / 32][kMaxTopk];
+  __shared__ int wi[kExpThreads / 32][kMaxTopk];
+  __shared__ float topz[kMaxTopk];
+  __shared__ int topi[kMaxTopk];
+  __shared__ unsigned long long red64[32];
+  __shared__ int sel[kMaxM];
+  __shared__ int sflag;
+
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int row = blockIdx.y, c = blockIdx.x;
+  const int b = row / a.m_l, s = row - b * a.m_l;
+  const int k = a.k;
+  int flag = 0, bad = 0;
+
+  int node = -1;
+  if (a.layer > 0) {
+    node = a.tree.frontier[b * a.m + s];
+    if (node < 0 || node >= a.C) bad = 1;
+  }
+  const float *zrow = nullptr;
+  if (!bad) {
+    long long r = a.row_of_node ? (long long)a.row_of_node[(long long)b * (a.C + 1) + node + 1] : (long long)row;
+    if (r < 0) bad = 1;
+    else zrow = a.logits + r * a.row_stride;
+  }
+
+  float v[4 * kExpVec];
+  const int c0 = c * kExpChunk;
+  load_chunk<kExpVec>(zrow, a.V, c0, a.vec4, v, flag);
+
+  // chunk max and sum of exp
+  float lm = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 4 * kExpVec; ++j) lm = fmaxf(lm, v[j]);
+  const float Mc = block_max<kExpThreads>(lm, redz);
+  float ls = 0.f;
+  if (Mc > -INFINITY) {
+#pragma unroll
+    for (int j = 0; j < 4 * kExpVec; ++j) ls += (v[j] > -INFINITY) ? expf(v[j] - Mc) : 0.f;
+  }
+  const float Sc = block_sum<kExpThreads>(ls, redz);
+
+  // per-warp top-k by repeated warp argmax (each lane pops its own best)
+  unsigned consumed = 0;
+  float bz = -INFINITY;
+  int bi = 0x7fffffff;
+#pragma unroll
+  for (int j = 0; j < 4 * kExpVec; ++j) {
+    const int id = chunk_id(c0, j, a.V);
+    if (ranks_before(v[j], id, bz, bi)) { bz = v[j]; bi = id; }
+  }
+  for (int r = 0; r < k; ++r) {
+    float z = bz;
+    int id = bi;
+    warp_best(z, id);
+    if (lane == 0) { wz[warp][r] = z; wi[warp][r] = id; }
+    if (id == bi && id != 0x7fffffff) {
+#pragma unroll
+      for (int j = 0; j < 4 * kExpVec; ++j)
+        if (chunk_id(c0, j, a.V) == id) consumed |= 1u << j;
+      bz = -INFINITY;
+      bi = 0x7fffffff;
+#pragma unroll
+      for (int j = 0; j < 4 * kExpVec; ++j) {
+        const int id2 = chunk_id(c0, j, a.V);
+        if (!((consumed >> j) & 1u) && ranks_before(v[j], id2, bz, bi)) { bz = v[j]; bi = id2; }
+      }
+    }
+  }
+  __syncthreads();
+  // block top-k: warp 0 merges the 8 warp lists
+  float *prt = a.part + ((long long)row * a.nchunk + c) * (2 + 2 * k);
+  if (warp == 0) {
+    float cz[kExpThreads / 32];
+    int ci[kExpThreads / 32];
+#pragma unroll
+    for (int q = 0; q < kExpThreads / 32; ++q) {
+      const int idx = lane + 32 * q;
+      if (idx < (kExpThreads / 32) * k) { cz[q] = wz[idx / k][idx % k]; ci[q] = wi[idx / k][idx % k]; }
+      else { cz[q] = -INFINITY; ci[q] = 0x7fffffff; }
+    }
+    for (int r = 0; r < k; ++r) {
+      float lz = -INFINITY;
+      int li = 0x7fffffff, lq = -1;
+#pragma unroll
+      for (int q = 0; q < kExpThreads / 32; ++q)
+        if (ranks_before(cz[q], ci[q], lz, li)) { lz = cz[q]; li = ci[q]; lq = q; }
+      float z = lz;
+      int id = li;
+      warp_best(z, id);
+      if (lane == 0) { prt[2 + 2 * r] = z; prt[3 + 2 * r] = __int_as_float(id); }
+      if (id == li && lq >= 0 && id != 0x7fffffff) {
+#pragma unroll
+        for (int q = 0; q < kExpThreads / 32; ++q)
+          if (q == lq) { cz[q] = -INFINITY; ci[q] = 0x7fffffff; }
+      }
+    }
+    if (lane == 0) { prt[0] = Mc; prt[1] = Sc; }
+  }
+  if (flag) flag_status(a.dev_status, ET_DEV_NONFINITE);
+  if (bad && c == 0 && t == 0) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
+
+  // ---- last block of this row: merge the chunks, write the children ----
+  if (!arrive_last(&a.row_cnt[row], (unsigned)a.nchunk, &sflag)) return;
+
+  const float *rp = a.part + (long long)row * a.nchunk * (2 + 2 * k);
+  float cm = -INFINITY, cs = 0.f;
+  if (t < a.nchunk) { cm = ld_cg(rp + t * (2 + 2 * k)); cs = ld_cg(rp + t * (2 + 2 * k) + 1); }
+  const float M = block_max<kExpThreads>(cm, redz);
+  const float S = block_sum<kExpThreads>((t < a.nchunk && cm > -INFINITY) ? cs * expf(cm - M) : 0.f, redz);
+  for (int i = t; i < a.nchunk * k; i += kExpThreads) {
+    const int cc = i / k, r = i - cc * k;
+    mz[i] = ld_cg(rp + cc * (2 + 2 * k) + 2 + 2 * r);
+    mi[i] = __float_as_int(ld_cg(rp + cc * (2 + 2 * k) + 3 + 2 * r));
+  }
+  __syncthreads();
+  float lz = -INFINITY;
+  int li = 0x7fffffff;
+  for (int i = t; i < a.nchunk * k; i += kExpThreads)
+    if (ranks_before(mz[i], mi[i], lz, li)) { lz = mz[i]; li = mi[i]; }
+  for (int r = 0; r < k; ++r) {
+    float z = lz;
+    int id = li;
+    block_best<kExpThreads>(z, id, redz, redi);
+    if (t == 0) { topz[r] = z; topi[r] = id; }
+    if (id == li && id != 0x7fffffff) {  // the owner pops it and rescans its slots
+      for (int i = t; i < a.nchunk * k; i += kExpThreads)
+        if (mi[i] == id) { mz[i] = -INFINITY; mi[i] = 0x7fffffff; }
+      lz = -INFINITY;
+      li = 0x7fffffff;
+      for (int i = t; i < a.nchunk * k; i += kExpThreads)
+        if (ranks_before(mz[i], mi[i], lz, li)) { lz = mz[i]; li = mi[i]; }
+    }
+  }
+  __syncthreads();
+  if (t < k) {
+    const float logS = (M > -INFINITY) ? logf(S) : 0.f;
+    const float z = topz[t];
+    const float lp = (M > -INFINITY && z > -INFINITY) ? (z - M) - logS : -INFINITY;
+    const long long pkey = node < 0 ? 0ll : a.tree.cand_key[(long long)b * a.C + node];
+    const int cid = a.base_next + s * k + t;
+    const long long o = (long long)b * a.C + cid;
+    const int tok = topi[t];
+    a.tree.cand_tok[o] = (tok == 0x7fffffff) ? -1 : tok;
+    a.tree.cand_parent[o] = node;
+    a.tree.cand_lp[o] = lp;
+    a.tree.cand_key[o] = add_keys(pkey, fixed_key(lp));
+  }
+
+  // ---- last row of this sequence: pick the next layer's frontier ----
+  if (!arrive_last(&a.seq_cnt[b], (unsigned)a.m_l, &sflag)) return;
+  if (a.m_next <= 0) return;
+  const int width = a.m_l * k;  // <= 1024
+  unsigned long long mine[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int i = t + q * kExpThreads;
+    mine[q] = ~0ull;
+    if (i < width) {
+      const int id = a.base_next + i;
+      mine[q] = rank_key(ld_cg(a.tree.cand_key + (long long)b * a.C + id), id);
+    }
+  }
+  for (int r = 0; r < a.m_next; ++r) {
+    unsigned long long lmin = ~0ull;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) lmin = mine[q] < lmin ? mine[q] : lmin;
+    const unsigned long long w = block_min_u64<kExpThreads>(lmin, red64);
+    if (t == 0) sel[r] = (int)(w & ((1ull << kIdBits) - 1));
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (mine[q] == w) mine[q] = ~0ull;
+  }
+  __syncthreads();
+  if (t < a.m) {
+    int out = -1;
+    if (t < a.m_next) {  // rank of sel[t] among the selected ids = its ascending slot
+      int rank = 0;
+      for (int j = 0; j < a.m_next; ++j) rank += sel[j] < sel[t];
+      out = rank;
+    }
+    if (t < a.m_next) a.tree.frontier[b * a.m + out] = sel[t];
+    else a.tree.frontier[b * a.m + t] = -1;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// rerank + flatten
+// ---------------------------------------------------------------------------
+constexpr int kRrThreads = 1024;
+constexpr int kRrPer = kMaxC / kRrThreads;  // 4 candidates per thread
+
+struct RerankArgs {
+  int B, C, n, N, depth;
+  int base[kMaxDepth + 2];
+  et_tree tree;
+  int32_t *dev_status;
+};
+
+__device__ __forceinline__ int block_excl_scan_1024(int v, int *tmp, int &total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) tmp[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int s = tmp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    tmp[lane] = s;  // inclusive prefix of warp totals
+  }
+  __syncthreads();
+  total = tmp[31];
+  const int before = w > 0 ? tmp[w - 1] : 0;
+  return before + x - v;
+}
+
+__global__ void __launch_bounds__(kRrThreads) k_rerank(RerankArgs a) {
+  __shared__ unsigned int hist[256];
+  __shared__ unsigned int sel_digit, sel_before;
+  __shared__ short flat_of[kMaxC];
+  __shared__ unsigned char kept[kMaxC];
+  __shared__ int tmp[32];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int b = blockIdx.x;
+  const int C = a.C;
+
+  unsigned long long rk[kRrPer];
+#pragma unroll
+  for (int q = 0; q < kRrPer; ++q) {
+    const int id = t + q * kRrThreads;
+    rk[q] = id < C ? rank_key(a.tree.cand_key[(long long)b * C + id], id) : ~0ull;
+  }
+  // MSB-first radix select of the n-th smallest rank key (keys are unique)
+  unsigned long long prefix = 0ull, pmask = 0ull;
+  unsigned int remaining = (unsigned)a.n;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    if (t < 256) hist[t] = 0u;
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < kRrPer; ++q) {
+      const int id = t + q * kRrThreads;
+      if (id < C && (rk[q] & pmask) == prefix) atomicAdd(&hist[(rk[q] >> shift) & 255ull], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      unsigned int loc[8], sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) { loc[j] = hist[8 * lane + j]; sum += loc[j]; }
+      unsigned int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned int excl = incl - sum;
+      if (excl < remaining && remaining <= incl) {
+        unsigned int run = excl;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (run + loc[j] >= remaining) { sel_digit = 8 * lane + j; sel_before = run; break; }
+          run += loc[j];
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= (unsigned long long)sel_digit << shift;
+    pmask |= 0xffull << shift;
+    remaining -= sel_before;
+    __syncthreads();
+  }
+  const unsigned long long thr = prefix;
+#pragma unroll
+  for (int q = 0; q < kRrPer; ++q) {
+    const int id = t + q * kRrThreads;
+    if (id < C) kept[id] = rk[q] <= thr ? 1 : 0;
+  }
+  __syncthreads();
+  // flatten: kept ids ascending -> rows 1..n
+  int cnt = 0;
+#pragma unroll
+  for (int j = 0; j < kRrPer; ++j) {
+    const int id = kRrPer * t + j;
+    cnt += (id < C && kept[id]) ? 1 : 0;
+  }
+  int total;
+  int run = block_excl_scan_1024(cnt, tmp, total);
+#pragma unroll
+  for (int j = 0; j < kRrPer; ++j) {
+    const int id = kRrPer * t + j;
+    if (id < C) flat_of[id] = kept[id] ? (short)(1 + run++) : (short)-1;
+  }
+  __syncthreads();
+  const long long fo = (long long)b * a.N;
+  int bad = 0;
+#pragma unroll
+  for (int j = 0; j < kRrPer; ++j) {
+    const int id = kRrPer * t + j;
+    if (id >= C || !kept[id]) continue;
+    const int row = flat_of[id];
+    if (row < 1 || row >= a.N) { bad = 1; continue; }  // never write outside the flat arrays
+    const int p = a.tree.cand_parent[(long long)b * C + id];
+    int prow = 0;
+    if (p >= 0) {
+      prow = (p < C) ? flat_of[p] : -1;
+      if (prow < 0) { bad = 1; prow = 0; }
+    }
+    int depth = 1;
+    for (int l = 1; l <= a.depth; ++l)
+      if (id >= a.base[l]) depth = l;
+    a.tree.flat_node[fo + row] = id;
+    a.tree.flat_tok[fo + row] = a.tree.cand_tok[(long long)b * C + id];
+    a.tree.flat_parent[fo + row] = prow;
+    a.tree.flat_depth[fo + row] = depth;
+  }
+  if (bad) flag_status(a.dev_status, ET_DEV_DISCONNECTED);
+  if (t == 0) {
+    a.tree.flat_node[fo] = -1;
+    a.tree.flat_tok[fo] = a.tree.root_tok ? a.tree.root_tok[b] : -1;
+    a.tree.flat_parent[fo] = -1;
+    a.tree.flat_depth[fo] = 0;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// ancestor mask + position ids
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kMaxN) k_mask_posids(int N, const int32_t *flat_parent, const int32_t *flat_depth,
+                                                      const int32_t *prefix_len, uint64_t *mask, int32_t *posids,
+                                                      int32_t *dev_status) {
+  __shared__ int par[kMaxN];
+  const int b = blockIdx.x, i = threadIdx.x;
+  const int W = (N + 63) >> 6;
+  if (i < N) par[i] = flat_parent[(long long)b * N + i];
+  __syncthreads();
+  if (i >= N) return;
+  uint64_t w0 = 0, w1 = 0;
+  int j = i, steps = 0, bad = 0;
+  while (j >= 0 && steps <= kMaxN) {  // parents have smaller rows: at most N steps
+    if (j < 64) w0 |= 1ull << j; else w1 |= 1ull << (j - 64);
+    const int p = par[j];
+    if (p >= j) { bad = 1; break; }
+    j = p;
+    ++steps;
+  }
+  uint64_t *mrow = mask + ((long long)b * N + i) * W;
+  mrow[0] = w0;
+  if (W > 1) mrow[1] = w1;
+  posids[(long long)b * N + i] = prefix_len[b] + flat_depth[(long long)b * N + i];
+  if (bad) flag_status(dev_status, ET_DEV_BAD_INDEX);
+}
+
+}  // namespace et
+
+using namespace et;
+
+// ---------------------------------------------------------------------------
+// workspace layout shared by et_tree_expand and et_verify_accept
+// ---------------------------------------------------------------------------
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct TreeWs {
+  size_t cnt_bytes, part_off, rowstat_off, total;
+  int rows;  // max rows of one launch
+};
+
+static int nchunk_of(int V) { return (V + kExpChunk - 1) / kExpChunk; }
+
+static TreeWs tree_ws_layout(const et_tree_cfg *cfg) {
+  TreeWs w{};
+  const int N = cfg->n + 1;
+  const int nch = nchunk_of(cfg->V);
+  const int rows = cfg->B * (cfg->m > N ? cfg->m : N);
+  w.rows = rows;
+  w.cnt_bytes = align256(sizeof(unsigned int) * (size_t)(rows + cfg->B));
+  const size_t exp_part = sizeof(float) * (size_t)cfg->B * cfg->m * nch * (2 + 2 * cfg->topk);
+  const size_t ver_part = sizeof(float) * (size_t)cfg->B * N * nch * 2;
+  w.part_off = w.cnt_bytes;
+  const size_t part = align256(exp_part > ver_part ? exp_part : ver_part);
+  w.rowstat_off = w.part_off + part;
+  w.total = w.rowstat_off + align256(sizeof(float) * 2 * (size_t)cfg->B * N);
+  return w;
+}
+
+extern "C" size_t et_tree_workspace_size(const et_tree_cfg *cfg) {
+  Geometry g;
+  if (!make_geometry(cfg, &g)) return 0;
+  return tree_ws_layout(cfg).total;
+}
+
+// used by et_verify.cu; not part of the ABI
+extern "C" __attribute__((visibility("hidden"))) size_t et_internal_tree_ws(const et_tree_cfg *cfg, size_t *cnt_bytes, size_t *part_off,
+                                      size_t *rowstat_off) {
+  TreeWs w = tree_ws_layout(cfg);
+  *cnt_bytes = w.cnt_bytes;
+  *part_off = w.part_off;
+  *rowstat_off = w.rowstat_off;
+  return w.total;
+}
+
+extern "C" int32_t et_num_candidates(const et_tree_cfg *cfg) {
+  Geometry g;
+  return make_geometry(cfg, &g) ? g.C : -1;
+}
+
+extern "C" int32_t et_layer_expanded(const et_tree_cfg *cfg, int32_t layer) {
+  Geometry g;
+  if (!make_geometry(cfg, &g) || layer < 0 || layer >= cfg->depth) return -1;
+  return g.expanded[layer];
+}
+
+extern "C" int32_t et_layer_base(const et_tree_cfg *cfg, int32_t layer) {
+  Geometry g;
+  if (!make_geometry(cfg, &g) || layer < 1 || layer > cfg->depth) return -1;
+  return g.base[layer];
+}
+
+static bool tree_ptrs_ok(const et_tree *t) {
+  return t && t->cand_tok && t->cand_parent && t->cand_lp && t->cand_key && t->frontier;
+}
+
+extern "C" et_status et_tree_expand(const et_tree_cfg *cfg, int32_t layer, const float *logits, int64_t row_stride,
+                                    const int32_t *row_of_node, et_tree *tree, int32_t *dev_status, void *ws,
+                                    size_t ws_bytes, et_stream_t stream) {
+  Geometry g;
+  ET_RETURN_IF(!make_geometry(cfg, &g), ET_ERR_INVALID_ARG);
+  ET_RETURN_IF(layer < 0 || layer >= cfg->depth, ET_ERR_INVALID_ARG);
+  ET_RETURN_IF(!logits || row_stride < cfg->V || !tree_ptrs_ok(tree), ET_ERR_INVALID_ARG);
+  ET_RETURN_IF(!et_aligned(logits, 4), ET_ERR_INVALID_ARG);
+  const TreeWs w = tree_ws_layout(cfg);
+  ET_RETURN_IF(!ws || ws_bytes < w.total || !et_aligned(ws, 256), ET_ERR_WORKSPACE);
+  const int m_l = g.expanded[layer];
+  ET_RETURN_IF((long long)cfg->B * m_l > 65535, ET_ERR_UNSUPPORTED);
+  ExpandArgs a;
+  a.logits = logits;
+  a.row_stride = row_stride;
+  a.row_of_node = row_of_node;
+  a.vec4 = et_aligned(logits, 16) && (row_stride % 4 == 0);
+  a.B = cfg->B; a.V = cfg->V; a.k = cfg->topk; a.m = cfg->m; a.C = g.C; a.layer = layer; a.m_l = m_l;
+  a.base_next = g.base[layer + 1];
+  a.m_next = (layer + 1 < cfg->depth) ? g.expanded[layer + 1] : 0;
+  a.nchunk = nchunk_of(cfg->V);
+  a.tree = *tree;
+  a.dev_status = dev_status;
+  unsigned char *base = static_cast<unsigned char *>(ws);
+  a.row_cnt = reinterpret_cast<unsigned int *>(base);
+  a.seq_cnt = a.row_cnt + w.rows;
+  a.part = reinterpret_cast<float *>(base + w.part_off);
+  dim3 grid(a.nchunk, cfg->B * m_l);
+  const size_t smem = (size_t)a.nchunk * a.k * (sizeof(float) + sizeof(int));
+  k_expand<<<grid, kExpThreads, smem, (cudaStream_t)stream>>>(a);
+  return et_launch_status();
+}
+
+extern "C" et_status et_tree_rerank(const et_tree_cfg *cfg, et_tree *tree, int32_t *dev_status, et_stream_t stream) {
+  Geometry g;
+  ET_RETURN_IF(!make_geometry(cfg, &g), ET_ERR_INVALID_ARG);
+  ET_RETURN_IF(!tree || !tree->cand_tok || !tree->cand_parent || !tree->cand_key || !tree->flat_node ||
+                   !tree->flat_tok || !tree->flat_parent || !tree->flat_depth,
+               ET_ERR_INVALID_ARG);
+  RerankArgs a;
+  a.B = cfg->B; a.C = g.C; a.n = cfg->n; a.N = cfg->n + 1; a.depth = cfg->depth;
+  for (int l = 0; l < kMaxDepth + 2; ++l) a.base[l] = (l <= cfg->depth + 1) ? g.base[l] : 0x7fffffff;
+  a.base[0] = 0;
+  a.tree = *tree;
+  a.dev_status = dev_status;
+  k_rerank<<<cfg->B, kRrThreads, 0, (cudaStream_t)stream>>>(a);
+  return et_launch_status();
+}
+
+extern "C" et_status et_tree_mask_posids(const et_tree_cfg *cfg, const et_tree *tree, const int32_t *prefix_len,
+                                         uint64_t *mask, int32_t *posids, et_stream_t stream) {
+  Geometry g;
+  ET_RETURN_IF(!make_geometry(cfg, &g), ET_ERR_INVALID_ARG);
+  ET_RETURN_IF(!tree || !tree->flat_parent || !tree->flat_depth || !prefix_len || !mask || !posids,
+               ET_ERR_INVALID_ARG);
+  ET_RETURN_IF(!et_aligned(mask, 8), ET_ERR_INVALID_ARG);
+  k_mask_posids<<<cfg->B, kMaxN, 0, (cudaStream_t)stream>>>(cfg->n + 1, tree->flat_parent, tree->flat_depth,
+                                                            prefix_len, mask, posids, nullptr);
+  return et_launch_status();
+}
+
+extern "C" et_status et_workspace_init(void *ws, size_t ws_bytes, et_stream_t stream) {
+  if (!ws_bytes) return ET_OK;
+  ET_RETURN_IF(!ws, ET_ERR_WORKSPACE);
+  return cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream) == cudaSuccess ? ET_OK : ET_ERR_CUDA;
+}
+
+extern "C" const char *et_status_string(et_status s) {
+  switch (s) {
+    case ET_OK: return "ok";
+    case ET_ERR_INVALID_ARG: return "invalid argument";
+    case ET_ERR_UNSUPPORTED: return "unsupported shape";
+    case ET_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case ET_ERR_CUDA: return "CUDA launch or runtime error";
+    case ET_ERR_TIMEOUT: return "bounded device wait gave up";
+  }
+  return "unknown status";
+}
+
+extern "C" int32_t et_abi_version(void) { return ET_ABI_VERSION; }

@@ -1,0 +1,392 @@
+// Lossless acceptance walk on sm_103a (EAGLE blog "大模型系列——论文解读：
+// eagle/eagle2", sections 1.1 and 1.2: one target pass verifies the whole
+// draft and the output distribution is unchanged, greedy or not).
+//
+// Phase 1 (all blocks): every flat row's target logits are streamed once with
+// 128-bit loads, split over blocks; each block reduces its slice (argmax, or
+// max and sum of exp at temperature T); the last block of a row merges them.
+// Phase 2 (the last row-block of a sequence): walk the tree from the root,
+// then draw the bonus token by an inverse CDF over the stopping row.
+#include "et_common.cuh"
+
+extern "C" __attribute__((visibility("hidden"))) size_t et_internal_tree_ws(const et_tree_cfg *cfg, size_t *cnt_bytes, size_t *part_off,
+                                      size_t *rowstat_off);
+
+namespace et {
+
+constexpr int kVThreads = 256;
+constexpr int kVVec = 2;
+constexpr int kVChunk = kVThreads * 4 * kVVec;
+
+struct VerifyArgs {
+  int mode;
+  int B, V, N, C, D, nchunk;
+  float T;
+  const float *tlog;
+  long long tstride;
+  const int32_t *tmap;
+  const float *dlog;
+  long long dstride;
+  const int32_t *dmap;
+  const float *uniforms;
+  const int32_t *flat_node, *flat_tok, *flat_parent;
+  int32_t *accept_len, *path, *tokens, *dev_status;
+  float *part;        // [B*N][nchunk][2]
+  float *rowstat;     // [B*N][2]
+  unsigned int *row_cnt, *seq_cnt;
+  int vec4t;
+};
+
+__device__ __forceinline__ const float *table_row(const float *tab, long long stride, const int32_t *map, int C,
+                                                  int b, int node, long long flat_row, int &bad) {
+  long long r;
+  if (map) {
+    if (node < -1 || node >= C) { bad = 1; return nullptr; }
+    r = map[(long long)b * (C + 1) + node + 1];
+  } else {
+    r = flat_row;
+  }
+  if (r < 0) { bad = 1; return nullptr; }
+  return tab + r * stride;
+}
+
+// Inverse CDF over a row: smallest v with sum_{u<=v} w(u) > uni * sum_u w(u),
+// accumulated in fp64 over contiguous per-thread segments.  `w(v)` must be
+// non-negative; falls back to the last v with w(v) > 0.
+template <typename WF>
+__device__ int block_inverse_cdf(int V, float uni, WF w, double *redd, int *redi) {
+  const int t = threadIdx.x;
+  const int seg = (V + kVThreads - 1) / kVThreads;
+  const int lo = t * seg, hi = min(V, lo + seg);
+  double loc = 0.0;
+  int lastpos = -1;
+  for (int v = lo; v < hi; ++v) {
+    const float x = w(v);
+    loc += (double)x;
+    if (x > 0.f) lastpos = v;
+  }
+  // exclusive scan of the segment sums
+  const int lane = t & 31, wp = t >> 5;
+  double incl = loc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    double y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  __syncthreads();
+  if (lane == 31) redd[wp] = incl;
+  __syncthreads();
+  if (wp == 0) {
+    double s = lane < kVThreads / 32 ? redd[lane] : 0.0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      double y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    if (lane < kVThreads / 32) redd[lane] = s;
+  }
+  __syncthreads();
+  const double total = redd[kVThreads / 32 - 1];
+  const double excl = (wp > 0 ? redd[wp - 1] : 0.0) + incl - loc;
+  const double thr = (double)uni * total;
+  __syncthreads();
+  if (t == 0) { redi[0] = 0x7fffffff; redi[1] = -1; }
+  __syncthreads();
+  if (lastpos >= 0) atomicMax(&redi[1], lastpos);
+  if (loc > 0.0 && excl <= thr && thr < excl + loc) {
+    double run = excl;
+    int found = -1;
+    for (int v = lo; v < hi; ++v) {
+      run += (double)w(v);
+      if (run > thr) { found = v; break; }
+    }
+    if (found >= 0) atomicMin(&redi[0], found);
+  }
+  __syncthreads();
+  const int r = redi[0] != 0x7fffffff ? redi[0] : redi[1];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kVThreads) k_verify(VerifyArgs a) {
+  __shared__ float redz[32];
+  __shared__ int redi[32];
+  __shared__ double redd[32];
+  __shared__ int sflag;
+  __shared__ int par[kMaxN], tokf[kMaxN], nodef[kMaxN];
+  __shared__ int rej[kMaxTopk];
+  __shared__ float zsh[kMaxTopk];
+  __shared__ int s_next, s_nrej, s_cur;
+
+  const int t = threadIdx.x, lane = t & 31;
+  const int row = blockIdx.y, c = blockIdx.x;
+  const int b = row / a.N;
+  int flag = 0, bad = 0;
+  const int node = a.flat_node[row];
+  const float *zrow = table_row(a.tlog, a.tstride, a.tmap, a.C, b, node, row, bad);
+
+  float v[4 * kVVec];
+  const int c0 = c * kVChunk;
+#pragma unroll
+  for (int u = 0; u < kVVec; ++u) {
+    const int e0 = c0 + (u * kVThreads + t) * 4;
+    if (zrow && a.vec4t && e0 + 3 < a.V) {
+      float4 f = __ldg(reinterpret_cast<const float4 *>(zrow + e0));
+      v[4 * u + 0] = f.x; v[4 * u + 1] = f.y; v[4 * u + 2] = f.z; v[4 * u + 3] = f.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[4 * u + j] = (zrow && e0 + j < a.V) ? __ldg(zrow + e0 + j) : -INFINITY;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (e0 + j < a.V) v[4 * u + j] = sanitize_logit(v[4 * u + j], flag);
+  }
+  float *prt = a.part + ((long long)row * a.nchunk + c) * 2;
+  if (a.mode == ET_ACCEPT_GREEDY) {
+    float bz = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < 4 * kVVec; ++j) {
+      const int e = c0 + ((j >> 2) * kVThreads + t) * 4 + (j & 3);
+      if (e < a.V && ranks_before(v[j], e, bz, bi)) { bz = v[j]; bi = e; }
+    }
+    block_best<kVThreads>(bz, bi, redz, redi);
+    if (t == 0) { prt[0] = bz; prt[1] = __int_as_float(bi); }
+  } else {
+    float lm = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 4 * kVVec; ++j) {
+      v[j] = v[j] / a.T;
+      lm = fmaxf(lm, v[j]);
+    }
+    const float Mc = block_max<kVThreads>(lm, redz);
+    float ls = 0.f;
+    if (Mc > -INFINITY) {
+#pragma unroll
+      for (int j = 0; j < 4 * kVVec; ++j) ls += v[j] > -INFINITY ? expf(v[j] - Mc) : 0.f;
+    }
+    const float Sc = block_sum<kVThreads>(ls, redz);
+    if (t == 0) { prt[0] = Mc; prt[1] = Sc; }
+  }
+  if (flag) flag_status(a.dev_status, ET_DEV_NONFINITE);
+  if (bad && c == 0 && t == 0) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
+
+  if (!arrive_last(&a.row_cnt[row], (unsigned)a.nchunk, &sflag)) return;
+  {
+    const float *rp = a.part + (long long)row * a.nchunk * 2;
+    if (a.mode == ET_ACCEPT_GREEDY) {
+      float bz = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int cc = t; cc < a.nchunk; cc += kVThreads) {
+        const float z = ld_cg(rp + 2 * cc);
+        const int id = __float_as_int(ld_cg(rp + 2 * cc + 1));
+        if (ranks_before(z, id, bz, bi)) { bz = z; bi = id; }
+      }
+      block_best<kVThreads>(bz, bi, redz, redi);
+      if (t == 0) { a.rowstat[2 * row] = __int_as_float(bi); a.rowstat[2 * row + 1] = bz; }
+    } else {
+      float cm = -INFINITY, cs = 0.f;
+      if (t < a.nchunk) { cm = ld_cg(rp + 2 * t); cs = ld_cg(rp + 2 * t + 1); }
+      const float M = block_max<kVThreads>(cm, redz);
+      const float S = block_sum<kVThreads>((t < a.nchunk && cm > -INFINITY) ? cs * expf(cm - M) : 0.f, redz);
+      if (t == 0) { a.rowstat[2 * row] = M; a.rowstat[2 * row + 1] = S; }
+    }
+  }
+  if (!arrive_last(&a.seq_cnt[b], (unsigned)a.N, &sflag)) return;
+
+  // ---------------- phase 2: the walk of sequence b ----------------
+  const int N = a.N;
+  const long long fo = (long long)b * N;
+  for (int j = t; j < N; j += kVThreads) {
+    par[j] = a.flat_parent[fo + j];
+    tokf[j] = a.flat_tok[fo + j];
+    nodef[j] = a.flat_node[fo + j];
+  }
+  if (t == 0) s_cur = 0;
+  __syncthreads();
+  int alen = 0;
+  int bonus = -1;
+  int badw = 0;
+  for (int iter = 0; iter <= a.D + 1; ++iter) {
+    const int cur = s_cur;
+    if (t == 0) a.path[(long long)b * (a.D + 1) + alen] = cur;
+    if (t == 0) { s_next = -1; s_nrej = 0; }
+    __syncthreads();
+    const float *zr = table_row(a.tlog, a.tstride, a.tmap, a.C, b, nodef[cur], fo + cur, badw);
+    if (a.mode == ET_ACCEPT_GREEDY) {
+      const int am = __float_as_int(ld_cg(a.rowstat + 2 * (fo + cur)));
+      if (t == 0) {  // children are the rows after cur whose parent is cur; first match wins
+        int best = -1;
+        for (int j = cur + 1; j < N; ++j)
+          if (par[j] == cur && tokf[j] == am) { best = j; break; }
+        s_next = best;
+      }
+      __syncthreads();
+      bonus = am;
+    } else if (a.mode == ET_ACCEPT_STOCH_POINT) {
+      const float M = ld_cg(a.rowstat + 2 * (fo + cur)), S = ld_cg(a.rowstat + 2 * (fo + cur) + 1);
+      if (t == 0 && zr) {
+        float R = 0.f;
+        int nrej = 0;
+        for (int j = cur + 1; j < N; ++j) {
+          if (par[j] != cur) continue;
+          const int x = tokf[j];
+          if (x < 0 || x >= a.V) { badw = 1; continue; }
+          const float px = expf(sanitize_logit(zr[x], flag) / a.T - M) / S;
+          const float ratio = (R < 1.f) ? px / (1.f - R) : INFINITY;
+          const float u = a.uniforms[fo + j];
+          if (u < ratio) { s_next = j; break; }
+          R += px;
+          if (nrej < kMaxTopk) rej[nrej++] = x;
+        }
+        s_nrej = nrej;
+      }
+      __syncthreads();
+      if (s_next < 0) {
+        const int nrej = s_nrej;
+        bonus = block_inverse_cdf(a.V, a.uniforms[fo], [&](int vv) -> float {
+          if (!zr) return 0.f;
+          for (int q = 0; q < nrej; ++q)
+            if (rej[q] == vv) return 0.f;
+          int f2 = 0;
+          const float y = sanitize_logit(zr[vv], f2) / a.T;
+          return y > -INFINITY ? expf(y - M) : 0.f;
+        }, redd, redi);
+      }
+    } else {  // ET_ACCEPT_STOCH_DRAFTQ
+      const float M = ld_cg(a.rowstat + 2 * (fo + cur)), S = ld_cg(a.rowstat + 2 * (fo + cur) + 1);
+      bool has_child = false;
+      for (int j = cur + 1; j < N; ++j)
+        if (par[j] == cur) { has_child = true; break; }
+      float Mq = 0.f, Sq = 1.f;
+      const float *qr = nullptr;
+      if (has_child) {
+        qr = table_row(a.dlog, a.dstride, a.dmap, a.C, b, nodef[cur], fo + cur, badw);
+        float lm = -INFINITY;
+        for (int vv = t; vv < a.V; vv += kVThreads) {
+          int f2 = 0;
+          lm = fmaxf(lm, qr ? sanitize_logit(qr[vv], f2) / a.T : -INFINITY);
+        }
+        Mq = block_max<kVThreads>(lm, redz);
+        float ls = 0.f;
+        for (int vv = t; vv < a.V; vv += kVThreads) {
+          int f2 = 0;
+          const float y = qr ? sanitize_logit(qr[vv], f2) / a.T : -INFINITY;
+          ls += y > -INFINITY ? expf(y - Mq) : 0.f;
+        }
+        Sq = block_sum<kVThreads>(ls, redz);
+      }
+      // r_j(v): p(v) with j residual updates applied (zsh[i] = 1/Z_{i+1}, 0 = kept)
+      int nz = 0;
+      auto pval = [&](int vv) -> float {
+        int f2 = 0;
+        const float y = zr ? sanitize_logit(zr[vv], f2) / a.T : -INFINITY;
+        return y > -INFINITY ? expf(y - M) / S : 0.f;
+      };
+      auto qval = [&](int vv) -> float {
+        int f2 = 0;
+        const float y = qr ? sanitize_logit(qr[vv], f2) / a.T : -INFINITY;
+        return y > -INFINITY ? expf(y - Mq) / Sq : 0.f;
+      };
+      auto rval = [&](int vv, int upto) -> float {
+        float r = pval(vv);
+        if (upto > 0) {
+          const float q = qval(vv);
+          for (int s2 = 0; s2 < upto; ++s2)
+            if (zsh[s2] > 0.f) r = fmaxf(r - q, 0.f) * zsh[s2];
+        }
+        return r;
+      };
+      for (int j = cur + 1; j < N; ++j) {
+        if (par[j] != cur) continue;
+        const int x = tokf[j];
+        if (x < 0 || x >= a.V) { badw = 1; continue; }
+        const float qx = qval(x);
+        const float rx = rval(x, nz);
+        const float ratio = qx <= 0.f ? 1.f : fminf(1.f, rx / qx);
+        if (a.uniforms[fo + j] < ratio) { if (t == 0) s_next = j; break; }
+        // residual update: Z = sum_v max(r(v) - q(v), 0)
+        double loc = 0.0;
+        for (int vv = t; vv < a.V; vv += kVThreads) loc += (double)fmaxf(rval(vv, nz) - qval(vv), 0.f);
+        const double Z = block_sum_d<kVThreads>(loc, redd);
+        __syncthreads();
+        if (t == 0 && nz < kMaxTopk) zsh[nz] = Z > 0.0 ? (float)(1.0 / Z) : 0.f;
+        __syncthreads();
+        if (nz < kMaxTopk) ++nz;
+      }
+      __syncthreads();
+      if (s_next < 0) {
+        const int nzf = nz;
+        bonus = block_inverse_cdf(a.V, a.uniforms[fo], [&](int vv) -> float { return rval(vv, nzf); }, redd, redi);
+      }
+    }
+    __syncthreads();
+    const int nxt = s_next;
+    if (nxt < 0 || alen >= a.D) {
+      if (nxt >= 0) bonus = -1;  // cannot happen: the tree is at most D deep
+      if (t == 0) a.tokens[(long long)b * (a.D + 1) + alen] = bonus;
+      break;
+    }
+    if (t == 0) {
+      a.tokens[(long long)b * (a.D + 1) + alen] = tokf[nxt];
+      s_cur = nxt;
+    }
+    ++alen;
+    __syncthreads();
+  }
+  if (t == 0) {
+    a.accept_len[b] = alen;
+    for (int j = alen + 1; j <= a.D; ++j) {
+      a.path[(long long)b * (a.D + 1) + j] = -1;
+      a.tokens[(long long)b * (a.D + 1) + j] = -1;
+    }
+  }
+  if (badw && t == 0) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
+  (void)lane;
+}
+
+}  // namespace et
+
+using namespace et;
+
+extern "C" et_status et_verify_accept(const et_tree_cfg *cfg, et_accept_mode mode, const et_tree *tree,
+                                      const float *target_logits, int64_t target_stride,
+                                      const int32_t *target_row_of_node, const float *draft_logits,
+                                      int64_t draft_stride, const int32_t *draft_row_of_node,
+                                      const float *uniforms, int32_t *accept_len, int32_t *path, int32_t *tokens,
+                                      int32_t *dev_status, void *ws, size_t ws_bytes, et_stream_t stream) {
+  Geometry g;
+  ET_RETURN_IF(!make_geometry(cfg, &g), ET_ERR_INVALID_ARG);
+  ET_RETURN_IF(mode != ET_ACCEPT_GREEDY && mode != ET_ACCEPT_STOCH_POINT && mode != ET_ACCEPT_STOCH_DRAFTQ,
+               ET_ERR_INVALID_ARG);
+  ET_RETURN_IF(!tree || !tree->flat_node || !tree->flat_tok || !tree->flat_parent, ET_ERR_INVALID_ARG);
+  ET_RETURN_IF(!target_logits || target_stride < cfg->V || !et_aligned(target_logits, 4), ET_ERR_INVALID_ARG);
+  ET_RETURN_IF(!accept_len || !path || !tokens, ET_ERR_INVALID_ARG);
+  ET_RETURN_IF(mode != ET_ACCEPT_GREEDY && !uniforms, ET_ERR_INVALID_ARG);
+  ET_RETURN_IF(mode == ET_ACCEPT_STOCH_DRAFTQ && (!draft_logits || draft_stride < cfg->V), ET_ERR_INVALID_ARG);
+  size_t cnt_bytes, part_off, rowstat_off;
+  const size_t need = et_internal_tree_ws(cfg, &cnt_bytes, &part_off, &rowstat_off);
+  ET_RETURN_IF(!ws || ws_bytes < need || !et_aligned(ws, 256), ET_ERR_WORKSPACE);
+  const int N = cfg->n + 1;
+  ET_RETURN_IF((long long)cfg->B * N > 65535, ET_ERR_UNSUPPORTED);
+  VerifyArgs a;
+  a.mode = (int)mode;
+  a.B = cfg->B; a.V = cfg->V; a.N = N; a.C = g.C; a.D = cfg->depth;
+  a.nchunk = (cfg->V + kVChunk - 1) / kVChunk;
+  a.T = cfg->temperature;
+  a.tlog = target_logits; a.tstride = target_stride; a.tmap = target_row_of_node;
+  a.dlog = draft_logits; a.dstride = draft_stride; a.dmap = draft_row_of_node;
+  a.uniforms = uniforms;
+  a.flat_node = tree->flat_node; a.flat_tok = tree->flat_tok; a.flat_parent = tree->flat_parent;
+  a.accept_len = accept_len; a.path = path; a.tokens = tokens; a.dev_status = dev_status;
+  unsigned char *base = static_cast<unsigned char *>(ws);
+  const int rows = cfg->B * (cfg->m > N ? cfg->m : N);
+  a.row_cnt = reinterpret_cast<unsigned int *>(base);
+  a.seq_cnt = a.row_cnt + rows;
+  a.part = reinterpret_cast<float *>(base + part_off);
+  a.rowstat = reinterpret_cast<float *>(base + rowstat_off);
+  a.vec4t = et_aligned(target_logits, 16) && target_stride % 4 == 0;
+  dim3 grid(a.nchunk, cfg->B * N);
+  k_verify<<<grid, kVThreads, 0, (cudaStream_t)stream>>>(a);
+  return et_launch_status();
+}

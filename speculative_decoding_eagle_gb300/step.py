@@ -1,0 +1,165 @@
+"""One EAGLE-2 draft-tree verification step on the GPU, as a chain of the five
+C-ABI calls (EAGLE-2 article on sbmmt.com: expansion, reranking, attention
+mask / positions, ancestor-masked attention; EAGLE blog 1.2: lossless
+acceptance).
+
+``StepInputs`` holds the device copies of one batch of synthetic inputs;
+``VerifyStep`` owns the output and workspace buffers and runs the calls in
+stream order.  No arithmetic of the method happens here.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, Optional
+
+import numpy as np
+import torch
+
+from . import binding as E
+from . import workloads as W
+
+
+@dataclasses.dataclass
+class StepInputs:
+    """Device tensors of one batch (all synthetic, seeded)."""
+
+    draft: torch.Tensor          # fp32 [B*(C+1), V] node-indexed draft rows
+    target: torch.Tensor         # fp32 [B*(C+1), V] node-indexed target rows
+    row_of_node: torch.Tensor    # int32 [B, C+1]
+    root_tok: torch.Tensor       # int32 [B]
+    prefix_len: torch.Tensor     # int32 [B]
+    kv_row0: torch.Tensor        # int64 [B]
+    q: torch.Tensor              # [B, N, Hq, d]
+    k_prefix: torch.Tensor       # [rows, d]
+    v_prefix: torch.Tensor       # [rows, d]
+    k_tree: torch.Tensor         # [B, N, Hkv, d]
+    v_tree: torch.Tensor         # [B, N, Hkv, d]
+    uniforms: torch.Tensor       # fp32 [B, N]
+    host: Dict[str, np.ndarray]  # the numpy originals (for the oracle)
+
+
+def tree_cfg(wl: W.Workload, B: Optional[int] = None) -> E.TreeCfg:
+    return E.TreeCfg(B=wl.B if B is None else B, V=wl.V, depth=wl.depth, topk=wl.topk, m=wl.m, n=wl.n,
+                     temperature=wl.temperature)
+
+
+def host_inputs(wl: W.Workload, C: int, B: Optional[int] = None, b0: int = 0) -> Dict[str, np.ndarray]:
+    """numpy inputs of sequences ``b0 .. b0+B-1``; ``C`` is the tree's candidate count."""
+    B = wl.B if B is None else B
+    # only nodes that can be expanded need draft rows: every layer but the last
+    cfg = tree_cfg(wl, B)
+    num_draft = E.et_layer_base(cfg, wl.depth) if wl.depth > 1 else 0
+    target, draft, rmap = W.logit_tables(wl, C, num_draft, batch=range(b0, b0 + B))
+    prefix = W.prefix_lengths(wl, b0 + B)[b0:b0 + B]
+    qs, kps, vps, kts, vts = [], [], [], [], []
+    for i in range(B):
+        x = W.qkv(wl, b0 + i, int(prefix[i]))
+        qs.append(x["q"]); kps.append(x["k_prefix"]); vps.append(x["v_prefix"])
+        kts.append(x["k_tree"]); vts.append(x["v_tree"])
+    kv_row0 = np.zeros(B, np.int64)
+    acc = 0
+    for i in range(B):
+        kv_row0[i] = acc
+        acc += wl.Hkv * int(prefix[i])
+    dt = qs[0].dtype
+    return dict(draft=draft, target=target, row_of_node=rmap, root_tok=W.root_tokens(wl, b0 + B)[b0:b0 + B],
+                prefix_len=prefix, kv_row0=kv_row0, q=np.stack(qs),
+                k_prefix=np.concatenate([k.reshape(-1, wl.d) for k in kps]) if acc else np.zeros((0, wl.d), dt),
+                v_prefix=np.concatenate([v.reshape(-1, wl.d) for v in vps]) if acc else np.zeros((0, wl.d), dt),
+                k_tree=np.stack(kts), v_tree=np.stack(vts),
+                uniforms=np.stack([W.uniforms(wl, b0 + i) for i in range(B)]))
+
+
+def to_device(wl: W.Workload, h: Dict[str, np.ndarray], device="cuda") -> StepInputs:
+    def up(x, kind=None):
+        x = np.ascontiguousarray(x)
+        if kind == "bf16":  # uint16 bit patterns -> bf16 tensor
+            return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+        return torch.from_numpy(x).to(device)
+    kind = "bf16" if wl.dtype == "bf16" else None
+    kp = h["k_prefix"] if h["k_prefix"].size else np.zeros((1, wl.d), h["q"].dtype)
+    vp = h["v_prefix"] if h["v_prefix"].size else np.zeros((1, wl.d), h["q"].dtype)
+    return StepInputs(draft=up(h["draft"]), target=up(h["target"]), row_of_node=up(h["row_of_node"]),
+                      root_tok=up(h["root_tok"]), prefix_len=up(h["prefix_len"]), kv_row0=up(h["kv_row0"]),
+                      q=up(h["q"], kind), k_prefix=up(kp, kind), v_prefix=up(vp, kind),
+                      k_tree=up(h["k_tree"], kind), v_tree=up(h["v_tree"], kind), uniforms=up(h["uniforms"]),
+                      host=h)
+
+
+class VerifyStep:
+    """Buffers and call chain of one verification step for a fixed shape."""
+
+    def __init__(self, wl: W.Workload, B: Optional[int] = None, mode: Optional[int] = None, device="cuda",
+                 num_splits: int = 0, max_prefix: Optional[int] = None):
+        self.wl = wl
+        self.cfg = tree_cfg(wl, B)
+        self.B = self.cfg.B
+        self.C = E.et_num_candidates(self.cfg)
+        if self.C < 0:
+            raise ValueError(f"workload {wl.name} is outside the library limits")
+        if mode is None:
+            mode = E.ET_ACCEPT_GREEDY if "greedy" in wl.accept else E.ET_ACCEPT_STOCH_POINT
+        self.mode = mode
+        self.device = device
+        N = self.cfg.N
+        self.tree = E.TreeBuffers.allocate(self.cfg, device)
+        self.ws = E.new_workspace(E.et_tree_workspace_size(self.cfg), device)
+        self.mask = torch.zeros((self.B, N, (N + 63) // 64), dtype=torch.int64, device=device)
+        self.posids = torch.zeros((self.B, N), dtype=torch.int32, device=device)
+        dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+        self.out = torch.zeros((self.B, N, wl.Hq, wl.d), dtype=dt, device=device)
+        self.lse = torch.zeros((self.B, wl.Hq, N), dtype=torch.float32, device=device)
+        self.accept_len = torch.zeros(self.B, dtype=torch.int32, device=device)
+        self.path = torch.zeros((self.B, wl.depth + 1), dtype=torch.int32, device=device)
+        self.tokens = torch.zeros((self.B, wl.depth + 1), dtype=torch.int32, device=device)
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.max_prefix = max_prefix
+        self.num_splits = num_splits
+        self.attn_ws = None
+        self.shape = None
+
+    def attn_shape(self, inp: StepInputs) -> E.AttnShape:
+        mp = self.max_prefix if self.max_prefix is not None else int(inp.host["prefix_len"].max())
+        return E.AttnShape(B=self.B, N=self.cfg.N, Hq=self.wl.Hq, Hkv=self.wl.Hkv, d=self.wl.d,
+                           dtype=E.ET_BF16 if self.wl.dtype == "bf16" else E.ET_F32, scale=self.wl.d ** -0.5,
+                           max_prefix=mp, kv_rows=inp.k_prefix.shape[0], num_splits=self.num_splits)
+
+    def prepare(self, inp: StepInputs) -> None:
+        shape = self.attn_shape(inp)
+        if self.shape != shape:
+            self.shape = shape
+            self.attn_ws = E.new_workspace(E.et_tree_attention_workspace_size(shape), self.device)
+        self.tree.root_tok = inp.root_tok
+
+    # the five calls -------------------------------------------------------
+    def build_tree(self, inp: StepInputs, stream=None) -> None:
+        self.tree.root_tok = inp.root_tok
+        for layer in range(self.cfg.depth):
+            E.et_tree_expand(self.cfg, layer, inp.draft, self.tree, self.ws, row_of_node=inp.row_of_node,
+                             dev_status=self.dev_status, stream=stream)
+        E.et_tree_rerank(self.cfg, self.tree, dev_status=self.dev_status, stream=stream)
+        E.et_tree_mask_posids(self.cfg, self.tree, inp.prefix_len, self.mask, self.posids, stream=stream)
+
+    def attention(self, inp: StepInputs, stream=None) -> None:
+        E.et_tree_attention(self.shape, inp.q, inp.k_prefix, inp.v_prefix, inp.kv_row0, inp.prefix_len,
+                            inp.k_tree, inp.v_tree, self.mask, self.out, lse=self.lse, ws=self.attn_ws,
+                            dev_status=self.dev_status, stream=stream)
+
+    def accept(self, inp: StepInputs, stream=None) -> None:
+        E.et_verify_accept(self.cfg, self.mode, self.tree, inp.target, self.accept_len, self.path, self.tokens,
+                           self.ws, target_row_of_node=inp.row_of_node,
+                           draft_logits=inp.draft if self.mode == E.ET_ACCEPT_STOCH_DRAFTQ else None,
+                           draft_row_of_node=inp.row_of_node if self.mode == E.ET_ACCEPT_STOCH_DRAFTQ else None,
+                           uniforms=inp.uniforms if self.mode != E.ET_ACCEPT_GREEDY else None,
+                           dev_status=self.dev_status, stream=stream)
+
+    def run(self, inp: StepInputs, stream=None) -> None:
+        """The whole step: D expands, rerank, mask/posids, attention, acceptance."""
+        self.prepare(inp)
+        self.build_tree(inp, stream)
+        self.attention(inp, stream)
+        self.accept(inp, stream)
+
+    def launches(self) -> int:
+        """Kernel launches of one step."""
+        return self.cfg.depth + 4

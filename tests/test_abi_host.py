@@ -1,0 +1,128 @@
+"""The C ABI without a GPU: the library builds and loads, exports every symbol
+the header declares, computes the tree geometry like the oracle, and rejects
+bad arguments on the host before any launch (host-side fault injection)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle as O
+from speculative_decoding_eagle_gb300 import binding as E
+from speculative_decoding_eagle_gb300 import build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 0x100000  # a non-null, 256-byte aligned address that is never dereferenced
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return E.load()
+
+
+def _declared():
+    txt = open(os.path.join(ROOT, "include", "eagle_tree.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return set(re.findall(r"^\s*(?:et_status|int32_t|size_t|const char \*)\s*(et_\w+)\s*\(", txt, flags=re.M))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 14
+    assert names == set(E.EXPORTED)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert lib.et_abi_version() == 1
+
+
+@pytest.mark.parametrize("D,k,m,n", [(4, 4, 4, 16), (6, 10, 10, 60), (8, 8, 8, 80), (1, 32, 1, 32), (16, 2, 2, 50),
+                                     (3, 5, 25, 100)])
+def test_geometry_matches_oracle(lib, D, k, m, n):
+    cfg = E.TreeCfg(B=3, V=1000, depth=D, topk=k, m=m, n=n)
+    oc = O.TreeCfg(B=3, V=1000, depth=D, topk=k, m=m, n=n)
+    assert E.et_num_candidates(cfg) == O.num_candidates(oc)
+    for layer in range(D):
+        assert E.et_layer_expanded(cfg, layer) == O.expanded_count(oc, layer)
+        if layer >= 1:
+            assert E.et_layer_base(cfg, layer) == O.layer_base(oc, layer)
+    assert E.et_layer_expanded(cfg, D) == -1
+    assert E.et_tree_workspace_size(cfg) > 0
+
+
+@pytest.mark.parametrize("bad", [dict(topk=0), dict(topk=33), dict(m=33), dict(depth=0), dict(depth=17),
+                                 dict(n=0), dict(n=128), dict(V=3, topk=4), dict(temperature=0.0), dict(B=0),
+                                 dict(depth=8, topk=32, m=32, n=10)])
+def test_invalid_cfg_rejected(lib, bad):
+    base = dict(B=1, V=1000, depth=4, topk=4, m=4, n=16, temperature=1.0)
+    base.update(bad)
+    cfg = E.TreeCfg(**base)
+    assert E.et_num_candidates(cfg) == -1
+    tree = E.TreeC(*([FAKE] * 10))
+    st = lib.et_tree_expand(ctypes.byref(cfg.c()), 0, FAKE, 1000, None, ctypes.byref(tree), None, FAKE, 1 << 20, None)
+    assert st == E.ET_ERR_INVALID_ARG
+
+
+def test_expand_argument_checks(lib):
+    cfg = E.TreeCfg(B=2, V=1000, depth=3, topk=4, m=4, n=10)
+    need = E.et_tree_workspace_size(cfg)
+    tree = E.TreeC(*([FAKE] * 10))
+    call = lambda layer=0, logits=FAKE, stride=1000, ws=FAKE, wsb=need, tr=tree: lib.et_tree_expand(
+        ctypes.byref(cfg.c()), layer, logits, stride, None, ctypes.byref(tr), None, ws, wsb, None)
+    assert call(layer=3) == E.ET_ERR_INVALID_ARG
+    assert call(layer=-1) == E.ET_ERR_INVALID_ARG
+    assert call(logits=None) == E.ET_ERR_INVALID_ARG
+    assert call(stride=999) == E.ET_ERR_INVALID_ARG
+    assert call(logits=FAKE + 2) == E.ET_ERR_INVALID_ARG      # not 4-byte aligned
+    assert call(ws=None) == E.ET_ERR_WORKSPACE
+    assert call(wsb=need - 1) == E.ET_ERR_WORKSPACE
+    assert call(ws=FAKE + 16) == E.ET_ERR_WORKSPACE          # not 256-byte aligned
+    t2 = E.TreeC(*([FAKE] * 10))
+    t2.cand_key = None
+    assert call(tr=t2) == E.ET_ERR_INVALID_ARG
+
+
+def test_attention_argument_checks(lib):
+    def shape(**kw):
+        s = dict(B=1, N=61, Hq=32, Hkv=32, d=128, dtype=E.ET_BF16, scale=0.088, max_prefix=1024,
+                 kv_rows=32 * 1024, kv_head_stride=0, num_splits=0)
+        s.update(kw)
+        return E.AttnShapeC(*s.values())
+
+    def call(sh, q=FAKE, ws=FAKE, wsb=1 << 30):
+        return lib.et_tree_attention(ctypes.byref(sh), q, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None,
+                                     ws, wsb, None)
+    assert call(shape(d=96)) == E.ET_ERR_UNSUPPORTED
+    assert call(shape(N=129)) == E.ET_ERR_INVALID_ARG
+    assert call(shape(N=0)) == E.ET_ERR_INVALID_ARG
+    assert call(shape(Hq=30, Hkv=4)) == E.ET_ERR_INVALID_ARG
+    assert call(shape(scale=0.0)) == E.ET_ERR_INVALID_ARG
+    assert call(shape(), q=FAKE + 8) == E.ET_ERR_INVALID_ARG   # bf16 tiles need 16-byte alignment
+    assert call(shape(), q=None) == E.ET_ERR_INVALID_ARG
+    assert call(shape(), ws=None) == E.ET_ERR_WORKSPACE
+    sz = lib.et_tree_attention_workspace_size(ctypes.byref(shape(num_splits=4)))
+    assert sz > 0
+    assert call(shape(num_splits=4), wsb=sz - 1) == E.ET_ERR_WORKSPACE
+    assert lib.et_tree_attention_splits(ctypes.byref(shape(num_splits=4))) == 4
+    assert lib.et_tree_attention_workspace_size(ctypes.byref(shape(num_splits=1))) == 0
+    assert lib.et_tree_attention_splits(ctypes.byref(shape(dtype=E.ET_F32))) == 1
+
+
+def test_verify_argument_checks(lib):
+    cfg = E.TreeCfg(B=1, V=1000, depth=3, topk=4, m=4, n=10)
+    need = E.et_tree_workspace_size(cfg)
+    tree = E.TreeC(*([FAKE] * 10))
+
+    def call(mode=E.ET_ACCEPT_GREEDY, uni=None, draft=None, wsb=need):
+        return lib.et_verify_accept(ctypes.byref(cfg.c()), mode, ctypes.byref(tree), FAKE, 1000, None, draft, 1000,
+                                    None, uni, FAKE, FAKE, FAKE, None, FAKE, wsb, None)
+    assert call(mode=7) == E.ET_ERR_INVALID_ARG
+    assert call(mode=E.ET_ACCEPT_STOCH_POINT) == E.ET_ERR_INVALID_ARG         # no uniforms
+    assert call(mode=E.ET_ACCEPT_STOCH_DRAFTQ, uni=FAKE) == E.ET_ERR_INVALID_ARG  # no draft table
+    assert call(wsb=need - 1) == E.ET_ERR_WORKSPACE
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert E.status_string(s)
+    assert E.status_string(99) == "unknown status"

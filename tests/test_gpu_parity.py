@@ -1,0 +1,335 @@
+"""CUDA path vs the CPU oracle on the same seeded inputs, through the C ABI.
+
+Bars: token ids, parents, frontiers, flat trees, masks, position ids and
+accepted tokens bit-exact; log-probs within 1e-5; bf16 attention within
+max-abs 2e-2 and rel-L2 5e-3 (fp32 path: 1e-4 / 1e-5).  Every case states
+the near-tie margins the oracle reports, so a bit-exact comparison is only
+demanded where fp32 rounding cannot decide it.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from speculative_decoding_eagle_gb300 import binding as E
+from speculative_decoding_eagle_gb300 import step as S
+from speculative_decoding_eagle_gb300 import workloads as W
+from tests.parity_util import (BF16_MAX_ABS, BF16_REL_L2, F32_MAX_ABS, F32_REL_L2, KEY_TOL_PER_LEVEL, compare_layer,
+                               gpu_tree_np, ocfg, oracle_attention_from_host, out_as_float, rel_l2,
+                               upload_oracle_tree)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from speculative_decoding_eagle_gb300 import build_lib
+    build_lib.build()
+    E.load()
+
+
+def _random_table(rows, V, seed, scale=2.0, ties=False):
+    rng = np.random.default_rng(seed)
+    if ties:
+        return rng.integers(-4, 4, (rows, V)).astype(np.float32)
+    return (rng.standard_normal((rows, V)) * scale).astype(np.float32)
+
+
+def _rmap(B, C):
+    return (np.arange(B)[:, None] * (C + 1) + np.arange(C + 1)[None, :]).astype(np.int32)
+
+
+# ---------------------------------------------------------------------------
+# expand, layer by layer, given the oracle's state before each layer
+# ---------------------------------------------------------------------------
+EXPAND_CASES = [
+    # (B, V, D, k, m, n, ties, stride_pad)
+    (1, 1000, 4, 4, 4, 16, False, 0),          # tiny shape
+    (2, 32000, 3, 10, 10, 60, False, 0),       # 7B vocabulary, ragged last chunk (32000 % 2048)
+    (3, 4099, 3, 7, 5, 20, False, 3),          # V % 4 != 0, unaligned row stride (scalar loads)
+    (2, 300, 3, 32, 32, 100, True, 0),         # k = m = 32, many tied logits
+    (1, 5000, 4, 1, 1, 4, False, 0),           # chain tree (k = 1)
+    (4, 2048, 3, 3, 8, 12, False, 0),          # m > layer width
+]
+
+
+@pytest.mark.parametrize("B,V,D,k,m,n,ties,pad", EXPAND_CASES)
+def test_expand_each_layer_matches_oracle(B, V, D, k, m, n, ties, pad):
+    cfg = E.TreeCfg(B=B, V=V, depth=D, topk=k, m=m, n=n)
+    C = E.et_num_candidates(cfg)
+    assert C == O.num_candidates(ocfg(cfg))
+    table = _random_table(B * (C + 1), V, seed=V + k, ties=ties)
+    rmap = _rmap(B, C)
+    # device table with optional row padding (row stride V + pad)
+    dev = torch.zeros((B * (C + 1), V + pad), dtype=torch.float32, device="cuda")
+    dev[:, :V] = torch.from_numpy(table)
+    dev_t = dev[:, :V] if pad else dev
+    tb = E.TreeBuffers.allocate(cfg)
+    ws = E.new_workspace(E.et_tree_workspace_size(cfg))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ot = O.Tree.empty(ocfg(cfg))
+    for layer in range(D):
+        upload_oracle_tree(ot, tb)
+        O.tree_expand(ot, layer, table, rmap)
+        E.et_tree_expand(cfg, layer, dev_t, tb, ws, row_of_node=torch.from_numpy(rmap).cuda(), dev_status=status)
+        ties_here = [x for x in O.near_tie_selections(ot) if x[1] == "frontier" and x[3] == layer + 1]
+        compare_layer(cfg, layer, gpu_tree_np(tb), ot, check_frontier=not ties_here)
+    assert int(status.item()) == 0
+
+
+def test_expand_slot_ordered_rows_and_nonfinite():
+    """Rows given in expansion order (no row map), with NaN / +-inf logits."""
+    B, V = 2, 3000
+    cfg = E.TreeCfg(B=B, V=V, depth=2, topk=5, m=3, n=8)
+    C = E.et_num_candidates(cfg)
+    ot = O.Tree.empty(ocfg(cfg))
+    tb = E.TreeBuffers.allocate(cfg)
+    ws = E.new_workspace(E.et_tree_workspace_size(cfg))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = _random_table(B, V, 1)
+    t0[0, 17] = np.nan
+    t0[1, 5] = -np.inf
+    t0[1, 6] = np.inf
+    O.tree_expand(ot, 0, t0, None)
+    E.et_tree_expand(cfg, 0, torch.from_numpy(t0).cuda(), tb, ws, dev_status=status)
+    compare_layer(cfg, 0, gpu_tree_np(tb), ot)
+    assert int(status.item()) & E.ET_DEV_NONFINITE
+    t1 = _random_table(B * 3, V, 2)
+    upload_oracle_tree(ot, tb)
+    O.tree_expand(ot, 1, t1, None)
+    E.et_tree_expand(cfg, 1, torch.from_numpy(t1).cuda(), tb, ws)
+    compare_layer(cfg, 1, gpu_tree_np(tb), ot)
+    assert C == 5 + 15
+
+
+def test_expand_all_neg_inf_row():
+    cfg = E.TreeCfg(B=1, V=100, depth=1, topk=3, m=1, n=3)
+    tb = E.TreeBuffers.allocate(cfg)
+    ws = E.new_workspace(E.et_tree_workspace_size(cfg))
+    z = np.full((1, 100), -np.inf, np.float32)
+    E.et_tree_expand(cfg, 0, torch.from_numpy(z).cuda(), tb, ws)
+    g = gpu_tree_np(tb)
+    assert list(g["cand_tok"][0]) == [0, 1, 2]
+    assert (g["cand_key"][0] == O.KEY_MIN).all()
+
+
+# ---------------------------------------------------------------------------
+# rerank + mask/posids, given the oracle's keys
+# ---------------------------------------------------------------------------
+RERANK_CASES = [(1, 4, 4, 4, 16), (3, 6, 10, 10, 60), (2, 8, 8, 8, 80), (2, 6, 10, 10, 100), (1, 3, 2, 2, 14),
+                (2, 16, 2, 1, 9), (1, 2, 32, 32, 127)]
+
+
+@pytest.mark.parametrize("B,D,k,m,n", RERANK_CASES)
+@pytest.mark.parametrize("ties", [False, True])
+def test_rerank_mask_posids_match_oracle(B, D, k, m, n, ties):
+    V = 64
+    cfg = E.TreeCfg(B=B, V=V, depth=D, topk=k, m=m, n=n)
+    C = E.et_num_candidates(cfg)
+    table = _random_table(B * (C + 1), V, seed=D * 100 + k, ties=ties)
+    if ties:  # many equal values across parents: shallow-first tie-break must hold
+        table[:] = np.round(table)
+    root = np.arange(B, dtype=np.int32) + 7
+    ot = O.build_tree(ocfg(cfg), table, _rmap(B, C), root)
+    tb = E.TreeBuffers.allocate(cfg, root_tok=torch.from_numpy(root).cuda())
+    upload_oracle_tree(ot, tb)
+    tb.flat_node.fill_(-5)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    E.et_tree_rerank(cfg, tb, dev_status=status)
+    g = gpu_tree_np(tb)
+    for name, want in (("flat_node", ot.flat_node), ("flat_tok", ot.flat_tok), ("flat_parent", ot.flat_parent),
+                       ("flat_depth", ot.flat_depth)):
+        np.testing.assert_array_equal(g[name], want, err_msg=name)
+    assert int(status.item()) == 0
+    prefix = (np.arange(B, dtype=np.int32) * 37 + 5)
+    N = cfg.N
+    mask = torch.zeros((B, N, (N + 63) // 64), dtype=torch.int64, device="cuda")
+    pos = torch.zeros((B, N), dtype=torch.int32, device="cuda")
+    E.et_tree_mask_posids(cfg, tb, torch.from_numpy(prefix).cuda(), mask, pos)
+    om, op = O.mask_posids(ot.flat_parent, ot.flat_depth, prefix)
+    np.testing.assert_array_equal(mask.cpu().numpy().view(np.uint64), om)
+    np.testing.assert_array_equal(pos.cpu().numpy(), op)
+
+
+# ---------------------------------------------------------------------------
+# attention
+# ---------------------------------------------------------------------------
+def _attn_case(B, N, Hq, Hkv, d, prefixes, dtype, seed, splits=0, head_stride=0):
+    rng = np.random.default_rng(seed)
+    wl = W.Workload("t", 99, V=16, Hq=Hq, Hkv=Hkv, d=d, prefix=0, dtype=dtype, depth=3, topk=2, m=2, n=N - 1,
+                    sigma=0.5, accept=("greedy",), B=B)
+    # random tree topology: parent of row i uniform in [0, i)
+    fp = np.full((B, N), -1, np.int32)
+    depth = np.zeros((B, N), np.int32)
+    for b in range(B):
+        for i in range(1, N):
+            fp[b, i] = rng.integers(0, i)
+            depth[b, i] = depth[b, fp[b, i]] + 1
+    mask, _ = O.mask_posids(fp, depth, np.zeros(B, np.int32))
+    L = np.asarray(prefixes, np.int32)
+    hs = head_stride
+    rows_per_seq = [Hkv * (hs if hs else int(L[b])) for b in range(B)]
+    kv_row0 = np.concatenate([[0], np.cumsum(rows_per_seq)[:-1]]).astype(np.int64)
+    total = max(int(sum(rows_per_seq)), 1)
+    f32 = lambda *s: rng.standard_normal(s).astype(np.float32)
+    enc = (lambda x: W.bf16_bits(x)) if dtype == "bf16" else (lambda x: x)
+    h = dict(q=enc(f32(B, N, Hq, d)), k_tree=enc(f32(B, N, Hkv, d)), v_tree=enc(f32(B, N, Hkv, d)),
+             k_prefix=enc(f32(total, d)), v_prefix=enc(f32(total, d)), prefix_len=L, kv_row0=kv_row0)
+    # oracle view of the prefix (respecting the head stride)
+    kpf, vpf = W.as_float(wl, h["k_prefix"]), W.as_float(wl, h["v_prefix"])
+    kp, vp = [], []
+    for b in range(B):
+        stride = hs if hs else int(L[b])
+        idx = kv_row0[b] + np.arange(Hkv)[:, None] * stride + np.arange(int(L[b]))[None, :]
+        kp.append(kpf[idx].astype(np.float64))
+        vp.append(vpf[idx].astype(np.float64))
+    ref, lse = O.tree_attention(W.as_float(wl, h["q"]).astype(np.float64), kp, vp,
+                                W.as_float(wl, h["k_tree"]).astype(np.float64),
+                                W.as_float(wl, h["v_tree"]).astype(np.float64), mask, d ** -0.5)
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+
+    def up(x):
+        if dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).cuda()
+        return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+    shape = E.AttnShape(B=B, N=N, Hq=Hq, Hkv=Hkv, d=d, dtype=E.ET_BF16 if dtype == "bf16" else E.ET_F32,
+                        scale=d ** -0.5, max_prefix=int(L.max()) if B else 0, kv_rows=total,
+                        kv_head_stride=hs, num_splits=splits)
+    out = torch.full((B, N, Hq, d), float("nan"), dtype=dt, device="cuda")
+    lse_g = torch.zeros((B, Hq, N), dtype=torch.float32, device="cuda")
+    ws = E.new_workspace(E.et_tree_attention_workspace_size(shape))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    E.et_tree_attention(shape, up(h["q"]), up(h["k_prefix"]), up(h["v_prefix"]),
+                        torch.from_numpy(kv_row0).cuda(), torch.from_numpy(L).cuda(), up(h["k_tree"]),
+                        up(h["v_tree"]), torch.from_numpy(mask.view(np.int64)).cuda(), out, lse=lse_g, ws=ws,
+                        dev_status=status)
+    torch.cuda.synchronize()
+    return out_as_float(out), lse_g.cpu().numpy(), ref, lse, int(status.item())
+
+
+ATTN_CASES = [
+    # B, N, Hq, Hkv, d, prefixes, dtype, splits, head_stride
+    (1, 17, 4, 4, 64, [128], "f32", 0, 0),          # tiny shape
+    (2, 9, 2, 1, 128, [70, 3], "f32", 0, 0),
+    (1, 61, 32, 32, 128, [1024], "bf16", 0, 0),     # 7B shape at its bench prefix
+    (1, 61, 4, 4, 128, [1000], "bf16", 1, 0),       # single split, ragged last tile
+    (1, 61, 4, 4, 128, [1000], "bf16", 7, 0),       # uneven splits
+    (2, 81, 16, 2, 128, [300, 129], "bf16", 0, 0),  # GQA group 8, two row tiles, N > 64
+    (3, 101, 4, 4, 128, [64, 0, 513], "bf16", 0, 0),  # empty prefix, N = 101 (two mask words)
+    (2, 33, 8, 2, 64, [200, 77], "bf16", 3, 0),     # d = 64
+    (2, 20, 4, 2, 128, [100, 60], "bf16", 2, 128),  # static cache layout (head stride)
+    (1, 128, 2, 2, 128, [257], "bf16", 0, 0),       # maximum N
+]
+
+
+@pytest.mark.parametrize("B,N,Hq,Hkv,d,prefixes,dtype,splits,hs", ATTN_CASES)
+def test_attention_matches_oracle(B, N, Hq, Hkv, d, prefixes, dtype, splits, hs):
+    got, lse_g, ref, lse_o, status = _attn_case(B, N, Hq, Hkv, d, prefixes, dtype, seed=N * 7 + d, splits=splits,
+                                                head_stride=hs)
+    assert status == 0
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref).max()
+    rl = rel_l2(got, ref)
+    if dtype == "bf16":
+        assert err <= BF16_MAX_ABS and rl <= BF16_REL_L2, (err, rl)
+    else:
+        assert err <= F32_MAX_ABS and rl <= F32_REL_L2, (err, rl)
+    assert np.abs(lse_g - lse_o).max() < 1e-3
+
+
+# ---------------------------------------------------------------------------
+# acceptance, given the oracle's flat tree
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("mode", [E.ET_ACCEPT_GREEDY, E.ET_ACCEPT_STOCH_POINT, E.ET_ACCEPT_STOCH_DRAFTQ])
+@pytest.mark.parametrize("wl_name,B", [("tiny", 4), ("llama2-7b", 2)])
+def test_verify_matches_oracle(mode, wl_name, B):
+    wl = W.WORKLOADS[wl_name].with_(B=B, temperature=0.7 if mode == E.ET_ACCEPT_STOCH_DRAFTQ else 1.0)
+    cfg = S.tree_cfg(wl)
+    C = E.et_num_candidates(cfg)
+    h = S.host_inputs(wl, C)
+    ot = O.build_tree(ocfg(cfg), h["draft"], h["row_of_node"], h["root_tok"])
+    ref = O.verify_accept(ocfg(cfg), mode, ot.flat_tok, ot.flat_parent, ot.flat_node, h["target"], h["row_of_node"],
+                          uniforms=h["uniforms"], draft_table=h["draft"], draft_row_of_node=h["row_of_node"])
+    inp = S.to_device(wl, h)
+    st = S.VerifyStep(wl, mode=mode)
+    upload_oracle_tree(ot, st.tree)
+    st.accept(inp)
+    torch.cuda.synchronize()
+    bad_b = {b for b, _, _ in ref.near_ties}
+    for b in range(B):
+        if b in bad_b:
+            continue
+        assert st.accept_len[b].item() == ref.accept_len[b]
+        np.testing.assert_array_equal(st.path[b].cpu().numpy(), ref.path[b])
+        np.testing.assert_array_equal(st.tokens[b].cpu().numpy(), ref.tokens[b])
+    assert len(bad_b) < B
+    assert int(st.dev_status.item()) == 0
+
+
+# ---------------------------------------------------------------------------
+# the whole step, every configuration
+# ---------------------------------------------------------------------------
+STEP_CASES = [("tiny", None, None), ("tiny", None, E.ET_ACCEPT_STOCH_POINT), ("llama2-7b", None, None),
+              ("llama2-13b", None, None), ("llama2-70b", None, None), ("llama2-70b", None, E.ET_ACCEPT_STOCH_POINT),
+              ("sweep-7b", 4, None)]
+
+
+@pytest.mark.parametrize("wl_name,B,mode", STEP_CASES)
+def test_full_step_matches_oracle(wl_name, B, mode):
+    wl = W.WORKLOADS[wl_name]
+    if B is not None:
+        wl = wl.with_(B=B)
+    st = S.VerifyStep(wl, mode=mode)
+    cfg = st.cfg
+    h = S.host_inputs(wl, st.C)
+    inp = S.to_device(wl, h)
+    st.run(inp)
+    torch.cuda.synchronize()
+    oc = ocfg(cfg)
+    ot = O.build_tree(oc, h["draft"], h["row_of_node"], h["root_tok"])
+    assert not O.near_tie_selections(ot), O.near_tie_selections(ot)
+    g = gpu_tree_np(st.tree)
+    for name, want in (("flat_node", ot.flat_node), ("flat_tok", ot.flat_tok), ("flat_parent", ot.flat_parent),
+                       ("flat_depth", ot.flat_depth), ("cand_tok", ot.tok), ("cand_parent", ot.parent)):
+        np.testing.assert_array_equal(g[name], want, err_msg=name)
+    assert np.abs(g["cand_lp"].astype(np.float64) - ot.lp).max() <= 1e-5
+    assert np.abs(g["cand_key"] - ot.key).max() <= KEY_TOL_PER_LEVEL * cfg.depth
+    om, op = O.mask_posids(ot.flat_parent, ot.flat_depth, h["prefix_len"])
+    np.testing.assert_array_equal(st.mask.cpu().numpy().view(np.uint64), om)
+    np.testing.assert_array_equal(st.posids.cpu().numpy(), op)
+    ref, _ = oracle_attention_from_host(wl, h, om, cfg.B)
+    got = out_as_float(st.out)
+    tol = (BF16_MAX_ABS, BF16_REL_L2) if wl.dtype == "bf16" else (F32_MAX_ABS, F32_REL_L2)
+    assert np.abs(got - ref).max() <= tol[0] and rel_l2(got, ref) <= tol[1]
+    acc = O.verify_accept(oc, st.mode, ot.flat_tok, ot.flat_parent, ot.flat_node, h["target"], h["row_of_node"],
+                          uniforms=h["uniforms"])
+    assert not acc.near_ties, acc.near_ties
+    np.testing.assert_array_equal(st.accept_len.cpu().numpy(), acc.accept_len)
+    np.testing.assert_array_equal(st.path.cpu().numpy(), acc.path)
+    np.testing.assert_array_equal(st.tokens.cpu().numpy(), acc.tokens)
+    assert int(st.dev_status.item()) == 0
+
+
+def test_step_is_deterministic_and_graph_capturable():
+    wl = W.WORKLOADS["llama2-7b"]
+    st = S.VerifyStep(wl)
+    h = S.host_inputs(wl, st.C)
+    inp = S.to_device(wl, h)
+    st.run(inp)
+    torch.cuda.synchronize()
+    first = (st.out.clone(), st.tokens.clone(), st.tree.flat_node.clone())
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        st.run(inp)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        st.run(inp)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(first[0], st.out) and torch.equal(first[1], st.tokens) and torch.equal(first[2], st.tree.flat_node)
