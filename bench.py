@@ -215,6 +215,8 @@ def run_gpu(args):
     wl = W.WORKLOADS[args.workload]
     if args.batch:
         wl = wl.with_(B=args.batch)
+    if args.prefix:
+        wl = wl.with_(prefix=args.prefix, ragged=False)
     mode = None if args.mode == "auto" else {"greedy": E.ET_ACCEPT_GREEDY, "stoch": E.ET_ACCEPT_STOCH_POINT,
                                               "draftq": E.ET_ACCEPT_STOCH_DRAFTQ}[args.mode]
     st = S.VerifyStep(wl, mode=mode, num_splits=args.splits)
@@ -408,6 +410,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--batch", type=int, default=0)
     ap.add_argument("--mode", default="auto", choices=["auto", "greedy", "stoch", "draftq"])
+    ap.add_argument("--prefix", type=int, default=0, help="override the workload's KV-prefix length")
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--sets", type=int, default=0)
     ap.add_argument("--eager", action="store_true")
