@@ -170,6 +170,37 @@ et_status et_tree_expand(const et_tree_cfg *cfg, int32_t layer,
                          void *ws, size_t ws_bytes, et_stream_t stream);
 
 /*
+ * et_tree_expand_noalloc -- et_tree_expand without a caller workspace.
+ * The pages have no counterpart: this is a deployment convenience.
+ *
+ * Some callers have no way to obtain device scratch memory: a plugin or
+ * custom operator that the host framework forbids to allocate inside its
+ * execute callback, a runtime that reserves all device memory up front and
+ * hands out only the tensors it manages, or code that must not call
+ * cudaMalloc while a stream is being captured.  This entry point computes
+ * exactly what et_tree_expand computes (same kernel, same arguments minus
+ * `ws`), taking its scratch from a 4 MiB array that the library places in
+ * device memory when it is loaded; it calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *
+ * Limit: 256-byte aligned counters (4 * (B*m_l + B) bytes) plus
+ * 4 * B * m_l * ceil(V / 2048) * (2 + 2k) bytes of partials must fit in
+ * 4 MiB (e.g. B*m_l <= 2900 at V = 32000, k = 10); larger shapes return
+ * ET_ERR_WORKSPACE and launch nothing.
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before capturing a stream into a CUDA graph.
+ * Sharing: every call on a device uses the same array and leaves its
+ * contents behind; each call clears the counters it needs on `stream`
+ * (cudaMemsetAsync) before its kernel.  Two calls whose work can overlap
+ * on the GPU (different streams, or concurrent host threads) race on the
+ * array: serialise them on one stream.
+ */
+et_status et_tree_expand_noalloc(const et_tree_cfg *cfg, int32_t layer,
+                                 const float *logits, int64_t row_stride, const int32_t *row_of_node,
+                                 et_tree *tree, int32_t *dev_status, et_stream_t stream);
+
+/*
  * et_tree_rerank -- reranking phase (EAGLE-2 article): keep the n candidates
  * with the largest (key desc, id asc) -- equal values keep the shallower
  * node, so the kept tree is connected -- and flatten them: row 0 is the

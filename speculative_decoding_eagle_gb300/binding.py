@@ -26,8 +26,8 @@ ET_ACCEPT_GREEDY, ET_ACCEPT_STOCH_POINT, ET_ACCEPT_STOCH_DRAFTQ = 0, 1, 2
 
 EXPORTED = ("et_num_candidates", "et_layer_expanded", "et_layer_base", "et_tree_workspace_size",
             "et_tree_attention_workspace_size", "et_tree_attention_splits", "et_workspace_init",
-            "et_status_string", "et_abi_version", "et_tree_expand", "et_tree_rerank", "et_tree_mask_posids",
-            "et_tree_attention", "et_verify_accept")
+            "et_status_string", "et_abi_version", "et_tree_expand", "et_tree_expand_noalloc", "et_tree_rerank",
+            "et_tree_mask_posids", "et_tree_attention", "et_verify_accept")
 
 
 class TreeCfgC(ctypes.Structure):
@@ -76,6 +76,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "et_status_string": (ctypes.c_char_p, [c_i32]),
         "et_abi_version": (c_i32, []),
         "et_tree_expand": (c_i32, [P(TreeCfgC), c_i32, c_vp, c_i64, c_vp, P(TreeC), c_vp, c_vp, c_sz, c_vp]),
+        "et_tree_expand_noalloc": (c_i32, [P(TreeCfgC), c_i32, c_vp, c_i64, c_vp, P(TreeC), c_vp, c_vp]),
         "et_tree_rerank": (c_i32, [P(TreeCfgC), P(TreeC), c_vp, c_vp]),
         "et_tree_mask_posids": (c_i32, [P(TreeCfgC), P(TreeC), c_vp, c_vp, c_vp, c_vp]),
         "et_tree_attention": (c_i32, [P(AttnShapeC), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
@@ -217,6 +218,27 @@ def et_tree_expand(cfg: TreeCfg, layer: int, logits: torch.Tensor, tree: TreeBuf
                                _ptr(dev_status, torch.int32, "dev_status"), _ptr(ws, None, "ws"),
                                ws.numel() * ws.element_size(), _stream(stream))
     _check("et_tree_expand", st)
+
+
+def et_tree_expand_noalloc(cfg: TreeCfg, layer: int, logits: torch.Tensor, tree: TreeBuffers,
+                           row_of_node: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None,
+                           stream=None) -> None:
+    """Same result as :func:`et_tree_expand` without a workspace argument.
+
+    For callers that cannot hand the library device scratch memory (their
+    framework forbids allocation inside its execute callback, all device
+    memory is pre-reserved, or a stream is being captured): the scratch is a
+    4 MiB array the library keeps on each device.  Calls on one device share
+    it, so they must not overlap on the GPU.
+    """
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be a [rows, >=V] fp32 table with unit inner stride")
+    if not logits.is_cuda or logits.dtype != torch.float32:
+        raise ValueError("logits must be a CUDA fp32 tensor")
+    st = load().et_tree_expand_noalloc(ctypes.byref(cfg.c()), layer, logits.data_ptr(), logits.stride(0),
+                                       _ptr(row_of_node, torch.int32, "row_of_node"), ctypes.byref(tree.c()),
+                                       _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check("et_tree_expand_noalloc", st)
 
 
 def et_tree_rerank(cfg: TreeCfg, tree: TreeBuffers, dev_status: Optional[torch.Tensor] = None, stream=None) -> None:

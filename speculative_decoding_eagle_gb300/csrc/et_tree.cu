@@ -568,3 +568,81 @@ extern "C" const char *et_status_string(et_status s) {
 }
 
 extern "C" int32_t et_abi_version(void) { return ET_ABI_VERSION; }
+
+// ---------------------------------------------------------------------------
+// et_tree_expand_noalloc: et_tree_expand with its scratch in a static device
+// array, for callers that must not allocate device memory themselves.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace et {
+// Scratch of et_tree_expand_noalloc: per-chunk partial results and arrival
+// counters.  Every GPU that loads this library holds one copy until exit.
+constexpr size_t kExpandScratchBytes = 4u << 20;  // 4 MiB
+static __device__ __align__(256) unsigned char g_expand_scratch[kExpandScratchBytes];
+
+constexpr int kMaxDevices = 64;
+static std::mutex g_scratch_mu;
+static void *g_scratch_ptr[kMaxDevices];  // device address of g_expand_scratch, per device
+
+// The array's name is only a host-side stand-in in host code; its device
+// address is looked up once per device, with that device current.
+static et_status expand_scratch(void **out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ET_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_expand_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return ET_ERR_CUDA;
+    }
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return ET_OK;
+}
+}  // namespace et
+
+extern "C" et_status et_tree_expand_noalloc(const et_tree_cfg *cfg, int32_t layer, const float *logits,
+                                            int64_t row_stride, const int32_t *row_of_node, et_tree *tree,
+                                            int32_t *dev_status, et_stream_t stream) {
+  Geometry g;
+  ET_RETURN_IF(!make_geometry(cfg, &g), ET_ERR_INVALID_ARG);
+  ET_RETURN_IF(layer < 0 || layer >= cfg->depth, ET_ERR_INVALID_ARG);
+  ET_RETURN_IF(!logits || row_stride < cfg->V || !tree_ptrs_ok(tree), ET_ERR_INVALID_ARG);
+  ET_RETURN_IF(!et_aligned(logits, 4), ET_ERR_INVALID_ARG);
+  const int m_l = g.expanded[layer];
+  ET_RETURN_IF((long long)cfg->B * m_l > 65535, ET_ERR_UNSUPPORTED);
+  // this launch's scratch: counters (rows + sequences), then the per-chunk partials
+  const int rows = cfg->B * m_l;
+  const int nchunk = nchunk_of(cfg->V);
+  const size_t cnt_bytes = align256(sizeof(unsigned int) * (size_t)(rows + cfg->B));
+  const size_t need = cnt_bytes + sizeof(float) * (size_t)rows * nchunk * (2 + 2 * cfg->topk);
+  ET_RETURN_IF(need > kExpandScratchBytes, ET_ERR_WORKSPACE);  // beyond the static scratch
+  void *scratch = nullptr;
+  const et_status s = expand_scratch(&scratch);
+  if (s != ET_OK) return s;
+  cudaStream_t st = (cudaStream_t)stream;
+  // counters must start at zero; clear them on the caller's stream (no allocation)
+  if (cudaMemsetAsync(scratch, 0, cnt_bytes, st) != cudaSuccess) return ET_ERR_CUDA;
+  ExpandArgs a;
+  a.logits = logits;
+  a.row_stride = row_stride;
+  a.row_of_node = row_of_node;
+  a.vec4 = et_aligned(logits, 16) && (row_stride % 4 == 0);
+  a.B = cfg->B; a.V = cfg->V; a.k = cfg->topk; a.m = cfg->m; a.C = g.C; a.layer = layer; a.m_l = m_l;
+  a.base_next = g.base[layer + 1];
+  a.m_next = (layer + 1 < cfg->depth) ? g.expanded[layer + 1] : 0;
+  a.nchunk = nchunk;
+  a.tree = *tree;
+  a.dev_status = dev_status;
+  unsigned char *base = static_cast<unsigned char *>(scratch);
+  a.row_cnt = reinterpret_cast<unsigned int *>(base);
+  a.seq_cnt = a.row_cnt + rows;
+  a.part = reinterpret_cast<float *>(base + cnt_bytes);
+  dim3 grid(a.nchunk, rows);
+  const size_t smem = (size_t)a.nchunk * a.k * (sizeof(float) + sizeof(int));
+  k_expand<<<grid, kExpThreads, smem, st>>>(a);
+  return et_launch_status();
+}
