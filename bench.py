@@ -219,7 +219,8 @@ def run_gpu(args):
         wl = wl.with_(prefix=args.prefix, ragged=False)
     mode = None if args.mode == "auto" else {"greedy": E.ET_ACCEPT_GREEDY, "stoch": E.ET_ACCEPT_STOCH_POINT,
                                               "draftq": E.ET_ACCEPT_STOCH_DRAFTQ}[args.mode]
-    st = S.VerifyStep(wl, mode=mode, num_splits=args.splits)
+    st = S.VerifyStep(wl, mode=mode, num_splits=args.splits,
+                      attn_impl={"auto": E.ATTN_AUTO, "mma": E.ATTN_MMA_SYNC, "tcgen05": E.ATTN_TCGEN05}[args.attn])
     cfg = st.cfg
     prefix = W.prefix_lengths(wl, cfg.B)
     expanded = sum(E.et_layer_expanded(cfg, l) for l in range(cfg.depth))
@@ -314,6 +315,8 @@ def run_gpu(args):
                    "prefix": int(prefix.max()), "depth": wl.depth, "topk": wl.topk, "m": wl.m, "n": wl.n,
                    "accept": {0: "greedy", 1: "stoch_point", 2: "stoch_draftq"}[st.mode],
                    "attention_splits": E.et_tree_attention_splits(st.shape),
+                   "attention_kernel": {0: "auto", 1: "mma.sync", 2: "tcgen05"}[st.attn_impl] if st.attn_impl else
+                   ("tcgen05" if wl.dtype == "bf16" and wl.d == 128 else "mma.sync"),
                    "l2": f"inputs larger than L2: {R} rotating input sets, {per_step / 1e6:.1f} MB read per step",
                    "cuda_graphs": bool(graphs), "parallelism": f"replicas x{world}"},
         "tree_attention": {"us_per_launch": round(attn_us, 3), "GBps": round(achieved, 1),
@@ -412,6 +415,7 @@ def main():
     ap.add_argument("--mode", default="auto", choices=["auto", "greedy", "stoch", "draftq"])
     ap.add_argument("--prefix", type=int, default=0, help="override the workload's KV-prefix length")
     ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--attn", default="auto", choices=["auto", "mma", "tcgen05"], help="attention kernel")
     ap.add_argument("--sets", type=int, default=0)
     ap.add_argument("--eager", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -121,6 +121,9 @@ typedef struct {
     int64_t kv_rows;          /* d-element rows in each of k_prefix / v_prefix (bounds check) */
     int64_t kv_head_stride;   /* rows between heads of one sequence's prefix; 0 = prefix_len[b] */
     int32_t num_splits;       /* KV splits per (sequence, head, row tile); 0 = library heuristic */
+    int32_t impl;             /* 0 = auto (tcgen05 for bf16 with d = 128, else mma.sync),
+                                 1 = mma.sync tensor-core path, 2 = tcgen05 path
+                                 (ET_ERR_UNSUPPORTED unless bf16 and d = 128) */
 } et_attn_shape;
 
 /* ---- geometry helpers (host, no device work) ---- */
@@ -243,8 +246,12 @@ et_status et_tree_mask_posids(const et_tree_cfg *cfg, const et_tree *tree,
  * lse           nullable fp32 [B, Hq, N]: natural-log log-sum-exp of the
  *               scaled scores of each row.
  * ws            et_tree_attention_workspace_size(shape) bytes (may be 0/null
- *               when that size is 0).
+ *               when that size is 0: the fp32 path, one split, or the
+ *               tcgen05 path, whose splits form a thread-block cluster and
+ *               merge through distributed shared memory).
  * Accumulation is fp32; P is rounded to the input dtype before P.V.
+ * tcgen05 path: at most 8 splits (one cluster); a bounded wait that expires
+ * sets ET_DEV_TIMEOUT in dev_status and leaves that tile's output undefined.
  */
 et_status et_tree_attention(const et_attn_shape *shape,
                             const void *q, const void *k_prefix, const void *v_prefix,

@@ -23,6 +23,7 @@ ET_OK, ET_ERR_INVALID_ARG, ET_ERR_UNSUPPORTED, ET_ERR_WORKSPACE, ET_ERR_CUDA, ET
 ET_DEV_NONFINITE, ET_DEV_BAD_INDEX, ET_DEV_DISCONNECTED, ET_DEV_TIMEOUT = 1, 2, 4, 8
 ET_BF16, ET_F32 = 0, 1
 ET_ACCEPT_GREEDY, ET_ACCEPT_STOCH_POINT, ET_ACCEPT_STOCH_DRAFTQ = 0, 1, 2
+ATTN_AUTO, ATTN_MMA_SYNC, ATTN_TCGEN05 = 0, 1, 2
 
 EXPORTED = ("et_num_candidates", "et_layer_expanded", "et_layer_base", "et_tree_workspace_size",
             "et_tree_attention_workspace_size", "et_tree_attention_splits", "et_workspace_init",
@@ -43,7 +44,7 @@ class TreeC(ctypes.Structure):
 class AttnShapeC(ctypes.Structure):
     _fields_ = [("B", c_i32), ("N", c_i32), ("Hq", c_i32), ("Hkv", c_i32), ("d", c_i32), ("dtype", c_i32),
                 ("scale", c_f32), ("max_prefix", c_i32), ("kv_rows", c_i64), ("kv_head_stride", c_i64),
-                ("num_splits", c_i32)]
+                ("num_splits", c_i32), ("impl", c_i32)]
 
 
 class EtError(RuntimeError):
@@ -268,11 +269,12 @@ class AttnShape:
     kv_rows: int = 0
     kv_head_stride: int = 0
     num_splits: int = 0
+    impl: int = ATTN_AUTO
 
     def c(self) -> AttnShapeC:
         sc = self.scale if self.scale > 0 else self.d ** -0.5
         return AttnShapeC(self.B, self.N, self.Hq, self.Hkv, self.d, self.dtype, sc, self.max_prefix,
-                          self.kv_rows, self.kv_head_stride, self.num_splits)
+                          self.kv_rows, self.kv_head_stride, self.num_splits, self.impl)
 
 
 def et_tree_attention_workspace_size(shape: AttnShape) -> int:

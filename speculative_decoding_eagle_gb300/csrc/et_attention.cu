@@ -9,9 +9,11 @@
 //    query head) rows of one KV head, so GQA groups share every K/V tile;
 //    K/V stream through a cp.async double buffer with an XOR-swizzled
 //    layout; splits are merged by the last block to finish (no waits);
-//  * bf16, tcgen05 (et_attention_tc.cu) when it is built and selected.
+//  * bf16 with d = 128: the tcgen05 / TMA / TMEM kernel of et_attention_tc.cu
+//    (the default; the mma.sync kernel stays selectable and covers d = 64).
 #include <cuda_bf16.h>
 
+#include "et_attn_internal.h"
 #include "et_common.cuh"
 
 namespace et {
@@ -438,6 +440,7 @@ static int sm_count() {
   if (!cached[dev]) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cudaGetLastError();
     cached[dev] = n;
   }
   return cached[dev];
@@ -449,39 +452,83 @@ static bool attn_shape_ok(const et_attn_shape *s) {
   if (s->d != 64 && s->d != 128) return false;
   if (s->dtype != ET_BF16 && s->dtype != ET_F32) return false;
   if (s->max_prefix < 0 || s->kv_rows < 0 || s->kv_head_stride < 0 || s->num_splits < 0) return false;
+  if (s->impl < 0 || s->impl > 2) return false;
   if (!(s->scale > 0.f)) return false;
   return true;
 }
 
-static int row_tiles(const et_attn_shape *s) { return (s->N * (s->Hq / s->Hkv) + kRows - 1) / kRows; }
+// How one call is carried out: path, row-tile height, tiles and splits.
+struct AttnPlan {
+  int impl;   // 0 fp32 CUDA cores, 1 mma.sync, 2 tcgen05
+  int rows;   // rows per tile
+  int MT;     // row tiles per KV head
+  int S;      // KV splits
+  size_t ws;  // workspace bytes
+  size_t cnt_off, ml_off, po_off;
+};
+
+static bool make_plan(const et_attn_shape *s, AttnPlan *p) {
+  if (!attn_shape_ok(s)) return false;
+  const bool tc_ok = s->dtype == ET_BF16 && s->d == kTcDim;
+  if (s->dtype == ET_F32) {
+    if (s->impl != 0) return false;
+    p->impl = 0; p->rows = 1; p->MT = s->N; p->S = 1;
+  } else if (s->impl == 2 || (s->impl == 0 && tc_ok)) {
+    if (!tc_ok) return false;
+    p->impl = 2; p->rows = kTcRows;
+  } else {
+    p->impl = 1; p->rows = kRows;
+  }
+  const int G = s->Hq / s->Hkv;
+  const int T = (s->max_prefix + kKeys - 1) / kKeys + (s->N + kKeys - 1) / kKeys;
+  if (p->impl != 0) {
+    p->MT = (s->N * G + p->rows - 1) / p->rows;
+    const long long base = (long long)s->B * s->Hkv * p->MT;
+    const int cap = T / 2 > 0 ? T / 2 : 1;  // at least two K/V tiles per split
+    int S = s->num_splits;
+    if (p->impl == 2) {
+      // the splits of a row tile form one thread-block cluster (<= 8 blocks,
+      // one block per SM); pick the most splits whose clusters all fit in one wave
+      if (S <= 0) {
+        S = 1;
+        for (int c = kTcMaxSplits; c >= 2; --c) {
+          if (c > cap) continue;
+          const int fit = tc_max_clusters(c);
+          if (fit > 0 && base <= fit) { S = c; break; }
+        }
+      }
+      if (S > kTcMaxSplits) S = kTcMaxSplits;
+    } else if (S <= 0) {  // two resident blocks per SM
+      S = (int)((2LL * sm_count() + base - 1) / base);
+      if (S > cap) S = cap;
+    }
+    if (S > T) S = T;
+    if (S > 32) S = 32;
+    if (S < 1) S = 1;
+    p->S = S;
+  }
+  p->ws = 0;
+  p->cnt_off = p->ml_off = p->po_off = 0;
+  if (p->impl == 1 && p->S > 1) {  // the tcgen05 path merges its splits on chip
+    const size_t tiles = (size_t)s->B * s->Hkv * p->MT;
+    const size_t cnt = (tiles * sizeof(unsigned int) + 255) & ~(size_t)255;
+    const size_t ml = (tiles * p->S * p->rows * sizeof(float2) + 255) & ~(size_t)255;
+    p->cnt_off = 0;
+    p->ml_off = cnt;
+    p->po_off = cnt + ml;
+    p->ws = cnt + ml + tiles * p->S * p->rows * (size_t)s->d * sizeof(float);
+  }
+  return true;
+}
 
 extern "C" int32_t et_tree_attention_splits(const et_attn_shape *s) {
-  if (!attn_shape_ok(s)) return -1;
-  if (s->dtype == ET_F32) return 1;
-  const int T = (s->max_prefix + kKeys - 1) / kKeys + (s->N + kKeys - 1) / kKeys;
-  int S = s->num_splits;
-  if (S <= 0) {
-    const long long base = (long long)s->B * s->Hkv * row_tiles(s);
-    const long long target = 2LL * sm_count();  // two resident blocks per SM
-    S = (int)((target + base - 1) / base);
-    // keep >= 2 KV tiles per split so the double buffer has something to overlap
-    const int cap = T / 2 > 0 ? T / 2 : 1;
-    if (S > cap) S = cap;
-  }
-  if (S > T) S = T;
-  if (S > 64) S = 64;
-  if (S < 1) S = 1;
-  return S;
+  AttnPlan p;
+  return make_plan(s, &p) ? p.S : -1;
 }
 
 extern "C" size_t et_tree_attention_workspace_size(const et_attn_shape *s) {
-  const int S = et_tree_attention_splits(s);
-  if (S <= 1) return 0;
-  const size_t tiles = (size_t)s->B * s->Hkv * row_tiles(s);
-  const size_t cnt = (tiles * sizeof(unsigned int) + 255) & ~(size_t)255;
-  const size_t ml = (tiles * S * kRows * sizeof(float2) + 255) & ~(size_t)255;
-  const size_t po = tiles * S * kRows * (size_t)s->d * sizeof(float);
-  return cnt + ml + po;
+  AttnPlan p;
+  return make_plan(s, &p) ? p.ws : 0;
 }
 
 extern "C" et_status et_tree_attention(const et_attn_shape *shape, const void *q, const void *k_prefix,
@@ -492,6 +539,8 @@ extern "C" et_status et_tree_attention(const et_attn_shape *shape, const void *q
   ET_RETURN_IF(!shape, ET_ERR_INVALID_ARG);
   if (shape->d != 64 && shape->d != 128 && shape->d > 0) return ET_ERR_UNSUPPORTED;
   ET_RETURN_IF(!attn_shape_ok(shape), ET_ERR_INVALID_ARG);
+  AttnPlan plan;
+  if (!make_plan(shape, &plan)) return ET_ERR_UNSUPPORTED;
   ET_RETURN_IF(!q || !k_tree || !v_tree || !mask || !out || !prefix_len, ET_ERR_INVALID_ARG);
   ET_RETURN_IF(shape->max_prefix > 0 && (!k_prefix || !v_prefix || !kv_row0), ET_ERR_INVALID_ARG);
   const size_t al = shape->dtype == ET_BF16 ? 16 : 4;
@@ -499,12 +548,29 @@ extern "C" et_status et_tree_attention(const et_attn_shape *shape, const void *q
                    (k_prefix && !et_aligned(k_prefix, al)) || (v_prefix && !et_aligned(v_prefix, al)) ||
                    !et_aligned(mask, 8),
                ET_ERR_INVALID_ARG);
-  const size_t need = et_tree_attention_workspace_size(shape);
-  ET_RETURN_IF(need > 0 && (!ws || ws_bytes < need || !et_aligned(ws, 256)), ET_ERR_WORKSPACE);
+  ET_RETURN_IF(plan.ws > 0 && (!ws || ws_bytes < plan.ws || !et_aligned(ws, 256)), ET_ERR_WORKSPACE);
+  cudaStream_t st = (cudaStream_t)stream;
+  unsigned char *wsb = static_cast<unsigned char *>(ws);
+
+  if (plan.impl == 2) {
+    TcLaunch t{};
+    t.B = shape->B; t.N = shape->N; t.Hq = shape->Hq; t.Hkv = shape->Hkv; t.G = shape->Hq / shape->Hkv;
+    t.MT = plan.MT; t.S = plan.S; t.W = (shape->N + 63) / 64;
+    t.scale_log2 = shape->scale * 1.4426950408889634f;
+    t.q = q; t.kp = k_prefix; t.vp = v_prefix; t.kt = k_tree; t.vt = v_tree;
+    t.kv_row0 = reinterpret_cast<const long long *>(kv_row0);
+    t.prefix_len = prefix_len;
+    t.kv_rows = shape->kv_rows;
+    t.kv_head_stride = shape->kv_head_stride;
+    t.mask = reinterpret_cast<const unsigned long long *>(mask);
+    t.out = out; t.lse = lse; t.dev_status = dev_status;
+    ET_RETURN_IF((long long)t.Hkv * t.MT > 65535 || t.B > 65535, ET_ERR_UNSUPPORTED);
+    return tc_attention_launch(t, st);
+  }
 
   AttnArgs a{};
   a.B = shape->B; a.N = shape->N; a.Hq = shape->Hq; a.Hkv = shape->Hkv; a.G = shape->Hq / shape->Hkv;
-  a.d = shape->d; a.MT = row_tiles(shape); a.S = et_tree_attention_splits(shape);
+  a.d = shape->d; a.MT = plan.MT; a.S = plan.S;
   a.scale_log2 = shape->scale * 1.4426950408889634f;
   a.W = (shape->N + 63) / 64;
   a.q = q; a.kp = k_prefix; a.vp = v_prefix; a.kt = k_tree; a.vt = v_tree;
@@ -514,21 +580,16 @@ extern "C" et_status et_tree_attention(const et_attn_shape *shape, const void *q
   a.kv_head_stride = shape->kv_head_stride;
   a.mask = reinterpret_cast<const unsigned long long *>(mask);
   a.out = out; a.lse = lse; a.dev_status = dev_status;
-  cudaStream_t st = (cudaStream_t)stream;
-  if (shape->dtype == ET_F32) {
+  if (plan.impl == 0) {
     dim3 grid(shape->N, shape->Hq, shape->B);
     if (shape->d == 64) k_attn_f32<64><<<grid, 128, 0, st>>>(a);
     else k_attn_f32<128><<<grid, 128, 0, st>>>(a);
     return et_launch_status();
   }
   if (a.S > 1) {
-    const size_t tiles = (size_t)a.B * a.Hkv * a.MT;
-    unsigned char *base = static_cast<unsigned char *>(ws);
-    const size_t cnt = (tiles * sizeof(unsigned int) + 255) & ~(size_t)255;
-    const size_t ml = (tiles * a.S * kRows * sizeof(float2) + 255) & ~(size_t)255;
-    a.cnt = reinterpret_cast<unsigned int *>(base);
-    a.part_ml = reinterpret_cast<float2 *>(base + cnt);
-    a.part_o = reinterpret_cast<float *>(base + cnt + ml);
+    a.cnt = reinterpret_cast<unsigned int *>(wsb + plan.cnt_off);
+    a.part_ml = reinterpret_cast<float2 *>(wsb + plan.ml_off);
+    a.part_o = reinterpret_cast<float *>(wsb + plan.po_off);
   }
   ET_RETURN_IF((long long)a.Hkv * a.MT > 65535 || a.B > 65535, ET_ERR_UNSUPPORTED);
   dim3 grid(a.S, a.Hkv * a.MT, a.B);

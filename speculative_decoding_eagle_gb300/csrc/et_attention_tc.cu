@@ -1,0 +1,713 @@
+// Tree-masked attention on the 5th-generation tensor cores (tcgen05) of
+// sm_103a: every flattened draft row attends the KV prefix and its own
+// in-tree ancestors (EAGLE-2 article on sbmmt.com, attention-mask
+// paragraph; EAGLE blog section 1.1: one target pass verifies the draft).
+//
+// One block per (KV split, KV head x 128-row tile, sequence), one block per
+// SM, 8 warps:
+//   warp 0     TMA producer: 64-key K and V tiles (128-byte swizzle) into a
+//              4-stage ring guarded by mbarriers (expect-tx / commit);
+//   warp 1     owns 256 TMEM columns and issues tcgen05.mma:
+//              S_j = Q K_j^T  (M=128, N=64, K=128)  into TMEM S[j%2],
+//              O  += P_j V_j  (M=128, N=128, K=64)  into TMEM O;
+//   warps 2-11 stage the Q tile (K-major, 128-byte swizzle) at the start;
+//   warps 4-11 softmax, two warps per TMEM lane quarter: both read the whole
+//              64-column S row of their 32 query rows (mask by prefix length
+//              / ancestor bits, row max), each then exponentiates its own 32
+//              columns (log2 domain), writes them to P_j (bf16, shared
+//              memory) and rescales its half of O in TMEM, lazily (only when
+//              the row max grows by more than 2^8).
+// A 128-row tile packs (token, query head) rows of one KV head, so a GQA
+// group shares every K/V tile.  The KV splits of one tile run as one thread
+// block cluster and merge their partial results through distributed shared
+// memory.  Every mbarrier wait is bounded: on expiry the block reports
+// ET_DEV_TIMEOUT, stops, frees its TMEM and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <mutex>
+
+#include "et_attn_internal.h"
+#include "et_common.cuh"
+
+namespace et {
+namespace {
+
+constexpr int kThreads = 384;
+constexpr int kStages = 4;
+constexpr uint32_t kHalfBytes = kTcKeys * 128;       // 64 rows x 128 B (64 of the 128 dims)
+constexpr uint32_t kTileBytes = 2 * kHalfBytes;      // one K or V tile
+constexpr uint32_t kQHalfBytes = kTcRows * 128;
+constexpr uint32_t kQBytes = 2 * kQHalfBytes;
+constexpr uint32_t kPBytes = kTcRows * 128;          // 128 rows x 64 keys bf16
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + kQBytes;
+constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
+constexpr uint32_t kOffP = kOffV + kStages * kTileBytes;
+constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
+constexpr uint32_t kOffMisc = kOffBar + 256;
+constexpr uint32_t kSmemBytes = kOffMisc + 256 + 1024;  // + slack for 1024-byte alignment
+constexpr uint32_t kColS0 = 0, kColS1 = 64, kColO = 128, kTmemCols = 256;
+constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the row max grows by more than 2^8
+constexpr long long kWaitCycles = 1ll << 32;  // ~2 s at 2 GHz
+
+// barrier slots
+constexpr int B_FULL = 0, B_EMPTY = 4, B_SFULL = 8, B_PFULL = 10, B_OFULL = 12, B_QFULL = 13;
+constexpr int kQWarps = 10;     // warps 2-11 stage Q
+constexpr int kSoftmaxWarps = 8; // warps 4-11: two per TMEM lane quarter, one per 32-column half
+
+__device__ __forceinline__ uint32_t saddr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase with this parity; false if it expired or another
+// role already gave up.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+  if (mbar_try(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try(bar, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag: used only to let copies already
+// in flight land before the block leaves.
+__device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try(bar, parity) && clock64() - t0 < kWaitCycles) {
+  }
+}
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"((unsigned long long)map), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"((unsigned long long)map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// 32 lanes x 32 bits x 64 columns: lane l of the warp gets 64 consecutive
+// fp32 columns of TMEM lane (quarter base + l), starting at the address's column.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+               : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+               :
+               : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// distributed shared memory (thread block cluster)
+__device__ __forceinline__ uint32_t cluster_map(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ float2 ld_cluster_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format):
+// start >> 4 in bits 0-13, leading byte offset >> 4 in 16-29, stride byte
+// offset >> 4 in 32-45, version 1 in 46-47, swizzle mode 2 in 61-63.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t start, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((start >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A
+// and B (bits 7-9, 10-12 = 1), A K-major, B K-major or MN-major (bit 16),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+constexpr uint32_t kIdescQK = idesc_bf16(kTcRows, kTcKeys, false);
+constexpr uint32_t kIdescPV = idesc_bf16(kTcRows, kTcDim, true);
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ void split_range_tc(int L, int N, int S, int s, int &t0, int &t1, int &nP) {
+  nP = (L + kTcKeys - 1) / kTcKeys;
+  const int T = nP + (N + kTcKeys - 1) / kTcKeys;
+  const int per = (T + S - 1) / S;
+  t0 = s * per;
+  t1 = min(T, t0 + per);
+  if (t0 > T) t0 = T;
+}
+
+
+// All lanes wait; the warp proceeds only if every lane saw the phase complete.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_attn_tc(const __grid_constant__ CUtensorMap tm_kp, const __grid_constant__ CUtensorMap tm_vp,
+              const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt, const TcLaunch a) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ int row_tok[kTcRows], row_head[kTcRows];
+  __shared__ float lpart[2][kTcRows];  // the two column halves' row sums
+  unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const uint32_t sb = saddr(sm);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kOffMisc);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffMisc + 16);
+  auto bar = [&](int i) -> uint32_t { return sb + kOffBar + 8u * (uint32_t)i; };
+
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int s = blockIdx.x, g = blockIdx.y / a.MT, mt = blockIdx.y - g * a.MT, b = blockIdx.z;
+  const int N = a.N;
+  const int L = a.prefix_len[b];
+  const long long S_b = a.kv_head_stride > 0 ? a.kv_head_stride : L;
+  const long long row0 = a.kv_row0 ? a.kv_row0[b] : 0;
+  int t0, t1, nP;
+  split_range_tc(L, N, a.S, s, t0, t1, nP);
+  const int T = t1 - t0;
+
+  if (t == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(bar(B_FULL + i), 1);
+      mbar_init(bar(B_EMPTY + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_SFULL + i), 1);
+      mbar_init(bar(B_PFULL + i), kSoftmaxWarps);
+    }
+    mbar_init(bar(B_OFULL), 1);
+    mbar_init(bar(B_QFULL), kQWarps);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (t < kTcRows) {
+    const int R = mt * kTcRows + t;
+    const int i = R / a.G;
+    row_tok[t] = i < N ? i : -1;
+    row_head[t] = g * a.G + (R - i * a.G);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (t == 0 && L > 0 && row0 + (long long)g * S_b + L > a.kv_rows) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
+
+  if (warp == 0) {
+    // ---------------- TMA producer (starts before Q is staged) ----------------
+    if (lane == 0 && T > 0) {
+      int issued = 0;  // tiles whose copies were started
+      for (int j = 0; j < T; ++j) {
+        const int stage = j % kStages;
+        if (j >= kStages && !mbar_wait(bar(B_EMPTY + stage), (uint32_t)((j / kStages) - 1) & 1u, abort_flag)) break;
+        const uint32_t fb = bar(B_FULL + stage);
+        mbar_expect_tx(fb, 2 * kTileBytes);
+        const uint32_t kd = sb + kOffK + stage * kTileBytes, vd = sb + kOffV + stage * kTileBytes;
+        const int tile = t0 + j;
+        if (tile < nP) {
+          const int row = (int)(row0 + (long long)g * S_b + (long long)tile * kTcKeys);
+          tma_2d(kd, &tm_kp, 0, row, fb);
+          tma_2d(kd + kHalfBytes, &tm_kp, 64, row, fb);
+          tma_2d(vd, &tm_vp, 0, row, fb);
+          tma_2d(vd + kHalfBytes, &tm_vp, 64, row, fb);
+        } else {
+          const int tr = b * N + (tile - nP) * kTcKeys;
+          tma_3d(kd, &tm_kt, 0, g, tr, fb);
+          tma_3d(kd + kHalfBytes, &tm_kt, 64, g, tr, fb);
+          tma_3d(vd, &tm_vt, 0, g, tr, fb);
+          tma_3d(vd + kHalfBytes, &tm_vt, 64, g, tr, fb);
+        }
+        issued = j + 1;
+      }
+      // do not leave while copies are in flight: the stages of all but the last
+      // kStages issued tiles were consumed already; wait (bounded) for those
+      const int first = issued > kStages ? issued - kStages : 0;
+      for (int j = first; j < issued; ++j) mbar_drain(bar(B_FULL + j % kStages), (uint32_t)(j / kStages) & 1u);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0 && T > 0) {
+      auto issue_s = [&](int j) {
+        const int stage = j % kStages;
+        const uint32_t d = tmem + ((j & 1) ? kColS1 : kColS0);
+        const uint32_t kbase = sb + kOffK + stage * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTcDim / 16; ++kk) {
+          const uint64_t ad = sw128_desc(sb + kOffQ + (kk >> 2) * kQHalfBytes + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sw128_desc(kbase + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+          tc_mma(d, ad, bd, kIdescQK, kk > 0);
+        }
+        tc_commit(bar(B_SFULL + (j & 1)));
+      };
+      bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag) && mbar_wait(bar(B_FULL + 0), 0, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+      }
+      for (int j = 0; ok && j < T; ++j) {
+        if (j + 1 < T) {
+          const int st1 = (j + 1) % kStages;
+          if (!mbar_wait(bar(B_FULL + st1), (uint32_t)((j + 1) / kStages) & 1u, abort_flag)) break;
+          tc_fence_after();
+          issue_s(j + 1);
+        }
+        if (!mbar_wait(bar(B_PFULL + (j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag)) break;
+        tc_fence_after();
+        const int stage = j % kStages;
+        const uint32_t pbase = sb + kOffP + (uint32_t)(j & 1) * kPBytes;
+        const uint32_t vbase = sb + kOffV + stage * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+          const uint64_t ad = sw128_desc(pbase + kk * 32, 16, 1024);
+          const uint64_t bd = sw128_desc(vbase + kk * 2048, kHalfBytes, 1024);
+          tc_mma(tmem + kColO, ad, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(bar(B_OFULL));
+        if (j + kStages < T) tc_commit(bar(B_EMPTY + stage));
+      }
+    }
+  }
+  if (warp >= 2) {
+    // ---------------- Q tile -> shared memory (warps 2-11) ----------------
+    const __nv_bfloat16 *Q = static_cast<const __nv_bfloat16 *>(a.q);
+    for (int x = t - 64; x < kTcRows * 16; x += kThreads - 64) {
+      const int r = x >> 4, c = x & 15;
+      const int i = row_tok[r];
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (i >= 0)
+        v = *reinterpret_cast<const uint4 *>(Q + (((long long)b * N + i) * a.Hq + row_head[r]) * kTcDim + c * 8);
+      const uint32_t dst = sb + kOffQ + (uint32_t)(c >> 3) * kQHalfBytes + (uint32_t)r * 128u +
+                           (uint32_t)(((c & 7) ^ (r & 7)) << 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                   : "memory");
+    }
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(B_QFULL));
+  }
+
+  // softmax geometry: warp w >= 4 reads TMEM lane quarter (w % 4) = tile rows
+  // 32*(w%4) .. +31 and owns the 32-column half hh of every S tile
+  const bool smx = warp >= 4;
+  const int quarter = warp & 3, hh = (warp - 4) >> 2;
+  const int r = 32 * quarter + lane;
+  float m_used = -INFINITY, l = 0.f;  // l: this half's share of the row sum
+  const int my_tok = smx ? row_tok[r] : -1;
+  bool ok_rows = true;
+  if (smx) {
+    const bool active = __any_sync(0xffffffffu, my_tok >= 0);  // warp-uniform: any real row here
+    unsigned long long mw0 = 0ull, mw1 = 0ull;
+    if (my_tok >= 0) {
+      mw0 = a.mask[((long long)b * N + my_tok) * a.W];
+      if (a.W > 1) mw1 = a.mask[((long long)b * N + my_tok) * a.W + 1];
+    }
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
+    const float scale = a.scale_log2;
+    uint32_t raw[64];
+    for (int j = 0; j < T; ++j) {
+      const int tile = t0 + j;
+      if (!warp_wait(bar(B_SFULL + (j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag)) { ok_rows = false; break; }
+      tc_fence_after();
+      if (active) {
+        tmem_ld64(lane_base + ((j & 1) ? kColS1 : kColS0), raw);
+        tmem_wait_ld();
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (tile < nP && L - tile * kTcKeys >= kTcKeys) {  // a full prefix tile: nothing to mask
+#pragma unroll
+          for (int c = 0; c < 64; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(raw[c]));
+        } else {
+          const int lim = tile < nP ? L - tile * kTcKeys : 0;
+          const unsigned long long w = tile < nP ? 0ull : ((tile - nP) == 0 ? mw0 : mw1);
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const bool keep = tile < nP ? (c < lim) : (((w >> c) & 1ull) != 0ull);
+            const float v = keep ? __uint_as_float(raw[c]) : -INFINITY;
+            raw[c] = __float_as_uint(v);
+            mx[c & 3] = fmaxf(mx[c & 3], v);
+          }
+        }
+        const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale;  // scale > 0
+        const float m_new = fmaxf(m_used, tmax);
+        const bool grow = m_new > m_used + kRescaleLog2;  // also true for the first finite max
+        // O in TMEM holds sum_{<j} P V relative to m_used: rescale this warp's
+        // 64 columns of it when the max grew by more than 2^8 (warp-collective)
+        if (__any_sync(0xffffffffu, grow && j > 0 && m_used > -INFINITY)) {
+          if (!warp_wait(bar(B_OFULL), (uint32_t)(j - 1) & 1u, abort_flag)) { ok_rows = false; break; }
+          tc_fence_after();
+          const float sc = (grow && m_used > -INFINITY) ? ex2(m_used - m_new) : 1.f;
+          uint32_t ov[32];
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+            const uint32_t oa = lane_base + kColO + 64 * hh + 32 * part;
+            tmem_ld32(oa, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * sc);
+            tmem_st32(oa, ov);
+          }
+          tmem_wait_st();
+          l *= sc;
+        }
+        if (grow) m_used = m_new;
+        const float nm = m_used == -INFINITY ? 0.f : -m_used;
+        float sm4[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t prow = sb + kOffP + (uint32_t)(j & 1) * kPBytes + (uint32_t)r * 128u;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {  // this half's 4 chunks of P (bf16, 128-byte swizzle)
+          uint32_t q4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int col = 32 * hh + 8 * c + 2 * e;
+            const float p0 = ex2(fmaf(__uint_as_float(raw[col]), scale, nm));
+            const float p1 = ex2(fmaf(__uint_as_float(raw[col + 1]), scale, nm));
+            sm4[c] += p0 + p1;
+            q4[e] = pack_bf16x2(p0, p1);
+          }
+          const uint32_t dst = prow + (uint32_t)(((4 * hh + c) ^ (r & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(q4[0]), "r"(q4[1]), "r"(q4[2]),
+                       "r"(q4[3])
+                       : "memory");
+        }
+        l += (sm4[0] + sm4[1]) + (sm4[2] + sm4[3]);
+      }
+      // the last, partial prefix tile: clear the V rows past the prefix so that
+      // whatever the cache holds there cannot reach P.V (0 * NaN); the eight
+      // softmax warps share the chunks
+      if (tile == nP - 1 && (L & (kTcKeys - 1))) {
+        const int stage = j % kStages;
+        if (!warp_wait(bar(B_FULL + stage), (uint32_t)(j / kStages) & 1u, abort_flag)) ok_rows = false;
+        const int first = L & (kTcKeys - 1);
+        unsigned char *vs = sm + kOffV + stage * kTileBytes;
+        for (int x = t - 128; x < (kTcKeys - first) * 16; x += 32 * kSoftmaxWarps) {
+          const int row = first + (x >> 4), c = x & 15;
+          *reinterpret_cast<uint4 *>(vs + (c >> 3) * kHalfBytes + row * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_PFULL + (j & 1)));
+      if (!__all_sync(0xffffffffu, ok_rows)) { ok_rows = false; break; }
+    }
+    // the last P.V must have landed before O is read
+    if (ok_rows && T > 0 && !warp_wait(bar(B_OFULL), (uint32_t)(T - 1) & 1u, abort_flag)) ok_rows = false;
+  }
+  if (smx) lpart[hh][r] = l;
+  __syncthreads();
+  tc_fence_after();
+  const bool aborted = *abort_flag != 0;
+  if (smx && !aborted) {
+    // ---------------- this block's rows: output, or the cluster merge buffer ----------------
+    const float lt = lpart[0][r] + lpart[1][r];
+    const bool active = __any_sync(0xffffffffu, my_tok >= 0);
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
+    const float inv = lt > 0.f ? 1.f / lt : 0.f;
+    if (active && T > 0) {
+      uint32_t ov[64];
+      tmem_ld64(lane_base + kColO + 64 * hh, ov);
+      tmem_wait_ld();
+      if (a.S == 1) {
+        if (my_tok >= 0) {
+          __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) +
+                                (((long long)b * N + my_tok) * a.Hq + row_head[r]) * kTcDim + 64 * hh;
+#pragma unroll
+          for (int c = 0; c < 64; c += 8) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv);
+            *reinterpret_cast<uint4 *>(orow + c) = v;
+          }
+        }
+      } else {  // unnormalised fp32 half row, 16-byte chunks swizzled by the row
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int chunk = 16 * hh + c;
+          const uint32_t dst = sb + kOffK + (uint32_t)r * 512u + (uint32_t)((chunk ^ (r & 31)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(ov[4 * c]), "r"(ov[4 * c + 1]),
+                       "r"(ov[4 * c + 2]), "r"(ov[4 * c + 3])
+                       : "memory");
+        }
+      }
+    } else if (a.S > 1) {  // no real row here, or no keys at all: contribute nothing
+      for (int c = 0; c < 16; ++c) {
+        const int chunk = 16 * hh + c;
+        const uint32_t dst = sb + kOffK + (uint32_t)r * 512u + (uint32_t)((chunk ^ (r & 31)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0u) : "memory");
+      }
+    }
+    if (hh == 0) {
+      if (a.S == 1) {
+        if (my_tok >= 0 && a.lse)
+          a.lse[((long long)b * a.Hq + row_head[r]) * N + my_tok] =
+              lt > 0.f ? (m_used + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
+      } else {
+        *reinterpret_cast<float2 *>(sm + kOffP + 8 * r) =
+            make_float2(T > 0 ? m_used : -INFINITY, T > 0 ? lt : 0.f);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+  if (aborted && t == 0) flag_status(a.dev_status, ET_DEV_TIMEOUT);
+  if (a.S == 1) return;
+
+  // ---------------- merge the S splits of this tile across the cluster ----------------
+  cluster_sync_all();  // every split's partial rows are in its shared memory
+  {
+    const int S = a.S;
+    const int per = (kTcRows + S - 1) / S;
+    const int r0 = s * per, r1 = min(kTcRows, r0 + per);
+    float *wts = reinterpret_cast<float *>(sm + kOffP + 2048);  // [per][kTcMaxSplits] weights / total
+    if (t < r1 - r0 && !aborted) {
+      const int rr = r0 + t;
+      float2 ml[kTcMaxSplits];
+#pragma unroll
+      for (int x = 0; x < kTcMaxSplits; ++x)  // all loads first: distributed shared memory latency overlaps
+        ml[x] = x < S ? ld_cluster_f2(cluster_map(sb + kOffP + 8 * rr, (uint32_t)x)) : make_float2(-INFINITY, 0.f);
+      float M = -INFINITY;
+#pragma unroll
+      for (int x = 0; x < kTcMaxSplits; ++x) M = fmaxf(M, ml[x].x);
+      float Ls = 0.f, w[kTcMaxSplits];
+#pragma unroll
+      for (int x = 0; x < kTcMaxSplits; ++x) {
+        w[x] = ml[x].x > -INFINITY ? exp2f(ml[x].x - M) : 0.f;
+        Ls += ml[x].y * w[x];
+      }
+      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+#pragma unroll
+      for (int x = 0; x < kTcMaxSplits; ++x) wts[t * kTcMaxSplits + x] = w[x] * inv;
+      const int i = row_tok[rr];
+      if (i >= 0 && a.lse)
+        a.lse[((long long)b * a.Hq + row_head[rr]) * N + i] =
+            Ls > 0.f ? (M + log2f(Ls)) * 0.69314718055994531f : -INFINITY;
+    }
+    __syncthreads();
+    __nv_bfloat16 *O = static_cast<__nv_bfloat16 *>(a.out);
+    for (int x = t; x < (r1 - r0) * 32 && !aborted; x += kThreads) {
+      const int lr = x >> 5, chunk = x & 31, rr = r0 + lr;
+      const int i = row_tok[rr];
+      if (i < 0) continue;
+      const uint32_t off = sb + kOffK + (uint32_t)rr * 512u + (uint32_t)((chunk ^ (rr & 31)) << 4);
+      float4 p[kTcMaxSplits];
+#pragma unroll
+      for (int sp = 0; sp < kTcMaxSplits; ++sp)
+        p[sp] = sp < S ? ld_cluster_f4(cluster_map(off, (uint32_t)sp)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int sp = 0; sp < kTcMaxSplits; ++sp) {
+        const float wv = sp < S ? wts[lr * kTcMaxSplits + sp] : 0.f;
+        acc.x = fmaf(wv, p[sp].x, acc.x);
+        acc.y = fmaf(wv, p[sp].y, acc.y);
+        acc.z = fmaf(wv, p[sp].z, acc.z);
+        acc.w = fmaf(wv, p[sp].w, acc.w);
+      }
+      uint2 v;
+      v.x = pack_bf16x2(acc.x, acc.y);
+      v.y = pack_bf16x2(acc.z, acc.w);
+      *reinterpret_cast<uint2 *>(O + (((long long)b * N + i) * a.Hq + row_head[rr]) * kTcDim + 4 * chunk) = v;
+    }
+  }
+  cluster_sync_all();  // peers may still read this block's shared memory until here
+}
+
+// ---------------------------------------------------------------------------
+// host: tensor maps and launch
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+bool make_map_2d(CUtensorMap *m, const void *base, long long rows) {
+  const cuuint64_t dims[2] = {(cuuint64_t)kTcDim, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kTcDim * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)kTcKeys};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// tree K/V [B*N rows][Hkv][d]: box = 64 rows of one head
+bool make_map_tree(CUtensorMap *m, const void *base, int Hkv, long long rows) {
+  const cuuint64_t dims[3] = {(cuuint64_t)kTcDim, (cuuint64_t)Hkv, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)kTcDim * 2, (cuuint64_t)Hkv * kTcDim * 2};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)kTcKeys};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t set_smem_attr() {
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  });
+  return err;
+}
+
+}  // namespace
+
+int tc_max_clusters(int cluster_size) {
+  static std::mutex mu;
+  static int cache[64][kTcMaxSplits + 1];
+  static bool filled[64][kTcMaxSplits + 1];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || cluster_size < 1 || cluster_size > kTcMaxSplits) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!filled[dev][cluster_size]) {
+    int n = 0;
+    if (set_smem_attr() == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(cluster_size, 1, 1);
+      cfg.blockDim = dim3(kThreads, 1, 1);
+      cfg.dynamicSmemBytes = kSmemBytes;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = cluster_size;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, k_attn_tc, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();
+    cache[dev][cluster_size] = n;
+    filled[dev][cluster_size] = true;
+  }
+  return cache[dev][cluster_size];
+}
+
+et_status tc_attention_launch(const TcLaunch &a, cudaStream_t stream) {
+  if (!encode_fn()) return ET_ERR_CUDA;
+  if (a.S < 1 || a.S > kTcMaxSplits) return ET_ERR_UNSUPPORTED;
+  if (a.kv_rows >= (1ll << 31) || (long long)a.B * a.N >= (1ll << 31)) return ET_ERR_UNSUPPORTED;
+  CUtensorMap m_kp, m_vp, m_kt, m_vt;
+  const long long tree_rows = (long long)a.B * a.N;
+  bool ok = make_map_tree(&m_kt, a.kt, a.Hkv, tree_rows) && make_map_tree(&m_vt, a.vt, a.Hkv, tree_rows);
+  if (a.kp && a.vp && a.kv_rows > 0) {
+    ok = ok && make_map_2d(&m_kp, a.kp, a.kv_rows) && make_map_2d(&m_vp, a.vp, a.kv_rows);
+  } else {  // no prefix anywhere: a valid map the kernel never uses
+    ok = ok && make_map_2d(&m_kp, a.kt, tree_rows * a.Hkv) && make_map_2d(&m_vp, a.vt, tree_rows * a.Hkv);
+  }
+  if (!ok) return ET_ERR_INVALID_ARG;
+  if (set_smem_attr() != cudaSuccess) return ET_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.S, a.Hkv * a.MT, a.B);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.S > 1 ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, k_attn_tc, m_kp, m_vp, m_kt, m_vt, a) != cudaSuccess) {
+    cudaGetLastError();
+    return ET_ERR_CUDA;
+  }
+  return et_launch_status();
+}
+
+}  // namespace et

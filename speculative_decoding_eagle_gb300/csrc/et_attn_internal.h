@@ -1,0 +1,36 @@
+// Internal interface between the attention entry point (et_attention.cu) and
+// the tcgen05 kernel (et_attention_tc.cu).  Not part of the C ABI.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "eagle_tree.h"
+
+#define ET_HIDDEN __attribute__((visibility("hidden")))
+
+namespace et {
+
+struct TcLaunch {
+  int B, N, Hq, Hkv, G, MT, S, W;  // MT row tiles of 128 per KV head, S splits (= cluster size)
+  float scale_log2;
+  const void *q, *kp, *vp, *kt, *vt;
+  const long long *kv_row0;
+  const int *prefix_len;
+  long long kv_rows, kv_head_stride;
+  const unsigned long long *mask;
+  void *out;
+  float *lse;
+  int *dev_status;
+};
+
+constexpr int kTcRows = 128;   // query rows per tile (TMEM lanes)
+constexpr int kTcKeys = 64;    // keys per K/V tile
+constexpr int kTcDim = 128;    // head dim of the tcgen05 path
+constexpr int kTcMaxSplits = 8;  // KV splits of one row tile = one thread-block cluster (portable size)
+
+ET_HIDDEN et_status tc_attention_launch(const TcLaunch &a, cudaStream_t stream);
+// How many clusters of `cluster_size` attention blocks fit on the device at once.
+ET_HIDDEN int tc_max_clusters(int cluster_size);
+
+}  // namespace et

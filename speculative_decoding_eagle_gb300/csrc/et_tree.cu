@@ -419,6 +419,258 @@ __global__ void __launch_bounds__(kMaxN) k_mask_posids(int N, const int32_t *fla
   if (bad) flag_status(dev_status, ET_DEV_BAD_INDEX);
 }
 
+// shared by the clustered expansion: exact top-k via a distance histogram
+constexpr int kHistBins = 64;      // 1/8-nat bins of "distance below the max"
+constexpr float kHistPerNat = 8.f;
+constexpr int kCandCap = 1024;     // candidates ranked by counting
+
+struct ExpandRowArgs {
+  const float *logits;
+  long long row_stride;
+  const int32_t *row_of_node;
+  int vec4;
+  int B, V, k, m, C, layer, m_l, base_next, m_next;
+  et_tree tree;
+  int32_t *dev_status;
+  unsigned int *seq_cnt;  // [B]
+};
+
+// ---------------------------------------------------------------------------
+// expand, one thread-block cluster per expanded row (V <= 32768): CTA q of the
+// cluster owns logits [4096 q, 4096 q + 4096) (4 float4 per thread), computes
+// its local max / sum of exp and its exact local top-k; the leader (rank 0)
+// gathers the partial results through distributed shared memory, merges
+// them by rank counting and writes the children; the last leader of a
+// sequence then picks the next frontier.  Spreading a row over up to 8 SMs
+// gives the load 8x the memory parallelism of one block per row.
+// ---------------------------------------------------------------------------
+constexpr int kClThreads = 256;
+constexpr int kClVec = 4;
+constexpr int kClSpan = kClThreads * 4 * kClVec;   // 4096 logits per CTA
+constexpr int kClMaxCtas = 8;
+constexpr int kClMaxV = kClSpan * kClMaxCtas;      // 32768
+
+struct TopkSmem {
+  float redz[32];
+  int redi[32];
+  unsigned int hist[kHistBins];
+  float cz[kCandCap];
+  int ci[kCandCap];
+  float topz[kMaxTopk];
+  int topi[kMaxTopk];
+  int ncand, sbin;
+};
+
+// Exact top-k by (z desc, id asc) of the NV values each thread holds; id_of(e)
+// is the token id of value e (INT_MAX for padding).  A histogram of each
+// value's distance below the block max (1/8-nat bins) bounds the candidates
+// to the first bins holding >= k values, which are then ranked by counting;
+// otherwise (heavy ties, all -inf) k rounds of block argmax.  Result in
+// ts.topz / ts.topi[0..k), padded with (-inf, INT_MAX).
+template <int NT, int NV, typename IdFn>
+__device__ void block_topk(float (&v)[NV], IdFn id_of, float M, int k, TopkSmem &ts) {
+  const int t = threadIdx.x, lane = t & 31;
+  if (t < kHistBins) ts.hist[t] = 0u;
+  if (t == 0) { ts.ncand = 0; ts.sbin = -1; }
+  __syncthreads();
+  if (M > -INFINITY) {
+#pragma unroll
+    for (int e = 0; e < NV; ++e) {
+      const float d = M - v[e];
+      if (d < (float)kHistBins / kHistPerNat) atomicAdd(&ts.hist[(int)(d * kHistPerNat)], 1u);
+    }
+  }
+  __syncthreads();
+  if (t < 32) {
+    const unsigned int c0 = ts.hist[2 * lane], c1 = ts.hist[2 * lane + 1];
+    unsigned int incl = c0 + c1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const unsigned int excl = incl - c0 - c1;
+    if (excl < (unsigned)k && incl >= (unsigned)k) ts.sbin = (excl + c0 >= (unsigned)k) ? 2 * lane : 2 * lane + 1;
+  }
+  __syncthreads();
+  bool fast = ts.sbin >= 0;
+  if (fast) {
+    const float dlim = (float)(ts.sbin + 1) / kHistPerNat;  // exact: bins count floor(d * 8) <= sbin
+#pragma unroll
+    for (int e = 0; e < NV; ++e) {
+      if (M - v[e] < dlim) {
+        const int pos = atomicAdd(&ts.ncand, 1);
+        if (pos < kCandCap) { ts.cz[pos] = v[e]; ts.ci[pos] = id_of(e); }
+      }
+    }
+    __syncthreads();
+    fast = ts.ncand <= kCandCap;
+  }
+  if (fast) {
+    const int nc = ts.ncand;
+    for (int i = t; i < nc; i += NT) {
+      const float z = ts.cz[i];
+      const int id = ts.ci[i];
+      int rank = 0;
+      for (int j = 0; j < nc; ++j) rank += ranks_before(ts.cz[j], ts.ci[j], z, id) ? 1 : 0;
+      if (rank < k) { ts.topz[rank] = z; ts.topi[rank] = id; }
+    }
+  } else {
+    unsigned int consumed = 0u;
+    float bz = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int e = 0; e < NV; ++e)
+      if (ranks_before(v[e], id_of(e), bz, bi)) { bz = v[e]; bi = id_of(e); }
+    for (int r = 0; r < k; ++r) {
+      float z = bz;
+      int id = bi;
+      block_best<NT>(z, id, ts.redz, ts.redi);
+      if (t == 0) { ts.topz[r] = z; ts.topi[r] = id; }
+      if (id == bi && id != 0x7fffffff) {
+#pragma unroll
+        for (int e = 0; e < NV; ++e)
+          if (id_of(e) == id) consumed |= 1u << e;
+        bz = -INFINITY;
+        bi = 0x7fffffff;
+#pragma unroll
+        for (int e = 0; e < NV; ++e)
+          if (!((consumed >> e) & 1u) && ranks_before(v[e], id_of(e), bz, bi)) { bz = v[e]; bi = id_of(e); }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kClThreads) k_expand_cl(ExpandRowArgs a) {
+  __shared__ TopkSmem ts;
+  __shared__ float part_ms[2];
+  __shared__ float pm[kClMaxCtas], ps[kClMaxCtas];
+  __shared__ float gz[kClMaxCtas * kMaxTopk];
+  __shared__ int gi[kClMaxCtas * kMaxTopk];
+  __shared__ float topz[kMaxTopk];
+  __shared__ int topi[kMaxTopk];
+  __shared__ unsigned long long fkey[1024];
+  __shared__ int sel[kMaxM];
+  __shared__ int sflag;
+
+  const int t = threadIdx.x;
+  const int R = gridDim.x;                 // CTAs per row = cluster size
+  const int q = (int)cl_rank();
+  const int row = blockIdx.y;
+  const int b = row / a.m_l, s = row - b * a.m_l;
+  const int k = a.k;
+  int flag = 0, bad = 0;
+  int node = -1;
+  if (a.layer > 0) {
+    node = a.tree.frontier[b * a.m + s];
+    if (node < 0 || node >= a.C) bad = 1;
+  }
+  const float *zrow = nullptr;
+  if (!bad) {
+    long long r = a.row_of_node ? (long long)a.row_of_node[(long long)b * (a.C + 1) + node + 1] : (long long)row;
+    if (r < 0) bad = 1;
+    else zrow = a.logits + r * a.row_stride;
+  }
+  const int base = q * kClSpan;
+  auto id_of = [&](int e) -> int {
+    const int id = base + (e >> 2) * (kClThreads * 4) + t * 4 + (e & 3);
+    return id < a.V ? id : 0x7fffffff;
+  };
+  float v[4 * kClVec];
+#pragma unroll
+  for (int u = 0; u < kClVec; ++u) {
+    const int e0 = base + u * kClThreads * 4 + t * 4;
+    if (zrow && a.vec4 && e0 + 3 < a.V) {
+      const float4 f = __ldcs(reinterpret_cast<const float4 *>(zrow + e0));
+      v[4 * u] = f.x; v[4 * u + 1] = f.y; v[4 * u + 2] = f.z; v[4 * u + 3] = f.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[4 * u + j] = (zrow && e0 + j < a.V) ? __ldcs(zrow + e0 + j) : -INFINITY;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (e0 + j < a.V) v[4 * u + j] = sanitize_logit(v[4 * u + j], flag);
+  }
+  float lm = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < 4 * kClVec; ++e) lm = fmaxf(lm, v[e]);
+  const float Mq = block_max<kClThreads>(lm, ts.redz);
+  float ls = 0.f;
+  if (Mq > -INFINITY) {
+#pragma unroll
+    for (int e = 0; e < 4 * kClVec; ++e) ls += exp_fast(v[e] - Mq);
+  }
+  const float Sq = block_sum<kClThreads>(ls, ts.redz);
+  block_topk<kClThreads, 4 * kClVec>(v, id_of, Mq, k, ts);
+  if (t == 0) { part_ms[0] = Mq; part_ms[1] = Sq; }
+  if (flag) flag_status(a.dev_status, ET_DEV_NONFINITE);
+  if (bad && q == 0 && t == 0) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
+  cl_sync();  // every CTA's partial result is in its shared memory
+  if (q == 0) {
+    if (t < R) {
+      pm[t] = cl_ld_f32(cl_map(&part_ms[0], t));
+      ps[t] = cl_ld_f32(cl_map(&part_ms[1], t));
+    }
+    for (int i = t; i < R * k; i += kClThreads) {
+      const int peer = i / k, e = i - peer * k;
+      gz[i] = cl_ld_f32(cl_map(&ts.topz[e], peer));
+      gi[i] = cl_ld_s32(cl_map(&ts.topi[e], peer));
+    }
+  }
+  cl_sync();  // the leader has everything; the others may leave
+  if (q != 0) return;
+  float M = -INFINITY;
+  for (int x = 0; x < R; ++x) M = fmaxf(M, pm[x]);
+  float S = 0.f;
+  for (int x = 0; x < R; ++x) S += pm[x] > -INFINITY ? ps[x] * expf(pm[x] - M) : 0.f;
+  for (int i = t; i < R * k; i += kClThreads) {
+    const float z = gz[i];
+    const int id = gi[i];
+    int rank = 0;
+    for (int j = 0; j < R * k; ++j) rank += ranks_before(gz[j], gi[j], z, id) ? 1 : 0;
+    if (rank < k) { topz[rank] = z; topi[rank] = id; }
+  }
+  __syncthreads();
+  if (t < k) {
+    const float logS = (M > -INFINITY) ? logf(S) : 0.f;
+    const float z = topz[t];
+    const float lp = (M > -INFINITY && z > -INFINITY) ? (z - M) - logS : -INFINITY;
+    const long long pkey = node < 0 ? 0ll : a.tree.cand_key[(long long)b * a.C + node];
+    const long long o = (long long)b * a.C + a.base_next + s * k + t;
+    const int tok = topi[t];
+    a.tree.cand_tok[o] = (tok == 0x7fffffff) ? -1 : tok;
+    a.tree.cand_parent[o] = node;
+    a.tree.cand_lp[o] = lp;
+    a.tree.cand_key[o] = add_keys(pkey, fixed_key(lp));
+  }
+  // ---- the last row of this sequence picks the next frontier (rank counting) ----
+  if (!arrive_last(&a.seq_cnt[b], (unsigned)a.m_l, &sflag)) return;
+  if (a.m_next <= 0) return;
+  const int width = a.m_l * k;  // <= 1024
+  for (int i = t; i < width; i += kClThreads) {
+    const int id = a.base_next + i;
+    fkey[i] = rank_key(ld_cg(a.tree.cand_key + (long long)b * a.C + id), id);
+  }
+  __syncthreads();
+  for (int i = t; i < width; i += kClThreads) {
+    const unsigned long long my = fkey[i];
+    int rank = 0;
+    for (int j = 0; j < width; ++j) rank += fkey[j] < my ? 1 : 0;
+    if (rank < a.m_next) sel[rank] = a.base_next + i;
+  }
+  __syncthreads();
+  if (t < a.m) {
+    if (t < a.m_next) {
+      int slot = 0;
+      for (int j = 0; j < a.m_next; ++j) slot += sel[j] < sel[t] ? 1 : 0;
+      a.tree.frontier[b * a.m + slot] = sel[t];
+    } else {
+      a.tree.frontier[b * a.m + t] = -1;
+    }
+  }
+}
+
 }  // namespace et
 
 using namespace et;
@@ -484,6 +736,34 @@ extern "C" int32_t et_layer_base(const et_tree_cfg *cfg, int32_t layer) {
   return g.base[layer];
 }
 
+// one block per expanded row; same arguments as the chunked kernel
+static et_status launch_expand_row(const ExpandArgs &c, cudaStream_t stream) {
+  ExpandRowArgs a;
+  a.logits = c.logits; a.row_stride = c.row_stride; a.row_of_node = c.row_of_node; a.vec4 = c.vec4;
+  a.B = c.B; a.V = c.V; a.k = c.k; a.m = c.m; a.C = c.C; a.layer = c.layer; a.m_l = c.m_l;
+  a.base_next = c.base_next; a.m_next = c.m_next;
+  a.tree = c.tree; a.dev_status = c.dev_status; a.seq_cnt = c.seq_cnt;
+  // one cluster of ceil(V / 4096) CTAs per expanded row
+  const int R = (c.V + kClSpan - 1) / kClSpan;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(R, c.B * c.m_l, 1);
+  cfg.blockDim = dim3(kClThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = R;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, k_expand_cl, a) != cudaSuccess) {
+    cudaGetLastError();
+    return ET_ERR_CUDA;
+  }
+  return et_launch_status();
+}
+
 static bool tree_ptrs_ok(const et_tree *t) {
   return t && t->cand_tok && t->cand_parent && t->cand_lp && t->cand_key && t->frontier;
 }
@@ -515,6 +795,7 @@ extern "C" et_status et_tree_expand(const et_tree_cfg *cfg, int32_t layer, const
   a.row_cnt = reinterpret_cast<unsigned int *>(base);
   a.seq_cnt = a.row_cnt + w.rows;
   a.part = reinterpret_cast<float *>(base + w.part_off);
+  if (cfg->V <= kClMaxV) return launch_expand_row(a, (cudaStream_t)stream);
   dim3 grid(a.nchunk, cfg->B * m_l);
   const size_t smem = (size_t)a.nchunk * a.k * (sizeof(float) + sizeof(int));
   k_expand<<<grid, kExpThreads, smem, (cudaStream_t)stream>>>(a);
@@ -641,6 +922,7 @@ extern "C" et_status et_tree_expand_noalloc(const et_tree_cfg *cfg, int32_t laye
   a.row_cnt = reinterpret_cast<unsigned int *>(base);
   a.seq_cnt = a.row_cnt + rows;
   a.part = reinterpret_cast<float *>(base + cnt_bytes);
+  if (cfg->V <= kClMaxV) return launch_expand_row(a, st);
   dim3 grid(a.nchunk, rows);
   const size_t smem = (size_t)a.nchunk * a.k * (sizeof(float) + sizeof(int));
   k_expand<<<grid, kExpThreads, smem, st>>>(a);

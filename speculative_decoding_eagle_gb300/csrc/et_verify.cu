@@ -53,10 +53,10 @@ __device__ __forceinline__ const float *table_row(const float *tab, long long st
 // Inverse CDF over a row: smallest v with sum_{u<=v} w(u) > uni * sum_u w(u),
 // accumulated in fp64 over contiguous per-thread segments.  `w(v)` must be
 // non-negative; falls back to the last v with w(v) > 0.
-template <typename WF>
+template <int NT, typename WF>
 __device__ int block_inverse_cdf(int V, float uni, WF w, double *redd, int *redi) {
   const int t = threadIdx.x;
-  const int seg = (V + kVThreads - 1) / kVThreads;
+  const int seg = (V + NT - 1) / NT;
   const int lo = t * seg, hi = min(V, lo + seg);
   double loc = 0.0;
   int lastpos = -1;
@@ -77,16 +77,16 @@ __device__ int block_inverse_cdf(int V, float uni, WF w, double *redd, int *redi
   if (lane == 31) redd[wp] = incl;
   __syncthreads();
   if (wp == 0) {
-    double s = lane < kVThreads / 32 ? redd[lane] : 0.0;
+    double s = lane < NT / 32 ? redd[lane] : 0.0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       double y = __shfl_up_sync(0xffffffffu, s, o);
       if (lane >= o) s += y;
     }
-    if (lane < kVThreads / 32) redd[lane] = s;
+    if (lane < NT / 32) redd[lane] = s;
   }
   __syncthreads();
-  const double total = redd[kVThreads / 32 - 1];
+  const double total = redd[NT / 32 - 1];
   const double excl = (wp > 0 ? redd[wp - 1] : 0.0) + incl - loc;
   const double thr = (double)uni * total;
   __syncthreads();
@@ -108,17 +108,267 @@ __device__ int block_inverse_cdf(int V, float uni, WF w, double *redd, int *redi
   return r;
 }
 
-__global__ void __launch_bounds__(kVThreads) k_verify(VerifyArgs a) {
-  __shared__ float redz[32];
-  __shared__ int redi[32];
-  __shared__ double redd[32];
-  __shared__ int sflag;
-  __shared__ int par[kMaxN], tokf[kMaxN], nodef[kMaxN];
-  __shared__ int rej[kMaxTopk];
-  __shared__ float zsh[kMaxTopk];
-  __shared__ int s_next, s_nrej, s_cur;
+struct WalkSmem {
+  float redz[32];
+  int redi[32];
+  double redd[32];
+  int par[kMaxN], tokf[kMaxN], nodef[kMaxN];
+  float rs0[kMaxN], rs1[kMaxN];  // per flat row: argmax id (bits) / max, -, / sum
+  float zc[kMaxN];               // target logit of each row's token in its parent's row
+  int opath[kMaxDepth + 2], otok[kMaxDepth + 2];
+  int rej[kMaxTopk];
+  float zsh[kMaxTopk];
+  int s_next, s_nrej, s_cur, s_alen;
+};
 
-  const int t = threadIdx.x, lane = t & 31;
+// Phase 2 of acceptance, run by the last row-block of sequence b: walk the
+// kept tree from the root (children in ascending flat row), then draw or take
+// the bonus token at the row where the walk stops.
+template <int NT>
+__device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
+  const int t = threadIdx.x;
+  int flag = 0;
+  float *redz = w.redz;
+  int *redi = w.redi;
+  double *redd = w.redd;
+  int *par = w.par, *tokf = w.tokf, *nodef = w.nodef, *rej = w.rej;
+  float *zsh = w.zsh;
+  int &s_next = w.s_next, &s_nrej = w.s_nrej, &s_cur = w.s_cur;
+  const int N = a.N;
+  const long long fo = (long long)b * N;
+  for (int j = t; j < N; j += NT) {
+    par[j] = a.flat_parent[fo + j];
+    tokf[j] = a.flat_tok[fo + j];
+    nodef[j] = a.flat_node[fo + j];
+  }
+  if (t == 0) s_cur = 0;
+  if (a.mode != ET_ACCEPT_STOCH_DRAFTQ) {
+    // ---- greedy / point-mass: everything the walk needs, fetched in parallel ----
+    int badp = 0;
+    for (int j = t; j < N; j += NT) {
+      w.rs0[j] = ld_cg(a.rowstat + 2 * (fo + j));
+      w.rs1[j] = ld_cg(a.rowstat + 2 * (fo + j) + 1);
+      if (a.mode == ET_ACCEPT_STOCH_POINT && j > 0) {
+        const int p = a.flat_parent[fo + j];
+        const int x = a.flat_tok[fo + j];
+        const float *zp = (p >= 0 && p < N) ? table_row(a.tlog, a.tstride, a.tmap, a.C, b, a.flat_node[fo + p], fo + p, badp)
+                                            : nullptr;
+        int f2 = 0;
+        w.zc[j] = (zp && x >= 0 && x < a.V) ? sanitize_logit(zp[x], f2) : -INFINITY;
+      }
+    }
+    __syncthreads();
+    if (t == 0) {
+      int cur = 0, alen = 0, nrej = 0;
+      w.opath[0] = 0;
+      for (int iter = 0; iter <= a.D; ++iter) {
+        int nxt = -1;
+        nrej = 0;
+        if (a.mode == ET_ACCEPT_GREEDY) {
+          const int am = __float_as_int(w.rs0[cur]);
+          for (int j = cur + 1; j < N; ++j)
+            if (par[j] == cur && tokf[j] == am) { nxt = j; break; }
+          if (nxt < 0) w.otok[alen] = am;
+        } else {
+          const float M = w.rs0[cur], S = w.rs1[cur];
+          float R = 0.f;
+          for (int j = cur + 1; j < N; ++j) {
+            if (par[j] != cur) continue;
+            const float px = S > 0.f ? expf(w.zc[j] / a.T - M) / S : 0.f;
+            const float ratio = (R < 1.f) ? px / (1.f - R) : INFINITY;
+            if (a.uniforms[fo + j] < ratio) { nxt = j; break; }
+            R += px;
+            if (nrej < kMaxTopk) rej[nrej++] = tokf[j];
+          }
+        }
+        if (nxt < 0 || alen >= a.D) break;
+        w.otok[alen] = tokf[nxt];
+        ++alen;
+        w.opath[alen] = nxt;
+        cur = nxt;
+      }
+      s_cur = cur;
+      s_nrej = nrej;
+      w.s_alen = alen;
+    }
+    __syncthreads();
+    const int alen = w.s_alen;
+    if (a.mode == ET_ACCEPT_STOCH_POINT) {  // bonus token: inverse CDF of the residual at the stop row
+      const int cur = s_cur, nrej = s_nrej;
+      int badz = 0;
+      const float *zr = table_row(a.tlog, a.tstride, a.tmap, a.C, b, nodef[cur], fo + cur, badz);
+      const float M = w.rs0[cur];
+      const int bonus = block_inverse_cdf<NT>(a.V, a.uniforms[fo], [&](int vv) -> float {
+        if (!zr) return 0.f;
+        for (int q = 0; q < nrej; ++q)
+          if (rej[q] == vv) return 0.f;
+        int f2 = 0;
+        const float y = sanitize_logit(zr[vv], f2) / a.T;
+        return y > -INFINITY ? expf(y - M) : 0.f;
+      }, redd, redi);
+      if (t == 0) w.otok[alen] = bonus;
+      badp |= badz;
+    }
+    __syncthreads();
+    const long long po = (long long)b * (a.D + 1);
+    for (int j = t; j <= a.D; j += NT) {
+      a.path[po + j] = j <= alen ? w.opath[j] : -1;
+      a.tokens[po + j] = j <= alen ? w.otok[j] : -1;
+    }
+    if (t == 0) a.accept_len[b] = alen;
+    if (badp) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
+    return;
+  }
+  __syncthreads();
+  int alen = 0;
+  int bonus = -1;
+  int badw = 0;
+  for (int iter = 0; iter <= a.D + 1; ++iter) {
+    const int cur = s_cur;
+    if (t == 0) a.path[(long long)b * (a.D + 1) + alen] = cur;
+    if (t == 0) { s_next = -1; s_nrej = 0; }
+    __syncthreads();
+    const float *zr = table_row(a.tlog, a.tstride, a.tmap, a.C, b, nodef[cur], fo + cur, badw);
+    if (a.mode == ET_ACCEPT_GREEDY) {
+      const int am = __float_as_int(ld_cg(a.rowstat + 2 * (fo + cur)));
+      if (t == 0) {  // children are the rows after cur whose parent is cur; first match wins
+        int best = -1;
+        for (int j = cur + 1; j < N; ++j)
+          if (par[j] == cur && tokf[j] == am) { best = j; break; }
+        s_next = best;
+      }
+      __syncthreads();
+      bonus = am;
+    } else if (a.mode == ET_ACCEPT_STOCH_POINT) {
+      const float M = ld_cg(a.rowstat + 2 * (fo + cur)), S = ld_cg(a.rowstat + 2 * (fo + cur) + 1);
+      if (t == 0 && zr) {
+        float R = 0.f;
+        int nrej = 0;
+        for (int j = cur + 1; j < N; ++j) {
+          if (par[j] != cur) continue;
+          const int x = tokf[j];
+          if (x < 0 || x >= a.V) { badw = 1; continue; }
+          const float px = expf(sanitize_logit(zr[x], flag) / a.T - M) / S;
+          const float ratio = (R < 1.f) ? px / (1.f - R) : INFINITY;
+          const float u = a.uniforms[fo + j];
+          if (u < ratio) { s_next = j; break; }
+          R += px;
+          if (nrej < kMaxTopk) rej[nrej++] = x;
+        }
+        s_nrej = nrej;
+      }
+      __syncthreads();
+      if (s_next < 0) {
+        const int nrej = s_nrej;
+        bonus = block_inverse_cdf<NT>(a.V, a.uniforms[fo], [&](int vv) -> float {
+          if (!zr) return 0.f;
+          for (int q = 0; q < nrej; ++q)
+            if (rej[q] == vv) return 0.f;
+          int f2 = 0;
+          const float y = sanitize_logit(zr[vv], f2) / a.T;
+          return y > -INFINITY ? expf(y - M) : 0.f;
+        }, redd, redi);
+      }
+    } else {  // ET_ACCEPT_STOCH_DRAFTQ
+      const float M = ld_cg(a.rowstat + 2 * (fo + cur)), S = ld_cg(a.rowstat + 2 * (fo + cur) + 1);
+      bool has_child = false;
+      for (int j = cur + 1; j < N; ++j)
+        if (par[j] == cur) { has_child = true; break; }
+      float Mq = 0.f, Sq = 1.f;
+      const float *qr = nullptr;
+      if (has_child) {
+        qr = table_row(a.dlog, a.dstride, a.dmap, a.C, b, nodef[cur], fo + cur, badw);
+        float lm = -INFINITY;
+        for (int vv = t; vv < a.V; vv += NT) {
+          int f2 = 0;
+          lm = fmaxf(lm, qr ? sanitize_logit(qr[vv], f2) / a.T : -INFINITY);
+        }
+        Mq = block_max<NT>(lm, redz);
+        float ls = 0.f;
+        for (int vv = t; vv < a.V; vv += NT) {
+          int f2 = 0;
+          const float y = qr ? sanitize_logit(qr[vv], f2) / a.T : -INFINITY;
+          ls += y > -INFINITY ? expf(y - Mq) : 0.f;
+        }
+        Sq = block_sum<NT>(ls, redz);
+      }
+      // r_j(v): p(v) with j residual updates applied (zsh[i] = 1/Z_{i+1}, 0 = kept)
+      int nz = 0;
+      auto pval = [&](int vv) -> float {
+        int f2 = 0;
+        const float y = zr ? sanitize_logit(zr[vv], f2) / a.T : -INFINITY;
+        return y > -INFINITY ? expf(y - M) / S : 0.f;
+      };
+      auto qval = [&](int vv) -> float {
+        int f2 = 0;
+        const float y = qr ? sanitize_logit(qr[vv], f2) / a.T : -INFINITY;
+        return y > -INFINITY ? expf(y - Mq) / Sq : 0.f;
+      };
+      auto rval = [&](int vv, int upto) -> float {
+        float r = pval(vv);
+        if (upto > 0) {
+          const float q = qval(vv);
+          for (int s2 = 0; s2 < upto; ++s2)
+            if (zsh[s2] > 0.f) r = fmaxf(r - q, 0.f) * zsh[s2];
+        }
+        return r;
+      };
+      for (int j = cur + 1; j < N; ++j) {
+        if (par[j] != cur) continue;
+        const int x = tokf[j];
+        if (x < 0 || x >= a.V) { badw = 1; continue; }
+        const float qx = qval(x);
+        const float rx = rval(x, nz);
+        const float ratio = qx <= 0.f ? 1.f : fminf(1.f, rx / qx);
+        if (a.uniforms[fo + j] < ratio) { if (t == 0) s_next = j; break; }
+        // residual update: Z = sum_v max(r(v) - q(v), 0)
+        double loc = 0.0;
+        for (int vv = t; vv < a.V; vv += NT) loc += (double)fmaxf(rval(vv, nz) - qval(vv), 0.f);
+        const double Z = block_sum_d<NT>(loc, redd);
+        __syncthreads();
+        if (t == 0 && nz < kMaxTopk) zsh[nz] = Z > 0.0 ? (float)(1.0 / Z) : 0.f;
+        __syncthreads();
+        if (nz < kMaxTopk) ++nz;
+      }
+      __syncthreads();
+      if (s_next < 0) {
+        const int nzf = nz;
+        bonus = block_inverse_cdf<NT>(a.V, a.uniforms[fo], [&](int vv) -> float { return rval(vv, nzf); }, redd, redi);
+      }
+    }
+    __syncthreads();
+    const int nxt = s_next;
+    if (nxt < 0 || alen >= a.D) {
+      if (nxt >= 0) bonus = -1;  // cannot happen: the tree is at most D deep
+      if (t == 0) a.tokens[(long long)b * (a.D + 1) + alen] = bonus;
+      break;
+    }
+    if (t == 0) {
+      a.tokens[(long long)b * (a.D + 1) + alen] = tokf[nxt];
+      s_cur = nxt;
+    }
+    ++alen;
+    __syncthreads();
+  }
+  if (t == 0) {
+    a.accept_len[b] = alen;
+    for (int j = alen + 1; j <= a.D; ++j) {
+      a.path[(long long)b * (a.D + 1) + j] = -1;
+      a.tokens[(long long)b * (a.D + 1) + j] = -1;
+    }
+  }
+  if (badw && t == 0) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
+  (void)flag;
+}
+
+
+__global__ void __launch_bounds__(kVThreads) k_verify(VerifyArgs a) {
+  __shared__ WalkSmem w;
+  __shared__ int sflag;
+  float *redz = w.redz;
+  int *redi = w.redi;
+
+  const int t = threadIdx.x;
   const int row = blockIdx.y, c = blockIdx.x;
   const int b = row / a.N;
   int flag = 0, bad = 0;
@@ -194,155 +444,104 @@ __global__ void __launch_bounds__(kVThreads) k_verify(VerifyArgs a) {
   }
   if (!arrive_last(&a.seq_cnt[b], (unsigned)a.N, &sflag)) return;
 
-  // ---------------- phase 2: the walk of sequence b ----------------
-  const int N = a.N;
-  const long long fo = (long long)b * N;
-  for (int j = t; j < N; j += kVThreads) {
-    par[j] = a.flat_parent[fo + j];
-    tokf[j] = a.flat_tok[fo + j];
-    nodef[j] = a.flat_node[fo + j];
+  verify_walk<kVThreads>(a, b, w);
+}
+
+// ---------------------------------------------------------------------------
+// phase 1 on a thread-block cluster per flat row (V <= 32768): CTA q reduces
+// logits [4096 q, 4096 q + 4096); the leader merges through distributed
+// shared memory and writes the row's statistic.
+// ---------------------------------------------------------------------------
+constexpr int kVClThreads = 256;
+constexpr int kVClVec = 4;
+constexpr int kVClSpan = kVClThreads * 4 * kVClVec;
+constexpr int kVClMaxCtas = 8;
+constexpr int kVClMaxV = kVClSpan * kVClMaxCtas;
+
+__global__ void __launch_bounds__(kVClThreads) k_verify_cl(VerifyArgs a) {
+  __shared__ WalkSmem w;
+  __shared__ float part[2];
+  __shared__ float gp0[kVClMaxCtas], gp1[kVClMaxCtas];
+  __shared__ int sflag;
+  const int t = threadIdx.x;
+  const int R = gridDim.x;
+  const int q = (int)cl_rank();
+  const int row = blockIdx.y;
+  const int b = row / a.N;
+  int flag = 0, bad = 0;
+  const int node = a.flat_node[row];
+  const float *zrow = table_row(a.tlog, a.tstride, a.tmap, a.C, b, node, row, bad);
+  const int base = q * kVClSpan;
+  float v[4 * kVClVec];
+#pragma unroll
+  for (int u = 0; u < kVClVec; ++u) {
+    const int e0 = base + u * kVClThreads * 4 + t * 4;
+    if (zrow && a.vec4t && e0 + 3 < a.V) {
+      const float4 f = __ldg(reinterpret_cast<const float4 *>(zrow + e0));
+      v[4 * u] = f.x; v[4 * u + 1] = f.y; v[4 * u + 2] = f.z; v[4 * u + 3] = f.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[4 * u + j] = (zrow && e0 + j < a.V) ? __ldg(zrow + e0 + j) : -INFINITY;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (e0 + j < a.V) v[4 * u + j] = sanitize_logit(v[4 * u + j], flag);
   }
-  if (t == 0) s_cur = 0;
+  if (a.mode == ET_ACCEPT_GREEDY) {
+    float bz = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int e = 0; e < 4 * kVClVec; ++e) {
+      const int id = base + (e >> 2) * (kVClThreads * 4) + t * 4 + (e & 3);
+      if (id < a.V && ranks_before(v[e], id, bz, bi)) { bz = v[e]; bi = id; }
+    }
+    block_best<kVClThreads>(bz, bi, w.redz, w.redi);
+    if (t == 0) { part[0] = bz; part[1] = __int_as_float(bi); }
+  } else {
+    float lm = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 4 * kVClVec; ++e) {
+      v[e] = v[e] / a.T;
+      lm = fmaxf(lm, v[e]);
+    }
+    const float Mq = block_max<kVClThreads>(lm, w.redz);
+    float ls = 0.f;
+    if (Mq > -INFINITY) {
+#pragma unroll
+      for (int e = 0; e < 4 * kVClVec; ++e) ls += exp_fast(v[e] - Mq);
+    }
+    const float Sq = block_sum<kVClThreads>(ls, w.redz);
+    if (t == 0) { part[0] = Mq; part[1] = Sq; }
+  }
+  if (flag) flag_status(a.dev_status, ET_DEV_NONFINITE);
+  if (bad && q == 0 && t == 0) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
+  cl_sync();
+  if (q == 0 && t < R) {
+    gp0[t] = cl_ld_f32(cl_map(&part[0], t));
+    gp1[t] = cl_ld_f32(cl_map(&part[1], t));
+  }
+  cl_sync();
+  if (q != 0) return;
   __syncthreads();
-  int alen = 0;
-  int bonus = -1;
-  int badw = 0;
-  for (int iter = 0; iter <= a.D + 1; ++iter) {
-    const int cur = s_cur;
-    if (t == 0) a.path[(long long)b * (a.D + 1) + alen] = cur;
-    if (t == 0) { s_next = -1; s_nrej = 0; }
-    __syncthreads();
-    const float *zr = table_row(a.tlog, a.tstride, a.tmap, a.C, b, nodef[cur], fo + cur, badw);
-    if (a.mode == ET_ACCEPT_GREEDY) {
-      const int am = __float_as_int(ld_cg(a.rowstat + 2 * (fo + cur)));
-      if (t == 0) {  // children are the rows after cur whose parent is cur; first match wins
-        int best = -1;
-        for (int j = cur + 1; j < N; ++j)
-          if (par[j] == cur && tokf[j] == am) { best = j; break; }
-        s_next = best;
-      }
-      __syncthreads();
-      bonus = am;
-    } else if (a.mode == ET_ACCEPT_STOCH_POINT) {
-      const float M = ld_cg(a.rowstat + 2 * (fo + cur)), S = ld_cg(a.rowstat + 2 * (fo + cur) + 1);
-      if (t == 0 && zr) {
-        float R = 0.f;
-        int nrej = 0;
-        for (int j = cur + 1; j < N; ++j) {
-          if (par[j] != cur) continue;
-          const int x = tokf[j];
-          if (x < 0 || x >= a.V) { badw = 1; continue; }
-          const float px = expf(sanitize_logit(zr[x], flag) / a.T - M) / S;
-          const float ratio = (R < 1.f) ? px / (1.f - R) : INFINITY;
-          const float u = a.uniforms[fo + j];
-          if (u < ratio) { s_next = j; break; }
-          R += px;
-          if (nrej < kMaxTopk) rej[nrej++] = x;
-        }
-        s_nrej = nrej;
-      }
-      __syncthreads();
-      if (s_next < 0) {
-        const int nrej = s_nrej;
-        bonus = block_inverse_cdf(a.V, a.uniforms[fo], [&](int vv) -> float {
-          if (!zr) return 0.f;
-          for (int q = 0; q < nrej; ++q)
-            if (rej[q] == vv) return 0.f;
-          int f2 = 0;
-          const float y = sanitize_logit(zr[vv], f2) / a.T;
-          return y > -INFINITY ? expf(y - M) : 0.f;
-        }, redd, redi);
-      }
-    } else {  // ET_ACCEPT_STOCH_DRAFTQ
-      const float M = ld_cg(a.rowstat + 2 * (fo + cur)), S = ld_cg(a.rowstat + 2 * (fo + cur) + 1);
-      bool has_child = false;
-      for (int j = cur + 1; j < N; ++j)
-        if (par[j] == cur) { has_child = true; break; }
-      float Mq = 0.f, Sq = 1.f;
-      const float *qr = nullptr;
-      if (has_child) {
-        qr = table_row(a.dlog, a.dstride, a.dmap, a.C, b, nodef[cur], fo + cur, badw);
-        float lm = -INFINITY;
-        for (int vv = t; vv < a.V; vv += kVThreads) {
-          int f2 = 0;
-          lm = fmaxf(lm, qr ? sanitize_logit(qr[vv], f2) / a.T : -INFINITY);
-        }
-        Mq = block_max<kVThreads>(lm, redz);
-        float ls = 0.f;
-        for (int vv = t; vv < a.V; vv += kVThreads) {
-          int f2 = 0;
-          const float y = qr ? sanitize_logit(qr[vv], f2) / a.T : -INFINITY;
-          ls += y > -INFINITY ? expf(y - Mq) : 0.f;
-        }
-        Sq = block_sum<kVThreads>(ls, redz);
-      }
-      // r_j(v): p(v) with j residual updates applied (zsh[i] = 1/Z_{i+1}, 0 = kept)
-      int nz = 0;
-      auto pval = [&](int vv) -> float {
-        int f2 = 0;
-        const float y = zr ? sanitize_logit(zr[vv], f2) / a.T : -INFINITY;
-        return y > -INFINITY ? expf(y - M) / S : 0.f;
-      };
-      auto qval = [&](int vv) -> float {
-        int f2 = 0;
-        const float y = qr ? sanitize_logit(qr[vv], f2) / a.T : -INFINITY;
-        return y > -INFINITY ? expf(y - Mq) / Sq : 0.f;
-      };
-      auto rval = [&](int vv, int upto) -> float {
-        float r = pval(vv);
-        if (upto > 0) {
-          const float q = qval(vv);
-          for (int s2 = 0; s2 < upto; ++s2)
-            if (zsh[s2] > 0.f) r = fmaxf(r - q, 0.f) * zsh[s2];
-        }
-        return r;
-      };
-      for (int j = cur + 1; j < N; ++j) {
-        if (par[j] != cur) continue;
-        const int x = tokf[j];
-        if (x < 0 || x >= a.V) { badw = 1; continue; }
-        const float qx = qval(x);
-        const float rx = rval(x, nz);
-        const float ratio = qx <= 0.f ? 1.f : fminf(1.f, rx / qx);
-        if (a.uniforms[fo + j] < ratio) { if (t == 0) s_next = j; break; }
-        // residual update: Z = sum_v max(r(v) - q(v), 0)
-        double loc = 0.0;
-        for (int vv = t; vv < a.V; vv += kVThreads) loc += (double)fmaxf(rval(vv, nz) - qval(vv), 0.f);
-        const double Z = block_sum_d<kVThreads>(loc, redd);
-        __syncthreads();
-        if (t == 0 && nz < kMaxTopk) zsh[nz] = Z > 0.0 ? (float)(1.0 / Z) : 0.f;
-        __syncthreads();
-        if (nz < kMaxTopk) ++nz;
-      }
-      __syncthreads();
-      if (s_next < 0) {
-        const int nzf = nz;
-        bonus = block_inverse_cdf(a.V, a.uniforms[fo], [&](int vv) -> float { return rval(vv, nzf); }, redd, redi);
-      }
-    }
-    __syncthreads();
-    const int nxt = s_next;
-    if (nxt < 0 || alen >= a.D) {
-      if (nxt >= 0) bonus = -1;  // cannot happen: the tree is at most D deep
-      if (t == 0) a.tokens[(long long)b * (a.D + 1) + alen] = bonus;
-      break;
-    }
-    if (t == 0) {
-      a.tokens[(long long)b * (a.D + 1) + alen] = tokf[nxt];
-      s_cur = nxt;
-    }
-    ++alen;
-    __syncthreads();
-  }
   if (t == 0) {
-    a.accept_len[b] = alen;
-    for (int j = alen + 1; j <= a.D; ++j) {
-      a.path[(long long)b * (a.D + 1) + j] = -1;
-      a.tokens[(long long)b * (a.D + 1) + j] = -1;
+    if (a.mode == ET_ACCEPT_GREEDY) {
+      float bz = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int x = 0; x < R; ++x)
+        if (ranks_before(gp0[x], __float_as_int(gp1[x]), bz, bi)) { bz = gp0[x]; bi = __float_as_int(gp1[x]); }
+      a.rowstat[2 * row] = __int_as_float(bi);
+      a.rowstat[2 * row + 1] = bz;
+    } else {
+      float M = -INFINITY;
+      for (int x = 0; x < R; ++x) M = fmaxf(M, gp0[x]);
+      float S = 0.f;
+      for (int x = 0; x < R; ++x) S += gp0[x] > -INFINITY ? gp1[x] * expf(gp0[x] - M) : 0.f;
+      a.rowstat[2 * row] = M;
+      a.rowstat[2 * row + 1] = S;
     }
   }
-  if (badw && t == 0) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
-  (void)lane;
+  if (!arrive_last(&a.seq_cnt[b], (unsigned)a.N, &sflag)) return;
+  verify_walk<kVClThreads>(a, b, w);
 }
 
 }  // namespace et
@@ -386,7 +585,26 @@ extern "C" et_status et_verify_accept(const et_tree_cfg *cfg, et_accept_mode mod
   a.part = reinterpret_cast<float *>(base + part_off);
   a.rowstat = reinterpret_cast<float *>(base + rowstat_off);
   a.vec4t = et_aligned(target_logits, 16) && target_stride % 4 == 0;
-  dim3 grid(a.nchunk, cfg->B * N);
-  k_verify<<<grid, kVThreads, 0, (cudaStream_t)stream>>>(a);
+  if (cfg->V <= kVClMaxV) {  // one cluster of ceil(V / 4096) CTAs per flat row
+    const int R = (cfg->V + kVClSpan - 1) / kVClSpan;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(R, cfg->B * N, 1);
+    lc.blockDim = dim3(kVClThreads, 1, 1);
+    lc.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = R;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&lc, k_verify_cl, a) != cudaSuccess) {
+      cudaGetLastError();
+      return ET_ERR_CUDA;
+    }
+  } else {
+    dim3 grid(a.nchunk, cfg->B * N);
+    k_verify<<<grid, kVThreads, 0, (cudaStream_t)stream>>>(a);
+  }
   return et_launch_status();
 }

@@ -90,7 +90,7 @@ class VerifyStep:
     """Buffers and call chain of one verification step for a fixed shape."""
 
     def __init__(self, wl: W.Workload, B: Optional[int] = None, mode: Optional[int] = None, device="cuda",
-                 num_splits: int = 0, max_prefix: Optional[int] = None):
+                 num_splits: int = 0, max_prefix: Optional[int] = None, attn_impl: int = E.ATTN_AUTO):
         self.wl = wl
         self.cfg = tree_cfg(wl, B)
         self.B = self.cfg.B
@@ -115,6 +115,7 @@ class VerifyStep:
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=device)
         self.max_prefix = max_prefix
         self.num_splits = num_splits
+        self.attn_impl = attn_impl
         self.attn_ws = None
         self.shape = None
 
@@ -122,7 +123,8 @@ class VerifyStep:
         mp = self.max_prefix if self.max_prefix is not None else int(inp.host["prefix_len"].max())
         return E.AttnShape(B=self.B, N=self.cfg.N, Hq=self.wl.Hq, Hkv=self.wl.Hkv, d=self.wl.d,
                            dtype=E.ET_BF16 if self.wl.dtype == "bf16" else E.ET_F32, scale=self.wl.d ** -0.5,
-                           max_prefix=mp, kv_rows=inp.k_prefix.shape[0], num_splits=self.num_splits)
+                           max_prefix=mp, kv_rows=inp.k_prefix.shape[0], num_splits=self.num_splits,
+                           impl=self.attn_impl)
 
     def prepare(self, inp: StepInputs) -> None:
         shape = self.attn_shape(inp)

@@ -85,7 +85,7 @@ def test_expand_argument_checks(lib):
 def test_attention_argument_checks(lib):
     def shape(**kw):
         s = dict(B=1, N=61, Hq=32, Hkv=32, d=128, dtype=E.ET_BF16, scale=0.088, max_prefix=1024,
-                 kv_rows=32 * 1024, kv_head_stride=0, num_splits=0)
+                 kv_rows=32 * 1024, kv_head_stride=0, num_splits=0, impl=0)
         s.update(kw)
         return E.AttnShapeC(*s.values())
 
@@ -93,19 +93,28 @@ def test_attention_argument_checks(lib):
         return lib.et_tree_attention(ctypes.byref(sh), q, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None,
                                      ws, wsb, None)
     assert call(shape(d=96)) == E.ET_ERR_UNSUPPORTED
+    assert call(shape(d=64, impl=2)) == E.ET_ERR_UNSUPPORTED     # tcgen05 path needs d = 128
+    assert call(shape(dtype=E.ET_F32, impl=2)) == E.ET_ERR_UNSUPPORTED
+    assert call(shape(impl=3)) == E.ET_ERR_INVALID_ARG
     assert call(shape(N=129)) == E.ET_ERR_INVALID_ARG
     assert call(shape(N=0)) == E.ET_ERR_INVALID_ARG
     assert call(shape(Hq=30, Hkv=4)) == E.ET_ERR_INVALID_ARG
     assert call(shape(scale=0.0)) == E.ET_ERR_INVALID_ARG
     assert call(shape(), q=FAKE + 8) == E.ET_ERR_INVALID_ARG   # bf16 tiles need 16-byte alignment
     assert call(shape(), q=None) == E.ET_ERR_INVALID_ARG
-    assert call(shape(), ws=None) == E.ET_ERR_WORKSPACE
-    sz = lib.et_tree_attention_workspace_size(ctypes.byref(shape(num_splits=4)))
+    assert call(shape(impl=1), ws=None) == E.ET_ERR_WORKSPACE    # the mma.sync path merges splits in ws
+    sz = lib.et_tree_attention_workspace_size(ctypes.byref(shape(num_splits=4, impl=1)))
     assert sz > 0
-    assert call(shape(num_splits=4), wsb=sz - 1) == E.ET_ERR_WORKSPACE
+    assert call(shape(num_splits=4, impl=1), wsb=sz - 1) == E.ET_ERR_WORKSPACE
     assert lib.et_tree_attention_splits(ctypes.byref(shape(num_splits=4))) == 4
+    # the tcgen05 path merges its splits on chip: no workspace, at most 8 splits
+    assert lib.et_tree_attention_workspace_size(ctypes.byref(shape(num_splits=4, impl=2))) == 0
+    assert lib.et_tree_attention_splits(ctypes.byref(shape(num_splits=20, impl=2))) == 8
     assert lib.et_tree_attention_workspace_size(ctypes.byref(shape(num_splits=1))) == 0
     assert lib.et_tree_attention_splits(ctypes.byref(shape(dtype=E.ET_F32))) == 1
+    # workspace: tiles x splits x rows-per-tile x d floats (+ counters and (max, sum) pairs)
+    mma = lib.et_tree_attention_workspace_size(ctypes.byref(shape(num_splits=4, impl=1)))
+    assert mma >= 32 * 4 * 64 * 128 * 4
 
 
 def test_verify_argument_checks(lib):

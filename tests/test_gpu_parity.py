@@ -156,7 +156,7 @@ def test_rerank_mask_posids_match_oracle(B, D, k, m, n, ties):
 # ---------------------------------------------------------------------------
 # attention
 # ---------------------------------------------------------------------------
-def _attn_case(B, N, Hq, Hkv, d, prefixes, dtype, seed, splits=0, head_stride=0):
+def _attn_case(B, N, Hq, Hkv, d, prefixes, dtype, seed, splits=0, head_stride=0, impl=E.ATTN_AUTO, nan_tail=False):
     rng = np.random.default_rng(seed)
     wl = W.Workload("t", 99, V=16, Hq=Hq, Hkv=Hkv, d=d, prefix=0, dtype=dtype, depth=3, topk=2, m=2, n=N - 1,
                     sigma=0.5, accept=("greedy",), B=B)
@@ -177,6 +177,13 @@ def _attn_case(B, N, Hq, Hkv, d, prefixes, dtype, seed, splits=0, head_stride=0)
     enc = (lambda x: W.bf16_bits(x)) if dtype == "bf16" else (lambda x: x)
     h = dict(q=enc(f32(B, N, Hq, d)), k_tree=enc(f32(B, N, Hkv, d)), v_tree=enc(f32(B, N, Hkv, d)),
              k_prefix=enc(f32(total, d)), v_prefix=enc(f32(total, d)), prefix_len=L, kv_row0=kv_row0)
+    if nan_tail and hs:  # cache rows past each prefix hold NaN: they must never reach the output
+        nan = W.bf16_bits(np.array([np.nan], np.float32))[0] if dtype == "bf16" else np.float32(np.nan)
+        for b in range(B):
+            for g in range(Hkv):
+                lo = kv_row0[b] + g * hs + int(L[b])
+                h["k_prefix"][lo:kv_row0[b] + (g + 1) * hs] = nan
+                h["v_prefix"][lo:kv_row0[b] + (g + 1) * hs] = nan
     # oracle view of the prefix (respecting the head stride)
     kpf, vpf = W.as_float(wl, h["k_prefix"]), W.as_float(wl, h["v_prefix"])
     kp, vp = [], []
@@ -197,7 +204,7 @@ def _attn_case(B, N, Hq, Hkv, d, prefixes, dtype, seed, splits=0, head_stride=0)
 
     shape = E.AttnShape(B=B, N=N, Hq=Hq, Hkv=Hkv, d=d, dtype=E.ET_BF16 if dtype == "bf16" else E.ET_F32,
                         scale=d ** -0.5, max_prefix=int(L.max()) if B else 0, kv_rows=total,
-                        kv_head_stride=hs, num_splits=splits)
+                        kv_head_stride=hs, num_splits=splits, impl=impl)
     out = torch.full((B, N, Hq, d), float("nan"), dtype=dt, device="cuda")
     lse_g = torch.zeros((B, Hq, N), dtype=torch.float32, device="cuda")
     ws = E.new_workspace(E.et_tree_attention_workspace_size(shape))
@@ -217,18 +224,29 @@ ATTN_CASES = [
     (1, 61, 32, 32, 128, [1024], "bf16", 0, 0),     # 7B shape at its bench prefix
     (1, 61, 4, 4, 128, [1000], "bf16", 1, 0),       # single split, ragged last tile
     (1, 61, 4, 4, 128, [1000], "bf16", 7, 0),       # uneven splits
-    (2, 81, 16, 2, 128, [300, 129], "bf16", 0, 0),  # GQA group 8, two row tiles, N > 64
+    (2, 81, 16, 2, 128, [300, 129], "bf16", 0, 0),  # GQA group 8, N > 64
+    (1, 81, 64, 8, 128, [700], "bf16", 0, 0),       # 70B heads: 648 rows per KV head, 6 row tiles
     (3, 101, 4, 4, 128, [64, 0, 513], "bf16", 0, 0),  # empty prefix, N = 101 (two mask words)
     (2, 33, 8, 2, 64, [200, 77], "bf16", 3, 0),     # d = 64
     (2, 20, 4, 2, 128, [100, 60], "bf16", 2, 128),  # static cache layout (head stride)
     (1, 128, 2, 2, 128, [257], "bf16", 0, 0),       # maximum N
+    (2, 7, 4, 4, 128, [0, 0], "bf16", 0, 0),        # no prefix at all
+    (1, 61, 8, 8, 128, [4096], "bf16", 32, 0),      # many splits (8 on the tcgen05 path: one cluster)
+    (1, 61, 8, 8, 128, [1000], "bf16", 5, 0),       # odd cluster size
 ]
 
 
+@pytest.mark.parametrize("impl", [E.ATTN_MMA_SYNC, E.ATTN_TCGEN05])
 @pytest.mark.parametrize("B,N,Hq,Hkv,d,prefixes,dtype,splits,hs", ATTN_CASES)
-def test_attention_matches_oracle(B, N, Hq, Hkv, d, prefixes, dtype, splits, hs):
+def test_attention_matches_oracle(B, N, Hq, Hkv, d, prefixes, dtype, splits, hs, impl):
+    if dtype == "f32":
+        if impl != E.ATTN_MMA_SYNC:
+            pytest.skip("fp32 has one path")
+        impl = E.ATTN_AUTO
+    if impl == E.ATTN_TCGEN05 and d != 128:
+        pytest.skip("the tcgen05 path is built for d = 128")
     got, lse_g, ref, lse_o, status = _attn_case(B, N, Hq, Hkv, d, prefixes, dtype, seed=N * 7 + d, splits=splits,
-                                                head_stride=hs)
+                                                head_stride=hs, impl=impl)
     assert status == 0
     assert np.isfinite(got).all()
     err = np.abs(got - ref).max()
@@ -238,6 +256,21 @@ def test_attention_matches_oracle(B, N, Hq, Hkv, d, prefixes, dtype, splits, hs)
     else:
         assert err <= F32_MAX_ABS and rl <= F32_REL_L2, (err, rl)
     assert np.abs(lse_g - lse_o).max() < 1e-3
+
+
+@pytest.mark.parametrize("impl", [E.ATTN_MMA_SYNC, E.ATTN_TCGEN05])
+def test_attention_ignores_cache_rows_past_the_prefix(impl):
+    """A static cache whose rows past the prefix hold NaN: the output stays exact."""
+    got, _, ref, _, status = _attn_case(2, 24, 4, 2, 128, [100, 37], "bf16", seed=5, splits=2, head_stride=192,
+                                        impl=impl, nan_tail=True)
+    assert status == 0 and np.isfinite(got).all()
+    assert np.abs(got - ref).max() <= BF16_MAX_ABS and rel_l2(got, ref) <= BF16_REL_L2
+
+
+def test_tcgen05_and_mma_paths_agree_at_the_7b_shape():
+    a = _attn_case(1, 61, 32, 32, 128, [1024], "bf16", seed=1, impl=E.ATTN_TCGEN05)[0]
+    b = _attn_case(1, 61, 32, 32, 128, [1024], "bf16", seed=1, impl=E.ATTN_MMA_SYNC)[0]
+    assert np.abs(a - b).max() <= 2 * BF16_MAX_ABS
 
 
 # ---------------------------------------------------------------------------
