@@ -487,15 +487,14 @@ static bool make_plan(const et_attn_shape *s, AttnPlan *p) {
     const int cap = T / 2 > 0 ? T / 2 : 1;  // at least two K/V tiles per split
     int S = s->num_splits;
     if (p->impl == 2) {
-      // the splits of a row tile form one thread-block cluster (<= 8 blocks,
-      // one block per SM); pick the most splits whose clusters all fit in one wave
+      // the splits of a row tile form one thread-block cluster (<= 8 blocks);
+      // two blocks fit per SM: aim at ~1.7 blocks per SM so that the
+      // clusters still find room in one wave (measured on GB300: 6 splits for
+      // 40 heads and 5 for 48 row tiles beat both fewer and more)
       if (S <= 0) {
-        S = 1;
-        for (int c = kTcMaxSplits; c >= 2; --c) {
-          if (c > cap) continue;
-          const int fit = tc_max_clusters(c);
-          if (fit > 0 && base <= fit) { S = c; break; }
-        }
+        S = (int)((17LL * sm_count()) / (10LL * base));
+        if (S > cap) S = cap;
+        if (S < 1) S = 1;
       }
       if (S > kTcMaxSplits) S = kTcMaxSplits;
     } else if (S <= 0) {  // two resident blocks per SM

@@ -3,23 +3,25 @@
 // in-tree ancestors (EAGLE-2 article on sbmmt.com, attention-mask
 // paragraph; EAGLE blog section 1.1: one target pass verifies the draft).
 //
-// One block per (KV split, KV head x 128-row tile, sequence), one block per
-// SM, 8 warps:
-//   warp 0     TMA producer: 64-key K and V tiles (128-byte swizzle) into a
-//              4-stage ring guarded by mbarriers (expect-tx / commit);
+// One block per (KV split, KV head x 128-row tile, sequence), two blocks per
+// SM, 8 warps each:
+//   warps 0, 2 TMA producers: 64-key K tiles (warp 0) and V tiles (warp 2),
+//              128-byte swizzle, each into its own 2-stage ring guarded by
+//              mbarriers (expect-tx / commit); a K stage is released as soon
+//              as its QK^T is done, a V stage after its P.V;
 //   warp 1     owns 256 TMEM columns and issues tcgen05.mma:
-//              S_j = Q K_j^T  (M=128, N=64, K=128)  into TMEM S[j%2],
-//              O  += P_j V_j  (M=128, N=128, K=64)  into TMEM O;
-//   warps 2-11 stage the Q tile (K-major, 128-byte swizzle) at the start;
-//   warps 4-11 softmax, two warps per TMEM lane quarter: both read the whole
-//              64-column S row of their 32 query rows (mask by prefix length
-//              / ancestor bits, row max), each then exponentiates its own 32
-//              columns (log2 domain), writes them to P_j (bf16, shared
-//              memory) and rescales its half of O in TMEM, lazily (only when
-//              the row max grows by more than 2^8).
-// A 128-row tile packs (token, query head) rows of one KV head, so a GQA
-// group shares every K/V tile.  The KV splits of one tile run as one thread
-// block cluster and merge their partial results through distributed shared
+//              S_j = Q K_j^T  (M=128, N=64, K=128)  into TMEM S (issued as
+//              soon as the softmax has read S_{j-1} into registers),
+//              O  += P_j V_j  (M=128, N=128, K=64, A = P_j read from TMEM);
+//   warps 3-7  stage the Q tile (K-major, 128-byte swizzle);
+//   warps 4-7  softmax, one thread per query row (= TMEM lane): mask by
+//              prefix length / ancestor bits, online softmax in the log2
+//              domain, P_j written to TMEM as bf16 pairs, lazy rescale of O
+//              (only when the row max grows by more than 2^8).
+// Two resident blocks per SM keep two independent pipelines in flight.  A
+// 128-row tile packs (token, query head) rows of one KV head, so a GQA group
+// shares every K/V tile.  The KV splits of one tile run as one thread block
+// cluster and merge their partial results through distributed shared
 // memory.  Every mbarrier wait is bounded: on expiry the block reports
 // ET_DEV_TIMEOUT, stops, frees its TMEM and exits.
 #include <cuda.h>
@@ -33,28 +35,28 @@
 namespace et {
 namespace {
 
-constexpr int kThreads = 384;
-constexpr int kStages = 4;
+constexpr int kThreads = 256;
+constexpr int kStages = 2;                           // K ring and V ring, 2 tiles each (two blocks per SM)
 constexpr uint32_t kHalfBytes = kTcKeys * 128;       // 64 rows x 128 B (64 of the 128 dims)
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;      // one K or V tile
 constexpr uint32_t kQHalfBytes = kTcRows * 128;
 constexpr uint32_t kQBytes = 2 * kQHalfBytes;
-constexpr uint32_t kPBytes = kTcRows * 128;          // 128 rows x 64 keys bf16
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQBytes;
 constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
-constexpr uint32_t kOffP = kOffV + kStages * kTileBytes;
-constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
+constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
 constexpr uint32_t kOffMisc = kOffBar + 256;
 constexpr uint32_t kSmemBytes = kOffMisc + 256 + 1024;  // + slack for 1024-byte alignment
-constexpr uint32_t kColS0 = 0, kColS1 = 64, kColO = 128, kTmemCols = 256;
+// TMEM columns: S, O accumulator, P (bf16 pairs) double buffer
+constexpr uint32_t kColS = 0, kColO = 64, kColP0 = 192, kColP1 = 224, kTmemCols = 256;
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the row max grows by more than 2^8
 constexpr long long kWaitCycles = 1ll << 32;  // ~2 s at 2 GHz
 
 // barrier slots
-constexpr int B_FULL = 0, B_EMPTY = 4, B_SFULL = 8, B_PFULL = 10, B_OFULL = 12, B_QFULL = 13;
-constexpr int kQWarps = 10;     // warps 2-11 stage Q
-constexpr int kSoftmaxWarps = 8; // warps 4-11: two per TMEM lane quarter, one per 32-column half
+constexpr int B_KFULL = 0, B_KEMPTY = 2, B_VFULL = 4, B_VEMPTY = 6, B_SFULL = 8, B_SFREE = 9, B_PFULL = 10,
+              B_OFULL = 12, B_QFULL = 13;
+constexpr int kQWarps = 5;       // warps 3-7 stage Q
+constexpr int kSoftmaxWarps = 4; // warps 4-7: one per TMEM lane quarter
 
 __device__ __forceinline__ uint32_t saddr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -147,6 +149,20 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
                : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
                : "memory");
 }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+               :
+               : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+               : "memory");
+}
+// D (TMEM) += A (TMEM, K-major rows = lanes) * B (shared memory descriptor)
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // distributed shared memory (thread block cluster)
@@ -215,12 +231,11 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     k_attn_tc(const __grid_constant__ CUtensorMap tm_kp, const __grid_constant__ CUtensorMap tm_vp,
               const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt, const TcLaunch a) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ int row_tok[kTcRows], row_head[kTcRows];
-  __shared__ float lpart[2][kTcRows];  // the two column halves' row sums
   unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = saddr(sm);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kOffMisc);
@@ -239,13 +254,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (t == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(bar(B_FULL + i), 1);
-      mbar_init(bar(B_EMPTY + i), 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(B_SFULL + i), 1);
+      mbar_init(bar(B_KFULL + i), 1);
+      mbar_init(bar(B_KEMPTY + i), 1);
+      mbar_init(bar(B_VFULL + i), 1);
+      mbar_init(bar(B_VEMPTY + i), 1);
       mbar_init(bar(B_PFULL + i), kSoftmaxWarps);
     }
+    mbar_init(bar(B_SFULL), 1);
+    mbar_init(bar(B_SFREE), kSoftmaxWarps);
     mbar_init(bar(B_OFULL), 1);
     mbar_init(bar(B_QFULL), kQWarps);
     *abort_flag = 0;
@@ -269,84 +285,85 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   if (t == 0 && L > 0 && row0 + (long long)g * S_b + L > a.kv_rows) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
 
-  if (warp == 0) {
-    // ---------------- TMA producer (starts before Q is staged) ----------------
+  if (warp == 0 || warp == 2) {
+    // ---------------- TMA producers: warp 0 streams K tiles, warp 2 V tiles ----------------
     if (lane == 0 && T > 0) {
-      int issued = 0;  // tiles whose copies were started
+      const bool isK = warp == 0;
+      const CUtensorMap *mp = isK ? &tm_kp : &tm_vp;
+      const CUtensorMap *mt_ = isK ? &tm_kt : &tm_vt;
+      const int bF = isK ? B_KFULL : B_VFULL, bE = isK ? B_KEMPTY : B_VEMPTY;
+      const uint32_t base = sb + (isK ? kOffK : kOffV);
+      int issued = 0;
       for (int j = 0; j < T; ++j) {
         const int stage = j % kStages;
-        if (j >= kStages && !mbar_wait(bar(B_EMPTY + stage), (uint32_t)((j / kStages) - 1) & 1u, abort_flag)) break;
-        const uint32_t fb = bar(B_FULL + stage);
-        mbar_expect_tx(fb, 2 * kTileBytes);
-        const uint32_t kd = sb + kOffK + stage * kTileBytes, vd = sb + kOffV + stage * kTileBytes;
+        if (j >= kStages && !mbar_wait(bar(bE + stage), (uint32_t)((j / kStages) - 1) & 1u, abort_flag)) break;
+        const uint32_t fb = bar(bF + stage);
+        mbar_expect_tx(fb, kTileBytes);
+        const uint32_t dst = base + stage * kTileBytes;
         const int tile = t0 + j;
         if (tile < nP) {
           const int row = (int)(row0 + (long long)g * S_b + (long long)tile * kTcKeys);
-          tma_2d(kd, &tm_kp, 0, row, fb);
-          tma_2d(kd + kHalfBytes, &tm_kp, 64, row, fb);
-          tma_2d(vd, &tm_vp, 0, row, fb);
-          tma_2d(vd + kHalfBytes, &tm_vp, 64, row, fb);
+          tma_2d(dst, mp, 0, row, fb);
+          tma_2d(dst + kHalfBytes, mp, 64, row, fb);
         } else {
           const int tr = b * N + (tile - nP) * kTcKeys;
-          tma_3d(kd, &tm_kt, 0, g, tr, fb);
-          tma_3d(kd + kHalfBytes, &tm_kt, 64, g, tr, fb);
-          tma_3d(vd, &tm_vt, 0, g, tr, fb);
-          tma_3d(vd + kHalfBytes, &tm_vt, 64, g, tr, fb);
+          tma_3d(dst, mt_, 0, g, tr, fb);
+          tma_3d(dst + kHalfBytes, mt_, 64, g, tr, fb);
         }
         issued = j + 1;
       }
-      // do not leave while copies are in flight: the stages of all but the last
-      // kStages issued tiles were consumed already; wait (bounded) for those
+      // do not leave while copies are in flight (the earlier stages were consumed)
       const int first = issued > kStages ? issued - kStages : 0;
-      for (int j = first; j < issued; ++j) mbar_drain(bar(B_FULL + j % kStages), (uint32_t)(j / kStages) & 1u);
+      for (int j = first; j < issued; ++j) mbar_drain(bar(bF + j % kStages), (uint32_t)(j / kStages) & 1u);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0 && T > 0) {
       auto issue_s = [&](int j) {
         const int stage = j % kStages;
-        const uint32_t d = tmem + ((j & 1) ? kColS1 : kColS0);
         const uint32_t kbase = sb + kOffK + stage * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kTcDim / 16; ++kk) {
           const uint64_t ad = sw128_desc(sb + kOffQ + (kk >> 2) * kQHalfBytes + (kk & 3) * 32, 16, 1024);
           const uint64_t bd = sw128_desc(kbase + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
-          tc_mma(d, ad, bd, kIdescQK, kk > 0);
+          tc_mma(tmem + kColS, ad, bd, kIdescQK, kk > 0);
         }
-        tc_commit(bar(B_SFULL + (j & 1)));
+        tc_commit(bar(B_SFULL));
+        if (j + kStages < T) tc_commit(bar(B_KEMPTY + stage));  // K tile consumed once S_j is done
       };
-      bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag) && mbar_wait(bar(B_FULL + 0), 0, abort_flag);
+      bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag) && mbar_wait(bar(B_KFULL + 0), 0, abort_flag);
       if (ok) {
         tc_fence_after();
         issue_s(0);
       }
       for (int j = 0; ok && j < T; ++j) {
+        // S_{j+1} as soon as the softmax has read S_j out of TMEM
         if (j + 1 < T) {
-          const int st1 = (j + 1) % kStages;
-          if (!mbar_wait(bar(B_FULL + st1), (uint32_t)((j + 1) / kStages) & 1u, abort_flag)) break;
+          if (!mbar_wait(bar(B_SFREE), (uint32_t)j & 1u, abort_flag)) break;
+          if (!mbar_wait(bar(B_KFULL + (j + 1) % kStages), (uint32_t)((j + 1) / kStages) & 1u, abort_flag)) break;
           tc_fence_after();
           issue_s(j + 1);
         }
-        if (!mbar_wait(bar(B_PFULL + (j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag)) break;
-        tc_fence_after();
         const int stage = j % kStages;
-        const uint32_t pbase = sb + kOffP + (uint32_t)(j & 1) * kPBytes;
+        if (!mbar_wait(bar(B_PFULL + (j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag)) break;
+        if (!mbar_wait(bar(B_VFULL + stage), (uint32_t)(j / kStages) & 1u, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t pcol = tmem + ((j & 1) ? kColP1 : kColP0);
         const uint32_t vbase = sb + kOffV + stage * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-          const uint64_t ad = sw128_desc(pbase + kk * 32, 16, 1024);
           const uint64_t bd = sw128_desc(vbase + kk * 2048, kHalfBytes, 1024);
-          tc_mma(tmem + kColO, ad, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_ts(tmem + kColO, pcol + 8 * kk, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(bar(B_OFULL));
-        if (j + kStages < T) tc_commit(bar(B_EMPTY + stage));
+        if (j + kStages < T) tc_commit(bar(B_VEMPTY + stage));
       }
     }
   }
-  if (warp >= 2) {
-    // ---------------- Q tile -> shared memory (warps 2-11) ----------------
+  if (warp >= 3) {
+    // ---------------- Q tile -> shared memory (warps 3-7) ----------------
     const __nv_bfloat16 *Q = static_cast<const __nv_bfloat16 *>(a.q);
-    for (int x = t - 64; x < kTcRows * 16; x += kThreads - 64) {
+    for (int x = t - 96; x < kTcRows * 16; x += kThreads - 96) {
       const int r = x >> 4, c = x & 15;
       const int i = row_tok[r];
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -362,12 +379,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) mbar_arrive(bar(B_QFULL));
   }
 
-  // softmax geometry: warp w >= 4 reads TMEM lane quarter (w % 4) = tile rows
-  // 32*(w%4) .. +31 and owns the 32-column half hh of every S tile
+  // softmax: warp w (4..7) owns TMEM lane quarter w - 4 = tile rows 32 (w-4) .. +31
   const bool smx = warp >= 4;
-  const int quarter = warp & 3, hh = (warp - 4) >> 2;
-  const int r = 32 * quarter + lane;
-  float m_used = -INFINITY, l = 0.f;  // l: this half's share of the row sum
+  const int r = t - 128;
+  float m_used = -INFINITY, l = 0.f;
   const int my_tok = smx ? row_tok[r] : -1;
   bool ok_rows = true;
   if (smx) {
@@ -377,22 +392,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       mw0 = a.mask[((long long)b * N + my_tok) * a.W];
       if (a.W > 1) mw1 = a.mask[((long long)b * N + my_tok) * a.W + 1];
     }
-    const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
+    const uint32_t lane_base = tmem + ((uint32_t)(r & ~31) << 16);
     const float scale = a.scale_log2;
     uint32_t raw[64];
     for (int j = 0; j < T; ++j) {
       const int tile = t0 + j;
-      if (!warp_wait(bar(B_SFULL + (j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag)) { ok_rows = false; break; }
+      if (!warp_wait(bar(B_SFULL), (uint32_t)j & 1u, abort_flag)) { ok_rows = false; break; }
       tc_fence_after();
       if (active) {
-        tmem_ld64(lane_base + ((j & 1) ? kColS1 : kColS0), raw);
+        tmem_ld64(lane_base + kColS, raw);
         tmem_wait_ld();
+      }
+      // S is free for S_{j+1} as soon as it sits in registers
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_SFREE));
+      if (active) {
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (tile < nP && L - tile * kTcKeys >= kTcKeys) {  // a full prefix tile: nothing to mask
+        const int lim = tile < nP ? L - tile * kTcKeys : 0;
+        if (tile < nP && lim >= kTcKeys) {  // a full prefix tile: nothing to mask
 #pragma unroll
           for (int c = 0; c < 64; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(raw[c]));
         } else {
-          const int lim = tile < nP ? L - tile * kTcKeys : 0;
           const unsigned long long w = tile < nP ? 0ull : ((tile - nP) == 0 ? mw0 : mw1);
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
@@ -405,16 +426,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale;  // scale > 0
         const float m_new = fmaxf(m_used, tmax);
         const bool grow = m_new > m_used + kRescaleLog2;  // also true for the first finite max
-        // O in TMEM holds sum_{<j} P V relative to m_used: rescale this warp's
-        // 64 columns of it when the max grew by more than 2^8 (warp-collective)
+        // O in TMEM holds sum_{<j} P V relative to m_used: rescale it when the
+        // max grew by more than 2^8 (warp-collective TMEM access)
         if (__any_sync(0xffffffffu, grow && j > 0 && m_used > -INFINITY)) {
           if (!warp_wait(bar(B_OFULL), (uint32_t)(j - 1) & 1u, abort_flag)) { ok_rows = false; break; }
           tc_fence_after();
           const float sc = (grow && m_used > -INFINITY) ? ex2(m_used - m_new) : 1.f;
           uint32_t ov[32];
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {
-            const uint32_t oa = lane_base + kColO + 64 * hh + 32 * part;
+          for (int part = 0; part < 4; ++part) {
+            const uint32_t oa = lane_base + kColO + 32 * part;
             tmem_ld32(oa, ov);
             tmem_wait_ld();
 #pragma unroll
@@ -427,39 +448,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (grow) m_used = m_new;
         const float nm = m_used == -INFINITY ? 0.f : -m_used;
         float sm4[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint32_t prow = sb + kOffP + (uint32_t)(j & 1) * kPBytes + (uint32_t)r * 128u;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {  // this half's 4 chunks of P (bf16, 128-byte swizzle)
-          uint32_t q4[4];
+        for (int h = 0; h < 2; ++h) {  // P = 2^(s * scale - m) as bf16 pairs, 32 keys at a time
+          uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int col = 32 * hh + 8 * c + 2 * e;
-            const float p0 = ex2(fmaf(__uint_as_float(raw[col]), scale, nm));
-            const float p1 = ex2(fmaf(__uint_as_float(raw[col + 1]), scale, nm));
-            sm4[c] += p0 + p1;
-            q4[e] = pack_bf16x2(p0, p1);
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ex2(fmaf(__uint_as_float(raw[32 * h + 2 * e]), scale, nm));
+            const float p1 = ex2(fmaf(__uint_as_float(raw[32 * h + 2 * e + 1]), scale, nm));
+            sm4[e & 3] += p0 + p1;
+            pk[e] = pack_bf16x2(p0, p1);
           }
-          const uint32_t dst = prow + (uint32_t)(((4 * hh + c) ^ (r & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(q4[0]), "r"(q4[1]), "r"(q4[2]),
-                       "r"(q4[3])
-                       : "memory");
+          tmem_st16(lane_base + ((j & 1) ? kColP1 : kColP0) + 16 * h, pk);
         }
+        tmem_wait_st();
         l += (sm4[0] + sm4[1]) + (sm4[2] + sm4[3]);
       }
       // the last, partial prefix tile: clear the V rows past the prefix so that
-      // whatever the cache holds there cannot reach P.V (0 * NaN); the eight
-      // softmax warps share the chunks
+      // whatever the cache holds there cannot reach P.V (0 * NaN)
       if (tile == nP - 1 && (L & (kTcKeys - 1))) {
         const int stage = j % kStages;
-        if (!warp_wait(bar(B_FULL + stage), (uint32_t)(j / kStages) & 1u, abort_flag)) ok_rows = false;
+        if (!warp_wait(bar(B_VFULL + stage), (uint32_t)(j / kStages) & 1u, abort_flag)) ok_rows = false;
         const int first = L & (kTcKeys - 1);
         unsigned char *vs = sm + kOffV + stage * kTileBytes;
-        for (int x = t - 128; x < (kTcKeys - first) * 16; x += 32 * kSoftmaxWarps) {
+        for (int x = r; x < (kTcKeys - first) * 16; x += 32 * kSoftmaxWarps) {
           const int row = first + (x >> 4), c = x & 15;
           *reinterpret_cast<uint4 *>(vs + (c >> 3) * kHalfBytes + row * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
         }
+        fence_async_smem();
       }
-      fence_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PFULL + (j & 1)));
@@ -468,60 +484,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the last P.V must have landed before O is read
     if (ok_rows && T > 0 && !warp_wait(bar(B_OFULL), (uint32_t)(T - 1) & 1u, abort_flag)) ok_rows = false;
   }
-  if (smx) lpart[hh][r] = l;
   __syncthreads();
   tc_fence_after();
   const bool aborted = *abort_flag != 0;
   if (smx && !aborted) {
     // ---------------- this block's rows: output, or the cluster merge buffer ----------------
-    const float lt = lpart[0][r] + lpart[1][r];
     const bool active = __any_sync(0xffffffffu, my_tok >= 0);
-    const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
-    const float inv = lt > 0.f ? 1.f / lt : 0.f;
+    const uint32_t lane_base = tmem + ((uint32_t)(r & ~31) << 16);
+    const float inv = l > 0.f ? 1.f / l : 0.f;
     if (active && T > 0) {
-      uint32_t ov[64];
-      tmem_ld64(lane_base + kColO + 64 * hh, ov);
-      tmem_wait_ld();
-      if (a.S == 1) {
-        if (my_tok >= 0) {
-          __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) +
-                                (((long long)b * N + my_tok) * a.Hq + row_head[r]) * kTcDim + 64 * hh;
+      uint32_t ov[32];
+#pragma unroll 1
+      for (int h = 0; h < 4; ++h) {
+        tmem_ld32(lane_base + kColO + 32 * h, ov);
+        tmem_wait_ld();
+        if (a.S == 1) {
+          if (my_tok >= 0) {
+            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) +
+                                  (((long long)b * N + my_tok) * a.Hq + row_head[r]) * kTcDim + 32 * h;
 #pragma unroll
-          for (int c = 0; c < 64; c += 8) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
-            v.y = pack_bf16x2(__uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv);
-            v.z = pack_bf16x2(__uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv);
-            v.w = pack_bf16x2(__uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv);
-            *reinterpret_cast<uint4 *>(orow + c) = v;
+            for (int c = 0; c < 32; c += 8) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
+              v.y = pack_bf16x2(__uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv);
+              v.z = pack_bf16x2(__uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv);
+              v.w = pack_bf16x2(__uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv);
+              *reinterpret_cast<uint4 *>(orow + c) = v;
+            }
           }
-        }
-      } else {  // unnormalised fp32 half row, 16-byte chunks swizzled by the row
+        } else {  // unnormalised fp32 row (K and V stages, 64 KB), 16-byte chunks swizzled by the row
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int chunk = 16 * hh + c;
-          const uint32_t dst = sb + kOffK + (uint32_t)r * 512u + (uint32_t)((chunk ^ (r & 31)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(ov[4 * c]), "r"(ov[4 * c + 1]),
-                       "r"(ov[4 * c + 2]), "r"(ov[4 * c + 3])
-                       : "memory");
+          for (int c = 0; c < 8; ++c) {
+            const int chunk = 8 * h + c;
+            const uint32_t dst = sb + kOffK + (uint32_t)r * 512u + (uint32_t)((chunk ^ (r & 31)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(ov[4 * c]), "r"(ov[4 * c + 1]),
+                         "r"(ov[4 * c + 2]), "r"(ov[4 * c + 3])
+                         : "memory");
+          }
         }
       }
     } else if (a.S > 1) {  // no real row here, or no keys at all: contribute nothing
-      for (int c = 0; c < 16; ++c) {
-        const int chunk = 16 * hh + c;
+      for (int chunk = 0; chunk < 32; ++chunk) {
         const uint32_t dst = sb + kOffK + (uint32_t)r * 512u + (uint32_t)((chunk ^ (r & 31)) << 4);
         asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0u) : "memory");
       }
     }
-    if (hh == 0) {
-      if (a.S == 1) {
-        if (my_tok >= 0 && a.lse)
-          a.lse[((long long)b * a.Hq + row_head[r]) * N + my_tok] =
-              lt > 0.f ? (m_used + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
-      } else {
-        *reinterpret_cast<float2 *>(sm + kOffP + 8 * r) =
-            make_float2(T > 0 ? m_used : -INFINITY, T > 0 ? lt : 0.f);
-      }
+    if (a.S == 1) {
+      if (my_tok >= 0 && a.lse)
+        a.lse[((long long)b * a.Hq + row_head[r]) * N + my_tok] =
+            l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+    } else {
+      *reinterpret_cast<float2 *>(sm + kOffQ + 8 * r) = make_float2(T > 0 ? m_used : -INFINITY, T > 0 ? l : 0.f);
     }
   }
   tc_fence_before();
@@ -535,18 +548,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (a.S == 1) return;
 
   // ---------------- merge the S splits of this tile across the cluster ----------------
+  // partial rows: [128][128] fp32 over the K and V stages; (max, sum) pairs and
+  // merge weights in the Q tile's space (all MMAs are done)
+  static_assert(kOffV == kOffK + 32768 && 2 * kStages * kTileBytes >= kTcRows * kTcDim * 4, "merge buffer");
   cluster_sync_all();  // every split's partial rows are in its shared memory
   {
     const int S = a.S;
     const int per = (kTcRows + S - 1) / S;
     const int r0 = s * per, r1 = min(kTcRows, r0 + per);
-    float *wts = reinterpret_cast<float *>(sm + kOffP + 2048);  // [per][kTcMaxSplits] weights / total
+    float *wts = reinterpret_cast<float *>(sm + kOffQ + 2048);  // [per][kTcMaxSplits] weights / total
     if (t < r1 - r0 && !aborted) {
       const int rr = r0 + t;
       float2 ml[kTcMaxSplits];
 #pragma unroll
       for (int x = 0; x < kTcMaxSplits; ++x)  // all loads first: distributed shared memory latency overlaps
-        ml[x] = x < S ? ld_cluster_f2(cluster_map(sb + kOffP + 8 * rr, (uint32_t)x)) : make_float2(-INFINITY, 0.f);
+        ml[x] = x < S ? ld_cluster_f2(cluster_map(sb + kOffQ + 8 * rr, (uint32_t)x)) : make_float2(-INFINITY, 0.f);
       float M = -INFINITY;
 #pragma unroll
       for (int x = 0; x < kTcMaxSplits; ++x) M = fmaxf(M, ml[x].x);
@@ -571,18 +587,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int i = row_tok[rr];
       if (i < 0) continue;
       const uint32_t off = sb + kOffK + (uint32_t)rr * 512u + (uint32_t)((chunk ^ (rr & 31)) << 4);
-      float4 p[kTcMaxSplits];
-#pragma unroll
-      for (int sp = 0; sp < kTcMaxSplits; ++sp)
-        p[sp] = sp < S ? ld_cluster_f4(cluster_map(off, (uint32_t)sp)) : make_float4(0.f, 0.f, 0.f, 0.f);
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int sp = 0; sp < kTcMaxSplits; ++sp) {
-        const float wv = sp < S ? wts[lr * kTcMaxSplits + sp] : 0.f;
-        acc.x = fmaf(wv, p[sp].x, acc.x);
-        acc.y = fmaf(wv, p[sp].y, acc.y);
-        acc.z = fmaf(wv, p[sp].z, acc.z);
-        acc.w = fmaf(wv, p[sp].w, acc.w);
+      for (int g4 = 0; g4 < kTcMaxSplits; g4 += 4) {  // four loads in flight at a time
+        float4 p[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          p[q] = g4 + q < S ? ld_cluster_f4(cluster_map(off, (uint32_t)(g4 + q))) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float wv = g4 + q < S ? wts[lr * kTcMaxSplits + g4 + q] : 0.f;
+          acc.x = fmaf(wv, p[q].x, acc.x);
+          acc.y = fmaf(wv, p[q].y, acc.y);
+          acc.z = fmaf(wv, p[q].z, acc.z);
+          acc.w = fmaf(wv, p[q].w, acc.w);
+        }
       }
       uint2 v;
       v.x = pack_bf16x2(acc.x, acc.y);
@@ -645,37 +664,6 @@ cudaError_t set_smem_attr() {
 }
 
 }  // namespace
-
-int tc_max_clusters(int cluster_size) {
-  static std::mutex mu;
-  static int cache[64][kTcMaxSplits + 1];
-  static bool filled[64][kTcMaxSplits + 1];
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || cluster_size < 1 || cluster_size > kTcMaxSplits) return 0;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!filled[dev][cluster_size]) {
-    int n = 0;
-    if (set_smem_attr() == cudaSuccess) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(cluster_size, 1, 1);
-      cfg.blockDim = dim3(kThreads, 1, 1);
-      cfg.dynamicSmemBytes = kSmemBytes;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = cluster_size;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&n, k_attn_tc, &cfg) != cudaSuccess) n = 0;
-    }
-    cudaGetLastError();
-    cache[dev][cluster_size] = n;
-    filled[dev][cluster_size] = true;
-  }
-  return cache[dev][cluster_size];
-}
 
 et_status tc_attention_launch(const TcLaunch &a, cudaStream_t stream) {
   if (!encode_fn()) return ET_ERR_CUDA;

@@ -30,7 +30,5 @@ constexpr int kTcDim = 128;    // head dim of the tcgen05 path
 constexpr int kTcMaxSplits = 8;  // KV splits of one row tile = one thread-block cluster (portable size)
 
 ET_HIDDEN et_status tc_attention_launch(const TcLaunch &a, cudaStream_t stream);
-// How many clusters of `cluster_size` attention blocks fit on the device at once.
-ET_HIDDEN int tc_max_clusters(int cluster_size);
 
 }  // namespace et
