@@ -245,10 +245,13 @@ et_status et_tree_mask_posids(const et_tree_cfg *cfg, const et_tree *tree,
  * mask          uint64 [B, N, W] from et_tree_mask_posids.
  * lse           nullable fp32 [B, Hq, N]: natural-log log-sum-exp of the
  *               scaled scores of each row.
- * ws            et_tree_attention_workspace_size(shape) bytes (may be 0/null
- *               when that size is 0: the fp32 path, one split, or the
- *               tcgen05 path, whose splits form a thread-block cluster and
- *               merge through distributed shared memory).
+ * ws            et_tree_attention_workspace_size(shape) bytes, 256-byte
+ *               aligned, owned by the caller, no initial contents required
+ *               (may be 0/null when that size is 0: the fp32 path or one
+ *               split).  Holds the fp32 partial rows and (max, sum) pairs of
+ *               the KV splits; the tcgen05 path drops its lines from L2 once
+ *               merged.  Calls that run at the same time need separate
+ *               workspaces.
  * Accumulation is fp32; P is rounded to the input dtype before P.V.
  * tcgen05 path: at most 8 splits (one cluster); a bounded wait that expires
  * sets ET_DEV_TIMEOUT in dev_status and leaves that tile's output undefined.

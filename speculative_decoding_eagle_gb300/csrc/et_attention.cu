@@ -508,7 +508,8 @@ static bool make_plan(const et_attn_shape *s, AttnPlan *p) {
   }
   p->ws = 0;
   p->cnt_off = p->ml_off = p->po_off = 0;
-  if (p->impl == 1 && p->S > 1) {  // the tcgen05 path merges its splits on chip
+  if (p->impl == 2) p->ws = tc_workspace_bytes((long long)s->B * s->Hkv * p->MT, p->S);
+  if (p->impl == 1 && p->S > 1) {
     const size_t tiles = (size_t)s->B * s->Hkv * p->MT;
     const size_t cnt = (tiles * sizeof(unsigned int) + 255) & ~(size_t)255;
     const size_t ml = (tiles * p->S * p->rows * sizeof(float2) + 255) & ~(size_t)255;
@@ -563,6 +564,7 @@ extern "C" et_status et_tree_attention(const et_attn_shape *shape, const void *q
     t.kv_head_stride = shape->kv_head_stride;
     t.mask = reinterpret_cast<const unsigned long long *>(mask);
     t.out = out; t.lse = lse; t.dev_status = dev_status;
+    t.ws = static_cast<float *>(ws);
     ET_RETURN_IF((long long)t.Hkv * t.MT > 65535 || t.B > 65535, ET_ERR_UNSUPPORTED);
     return tc_attention_launch(t, st);
   }

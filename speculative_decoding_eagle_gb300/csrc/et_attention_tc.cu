@@ -13,16 +13,20 @@
 //              S_j = Q K_j^T  (M=128, N=64, K=128)  into TMEM S (issued as
 //              soon as the softmax has read S_{j-1} into registers),
 //              O  += P_j V_j  (M=128, N=128, K=64, A = P_j read from TMEM);
-//   warps 3-7  stage the Q tile (K-major, 128-byte swizzle);
+//   warps 3-7  stage the Q tile (K-major, 128-byte swizzle) when it cannot
+//              come by TMA (G not a divisor of 128);
 //   warps 4-7  softmax, one thread per query row (= TMEM lane): mask by
 //              prefix length / ancestor bits, online softmax in the log2
 //              domain, P_j written to TMEM as bf16 pairs, lazy rescale of O
 //              (only when the row max grows by more than 2^8).
 // Two resident blocks per SM keep two independent pipelines in flight.  A
 // 128-row tile packs (token, query head) rows of one KV head, so a GQA group
-// shares every K/V tile.  The KV splits of one tile run as one thread block
-// cluster and merge their partial results through distributed shared
-// memory.  Every mbarrier wait is bounded: on expiry the block reports
+// shares every K/V tile.  The KV splits of one tile run as one thread-block
+// cluster: each split writes its partial rows to an L2-resident workspace,
+// one cluster barrier orders them, each split merges a slice of the rows and
+// drops the scratch lines from L2 (measured on GB300, moving the same bytes
+// through distributed shared memory took about four times as long).  Every
+// mbarrier wait is bounded: on expiry the block reports
 // ET_DEV_TIMEOUT, stops, frees its TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -107,6 +111,14 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int
       ::"r"(dst), "l"((unsigned long long)map), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
+                                       uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(dst),
+      "l"((unsigned long long)map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
@@ -166,23 +178,9 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // distributed shared memory (thread block cluster)
-__device__ __forceinline__ uint32_t cluster_map(uint32_t local, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-__device__ __forceinline__ float2 ld_cluster_f2(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
-  return v;
+// drop a 128-byte line of merge scratch from L2 without writing it back
+__device__ __forceinline__ void discard_l2_line(const void *p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
 }
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -219,10 +217,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ void split_range_tc(int L, int N, int S, int s, int &t0, int &t1, int &nP) {
   nP = (L + kTcKeys - 1) / kTcKeys;
   const int T = nP + (N + kTcKeys - 1) / kTcKeys;
-  const int per = (T + S - 1) / S;
-  t0 = s * per;
-  t1 = min(T, t0 + per);
-  if (t0 > T) t0 = T;
+  const int base = T / S, rem = T - base * S;  // split sizes differ by at most one tile
+  t0 = s * base + min(s, rem);
+  t1 = t0 + base + (s < rem ? 1 : 0);
 }
 
 
@@ -233,7 +230,8 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 
 __global__ void __launch_bounds__(kThreads, 2)
     k_attn_tc(const __grid_constant__ CUtensorMap tm_kp, const __grid_constant__ CUtensorMap tm_vp,
-              const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt, const TcLaunch a) {
+              const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt,
+              const __grid_constant__ CUtensorMap tm_q, const TcLaunch a) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ int row_tok[kTcRows], row_head[kTcRows];
   unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -263,9 +261,37 @@ __global__ void __launch_bounds__(kThreads, 2)
     mbar_init(bar(B_SFULL), 1);
     mbar_init(bar(B_SFREE), kSoftmaxWarps);
     mbar_init(bar(B_OFULL), 1);
-    mbar_init(bar(B_QFULL), kQWarps);
+    mbar_init(bar(B_QFULL), a.q_tma ? 1 : kQWarps);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // the first K and V tiles and the Q tile go out before anything else
+    // (TMEM allocation, row tables): their round trip is the longest latency
+    // of the prologue
+    for (int j = 0; j < T && j < kStages; ++j) {
+      const int tile = t0 + j;
+#pragma unroll
+      for (int kv = 0; kv < 2; ++kv) {
+        const uint32_t fb = bar((kv ? B_VFULL : B_KFULL) + j);
+        mbar_expect_tx(fb, kTileBytes);
+        const uint32_t dst = sb + (kv ? kOffV : kOffK) + j * kTileBytes;
+        if (tile < nP) {
+          const int row = (int)(row0 + (long long)g * S_b + (long long)tile * kTcKeys);
+          tma_2d(dst, kv ? &tm_vp : &tm_kp, 0, row, fb);
+          tma_2d(dst + kHalfBytes, kv ? &tm_vp : &tm_kp, 64, row, fb);
+        } else {
+          const int tr = b * N + (tile - nP) * kTcKeys;
+          tma_3d(dst, kv ? &tm_vt : &tm_kt, 0, g, tr, fb);
+          tma_3d(dst + kHalfBytes, kv ? &tm_vt : &tm_kt, 64, g, tr, fb);
+        }
+      }
+    }
+    if (a.q_tma) {  // rows (token, head in group) of KV head g: one 4-D box per 64 dims
+      const uint32_t qb = bar(B_QFULL);
+      mbar_expect_tx(qb, kQBytes);
+      const int tok0 = b * N + mt * (kTcRows / a.G);
+      tma_4d(sb + kOffQ, &tm_q, 0, 0, g, tok0, qb);
+      tma_4d(sb + kOffQ + kQHalfBytes, &tm_q, 64, 0, g, tok0, qb);
+    }
   }
   if (t < kTcRows) {
     const int R = mt * kTcRows + t;
@@ -293,8 +319,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       const CUtensorMap *mt_ = isK ? &tm_kt : &tm_vt;
       const int bF = isK ? B_KFULL : B_VFULL, bE = isK ? B_KEMPTY : B_VEMPTY;
       const uint32_t base = sb + (isK ? kOffK : kOffV);
-      int issued = 0;
-      for (int j = 0; j < T; ++j) {
+      int issued = T < kStages ? T : kStages;  // the first stages went out at the top
+      for (int j = issued; j < T; ++j) {
         const int stage = j % kStages;
         if (j >= kStages && !mbar_wait(bar(bE + stage), (uint32_t)((j / kStages) - 1) & 1u, abort_flag)) break;
         const uint32_t fb = bar(bF + stage);
@@ -360,8 +386,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
   }
-  if (warp >= 3) {
-    // ---------------- Q tile -> shared memory (warps 3-7) ----------------
+  if (warp >= 3 && !a.q_tma) {
+    // ---------------- Q tile -> shared memory (warps 3-7) when G does not divide 128 ----------------
     const __nv_bfloat16 *Q = static_cast<const __nv_bfloat16 *>(a.q);
     for (int x = t - 96; x < kTcRows * 16; x += kThreads - 96) {
       const int r = x >> 4, c = x & 15;
@@ -487,56 +513,79 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc_fence_after();
   const bool aborted = *abort_flag != 0;
-  if (smx && !aborted) {
-    // ---------------- this block's rows: output, or the cluster merge buffer ----------------
-    const bool active = __any_sync(0xffffffffu, my_tok >= 0);
-    const uint32_t lane_base = tmem + ((uint32_t)(r & ~31) << 16);
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    if (active && T > 0) {
+  if (a.S == 1) {
+    // ---------------- single split: normalise and write this block's rows ----------------
+    if (smx && !aborted && __any_sync(0xffffffffu, my_tok >= 0) && T > 0) {
+      const uint32_t lane_base = tmem + ((uint32_t)(r & ~31) << 16);
+      const float inv = l > 0.f ? 1.f / l : 0.f;
       uint32_t ov[32];
 #pragma unroll 1
       for (int h = 0; h < 4; ++h) {
         tmem_ld32(lane_base + kColO + 32 * h, ov);
         tmem_wait_ld();
-        if (a.S == 1) {
-          if (my_tok >= 0) {
-            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) +
-                                  (((long long)b * N + my_tok) * a.Hq + row_head[r]) * kTcDim + 32 * h;
+        if (my_tok >= 0) {
+          __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) +
+                                (((long long)b * N + my_tok) * a.Hq + row_head[r]) * kTcDim + 32 * h;
 #pragma unroll
-            for (int c = 0; c < 32; c += 8) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
-              v.y = pack_bf16x2(__uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv);
-              v.z = pack_bf16x2(__uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv);
-              v.w = pack_bf16x2(__uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv);
-              *reinterpret_cast<uint4 *>(orow + c) = v;
-            }
-          }
-        } else {  // unnormalised fp32 row (K and V stages, 64 KB), 16-byte chunks swizzled by the row
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const int chunk = 8 * h + c;
-            const uint32_t dst = sb + kOffK + (uint32_t)r * 512u + (uint32_t)((chunk ^ (r & 31)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(ov[4 * c]), "r"(ov[4 * c + 1]),
-                         "r"(ov[4 * c + 2]), "r"(ov[4 * c + 3])
-                         : "memory");
+          for (int c = 0; c < 32; c += 8) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv);
+            *reinterpret_cast<uint4 *>(orow + c) = v;
           }
         }
       }
-    } else if (a.S > 1) {  // no real row here, or no keys at all: contribute nothing
-      for (int chunk = 0; chunk < 32; ++chunk) {
-        const uint32_t dst = sb + kOffK + (uint32_t)r * 512u + (uint32_t)((chunk ^ (r & 31)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0u) : "memory");
-      }
-    }
-    if (a.S == 1) {
       if (my_tok >= 0 && a.lse)
         a.lse[((long long)b * a.Hq + row_head[r]) * N + my_tok] =
             l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-    } else {
-      *reinterpret_cast<float2 *>(sm + kOffQ + 8 * r) = make_float2(T > 0 ? m_used : -INFINITY, T > 0 ? l : 0.f);
     }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+      __syncwarp();
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+    if (aborted && t == 0) flag_status(a.dev_status, ET_DEV_TIMEOUT);
+    return;
   }
+
+  // ---------------- S splits: partial rows through L2, merged by their owners ----------------
+  // Each split stages its unnormalised fp32 rows in shared memory (the K and
+  // V stages, free now), copies the real rows to the workspace as coalesced
+  // 512-byte row writes and posts (max, sum) per row.  After one cluster
+  // barrier, split s merges rows [s * per, (s + 1) * per) of the tile from
+  // all S partials, then drops those scratch lines from L2 so that they are
+  // never written back to DRAM.
+  const int S = a.S;
+  const int nvalid = min(kTcRows, N * a.G - mt * kTcRows);  // the real rows are a prefix of the tile
+  const long long tile_id = (long long)blockIdx.z * gridDim.y + blockIdx.y;
+  const long long n_tiles = (long long)gridDim.y * gridDim.z;
+  float *ws_o = a.ws;                                                                  // [tiles][S][128][128]
+  float2 *ws_ml = reinterpret_cast<float2 *>(a.ws + n_tiles * S * kTcRows * kTcDim);  // [tiles][S][128]
+  const bool have = !aborted && T > 0;
+  if (smx) {
+    if (have && __any_sync(0xffffffffu, my_tok >= 0)) {
+      const uint32_t lane_base = tmem + ((uint32_t)(r & ~31) << 16);
+      uint32_t ov[32];
+#pragma unroll 1
+      for (int h = 0; h < 4; ++h) {
+        tmem_ld32(lane_base + kColO + 32 * h, ov);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {  // 16-byte chunk j of row r sits at j ^ (r & 31): no bank conflicts
+          const uint32_t dst = sb + kOffK + (uint32_t)r * 512u + (uint32_t)(((8 * h + c) ^ (r & 31)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(ov[4 * c]), "r"(ov[4 * c + 1]),
+                       "r"(ov[4 * c + 2]), "r"(ov[4 * c + 3])
+                       : "memory");
+        }
+      }
+    }
+    ws_ml[(tile_id * S + s) * kTcRows + r] = make_float2(have ? m_used : -INFINITY, have ? l : 0.f);
+  }
+  static_assert(2 * kStages * kTileBytes >= kTcRows * kTcDim * 4, "staging buffer");
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -544,72 +593,76 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncwarp();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
-  if (aborted && t == 0) flag_status(a.dev_status, ET_DEV_TIMEOUT);
-  if (a.S == 1) return;
-
-  // ---------------- merge the S splits of this tile across the cluster ----------------
-  // partial rows: [128][128] fp32 over the K and V stages; (max, sum) pairs and
-  // merge weights in the Q tile's space (all MMAs are done)
-  static_assert(kOffV == kOffK + 32768 && 2 * kStages * kTileBytes >= kTcRows * kTcDim * 4, "merge buffer");
-  cluster_sync_all();  // every split's partial rows are in its shared memory
-  {
-    const int S = a.S;
-    const int per = (kTcRows + S - 1) / S;
-    const int r0 = s * per, r1 = min(kTcRows, r0 + per);
-    float *wts = reinterpret_cast<float *>(sm + kOffQ + 2048);  // [per][kTcMaxSplits] weights / total
-    if (t < r1 - r0 && !aborted) {
-      const int rr = r0 + t;
-      float2 ml[kTcMaxSplits];
-#pragma unroll
-      for (int x = 0; x < kTcMaxSplits; ++x)  // all loads first: distributed shared memory latency overlaps
-        ml[x] = x < S ? ld_cluster_f2(cluster_map(sb + kOffQ + 8 * rr, (uint32_t)x)) : make_float2(-INFINITY, 0.f);
-      float M = -INFINITY;
-#pragma unroll
-      for (int x = 0; x < kTcMaxSplits; ++x) M = fmaxf(M, ml[x].x);
-      float Ls = 0.f, w[kTcMaxSplits];
-#pragma unroll
-      for (int x = 0; x < kTcMaxSplits; ++x) {
-        w[x] = ml[x].x > -INFINITY ? exp2f(ml[x].x - M) : 0.f;
-        Ls += ml[x].y * w[x];
-      }
-      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-#pragma unroll
-      for (int x = 0; x < kTcMaxSplits; ++x) wts[t * kTcMaxSplits + x] = w[x] * inv;
-      const int i = row_tok[rr];
-      if (i >= 0 && a.lse)
-        a.lse[((long long)b * a.Hq + row_head[rr]) * N + i] =
-            Ls > 0.f ? (M + log2f(Ls)) * 0.69314718055994531f : -INFINITY;
-    }
-    __syncthreads();
-    __nv_bfloat16 *O = static_cast<__nv_bfloat16 *>(a.out);
-    for (int x = t; x < (r1 - r0) * 32 && !aborted; x += kThreads) {
-      const int lr = x >> 5, chunk = x & 31, rr = r0 + lr;
-      const int i = row_tok[rr];
-      if (i < 0) continue;
-      const uint32_t off = sb + kOffK + (uint32_t)rr * 512u + (uint32_t)((chunk ^ (rr & 31)) << 4);
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int g4 = 0; g4 < kTcMaxSplits; g4 += 4) {  // four loads in flight at a time
-        float4 p[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          p[q] = g4 + q < S ? ld_cluster_f4(cluster_map(off, (uint32_t)(g4 + q))) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float wv = g4 + q < S ? wts[lr * kTcMaxSplits + g4 + q] : 0.f;
-          acc.x = fmaf(wv, p[q].x, acc.x);
-          acc.y = fmaf(wv, p[q].y, acc.y);
-          acc.z = fmaf(wv, p[q].z, acc.z);
-          acc.w = fmaf(wv, p[q].w, acc.w);
-        }
-      }
-      uint2 v;
-      v.x = pack_bf16x2(acc.x, acc.y);
-      v.y = pack_bf16x2(acc.z, acc.w);
-      *reinterpret_cast<uint2 *>(O + (((long long)b * N + i) * a.Hq + row_head[rr]) * kTcDim + 4 * chunk) = v;
+  if (have) {
+    float4 *dst = reinterpret_cast<float4 *>(ws_o + (tile_id * S + s) * (kTcRows * kTcDim));
+    for (int x = t; x < nvalid * 32; x += kThreads) {
+      const int rr = x >> 5, chunk = x & 31;
+      dst[x] = *reinterpret_cast<const float4 *>(sm + kOffK + rr * 512 + ((chunk ^ (rr & 31)) << 4));
     }
   }
-  cluster_sync_all();  // peers may still read this block's shared memory until here
+  cluster_sync_all();  // release / acquire at cluster scope: every split's rows are in L2
+  if (aborted) {
+    if (t == 0) flag_status(a.dev_status, ET_DEV_TIMEOUT);
+    return;
+  }
+  const int per = (kTcRows + S - 1) / S;
+  const int r0 = s * per, r1 = min(nvalid, r0 + per);
+  if (r1 <= r0) return;
+  float *wts = reinterpret_cast<float *>(sm + kOffQ);  // [per][kTcMaxSplits] weight / total
+  if (t < r1 - r0) {
+    float2 ml[kTcMaxSplits];
+#pragma unroll
+    for (int x = 0; x < kTcMaxSplits; ++x)
+      ml[x] = x < S ? __ldcg(ws_ml + (tile_id * S + x) * kTcRows + r0 + t) : make_float2(-INFINITY, 0.f);
+    float M = -INFINITY;
+#pragma unroll
+    for (int x = 0; x < kTcMaxSplits; ++x) M = fmaxf(M, ml[x].x);
+    float Ls = 0.f, w[kTcMaxSplits];
+#pragma unroll
+    for (int x = 0; x < kTcMaxSplits; ++x) {
+      w[x] = ml[x].x > -INFINITY ? exp2f(ml[x].x - M) : 0.f;
+      Ls += ml[x].y * w[x];
+    }
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+#pragma unroll
+    for (int x = 0; x < kTcMaxSplits; ++x) wts[t * kTcMaxSplits + x] = w[x] * inv;
+    const int i = row_tok[r0 + t];
+    if (i >= 0 && a.lse)
+      a.lse[((long long)b * a.Hq + row_head[r0 + t]) * N + i] =
+          Ls > 0.f ? (M + log2f(Ls)) * 0.69314718055994531f : -INFINITY;
+  }
+  __syncthreads();
+  __nv_bfloat16 *O = static_cast<__nv_bfloat16 *>(a.out);
+  const float4 *src = reinterpret_cast<const float4 *>(ws_o + tile_id * S * (kTcRows * kTcDim));
+  for (int x = t; x < (r1 - r0) * 32; x += kThreads) {
+    const int lr = x >> 5, chunk = x & 31, rr = r0 + lr;
+    float4 p[kTcMaxSplits];
+#pragma unroll
+    for (int sp = 0; sp < kTcMaxSplits; ++sp) {  // every load in flight before the sums
+      p[sp] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (sp < S && wts[lr * kTcMaxSplits + sp] != 0.f) p[sp] = __ldcg(src + (sp * kTcRows + rr) * 32 + chunk);
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int sp = 0; sp < kTcMaxSplits; ++sp) {
+      const float w = sp < S ? wts[lr * kTcMaxSplits + sp] : 0.f;
+      if (w != 0.f) {  // a split without keys for this row wrote no partial row
+        acc.x = fmaf(w, p[sp].x, acc.x);
+        acc.y = fmaf(w, p[sp].y, acc.y);
+        acc.z = fmaf(w, p[sp].z, acc.z);
+        acc.w = fmaf(w, p[sp].w, acc.w);
+      }
+    }
+    uint2 v;
+    v.x = pack_bf16x2(acc.x, acc.y);
+    v.y = pack_bf16x2(acc.z, acc.w);
+    *reinterpret_cast<uint2 *>(O + (((long long)b * N + row_tok[rr]) * a.Hq + row_head[rr]) * kTcDim + 4 * chunk) = v;
+  }
+  __syncthreads();  // every read of this block's rows has returned
+  for (int x = t; x < (r1 - r0) * S * 4; x += kThreads) {
+    const int line = x & 3, lr = (x >> 2) % (r1 - r0), sp = (x >> 2) / (r1 - r0);
+    discard_l2_line(src + (sp * kTcRows + r0 + lr) * 32 + line * 8);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -654,6 +707,19 @@ bool make_map_tree(CUtensorMap *m, const void *base, int Hkv, long long rows) {
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Q [B*N tokens][Hkv][G][d]: box = 128/G tokens x G heads of one KV head,
+// rows ordered (token, head in group) like the tile
+bool make_map_q(CUtensorMap *m, const void *base, int G, int Hkv, long long tokens) {
+  const cuuint64_t dims[4] = {(cuuint64_t)kTcDim, (cuuint64_t)G, (cuuint64_t)Hkv, (cuuint64_t)tokens};
+  const cuuint64_t strides[3] = {(cuuint64_t)kTcDim * 2, (cuuint64_t)G * kTcDim * 2,
+                                 (cuuint64_t)Hkv * G * kTcDim * 2};
+  const cuuint32_t box[4] = {64, (cuuint32_t)G, 1, (cuuint32_t)(kTcRows / G)};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t set_smem_attr() {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
@@ -669,7 +735,8 @@ et_status tc_attention_launch(const TcLaunch &a, cudaStream_t stream) {
   if (!encode_fn()) return ET_ERR_CUDA;
   if (a.S < 1 || a.S > kTcMaxSplits) return ET_ERR_UNSUPPORTED;
   if (a.kv_rows >= (1ll << 31) || (long long)a.B * a.N >= (1ll << 31)) return ET_ERR_UNSUPPORTED;
-  CUtensorMap m_kp, m_vp, m_kt, m_vt;
+  if (a.S > 1 && !a.ws) return ET_ERR_WORKSPACE;
+  CUtensorMap m_kp, m_vp, m_kt, m_vt, m_q;
   const long long tree_rows = (long long)a.B * a.N;
   bool ok = make_map_tree(&m_kt, a.kt, a.Hkv, tree_rows) && make_map_tree(&m_vt, a.vt, a.Hkv, tree_rows);
   if (a.kp && a.vp && a.kv_rows > 0) {
@@ -677,6 +744,10 @@ et_status tc_attention_launch(const TcLaunch &a, cudaStream_t stream) {
   } else {  // no prefix anywhere: a valid map the kernel never uses
     ok = ok && make_map_2d(&m_kp, a.kt, tree_rows * a.Hkv) && make_map_2d(&m_vp, a.vt, tree_rows * a.Hkv);
   }
+  TcLaunch la = a;
+  la.q_tma = (a.G <= kTcRows && kTcRows % a.G == 0) ? 1 : 0;
+  if (la.q_tma) ok = ok && make_map_q(&m_q, a.q, a.G, a.Hkv, tree_rows);
+  else m_q = m_kt;  // not read
   if (!ok) return ET_ERR_INVALID_ARG;
   if (set_smem_attr() != cudaSuccess) return ET_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
@@ -691,7 +762,7 @@ et_status tc_attention_launch(const TcLaunch &a, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.S > 1 ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, k_attn_tc, m_kp, m_vp, m_kt, m_vt, a) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, k_attn_tc, m_kp, m_vp, m_kt, m_vt, m_q, la) != cudaSuccess) {
     cudaGetLastError();
     return ET_ERR_CUDA;
   }

@@ -22,12 +22,20 @@ struct TcLaunch {
   void *out;
   float *lse;
   int *dev_status;
+  float *ws;   // S > 1: partial rows [B*Hkv*MT][S][128][128], then (max, sum) [B*Hkv*MT][S][128]
+  int q_tma;   // set by the launcher: the Q tile comes by TMA (G divides 128)
 };
 
 constexpr int kTcRows = 128;   // query rows per tile (TMEM lanes)
 constexpr int kTcKeys = 64;    // keys per K/V tile
 constexpr int kTcDim = 128;    // head dim of the tcgen05 path
 constexpr int kTcMaxSplits = 8;  // KV splits of one row tile = one thread-block cluster (portable size)
+
+// workspace bytes of the tcgen05 path: the split merge's partial rows and
+// (max, sum) pairs (0 for one split)
+inline size_t tc_workspace_bytes(long long tiles, int S) {
+  return S > 1 ? (size_t)tiles * S * kTcRows * (kTcDim * 4 + 8) : 0;
+}
 
 ET_HIDDEN et_status tc_attention_launch(const TcLaunch &a, cudaStream_t stream);
 

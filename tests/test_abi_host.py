@@ -107,8 +107,13 @@ def test_attention_argument_checks(lib):
     assert sz > 0
     assert call(shape(num_splits=4, impl=1), wsb=sz - 1) == E.ET_ERR_WORKSPACE
     assert lib.et_tree_attention_splits(ctypes.byref(shape(num_splits=4))) == 4
-    # the tcgen05 path merges its splits on chip: no workspace, at most 8 splits
-    assert lib.et_tree_attention_workspace_size(ctypes.byref(shape(num_splits=4, impl=2))) == 0
+    # the tcgen05 path: the splits of a tile form one cluster (at most 8) and
+    # merge through the workspace: per split and 128-row tile, fp32 rows and a (max, sum) pair per row
+    tc4 = lib.et_tree_attention_workspace_size(ctypes.byref(shape(num_splits=4, impl=2)))
+    assert tc4 == 32 * 1 * 4 * 128 * (128 * 4 + 8)
+    assert call(shape(num_splits=4, impl=2), ws=None) == E.ET_ERR_WORKSPACE
+    assert call(shape(num_splits=4, impl=2), wsb=tc4 - 1) == E.ET_ERR_WORKSPACE
+    assert lib.et_tree_attention_workspace_size(ctypes.byref(shape(num_splits=1, impl=2))) == 0
     assert lib.et_tree_attention_splits(ctypes.byref(shape(num_splits=20, impl=2))) == 8
     assert lib.et_tree_attention_workspace_size(ctypes.byref(shape(num_splits=1))) == 0
     assert lib.et_tree_attention_splits(ctypes.byref(shape(dtype=E.ET_F32))) == 1
