@@ -235,6 +235,133 @@ __device__ __forceinline__ int cl_ld_s32(uint32_t addr) {
 __device__ __forceinline__ void cl_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// split cluster barrier: arrive (release, or relaxed when it only has to
+// show that every block of the cluster has started) ... wait (acquire)
+__device__ __forceinline__ void cl_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cl_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cl_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cl_st_u64(uint32_t addr, unsigned long long v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+__device__ __forceinline__ void cl_st_f32x2(uint32_t addr, float a, float b) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+
+// ---- (value desc, id asc) as one ascending 64-bit key ----
+// high word: the order-reversed image of z (larger z -> smaller word; -0 and
+// +0 are one value), low word: the id.  Sanitised logits only (no NaN).
+__device__ __forceinline__ unsigned long long zid_key(float z, unsigned int id) {
+  if (z == 0.f) z = 0.f;  // -0 -> +0
+  const unsigned int u = __float_as_uint(z);
+  const unsigned int ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // ascending with z
+  return ((unsigned long long)(~ord) << 32) | id;
+}
+__device__ __forceinline__ float zid_value(unsigned long long key) {
+  const unsigned int ord = ~(unsigned int)(key >> 32);
+  return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7fffffffu) : ~ord);
+}
+__device__ __forceinline__ unsigned int zid_id(unsigned long long key) { return (unsigned int)key; }
+
+// (max, sum of exp(x - max)) pairs: merge two
+__device__ __forceinline__ void ms_merge(float &m, float &s, float m2, float s2) {
+  const float M = fmaxf(m, m2);
+  if (M == -INFINITY) { m = M; s = 0.f; return; }
+  s = (m > -INFINITY ? s * exp_fast(m - M) : 0.f) + (m2 > -INFINITY ? s2 * exp_fast(m2 - M) : 0.f);
+  m = M;
+}
+
+// Exact k smallest keys (k <= 32) of the NV keys each lane of a warp holds,
+// ascending, into out[0..k) (shared memory).  Keys must be distinct.  The
+// k-th smallest of the 32 lane minima bounds the answer from above (k lanes
+// hold a key at or below it), so only keys at or below that bound compete;
+// they are ranked by counting in `cand` (cap keys).  When more than cap keys
+// compete (heavy ties), k rounds of warp argmin decide instead.
+template <int NV>
+__device__ __forceinline__ void warp_topk_keys(const unsigned long long (&key)[NV], int k, unsigned long long *cand,
+                                               int cap, unsigned long long *out) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long best = ~0ull;
+#pragma unroll
+  for (int e = 0; e < NV; ++e) best = key[e] < best ? key[e] : best;
+  int rank = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) rank += __shfl_sync(0xffffffffu, best, j) < best ? 1 : 0;
+  const unsigned int hit = __ballot_sync(0xffffffffu, rank == k - 1);
+  const unsigned long long tau = __shfl_sync(0xffffffffu, best, __ffs(hit) - 1);
+  int c = 0;
+#pragma unroll
+  for (int e = 0; e < NV; ++e) c += key[e] <= tau ? 1 : 0;
+  int incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const int nc = __shfl_sync(0xffffffffu, incl, 31);
+  if (nc <= cap) {
+    int pos = incl - c;
+#pragma unroll
+    for (int e = 0; e < NV; ++e)
+      if (key[e] <= tau) cand[pos++] = key[e];
+    __syncwarp();
+    for (int i = lane; i < nc; i += 32) {
+      const unsigned long long mine = cand[i];
+      int r = 0;
+      for (int j0 = 0; j0 < nc; j0 += 8) {  // eight independent loads per round
+#pragma unroll
+        for (int j = j0; j < j0 + 8; ++j) r += (j < nc && cand[j] < mine) ? 1 : 0;
+      }
+      if (r < k) out[r] = mine;
+    }
+  } else {
+    unsigned int used = 0u;
+    for (int r = 0; r < k; ++r) {
+      unsigned long long m = best;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long w = __shfl_xor_sync(0xffffffffu, m, o);
+        m = w < m ? w : m;
+      }
+      if (lane == 0) out[r] = m;
+      if (best == m) {
+        best = ~0ull;
+#pragma unroll
+        for (int e = 0; e < NV; ++e) {
+          if (key[e] == m) used |= 1u << e;
+          if (!((used >> e) & 1u) && key[e] < best) best = key[e];
+        }
+      }
+    }
+  }
+  __syncwarp();
+}
+
+// The n smallest of P distinct keys in shared memory, by rank: emit(r, key)
+// runs once for each key of rank r < n.  Every thread of the block (NT
+// threads) calls it.  Ranks are counted pairwise: G lanes share a key, each
+// scanning every G-th key with eight independent loads per round, then a
+// shuffle sum; G is the largest power of two (<= 32) with G * P <= NT.
+template <int NT, typename Emit>
+__device__ __forceinline__ void block_select(const unsigned long long *keys, int P, int n, Emit emit) {
+  int G = 1;
+  while (G < 32 && 2 * G * P <= NT) G *= 2;
+  const int t = threadIdx.x;
+  for (int base = 0; base < P * G; base += NT) {  // same trip count in every thread
+    const int idx = base + t, i = idx / G, g = idx & (G - 1);
+    const unsigned long long mine = i < P ? keys[i] : 0ull;
+    int cnt = 0;
+    if (i < P) {
+      int j = g;
+      for (; j + 7 * G < P; j += 8 * G) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) cnt += keys[j + u * G] < mine ? 1 : 0;
+      }
+      for (; j < P; j += G) cnt += keys[j] < mine ? 1 : 0;
+    }
+    for (int o = G >> 1; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if (i < P && g == 0 && cnt < n) emit(cnt, mine);
+  }
+}
 
 }  // namespace et
 

@@ -419,11 +419,6 @@ __global__ void __launch_bounds__(kMaxN) k_mask_posids(int N, const int32_t *fla
   if (bad) flag_status(dev_status, ET_DEV_BAD_INDEX);
 }
 
-// shared by the clustered expansion: exact top-k via a distance histogram
-constexpr int kHistBins = 64;      // 1/8-nat bins of "distance below the max"
-constexpr float kHistPerNat = 8.f;
-constexpr int kCandCap = 1024;     // candidates ranked by counting
-
 struct ExpandRowArgs {
   const float *logits;
   long long row_stride;
@@ -437,129 +432,45 @@ struct ExpandRowArgs {
 
 // ---------------------------------------------------------------------------
 // expand, one thread-block cluster per expanded row (V <= 32768): CTA q of the
-// cluster owns logits [4096 q, 4096 q + 4096) (4 float4 per thread), computes
-// its local max / sum of exp and its exact local top-k; the leader (rank 0)
-// gathers the partial results through distributed shared memory, merges
-// them by rank counting and writes the children; the last leader of a
-// sequence then picks the next frontier.  Spreading a row over up to 8 SMs
-// gives the load 8x the memory parallelism of one block per row.
+// cluster owns logits [4096 q, 4096 q + 4096) (16 per thread).  Each warp
+// finds the exact top-k of its 512 logits; after one block barrier the block
+// selects its top-k from the 8 warp lists (pairwise rank counting over all
+// threads), sums exp(z - block max) and stores both straight into the
+// leader's (rank 0) shared memory; after one cluster barrier the leader
+// selects the row's top-k from the R block lists and writes the children.
+// The last leader of a sequence then picks the next frontier among the
+// first m children of every row.  Spreading a row over up to 8 SMs gives the
+// load 8x the memory parallelism of one block per row.
 // ---------------------------------------------------------------------------
 constexpr int kClThreads = 256;
+constexpr int kClWarps = kClThreads / 32;
 constexpr int kClVec = 4;
 constexpr int kClSpan = kClThreads * 4 * kClVec;   // 4096 logits per CTA
 constexpr int kClMaxCtas = 8;
 constexpr int kClMaxV = kClSpan * kClMaxCtas;      // 32768
+constexpr int kWarpCand = 64;                      // keys a warp ranks by counting
 
-struct TopkSmem {
-  float redz[32];
-  int redi[32];
-  unsigned int hist[kHistBins];
-  float cz[kCandCap];
-  int ci[kCandCap];
-  float topz[kMaxTopk];
-  int topi[kMaxTopk];
-  int ncand, sbin;
+struct ExpandClSmem {
+  unsigned long long cand[kClWarps][kWarpCand];
+  unsigned long long wl[kClWarps * kMaxTopk];    // warp w's sorted top-k at w * k
+  unsigned long long gl[kClMaxCtas * kMaxTopk];  // leader: CTA q's top-k at q * k
+  float2 gms[kClMaxCtas];                         // leader: (max, sum) of each CTA
+  unsigned long long fl[kMaxM * kMaxTopk];       // last leader: frontier candidates
+  float wsum[kClWarps];
+  int sel[kMaxM];
+  int last;
 };
 
-// Exact top-k by (z desc, id asc) of the NV values each thread holds; id_of(e)
-// is the token id of value e (INT_MAX for padding).  A histogram of each
-// value's distance below the block max (1/8-nat bins) bounds the candidates
-// to the first bins holding >= k values, which are then ranked by counting;
-// otherwise (heavy ties, all -inf) k rounds of block argmax.  Result in
-// ts.topz / ts.topi[0..k), padded with (-inf, INT_MAX).
-template <int NT, int NV, typename IdFn>
-__device__ void block_topk(float (&v)[NV], IdFn id_of, float M, int k, TopkSmem &ts) {
-  const int t = threadIdx.x, lane = t & 31;
-  if (t < kHistBins) ts.hist[t] = 0u;
-  if (t == 0) { ts.ncand = 0; ts.sbin = -1; }
-  __syncthreads();
-  if (M > -INFINITY) {
-#pragma unroll
-    for (int e = 0; e < NV; ++e) {
-      const float d = M - v[e];
-      if (d < (float)kHistBins / kHistPerNat) atomicAdd(&ts.hist[(int)(d * kHistPerNat)], 1u);
-    }
-  }
-  __syncthreads();
-  if (t < 32) {
-    const unsigned int c0 = ts.hist[2 * lane], c1 = ts.hist[2 * lane + 1];
-    unsigned int incl = c0 + c1;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const unsigned int excl = incl - c0 - c1;
-    if (excl < (unsigned)k && incl >= (unsigned)k) ts.sbin = (excl + c0 >= (unsigned)k) ? 2 * lane : 2 * lane + 1;
-  }
-  __syncthreads();
-  bool fast = ts.sbin >= 0;
-  if (fast) {
-    const float dlim = (float)(ts.sbin + 1) / kHistPerNat;  // exact: bins count floor(d * 8) <= sbin
-#pragma unroll
-    for (int e = 0; e < NV; ++e) {
-      if (M - v[e] < dlim) {
-        const int pos = atomicAdd(&ts.ncand, 1);
-        if (pos < kCandCap) { ts.cz[pos] = v[e]; ts.ci[pos] = id_of(e); }
-      }
-    }
-    __syncthreads();
-    fast = ts.ncand <= kCandCap;
-  }
-  if (fast) {
-    const int nc = ts.ncand;
-    for (int i = t; i < nc; i += NT) {
-      const float z = ts.cz[i];
-      const int id = ts.ci[i];
-      int rank = 0;
-      for (int j = 0; j < nc; ++j) rank += ranks_before(ts.cz[j], ts.ci[j], z, id) ? 1 : 0;
-      if (rank < k) { ts.topz[rank] = z; ts.topi[rank] = id; }
-    }
-  } else {
-    unsigned int consumed = 0u;
-    float bz = -INFINITY;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int e = 0; e < NV; ++e)
-      if (ranks_before(v[e], id_of(e), bz, bi)) { bz = v[e]; bi = id_of(e); }
-    for (int r = 0; r < k; ++r) {
-      float z = bz;
-      int id = bi;
-      block_best<NT>(z, id, ts.redz, ts.redi);
-      if (t == 0) { ts.topz[r] = z; ts.topi[r] = id; }
-      if (id == bi && id != 0x7fffffff) {
-#pragma unroll
-        for (int e = 0; e < NV; ++e)
-          if (id_of(e) == id) consumed |= 1u << e;
-        bz = -INFINITY;
-        bi = 0x7fffffff;
-#pragma unroll
-        for (int e = 0; e < NV; ++e)
-          if (!((consumed >> e) & 1u) && ranks_before(v[e], id_of(e), bz, bi)) { bz = v[e]; bi = id_of(e); }
-      }
-    }
-  }
-  __syncthreads();
-}
-
 __global__ void __launch_bounds__(kClThreads) k_expand_cl(ExpandRowArgs a) {
-  __shared__ TopkSmem ts;
-  __shared__ float part_ms[2];
-  __shared__ float pm[kClMaxCtas], ps[kClMaxCtas];
-  __shared__ float gz[kClMaxCtas * kMaxTopk];
-  __shared__ int gi[kClMaxCtas * kMaxTopk];
-  __shared__ float topz[kMaxTopk];
-  __shared__ int topi[kMaxTopk];
-  __shared__ unsigned long long fkey[1024];
-  __shared__ int sel[kMaxM];
-  __shared__ int sflag;
-
-  const int t = threadIdx.x;
+  __shared__ ExpandClSmem sh;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int R = gridDim.x;                 // CTAs per row = cluster size
   const int q = (int)cl_rank();
   const int row = blockIdx.y;
   const int b = row / a.m_l, s = row - b * a.m_l;
   const int k = a.k;
+  cl_arrive_relaxed();  // phase 0: this block has started (waited on before any remote store)
+
   int flag = 0, bad = 0;
   int node = -1;
   if (a.layer > 0) {
@@ -573,10 +484,6 @@ __global__ void __launch_bounds__(kClThreads) k_expand_cl(ExpandRowArgs a) {
     else zrow = a.logits + r * a.row_stride;
   }
   const int base = q * kClSpan;
-  auto id_of = [&](int e) -> int {
-    const int id = base + (e >> 2) * (kClThreads * 4) + t * 4 + (e & 3);
-    return id < a.V ? id : 0x7fffffff;
-  };
   float v[4 * kClVec];
 #pragma unroll
   for (int u = 0; u < kClVec; ++u) {
@@ -588,83 +495,101 @@ __global__ void __launch_bounds__(kClThreads) k_expand_cl(ExpandRowArgs a) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) v[4 * u + j] = (zrow && e0 + j < a.V) ? __ldcs(zrow + e0 + j) : -INFINITY;
     }
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (e0 + j < a.V) v[4 * u + j] = sanitize_logit(v[4 * u + j], flag);
   }
-  float lm = -INFINITY;
+  // the parent's path key, fetched while the logits are in flight
+  const long long pkey = (q == 0 && node >= 0 && !bad) ? ld_cg(a.tree.cand_key + (long long)b * a.C + node) : 0ll;
+  unsigned long long key[4 * kClVec];
 #pragma unroll
-  for (int e = 0; e < 4 * kClVec; ++e) lm = fmaxf(lm, v[e]);
-  const float Mq = block_max<kClThreads>(lm, ts.redz);
-  float ls = 0.f;
-  if (Mq > -INFINITY) {
+  for (int u = 0; u < kClVec; ++u) {
 #pragma unroll
-    for (int e = 0; e < 4 * kClVec; ++e) ls += exp_fast(v[e] - Mq);
+    for (int j = 0; j < 4; ++j) {
+      const int e = 4 * u + j, id = base + u * kClThreads * 4 + t * 4 + j;  // ids >= V are padding
+      if (id < a.V) v[e] = sanitize_logit(v[e], flag);
+      key[e] = zid_key(v[e], (unsigned int)id);
+    }
   }
-  const float Sq = block_sum<kClThreads>(ls, ts.redz);
-  block_topk<kClThreads, 4 * kClVec>(v, id_of, Mq, k, ts);
-  if (t == 0) { part_ms[0] = Mq; part_ms[1] = Sq; }
+  warp_topk_keys<4 * kClVec>(key, k, sh.cand[warp], kWarpCand, sh.wl + warp * k);
   if (flag) flag_status(a.dev_status, ET_DEV_NONFINITE);
   if (bad && q == 0 && t == 0) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
-  cl_sync();  // every CTA's partial result is in its shared memory
-  if (q == 0) {
-    if (t < R) {
-      pm[t] = cl_ld_f32(cl_map(&part_ms[0], t));
-      ps[t] = cl_ld_f32(cl_map(&part_ms[1], t));
-    }
-    for (int i = t; i < R * k; i += kClThreads) {
-      const int peer = i / k, e = i - peer * k;
-      gz[i] = cl_ld_f32(cl_map(&ts.topz[e], peer));
-      gi[i] = cl_ld_s32(cl_map(&ts.topi[e], peer));
-    }
-  }
-  cl_sync();  // the leader has everything; the others may leave
-  if (q != 0) return;
-  float M = -INFINITY;
-  for (int x = 0; x < R; ++x) M = fmaxf(M, pm[x]);
-  float S = 0.f;
-  for (int x = 0; x < R; ++x) S += pm[x] > -INFINITY ? ps[x] * expf(pm[x] - M) : 0.f;
-  for (int i = t; i < R * k; i += kClThreads) {
-    const float z = gz[i];
-    const int id = gi[i];
-    int rank = 0;
-    for (int j = 0; j < R * k; ++j) rank += ranks_before(gz[j], gi[j], z, id) ? 1 : 0;
-    if (rank < k) { topz[rank] = z; topi[rank] = id; }
-  }
   __syncthreads();
-  if (t < k) {
-    const float logS = (M > -INFINITY) ? logf(S) : 0.f;
-    const float z = topz[t];
+
+  // ---- the block's max (head of the warp lists) and sum of exp ----
+  unsigned long long head = sh.wl[0];
+#pragma unroll
+  for (int w = 1; w < kClWarps; ++w) head = sh.wl[w * k] < head ? sh.wl[w * k] : head;
+  const float Mq = zid_value(head);
+  float sum = 0.f;
+  if (Mq > -INFINITY) {
+#pragma unroll
+    for (int e = 0; e < 4 * kClVec; ++e) sum += exp_fast(v[e] - Mq);
+  }
+  sum = warp_sum(sum);
+  if (lane == 0) sh.wsum[warp] = sum;  // summed in warp order below: deterministic
+
+  // ---- the block's top-k -> the leader's shared memory ----
+  cl_wait();  // phase 0 done: every block of the cluster runs
+  const uint32_t gl_remote = cl_map(&sh.gl[q * k], 0);
+  block_select<kClThreads>(sh.wl, kClWarps * k, k,
+                           [&](int r, unsigned long long key_r) { cl_st_u64(gl_remote + 8u * (uint32_t)r, key_r); });
+  __syncthreads();  // every warp's sum is in
+  if (t == 0) {
+    float cs = 0.f;
+#pragma unroll
+    for (int w = 0; w < kClWarps; ++w) cs += sh.wsum[w];
+    cl_st_f32x2(cl_map(&sh.gms[q], 0), Mq, cs);
+  }
+  cl_arrive();  // phase 1: release this block's stores
+  if (q != 0) return;
+  cl_wait();
+
+  // ---- leader: the row's top-k from the R block lists; write the children ----
+  float M = -INFINITY, S = 0.f;
+  {
+    float2 gq[kClMaxCtas];
+#pragma unroll
+    for (int x = 0; x < kClMaxCtas; ++x) {
+      gq[x] = x < R ? sh.gms[x] : make_float2(-INFINITY, 0.f);
+      M = fmaxf(M, gq[x].x);
+    }
+#pragma unroll
+    for (int x = 0; x < kClMaxCtas; ++x) S += gq[x].x > -INFINITY ? gq[x].y * expf(gq[x].x - M) : 0.f;
+  }
+  const float logS = (M > -INFINITY) ? logf(S) : 0.f;
+  block_select<kClThreads>(sh.gl, R * k, k, [&](int r, unsigned long long key_r) {
+    const float z = zid_value(key_r);
+    const int id = (int)zid_id(key_r);
     const float lp = (M > -INFINITY && z > -INFINITY) ? (z - M) - logS : -INFINITY;
-    const long long pkey = node < 0 ? 0ll : a.tree.cand_key[(long long)b * a.C + node];
-    const long long o = (long long)b * a.C + a.base_next + s * k + t;
-    const int tok = topi[t];
-    a.tree.cand_tok[o] = (tok == 0x7fffffff) ? -1 : tok;
+    const long long o = (long long)b * a.C + a.base_next + s * k + r;
+    a.tree.cand_tok[o] = id < a.V ? id : -1;
     a.tree.cand_parent[o] = node;
     a.tree.cand_lp[o] = lp;
     a.tree.cand_key[o] = add_keys(pkey, fixed_key(lp));
-  }
-  // ---- the last row of this sequence picks the next frontier (rank counting) ----
-  if (!arrive_last(&a.seq_cnt[b], (unsigned)a.m_l, &sflag)) return;
-  if (a.m_next <= 0) return;
-  const int width = a.m_l * k;  // <= 1024
-  for (int i = t; i < width; i += kClThreads) {
-    const int id = a.base_next + i;
-    fkey[i] = rank_key(ld_cg(a.tree.cand_key + (long long)b * a.C + id), id);
+  });
+  if (a.m_next <= 0) return;  // last layer: no frontier to pick
+
+  // ---- the last row of this sequence picks the next frontier ----
+  if (!arrive_last(&a.seq_cnt[b], (unsigned)a.m_l, &sh.last)) return;
+  // A child at position e of its row has e better siblings, so only the
+  // first m_next of every row can rank below m_next, and among them ranks
+  // below m_next are exact.
+  const int nk = k < a.m_next ? k : a.m_next;
+  const int P = a.m_l * nk;  // <= 1024
+  for (int c = t; c < P; c += kClThreads) {
+    const int rs = c / nk, e = c - rs * nk;
+    const int id = a.base_next + rs * k + e;
+    sh.fl[c] = rank_key(ld_cg(a.tree.cand_key + (long long)b * a.C + id), id);
   }
   __syncthreads();
-  for (int i = t; i < width; i += kClThreads) {
-    const unsigned long long my = fkey[i];
-    int rank = 0;
-    for (int j = 0; j < width; ++j) rank += fkey[j] < my ? 1 : 0;
-    if (rank < a.m_next) sel[rank] = a.base_next + i;
-  }
+  block_select<kClThreads>(sh.fl, P, a.m_next, [&](int r, unsigned long long key_r) {
+    sh.sel[r] = (int)(key_r & ((1ull << kIdBits) - 1));
+  });
   __syncthreads();
   if (t < a.m) {
     if (t < a.m_next) {
       int slot = 0;
-      for (int j = 0; j < a.m_next; ++j) slot += sel[j] < sel[t] ? 1 : 0;
-      a.tree.frontier[b * a.m + slot] = sel[t];
+      const int mine = sh.sel[t];
+      for (int j = 0; j < a.m_next; ++j) slot += sh.sel[j] < mine ? 1 : 0;
+      a.tree.frontier[b * a.m + slot] = mine;
     } else {
       a.tree.frontier[b * a.m + t] = -1;
     }

@@ -115,6 +115,25 @@ def test_expand_all_neg_inf_row():
     assert (g["cand_key"][0] == O.KEY_MIN).all()
 
 
+@pytest.mark.parametrize("k", [10, 32])
+def test_expand_constant_row_takes_lowest_ids(k):
+    # every logit equal: the top-k by (value desc, id asc) are ids 0..k-1, each
+    # with log-prob -ln V (k = 32 makes every warp rank more tied keys than it
+    # counts directly, so the exact argmin rounds decide)
+    V = 32000
+    cfg = E.TreeCfg(B=2, V=V, depth=2, topk=k, m=k, n=k + 1)
+    tb = E.TreeBuffers.allocate(cfg)
+    ws = E.new_workspace(E.et_tree_workspace_size(cfg))
+    z = np.full((2, V), 1.25, np.float32)
+    z[1] = -3.5
+    E.et_tree_expand(cfg, 0, torch.from_numpy(z).cuda(), tb, ws)
+    g = gpu_tree_np(tb)
+    for b in range(2):
+        assert list(g["cand_tok"][b][:k]) == list(range(k))
+        np.testing.assert_allclose(g["cand_lp"][b][:k], -np.log(V), rtol=1e-5)
+        assert list(g["frontier"][b][:k]) == list(range(k))
+
+
 # ---------------------------------------------------------------------------
 # rerank + mask/posids, given the oracle's keys
 # ---------------------------------------------------------------------------
