@@ -43,6 +43,8 @@ struct AttnArgs {
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(128) k_attn_f32(AttnArgs a) {
+  pdl_wait();     // the previous kernel in the stream has completed
+  pdl_trigger();  // only now may the next kernel launch: at most one waits ahead
   constexpr int PL = D / 32;  // dims per lane
   __shared__ float qs[D];
   __shared__ float wm[4], wl[4];
@@ -166,6 +168,8 @@ __device__ __forceinline__ void split_range(int L, int N, int S, int s, int &t0,
 
 template <int D>
 __global__ void __launch_bounds__(kMmaThreads, 2) k_attn_mma(AttnArgs a) {
+  pdl_wait();     // the previous kernel in the stream has completed
+  pdl_trigger();  // only now may the next kernel launch: at most one waits ahead
   constexpr int CH = D / 8;  // 16-byte chunks per row
   extern __shared__ __align__(128) unsigned char sm[];
   unsigned char *qs = sm;                            // [64][D]
@@ -583,9 +587,8 @@ extern "C" et_status et_tree_attention(const et_attn_shape *shape, const void *q
   a.out = out; a.lse = lse; a.dev_status = dev_status;
   if (plan.impl == 0) {
     dim3 grid(shape->N, shape->Hq, shape->B);
-    if (shape->d == 64) k_attn_f32<64><<<grid, 128, 0, st>>>(a);
-    else k_attn_f32<128><<<grid, 128, 0, st>>>(a);
-    return et_launch_status();
+    if (shape->d == 64) return et_launch(k_attn_f32<64>, grid, dim3(128), 0, st, 0, a);
+    return et_launch(k_attn_f32<128>, grid, dim3(128), 0, st, 0, a);
   }
   if (a.S > 1) {
     a.cnt = reinterpret_cast<unsigned int *>(wsb + plan.cnt_off);
@@ -598,12 +601,11 @@ extern "C" et_status et_tree_attention(const et_attn_shape *shape, const void *q
     const int smem = kRows * 64 * 2 + 4 * kKeys * 64 * 2;
     static bool attr64 = false;
     if (!attr64) { cudaFuncSetAttribute(k_attn_mma<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); attr64 = true; }
-    k_attn_mma<64><<<grid, kMmaThreads, smem, st>>>(a);
+    return et_launch(k_attn_mma<64>, grid, dim3(kMmaThreads), smem, st, 0, a);
   } else {
     const int smem = kRows * 128 * 2 + 4 * kKeys * 128 * 2;
     static bool attr128 = false;
     if (!attr128) { cudaFuncSetAttribute(k_attn_mma<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); attr128 = true; }
-    k_attn_mma<128><<<grid, kMmaThreads, smem, st>>>(a);
+    return et_launch(k_attn_mma<128>, grid, dim3(kMmaThreads), smem, st, 0, a);
   }
-  return et_launch_status();
 }

@@ -232,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     k_attn_tc(const __grid_constant__ CUtensorMap tm_kp, const __grid_constant__ CUtensorMap tm_vp,
               const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt,
               const __grid_constant__ CUtensorMap tm_q, const TcLaunch a) {
+  pdl_wait();  // the previous kernel in the stream has completed (inputs may come from it)
   extern __shared__ unsigned char smem_raw[];
   __shared__ int row_tok[kTcRows], row_head[kTcRows];
   unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -309,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_trigger();  // only now: a waiting dependent block must not hold the TMEM this block needs
   if (t == 0 && L > 0 && row0 + (long long)g * S_b + L > a.kv_rows) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
 
   if (warp == 0 || warp == 2) {
@@ -750,23 +752,8 @@ et_status tc_attention_launch(const TcLaunch &a, cudaStream_t stream) {
   else m_q = m_kt;  // not read
   if (!ok) return ET_ERR_INVALID_ARG;
   if (set_smem_attr() != cudaSuccess) return ET_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.S, a.Hkv * a.MT, a.B);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = a.S;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = a.S > 1 ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, k_attn_tc, m_kp, m_vp, m_kt, m_vt, m_q, la) != cudaSuccess) {
-    cudaGetLastError();
-    return ET_ERR_CUDA;
-  }
-  return et_launch_status();
+  return et_launch(k_attn_tc, dim3(a.S, a.Hkv * a.MT, a.B), dim3(kThreads), kSmemBytes, stream, a.S > 1 ? a.S : 0,
+                   m_kp, m_vp, m_kt, m_vt, m_q, la);
 }
 
 }  // namespace et

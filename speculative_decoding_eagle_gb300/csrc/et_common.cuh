@@ -209,6 +209,18 @@ __device__ __forceinline__ float exp_fast(float x) {
   return y;
 }
 
+// ---- programmatic dependent launch ----
+// Every kernel of this library is launched with programmatic stream
+// serialization: it may start while the previous kernel in the stream is
+// still running.  pdl_wait() blocks until that kernel has completed and its
+// memory is visible, so it comes before the first global memory access;
+// pdl_trigger() lets the next kernel start launching (it still waits for
+// this one to complete before touching memory).  Triggering only after the
+// wait keeps at most one kernel waiting ahead: triggering first lets a whole
+// chain of launches pile up on the SMs.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- thread-block clusters: distributed shared memory ----
 __device__ __forceinline__ uint32_t cl_rank() {
   uint32_t r;
@@ -376,3 +388,34 @@ static inline et_status et_launch_status() {
   return e == cudaSuccess ? ET_OK : ET_ERR_CUDA;
 }
 static inline bool et_aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Launch with programmatic stream serialization (and, when cluster_x > 0,
+// clusters of cluster_x blocks along x).
+template <typename... KArgs, typename... Args>
+static inline et_status et_launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                  int cluster_x, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 0) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  if (cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...) != cudaSuccess) {
+    cudaGetLastError();
+    return ET_ERR_CUDA;
+  }
+  return et_launch_status();
+}

@@ -55,6 +55,8 @@ __device__ __forceinline__ int chunk_id(int c0, int j, int V) {
 }
 
 __global__ void __launch_bounds__(kExpThreads) k_expand(ExpandArgs a) {
+  pdl_wait();     // the previous kernel in the stream has completed
+  pdl_trigger();  // only now may the next kernel launch: at most one waits ahead
   extern __shared__ unsigned char smem_raw[];
   float *mz = reinterpret_cast<float *>(smem_raw);              // [nchunk*k]
   int *mi = reinterpret_cast<int *>(mz + a.nchunk * a.k);       // [nchunk*k]
@@ -285,6 +287,8 @@ __device__ __forceinline__ int block_excl_scan_1024(int v, int *tmp, int &total)
 }
 
 __global__ void __launch_bounds__(kRrThreads) k_rerank(RerankArgs a) {
+  pdl_wait();     // the previous kernel in the stream has completed
+  pdl_trigger();  // only now may the next kernel launch: at most one waits ahead
   __shared__ unsigned int hist[256];
   __shared__ unsigned int sel_digit, sel_before;
   __shared__ short flat_of[kMaxC];
@@ -397,6 +401,8 @@ __global__ void __launch_bounds__(kRrThreads) k_rerank(RerankArgs a) {
 __global__ void __launch_bounds__(kMaxN) k_mask_posids(int N, const int32_t *flat_parent, const int32_t *flat_depth,
                                                       const int32_t *prefix_len, uint64_t *mask, int32_t *posids,
                                                       int32_t *dev_status) {
+  pdl_wait();     // the previous kernel in the stream has completed
+  pdl_trigger();  // only now may the next kernel launch: at most one waits ahead
   __shared__ int par[kMaxN];
   const int b = blockIdx.x, i = threadIdx.x;
   const int W = (N + 63) >> 6;
@@ -470,6 +476,8 @@ __global__ void __launch_bounds__(kClThreads) k_expand_cl(ExpandRowArgs a) {
   const int b = row / a.m_l, s = row - b * a.m_l;
   const int k = a.k;
   cl_arrive_relaxed();  // phase 0: this block has started (waited on before any remote store)
+  pdl_wait();     // the previous kernel in the stream has completed
+  pdl_trigger();  // only now may the next kernel launch: at most one waits ahead
 
   int flag = 0, bad = 0;
   int node = -1;
@@ -670,23 +678,7 @@ static et_status launch_expand_row(const ExpandArgs &c, cudaStream_t stream) {
   a.tree = c.tree; a.dev_status = c.dev_status; a.seq_cnt = c.seq_cnt;
   // one cluster of ceil(V / 4096) CTAs per expanded row
   const int R = (c.V + kClSpan - 1) / kClSpan;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(R, c.B * c.m_l, 1);
-  cfg.blockDim = dim3(kClThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = R;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, k_expand_cl, a) != cudaSuccess) {
-    cudaGetLastError();
-    return ET_ERR_CUDA;
-  }
-  return et_launch_status();
+  return et_launch(k_expand_cl, dim3(R, c.B * c.m_l, 1), dim3(kClThreads, 1, 1), 0, stream, R, a);
 }
 
 static bool tree_ptrs_ok(const et_tree *t) {
@@ -723,8 +715,7 @@ extern "C" et_status et_tree_expand(const et_tree_cfg *cfg, int32_t layer, const
   if (cfg->V <= kClMaxV) return launch_expand_row(a, (cudaStream_t)stream);
   dim3 grid(a.nchunk, cfg->B * m_l);
   const size_t smem = (size_t)a.nchunk * a.k * (sizeof(float) + sizeof(int));
-  k_expand<<<grid, kExpThreads, smem, (cudaStream_t)stream>>>(a);
-  return et_launch_status();
+  return et_launch(k_expand, grid, dim3(kExpThreads), smem, (cudaStream_t)stream, 0, a);
 }
 
 extern "C" et_status et_tree_rerank(const et_tree_cfg *cfg, et_tree *tree, int32_t *dev_status, et_stream_t stream) {
@@ -739,8 +730,7 @@ extern "C" et_status et_tree_rerank(const et_tree_cfg *cfg, et_tree *tree, int32
   a.base[0] = 0;
   a.tree = *tree;
   a.dev_status = dev_status;
-  k_rerank<<<cfg->B, kRrThreads, 0, (cudaStream_t)stream>>>(a);
-  return et_launch_status();
+  return et_launch(k_rerank, dim3(cfg->B), dim3(kRrThreads), 0, (cudaStream_t)stream, 0, a);
 }
 
 extern "C" et_status et_tree_mask_posids(const et_tree_cfg *cfg, const et_tree *tree, const int32_t *prefix_len,
@@ -750,9 +740,9 @@ extern "C" et_status et_tree_mask_posids(const et_tree_cfg *cfg, const et_tree *
   ET_RETURN_IF(!tree || !tree->flat_parent || !tree->flat_depth || !prefix_len || !mask || !posids,
                ET_ERR_INVALID_ARG);
   ET_RETURN_IF(!et_aligned(mask, 8), ET_ERR_INVALID_ARG);
-  k_mask_posids<<<cfg->B, kMaxN, 0, (cudaStream_t)stream>>>(cfg->n + 1, tree->flat_parent, tree->flat_depth,
-                                                            prefix_len, mask, posids, nullptr);
-  return et_launch_status();
+  return et_launch(k_mask_posids, dim3(cfg->B), dim3(kMaxN), 0, (cudaStream_t)stream, 0, cfg->n + 1,
+                   (const int32_t *)tree->flat_parent, (const int32_t *)tree->flat_depth, prefix_len, mask, posids,
+                   (int32_t *)nullptr);
 }
 
 extern "C" et_status et_workspace_init(void *ws, size_t ws_bytes, et_stream_t stream) {
@@ -850,6 +840,5 @@ extern "C" et_status et_tree_expand_noalloc(const et_tree_cfg *cfg, int32_t laye
   if (cfg->V <= kClMaxV) return launch_expand_row(a, st);
   dim3 grid(a.nchunk, rows);
   const size_t smem = (size_t)a.nchunk * a.k * (sizeof(float) + sizeof(int));
-  k_expand<<<grid, kExpThreads, smem, st>>>(a);
-  return et_launch_status();
+  return et_launch(k_expand, grid, dim3(kExpThreads), smem, st, 0, a);
 }

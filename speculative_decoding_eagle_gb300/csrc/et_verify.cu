@@ -363,6 +363,8 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
 
 
 __global__ void __launch_bounds__(kVThreads) k_verify(VerifyArgs a) {
+  pdl_wait();     // the previous kernel in the stream has completed
+  pdl_trigger();  // only now may the next kernel launch: at most one waits ahead
   __shared__ WalkSmem w;
   __shared__ int sflag;
   float *redz = w.redz;
@@ -459,6 +461,8 @@ constexpr int kVClMaxCtas = 8;
 constexpr int kVClMaxV = kVClSpan * kVClMaxCtas;
 
 __global__ void __launch_bounds__(kVClThreads) k_verify_cl(VerifyArgs a) {
+  pdl_wait();     // the previous kernel in the stream has completed
+  pdl_trigger();  // only now may the next kernel launch: at most one waits ahead
   __shared__ WalkSmem w;
   __shared__ float part[2];
   __shared__ float gp0[kVClMaxCtas], gp1[kVClMaxCtas];
@@ -587,24 +591,7 @@ extern "C" et_status et_verify_accept(const et_tree_cfg *cfg, et_accept_mode mod
   a.vec4t = et_aligned(target_logits, 16) && target_stride % 4 == 0;
   if (cfg->V <= kVClMaxV) {  // one cluster of ceil(V / 4096) CTAs per flat row
     const int R = (cfg->V + kVClSpan - 1) / kVClSpan;
-    cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3(R, cfg->B * N, 1);
-    lc.blockDim = dim3(kVClThreads, 1, 1);
-    lc.stream = (cudaStream_t)stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = R;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    lc.attrs = attr;
-    lc.numAttrs = 1;
-    if (cudaLaunchKernelEx(&lc, k_verify_cl, a) != cudaSuccess) {
-      cudaGetLastError();
-      return ET_ERR_CUDA;
-    }
-  } else {
-    dim3 grid(a.nchunk, cfg->B * N);
-    k_verify<<<grid, kVThreads, 0, (cudaStream_t)stream>>>(a);
+    return et_launch(k_verify_cl, dim3(R, cfg->B * N, 1), dim3(kVClThreads), 0, (cudaStream_t)stream, R, a);
   }
-  return et_launch_status();
+  return et_launch(k_verify, dim3(a.nchunk, cfg->B * N), dim3(kVThreads), 0, (cudaStream_t)stream, 0, a);
 }
