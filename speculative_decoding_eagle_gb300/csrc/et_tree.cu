@@ -253,6 +253,9 @@ __global__ void __launch_bounds__(kExpThreads) k_expand(ExpandArgs a) {
 // ---------------------------------------------------------------------------
 constexpr int kRrThreads = 1024;
 constexpr int kRrPer = kMaxC / kRrThreads;  // 4 candidates per thread
+constexpr int kRrBinBits = 11;
+constexpr int kRrBins = 1 << kRrBinBits;    // two per thread
+constexpr int kRrBinCap = 64;               // keys of one bin ranked by counting
 
 struct RerankArgs {
   int B, C, n, N, depth;
@@ -289,8 +292,11 @@ __device__ __forceinline__ int block_excl_scan_1024(int v, int *tmp, int &total)
 __global__ void __launch_bounds__(kRrThreads) k_rerank(RerankArgs a) {
   pdl_wait();     // the previous kernel in the stream has completed
   pdl_trigger();  // only now may the next kernel launch: at most one waits ahead
-  __shared__ unsigned int hist[256];
-  __shared__ unsigned int sel_digit, sel_before;
+  __shared__ unsigned int hist[kRrBins];
+  __shared__ unsigned long long red_lo[32], red_hi[32], bin_keys[kRrBinCap];
+  __shared__ unsigned long long s_lo, s_hi, s_thr;
+  __shared__ int s_bin;
+  __shared__ unsigned int s_before, s_nb, s_cnt;
   __shared__ short flat_of[kMaxC];
   __shared__ unsigned char kept[kMaxC];
   __shared__ int tmp[32];
@@ -304,45 +310,84 @@ __global__ void __launch_bounds__(kRrThreads) k_rerank(RerankArgs a) {
     const int id = t + q * kRrThreads;
     rk[q] = id < C ? rank_key(a.tree.cand_key[(long long)b * C + id], id) : ~0ull;
   }
-  // MSB-first radix select of the n-th smallest rank key (keys are unique)
-  unsigned long long prefix = 0ull, pmask = 0ull;
-  unsigned int remaining = (unsigned)a.n;
-  for (int shift = 56; shift >= 0; shift -= 8) {
-    if (t < 256) hist[t] = 0u;
-    __syncthreads();
+  // The n-th smallest rank key (keys are unique): a 2048-bin histogram over
+  // [min, max] puts it in one bin; that bin's keys are ranked by counting
+  // when few, else the bin's range is histogrammed again (each pass narrows
+  // the range by 2^11, so six passes reach single keys).
+  unsigned long long mn = ~0ull, mx = 0ull;
 #pragma unroll
-    for (int q = 0; q < kRrPer; ++q) {
-      const int id = t + q * kRrThreads;
-      if (id < C && (rk[q] & pmask) == prefix) atomicAdd(&hist[(rk[q] >> shift) & 255ull], 1u);
+  for (int q = 0; q < kRrPer; ++q) {
+    if (t + q * kRrThreads < C) {
+      mn = rk[q] < mn ? rk[q] : mn;
+      mx = rk[q] > mx ? rk[q] : mx;
+    }
+  }
+  mn = warp_min_u64(mn);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long y = __shfl_xor_sync(0xffffffffu, mx, o);
+    mx = y > mx ? y : mx;
+  }
+  if (lane == 0) { red_lo[warp] = mn; red_hi[warp] = mx; }
+  for (int i = t; i < kRrBins; i += kRrThreads) hist[i] = 0u;
+  if (t == 0) s_cnt = 0u;
+  __syncthreads();
+  if (warp == 0) {
+    mn = warp_min_u64(red_lo[lane]);
+    mx = red_hi[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long y = __shfl_xor_sync(0xffffffffu, mx, o);
+      mx = y > mx ? y : mx;
+    }
+    if (lane == 0) { s_lo = mn; s_hi = mx; s_thr = ~0ull; }
+  }
+  __syncthreads();
+  unsigned long long lo = s_lo, hi = s_hi;
+  unsigned int remaining = (unsigned)a.n;  // 1-based rank of the wanted key among keys in [lo, hi]
+  for (int pass = 0; pass < 7; ++pass) {
+    const unsigned long long range = hi - lo;
+    const int bits = range ? 64 - __clzll((long long)range) : 0;
+    const int shift = bits > kRrBinBits ? bits - kRrBinBits : 0;
+#pragma unroll
+    for (int q = 0; q < kRrPer; ++q)
+      if (t + q * kRrThreads < C && rk[q] >= lo && rk[q] <= hi) atomicAdd(&hist[(rk[q] - lo) >> shift], 1u);
+    __syncthreads();
+    const unsigned int h0 = hist[2 * t], h1 = hist[2 * t + 1];  // kRrBins = 2 * kRrThreads
+    int total;
+    const unsigned int excl = (unsigned)block_excl_scan_1024((int)(h0 + h1), tmp, total);
+    if (excl < remaining && remaining <= excl + h0 + h1) {
+      const bool first = excl + h0 >= remaining;
+      s_bin = first ? 2 * t : 2 * t + 1;
+      s_before = first ? excl : excl + h0;
+      s_nb = first ? h0 : h1;
     }
     __syncthreads();
-    if (warp == 0) {
-      unsigned int loc[8], sum = 0;
+    const int B = s_bin;
+    const unsigned int nb = s_nb;
+    remaining -= s_before;
+    const unsigned long long blo = lo + ((unsigned long long)B << shift);
+    const unsigned long long bhi = shift ? (hi - blo < (1ull << shift) - 1 ? hi : blo + ((1ull << shift) - 1)) : blo;
+    if (nb <= (unsigned)kRrBinCap) {  // always so for shift == 0 (one key per value)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) { loc[j] = hist[8 * lane + j]; sum += loc[j]; }
-      unsigned int incl = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+      for (int q = 0; q < kRrPer; ++q)
+        if (t + q * kRrThreads < C && rk[q] >= blo && rk[q] <= bhi) bin_keys[atomicAdd(&s_cnt, 1u)] = rk[q];
+      __syncthreads();
+      if (t < (int)nb) {
+        const unsigned long long mine = bin_keys[t];
+        unsigned int r = 0;
+        for (unsigned int j = 0; j < nb; ++j) r += bin_keys[j] < mine ? 1u : 0u;
+        if (r + 1 == remaining) s_thr = mine;
       }
-      const unsigned int excl = incl - sum;
-      if (excl < remaining && remaining <= incl) {
-        unsigned int run = excl;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (run + loc[j] >= remaining) { sel_digit = 8 * lane + j; sel_before = run; break; }
-          run += loc[j];
-        }
-      }
+      __syncthreads();
+      break;
     }
-    __syncthreads();
-    prefix |= (unsigned long long)sel_digit << shift;
-    pmask |= 0xffull << shift;
-    remaining -= sel_before;
+    lo = blo;
+    hi = bhi;
+    for (int i = t; i < kRrBins; i += kRrThreads) hist[i] = 0u;
     __syncthreads();
   }
-  const unsigned long long thr = prefix;
+  const unsigned long long thr = s_thr;
 #pragma unroll
   for (int q = 0; q < kRrPer; ++q) {
     const int id = t + q * kRrThreads;
