@@ -158,38 +158,61 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
       }
     }
     __syncthreads();
-    if (t == 0) {
+    if (t < 32) {  // one warp walks: 32 candidate rows per ballot
+      const int lane = t;
       int cur = 0, alen = 0, nrej = 0;
-      w.opath[0] = 0;
+      if (lane == 0) w.opath[0] = 0;
       for (int iter = 0; iter <= a.D; ++iter) {
         int nxt = -1;
         nrej = 0;
         if (a.mode == ET_ACCEPT_GREEDY) {
           const int am = __float_as_int(w.rs0[cur]);
-          for (int j = cur + 1; j < N; ++j)
-            if (par[j] == cur && tokf[j] == am) { nxt = j; break; }
-          if (nxt < 0) w.otok[alen] = am;
+          for (int j0 = cur + 1; j0 < N; j0 += 32) {  // first row (ascending) that is a child with token am
+            const int j = j0 + lane;
+            const unsigned int hit = __ballot_sync(0xffffffffu, j < N && par[j] == cur && tokf[j] == am);
+            if (hit) { nxt = j0 + __ffs(hit) - 1; break; }
+          }
+          if (nxt < 0 && lane == 0) w.otok[alen] = am;
         } else {
           const float M = w.rs0[cur], S = w.rs1[cur];
           float R = 0.f;
-          for (int j = cur + 1; j < N; ++j) {
-            if (par[j] != cur) continue;
-            const float px = S > 0.f ? expf(w.zc[j] / a.T - M) / S : 0.f;
-            const float ratio = (R < 1.f) ? px / (1.f - R) : INFINITY;
-            if (a.uniforms[fo + j] < ratio) { nxt = j; break; }
-            R += px;
-            if (nrej < kMaxTopk) rej[nrej++] = tokf[j];
+          for (int j0 = cur + 1; j0 < N && nxt < 0; j0 += 32) {
+            const int j = j0 + lane;
+            const bool child = j < N && par[j] == cur;
+            // p(x) and the uniform of every child in parallel; R accumulates in row order
+            const float px = (child && S > 0.f) ? expf(w.zc[j] / a.T - M) / S : 0.f;
+            const float u = child ? a.uniforms[fo + j] : 0.f;
+            const int x = child ? tokf[j] : -1;
+            unsigned int kids = __ballot_sync(0xffffffffu, child);
+            while (kids) {
+              const int l = __ffs(kids) - 1;
+              kids &= kids - 1;
+              const float pl = __shfl_sync(0xffffffffu, px, l);
+              const float ul = __shfl_sync(0xffffffffu, u, l);
+              const int xl = __shfl_sync(0xffffffffu, x, l);
+              const float ratio = (R < 1.f) ? pl / (1.f - R) : INFINITY;
+              if (ul < ratio) { nxt = j0 + l; break; }
+              R += pl;
+              if (nrej < kMaxTopk) {
+                if (lane == 0) rej[nrej] = xl;
+                ++nrej;
+              }
+            }
           }
         }
         if (nxt < 0 || alen >= a.D) break;
-        w.otok[alen] = tokf[nxt];
+        if (lane == 0) {
+          w.otok[alen] = tokf[nxt];
+          w.opath[alen + 1] = nxt;
+        }
         ++alen;
-        w.opath[alen] = nxt;
         cur = nxt;
       }
-      s_cur = cur;
-      s_nrej = nrej;
-      w.s_alen = alen;
+      if (lane == 0) {
+        s_cur = cur;
+        s_nrej = nrej;
+        w.s_alen = alen;
+      }
     }
     __syncthreads();
     const int alen = w.s_alen;
@@ -451,8 +474,9 @@ __global__ void __launch_bounds__(kVThreads) k_verify(VerifyArgs a) {
 
 // ---------------------------------------------------------------------------
 // phase 1 on a thread-block cluster per flat row (V <= 32768): CTA q reduces
-// logits [4096 q, 4096 q + 4096); the leader merges through distributed
-// shared memory and writes the row's statistic.
+// logits [4096 q, 4096 q + 4096) and stores its result straight into the
+// leader's shared memory; after one cluster barrier the leader merges them
+// and writes the row's statistic.
 // ---------------------------------------------------------------------------
 constexpr int kVClThreads = 256;
 constexpr int kVClVec = 4;
@@ -461,17 +485,19 @@ constexpr int kVClMaxCtas = 8;
 constexpr int kVClMaxV = kVClSpan * kVClMaxCtas;
 
 __global__ void __launch_bounds__(kVClThreads) k_verify_cl(VerifyArgs a) {
-  pdl_wait();     // the previous kernel in the stream has completed
-  pdl_trigger();  // only now may the next kernel launch: at most one waits ahead
   __shared__ WalkSmem w;
-  __shared__ float part[2];
-  __shared__ float gp0[kVClMaxCtas], gp1[kVClMaxCtas];
+  __shared__ unsigned long long wkey[kVClThreads / 32], gkey[kVClMaxCtas];
+  __shared__ float wmax[kVClThreads / 32], wsum[kVClThreads / 32];
+  __shared__ float2 gms[kVClMaxCtas];
   __shared__ int sflag;
-  const int t = threadIdx.x;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int R = gridDim.x;
   const int q = (int)cl_rank();
   const int row = blockIdx.y;
   const int b = row / a.N;
+  cl_arrive_relaxed();  // phase 0: this block has started (waited on before any remote store)
+  pdl_wait();           // the previous kernel in the stream has completed
+  pdl_trigger();        // only now may the next kernel launch: at most one waits ahead
   int flag = 0, bad = 0;
   const int node = a.flat_node[row];
   const float *zrow = table_row(a.tlog, a.tstride, a.tmap, a.C, b, node, row, bad);
@@ -491,16 +517,19 @@ __global__ void __launch_bounds__(kVClThreads) k_verify_cl(VerifyArgs a) {
     for (int j = 0; j < 4; ++j)
       if (e0 + j < a.V) v[4 * u + j] = sanitize_logit(v[4 * u + j], flag);
   }
-  if (a.mode == ET_ACCEPT_GREEDY) {
-    float bz = -INFINITY;
-    int bi = 0x7fffffff;
+  const bool greedy = a.mode == ET_ACCEPT_GREEDY;
+  if (greedy) {  // (z desc, id asc) as one ascending key: the warp's best is its minimum
+    unsigned long long best = ~0ull;
 #pragma unroll
     for (int e = 0; e < 4 * kVClVec; ++e) {
       const int id = base + (e >> 2) * (kVClThreads * 4) + t * 4 + (e & 3);
-      if (id < a.V && ranks_before(v[e], id, bz, bi)) { bz = v[e]; bi = id; }
+      if (id < a.V) {
+        const unsigned long long kk = zid_key(v[e], (unsigned int)id);
+        best = kk < best ? kk : best;
+      }
     }
-    block_best<kVClThreads>(bz, bi, w.redz, w.redi);
-    if (t == 0) { part[0] = bz; part[1] = __int_as_float(bi); }
+    best = warp_min_u64(best);
+    if (lane == 0) wkey[warp] = best;
   } else {
     float lm = -INFINITY;
 #pragma unroll
@@ -508,38 +537,51 @@ __global__ void __launch_bounds__(kVClThreads) k_verify_cl(VerifyArgs a) {
       v[e] = v[e] / a.T;
       lm = fmaxf(lm, v[e]);
     }
-    const float Mq = block_max<kVClThreads>(lm, w.redz);
+    lm = warp_max(lm);
+    if (lane == 0) wmax[warp] = lm;
+  }
+  if (flag) flag_status(a.dev_status, ET_DEV_NONFINITE);
+  if (bad && q == 0 && t == 0) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
+  __syncthreads();
+  cl_wait();  // phase 0 done: every block of the cluster runs
+  if (greedy) {
+    if (warp == 0) {
+      const unsigned long long kk = warp_min_u64(wkey[lane & (kVClThreads / 32 - 1)]);
+      if (lane == 0) cl_st_u64(cl_map(&gkey[q], 0), kk);
+    }
+  } else {
+    float Mq = wmax[0];
+#pragma unroll
+    for (int x = 1; x < kVClThreads / 32; ++x) Mq = fmaxf(Mq, wmax[x]);
     float ls = 0.f;
     if (Mq > -INFINITY) {
 #pragma unroll
       for (int e = 0; e < 4 * kVClVec; ++e) ls += exp_fast(v[e] - Mq);
     }
-    const float Sq = block_sum<kVClThreads>(ls, w.redz);
-    if (t == 0) { part[0] = Mq; part[1] = Sq; }
+    ls = warp_sum(ls);
+    if (lane == 0) wsum[warp] = ls;
+    __syncthreads();
+    if (t == 0) {
+      float Sq = 0.f;
+#pragma unroll
+      for (int x = 0; x < kVClThreads / 32; ++x) Sq += wsum[x];
+      cl_st_f32x2(cl_map(&gms[q], 0), Mq, Sq);
+    }
   }
-  if (flag) flag_status(a.dev_status, ET_DEV_NONFINITE);
-  if (bad && q == 0 && t == 0) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
-  cl_sync();
-  if (q == 0 && t < R) {
-    gp0[t] = cl_ld_f32(cl_map(&part[0], t));
-    gp1[t] = cl_ld_f32(cl_map(&part[1], t));
-  }
-  cl_sync();
+  cl_arrive();  // phase 1: release this block's stores
   if (q != 0) return;
-  __syncthreads();
+  cl_wait();
   if (t == 0) {
-    if (a.mode == ET_ACCEPT_GREEDY) {
-      float bz = -INFINITY;
-      int bi = 0x7fffffff;
-      for (int x = 0; x < R; ++x)
-        if (ranks_before(gp0[x], __float_as_int(gp1[x]), bz, bi)) { bz = gp0[x]; bi = __float_as_int(gp1[x]); }
-      a.rowstat[2 * row] = __int_as_float(bi);
-      a.rowstat[2 * row + 1] = bz;
+    if (greedy) {
+      unsigned long long kk = gkey[0];
+      for (int x = 1; x < R; ++x) kk = gkey[x] < kk ? gkey[x] : kk;
+      a.rowstat[2 * row] = __int_as_float((int)zid_id(kk));
+      a.rowstat[2 * row + 1] = zid_value(kk);
     } else {
       float M = -INFINITY;
-      for (int x = 0; x < R; ++x) M = fmaxf(M, gp0[x]);
+      for (int x = 0; x < R; ++x) M = fmaxf(M, gms[x].x);
       float S = 0.f;
-      for (int x = 0; x < R; ++x) S += gp0[x] > -INFINITY ? gp1[x] * expf(gp0[x] - M) : 0.f;
+      for (int x = 0; x < R; ++x) S += gms[x].x > -INFINITY ? gms[x].y * expf(gms[x].x - M) : 0.f;
       a.rowstat[2 * row] = M;
       a.rowstat[2 * row + 1] = S;
     }
