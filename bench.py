@@ -193,6 +193,31 @@ def oracle_baseline(name, budget_s=12.0, max_steps=40):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+# replicas: each rank runs whole steps on its own sequences (no data-path
+# collective); only the timing is reduced, as the maximum over ranks
+# ---------------------------------------------------------------------------
+def shard_offsets(rank: int, n_sets: int, batch: int):
+    """First sequence index of each of rank `rank`'s input sets: ranks and
+    sets cover disjoint, consecutive blocks of `batch` sequences."""
+    return [(rank * n_sets + r) * batch for r in range(n_sets)]
+
+
+def reduce_step_ms(step_ms: float, world: int, device=None) -> float:
+    """The slowest rank's time per step (all ranks wait for it)."""
+    if world <= 1:
+        return step_ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([step_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(step_ms: float, world: int) -> float:
+    """Steps per second of all ranks together (weak scaling: one step per rank)."""
+    return world * 1000.0 / step_ms
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -228,8 +253,7 @@ def run_gpu(args):
     R = args.sets or max(2, int(np.ceil(2 * L2_BYTES / per_step)) + 1)
     # rank r's sequences are disjoint from every other rank's (weak scaling)
     sets = []
-    for r in range(R):
-        b0 = (rank * R + r) * cfg.B
+    for b0 in shard_offsets(rank, R, cfg.B):
         sets.append(S.to_device(wl, S.host_inputs(wl, st.C, cfg.B, b0=b0)))
     st.prepare(sets[0])
     torch.cuda.synchronize()
@@ -272,12 +296,8 @@ def run_gpu(args):
         ev1.record(cur)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
-    step_ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([step_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
-    steps_per_s = world * 1000.0 / step_ms
+    step_ms = reduce_step_ms(ev0.elapsed_time(ev1) / args.steps, world, device="cuda")
+    steps_per_s = whole_job_rate(step_ms, world)
 
     # ---- attention alone: a graph of K launches over the rotating sets ----
     K = max(8, min(200, args.steps))
