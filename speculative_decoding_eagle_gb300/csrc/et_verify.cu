@@ -35,6 +35,7 @@ struct VerifyArgs {
   float *rowstat;     // [B*N][2]
   unsigned int *row_cnt, *seq_cnt;
   int vec4t;
+  int cdf_span, cdf_nch;  // STOCH_POINT: chunk statistics (max, sum) of each row in part, span tokens each
 };
 
 __device__ __forceinline__ const float *table_row(const float *tab, long long stride, const int32_t *map, int C,
@@ -50,59 +51,228 @@ __device__ __forceinline__ const float *table_row(const float *tab, long long st
   return tab + r * stride;
 }
 
-// Inverse CDF over a row: smallest v with sum_{u<=v} w(u) > uni * sum_u w(u),
-// accumulated in fp64 over contiguous per-thread segments.  `w(v)` must be
-// non-negative; falls back to the last v with w(v) > 0.
+// Inverse CDF over a row: smallest v with sum_{u<=v} w(u) > uni * sum_u w(u)
+// (falls back to the last v with w(v) > 0).  `w(v)` must be non-negative and
+// give the same value on every call.  Pass 1 walks the row in tiles of 4·NT
+// tokens, four consecutive tokens per thread (coalesced), summing each tile
+// per warp in fp32; one warp adds the tiles in fp64 and finds the tile where
+// the cumulative sum crosses; pass 2 rescans that tile alone with an fp64
+// block scan.
+constexpr int kCdfTileMax = kMaxV / (256 * 4);  // tiles of the largest row at 256 threads
+
 template <int NT, typename WF>
-__device__ int block_inverse_cdf(int V, float uni, WF w, double *redd, int *redi) {
-  const int t = threadIdx.x;
-  const int seg = (V + NT - 1) / NT;
-  const int lo = t * seg, hi = min(V, lo + seg);
-  double loc = 0.0;
+__device__ int block_inverse_cdf(int V, float uni, WF w, double *redd, int *redi, float *tpart, double *tsum) {
+  static_assert(NT == 256, "tile bookkeeping sized for 256 threads");
+  constexpr int NW = NT / 32, TILE = NT * 4;
+  const int t = threadIdx.x, lane = t & 31, wp = t >> 5;
+  const int ntile = (V + TILE - 1) / TILE;
   int lastpos = -1;
-  for (int v = lo; v < hi; ++v) {
-    const float x = w(v);
-    loc += (double)x;
-    if (x > 0.f) lastpos = v;
-  }
-  // exclusive scan of the segment sums
-  const int lane = t & 31, wp = t >> 5;
-  double incl = loc;
+  for (int tile = 0; tile < ntile; ++tile) {
+    float sl = 0.f;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    double y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  __syncthreads();
-  if (lane == 31) redd[wp] = incl;
-  __syncthreads();
-  if (wp == 0) {
-    double s = lane < NT / 32 ? redd[lane] : 0.0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      double y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
+    for (int j = 0; j < 4; ++j) {
+      const int v = tile * TILE + 4 * t + j;
+      if (v < V) {
+        const float x = w(v);
+        sl += x;
+        if (x > 0.f) lastpos = v;
+      }
     }
-    if (lane < NT / 32) redd[lane] = s;
+    sl = warp_sum(sl);
+    if (lane == 0) tpart[tile * NW + wp] = sl;
   }
-  __syncthreads();
-  const double total = redd[NT / 32 - 1];
-  const double excl = (wp > 0 ? redd[wp - 1] : 0.0) + incl - loc;
-  const double thr = (double)uni * total;
-  __syncthreads();
-  if (t == 0) { redi[0] = 0x7fffffff; redi[1] = -1; }
+  if (t == 0) { redi[0] = 0x7fffffff; redi[1] = -1; redi[3] = -1; }
   __syncthreads();
   if (lastpos >= 0) atomicMax(&redi[1], lastpos);
-  if (loc > 0.0 && excl <= thr && thr < excl + loc) {
-    double run = excl;
-    int found = -1;
-    for (int v = lo; v < hi; ++v) {
-      run += (double)w(v);
-      if (run > thr) { found = v; break; }
+  if (wp == 0) {
+    double total = 0.0;
+    for (int c0 = 0; c0 < ntile; c0 += 32) {
+      const int tile = c0 + lane;
+      double ts = 0.0;
+      if (tile < ntile) {
+#pragma unroll
+        for (int x = 0; x < NW; ++x) ts += (double)tpart[tile * NW + x];
+        tsum[tile] = ts;
+      }
+      total += warp_sum_d(ts);
     }
-    if (found >= 0) atomicMin(&redi[0], found);
+    const double thr = (double)uni * total;
+    double run = 0.0;
+    int J = -1;
+    double before = 0.0;
+    for (int c0 = 0; c0 < ntile && J < 0; c0 += 32) {
+      const int tile = c0 + lane;
+      const double ts = tile < ntile ? tsum[tile] : 0.0;
+      double incl = ts;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned int hit = __ballot_sync(0xffffffffu, tile < ntile && run + incl > thr);
+      if (hit) {
+        const int l = __ffs(hit) - 1;
+        J = c0 + l;
+        before = run + __shfl_sync(0xffffffffu, incl, l) - __shfl_sync(0xffffffffu, ts, l);
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      redd[0] = before;
+      redd[1] = thr;
+      redi[2] = J;
+    }
   }
   __syncthreads();
+  const int J = redi[2];
+  if (J >= 0) {  // pass 2: the crossing tile only
+    float x[4];
+    double mine = 0.0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int v = J * TILE + 4 * t + j;
+      x[j] = v < V ? w(v) : 0.f;
+      mine += (double)x[j];
+    }
+    double incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) tsum[wp] = incl;  // the tile sums are no longer needed
+    __syncthreads();
+    double wbase = 0.0;
+    for (int x2 = 0; x2 < wp; ++x2) wbase += tsum[x2];
+    double run = redd[0] + wbase + incl - mine;
+    const double thr = redd[1];
+    int lastJ = -1;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (x[j] > 0.f) lastJ = J * TILE + 4 * t + j;
+      run += (double)x[j];
+      if (x[j] > 0.f && run > thr) { atomicMin(&redi[0], J * TILE + 4 * t + j); break; }
+    }
+    if (lastJ >= 0) atomicMax(&redi[3], lastJ);
+  }
+  __syncthreads();
+  // not crossed inside the tile (its two sums differ in the last bits): the
+  // crossing is at its end, so take its last token of positive weight
+  const int r = redi[0] != 0x7fffffff ? redi[0] : (redi[3] >= 0 ? redi[3] : redi[1]);
+  __syncthreads();
+  return r;
+}
+
+// STOCH_POINT bonus token: the inverse CDF of the residual p at the stop row
+// (rejected children removed) from the row's chunk statistics.  Chunk c holds
+// tokens [c·span, (c+1)·span) with (max, sum of exp) (Mc, Sc) from phase 1, so
+// its weight is Sc·exp(Mc − M) minus the weights of the rejected children it
+// contains; one warp finds the chunk where the cumulative weight crosses
+// uni·total, then the block rescans that chunk alone (fp64 block scan).
+template <int NT>
+__device__ int bonus_from_chunks(const VerifyArgs &a, const float *zr, const float *cstat, float M, float uni,
+                                 const int *rej, const float *rejw, int nrej, double *redd, int *redi,
+                                 double *tsum) {
+  const int t = threadIdx.x, lane = t & 31, wp = t >> 5;
+  const int span = a.cdf_span, nch = a.cdf_nch;
+  if (t == 0) { redi[0] = 0x7fffffff; redi[1] = -1; }
+  if (wp == 0) {
+    double total = 0.0;
+    for (int c0 = 0; c0 < nch; c0 += 32) {
+      const int c = c0 + lane;
+      double wc = 0.0;
+      if (c < nch) {
+        const float mc = ld_cg(cstat + 2 * c), sc = ld_cg(cstat + 2 * c + 1);
+        wc = mc > -INFINITY ? (double)sc * (double)expf(mc - M) : 0.0;
+        for (int q = 0; q < nrej; ++q)
+          if (rej[q] >= 0 && rej[q] / span == c) wc -= (double)rejw[q];
+        wc = wc > 0.0 ? wc : 0.0;
+        tsum[c] = wc;
+      }
+      total += warp_sum_d(wc);
+    }
+    const double thr = (double)uni * total;
+    double run = 0.0, before = 0.0;
+    int J = -1, lastc = -1;
+    for (int c0 = 0; c0 < nch; c0 += 32) {
+      const int c = c0 + lane;
+      const double wc = c < nch ? tsum[c] : 0.0;
+      double incl = wc;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned int pos = __ballot_sync(0xffffffffu, c < nch && wc > 0.0);
+      if (pos) lastc = c0 + 31 - __clz(pos);
+      const unsigned int hit = __ballot_sync(0xffffffffu, c < nch && wc > 0.0 && run + incl > thr);
+      if (hit && J < 0) {
+        const int l = __ffs(hit) - 1;
+        J = c0 + l;
+        before = run + __shfl_sync(0xffffffffu, incl, l) - __shfl_sync(0xffffffffu, wc, l);
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (J < 0) {  // thr at or beyond the total (rounding): the last chunk with weight
+      J = lastc;
+      before = -1.0;
+    }
+    if (lane == 0) {
+      redd[0] = before;
+      redd[1] = thr;
+      redi[2] = J;
+    }
+  }
+  __syncthreads();
+  const int J = redi[2];
+  if (J < 0 || !zr) {
+    __syncthreads();
+    return -1;
+  }
+  // pass over chunk J: per thread a contiguous run of span / NT tokens
+  const int per = (span + NT - 1) / NT;
+  const int v0 = J * span + t * per;
+  double mine = 0.0;
+  int lastv = -1;
+  for (int j = 0; j < per; ++j) {
+    const int v = v0 + j;
+    if (v >= a.V || v >= (J + 1) * span) break;
+    bool rejected = false;
+    for (int q = 0; q < nrej; ++q) rejected |= (rej[q] == v);
+    int f2 = 0;
+    const float y = sanitize_logit(zr[v], f2) / a.T;
+    const float x = (!rejected && y > -INFINITY) ? expf(y - M) : 0.f;
+    mine += (double)x;
+    if (x > 0.f) lastv = v;
+  }
+  double incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) tsum[wp] = incl;
+  if (lastv >= 0) atomicMax(&redi[1], lastv);
+  __syncthreads();
+  const double before = redd[0], thr = redd[1];
+  if (before >= 0.0) {
+    double run = before + incl - mine;
+    for (int x2 = 0; x2 < wp; ++x2) run += tsum[x2];
+    for (int j = 0; j < per; ++j) {
+      const int v = v0 + j;
+      if (v >= a.V || v >= (J + 1) * span) break;
+      bool rejected = false;
+      for (int q = 0; q < nrej; ++q) rejected |= (rej[q] == v);
+      int f2 = 0;
+      const float y = sanitize_logit(zr[v], f2) / a.T;
+      const float x = (!rejected && y > -INFINITY) ? expf(y - M) : 0.f;
+      run += (double)x;
+      if (x > 0.f && run > thr) { atomicMin(&redi[0], v); break; }
+    }
+  }
+  __syncthreads();
+  // not crossed inside the chunk (its two sums differ in the last bits): the
+  // crossing is at its end, so take its last token of positive weight
   const int r = redi[0] != 0x7fffffff ? redi[0] : redi[1];
   __syncthreads();
   return r;
@@ -112,11 +282,15 @@ struct WalkSmem {
   float redz[32];
   int redi[32];
   double redd[32];
+  float cdf_tpart[kCdfTileMax * 8];  // per tile, per warp sums of the inverse CDF
+  double cdf_tsum[kCdfTileMax];
   int par[kMaxN], tokf[kMaxN], nodef[kMaxN];
   float rs0[kMaxN], rs1[kMaxN];  // per flat row: argmax id (bits) / max, -, / sum
   float zc[kMaxN];               // target logit of each row's token in its parent's row
   int opath[kMaxDepth + 2], otok[kMaxDepth + 2];
   int rej[kMaxTopk];
+  float rejw[kMaxTopk];  // exp(z/T - M) of each rejected child at the stop row
+  float uni[kMaxN];      // this sequence's uniforms
   float zsh[kMaxTopk];
   int s_next, s_nrej, s_cur, s_alen;
 };
@@ -148,6 +322,7 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
     for (int j = t; j < N; j += NT) {
       w.rs0[j] = ld_cg(a.rowstat + 2 * (fo + j));
       w.rs1[j] = ld_cg(a.rowstat + 2 * (fo + j) + 1);
+      if (a.mode == ET_ACCEPT_STOCH_POINT) w.uni[j] = a.uniforms[fo + j];
       if (a.mode == ET_ACCEPT_STOCH_POINT && j > 0) {
         const int p = a.flat_parent[fo + j];
         const int x = a.flat_tok[fo + j];
@@ -180,8 +355,9 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
             const int j = j0 + lane;
             const bool child = j < N && par[j] == cur;
             // p(x) and the uniform of every child in parallel; R accumulates in row order
-            const float px = (child && S > 0.f) ? expf(w.zc[j] / a.T - M) / S : 0.f;
-            const float u = child ? a.uniforms[fo + j] : 0.f;
+            const float wx = child ? expf(w.zc[j] / a.T - M) : 0.f;
+            const float px = (child && S > 0.f) ? wx / S : 0.f;
+            const float u = child ? w.uni[j] : 0.f;
             const int x = child ? tokf[j] : -1;
             unsigned int kids = __ballot_sync(0xffffffffu, child);
             while (kids) {
@@ -190,11 +366,12 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
               const float pl = __shfl_sync(0xffffffffu, px, l);
               const float ul = __shfl_sync(0xffffffffu, u, l);
               const int xl = __shfl_sync(0xffffffffu, x, l);
+              const float wl = __shfl_sync(0xffffffffu, wx, l);
               const float ratio = (R < 1.f) ? pl / (1.f - R) : INFINITY;
               if (ul < ratio) { nxt = j0 + l; break; }
               R += pl;
               if (nrej < kMaxTopk) {
-                if (lane == 0) rej[nrej] = xl;
+                if (lane == 0) { rej[nrej] = xl; w.rejw[nrej] = wl; }
                 ++nrej;
               }
             }
@@ -220,15 +397,8 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
       const int cur = s_cur, nrej = s_nrej;
       int badz = 0;
       const float *zr = table_row(a.tlog, a.tstride, a.tmap, a.C, b, nodef[cur], fo + cur, badz);
-      const float M = w.rs0[cur];
-      const int bonus = block_inverse_cdf<NT>(a.V, a.uniforms[fo], [&](int vv) -> float {
-        if (!zr) return 0.f;
-        for (int q = 0; q < nrej; ++q)
-          if (rej[q] == vv) return 0.f;
-        int f2 = 0;
-        const float y = sanitize_logit(zr[vv], f2) / a.T;
-        return y > -INFINITY ? expf(y - M) : 0.f;
-      }, redd, redi);
+      const int bonus = bonus_from_chunks<NT>(a, zr, a.part + (fo + cur) * (long long)a.nchunk * 2, w.rs0[cur],
+                                              w.uni[0], rej, w.rejw, nrej, redd, redi, w.cdf_tsum);
       if (t == 0) w.otok[alen] = bonus;
       badp |= badz;
     }
@@ -290,7 +460,7 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
           int f2 = 0;
           const float y = sanitize_logit(zr[vv], f2) / a.T;
           return y > -INFINITY ? expf(y - M) : 0.f;
-        }, redd, redi);
+        }, redd, redi, w.cdf_tpart, w.cdf_tsum);
       }
     } else {  // ET_ACCEPT_STOCH_DRAFTQ
       const float M = ld_cg(a.rowstat + 2 * (fo + cur)), S = ld_cg(a.rowstat + 2 * (fo + cur) + 1);
@@ -356,7 +526,7 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
       __syncthreads();
       if (s_next < 0) {
         const int nzf = nz;
-        bonus = block_inverse_cdf<NT>(a.V, a.uniforms[fo], [&](int vv) -> float { return rval(vv, nzf); }, redd, redi);
+        bonus = block_inverse_cdf<NT>(a.V, a.uniforms[fo], [&](int vv) -> float { return rval(vv, nzf); }, redd, redi, w.cdf_tpart, w.cdf_tsum);
       }
     }
     __syncthreads();
@@ -584,6 +754,8 @@ __global__ void __launch_bounds__(kVClThreads) k_verify_cl(VerifyArgs a) {
       for (int x = 0; x < R; ++x) S += gms[x].x > -INFINITY ? gms[x].y * expf(gms[x].x - M) : 0.f;
       a.rowstat[2 * row] = M;
       a.rowstat[2 * row + 1] = S;
+      float *cst = a.part + (long long)row * a.nchunk * 2;  // chunk statistics for the bonus draw
+      for (int x = 0; x < R; ++x) { cst[2 * x] = gms[x].x; cst[2 * x + 1] = gms[x].y; }
     }
   }
   if (!arrive_last(&a.seq_cnt[b], (unsigned)a.N, &sflag)) return;
@@ -633,7 +805,11 @@ extern "C" et_status et_verify_accept(const et_tree_cfg *cfg, et_accept_mode mod
   a.vec4t = et_aligned(target_logits, 16) && target_stride % 4 == 0;
   if (cfg->V <= kVClMaxV) {  // one cluster of ceil(V / 4096) CTAs per flat row
     const int R = (cfg->V + kVClSpan - 1) / kVClSpan;
+    a.cdf_span = kVClSpan;
+    a.cdf_nch = R;
     return et_launch(k_verify_cl, dim3(R, cfg->B * N, 1), dim3(kVClThreads), 0, (cudaStream_t)stream, R, a);
   }
+  a.cdf_span = kVChunk;
+  a.cdf_nch = a.nchunk;
   return et_launch(k_verify, dim3(a.nchunk, cfg->B * N), dim3(kVThreads), 0, (cudaStream_t)stream, 0, a);
 }
