@@ -9,6 +9,7 @@
  *   for layer = 0 .. depth-1:  et_tree_expand      (expansion phase)
  *   et_tree_rerank                                  (reranking phase, flatten)
  *   et_tree_mask_posids                             (attention mask, positions)
+ *     (or et_tree_rerank_mask: both in one launch)
  *   et_tree_attention  (inside each target layer)   (ancestor-masked attention)
  *   et_verify_accept                                (lossless acceptance)
  *
@@ -208,7 +209,7 @@ et_status et_tree_expand_noalloc(const et_tree_cfg *cfg, int32_t layer,
  * with the largest (key desc, id asc) -- equal values keep the shallower
  * node, so the kept tree is connected -- and flatten them: row 0 is the
  * root, rows 1..n the kept ids ascending.  Writes tree->flat_*.
- * One CTA per sequence (segmented radix select over C 64-bit keys).
+ * One CTA per sequence (histogram select over C 64-bit keys).
  */
 et_status et_tree_rerank(const et_tree_cfg *cfg, et_tree *tree, int32_t *dev_status,
                          et_stream_t stream);
@@ -225,6 +226,18 @@ et_status et_tree_rerank(const et_tree_cfg *cfg, et_tree *tree, int32_t *dev_sta
 et_status et_tree_mask_posids(const et_tree_cfg *cfg, const et_tree *tree,
                               const int32_t *prefix_len, uint64_t *mask, int32_t *posids,
                               et_stream_t stream);
+
+/*
+ * et_tree_rerank_mask -- et_tree_rerank followed by et_tree_mask_posids in
+ * one launch (EAGLE-2 article: reranking phase, then the attention mask and
+ * position encoding of the flattened tree).  Writes exactly what the two
+ * calls write (tree->flat_*, mask, posids); the rerank CTA of each sequence
+ * builds the mask from the parent rows it has just produced, which saves a
+ * launch and a round trip through memory.  Arguments as in the two calls;
+ * a parent row that does not precede its child sets ET_DEV_BAD_INDEX.
+ */
+et_status et_tree_rerank_mask(const et_tree_cfg *cfg, et_tree *tree, const int32_t *prefix_len,
+                              uint64_t *mask, int32_t *posids, int32_t *dev_status, et_stream_t stream);
 
 /*
  * et_tree_attention -- attention of the N flattened draft rows over the KV

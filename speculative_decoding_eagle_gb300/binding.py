@@ -27,7 +27,7 @@ ATTN_AUTO, ATTN_MMA_SYNC, ATTN_TCGEN05 = 0, 1, 2
 
 EXPORTED = ("et_num_candidates", "et_layer_expanded", "et_layer_base", "et_tree_workspace_size",
             "et_tree_attention_workspace_size", "et_tree_attention_splits", "et_workspace_init",
-            "et_status_string", "et_abi_version", "et_tree_expand", "et_tree_expand_noalloc", "et_tree_rerank",
+            "et_status_string", "et_abi_version", "et_tree_expand", "et_tree_expand_noalloc", "et_tree_rerank", "et_tree_rerank_mask",
             "et_tree_mask_posids", "et_tree_attention", "et_verify_accept")
 
 
@@ -79,6 +79,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "et_tree_expand": (c_i32, [P(TreeCfgC), c_i32, c_vp, c_i64, c_vp, P(TreeC), c_vp, c_vp, c_sz, c_vp]),
         "et_tree_expand_noalloc": (c_i32, [P(TreeCfgC), c_i32, c_vp, c_i64, c_vp, P(TreeC), c_vp, c_vp]),
         "et_tree_rerank": (c_i32, [P(TreeCfgC), P(TreeC), c_vp, c_vp]),
+        "et_tree_rerank_mask": (c_i32, [P(TreeCfgC), P(TreeC), c_vp, c_vp, c_vp, c_vp, c_vp]),
         "et_tree_mask_posids": (c_i32, [P(TreeCfgC), P(TreeC), c_vp, c_vp, c_vp, c_vp]),
         "et_tree_attention": (c_i32, [P(AttnShapeC), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                       c_vp, c_vp, c_sz, c_vp]),
@@ -246,6 +247,15 @@ def et_tree_rerank(cfg: TreeCfg, tree: TreeBuffers, dev_status: Optional[torch.T
     st = load().et_tree_rerank(ctypes.byref(cfg.c()), ctypes.byref(tree.c()),
                                _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
     _check("et_tree_rerank", st)
+
+
+def et_tree_rerank_mask(cfg: TreeCfg, tree: TreeBuffers, prefix_len: torch.Tensor, mask: torch.Tensor,
+                        posids: torch.Tensor, dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    st = load().et_tree_rerank_mask(ctypes.byref(cfg.c()), ctypes.byref(tree.c()),
+                                    _ptr(prefix_len, torch.int32, "prefix_len"), _ptr(mask, torch.int64, "mask"),
+                                    _ptr(posids, torch.int32, "posids"), _ptr(dev_status, torch.int32, "dev_status"),
+                                    _stream(stream))
+    _check("et_tree_rerank_mask", st)
 
 
 def et_tree_mask_posids(cfg: TreeCfg, tree: TreeBuffers, prefix_len: torch.Tensor, mask: torch.Tensor,

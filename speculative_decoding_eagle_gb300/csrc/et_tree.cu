@@ -262,7 +262,27 @@ struct RerankArgs {
   int base[kMaxDepth + 2];
   et_tree tree;
   int32_t *dev_status;
+  // optional (et_tree_rerank_mask): ancestor mask and position ids as well
+  const int32_t *prefix_len;
+  uint64_t *mask;
+  int32_t *posids;
 };
+
+// Ancestor bitmask of flat row i from its parent rows (parents precede
+// children): bit j set iff row j is i or an ancestor of i.  Returns false on
+// a parent that does not precede its child.
+__device__ __forceinline__ bool ancestor_bits(const int *par, int i, uint64_t &w0, uint64_t &w1) {
+  w0 = 0; w1 = 0;
+  int j = i, steps = 0;
+  while (j >= 0 && steps <= kMaxN) {  // parents have smaller rows: at most N steps
+    if (j < 64) w0 |= 1ull << j; else w1 |= 1ull << (j - 64);
+    const int p = par[j];
+    if (p >= j) return false;
+    j = p;
+    ++steps;
+  }
+  return true;
+}
 
 __device__ __forceinline__ int block_excl_scan_1024(int v, int *tmp, int &total) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -300,6 +320,7 @@ __global__ void __launch_bounds__(kRrThreads) k_rerank(RerankArgs a) {
   __shared__ short flat_of[kMaxC];
   __shared__ unsigned char kept[kMaxC];
   __shared__ int tmp[32];
+  __shared__ int row_par[kMaxN], row_dep[kMaxN];  // fused mask: parent row and depth of each flat row
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int b = blockIdx.x;
   const int C = a.C;
@@ -310,6 +331,7 @@ __global__ void __launch_bounds__(kRrThreads) k_rerank(RerankArgs a) {
     const int id = t + q * kRrThreads;
     rk[q] = id < C ? rank_key(a.tree.cand_key[(long long)b * C + id], id) : ~0ull;
   }
+  if (t < kMaxN) { row_par[t] = 0; row_dep[t] = 0; }  // rows a broken tree leaves unwritten
   // The n-th smallest rank key (keys are unique): a 2048-bin histogram over
   // [min, max] puts it in one bin; that bin's keys are ranked by counting
   // when few, else the bin's range is histogrammed again (each pass narrows
@@ -430,6 +452,8 @@ __global__ void __launch_bounds__(kRrThreads) k_rerank(RerankArgs a) {
     a.tree.flat_tok[fo + row] = a.tree.cand_tok[(long long)b * C + id];
     a.tree.flat_parent[fo + row] = prow;
     a.tree.flat_depth[fo + row] = depth;
+    row_par[row] = prow;
+    row_dep[row] = depth;
   }
   if (bad) flag_status(a.dev_status, ET_DEV_DISCONNECTED);
   if (t == 0) {
@@ -437,6 +461,21 @@ __global__ void __launch_bounds__(kRrThreads) k_rerank(RerankArgs a) {
     a.tree.flat_tok[fo] = a.tree.root_tok ? a.tree.root_tok[b] : -1;
     a.tree.flat_parent[fo] = -1;
     a.tree.flat_depth[fo] = 0;
+    row_par[0] = -1;
+    row_dep[0] = 0;
+  }
+  if (!a.mask) return;
+  // ---- fused: ancestor mask + position ids of the rows just written ----
+  __syncthreads();
+  const int N = a.N, W = (N + 63) >> 6;
+  if (t < N) {
+    uint64_t w0, w1;
+    const bool ok = ancestor_bits(row_par, t, w0, w1);
+    uint64_t *mrow = a.mask + ((long long)b * N + t) * W;
+    mrow[0] = w0;
+    if (W > 1) mrow[1] = w1;
+    a.posids[(long long)b * N + t] = a.prefix_len[b] + row_dep[t];
+    if (!ok) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
   }
 }
 
@@ -454,15 +493,8 @@ __global__ void __launch_bounds__(kMaxN) k_mask_posids(int N, const int32_t *fla
   if (i < N) par[i] = flat_parent[(long long)b * N + i];
   __syncthreads();
   if (i >= N) return;
-  uint64_t w0 = 0, w1 = 0;
-  int j = i, steps = 0, bad = 0;
-  while (j >= 0 && steps <= kMaxN) {  // parents have smaller rows: at most N steps
-    if (j < 64) w0 |= 1ull << j; else w1 |= 1ull << (j - 64);
-    const int p = par[j];
-    if (p >= j) { bad = 1; break; }
-    j = p;
-    ++steps;
-  }
+  uint64_t w0, w1;
+  const int bad = ancestor_bits(par, i, w0, w1) ? 0 : 1;
   uint64_t *mrow = mask + ((long long)b * N + i) * W;
   mrow[0] = w0;
   if (W > 1) mrow[1] = w1;
@@ -763,7 +795,8 @@ extern "C" et_status et_tree_expand(const et_tree_cfg *cfg, int32_t layer, const
   return et_launch(k_expand, grid, dim3(kExpThreads), smem, (cudaStream_t)stream, 0, a);
 }
 
-extern "C" et_status et_tree_rerank(const et_tree_cfg *cfg, et_tree *tree, int32_t *dev_status, et_stream_t stream) {
+static et_status launch_rerank(const et_tree_cfg *cfg, et_tree *tree, int32_t *dev_status, const int32_t *prefix_len,
+                               uint64_t *mask, int32_t *posids, et_stream_t stream) {
   Geometry g;
   ET_RETURN_IF(!make_geometry(cfg, &g), ET_ERR_INVALID_ARG);
   ET_RETURN_IF(!tree || !tree->cand_tok || !tree->cand_parent || !tree->cand_key || !tree->flat_node ||
@@ -775,7 +808,21 @@ extern "C" et_status et_tree_rerank(const et_tree_cfg *cfg, et_tree *tree, int32
   a.base[0] = 0;
   a.tree = *tree;
   a.dev_status = dev_status;
+  a.prefix_len = prefix_len;
+  a.mask = mask;
+  a.posids = posids;
   return et_launch(k_rerank, dim3(cfg->B), dim3(kRrThreads), 0, (cudaStream_t)stream, 0, a);
+}
+
+extern "C" et_status et_tree_rerank(const et_tree_cfg *cfg, et_tree *tree, int32_t *dev_status, et_stream_t stream) {
+  return launch_rerank(cfg, tree, dev_status, nullptr, nullptr, nullptr, stream);
+}
+
+extern "C" et_status et_tree_rerank_mask(const et_tree_cfg *cfg, et_tree *tree, const int32_t *prefix_len,
+                                         uint64_t *mask, int32_t *posids, int32_t *dev_status, et_stream_t stream) {
+  ET_RETURN_IF(!prefix_len || !mask || !posids, ET_ERR_INVALID_ARG);
+  ET_RETURN_IF(!et_aligned(mask, 8), ET_ERR_INVALID_ARG);
+  return launch_rerank(cfg, tree, dev_status, prefix_len, mask, posids, stream);
 }
 
 extern "C" et_status et_tree_mask_posids(const et_tree_cfg *cfg, const et_tree *tree, const int32_t *prefix_len,

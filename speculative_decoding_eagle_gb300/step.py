@@ -139,8 +139,8 @@ class VerifyStep:
         for layer in range(self.cfg.depth):
             E.et_tree_expand(self.cfg, layer, inp.draft, self.tree, self.ws, row_of_node=inp.row_of_node,
                              dev_status=self.dev_status, stream=stream)
-        E.et_tree_rerank(self.cfg, self.tree, dev_status=self.dev_status, stream=stream)
-        E.et_tree_mask_posids(self.cfg, self.tree, inp.prefix_len, self.mask, self.posids, stream=stream)
+        E.et_tree_rerank_mask(self.cfg, self.tree, inp.prefix_len, self.mask, self.posids, dev_status=self.dev_status,
+                              stream=stream)
 
     def attention(self, inp: StepInputs, stream=None) -> None:
         E.et_tree_attention(self.shape, inp.q, inp.k_prefix, inp.v_prefix, inp.kv_row0, inp.prefix_len,
@@ -156,12 +156,12 @@ class VerifyStep:
                            dev_status=self.dev_status, stream=stream)
 
     def run(self, inp: StepInputs, stream=None) -> None:
-        """The whole step: D expands, rerank, mask/posids, attention, acceptance."""
+        """The whole step: D expands, rerank with mask/posids (one launch), attention, acceptance."""
         self.prepare(inp)
         self.build_tree(inp, stream)
         self.attention(inp, stream)
         self.accept(inp, stream)
 
     def launches(self) -> int:
-        """Kernel launches of one step."""
-        return self.cfg.depth + 4
+        """Kernel launches of one step: D expands, rerank with mask, attention, acceptance."""
+        return self.cfg.depth + 3

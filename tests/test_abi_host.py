@@ -136,6 +136,18 @@ def test_verify_argument_checks(lib):
     assert call(wsb=need - 1) == E.ET_ERR_WORKSPACE
 
 
+def test_rerank_mask_argument_checks(lib):
+    cfg = E.TreeCfg(B=1, V=1000, depth=3, topk=4, m=4, n=10)
+    tree = E.TreeC(*([FAKE] * 10))
+    call = lambda pl=FAKE, mask=FAKE, pos=FAKE, c=cfg: lib.et_tree_rerank_mask(
+        ctypes.byref(c.c()), ctypes.byref(tree), pl, mask, pos, None, None)
+    assert call(pl=None) == E.ET_ERR_INVALID_ARG
+    assert call(mask=None) == E.ET_ERR_INVALID_ARG
+    assert call(pos=None) == E.ET_ERR_INVALID_ARG
+    assert call(mask=FAKE + 4) == E.ET_ERR_INVALID_ARG   # mask words need 8-byte alignment
+    assert call(c=E.TreeCfg(B=1, V=1000, depth=3, topk=4, m=4, n=200)) == E.ET_ERR_INVALID_ARG
+
+
 def test_status_strings(lib):
     for s in range(6):
         assert E.status_string(s)

@@ -170,6 +170,19 @@ def test_rerank_mask_posids_match_oracle(B, D, k, m, n, ties):
     om, op = O.mask_posids(ot.flat_parent, ot.flat_depth, prefix)
     np.testing.assert_array_equal(mask.cpu().numpy().view(np.uint64), om)
     np.testing.assert_array_equal(pos.cpu().numpy(), op)
+    # the fused call writes the same flat tree, mask and positions in one launch
+    for buf in (tb.flat_node, tb.flat_tok, tb.flat_parent, tb.flat_depth):
+        buf.fill_(-5)
+    mask.fill_(-1)
+    pos.fill_(-1)
+    E.et_tree_rerank_mask(cfg, tb, torch.from_numpy(prefix).cuda(), mask, pos, dev_status=status)
+    g = gpu_tree_np(tb)
+    for name, want in (("flat_node", ot.flat_node), ("flat_tok", ot.flat_tok), ("flat_parent", ot.flat_parent),
+                       ("flat_depth", ot.flat_depth)):
+        np.testing.assert_array_equal(g[name], want, err_msg="fused " + name)
+    np.testing.assert_array_equal(mask.cpu().numpy().view(np.uint64), om)
+    np.testing.assert_array_equal(pos.cpu().numpy(), op)
+    assert int(status.item()) == 0
 
 
 # ---------------------------------------------------------------------------
