@@ -354,6 +354,9 @@ def run_gpu(args):
     hbm_peak, bf16_peak, peak_src = _peaks()
     achieved = attn_b / (attn_us * 1e-6) / 1e9
 
+    # ---- KV commit of the accepted paths (the step after acceptance), timed alone ----
+    commit = time_kv_commit(st, sets[0], wl, cfg, prefix, stream, K)
+
     # ---- end to end through the public API with host buffers ----
     e2e = run_e2e(args, st, sets, wl, stream)
 
@@ -380,6 +383,7 @@ def run_gpu(args):
                      recorded_attention_traffic(wl.name, cfg.B, int(prefix.max())),
                      "peak_source": peak_src, "kernel": "et_tree_attention"},
         "e2e": e2e,
+        "kv_commit": commit,
         "gpu_launches": launches,
         "clocks": clk.summary(),
     }
@@ -393,6 +397,50 @@ def run_gpu(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+def time_kv_commit(st, inp, wl, cfg, prefix, stream, K):
+    """et_kv_commit of the accepted paths of one step into caches with room
+    for them; algorithmic bytes = read + write of the committed K/V rows."""
+    import torch
+    from speculative_decoding_eagle_gb300 import binding as E
+    B, Hkv, d = cfg.B, wl.Hkv, wl.d
+    dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    cap = int(prefix.max()) + wl.depth + 1
+    kc = torch.zeros((B * Hkv * cap, d), dtype=dt, device="cuda")
+    vc = torch.zeros_like(kc)
+    kv_row0 = torch.arange(B, dtype=torch.int64, device="cuda") * Hkv * cap
+    new_len = torch.zeros(B, dtype=torch.int32, device="cuda")
+    shape = E.CommitShape(B=B, N=cfg.N, Hkv=Hkv, d=d, path_len=wl.depth + 1,
+                          dtype=E.ET_BF16 if wl.dtype == "bf16" else E.ET_F32, kv_head_stride=cap,
+                          kv_rows=B * Hkv * cap)
+    with torch.cuda.stream(stream):
+        st.run(inp, stream=stream)
+    stream.synchronize()
+
+    def one():
+        E.et_kv_commit(shape, inp.k_tree, inp.v_tree, st.accept_len, st.path, kc, vc, kv_row0, inp.prefix_len,
+                       new_len, dev_status=st.dev_status, stream=stream)
+    with torch.cuda.stream(stream):
+        one()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(K):
+            one()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream()
+    e0.record(cur)
+    g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / K
+    rows = int(st.accept_len.sum().item()) + B
+    nbytes = rows * Hkv * d * kc.element_size() * 2 * 2
+    return {"us_per_launch": round(us, 3), "rows_committed": rows, "bytes": nbytes,
+            "GBps": round(nbytes / (us * 1e-6) / 1e9, 2), "bound": "latency (a few KB per sequence)"}
 
 
 def run_e2e(args, st, sets, wl, stream):

@@ -12,6 +12,7 @@
  *     (or et_tree_rerank_mask: both in one launch)
  *   et_tree_attention  (inside each target layer)   (ancestor-masked attention)
  *   et_verify_accept                                (lossless acceptance)
+ *   et_kv_commit                                    (accepted rows -> KV cache)
  *
  * Conventions shared by every call
  * --------------------------------
@@ -126,6 +127,16 @@ typedef struct {
                                  1 = mma.sync tensor-core path, 2 = tcgen05 path
                                  (ET_ERR_UNSUPPORTED unless bf16 and d = 128) */
 } et_attn_shape;
+
+/* KV commit shape (host struct), see et_kv_commit. */
+typedef struct {
+    int32_t B, N, Hkv, d;     /* as in et_attn_shape; d * sizeof(dtype) a multiple of 16 bytes */
+    int32_t path_len;         /* D + 1 (columns of path), <= 17 */
+    et_dtype dtype;           /* of k/v tree, the caches and the features */
+    int64_t kv_head_stride;   /* rows between heads of one sequence's cache = its capacity (> 0) */
+    int64_t kv_rows;          /* d-element rows in each of k_cache / v_cache (bounds check) */
+    int32_t feat_dim;         /* F: elements per feature row (0 = no features); F * sizeof(dtype) % 16 == 0 */
+} et_commit_shape;
 
 /* ---- geometry helpers (host, no device work) ---- */
 
@@ -313,6 +324,37 @@ et_status et_verify_accept(const et_tree_cfg *cfg, et_accept_mode mode, const et
                            const float *uniforms,
                            int32_t *accept_len, int32_t *path, int32_t *tokens,
                            int32_t *dev_status, void *ws, size_t ws_bytes, et_stream_t stream);
+
+/*
+ * et_kv_commit -- after acceptance, append the accepted path to the KV cache
+ * (EAGLE-2 article: the flattened tree's row 0 is the root and every row
+ * attends the prefix plus its ancestors; EAGLE blog 1.1: the accepted tokens
+ * of one verification forward are kept, the bonus token starts the next step).
+ *
+ * For each sequence b with A = accept_len[b] and rows r_i = path[b, i]
+ * (r_0 = 0, the root), i = 0..A:
+ *   k_cache/v_cache row kv_row0[b] + g * kv_head_stride + prefix_len[b] + i
+ *       <- k_tree/v_tree[b, r_i, g, :]            for every KV head g,
+ *   feat_out[b, i, :] <- features[b, r_i, :]      (rows i > A are zeroed),
+ *   new_prefix_len[b] = prefix_len[b] + A + 1.
+ *
+ * k_tree, v_tree  [B, N, Hkv, d] (the K/V the target forward computed for the
+ *                 flattened tree, already rotated).
+ * accept_len, path  outputs of et_verify_accept.
+ * k_cache, v_cache  rows of d elements; each sequence's heads are
+ *                 kv_head_stride rows apart (its capacity); written in place.
+ * kv_row0, prefix_len  as in et_tree_attention; prefix_len is read only.
+ * new_prefix_len  int32 [B], must not alias prefix_len.
+ * features, feat_out  [B, N, F] and [B, D+1, F] (nullable when feat_dim = 0):
+ *                 the target hidden states the draft model reads next.
+ * Tensors 16-byte aligned.  A path row outside [0, N), an accept_len outside
+ * [0, D], or a position past the capacity sets ET_DEV_BAD_INDEX and that row
+ * (or sequence) is skipped.  No workspace.
+ */
+et_status et_kv_commit(const et_commit_shape *shape, const void *k_tree, const void *v_tree,
+                       const int32_t *accept_len, const int32_t *path, void *k_cache, void *v_cache,
+                       const int64_t *kv_row0, const int32_t *prefix_len, int32_t *new_prefix_len,
+                       const void *features, void *feat_out, int32_t *dev_status, et_stream_t stream);
 
 #ifdef __cplusplus
 }

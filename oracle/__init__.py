@@ -8,3 +8,4 @@ it; the library never does, and it never imports the library.
 from .eagle_tree_oracle import *  # noqa: F401,F403
 from .eagle_tree_oracle import (TreeCfg, Tree, AcceptResult, GREEDY, STOCH_POINT, STOCH_DRAFTQ,  # noqa: F401
                                 FRAC_BITS, KEY_MIN)
+from .kv_commit_oracle import kv_commit  # noqa: F401

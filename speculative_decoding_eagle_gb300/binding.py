@@ -28,7 +28,7 @@ ATTN_AUTO, ATTN_MMA_SYNC, ATTN_TCGEN05 = 0, 1, 2
 EXPORTED = ("et_num_candidates", "et_layer_expanded", "et_layer_base", "et_tree_workspace_size",
             "et_tree_attention_workspace_size", "et_tree_attention_splits", "et_workspace_init",
             "et_status_string", "et_abi_version", "et_tree_expand", "et_tree_expand_noalloc", "et_tree_rerank", "et_tree_rerank_mask",
-            "et_tree_mask_posids", "et_tree_attention", "et_verify_accept")
+            "et_tree_mask_posids", "et_tree_attention", "et_verify_accept", "et_kv_commit")
 
 
 class TreeCfgC(ctypes.Structure):
@@ -45,6 +45,11 @@ class AttnShapeC(ctypes.Structure):
     _fields_ = [("B", c_i32), ("N", c_i32), ("Hq", c_i32), ("Hkv", c_i32), ("d", c_i32), ("dtype", c_i32),
                 ("scale", c_f32), ("max_prefix", c_i32), ("kv_rows", c_i64), ("kv_head_stride", c_i64),
                 ("num_splits", c_i32), ("impl", c_i32)]
+
+
+class CommitShapeC(ctypes.Structure):
+    _fields_ = [("B", c_i32), ("N", c_i32), ("Hkv", c_i32), ("d", c_i32), ("path_len", c_i32), ("dtype", c_i32),
+                ("kv_head_stride", c_i64), ("kv_rows", c_i64), ("feat_dim", c_i32)]
 
 
 class EtError(RuntimeError):
@@ -83,6 +88,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "et_tree_mask_posids": (c_i32, [P(TreeCfgC), P(TreeC), c_vp, c_vp, c_vp, c_vp]),
         "et_tree_attention": (c_i32, [P(AttnShapeC), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                       c_vp, c_vp, c_sz, c_vp]),
+        "et_kv_commit": (c_i32, [P(CommitShapeC), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                 c_vp, c_vp]),
         "et_verify_accept": (c_i32, [P(TreeCfgC), c_i32, P(TreeC), c_vp, c_i64, c_vp, c_vp, c_i64, c_vp, c_vp,
                                      c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
     }
@@ -324,3 +331,37 @@ def et_verify_accept(cfg: TreeCfg, mode: int, tree: TreeBuffers, target_logits: 
         _ptr(tokens, torch.int32, "tokens"), _ptr(dev_status, torch.int32, "dev_status"), _ptr(ws, None, "ws"),
         ws.numel() * ws.element_size(), _stream(stream))
     _check("et_verify_accept", st)
+
+
+@dataclasses.dataclass(frozen=True)
+class CommitShape:
+    B: int
+    N: int
+    Hkv: int
+    d: int
+    path_len: int
+    dtype: int = ET_BF16
+    kv_head_stride: int = 0
+    kv_rows: int = 0
+    feat_dim: int = 0
+
+    def c(self) -> CommitShapeC:
+        return CommitShapeC(self.B, self.N, self.Hkv, self.d, self.path_len, self.dtype, self.kv_head_stride,
+                            self.kv_rows, self.feat_dim)
+
+
+def et_kv_commit(shape: CommitShape, k_tree: torch.Tensor, v_tree: torch.Tensor, accept_len: torch.Tensor,
+                 path: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, kv_row0: torch.Tensor,
+                 prefix_len: torch.Tensor, new_prefix_len: torch.Tensor, features: Optional[torch.Tensor] = None,
+                 feat_out: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None,
+                 stream=None) -> None:
+    """Append each sequence's accepted path (root first) to the KV cache and gather its features."""
+    dt = torch.bfloat16 if shape.dtype == ET_BF16 else torch.float32
+    st = load().et_kv_commit(
+        ctypes.byref(shape.c()), _ptr(k_tree, dt, "k_tree"), _ptr(v_tree, dt, "v_tree"),
+        _ptr(accept_len, torch.int32, "accept_len"), _ptr(path, torch.int32, "path"),
+        _ptr(k_cache, dt, "k_cache"), _ptr(v_cache, dt, "v_cache"), _ptr(kv_row0, torch.int64, "kv_row0"),
+        _ptr(prefix_len, torch.int32, "prefix_len"), _ptr(new_prefix_len, torch.int32, "new_prefix_len"),
+        _ptr(features, dt, "features"), _ptr(feat_out, dt, "feat_out"), _ptr(dev_status, torch.int32, "dev_status"),
+        _stream(stream))
+    _check("et_kv_commit", st)

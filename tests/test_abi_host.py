@@ -148,6 +148,27 @@ def test_rerank_mask_argument_checks(lib):
     assert call(c=E.TreeCfg(B=1, V=1000, depth=3, topk=4, m=4, n=200)) == E.ET_ERR_INVALID_ARG
 
 
+def test_kv_commit_argument_checks(lib):
+    def shape(**kw):
+        s = dict(B=2, N=61, Hkv=32, d=128, path_len=7, dtype=E.ET_BF16, kv_head_stride=4096, kv_rows=2 * 32 * 4096,
+                 feat_dim=0)
+        s.update(kw)
+        return E.CommitShapeC(*s.values())
+
+    def call(sh, kt=FAKE, npl=FAKE + 256, feat=None, fout=None):
+        return lib.et_kv_commit(ctypes.byref(sh), kt, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, npl, feat, fout,
+                                None, None)
+    assert call(shape(d=100)) == E.ET_ERR_UNSUPPORTED            # rows must be whole 16-byte chunks
+    assert call(shape(dtype=7)) == E.ET_ERR_INVALID_ARG
+    assert call(shape(path_len=18)) == E.ET_ERR_INVALID_ARG      # depth <= 16
+    assert call(shape(N=129)) == E.ET_ERR_INVALID_ARG
+    assert call(shape(kv_head_stride=0)) == E.ET_ERR_INVALID_ARG  # appending needs a capacity per head
+    assert call(shape(), kt=None) == E.ET_ERR_INVALID_ARG
+    assert call(shape(), kt=FAKE + 8) == E.ET_ERR_INVALID_ARG     # 16-byte alignment
+    assert call(shape(), npl=FAKE) == E.ET_ERR_INVALID_ARG        # new_prefix_len must not alias prefix_len
+    assert call(shape(feat_dim=4096)) == E.ET_ERR_INVALID_ARG     # features asked for, no buffers
+
+
 def test_status_strings(lib):
     for s in range(6):
         assert E.status_string(s)

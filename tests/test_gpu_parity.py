@@ -404,3 +404,81 @@ def test_step_is_deterministic_and_graph_capturable():
         g.replay()
     torch.cuda.synchronize()
     assert torch.equal(first[0], st.out) and torch.equal(first[1], st.tokens) and torch.equal(first[2], st.tree.flat_node)
+
+
+# ---------------------------------------------------------------------------
+# KV commit (the step after acceptance)
+# ---------------------------------------------------------------------------
+COMMIT_CASES = [  # (B, N, Hkv, d, depth, dtype, F)
+    (3, 17, 4, 64, 4, "f32", 64),
+    (2, 61, 32, 128, 6, "bf16", 4096),
+    (4, 81, 8, 128, 8, "bf16", 0),
+]
+
+
+@pytest.mark.parametrize("B,N,Hkv,d,D,dtype,F", COMMIT_CASES)
+def test_kv_commit_matches_oracle(B, N, Hkv, d, D, dtype, F):
+    rng = np.random.default_rng(B * 1000 + N)
+    np_dt = np.float32
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    cap = 300
+    prefix = rng.integers(0, cap - D - 1, B).astype(np.int32)
+    kv_row0 = (np.arange(B) * Hkv * cap).astype(np.int64)
+    rows = B * Hkv * cap
+    # accepted paths: a root-first chain of increasing flat rows, lengths 0..D
+    alen = rng.integers(0, D + 1, B).astype(np.int32)
+    alen[0] = D
+    path = np.full((B, D + 1), -1, np.int32)
+    for b in range(B):
+        path[b, 0] = 0
+        path[b, 1:alen[b] + 1] = np.sort(rng.choice(np.arange(1, N), alen[b], replace=False))
+
+    def rnd(*shape):  # values exactly representable in the compute dtype
+        x = rng.standard_normal(shape).astype(np_dt)
+        return torch.from_numpy(x).to(tdt).float().numpy()
+    kt, vt, kc, vc = rnd(B, N, Hkv, d), rnd(B, N, Hkv, d), rnd(rows, d), rnd(rows, d)
+    feats = rnd(B, N, F) if F else None
+    okc, ovc, olen, ofe = O.kv_commit(kt, vt, alen, path, kc, vc, kv_row0, prefix, cap, feats)
+    dev = lambda x: torch.from_numpy(x).cuda()
+    dkc, dvc = dev(kc).to(tdt), dev(vc).to(tdt)
+    new_len = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+    fout = torch.full((B, D + 1, F), 5.0, dtype=tdt, device="cuda") if F else None
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    shape = E.CommitShape(B=B, N=N, Hkv=Hkv, d=d, path_len=D + 1, dtype=E.ET_BF16 if dtype == "bf16" else E.ET_F32,
+                          kv_head_stride=cap, kv_rows=rows, feat_dim=F)
+    E.et_kv_commit(shape, dev(kt).to(tdt), dev(vt).to(tdt), dev(alen), dev(path), dkc, dvc, dev(kv_row0),
+                   dev(prefix), new_len, features=None if feats is None else dev(feats).to(tdt), feat_out=fout,
+                   dev_status=status)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(dkc.float().cpu().numpy(), okc)
+    np.testing.assert_array_equal(dvc.float().cpu().numpy(), ovc)
+    np.testing.assert_array_equal(new_len.cpu().numpy(), olen)
+    if F:
+        np.testing.assert_array_equal(fout.float().cpu().numpy(), ofe)
+    assert int(status.item()) == 0
+
+
+def test_kv_commit_skips_and_flags_bad_rows():
+    B, N, Hkv, d, D, cap = 2, 9, 2, 64, 3, 6
+    tdt = torch.float32
+    kt = torch.randn(B, N, Hkv, d, device="cuda")
+    vt = torch.randn(B, N, Hkv, d, device="cuda")
+    kc = torch.zeros(B * Hkv * cap, d, device="cuda")
+    vc = torch.zeros_like(kc)
+    kv_row0 = torch.tensor([0, Hkv * cap], dtype=torch.int64, device="cuda")
+    prefix = torch.tensor([1, 4], dtype=torch.int32, device="cuda")   # sequence 1: only 2 free slots
+    alen = torch.tensor([2, 3], dtype=torch.int32, device="cuda")
+    path = torch.tensor([[0, 3, 99, -1], [0, 1, 2, 5]], dtype=torch.int32, device="cuda")  # 99 is no row
+    new_len = torch.zeros(B, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    shape = E.CommitShape(B=B, N=N, Hkv=Hkv, d=d, path_len=D + 1, dtype=E.ET_F32, kv_head_stride=cap,
+                          kv_rows=B * Hkv * cap)
+    E.et_kv_commit(shape, kt, vt, alen, path, kc, vc, kv_row0, prefix, new_len, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & E.ET_DEV_BAD_INDEX
+    # valid rows landed, the bad ones were skipped
+    assert torch.equal(kc[0 * cap + 1], kt[0, 0, 0]) and torch.equal(kc[1 * cap + 2], kt[0, 3, 1])
+    assert torch.count_nonzero(kc[0 * cap + 3]) == 0               # row 99 skipped
+    assert torch.equal(kc[Hkv * cap + 0 * cap + 4], kt[1, 0, 0])   # positions 4 and 5 fit
+    assert torch.equal(kc[Hkv * cap + 0 * cap + 5], kt[1, 1, 0])
+    assert new_len.cpu().tolist() == [4, 8]

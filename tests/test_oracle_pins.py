@@ -551,3 +551,33 @@ def test_uniform_slot_usage():
         u2[0, s] = 1.0 - u2[0, s]
         r = O.verify_accept(cfg, O.STOCH_POINT, tok, par, node, z, None, uniforms=u2)
         assert (r.tokens == base.tokens).all()
+
+
+# ---------------------------------------------------------------------------
+# KV commit after acceptance: the root row and the accepted rows, in path
+# order, land at prefix_len.. of every head; values typed out by hand
+# ---------------------------------------------------------------------------
+def test_kv_commit_hand_example():
+    B, N, Hkv = 2, 4, 2
+    k_tree = np.zeros((B, N, Hkv, 1), np.float32)
+    for b in range(B):
+        for r in range(N):
+            for g in range(Hkv):
+                k_tree[b, r, g, 0] = 100 * b + 10 * r + g
+    v_tree = -k_tree
+    path = np.array([[0, 2, 3], [0, -1, -1]], np.int32)
+    alen = np.array([2, 0], np.int32)
+    feats = np.array([[[0.], [1.], [2.], [3.]], [[1000.], [1001.], [1002.], [1003.]]], np.float32)
+    cache = np.full((32, 1), 7.0, np.float32)
+    kc, vc, new_len, fo = O.kv_commit(k_tree, v_tree, alen, path, cache, cache, np.array([0, 16]),
+                                      np.array([3, 5], np.int32), 8, feats)
+    want = np.full(32, 7.0, np.float32)
+    want[[3, 4, 5]] = [0, 20, 30]      # sequence 0, head 0: rows 0, 2, 3 at positions 3, 4, 5
+    want[[11, 12, 13]] = [1, 21, 31]   # sequence 0, head 1 (8 rows further)
+    want[21] = 100                     # sequence 1 (base row 16), head 0: the root at position 5
+    want[29] = 101                     # sequence 1, head 1
+    np.testing.assert_array_equal(kc[:, 0], want)
+    np.testing.assert_array_equal(vc[:, 0], np.where(want == 7.0, 7.0, -want))
+    assert list(new_len) == [6, 6]
+    np.testing.assert_array_equal(fo[:, :, 0], [[0, 2, 3], [1000, 0, 0]])
+    assert cache[3, 0] == 7.0  # inputs untouched
