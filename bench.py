@@ -357,6 +357,9 @@ def run_gpu(args):
     # ---- KV commit of the accepted paths (the step after acceptance), timed alone ----
     commit = time_kv_commit(st, sets[0], wl, cfg, prefix, stream, K)
 
+    # ---- a static draft tree of the same size, flattened from the same draft table ----
+    static = time_static_tree(wl, cfg, sets[0], stream, K)
+
     # ---- end to end through the public API with host buffers ----
     e2e = run_e2e(args, st, sets, wl, stream)
 
@@ -384,6 +387,7 @@ def run_gpu(args):
                      "peak_source": peak_src, "kernel": "et_tree_attention"},
         "e2e": e2e,
         "kv_commit": commit,
+        "static_tree": static,
         "gpu_launches": launches,
         "clocks": clk.summary(),
     }
@@ -441,6 +445,51 @@ def time_kv_commit(st, inp, wl, cfg, prefix, stream, K):
     nbytes = rows * Hkv * d * kc.element_size() * 2 * 2
     return {"us_per_launch": round(us, 3), "rows_committed": rows, "bytes": nbytes,
             "GBps": round(nbytes / (us * 1e-6) / 1e9, 2), "bound": "latency (a few KB per sequence)"}
+
+
+STATIC_WIDTHS = (4, 2, 2, 1, 1)  # 61 flat rows, the size of the 7B dynamic tree
+
+
+def time_static_tree(wl, cfg, inp, stream, K):
+    """et_static_tree over the step's draft table (one launch per step)."""
+    import numpy as np
+    import torch
+    from speculative_decoding_eagle_gb300 import binding as E
+    from speculative_decoding_eagle_gb300 import workloads as W
+    if wl.V > 32768:
+        return None
+    parent, rank = W.static_shape(STATIC_WIDTHS)
+    B, N = cfg.B, parent.size
+    per_seq = inp.draft.shape[0] // B
+    if per_seq < N:
+        return None
+    rmap = torch.from_numpy((np.arange(B)[:, None] * per_seq + np.arange(N)[None, :]).astype(np.int32)).cuda()
+    tb = E.TreeBuffers.allocate_flat(B, N, root_tok=inp.root_tok)
+    par_d, rank_d = torch.from_numpy(parent).cuda(), torch.from_numpy(rank).cuda()
+    k = max(STATIC_WIDTHS)
+
+    def one():
+        E.et_static_tree(B, wl.V, k, par_d, rank_d, inp.draft, rmap, tb, stream=stream)
+    with torch.cuda.stream(stream):
+        one()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(K):
+            one()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream()
+    e0.record(cur)
+    g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / K
+    internal = int(np.unique(parent[1:]).size)
+    nbytes = B * internal * wl.V * 4
+    return {"widths": list(STATIC_WIDTHS), "rows": N, "us_per_launch": round(us, 3), "bytes": nbytes,
+            "GBps": round(nbytes / (us * 1e-6) / 1e9, 1), "bound": "latency at batch 1"}
 
 
 def run_e2e(args, st, sets, wl, stream):

@@ -7,6 +7,7 @@
  * A100") describes it, is:
  *
  *   for layer = 0 .. depth-1:  et_tree_expand      (expansion phase)
+ *     (or et_static_tree: a fixed tree shape, EAGLE-1 / Medusa style)
  *   et_tree_rerank                                  (reranking phase, flatten)
  *   et_tree_mask_posids                             (attention mask, positions)
  *     (or et_tree_rerank_mask: both in one launch)
@@ -127,6 +128,13 @@ typedef struct {
                                  1 = mma.sync tensor-core path, 2 = tcgen05 path
                                  (ET_ERR_UNSUPPORTED unless bf16 and d = 128) */
 } et_attn_shape;
+
+/* Static draft tree configuration (host struct), see et_static_tree. */
+typedef struct {
+    int32_t B, V;   /* sequences, vocabulary (V <= 32768) */
+    int32_t N;      /* flat rows including the root, <= 128 */
+    int32_t topk;   /* ranks used: every rank[i] < topk <= 32 */
+} et_static_cfg;
 
 /* KV commit shape (host struct), see et_kv_commit. */
 typedef struct {
@@ -324,6 +332,31 @@ et_status et_verify_accept(const et_tree_cfg *cfg, et_accept_mode mode, const et
                            const float *uniforms,
                            int32_t *accept_len, int32_t *path, int32_t *tokens,
                            int32_t *dev_status, void *ws, size_t ws_bytes, et_stream_t stream);
+
+/*
+ * et_static_tree -- a static draft tree (EAGLE-1 / Medusa style, which the
+ * EAGLE-2 article contrasts with its dynamic tree): the shape is fixed in
+ * advance as flat rows, row 0 the root and row i > 0 a child of row
+ * parent[i] < i with rank rank[i]; row i's token is the rank[i]-th best
+ * token (largest draft logit first, lower id on ties) of the draft logits at
+ * its parent.  Writes tree->flat_tok / flat_parent / flat_depth / flat_node
+ * (node = row - 1, root -1; flat_tok[:, 0] = root_tok), the same flattened
+ * tree et_tree_rerank produces, so et_tree_mask_posids, et_tree_attention,
+ * et_verify_accept (maps indexed by node + 1 = flat row) and et_kv_commit
+ * apply unchanged.
+ *
+ * parent, rank  int32 [N] (device), parent[0] = -1, 0 <= rank[i] < topk.
+ * logits        fp32 draft table, row_stride >= V.
+ * row_of_flat   int32 [B, N]: table row of each flat row's draft logits
+ *               (read only for rows that have children).
+ * A malformed shape (a parent not preceding its child, a rank outside
+ * [0, topk), a negative table row) sets ET_DEV_BAD_INDEX; the affected
+ * tokens are -1.  One thread-block cluster of ceil(V / 4096) blocks per
+ * (sequence, flat row).  No workspace.
+ */
+et_status et_static_tree(const et_static_cfg *cfg, const int32_t *parent, const int32_t *rank,
+                         const float *logits, int64_t row_stride, const int32_t *row_of_flat,
+                         et_tree *tree, int32_t *dev_status, et_stream_t stream);
 
 /*
  * et_kv_commit -- after acceptance, append the accepted path to the KV cache

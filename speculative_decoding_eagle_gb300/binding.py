@@ -28,7 +28,7 @@ ATTN_AUTO, ATTN_MMA_SYNC, ATTN_TCGEN05 = 0, 1, 2
 EXPORTED = ("et_num_candidates", "et_layer_expanded", "et_layer_base", "et_tree_workspace_size",
             "et_tree_attention_workspace_size", "et_tree_attention_splits", "et_workspace_init",
             "et_status_string", "et_abi_version", "et_tree_expand", "et_tree_expand_noalloc", "et_tree_rerank", "et_tree_rerank_mask",
-            "et_tree_mask_posids", "et_tree_attention", "et_verify_accept", "et_kv_commit")
+            "et_tree_mask_posids", "et_tree_attention", "et_verify_accept", "et_kv_commit", "et_static_tree")
 
 
 class TreeCfgC(ctypes.Structure):
@@ -45,6 +45,10 @@ class AttnShapeC(ctypes.Structure):
     _fields_ = [("B", c_i32), ("N", c_i32), ("Hq", c_i32), ("Hkv", c_i32), ("d", c_i32), ("dtype", c_i32),
                 ("scale", c_f32), ("max_prefix", c_i32), ("kv_rows", c_i64), ("kv_head_stride", c_i64),
                 ("num_splits", c_i32), ("impl", c_i32)]
+
+
+class StaticCfgC(ctypes.Structure):
+    _fields_ = [("B", c_i32), ("V", c_i32), ("N", c_i32), ("topk", c_i32)]
 
 
 class CommitShapeC(ctypes.Structure):
@@ -88,6 +92,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "et_tree_mask_posids": (c_i32, [P(TreeCfgC), P(TreeC), c_vp, c_vp, c_vp, c_vp]),
         "et_tree_attention": (c_i32, [P(AttnShapeC), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                       c_vp, c_vp, c_sz, c_vp]),
+        "et_static_tree": (c_i32, [P(StaticCfgC), c_vp, c_vp, c_vp, c_i64, c_vp, P(TreeC), c_vp, c_vp]),
         "et_kv_commit": (c_i32, [P(CommitShapeC), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                  c_vp, c_vp]),
         "et_verify_accept": (c_i32, [P(TreeCfgC), c_i32, P(TreeC), c_vp, c_i64, c_vp, c_vp, c_i64, c_vp, c_vp,
@@ -196,6 +201,15 @@ class TreeBuffers:
                            torch.full((B, cfg.m), -1, **i32), torch.full((B, N), -1, **i32),
                            torch.full((B, N), -1, **i32), torch.full((B, N), -1, **i32),
                            torch.zeros((B, N), **i32), root_tok)
+
+    @staticmethod
+    def allocate_flat(B: int, N: int, device="cuda", root_tok: Optional[torch.Tensor] = None) -> "TreeBuffers":
+        """Only the flattened [B, N] arrays (a static tree has no candidate arrays)."""
+        i32 = dict(dtype=torch.int32, device=device)
+        one = lambda dt: torch.zeros(1, dtype=dt, device=device)
+        return TreeBuffers(None, one(torch.int32), one(torch.int32), one(torch.float32), one(torch.int64),
+                           one(torch.int32), torch.full((B, N), -1, **i32), torch.full((B, N), -1, **i32),
+                           torch.full((B, N), -1, **i32), torch.zeros((B, N), **i32), root_tok)
 
     def c(self) -> TreeC:
         return TreeC(_ptr(self.cand_tok, torch.int32), _ptr(self.cand_parent, torch.int32),
@@ -365,3 +379,17 @@ def et_kv_commit(shape: CommitShape, k_tree: torch.Tensor, v_tree: torch.Tensor,
         _ptr(features, dt, "features"), _ptr(feat_out, dt, "feat_out"), _ptr(dev_status, torch.int32, "dev_status"),
         _stream(stream))
     _check("et_kv_commit", st)
+
+
+def et_static_tree(B: int, V: int, topk: int, parent: torch.Tensor, rank: torch.Tensor, logits: torch.Tensor,
+                   row_of_flat: torch.Tensor, tree: "TreeBuffers", dev_status: Optional[torch.Tensor] = None,
+                   stream=None) -> None:
+    """Flatten a static draft tree (fixed parent / rank per flat row) from the draft logits at each parent."""
+    if logits.dim() != 2 or logits.stride(1) != 1 or logits.dtype != torch.float32 or not logits.is_cuda:
+        raise ValueError("logits must be a CUDA fp32 [rows, >=V] table with unit inner stride")
+    N = parent.numel()
+    st = load().et_static_tree(ctypes.byref(StaticCfgC(B, V, N, topk)), _ptr(parent, torch.int32, "parent"),
+                               _ptr(rank, torch.int32, "rank"), logits.data_ptr(), logits.stride(0),
+                               _ptr(row_of_flat, torch.int32, "row_of_flat"), ctypes.byref(tree.c()),
+                               _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check("et_static_tree", st)

@@ -25,7 +25,7 @@ regenerated alone.
 from __future__ import annotations
 
 import dataclasses
-from typing import Dict, Optional, Tuple
+from typing import Dict, Optional, Sequence, Tuple
 
 import numpy as np
 
@@ -196,3 +196,20 @@ def root_tokens(wl: Workload, B: Optional[int] = None) -> np.ndarray:
     """Token id of each sequence's root (the last accepted token)."""
     B = wl.B if B is None else B
     return _rng(wl.seed, 0x7007).integers(0, wl.V, B).astype(np.int32)
+
+
+def static_shape(widths: Sequence[int]):
+    """A static draft tree's shape as flat rows: every node at depth d gets
+    widths[d] children with ranks 0..widths[d]-1, rows numbered depth by
+    depth (parents first).  Returns (parent, rank) int32 [N], parent[0] = -1."""
+    parent, rank = [-1], [-1]
+    level = [0]
+    for w in widths:
+        nxt = []
+        for p in level:
+            for r in range(w):
+                parent.append(p)
+                rank.append(r)
+                nxt.append(len(parent) - 1)
+        level = nxt
+    return np.asarray(parent, np.int32), np.asarray(rank, np.int32)

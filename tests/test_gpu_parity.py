@@ -482,3 +482,84 @@ def test_kv_commit_skips_and_flags_bad_rows():
     assert torch.equal(kc[Hkv * cap + 0 * cap + 4], kt[1, 0, 0])   # positions 4 and 5 fit
     assert torch.equal(kc[Hkv * cap + 0 * cap + 5], kt[1, 1, 0])
     assert new_len.cpu().tolist() == [4, 8]
+
+
+# ---------------------------------------------------------------------------
+# static draft tree (fixed shape) -> flat tree -> verification
+# ---------------------------------------------------------------------------
+STATIC_CASES = [  # (B, V, widths, ties)
+    (2, 1000, (3, 2, 1), False),
+    (2, 32000, (4, 2, 2, 1, 1), False),
+    (3, 300, (8, 4), True),
+    (1, 5000, (1, 1, 1, 1), False),
+]
+
+
+def _static_case(B, V, widths, ties, seed=11):
+    parent, rank = W.static_shape(widths)
+    N = parent.size
+    table = _random_table(B * N, V, seed=seed + V, ties=ties)
+    rmap = (np.arange(B)[:, None] * N + np.arange(N)[None, :]).astype(np.int32)
+    root = (np.arange(B) + 3).astype(np.int32)
+    return parent, rank, table, rmap, root
+
+
+@pytest.mark.parametrize("B,V,widths,ties", STATIC_CASES)
+def test_static_tree_matches_oracle(B, V, widths, ties):
+    parent, rank, table, rmap, root = _static_case(B, V, widths, ties)
+    N, k = parent.size, max(widths)
+    tb = E.TreeBuffers.allocate_flat(B, N, root_tok=torch.from_numpy(root).cuda())
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    E.et_static_tree(B, V, k, torch.from_numpy(parent).cuda(), torch.from_numpy(rank).cuda(),
+                     torch.from_numpy(table).cuda(), torch.from_numpy(rmap).cuda(), tb, dev_status=status)
+    g = gpu_tree_np(tb)
+    tok, fpar, fdep, node = O.static_tree(parent, rank, table, rmap, root)
+    np.testing.assert_array_equal(g["flat_tok"], tok)
+    np.testing.assert_array_equal(g["flat_parent"], fpar)
+    np.testing.assert_array_equal(g["flat_depth"], fdep)
+    np.testing.assert_array_equal(g["flat_node"], node)
+    assert int(status.item()) == 0
+
+
+def test_static_tree_then_mask_and_greedy_acceptance():
+    B, V, widths = 3, 32000, (4, 2, 2, 1, 1)
+    parent, rank, table, rmap, root = _static_case(B, V, widths, False, seed=3)
+    N, D = parent.size, len(widths)
+    tb = E.TreeBuffers.allocate_flat(B, N, root_tok=torch.from_numpy(root).cuda())
+    E.et_static_tree(B, V, max(widths), torch.from_numpy(parent).cuda(), torch.from_numpy(rank).cuda(),
+                     torch.from_numpy(table).cuda(), torch.from_numpy(rmap).cuda(), tb)
+    # target rows in flat order: the target agrees with the draft's top token often enough to accept a few
+    rng = np.random.default_rng(9)
+    target = (table + 0.3 * rng.standard_normal(table.shape)).astype(np.float32)
+    cfg = E.TreeCfg(B=B, V=V, depth=D, topk=4, m=4, n=N - 1)
+    prefix = np.array([10, 20, 30], np.int32)
+    mask = torch.zeros((B, N, (N + 63) // 64), dtype=torch.int64, device="cuda")
+    pos = torch.zeros((B, N), dtype=torch.int32, device="cuda")
+    E.et_tree_mask_posids(cfg, tb, torch.from_numpy(prefix).cuda(), mask, pos)
+    ws = E.new_workspace(E.et_tree_workspace_size(cfg))
+    alen = torch.zeros(B, dtype=torch.int32, device="cuda")
+    path = torch.zeros((B, D + 1), dtype=torch.int32, device="cuda")
+    toks = torch.zeros((B, D + 1), dtype=torch.int32, device="cuda")
+    E.et_verify_accept(cfg, E.ET_ACCEPT_GREEDY, tb, torch.from_numpy(target).cuda(), alen, path, toks, ws)
+    tok, fpar, fdep, node = O.static_tree(parent, rank, table, rmap, root)
+    om, op = O.mask_posids(fpar, fdep, prefix)
+    np.testing.assert_array_equal(mask.cpu().numpy().view(np.uint64), om)
+    np.testing.assert_array_equal(pos.cpu().numpy(), op)
+    ref = O.verify_accept(ocfg(cfg), O.GREEDY, tok, fpar, node, target, None)
+    np.testing.assert_array_equal(alen.cpu().numpy(), ref.accept_len)
+    np.testing.assert_array_equal(path.cpu().numpy(), ref.path)
+    np.testing.assert_array_equal(toks.cpu().numpy(), ref.tokens)
+
+
+def test_static_tree_flags_a_bad_rank():
+    parent = np.array([-1, 0, 0], np.int32)
+    rank = np.array([-1, 0, 5], np.int32)  # rank 5 with topk 2
+    table = _random_table(3, 100, seed=1)
+    tb = E.TreeBuffers.allocate_flat(1, 3)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    E.et_static_tree(1, 100, 2, torch.from_numpy(parent).cuda(), torch.from_numpy(rank).cuda(),
+                     torch.from_numpy(table).cuda(), torch.from_numpy(np.arange(3, dtype=np.int32)[None]).cuda(),
+                     tb, dev_status=status)
+    g = gpu_tree_np(tb)
+    assert int(status.item()) & E.ET_DEV_BAD_INDEX
+    assert g["flat_tok"][0, 2] == -1 and g["flat_tok"][0, 1] == int(np.argmax(table[0]))

@@ -581,3 +581,32 @@ def test_kv_commit_hand_example():
     assert list(new_len) == [6, 6]
     np.testing.assert_array_equal(fo[:, :, 0], [[0, 2, 3], [1000, 0, 0]])
     assert cache[3, 0] == 7.0  # inputs untouched
+
+
+# ---------------------------------------------------------------------------
+# static draft tree: each row's token is the rank-th best token at its parent
+# ---------------------------------------------------------------------------
+def test_static_tree_hand_example():
+    # root row 0 -> rows 1, 2 (ranks 0, 1); row 1 -> row 3 (rank 0); row 2 -> row 4 (rank 2)
+    parent = np.array([-1, 0, 0, 1, 2], np.int32)
+    rank = np.array([-1, 0, 1, 0, 2], np.int32)
+    table = np.array([[0.5, 3.0, -1.0, 3.0, 2.0, 0.0],     # root: order 1, 3 (tie -> lower id), 4, 0, 5, 2
+                      [9.0, 0.0, 0.0, 0.0, 0.0, 0.0],      # row 1: best 0
+                      [1.0, 2.0, 3.0, 4.0, 5.0, 6.0],      # row 2: order 5, 4, 3, ...
+                      [0.0] * 6, [0.0] * 6], np.float32)
+    tok, fpar, fdep, node = O.static_tree(parent, rank, table, np.array([[0, 1, 2, 3, 4]], np.int32),
+                                          np.array([42], np.int32))
+    assert tok.tolist() == [[42, 1, 3, 0, 3]]
+    assert fpar.tolist() == [[-1, 0, 0, 1, 2]]
+    assert fdep.tolist() == [[0, 1, 1, 2, 2]]
+    assert node.tolist() == [[-1, 0, 1, 2, 3]]
+
+
+def test_static_tree_chain_is_greedy_argmax():
+    rng = np.random.default_rng(5)
+    table = rng.standard_normal((6, 50)).astype(np.float32)
+    parent = np.arange(-1, 5, dtype=np.int32)
+    rank = np.zeros(6, np.int32)
+    tok, _, fdep, _ = O.static_tree(parent, rank, table, np.arange(6, dtype=np.int32)[None], np.array([0]))
+    assert tok[0, 1:].tolist() == [int(np.argmax(table[i])) for i in range(5)]
+    assert fdep[0].tolist() == [0, 1, 2, 3, 4, 5]
