@@ -360,6 +360,9 @@ def run_gpu(args):
     # ---- a static draft tree of the same size, flattened from the same draft table ----
     static = time_static_tree(wl, cfg, sets[0], stream, K)
 
+    # ---- the draft LM head that produces one layer's logits (tcgen05) ----
+    lm_head = time_lm_head(wl, cfg, stream, K, hbm_peak)
+
     # ---- end to end through the public API with host buffers ----
     e2e = run_e2e(args, st, sets, wl, stream)
 
@@ -388,6 +391,7 @@ def run_gpu(args):
         "e2e": e2e,
         "kv_commit": commit,
         "static_tree": static,
+        "lm_head": lm_head,
         "gpu_launches": launches,
         "clocks": clk.summary(),
     }
@@ -445,6 +449,49 @@ def time_kv_commit(st, inp, wl, cfg, prefix, stream, K):
     nbytes = rows * Hkv * d * kc.element_size() * 2 * 2
     return {"us_per_launch": round(us, 3), "rows_committed": rows, "bytes": nbytes,
             "GBps": round(nbytes / (us * 1e-6) / 1e9, 2), "bound": "latency (a few KB per sequence)"}
+
+
+LM_HIDDEN = {"llama2-7b": 4096, "llama2-13b": 5120, "llama2-70b": 8192, "sweep-7b": 4096}
+
+
+def time_lm_head(wl, cfg, stream, K, hbm_peak):
+    """et_lm_head for one expansion layer (B x m feature rows) against a
+    synthetic bf16 LM head [V, H]; two weight copies alternate so that every
+    launch streams its weight from HBM (each is larger than L2)."""
+    import torch
+    from speculative_decoding_eagle_gb300 import binding as E
+    H = LM_HIDDEN.get(wl.name)
+    M = cfg.B * wl.m
+    if H is None or M > 64:
+        return None
+    g = torch.Generator(device="cuda").manual_seed(0xEA61)
+    ws = [(0.02 * torch.randn((wl.V, H), device="cuda", generator=g)).to(torch.bfloat16) for _ in range(2)]
+    x = torch.randn((M, H), device="cuda", generator=g).to(torch.bfloat16)
+    out = torch.empty((M, wl.V), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with torch.cuda.stream(stream):
+        for w in ws:
+            E.et_lm_head(x, w, out, dev_status=status, stream=stream)
+    stream.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        for i in range(K):
+            E.et_lm_head(x, ws[i % 2], out, dev_status=status, stream=stream)
+    gr.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream()
+    e0.record(cur)
+    gr.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / K
+    nbytes = wl.V * H * 2 + M * H * 2 + M * wl.V * 4
+    gbs = nbytes / (us * 1e-6) / 1e9
+    del ws
+    return {"M": M, "H": H, "V": wl.V, "us_per_launch": round(us, 3), "bytes": nbytes, "GBps": round(gbs, 1),
+            "frac": round(gbs / hbm_peak, 4), "bound": "hbm (weight streamed once)",
+            "status": int(status.item())}
 
 
 STATIC_WIDTHS = (4, 2, 2, 1, 1)  # 61 flat rows, the size of the 7B dynamic tree

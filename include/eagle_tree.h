@@ -6,7 +6,8 @@
  * lossless acceleration: EAGLE-2 lets an RTX 3060 generate faster than an
  * A100") describes it, is:
  *
- *   for layer = 0 .. depth-1:  et_tree_expand      (expansion phase)
+ *   for layer = 0 .. depth-1:  [et_lm_head: draft features -> logits]
+ *                              et_tree_expand      (expansion phase)
  *     (or et_static_tree: a fixed tree shape, EAGLE-1 / Medusa style)
  *   et_tree_rerank                                  (reranking phase, flatten)
  *   et_tree_mask_posids                             (attention mask, positions)
@@ -128,6 +129,14 @@ typedef struct {
                                  1 = mma.sync tensor-core path, 2 = tcgen05 path
                                  (ET_ERR_UNSUPPORTED unless bf16 and d = 128) */
 } et_attn_shape;
+
+/* Draft LM head shape (host struct), see et_lm_head. */
+typedef struct {
+    int32_t M;      /* feature rows (nodes being expanded), 1..64 */
+    int32_t H;      /* hidden size, a multiple of 64 */
+    int32_t V;      /* vocabulary */
+    int64_t ldo;    /* row stride of logits in elements, >= V */
+} et_lmhead_shape;
 
 /* Static draft tree configuration (host struct), see et_static_tree. */
 typedef struct {
@@ -332,6 +341,24 @@ et_status et_verify_accept(const et_tree_cfg *cfg, et_accept_mode mode, const et
                            const float *uniforms,
                            int32_t *accept_len, int32_t *path, int32_t *tokens,
                            int32_t *dev_status, void *ws, size_t ws_bytes, et_stream_t stream);
+
+/*
+ * et_lm_head -- the draft model's logits for the nodes being expanded (EAGLE
+ * blog 1.2: the draft reuses the target's LM head on the features its extra
+ * decoder layer produces): logits[m, v] = sum_h features[m, h] * weight[v, h],
+ * bf16 inputs, fp32 accumulation and output.  The rows feed et_tree_expand
+ * as its logits table (row m = the m-th expanded node, so with row_of_node =
+ * NULL the features are ordered by (sequence, frontier slot)).
+ *
+ * features  bf16 [M, H], row-major, 16-byte aligned.
+ * weight    bf16 [V, H], row-major (the LM head), 16-byte aligned.
+ * logits    fp32 [M, ldo].
+ * Runs on tcgen05 tensor cores, one block per 128 vocabulary rows; bound by
+ * streaming the weight once (V x H x 2 bytes).  A bounded wait that expires
+ * sets ET_DEV_TIMEOUT and leaves that block's logits unwritten.  No workspace.
+ */
+et_status et_lm_head(const et_lmhead_shape *shape, const void *features, const void *weight, float *logits,
+                     int32_t *dev_status, et_stream_t stream);
 
 /*
  * et_static_tree -- a static draft tree (EAGLE-1 / Medusa style, which the

@@ -28,7 +28,7 @@ ATTN_AUTO, ATTN_MMA_SYNC, ATTN_TCGEN05 = 0, 1, 2
 EXPORTED = ("et_num_candidates", "et_layer_expanded", "et_layer_base", "et_tree_workspace_size",
             "et_tree_attention_workspace_size", "et_tree_attention_splits", "et_workspace_init",
             "et_status_string", "et_abi_version", "et_tree_expand", "et_tree_expand_noalloc", "et_tree_rerank", "et_tree_rerank_mask",
-            "et_tree_mask_posids", "et_tree_attention", "et_verify_accept", "et_kv_commit", "et_static_tree")
+            "et_tree_mask_posids", "et_tree_attention", "et_verify_accept", "et_kv_commit", "et_static_tree", "et_lm_head")
 
 
 class TreeCfgC(ctypes.Structure):
@@ -45,6 +45,10 @@ class AttnShapeC(ctypes.Structure):
     _fields_ = [("B", c_i32), ("N", c_i32), ("Hq", c_i32), ("Hkv", c_i32), ("d", c_i32), ("dtype", c_i32),
                 ("scale", c_f32), ("max_prefix", c_i32), ("kv_rows", c_i64), ("kv_head_stride", c_i64),
                 ("num_splits", c_i32), ("impl", c_i32)]
+
+
+class LmHeadShapeC(ctypes.Structure):
+    _fields_ = [("M", c_i32), ("H", c_i32), ("V", c_i32), ("ldo", c_i64)]
 
 
 class StaticCfgC(ctypes.Structure):
@@ -92,6 +96,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "et_tree_mask_posids": (c_i32, [P(TreeCfgC), P(TreeC), c_vp, c_vp, c_vp, c_vp]),
         "et_tree_attention": (c_i32, [P(AttnShapeC), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                       c_vp, c_vp, c_sz, c_vp]),
+        "et_lm_head": (c_i32, [P(LmHeadShapeC), c_vp, c_vp, c_vp, c_vp, c_vp]),
         "et_static_tree": (c_i32, [P(StaticCfgC), c_vp, c_vp, c_vp, c_i64, c_vp, P(TreeC), c_vp, c_vp]),
         "et_kv_commit": (c_i32, [P(CommitShapeC), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                  c_vp, c_vp]),
@@ -393,3 +398,17 @@ def et_static_tree(B: int, V: int, topk: int, parent: torch.Tensor, rank: torch.
                                _ptr(row_of_flat, torch.int32, "row_of_flat"), ctypes.byref(tree.c()),
                                _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
     _check("et_static_tree", st)
+
+
+def et_lm_head(features: torch.Tensor, weight: torch.Tensor, logits: torch.Tensor,
+               dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """logits[m, :V] = features[m] @ weight.T (bf16 in, fp32 out) on the tcgen05 tensor cores."""
+    M, H = features.shape
+    V = weight.shape[0]
+    if weight.shape[1] != H or logits.dim() != 2 or logits.shape[0] < M or logits.stride(1) != 1:
+        raise ValueError("features [M, H], weight [V, H], logits [>=M, >=V] with unit inner stride")
+    st = load().et_lm_head(ctypes.byref(LmHeadShapeC(M, H, V, logits.stride(0))),
+                           _ptr(features, torch.bfloat16, "features"), _ptr(weight, torch.bfloat16, "weight"),
+                           logits.data_ptr() if logits.dtype == torch.float32 and logits.is_cuda else None,
+                           _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check("et_lm_head", st)

@@ -169,6 +169,17 @@ def test_kv_commit_argument_checks(lib):
     assert call(shape(feat_dim=4096)) == E.ET_ERR_INVALID_ARG     # features asked for, no buffers
 
 
+def test_lm_head_argument_checks(lib):
+    def call(M=10, H=4096, V=32000, ldo=32000, x=FAKE, w=FAKE, out=FAKE):
+        return lib.et_lm_head(ctypes.byref(E.LmHeadShapeC(M, H, V, ldo)), x, w, out, None, None)
+    assert call(M=0) == E.ET_ERR_INVALID_ARG
+    assert call(M=65) == E.ET_ERR_INVALID_ARG          # at most 64 feature rows per call
+    assert call(H=100) == E.ET_ERR_UNSUPPORTED         # whole 64-element k slices
+    assert call(ldo=31999) == E.ET_ERR_INVALID_ARG
+    assert call(x=FAKE + 8) == E.ET_ERR_INVALID_ARG    # TMA needs 16-byte aligned operands
+    assert call(w=None) == E.ET_ERR_INVALID_ARG
+
+
 def test_status_strings(lib):
     for s in range(6):
         assert E.status_string(s)

@@ -563,3 +563,50 @@ def test_static_tree_flags_a_bad_rank():
     g = gpu_tree_np(tb)
     assert int(status.item()) & E.ET_DEV_BAD_INDEX
     assert g["flat_tok"][0, 2] == -1 and g["flat_tok"][0, 1] == int(np.argmax(table[0]))
+
+
+# ---------------------------------------------------------------------------
+# draft LM head on tcgen05, and its logits feeding the expansion
+# ---------------------------------------------------------------------------
+LMHEAD_CASES = [(1, 64, 1000), (10, 4096, 32000), (37, 512, 5000), (64, 128, 130), (16, 256, 128)]
+
+
+def _lm_operands(M, H, V, seed):
+    rng = np.random.default_rng(seed)
+    x = torch.from_numpy(rng.standard_normal((M, H)).astype(np.float32)).to(torch.bfloat16)
+    w = torch.from_numpy((0.05 * rng.standard_normal((V, H))).astype(np.float32)).to(torch.bfloat16)
+    return x, w
+
+
+@pytest.mark.parametrize("M,H,V", LMHEAD_CASES)
+def test_lm_head_matches_oracle(M, H, V):
+    x, w = _lm_operands(M, H, V, seed=M * 7 + V)
+    ldo = V + 37
+    out = torch.full((M, ldo), 12345.0, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    E.et_lm_head(x.cuda(), w.cuda(), out, dev_status=status)
+    got = out.cpu().numpy()
+    xf, wf = x.float().numpy(), w.float().numpy()
+    ref = O.lm_head_logits(xf, wf)
+    bound = O.lm_head_error_bound(xf, wf) + 1e-30
+    err = np.abs(got[:, :V] - ref)
+    assert np.all(err <= bound), float((err / bound).max())
+    assert np.all(got[:, V:] == 12345.0)  # past the vocabulary: untouched
+    assert int(status.item()) == 0
+
+
+def test_lm_head_logits_feed_the_expansion():
+    # one layer-0 expansion per sequence straight from the head's logits rows
+    B, H, V, k = 3, 1024, 32000, 10
+    x, w = _lm_operands(B, H, V, seed=2)
+    logits = torch.zeros((B, V), device="cuda")
+    E.et_lm_head(x.cuda(), w.cuda(), logits)
+    cfg = E.TreeCfg(B=B, V=V, depth=2, topk=k, m=k, n=20)
+    tb = E.TreeBuffers.allocate(cfg)
+    ws = E.new_workspace(E.et_tree_workspace_size(cfg))
+    E.et_tree_expand(cfg, 0, logits, tb, ws)
+    g = gpu_tree_np(tb)
+    table = logits.cpu().numpy()
+    for b in range(B):
+        want = O.topk_children(table[b], k)
+        assert list(g["cand_tok"][b][:k]) == list(want)

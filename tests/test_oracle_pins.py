@@ -610,3 +610,17 @@ def test_static_tree_chain_is_greedy_argmax():
     tok, _, fdep, _ = O.static_tree(parent, rank, table, np.arange(6, dtype=np.int32)[None], np.array([0]))
     assert tok[0, 1:].tolist() == [int(np.argmax(table[i])) for i in range(5)]
     assert fdep[0].tolist() == [0, 1, 2, 3, 4, 5]
+
+
+# ---------------------------------------------------------------------------
+# draft LM head: logits = W x, pinned on integers (exact in any precision)
+# ---------------------------------------------------------------------------
+def test_lm_head_integer_example():
+    x = np.array([[1, 2, 3], [0, -1, 4]], np.float32)
+    w = np.array([[1, 0, 0], [0, 1, 0], [1, 1, 1], [2, -1, 0.5]], np.float32)
+    np.testing.assert_array_equal(O.lm_head_logits(x, w), [[1, 2, 6, 1.5], [0, -1, 3, 3]])
+    b = O.lm_head_error_bound(x, w)
+    # H * 2^-24 * sum |x w|: row 0 . w row 0 has sum |x w| = 1; row 1 . w row 0 has none
+    np.testing.assert_allclose(b[0, 0], 3 * 2.0 ** -24)
+    assert b[1, 0] == 0.0
+    np.testing.assert_allclose(b[0, 2], 3 * 2.0 ** -24 * 6)
