@@ -378,7 +378,7 @@ def run_gpu(args):
                    "accept": {0: "greedy", 1: "stoch_point", 2: "stoch_draftq"}[st.mode],
                    "attention_splits": E.et_tree_attention_splits(st.shape),
                    "attention_kernel": {0: "auto", 1: "mma.sync", 2: "tcgen05"}[st.attn_impl] if st.attn_impl else
-                   ("tcgen05" if wl.dtype == "bf16" and wl.d == 128 else "mma.sync"),
+                   ("fp32 cores" if wl.dtype != "bf16" else ("tcgen05" if wl.d == 128 else "mma.sync")),
                    "l2": f"inputs larger than L2: {R} rotating input sets, {per_step / 1e6:.1f} MB read per step",
                    "cuda_graphs": bool(graphs), "parallelism": f"replicas x{world}"},
         "tree_attention": {"us_per_launch": round(attn_us, 3), "GBps": round(achieved, 1),

@@ -332,6 +332,15 @@ __global__ void __launch_bounds__(kRrThreads) k_rerank(RerankArgs a) {
     rk[q] = id < C ? rank_key(a.tree.cand_key[(long long)b * C + id], id) : ~0ull;
   }
   if (t < kMaxN) { row_par[t] = 0; row_dep[t] = 0; }  // rows a broken tree leaves unwritten
+  // the token and parent of this thread's flatten ids, fetched now (they are
+  // needed only after the selection)
+  int pre_tok[kRrPer], pre_par[kRrPer];
+#pragma unroll
+  for (int j = 0; j < kRrPer; ++j) {
+    const int id = kRrPer * t + j;
+    pre_tok[j] = id < C ? a.tree.cand_tok[(long long)b * C + id] : -1;
+    pre_par[j] = id < C ? a.tree.cand_parent[(long long)b * C + id] : -1;
+  }
   // The n-th smallest rank key (keys are unique): a 2048-bin histogram over
   // [min, max] puts it in one bin; that bin's keys are ranked by counting
   // when few, else the bin's range is histogrammed again (each pass narrows
@@ -439,7 +448,7 @@ __global__ void __launch_bounds__(kRrThreads) k_rerank(RerankArgs a) {
     if (id >= C || !kept[id]) continue;
     const int row = flat_of[id];
     if (row < 1 || row >= a.N) { bad = 1; continue; }  // never write outside the flat arrays
-    const int p = a.tree.cand_parent[(long long)b * C + id];
+    const int p = pre_par[j];
     int prow = 0;
     if (p >= 0) {
       prow = (p < C) ? flat_of[p] : -1;
@@ -449,7 +458,7 @@ __global__ void __launch_bounds__(kRrThreads) k_rerank(RerankArgs a) {
     for (int l = 1; l <= a.depth; ++l)
       if (id >= a.base[l]) depth = l;
     a.tree.flat_node[fo + row] = id;
-    a.tree.flat_tok[fo + row] = a.tree.cand_tok[(long long)b * C + id];
+    a.tree.flat_tok[fo + row] = pre_tok[j];
     a.tree.flat_parent[fo + row] = prow;
     a.tree.flat_depth[fo + row] = depth;
     row_par[row] = prow;
