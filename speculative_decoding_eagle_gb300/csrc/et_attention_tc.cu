@@ -99,7 +99,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     k_attn_tc(const __grid_constant__ CUtensorMap tm_kp, const __grid_constant__ CUtensorMap tm_vp,
               const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt,
               const __grid_constant__ CUtensorMap tm_q, const TcLaunch a) {
-  pdl_wait();  // the previous kernel in the stream has completed (inputs may come from it)
   extern __shared__ unsigned char smem_raw[];
   __shared__ int row_tok[kTcRows], row_head[kTcRows];
   unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -111,13 +110,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int s = blockIdx.x, g = blockIdx.y / a.MT, mt = blockIdx.y - g * a.MT, b = blockIdx.z;
   const int N = a.N;
-  const int L = a.prefix_len[b];
-  const long long S_b = a.kv_head_stride > 0 ? a.kv_head_stride : L;
-  const long long row0 = a.kv_row0 ? a.kv_row0[b] : 0;
-  int t0, t1, nP;
-  split_range_tc(L, N, a.S, s, t0, t1, nP);
-  const int T = t1 - t0;
 
+  // ---- set-up that touches no global memory (it overlaps the previous kernel's tail) ----
   if (t == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bar(B_KFULL + i), 1);
@@ -132,9 +126,35 @@ __global__ void __launch_bounds__(kThreads, 2)
     mbar_init(bar(B_QFULL), a.q_tma ? 1 : kQWarps);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    // the first K and V tiles and the Q tile go out before anything else
-    // (TMEM allocation, row tables): their round trip is the longest latency
-    // of the prologue
+  }
+  if (t < kTcRows) {
+    const int R = mt * kTcRows + t;
+    const int i = R / a.G;
+    row_tok[t] = i < N ? i : -1;
+    row_head[t] = g * a.G + (R - i * a.G);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  pdl_wait();     // the previous kernel in the stream has completed (the inputs may come from it)
+  pdl_trigger();  // after the TMEM allocation: a waiting dependent block must not hold the TMEM this block needs
+  const int L = a.prefix_len[b];
+  const long long S_b = a.kv_head_stride > 0 ? a.kv_head_stride : L;
+  const long long row0 = a.kv_row0 ? a.kv_row0[b] : 0;
+  int t0, t1, nP;
+  split_range_tc(L, N, a.S, s, t0, t1, nP);
+  const int T = t1 - t0;
+  if (t == 0) {
+    // the first K and V tiles and the Q tile go out first: their round trip
+    // is the longest latency of the prologue
     for (int j = 0; j < T && j < kStages; ++j) {
       const int tile = t0 + j;
 #pragma unroll
@@ -161,23 +181,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       tma_4d(sb + kOffQ + kQHalfBytes, &tm_q, 64, 0, g, tok0, qb);
     }
   }
-  if (t < kTcRows) {
-    const int R = mt * kTcRows + t;
-    const int i = R / a.G;
-    row_tok[t] = i < N ? i : -1;
-    row_head[t] = g * a.G + (R - i * a.G);
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tmem_slot)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  pdl_trigger();  // only now: a waiting dependent block must not hold the TMEM this block needs
   if (t == 0 && L > 0 && row0 + (long long)g * S_b + L > a.kv_rows) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
 
   if (warp == 0 || warp == 2) {
@@ -474,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (t == 0) flag_status(a.dev_status, ET_DEV_TIMEOUT);
     return;
   }
-  const int per = (kTcRows + S - 1) / S;
+  const int per = (nvalid + S - 1) / S;  // the real rows, spread over every split
   const int r0 = s * per, r1 = min(nvalid, r0 + per);
   if (r1 <= r0) return;
   float *wts = reinterpret_cast<float *>(sm + kOffQ);  // [per][kTcMaxSplits] weight / total
