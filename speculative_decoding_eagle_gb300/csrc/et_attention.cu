@@ -13,6 +13,8 @@
 //    (the default; the mma.sync kernel stays selectable and covers d = 64).
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "et_attn_internal.h"
 #include "et_common.cuh"
 
@@ -437,17 +439,17 @@ using namespace et;
 // host side
 // ---------------------------------------------------------------------------
 static int sm_count() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];  // zero-initialised (static storage)
   int dev = 0;
-  cudaGetDevice(&dev);
+  if (cudaGetDevice(&dev) != cudaSuccess) cudaGetLastError();
   if (dev < 0 || dev >= 64) dev = 0;
-  if (!cached[dev]) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
     cudaGetLastError();
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 static bool attn_shape_ok(const et_attn_shape *s) {
@@ -599,13 +601,11 @@ extern "C" et_status et_tree_attention(const et_attn_shape *shape, const void *q
   dim3 grid(a.S, a.Hkv * a.MT, a.B);
   if (shape->d == 64) {
     const int smem = kRows * 64 * 2 + 4 * kKeys * 64 * 2;
-    static bool attr64 = false;
-    if (!attr64) { cudaFuncSetAttribute(k_attn_mma<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); attr64 = true; }
+    ET_RETURN_IF(et_smem_attr((const void *)k_attn_mma<64>, smem) != cudaSuccess, ET_ERR_CUDA);
     return et_launch(k_attn_mma<64>, grid, dim3(kMmaThreads), smem, st, 0, a);
   } else {
     const int smem = kRows * 128 * 2 + 4 * kKeys * 128 * 2;
-    static bool attr128 = false;
-    if (!attr128) { cudaFuncSetAttribute(k_attn_mma<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); attr128 = true; }
+    ET_RETURN_IF(et_smem_attr((const void *)k_attn_mma<128>, smem) != cudaSuccess, ET_ERR_CUDA);
     return et_launch(k_attn_mma<128>, grid, dim3(kMmaThreads), smem, st, 0, a);
   }
 }

@@ -574,14 +574,7 @@ bool make_map_q(CUtensorMap *m, const void *base, int G, int Hkv, long long toke
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t set_smem_attr() {
-  static std::once_flag once;
-  static cudaError_t err = cudaSuccess;
-  std::call_once(once, [] {
-    err = cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-  });
-  return err;
-}
+cudaError_t set_smem_attr() { return et_smem_attr((const void *)k_attn_tc, (int)kSmemBytes); }
 
 }  // namespace
 

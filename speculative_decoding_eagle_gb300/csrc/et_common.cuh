@@ -389,6 +389,30 @@ static inline et_status et_launch_status() {
 }
 static inline bool et_aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device): the
+// attribute lives in the current device's context, so every device that runs
+// the kernel needs its own call.  Thread-safe.
+#include <mutex>
+static inline cudaError_t et_smem_attr(const void *kernel, int bytes) {
+  static std::mutex mu;
+  static const void *done_fn[64];
+  static int done_dev[64];
+  static int ndone = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < ndone; ++i)
+    if (done_fn[i] == kernel && done_dev[i] == dev) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  if (ndone < 64) {
+    done_fn[ndone] = kernel;
+    done_dev[ndone] = dev;
+    ++ndone;
+  }
+  return cudaSuccess;
+}
+
 // Launch with programmatic stream serialization (and, when cluster_x > 0,
 // clusters of cluster_x blocks along x).
 template <typename... KArgs, typename... Args>

@@ -167,12 +167,7 @@ extern "C" et_status et_lm_head(const et_lmhead_shape *s, const void *features, 
   CUtensorMap m_w, m_x;
   if (!make_map_rows(&m_w, weight, s->V, s->H, kLmRows) || !make_map_rows(&m_x, features, s->M, s->H, Mp))
     return ET_ERR_INVALID_ARG;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(k_lmhead_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmemMax);
-  });
-  if (attr_err != cudaSuccess) return ET_ERR_CUDA;
+  if (et_smem_attr((const void *)k_lmhead_tc, kLmSmemMax) != cudaSuccess) return ET_ERR_CUDA;
   LmArgs a;
   a.M = s->M; a.Mp = Mp; a.H = s->H; a.V = s->V; a.stages = stages; a.ldo = s->ldo;
   a.out = logits;
