@@ -624,3 +624,30 @@ def test_lm_head_integer_example():
     np.testing.assert_allclose(b[0, 0], 3 * 2.0 ** -24)
     assert b[1, 0] == 0.0
     np.testing.assert_allclose(b[0, 2], 3 * 2.0 ** -24 * 6)
+
+
+# ---------------------------------------------------------------------------
+# temperature: p(z / T), closed forms on two tokens
+# ---------------------------------------------------------------------------
+def test_softmax_temperature_closed_form():
+    z = np.array([0.0, np.log(3.0)], np.float32)
+    l3 = float(np.float32(np.log(3.0)))  # the logit as stored
+    np.testing.assert_allclose(O.softmax_t(z, 2.0)[1], np.exp(l3 / 2) / (1 + np.exp(l3 / 2)), rtol=1e-12)
+    np.testing.assert_allclose(O.softmax_t(z, 0.5)[1], np.exp(2 * l3) / (1 + np.exp(2 * l3)), rtol=1e-12)
+    np.testing.assert_allclose(O.softmax_t(z, 0.5)[1], 0.9, atol=1e-6)
+
+
+def test_stoch_acceptance_depends_on_temperature():
+    # root row p = softmax([0, ln 3] / T): token 1 has p = 0.9 at T = 1/2 and 0.75 at T = 1;
+    # its one child (token 1) meets the uniform 0.85
+    tok = np.array([[7, 1]], np.int32)
+    par = np.array([[-1, 0]], np.int32)
+    node = np.array([[-1, 0]], np.int32)
+    table = np.array([[0.0, np.log(3.0)], [0.0, 0.0]], np.float32)
+    u = np.array([[0.5, 0.85]], np.float32)
+    hot = O.verify_accept(O.TreeCfg(B=1, V=2, depth=1, topk=1, m=1, n=1, temperature=0.5), O.STOCH_POINT,
+                          tok, par, node, table, None, uniforms=u)
+    cold = O.verify_accept(O.TreeCfg(B=1, V=2, depth=1, topk=1, m=1, n=1, temperature=1.0), O.STOCH_POINT,
+                           tok, par, node, table, None, uniforms=u)
+    assert hot.accept_len[0] == 1 and hot.tokens[0, 0] == 1
+    assert cold.accept_len[0] == 0 and cold.tokens[0, 0] == 0  # rejected: the residual keeps token 0 only
