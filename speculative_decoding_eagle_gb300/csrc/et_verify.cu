@@ -163,6 +163,9 @@ __device__ int block_inverse_cdf(int V, float uni, WF w, double *redd, int *redi
   return r;
 }
 
+constexpr int kMaxSpan = 4096;                  // chunk tokens (the clustered phase 1)
+constexpr int kMaxSpanWords = kMaxSpan / 32;
+constexpr int kMaxPer = kMaxSpan / 256;         // tokens per thread in the chunk pass
 // STOCH_POINT bonus token: the inverse CDF of the residual p at the stop row
 // (rejected children removed) from the row's chunk statistics.  Chunk c holds
 // tokens [c·span, (c+1)·span) with (max, sum of exp) (Mc, Sc) from phase 1, so
@@ -172,7 +175,7 @@ __device__ int block_inverse_cdf(int V, float uni, WF w, double *redd, int *redi
 template <int NT>
 __device__ int bonus_from_chunks(const VerifyArgs &a, const float *zr, const float *cstat, float M, float uni,
                                  const int *rej, const float *rejw, int nrej, double *redd, int *redi,
-                                 double *tsum) {
+                                 double *tsum, unsigned int *rejbits) {
   const int t = threadIdx.x, lane = t & 31, wp = t >> 5;
   const int span = a.cdf_span, nch = a.cdf_nch;
   if (t == 0) { redi[0] = 0x7fffffff; redi[1] = -1; }
@@ -184,8 +187,9 @@ __device__ int bonus_from_chunks(const VerifyArgs &a, const float *zr, const flo
       if (c < nch) {
         const float mc = ld_cg(cstat + 2 * c), sc = ld_cg(cstat + 2 * c + 1);
         wc = mc > -INFINITY ? (double)sc * (double)expf(mc - M) : 0.0;
+        const int lo = c * span, hi = lo + span;
         for (int q = 0; q < nrej; ++q)
-          if (rej[q] >= 0 && rej[q] / span == c) wc -= (double)rejw[q];
+          if (rej[q] >= lo && rej[q] < hi) wc -= (double)rejw[q];
         wc = wc > 0.0 ? wc : 0.0;
         tsum[c] = wc;
       }
@@ -223,29 +227,47 @@ __device__ int bonus_from_chunks(const VerifyArgs &a, const float *zr, const flo
       redi[2] = J;
     }
   }
+  // the rejected children inside a chunk, as a bitmap (span <= 4096 bits)
+  for (int x = t; x < kMaxSpanWords; x += NT) rejbits[x] = 0u;
   __syncthreads();
   const int J = redi[2];
   if (J < 0 || !zr) {
     __syncthreads();
     return -1;
   }
-  // pass over chunk J: per thread a contiguous run of span / NT tokens
-  const int per = (span + NT - 1) / NT;
-  const int v0 = J * span + t * per;
-  double mine = 0.0;
-  int lastv = -1;
-  for (int j = 0; j < per; ++j) {
-    const int v = v0 + j;
-    if (v >= a.V || v >= (J + 1) * span) break;
-    bool rejected = false;
-    for (int q = 0; q < nrej; ++q) rejected |= (rej[q] == v);
-    int f2 = 0;
-    const float y = sanitize_logit(zr[v], f2) / a.T;
-    const float x = (!rejected && y > -INFINITY) ? expf(y - M) : 0.f;
-    mine += (double)x;
-    if (x > 0.f) lastv = v;
+  for (int q = t; q < nrej; q += NT) {
+    const int off = rej[q] - J * span;
+    if (off >= 0 && off < span) atomicOr(&rejbits[off >> 5], 1u << (off & 31));
   }
-  double incl = mine;
+  __syncthreads();
+  // pass over chunk J: per thread a contiguous run of span / NT (<= 16) tokens, kept in registers
+  const int per = span / NT;
+  const int v0 = J * span + t * per;
+  float x[kMaxPer];
+  float mine = 0.f;
+  int lastv = -1;
+#pragma unroll
+  for (int j = 0; j < kMaxPer; j += 4) {
+    float z4[4];
+    if (j < per && a.vec4t && v0 + j + 3 < a.V) {
+      const float4 f = *reinterpret_cast<const float4 *>(zr + v0 + j);
+      z4[0] = f.x; z4[1] = f.y; z4[2] = f.z; z4[3] = f.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) z4[e] = (j + e < per && v0 + j + e < a.V) ? zr[v0 + j + e] : -INFINITY;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int jj = j + e, off = t * per + jj;
+      int f2 = 0;
+      const float y = sanitize_logit(z4[e], f2) / a.T;
+      const bool rejected = jj < per && ((rejbits[off >> 5] >> (off & 31)) & 1u);
+      x[jj] = (jj < per && !rejected && y > -INFINITY) ? expf(y - M) : 0.f;
+      mine += x[jj];
+      if (x[jj] > 0.f) lastv = v0 + jj;
+    }
+  }
+  double incl = (double)mine;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const double y = __shfl_up_sync(0xffffffffu, incl, o);
@@ -256,18 +278,18 @@ __device__ int bonus_from_chunks(const VerifyArgs &a, const float *zr, const flo
   __syncthreads();
   const double before = redd[0], thr = redd[1];
   if (before >= 0.0) {
-    double run = before + incl - mine;
-    for (int x2 = 0; x2 < wp; ++x2) run += tsum[x2];
-    for (int j = 0; j < per; ++j) {
-      const int v = v0 + j;
-      if (v >= a.V || v >= (J + 1) * span) break;
-      bool rejected = false;
-      for (int q = 0; q < nrej; ++q) rejected |= (rej[q] == v);
-      int f2 = 0;
-      const float y = sanitize_logit(zr[v], f2) / a.T;
-      const float x = (!rejected && y > -INFINITY) ? expf(y - M) : 0.f;
-      run += (double)x;
-      if (x > 0.f && run > thr) { atomicMin(&redi[0], v); break; }
+    double base = before + incl - (double)mine;
+    for (int x2 = 0; x2 < wp; ++x2) base += tsum[x2];
+    // the threshold relative to this thread's run, then an fp32 walk over its tokens
+    const double rel = thr - base;
+    if (rel < (double)mine) {
+      float run = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < kMaxPer; ++jj) {
+        if (jj >= per) break;
+        run += x[jj];
+        if (x[jj] > 0.f && (double)run > rel) { atomicMin(&redi[0], v0 + jj); break; }
+      }
     }
   }
   __syncthreads();
@@ -290,6 +312,7 @@ struct WalkSmem {
   int opath[kMaxDepth + 2], otok[kMaxDepth + 2];
   int rej[kMaxTopk];
   float rejw[kMaxTopk];  // exp(z/T - M) of each rejected child at the stop row
+  unsigned int rejbits[kMaxSpanWords];  // rejected children inside the chunk being scanned
   float uni[kMaxN];      // this sequence's uniforms
   float zsh[kMaxTopk];
   int s_next, s_nrej, s_cur, s_alen;
@@ -354,28 +377,30 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
           for (int j0 = cur + 1; j0 < N && nxt < 0; j0 += 32) {
             const int j = j0 + lane;
             const bool child = j < N && par[j] == cur;
-            // p(x) and the uniform of every child in parallel; R accumulates in row order
+            // p(x) and the uniform of every child at once; R (the mass of the
+            // siblings rejected before a child) as a prefix sum in row order
             const float wx = child ? expf(w.zc[j] / a.T - M) : 0.f;
             const float px = (child && S > 0.f) ? wx / S : 0.f;
-            const float u = child ? w.uni[j] : 0.f;
-            const int x = child ? tokf[j] : -1;
-            unsigned int kids = __ballot_sync(0xffffffffu, child);
-            while (kids) {
-              const int l = __ffs(kids) - 1;
-              kids &= kids - 1;
-              const float pl = __shfl_sync(0xffffffffu, px, l);
-              const float ul = __shfl_sync(0xffffffffu, u, l);
-              const int xl = __shfl_sync(0xffffffffu, x, l);
-              const float wl = __shfl_sync(0xffffffffu, wx, l);
-              const float ratio = (R < 1.f) ? pl / (1.f - R) : INFINITY;
-              if (ul < ratio) { nxt = j0 + l; break; }
-              R += pl;
-              if (nrej < kMaxTopk) {
-                if (lane == 0) { rej[nrej] = xl; w.rejw[nrej] = wl; }
-                ++nrej;
-              }
+            float incl = px;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const float y = __shfl_up_sync(0xffffffffu, incl, o);
+              if (lane >= o) incl += y;
             }
+            const float Rj = R + (incl - px);
+            const bool acc = child && w.uni[j] < ((Rj < 1.f) ? px / (1.f - Rj) : INFINITY);
+            const unsigned int kids = __ballot_sync(0xffffffffu, child);
+            const unsigned int hit = __ballot_sync(0xffffffffu, acc);
+            const unsigned int rejected = hit ? (kids & ((1u << (__ffs(hit) - 1)) - 1u)) : kids;
+            if ((rejected >> lane) & 1u) {  // children before the accepted one, in row order
+              const int slot = nrej + __popc(rejected & ((1u << lane) - 1u));
+              if (slot < kMaxTopk) { rej[slot] = tokf[j]; w.rejw[slot] = wx; }
+            }
+            nrej += __popc(rejected);
+            R += __shfl_sync(0xffffffffu, incl, 31);
+            if (hit) nxt = j0 + __ffs(hit) - 1;
           }
+          if (nrej > kMaxTopk) nrej = kMaxTopk;
         }
         if (nxt < 0 || alen >= a.D) break;
         if (lane == 0) {
@@ -398,7 +423,7 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
       int badz = 0;
       const float *zr = table_row(a.tlog, a.tstride, a.tmap, a.C, b, nodef[cur], fo + cur, badz);
       const int bonus = bonus_from_chunks<NT>(a, zr, a.part + (fo + cur) * (long long)a.nchunk * 2, w.rs0[cur],
-                                              w.uni[0], rej, w.rejw, nrej, redd, redi, w.cdf_tsum);
+                                              w.uni[0], rej, w.rejw, nrej, redd, redi, w.cdf_tsum, w.rejbits);
       if (t == 0) w.otok[alen] = bonus;
       badp |= badz;
     }
