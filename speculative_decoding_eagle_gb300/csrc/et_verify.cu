@@ -244,6 +244,7 @@ __device__ int bonus_from_chunks(const VerifyArgs &a, const float *zr, const flo
   const int per = span / NT;
   const int v0 = J * span + t * per;
   float x[kMaxPer];
+  const float invT = 1.f / a.T;
   float mine = 0.f;
   int lastv = -1;
 #pragma unroll
@@ -260,9 +261,9 @@ __device__ int bonus_from_chunks(const VerifyArgs &a, const float *zr, const flo
     for (int e = 0; e < 4; ++e) {
       const int jj = j + e, off = t * per + jj;
       int f2 = 0;
-      const float y = sanitize_logit(z4[e], f2) / a.T;
+      const float y = sanitize_logit(z4[e], f2) * invT;
       const bool rejected = jj < per && ((rejbits[off >> 5] >> (off & 31)) & 1u);
-      x[jj] = (jj < per && !rejected && y > -INFINITY) ? expf(y - M) : 0.f;
+      x[jj] = (jj < per && !rejected && y > -INFINITY) ? exp_fast(y - M) : 0.f;  // as the chunk sums
       mine += x[jj];
       if (x[jj] > 0.f) lastv = v0 + jj;
     }
@@ -727,9 +728,10 @@ __global__ void __launch_bounds__(kVClThreads) k_verify_cl(VerifyArgs a) {
     if (lane == 0) wkey[warp] = best;
   } else {
     float lm = -INFINITY;
+    const float invT = 1.f / a.T;
 #pragma unroll
     for (int e = 0; e < 4 * kVClVec; ++e) {
-      v[e] = v[e] / a.T;
+      v[e] = v[e] * invT;
       lm = fmaxf(lm, v[e]);
     }
     lm = warp_max(lm);
