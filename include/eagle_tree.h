@@ -142,7 +142,8 @@ typedef struct {
 typedef struct {
     int32_t B, V;   /* sequences, vocabulary (V <= 32768) */
     int32_t N;      /* flat rows including the root, <= 128 */
-    int32_t topk;   /* ranks used: every rank[i] < topk <= 32 */
+    int32_t topk;   /* ranks used: every rank[i] < topk <= 32 (et_static_tree) */
+    float temperature; /* q = softmax(draft / temperature) (et_static_tree_sampled) */
 } et_static_cfg;
 
 /* KV commit shape (host struct), see et_kv_commit. */
@@ -384,6 +385,28 @@ et_status et_lm_head(const et_lmhead_shape *shape, const void *features, const v
 et_status et_static_tree(const et_static_cfg *cfg, const int32_t *parent, const int32_t *rank,
                          const float *logits, int64_t row_stride, const int32_t *row_of_flat,
                          et_tree *tree, int32_t *dev_status, et_stream_t stream);
+
+/*
+ * et_static_tree_sampled -- a static tree whose children are independent
+ * draws from the draft distribution at their parent, q = softmax(draft /
+ * temperature): row i > 0 takes the smallest token t with
+ * sum_{v <= t} q(v) > uniforms[b, i] (the proposal under which the draft-q
+ * acceptance rule, ET_ACCEPT_STOCH_DRAFTQ, is lossless -- the speculative
+ * sampling the EAGLE blog 1.1 cites).  Shape as in et_static_tree (rank is
+ * not used); writes the same flat arrays.
+ *
+ * uniforms  fp32 [B, N] in [0, 1); slot i draws row i (slot 0 unused).
+ * ws        et_static_tree_workspace_size(cfg) bytes, 256-byte aligned, no
+ *           initial contents (the per-chunk (max, sum) of every parent row).
+ * Two launches: chunk statistics of the rows with children (one block per
+ * 4096 tokens), then one block per child row that locates the chunk where
+ * its uniform falls and rescans it.  V <= 32768.
+ */
+size_t et_static_tree_workspace_size(const et_static_cfg *cfg);
+et_status et_static_tree_sampled(const et_static_cfg *cfg, const int32_t *parent, const float *logits,
+                                 int64_t row_stride, const int32_t *row_of_flat, const float *uniforms,
+                                 et_tree *tree, int32_t *dev_status, void *ws, size_t ws_bytes,
+                                 et_stream_t stream);
 
 /*
  * et_kv_commit -- after acceptance, append the accepted path to the KV cache

@@ -9,5 +9,5 @@ from .eagle_tree_oracle import *  # noqa: F401,F403
 from .eagle_tree_oracle import (TreeCfg, Tree, AcceptResult, GREEDY, STOCH_POINT, STOCH_DRAFTQ,  # noqa: F401
                                 FRAC_BITS, KEY_MIN)
 from .kv_commit_oracle import kv_commit  # noqa: F401
-from .static_tree_oracle import static_tree, static_depths  # noqa: F401
+from .static_tree_oracle import static_tree, static_tree_sampled, static_depths  # noqa: F401
 from .lm_head_oracle import lm_head_logits, lm_head_error_bound  # noqa: F401

@@ -47,3 +47,31 @@ def static_tree(parent: np.ndarray, rank: np.ndarray, draft_table: np.ndarray, r
     fdepth = np.tile(depth, (B, 1))
     node = np.tile(np.arange(-1, N - 1, dtype=np.int32), (B, 1))
     return tok, fparent, fdepth, node
+
+
+def static_tree_sampled(parent: np.ndarray, draft_table: np.ndarray, row_of_flat: np.ndarray,
+                        uniforms: np.ndarray, temperature: float, root_tok: np.ndarray):
+    """A static tree whose children are independent draws from the draft
+    distribution at their parent, q = softmax(draft / T) (the proposal the
+    draft-q acceptance rule needs to stay lossless): row i > 0 takes the
+    smallest token t with sum_{v <= t} q(v) > uniforms[b, i].
+
+    Returns (tok, parent, depth, node) like ``static_tree`` and the near-tie
+    margin of every draw (distance of the uniform to the nearest CDF step)."""
+    from .eagle_tree_oracle import _inverse_cdf, softmax_t
+    B, N = row_of_flat.shape
+    depth = static_depths(parent)
+    tok = np.zeros((B, N), np.int32)
+    gaps = np.full((B, N), np.inf)
+    for b in range(B):
+        tok[b, 0] = root_tok[b]
+        for i in range(1, N):
+            p = int(parent[i])
+            q = softmax_t(draft_table[int(row_of_flat[b, p])], temperature)
+            t, gap = _inverse_cdf(q, float(uniforms[b, i]), float(q.sum()))
+            tok[b, i] = t
+            gaps[b, i] = gap
+    fparent = np.tile(parent.astype(np.int32), (B, 1))
+    fdepth = np.tile(depth, (B, 1))
+    node = np.tile(np.arange(-1, N - 1, dtype=np.int32), (B, 1))
+    return tok, fparent, fdepth, node, gaps

@@ -28,7 +28,8 @@ ATTN_AUTO, ATTN_MMA_SYNC, ATTN_TCGEN05 = 0, 1, 2
 EXPORTED = ("et_num_candidates", "et_layer_expanded", "et_layer_base", "et_tree_workspace_size",
             "et_tree_attention_workspace_size", "et_tree_attention_splits", "et_workspace_init",
             "et_status_string", "et_abi_version", "et_tree_expand", "et_tree_expand_noalloc", "et_tree_rerank", "et_tree_rerank_mask",
-            "et_tree_mask_posids", "et_tree_attention", "et_verify_accept", "et_kv_commit", "et_static_tree", "et_lm_head")
+            "et_tree_mask_posids", "et_tree_attention", "et_verify_accept", "et_kv_commit", "et_static_tree", "et_lm_head", "et_static_tree_sampled",
+            "et_static_tree_workspace_size")
 
 
 class TreeCfgC(ctypes.Structure):
@@ -52,7 +53,7 @@ class LmHeadShapeC(ctypes.Structure):
 
 
 class StaticCfgC(ctypes.Structure):
-    _fields_ = [("B", c_i32), ("V", c_i32), ("N", c_i32), ("topk", c_i32)]
+    _fields_ = [("B", c_i32), ("V", c_i32), ("N", c_i32), ("topk", c_i32), ("temperature", c_f32)]
 
 
 class CommitShapeC(ctypes.Structure):
@@ -96,6 +97,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "et_tree_mask_posids": (c_i32, [P(TreeCfgC), P(TreeC), c_vp, c_vp, c_vp, c_vp]),
         "et_tree_attention": (c_i32, [P(AttnShapeC), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                       c_vp, c_vp, c_sz, c_vp]),
+        "et_static_tree_workspace_size": (c_sz, [P(StaticCfgC)]),
+        "et_static_tree_sampled": (c_i32, [P(StaticCfgC), c_vp, c_vp, c_i64, c_vp, c_vp, P(TreeC), c_vp, c_vp, c_sz,
+                                           c_vp]),
         "et_lm_head": (c_i32, [P(LmHeadShapeC), c_vp, c_vp, c_vp, c_vp, c_vp]),
         "et_static_tree": (c_i32, [P(StaticCfgC), c_vp, c_vp, c_vp, c_i64, c_vp, P(TreeC), c_vp, c_vp]),
         "et_kv_commit": (c_i32, [P(CommitShapeC), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
@@ -393,7 +397,7 @@ def et_static_tree(B: int, V: int, topk: int, parent: torch.Tensor, rank: torch.
     if logits.dim() != 2 or logits.stride(1) != 1 or logits.dtype != torch.float32 or not logits.is_cuda:
         raise ValueError("logits must be a CUDA fp32 [rows, >=V] table with unit inner stride")
     N = parent.numel()
-    st = load().et_static_tree(ctypes.byref(StaticCfgC(B, V, N, topk)), _ptr(parent, torch.int32, "parent"),
+    st = load().et_static_tree(ctypes.byref(StaticCfgC(B, V, N, topk, 1.0)), _ptr(parent, torch.int32, "parent"),
                                _ptr(rank, torch.int32, "rank"), logits.data_ptr(), logits.stride(0),
                                _ptr(row_of_flat, torch.int32, "row_of_flat"), ctypes.byref(tree.c()),
                                _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
@@ -412,3 +416,22 @@ def et_lm_head(features: torch.Tensor, weight: torch.Tensor, logits: torch.Tenso
                            logits.data_ptr() if logits.dtype == torch.float32 and logits.is_cuda else None,
                            _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
     _check("et_lm_head", st)
+
+
+def et_static_tree_sampled(B: int, V: int, temperature: float, parent: torch.Tensor, logits: torch.Tensor,
+                           row_of_flat: torch.Tensor, uniforms: torch.Tensor, tree: "TreeBuffers",
+                           ws: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None,
+                           stream=None) -> None:
+    """Flatten a static tree whose children are draws from softmax(draft / T) at their parent."""
+    if logits.dim() != 2 or logits.stride(1) != 1 or logits.dtype != torch.float32 or not logits.is_cuda:
+        raise ValueError("logits must be a CUDA fp32 [rows, >=V] table with unit inner stride")
+    N = parent.numel()
+    cfg = StaticCfgC(B, V, N, 1, temperature)
+    if ws is None:
+        ws = new_workspace(load().et_static_tree_workspace_size(ctypes.byref(cfg)), logits.device)
+    st = load().et_static_tree_sampled(ctypes.byref(cfg), _ptr(parent, torch.int32, "parent"), logits.data_ptr(),
+                                       logits.stride(0), _ptr(row_of_flat, torch.int32, "row_of_flat"),
+                                       _ptr(uniforms, torch.float32, "uniforms"), ctypes.byref(tree.c()),
+                                       _ptr(dev_status, torch.int32, "dev_status"), _ptr(ws, None, "ws"),
+                                       ws.numel() * ws.element_size(), _stream(stream))
+    _check("et_static_tree_sampled", st)

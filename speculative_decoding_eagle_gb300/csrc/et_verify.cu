@@ -8,6 +8,7 @@
 // Phase 2 (the last row-block of a sequence): walk the tree from the root,
 // then draw the bonus token by an inverse CDF over the stopping row.
 #include "et_common.cuh"
+#include "et_cdf.cuh"
 
 extern "C" __attribute__((visibility("hidden"))) size_t et_internal_tree_ws(const et_tree_cfg *cfg, size_t *cnt_bytes, size_t *part_off,
                                       size_t *rowstat_off);
@@ -163,144 +164,6 @@ __device__ int block_inverse_cdf(int V, float uni, WF w, double *redd, int *redi
   return r;
 }
 
-constexpr int kMaxSpan = 4096;                  // chunk tokens (the clustered phase 1)
-constexpr int kMaxSpanWords = kMaxSpan / 32;
-constexpr int kMaxPer = kMaxSpan / 256;         // tokens per thread in the chunk pass
-// STOCH_POINT bonus token: the inverse CDF of the residual p at the stop row
-// (rejected children removed) from the row's chunk statistics.  Chunk c holds
-// tokens [c·span, (c+1)·span) with (max, sum of exp) (Mc, Sc) from phase 1, so
-// its weight is Sc·exp(Mc − M) minus the weights of the rejected children it
-// contains; one warp finds the chunk where the cumulative weight crosses
-// uni·total, then the block rescans that chunk alone (fp64 block scan).
-template <int NT>
-__device__ int bonus_from_chunks(const VerifyArgs &a, const float *zr, const float *cstat, float M, float uni,
-                                 const int *rej, const float *rejw, int nrej, double *redd, int *redi,
-                                 double *tsum, unsigned int *rejbits) {
-  const int t = threadIdx.x, lane = t & 31, wp = t >> 5;
-  const int span = a.cdf_span, nch = a.cdf_nch;
-  if (t == 0) { redi[0] = 0x7fffffff; redi[1] = -1; }
-  if (wp == 0) {
-    double total = 0.0;
-    for (int c0 = 0; c0 < nch; c0 += 32) {
-      const int c = c0 + lane;
-      double wc = 0.0;
-      if (c < nch) {
-        const float mc = ld_cg(cstat + 2 * c), sc = ld_cg(cstat + 2 * c + 1);
-        wc = mc > -INFINITY ? (double)sc * (double)expf(mc - M) : 0.0;
-        const int lo = c * span, hi = lo + span;
-        for (int q = 0; q < nrej; ++q)
-          if (rej[q] >= lo && rej[q] < hi) wc -= (double)rejw[q];
-        wc = wc > 0.0 ? wc : 0.0;
-        tsum[c] = wc;
-      }
-      total += warp_sum_d(wc);
-    }
-    const double thr = (double)uni * total;
-    double run = 0.0, before = 0.0;
-    int J = -1, lastc = -1;
-    for (int c0 = 0; c0 < nch; c0 += 32) {
-      const int c = c0 + lane;
-      const double wc = c < nch ? tsum[c] : 0.0;
-      double incl = wc;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const unsigned int pos = __ballot_sync(0xffffffffu, c < nch && wc > 0.0);
-      if (pos) lastc = c0 + 31 - __clz(pos);
-      const unsigned int hit = __ballot_sync(0xffffffffu, c < nch && wc > 0.0 && run + incl > thr);
-      if (hit && J < 0) {
-        const int l = __ffs(hit) - 1;
-        J = c0 + l;
-        before = run + __shfl_sync(0xffffffffu, incl, l) - __shfl_sync(0xffffffffu, wc, l);
-      }
-      run += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (J < 0) {  // thr at or beyond the total (rounding): the last chunk with weight
-      J = lastc;
-      before = -1.0;
-    }
-    if (lane == 0) {
-      redd[0] = before;
-      redd[1] = thr;
-      redi[2] = J;
-    }
-  }
-  // the rejected children inside a chunk, as a bitmap (span <= 4096 bits)
-  for (int x = t; x < kMaxSpanWords; x += NT) rejbits[x] = 0u;
-  __syncthreads();
-  const int J = redi[2];
-  if (J < 0 || !zr) {
-    __syncthreads();
-    return -1;
-  }
-  for (int q = t; q < nrej; q += NT) {
-    const int off = rej[q] - J * span;
-    if (off >= 0 && off < span) atomicOr(&rejbits[off >> 5], 1u << (off & 31));
-  }
-  __syncthreads();
-  // pass over chunk J: per thread a contiguous run of span / NT (<= 16) tokens, kept in registers
-  const int per = span / NT;
-  const int v0 = J * span + t * per;
-  float x[kMaxPer];
-  const float invT = 1.f / a.T;
-  float mine = 0.f;
-  int lastv = -1;
-#pragma unroll
-  for (int j = 0; j < kMaxPer; j += 4) {
-    float z4[4];
-    if (j < per && a.vec4t && v0 + j + 3 < a.V) {
-      const float4 f = *reinterpret_cast<const float4 *>(zr + v0 + j);
-      z4[0] = f.x; z4[1] = f.y; z4[2] = f.z; z4[3] = f.w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) z4[e] = (j + e < per && v0 + j + e < a.V) ? zr[v0 + j + e] : -INFINITY;
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int jj = j + e, off = t * per + jj;
-      int f2 = 0;
-      const float y = sanitize_logit(z4[e], f2) * invT;
-      const bool rejected = jj < per && ((rejbits[off >> 5] >> (off & 31)) & 1u);
-      x[jj] = (jj < per && !rejected && y > -INFINITY) ? exp_fast(y - M) : 0.f;  // as the chunk sums
-      mine += x[jj];
-      if (x[jj] > 0.f) lastv = v0 + jj;
-    }
-  }
-  double incl = (double)mine;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) tsum[wp] = incl;
-  if (lastv >= 0) atomicMax(&redi[1], lastv);
-  __syncthreads();
-  const double before = redd[0], thr = redd[1];
-  if (before >= 0.0) {
-    double base = before + incl - (double)mine;
-    for (int x2 = 0; x2 < wp; ++x2) base += tsum[x2];
-    // the threshold relative to this thread's run, then an fp32 walk over its tokens
-    const double rel = thr - base;
-    if (rel < (double)mine) {
-      float run = 0.f;
-#pragma unroll
-      for (int jj = 0; jj < kMaxPer; ++jj) {
-        if (jj >= per) break;
-        run += x[jj];
-        if (x[jj] > 0.f && (double)run > rel) { atomicMin(&redi[0], v0 + jj); break; }
-      }
-    }
-  }
-  __syncthreads();
-  // not crossed inside the chunk (its two sums differ in the last bits): the
-  // crossing is at its end, so take its last token of positive weight
-  const int r = redi[0] != 0x7fffffff ? redi[0] : redi[1];
-  __syncthreads();
-  return r;
-}
-
 struct WalkSmem {
   float redz[32];
   int redi[32];
@@ -423,7 +286,8 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
       const int cur = s_cur, nrej = s_nrej;
       int badz = 0;
       const float *zr = table_row(a.tlog, a.tstride, a.tmap, a.C, b, nodef[cur], fo + cur, badz);
-      const int bonus = bonus_from_chunks<NT>(a, zr, a.part + (fo + cur) * (long long)a.nchunk * 2, w.rs0[cur],
+      const CdfRow cdf{a.cdf_span, a.cdf_nch, a.V, a.vec4t, a.T};
+      const int bonus = bonus_from_chunks<NT>(cdf, zr, a.part + (fo + cur) * (long long)a.nchunk * 2, w.rs0[cur],
                                               w.uni[0], rej, w.rejw, nrej, redd, redi, w.cdf_tsum, w.rejbits);
       if (t == 0) w.otok[alen] = bonus;
       badp |= badz;

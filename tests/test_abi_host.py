@@ -180,6 +180,20 @@ def test_lm_head_argument_checks(lib):
     assert call(w=None) == E.ET_ERR_INVALID_ARG
 
 
+def test_static_tree_sampled_argument_checks(lib):
+    cfg = E.StaticCfgC(2, 32000, 61, 1, 1.0)
+    need = lib.et_static_tree_workspace_size(ctypes.byref(cfg))
+    assert need == (2 * 61 * 8 * 2 * 4 + 255) // 256 * 256  # (max, sum) per 4096-token chunk of every row, 256-byte rounded
+    tree = E.TreeC(*([FAKE] * 10))
+    call = lambda c=cfg, u=FAKE, ws=FAKE, wsb=need: lib.et_static_tree_sampled(
+        ctypes.byref(c), FAKE, FAKE, 32000, FAKE, u, ctypes.byref(tree), None, ws, wsb, None)
+    assert call(c=E.StaticCfgC(2, 32000, 61, 1, 0.0)) == E.ET_ERR_INVALID_ARG   # temperature must be > 0
+    assert call(c=E.StaticCfgC(2, 40000, 61, 1, 1.0)) == E.ET_ERR_UNSUPPORTED   # one cluster covers 32768 tokens
+    assert call(u=None) == E.ET_ERR_INVALID_ARG
+    assert call(wsb=need - 1) == E.ET_ERR_WORKSPACE
+    assert call(ws=FAKE + 64) == E.ET_ERR_WORKSPACE
+
+
 def test_status_strings(lib):
     for s in range(6):
         assert E.status_string(s)

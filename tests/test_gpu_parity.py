@@ -610,3 +610,58 @@ def test_lm_head_logits_feed_the_expansion():
     for b in range(B):
         want = O.topk_children(table[b], k)
         assert list(g["cand_tok"][b][:k]) == list(want)
+
+
+SAMPLED_CASES = [(2, 1000, (3, 2, 1), 1.0), (2, 32000, (4, 2, 2, 1, 1), 1.0), (3, 5000, (6, 3), 0.7)]
+
+
+@pytest.mark.parametrize("B,V,widths,T", SAMPLED_CASES)
+def test_static_tree_sampled_matches_oracle(B, V, widths, T):
+    parent, _, table, rmap, root = _static_case(B, V, widths, False, seed=21)
+    N = parent.size
+    u = np.random.default_rng(V + B).random((B, N)).astype(np.float32)
+    tb = E.TreeBuffers.allocate_flat(B, N, root_tok=torch.from_numpy(root).cuda())
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    E.et_static_tree_sampled(B, V, T, torch.from_numpy(parent).cuda(), torch.from_numpy(table).cuda(),
+                             torch.from_numpy(rmap).cuda(), torch.from_numpy(u).cuda(), tb, dev_status=status)
+    g = gpu_tree_np(tb)
+    tok, fpar, fdep, node, gaps = O.static_tree_sampled(parent, table, rmap, u, T, root)
+    np.testing.assert_array_equal(g["flat_parent"], fpar)
+    np.testing.assert_array_equal(g["flat_depth"], fdep)
+    np.testing.assert_array_equal(g["flat_node"], node)
+    clear = gaps >= O.TIE_REL_CDF  # a uniform within 1e-5 of a CDF step may land on either side in fp32
+    clear[:, 0] = True
+    np.testing.assert_array_equal(g["flat_tok"][clear], tok[clear])
+    assert clear.mean() > 0.5  # high-entropy rows at V = 32000 have CDF steps of about 1e-5: many near ties
+    assert int(status.item()) == 0
+
+
+def test_static_tree_sampled_then_draftq_acceptance():
+    B, V, widths, T = 3, 32000, (4, 2, 2, 1, 1), 1.0
+    parent, _, draft, rmap, root = _static_case(B, V, widths, False, seed=5)
+    N, D = parent.size, len(widths)
+    rng = np.random.default_rng(77)
+    u_tree = rng.random((B, N)).astype(np.float32)
+    u_acc = rng.random((B, N)).astype(np.float32)
+    target = (draft + 0.5 * rng.standard_normal(draft.shape)).astype(np.float32)
+    tb = E.TreeBuffers.allocate_flat(B, N, root_tok=torch.from_numpy(root).cuda())
+    E.et_static_tree_sampled(B, V, T, torch.from_numpy(parent).cuda(), torch.from_numpy(draft).cuda(),
+                             torch.from_numpy(rmap).cuda(), torch.from_numpy(u_tree).cuda(), tb)
+    cfg = E.TreeCfg(B=B, V=V, depth=D, topk=4, m=4, n=N - 1, temperature=T)
+    ws = E.new_workspace(E.et_tree_workspace_size(cfg))
+    alen = torch.zeros(B, dtype=torch.int32, device="cuda")
+    path = torch.zeros((B, D + 1), dtype=torch.int32, device="cuda")
+    toks = torch.zeros((B, D + 1), dtype=torch.int32, device="cuda")
+    E.et_verify_accept(cfg, E.ET_ACCEPT_STOCH_DRAFTQ, tb, torch.from_numpy(target).cuda(), alen, path, toks, ws,
+                       draft_logits=torch.from_numpy(draft).cuda(), uniforms=torch.from_numpy(u_acc).cuda())
+    g = gpu_tree_np(tb)
+    ref = O.verify_accept(ocfg(cfg), O.STOCH_DRAFTQ, g["flat_tok"], g["flat_parent"], g["flat_node"], target, None,
+                          uniforms=u_acc, draft_table=draft, draft_row_of_node=None)
+    tied = {b for b, _, _ in ref.near_ties}
+    for b in range(B):
+        if b in tied:
+            continue
+        assert alen[b].item() == ref.accept_len[b]
+        np.testing.assert_array_equal(path[b].cpu().numpy(), ref.path[b])
+        np.testing.assert_array_equal(toks[b].cpu().numpy(), ref.tokens[b])
+    assert len(tied) < B

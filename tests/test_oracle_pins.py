@@ -651,3 +651,19 @@ def test_stoch_acceptance_depends_on_temperature():
                            tok, par, node, table, None, uniforms=u)
     assert hot.accept_len[0] == 1 and hot.tokens[0, 0] == 1
     assert cold.accept_len[0] == 0 and cold.tokens[0, 0] == 0  # rejected: the residual keeps token 0 only
+
+
+def test_static_tree_sampled_inverse_cdf_by_hand():
+    # q = softmax([0, ln 3, 0]) = (0.2, 0.6, 0.2): uniforms 0.1 / 0.5 / 0.9 pick tokens 0 / 1 / 2
+    parent = np.array([-1, 0, 0, 0], np.int32)
+    table = np.array([[0.0, np.log(3.0), 0.0]] + [[0.0, 0.0, 0.0]] * 3, np.float32)
+    u = np.array([[0.0, 0.1, 0.5, 0.9]], np.float32)
+    tok, fpar, fdep, node, gaps = O.static_tree_sampled(parent, table, np.array([[0, 1, 2, 3]], np.int32), u, 1.0,
+                                                        np.array([9], np.int32))
+    assert tok.tolist() == [[9, 0, 1, 2]]
+    assert fdep.tolist() == [[0, 1, 1, 1]]
+    np.testing.assert_allclose(gaps[0, 1:], [0.1, 0.3, 0.1], atol=1e-6)  # CDF steps at 0.2, 0.8, 1.0
+    # temperature 1/2 sharpens q to (0.1/1.1... ): (1, 9, 1) / 11 -> u = 0.5 still picks token 1, u = 0.95 token 2
+    tok2, *_ = O.static_tree_sampled(parent, table, np.array([[0, 1, 2, 3]], np.int32),
+                                     np.array([[0, 0.05, 0.5, 0.95]], np.float32), 0.5, np.array([9], np.int32))
+    assert tok2.tolist() == [[9, 0, 1, 2]]
