@@ -1,8 +1,8 @@
-// Inverse CDF of a softmax row from its chunk statistics: the row's tokens
-// are split in chunks of `span` tokens with (max, sum of exp) (Mc, Sc)
-// already known, so one warp finds the chunk where the cumulative weight
-// crosses uni * total and the block rescans that chunk alone.  Shared by the
-// bonus draw of the acceptance walk and the sampled static tree.
+// Inverse CDF of a row from its chunk statistics: the row's tokens are split
+// in chunks of `span` tokens whose weights (Mc, Sc) are already known, so one
+// warp finds the chunk where the cumulative weight crosses uni * total and the
+// block rescans that chunk alone.  Shared by the bonus draws of the acceptance
+// walk and the sampled static tree.
 #pragma once
 
 #include "et_common.cuh"
@@ -18,16 +18,15 @@ struct CdfRow {
 constexpr int kMaxSpan = 4096;                  // chunk tokens (the clustered phase 1)
 constexpr int kMaxSpanWords = kMaxSpan / 32;
 constexpr int kMaxPer = kMaxSpan / 256;         // tokens per thread in the chunk pass
-// The inverse CDF of the residual p of a row
-// (rejected children removed) from the row's chunk statistics.  Chunk c holds
-// tokens [c·span, (c+1)·span) with (max, sum of exp) (Mc, Sc) from phase 1, so
-// its weight is Sc·exp(Mc − M) minus the weights of the rejected children it
-// contains; one warp finds the chunk where the cumulative weight crosses
-// uni·total, then the block rescans that chunk alone (fp64 block scan).
-template <int NT>
-__device__ int bonus_from_chunks(const CdfRow &a, const float *zr, const float *cstat, float M, float uni,
-                                 const int *rej, const float *rejw, int nrej, double *redd, int *redi,
-                                 double *tsum, unsigned int *rejbits) {
+// Chunk c holds tokens [c·span, (c+1)·span) with statistics (Mc, Sc): its
+// weight is Sc·exp(Mc − M) minus the weights of the rejected tokens it
+// contains.  The rescan weighs token v as wf(zt, zd), zt and zd its sanitised
+// target and draft logits (zd = −inf without a draft row), rejected tokens 0;
+// wf must give the weights the chunk statistics sum.
+template <int NT, bool kDraft, typename WF>
+__device__ int chunk_inverse_cdf(const CdfRow &a, const float *zr, const float *dr, int vec4d, const float *cstat,
+                                 float M, float uni, const int *rej, const float *rejw, int nrej, double *redd,
+                                 int *redi, double *tsum, unsigned int *rejbits, WF wf) {
   const int t = threadIdx.x, lane = t & 31, wp = t >> 5;
   const int span = a.span, nch = a.nch;
   if (t == 0) { redi[0] = 0x7fffffff; redi[1] = -1; }
@@ -96,7 +95,6 @@ __device__ int bonus_from_chunks(const CdfRow &a, const float *zr, const float *
   const int per = span / NT;
   const int v0 = J * span + t * per;
   float x[kMaxPer];
-  const float invT = 1.f / a.T;
   float mine = 0.f;
   int lastv = -1;
 #pragma unroll
@@ -109,13 +107,24 @@ __device__ int bonus_from_chunks(const CdfRow &a, const float *zr, const float *
 #pragma unroll
       for (int e = 0; e < 4; ++e) z4[e] = (j + e < per && v0 + j + e < a.V) ? zr[v0 + j + e] : -INFINITY;
     }
+    float d4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    if (kDraft && dr) {
+      if (j < per && vec4d && v0 + j + 3 < a.V) {
+        const float4 f = *reinterpret_cast<const float4 *>(dr + v0 + j);
+        d4[0] = f.x; d4[1] = f.y; d4[2] = f.z; d4[3] = f.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) d4[e] = (j + e < per && v0 + j + e < a.V) ? dr[v0 + j + e] : -INFINITY;
+      }
+    }
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int jj = j + e, off = t * per + jj;
       int f2 = 0;
-      const float y = sanitize_logit(z4[e], f2) * invT;
+      const float zt = sanitize_logit(z4[e], f2);
+      const float zd = kDraft ? sanitize_logit(d4[e], f2) : -INFINITY;
       const bool rejected = jj < per && ((rejbits[off >> 5] >> (off & 31)) & 1u);
-      x[jj] = (jj < per && !rejected && y > -INFINITY) ? exp_fast(y - M) : 0.f;  // as the chunk sums
+      x[jj] = (jj < per && !rejected) ? wf(zt, zd) : 0.f;
       mine += x[jj];
       if (x[jj] > 0.f) lastv = v0 + jj;
     }
@@ -151,6 +160,20 @@ __device__ int bonus_from_chunks(const CdfRow &a, const float *zr, const float *
   const int r = redi[0] != 0x7fffffff ? redi[0] : redi[1];
   __syncthreads();
   return r;
+}
+
+// The inverse CDF of the softmax row p at temperature T (rejected children
+// removed) from its chunk statistics (max, sum of exp(z/T − max)).
+template <int NT>
+__device__ int bonus_from_chunks(const CdfRow &a, const float *zr, const float *cstat, float M, float uni,
+                                 const int *rej, const float *rejw, int nrej, double *redd, int *redi,
+                                 double *tsum, unsigned int *rejbits) {
+  const float invT = 1.f / a.T;
+  return chunk_inverse_cdf<NT, false>(a, zr, nullptr, 0, cstat, M, uni, rej, rejw, nrej, redd, redi, tsum, rejbits,
+                                      [&](float zt, float) -> float {
+                                        const float y = zt * invT;
+                                        return y > -INFINITY ? exp_fast(y - M) : 0.f;  // as the chunk sums
+                                      });
 }
 
 }  // namespace

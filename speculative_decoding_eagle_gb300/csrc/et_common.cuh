@@ -258,6 +258,13 @@ __device__ __forceinline__ void cl_st_u64(uint32_t addr, unsigned long long v) {
 __device__ __forceinline__ void cl_st_f32x2(uint32_t addr, float a, float b) {
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
+__device__ __forceinline__ void cl_st_f32(uint32_t addr, float a) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(a) : "memory");
+}
+__device__ __forceinline__ void cl_st_f32x4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
 
 // ---- (value desc, id asc) as one ascending 64-bit key ----
 // high word: the order-reversed image of z (larger z -> smaller word; -0 and

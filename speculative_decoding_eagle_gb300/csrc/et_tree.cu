@@ -700,7 +700,7 @@ using namespace et;
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct TreeWs {
-  size_t cnt_bytes, part_off, rowstat_off, total;
+  size_t cnt_bytes, part_off, rowstat_off, dq_off, total;
   int rows;  // max rows of one launch
 };
 
@@ -718,7 +718,9 @@ static TreeWs tree_ws_layout(const et_tree_cfg *cfg) {
   w.part_off = w.cnt_bytes;
   const size_t part = align256(exp_part > ver_part ? exp_part : ver_part);
   w.rowstat_off = w.part_off + part;
-  w.total = w.rowstat_off + align256(sizeof(float) * 2 * (size_t)cfg->B * N);
+  // draft-q acceptance: per flat row q's max and sum and the residual pairs (c, F)
+  w.dq_off = w.rowstat_off + align256(sizeof(float) * 2 * (size_t)cfg->B * N);
+  w.total = w.dq_off + align256(sizeof(float) * 8 * (size_t)cfg->B * N);
   return w;
 }
 
@@ -730,8 +732,9 @@ extern "C" size_t et_tree_workspace_size(const et_tree_cfg *cfg) {
 
 // used by et_verify.cu; not part of the ABI
 extern "C" __attribute__((visibility("hidden"))) size_t et_internal_tree_ws(const et_tree_cfg *cfg, size_t *cnt_bytes, size_t *part_off,
-                                      size_t *rowstat_off) {
+                                      size_t *rowstat_off, size_t *dq_off) {
   TreeWs w = tree_ws_layout(cfg);
+  *dq_off = w.dq_off;
   *cnt_bytes = w.cnt_bytes;
   *part_off = w.part_off;
   *rowstat_off = w.rowstat_off;

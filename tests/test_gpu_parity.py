@@ -309,9 +309,12 @@ def test_tcgen05_and_mma_paths_agree_at_the_7b_shape():
 # acceptance, given the oracle's flat tree
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("mode", [E.ET_ACCEPT_GREEDY, E.ET_ACCEPT_STOCH_POINT, E.ET_ACCEPT_STOCH_DRAFTQ])
-@pytest.mark.parametrize("wl_name,B", [("tiny", 4), ("llama2-7b", 2)])
-def test_verify_matches_oracle(mode, wl_name, B):
+@pytest.mark.parametrize("wl_name,B,V", [("tiny", 4, None), ("llama2-7b", 2, None), ("tiny", 3, 50000)])
+def test_verify_matches_oracle(mode, wl_name, B, V):
+    """V = 50000 is past one cluster (32768 tokens): one block per 2048-token chunk, merged by the last."""
     wl = W.WORKLOADS[wl_name].with_(B=B, temperature=0.7 if mode == E.ET_ACCEPT_STOCH_DRAFTQ else 1.0)
+    if V is not None:
+        wl = wl.with_(V=V)
     cfg = S.tree_cfg(wl)
     C = E.et_num_candidates(cfg)
     h = S.host_inputs(wl, C)
@@ -331,6 +334,42 @@ def test_verify_matches_oracle(mode, wl_name, B):
         np.testing.assert_array_equal(st.path[b].cpu().numpy(), ref.path[b])
         np.testing.assert_array_equal(st.tokens[b].cpu().numpy(), ref.tokens[b])
     assert len(bad_b) < B
+    assert int(st.dev_status.item()) == 0
+
+
+@pytest.mark.parametrize("wl_name,B,V,T,squeeze", [("tiny", 8, None, 1.3, 0.1), ("llama2-7b", 4, None, 0.7, 0.02),
+                                                    ("tiny", 4, 50000, 0.7, 0.02)])
+def test_draftq_chained_rejections(wl_name, B, V, T, squeeze):
+    """Uniforms pushed toward 1 reject several children in a row: the residual
+    after each rejection (its sum from phase 1, replayed per token by the walk)
+    and the bonus draw from the last residual, on both phase-1 layouts."""
+    wl = W.WORKLOADS[wl_name].with_(B=B, temperature=T)
+    if V is not None:
+        wl = wl.with_(V=V)
+    cfg = S.tree_cfg(wl)
+    C = E.et_num_candidates(cfg)
+    h = S.host_inputs(wl, C)
+    h["uniforms"] = (1.0 - (1.0 - h["uniforms"].astype(np.float64)) * squeeze).astype(np.float32)
+    ot = O.build_tree(ocfg(cfg), h["draft"], h["row_of_node"], h["root_tok"])
+    ref = O.verify_accept(ocfg(cfg), O.STOCH_DRAFTQ, ot.flat_tok, ot.flat_parent, ot.flat_node, h["target"],
+                          h["row_of_node"], uniforms=h["uniforms"], draft_table=h["draft"],
+                          draft_row_of_node=h["row_of_node"])
+    inp = S.to_device(wl, h)
+    st = S.VerifyStep(wl, mode=E.ET_ACCEPT_STOCH_DRAFTQ)
+    upload_oracle_tree(ot, st.tree)
+    st.accept(inp)
+    torch.cuda.synchronize()
+    bad_b = {b for b, _, _ in ref.near_ties}
+    multi = 0
+    for b in range(B):
+        if b in bad_b:
+            continue
+        a = int(ref.accept_len[b])
+        multi += int((ot.flat_parent[b] == ref.path[b][a]).sum()) >= 2
+        assert st.accept_len[b].item() == a
+        np.testing.assert_array_equal(st.path[b].cpu().numpy(), ref.path[b])
+        np.testing.assert_array_equal(st.tokens[b].cpu().numpy(), ref.tokens[b])
+    assert len(bad_b) < B and multi >= 1  # at least one bonus drawn after two or more rejections
     assert int(st.dev_status.item()) == 0
 
 
