@@ -22,59 +22,60 @@ constexpr int kMaxPer = kMaxSpan / 256;         // tokens per thread in the chun
 // weight is Sc·exp(Mc − M) minus the weights of the rejected tokens it
 // contains.  The rescan weighs token v as wf(zt, zd), zt and zd its sanitised
 // target and draft logits (zd = −inf without a draft row), rejected tokens 0;
-// wf must give the weights the chunk statistics sum.
+// wf must give the weights the chunk statistics sum.  Sums are fp32 (the
+// weights themselves are fp32 values with ~1e-7 relative error); the threshold
+// inside the crossing chunk is taken relative to the chunk's start.
 template <int NT, bool kDraft, typename WF>
 __device__ int chunk_inverse_cdf(const CdfRow &a, const float *zr, const float *dr, int vec4d, const float *cstat,
-                                 float M, float uni, const int *rej, const float *rejw, int nrej, double *redd,
-                                 int *redi, double *tsum, unsigned int *rejbits, WF wf) {
+                                 float M, float uni, const int *rej, const float *rejw, int nrej, float *redf,
+                                 int *redi, float *tsum, unsigned int *rejbits, WF wf) {
   const int t = threadIdx.x, lane = t & 31, wp = t >> 5;
   const int span = a.span, nch = a.nch;
   if (t == 0) { redi[0] = 0x7fffffff; redi[1] = -1; }
   if (wp == 0) {
-    double total = 0.0;
+    float total = 0.f;
     for (int c0 = 0; c0 < nch; c0 += 32) {
       const int c = c0 + lane;
-      double wc = 0.0;
+      float wc = 0.f;
       if (c < nch) {
         const float mc = ld_cg(cstat + 2 * c), sc = ld_cg(cstat + 2 * c + 1);
-        wc = mc > -INFINITY ? (double)sc * (double)expf(mc - M) : 0.0;
+        wc = mc > -INFINITY ? sc * expf(mc - M) : 0.f;
         const int lo = c * span, hi = lo + span;
         for (int q = 0; q < nrej; ++q)
-          if (rej[q] >= lo && rej[q] < hi) wc -= (double)rejw[q];
-        wc = wc > 0.0 ? wc : 0.0;
+          if (rej[q] >= lo && rej[q] < hi) wc -= rejw[q];
+        wc = fmaxf(wc, 0.f);
         tsum[c] = wc;
       }
-      total += warp_sum_d(wc);
+      total += warp_sum(wc);
     }
-    const double thr = (double)uni * total;
-    double run = 0.0, before = 0.0;
+    const float thr = uni * total;
+    float run = 0.f, rel = 0.f;
     int J = -1, lastc = -1;
     for (int c0 = 0; c0 < nch; c0 += 32) {
       const int c = c0 + lane;
-      const double wc = c < nch ? tsum[c] : 0.0;
-      double incl = wc;
+      const float wc = c < nch ? tsum[c] : 0.f;
+      float incl = wc;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, incl, o);
+        const float y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
       }
-      const unsigned int pos = __ballot_sync(0xffffffffu, c < nch && wc > 0.0);
+      const unsigned int pos = __ballot_sync(0xffffffffu, c < nch && wc > 0.f);
       if (pos) lastc = c0 + 31 - __clz(pos);
-      const unsigned int hit = __ballot_sync(0xffffffffu, c < nch && wc > 0.0 && run + incl > thr);
+      const unsigned int hit = __ballot_sync(0xffffffffu, c < nch && wc > 0.f && run + incl > thr);
       if (hit && J < 0) {
         const int l = __ffs(hit) - 1;
         J = c0 + l;
-        before = run + __shfl_sync(0xffffffffu, incl, l) - __shfl_sync(0xffffffffu, wc, l);
+        rel = thr - (run + __shfl_sync(0xffffffffu, incl, l) - __shfl_sync(0xffffffffu, wc, l));
       }
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (J < 0) {  // thr at or beyond the total (rounding): the last chunk with weight
       J = lastc;
-      before = -1.0;
+      rel = -1.f;
     }
     if (lane == 0) {
-      redd[0] = before;
-      redd[1] = thr;
+      redf[0] = rel;  // the threshold relative to chunk J's start; < 0: take its last token
       redi[2] = J;
     }
   }
@@ -129,28 +130,28 @@ __device__ int chunk_inverse_cdf(const CdfRow &a, const float *zr, const float *
       if (x[jj] > 0.f) lastv = v0 + jj;
     }
   }
-  double incl = (double)mine;
+  float incl = mine;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_up_sync(0xffffffffu, incl, o);
+    const float y = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += y;
   }
-  if (lane == 31) tsum[wp] = incl;
+  if (lane == 31) tsum[wp] = incl;  // the chunk weights are no longer needed
   if (lastv >= 0) atomicMax(&redi[1], lastv);
   __syncthreads();
-  const double before = redd[0], thr = redd[1];
-  if (before >= 0.0) {
-    double base = before + incl - (double)mine;
-    for (int x2 = 0; x2 < wp; ++x2) base += tsum[x2];
-    // the threshold relative to this thread's run, then an fp32 walk over its tokens
-    const double rel = thr - base;
-    if (rel < (double)mine) {
+  const float relJ = redf[0];
+  if (relJ >= 0.f) {
+    float wbase = 0.f;
+    for (int x2 = 0; x2 < wp; ++x2) wbase += tsum[x2];
+    // the threshold relative to this thread's run, then a walk over its tokens
+    const float rel = relJ - (wbase + (incl - mine));
+    if (rel < mine) {
       float run = 0.f;
 #pragma unroll
       for (int jj = 0; jj < kMaxPer; ++jj) {
         if (jj >= per) break;
         run += x[jj];
-        if (x[jj] > 0.f && (double)run > rel) { atomicMin(&redi[0], v0 + jj); break; }
+        if (x[jj] > 0.f && run > rel) { atomicMin(&redi[0], v0 + jj); break; }
       }
     }
   }
@@ -166,10 +167,10 @@ __device__ int chunk_inverse_cdf(const CdfRow &a, const float *zr, const float *
 // removed) from its chunk statistics (max, sum of exp(z/T − max)).
 template <int NT>
 __device__ int bonus_from_chunks(const CdfRow &a, const float *zr, const float *cstat, float M, float uni,
-                                 const int *rej, const float *rejw, int nrej, double *redd, int *redi,
-                                 double *tsum, unsigned int *rejbits) {
+                                 const int *rej, const float *rejw, int nrej, float *redf, int *redi,
+                                 float *tsum, unsigned int *rejbits) {
   const float invT = 1.f / a.T;
-  return chunk_inverse_cdf<NT, false>(a, zr, nullptr, 0, cstat, M, uni, rej, rejw, nrej, redd, redi, tsum, rejbits,
+  return chunk_inverse_cdf<NT, false>(a, zr, nullptr, 0, cstat, M, uni, rej, rejw, nrej, redf, redi, tsum, rejbits,
                                       [&](float zt, float) -> float {
                                         const float y = zt * invT;
                                         return y > -INFINITY ? exp_fast(y - M) : 0.f;  // as the chunk sums

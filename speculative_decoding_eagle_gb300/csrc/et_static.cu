@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kStThreads) k_static_stats(SampledArgs a) {
 }
 
 __global__ void __launch_bounds__(kStThreads) k_static_draw(SampledArgs a) {
-  __shared__ double redd[32], tsum[32];
+  __shared__ float redf[32], tsum[32];
   __shared__ int redi[32];
   __shared__ unsigned int rejbits[kMaxSpanWords];
   pdl_wait();     // the previous kernel in the stream has completed
@@ -247,7 +247,7 @@ __global__ void __launch_bounds__(kStThreads) k_static_draw(SampledArgs a) {
   float M = -INFINITY;
   for (int x = 0; x < a.R; ++x) M = fmaxf(M, ld_cg(cst + 2 * x));
   const CdfRow cdf{kStSpan, a.R, a.V, a.vec4, a.T};
-  const int tok = bonus_from_chunks<kStThreads>(cdf, zr, cst, M, a.uniforms[fo + i], nullptr, nullptr, 0, redd, redi,
+  const int tok = bonus_from_chunks<kStThreads>(cdf, zr, cst, M, a.uniforms[fo + i], nullptr, nullptr, 0, redf, redi,
                                                 tsum, rejbits);
   if (threadIdx.x == 0) a.flat_tok[fo + i] = tok;
 }

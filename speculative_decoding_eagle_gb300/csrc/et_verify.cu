@@ -34,7 +34,8 @@ struct VerifyArgs {
   int32_t *accept_len, *path, *tokens, *dev_status;
   float *part;        // [B*N][nchunk][2]
   float *rowstat;     // [B*N][2]
-  float *dq;          // [B*N][8] draft-q: q's max and sum, final (c, F) at the row; (c, F) as a child; 2 spare
+  float *dq;          // [B*N][8]: draft-q q's max and sum and final (c, F) at the row, (c, F) as a child;
+                      // the target and draft logits of the row's token in its parent's row
   unsigned int *row_cnt, *seq_cnt;
   int vec4t, vec4d;       // 16-byte aligned target / draft rows
   int cdf_span, cdf_nch;  // chunk statistics of each row in part: span tokens each, nch chunks
@@ -68,6 +69,26 @@ __device__ __forceinline__ float dq_weight(float y, float M, float inv_sum) {
 }
 __device__ __forceinline__ float dq_excess(float p, float q, float c) { return fmaxf(fmaf(-c, q, p), 0.f); }
 
+// Phase 1 of a row with children (stochastic modes): the block holding token
+// x_j of each child j in [lo, hi) stores the target (and draft) logit of x_j
+// at this row into j's record, so the walk reads one value per child; block
+// 0 covers tokens outside [0, V).
+__device__ __forceinline__ void store_child_logits(const VerifyArgs &a, long long fo, const int *kid, int nkid,
+                                                   const float *zrow, const float *drow, int lo, int hi, bool first) {
+  for (int k = threadIdx.x; k < nkid; k += blockDim.x) {
+    const long long j = fo + kid[k];
+    const int x = a.flat_tok[j];
+    const bool ok = x >= 0 && x < a.V;
+    if (ok ? (x >= lo && x < hi) : first) {
+      int f2 = 0;
+      a.dq[8 * j + 6] = (zrow && ok) ? sanitize_logit(__ldg(zrow + x), f2) : -INFINITY;
+      if (drow) a.dq[8 * j + 7] = ok ? sanitize_logit(__ldg(drow + x), f2) : -INFINITY;
+      if (!ok && drow) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
+      __threadfence();  // device-wide before this block's next barrier (the walk may run in another cluster)
+    }
+  }
+}
+
 // The children of row i (rows after i whose parent is i), in row order, by
 // warp 0; every thread gets the count.  parents = the sequence's flat_parent.
 template <int NT>
@@ -91,8 +112,7 @@ __device__ int child_list(const int32_t *parents, int N, int i, int *list, int *
 struct WalkSmem {
   float redz[32];
   int redi[32];
-  double redd[32];
-  double cdf_tsum[kMaxV / kVChunk];  // per chunk weights of the bonus draw
+  float cdf_tsum[kMaxV / kVChunk];  // per chunk weights of the bonus draw
   int par[kMaxN], tokf[kMaxN], nodef[kMaxN];
   float rs0[kMaxN], rs1[kMaxN];  // per flat row: argmax id (bits) / max, -, / sum
   float qs0[kMaxN], qs1[kMaxN];  // draft-q: max and sum of q at each row
@@ -131,26 +151,17 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
     w.rs0[j] = ld_cg(a.rowstat + 2 * (fo + j));
     w.rs1[j] = ld_cg(a.rowstat + 2 * (fo + j) + 1);
     if (!greedy) w.uni[j] = a.uniforms[fo + j];
-    if (dq) {
-      const float4 s4 = ld_cg(reinterpret_cast<const float4 *>(a.dq) + 2 * (fo + j));
-      const float2 s2 = ld_cg(reinterpret_cast<const float2 *>(a.dq) + 4 * (fo + j) + 2);
-      w.qs0[j] = s4.x;
-      w.qs1[j] = s4.y;
-      w.cf[j] = s4.z;
-      w.cb[j] = s2.x;
-      w.Fb[j] = s2.y;
-    }
-    if (!greedy && j > 0) {
-      const bool okp = p >= 0 && p < N, okx = x >= 0 && x < a.V;
-      int f2 = 0;
-      const float *zp = okp ? table_row(a.tlog, a.tstride, a.tmap, a.C, b, a.flat_node[fo + p], fo + p, badp)
-                            : nullptr;
-      w.zc[j] = (zp && okx) ? sanitize_logit(zp[x], f2) : -INFINITY;
+    if (!greedy) {  // the row's record, written in phase 1
+      const float4 hi4 = ld_cg(reinterpret_cast<const float4 *>(a.dq) + 2 * (fo + j) + 1);
+      w.zc[j] = (j > 0 && p >= 0 && p < j) ? hi4.z : -INFINITY;
       if (dq) {
-        const float *dp = okp ? table_row(a.dlog, a.dstride, a.dmap, a.C, b, a.flat_node[fo + p], fo + p, badp)
-                              : nullptr;
-        w.dc[j] = (dp && okx) ? sanitize_logit(dp[x], f2) : -INFINITY;
-        if (!okx) badp = 1;
+        const float4 lo4 = ld_cg(reinterpret_cast<const float4 *>(a.dq) + 2 * (fo + j));
+        w.qs0[j] = lo4.x;
+        w.qs1[j] = lo4.y;
+        w.cf[j] = lo4.z;
+        w.cb[j] = hi4.x;
+        w.Fb[j] = hi4.y;
+        w.dc[j] = (j > 0 && p >= 0 && p < j) ? hi4.w : -INFINITY;
       }
     }
   }
@@ -251,13 +262,13 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
       const float *dr = table_row(a.dlog, a.dstride, a.dmap, a.C, b, nodef[cur], fo + cur, badz);
       const float M = w.rs0[cur], S = w.rs1[cur], Mq = w.qs0[cur], Sq = w.qs1[cur], c = w.cf[cur];
       const float invS = S > 0.f ? 1.f / S : 0.f, invSq = Sq > 0.f ? 1.f / Sq : 0.f;
-      bonus = chunk_inverse_cdf<NT, true>(cdf, zr, dr, a.vec4d, cst, M, w.uni[0], nullptr, nullptr, 0, w.redd,
+      bonus = chunk_inverse_cdf<NT, true>(cdf, zr, dr, a.vec4d, cst, M, w.uni[0], nullptr, nullptr, 0, w.redz,
                                           w.redi, w.cdf_tsum, w.rejbits, [&](float zt, float zd) -> float {
                                             return dq_excess(dq_weight(__fmul_rn(zt, invT), M, invS),
                                                              dq_weight(__fmul_rn(zd, invT), Mq, invSq), c);
                                           });
     } else {  // point-mass residual (rejected children removed), or a leaf: p itself
-      bonus = bonus_from_chunks<NT>(cdf, zr, cst, w.rs0[cur], w.uni[0], rej, w.rejw, dq ? 0 : w.s_nrej, w.redd,
+      bonus = bonus_from_chunks<NT>(cdf, zr, cst, w.rs0[cur], w.uni[0], rej, w.rejw, dq ? 0 : w.s_nrej, w.redz,
                                     w.redi, w.cdf_tsum, w.rejbits);
     }
     if (t == 0) w.otok[alen] = bonus;
@@ -357,6 +368,14 @@ __global__ void __launch_bounds__(kVThreads) k_verify(VerifyArgs a) {
 #pragma unroll
     for (int j = 0; j < 4; ++j)
       if (e0 + j < a.V) v[4 * u + j] = sanitize_logit(v[4 * u + j], flag);
+  }
+  if (a.mode != ET_ACCEPT_GREEDY) {  // children's logits at this row, from the block holding their token
+    const int i = row - b * a.N;
+    const long long fo = (long long)row - i;
+    const int nkid = child_list<kVThreads>(a.flat_parent + fo, a.N, i, w.kid, &w.s_nkid);
+    const float *drow = (a.mode == ET_ACCEPT_STOCH_DRAFTQ && nkid > 0)
+                            ? table_row(a.dlog, a.dstride, a.dmap, a.C, b, node, row, bad) : nullptr;
+    if (nkid > 0) store_child_logits(a, fo, w.kid, nkid, zrow, drow, c0, c0 + kVChunk, c == 0);
   }
   float *prt = a.part + ((long long)row * a.nchunk + c) * 2;
   if (a.mode == ET_ACCEPT_GREEDY) {
@@ -476,12 +495,14 @@ __global__ void __launch_bounds__(kVClThreads) k_verify_cl(VerifyArgs a) {
   float v[4 * kVClVec];
   cl_load_span(zrow, base, a.vec4t, a.V, v, flag);
   const bool greedy = a.mode == ET_ACCEPT_GREEDY;
+  const long long fo = (long long)row - i;
   int nkid = 0;
-  if (kDraftQ)  // the children of this row (every block of the cluster finds the same)
-    nkid = child_list<kVClThreads>(a.flat_parent + (long long)b * a.N, a.N, i, w.kid, &w.s_nkid);
-  if (nkid > 0) {
+  if (!greedy)  // the children of this row (every block of the cluster finds the same)
+    nkid = child_list<kVClThreads>(a.flat_parent + fo, a.N, i, w.kid, &w.s_nkid);
+  const float *drow = (kDraftQ && nkid > 0) ? table_row(a.dlog, a.dstride, a.dmap, a.C, b, node, row, bad) : nullptr;
+  if (nkid > 0) store_child_logits(a, fo, w.kid, nkid, zrow, drow, base, base + kVClSpan, q == 0);
+  if (kDraftQ && nkid > 0) {
     const float invT = 1.f / a.T;
-    const float *drow = table_row(a.dlog, a.dstride, a.dmap, a.C, b, node, row, bad);
     float d[4 * kVClVec];
     cl_load_span(drow, base, a.vec4d, a.V, d, flag);
     float lm = -INFINITY, lq = -INFINITY;
@@ -533,7 +554,6 @@ __global__ void __launch_bounds__(kVClThreads) k_verify_cl(VerifyArgs a) {
       v[e] = dq_weight(v[e], M, invS);    // p
       d[e] = dq_weight(d[e], Mq, invSq);  // q
     }
-    const long long fo = (long long)row - i;
     float c = 0.f, F = 1.f;  // the residual in force: max(p - c q, 0) / F
     for (int k = 0; k < nkid; ++k) {  // each child in row order: one rejection more
       if (q == 0 && t == 0) {
