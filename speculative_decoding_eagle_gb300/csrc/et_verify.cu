@@ -34,8 +34,9 @@ struct VerifyArgs {
   int32_t *accept_len, *path, *tokens, *dev_status;
   float *part;        // [B*N][nchunk][2]
   float *rowstat;     // [B*N][2]
-  float *dq;          // [B*N][8]: draft-q q's max and sum and final (c, F) at the row, (c, F) as a child;
-                      // the target and draft logits of the row's token in its parent's row
+  float *dq;          // [B*N][8] per flat row: draft-q q's max and sum, the residual's c once every child is
+                      // rejected, the accepted child (int bits: row, -1 leaf, -2 all rejected); [6] point-mass:
+                      // the target logit of the row's token in its parent's row
   unsigned int *row_cnt, *seq_cnt;
   int vec4t, vec4d;       // 16-byte aligned target / draft rows
   int cdf_span, cdf_nch;  // chunk statistics of each row in part: span tokens each, nch chunks
@@ -61,20 +62,20 @@ __device__ __forceinline__ const float *table_row(const float *tab, long long st
 // (c, F) = (0, 1) at first, and a rejection moves to c' = c + F, F' = F(c')
 // (when F' > 0), because max(max(p - c q, 0) / F - q, 0) = max(p - c' q, 0) / F.
 // The pairs depend on the row and on how many children were rejected, not on
-// which tokens they were, so phase 1 computes them for every row in parallel
-// and the walk and the bonus draw evaluate r token by token.  Both sides use
-// these functions in the same order, so they agree to the bit.
+// which tokens they were, and a child's test needs only p and q at its token,
+// so phase 1 decides every row's acceptance in parallel (stopping at the first
+// accepted child) and the walk follows the accepted children.
 __device__ __forceinline__ float dq_weight(float y, float M, float inv_sum) {
   return y > -INFINITY ? exp_fast(y - M) * inv_sum : 0.f;
 }
 __device__ __forceinline__ float dq_excess(float p, float q, float c) { return fmaxf(fmaf(-c, q, p), 0.f); }
 
-// Phase 1 of a row with children (stochastic modes): the block holding token
-// x_j of each child j in [lo, hi) stores the target (and draft) logit of x_j
-// at this row into j's record, so the walk reads one value per child; block
-// 0 covers tokens outside [0, V).
+// Phase 1 of a row with children (point-mass): the block holding token x_j
+// of each child j in [lo, hi) stores the target logit of x_j at this row into
+// j's record, so the walk reads one value per child; block 0 covers tokens
+// outside [0, V).
 __device__ __forceinline__ void store_child_logits(const VerifyArgs &a, long long fo, const int *kid, int nkid,
-                                                   const float *zrow, const float *drow, int lo, int hi, bool first) {
+                                                   const float *zrow, int lo, int hi, bool first) {
   for (int k = threadIdx.x; k < nkid; k += blockDim.x) {
     const long long j = fo + kid[k];
     const int x = a.flat_tok[j];
@@ -82,11 +83,21 @@ __device__ __forceinline__ void store_child_logits(const VerifyArgs &a, long lon
     if (ok ? (x >= lo && x < hi) : first) {
       int f2 = 0;
       a.dq[8 * j + 6] = (zrow && ok) ? sanitize_logit(__ldg(zrow + x), f2) : -INFINITY;
-      if (drow) a.dq[8 * j + 7] = ok ? sanitize_logit(__ldg(drow + x), f2) : -INFINITY;
-      if (!ok && drow) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
       __threadfence();  // device-wide before this block's next barrier (the walk may run in another cluster)
     }
   }
+}
+
+// Draft-q test of one child from p and q at its token and the residual
+// (c, F) in force: u < min(1, r(x) / q(x)).  Phase 1 evaluates it identically
+// in every block of a row's cluster.
+__device__ __forceinline__ bool dq_accept(float zt, float zd, bool ok, float u, float invT, float M, float invS,
+                                          float Mq, float invSq, float c, float F) {
+  const float qx = dq_weight(__fmul_rn(zd, invT), Mq, invSq);
+  const float px = dq_weight(__fmul_rn(zt, invT), M, invS);
+  const float r = F > 0.f ? dq_excess(px, qx, c) / F : 0.f;
+  const float ratio = qx <= 0.f ? 1.f : fminf(1.f, r / qx);
+  return ok && u < ratio;
 }
 
 // The children of row i (rows after i whose parent is i), in row order, by
@@ -117,9 +128,9 @@ struct WalkSmem {
   float rs0[kMaxN], rs1[kMaxN];  // per flat row: argmax id (bits) / max, -, / sum
   float qs0[kMaxN], qs1[kMaxN];  // draft-q: max and sum of q at each row
   float zc[kMaxN];               // target logit of each row's token in its parent's row
-  float dc[kMaxN];               // draft-q: draft logit of each row's token in its parent's row
-  float cb[kMaxN], Fb[kMaxN];    // draft-q: (c, F) of the residual in force when a row's token is tested
+  float dc[kMaxN];               // phase 1, draft-q: draft logit of each child's token (by child rank)
   float cf[kMaxN];               // draft-q: c of the residual once all of a row's children are rejected
+  int acc[kMaxN];                // draft-q: accepted child of each row (-1 leaf, -2 all rejected)
   int kid[kMaxN];                // phase 1: the children of the block's row
   int opath[kMaxDepth + 2], otok[kMaxDepth + 2];
   int rej[kMaxTopk];
@@ -151,18 +162,15 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
     w.rs0[j] = ld_cg(a.rowstat + 2 * (fo + j));
     w.rs1[j] = ld_cg(a.rowstat + 2 * (fo + j) + 1);
     if (!greedy) w.uni[j] = a.uniforms[fo + j];
-    if (!greedy) {  // the row's record, written in phase 1
-      const float4 hi4 = ld_cg(reinterpret_cast<const float4 *>(a.dq) + 2 * (fo + j) + 1);
-      w.zc[j] = (j > 0 && p >= 0 && p < j) ? hi4.z : -INFINITY;
-      if (dq) {
-        const float4 lo4 = ld_cg(reinterpret_cast<const float4 *>(a.dq) + 2 * (fo + j));
-        w.qs0[j] = lo4.x;
-        w.qs1[j] = lo4.y;
-        w.cf[j] = lo4.z;
-        w.cb[j] = hi4.x;
-        w.Fb[j] = hi4.y;
-        w.dc[j] = (j > 0 && p >= 0 && p < j) ? hi4.w : -INFINITY;
-      }
+    if (dq) {  // the row's record, written in phase 1
+      const float4 lo4 = ld_cg(reinterpret_cast<const float4 *>(a.dq) + 2 * (fo + j));
+      w.qs0[j] = lo4.x;
+      w.qs1[j] = lo4.y;
+      w.cf[j] = lo4.z;
+      const int ac = __float_as_int(lo4.w);
+      w.acc[j] = (ac > j && ac < N) || ac == -2 ? ac : -1;
+    } else if (!greedy) {
+      w.zc[j] = (j > 0 && p >= 0 && p < j) ? ld_cg(a.dq + 8 * (fo + j) + 6) : -INFINITY;
     }
   }
   __syncthreads();
@@ -212,27 +220,10 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
           if (hit) nxt = j0 + __ffs(hit) - 1;
         }
         if (nrej > kMaxTopk) nrej = kMaxTopk;
-      } else {
-        // draft-q: child j is accepted when u_j < min(1, r(x_j) / q(x_j)), r
-        // the residual left by the siblings rejected before it: (c, F) from phase 1
-        const float M = w.rs0[cur], S = w.rs1[cur], Mq = w.qs0[cur], Sq = w.qs1[cur];
-        const float invS = S > 0.f ? 1.f / S : 0.f, invSq = Sq > 0.f ? 1.f / Sq : 0.f;
-        for (int j0 = cur + 1; j0 < N && nxt < 0; j0 += 32) {
-          const int j = j0 + lane;
-          const bool child = j < N && par[j] == cur;
-          bool acc = false;
-          if (child) {
-            const float qx = dq_weight(__fmul_rn(w.dc[j], invT), Mq, invSq);
-            const float px = dq_weight(__fmul_rn(w.zc[j], invT), M, invS);
-            const float Fj = w.Fb[j];
-            const float r = Fj > 0.f ? dq_excess(px, qx, w.cb[j]) / Fj : 0.f;
-            const float ratio = qx <= 0.f ? 1.f : fminf(1.f, r / qx);
-            acc = tokf[j] >= 0 && tokf[j] < a.V && w.uni[j] < ratio;
-          }
-          kids += __popc(__ballot_sync(0xffffffffu, child));
-          const unsigned int hit = __ballot_sync(0xffffffffu, acc);
-          if (hit) nxt = j0 + __ffs(hit) - 1;
-        }
+      } else {  // draft-q: phase 1 decided every row
+        const int ac = w.acc[cur];
+        nxt = ac >= 0 ? ac : -1;
+        kids = ac == -2;
       }
       if (nxt < 0 || alen >= a.D) break;
       if (lane == 0) {
@@ -284,10 +275,11 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
   if (badp) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
 }
 
-// Draft-q phase 1 of one row with children, by one block (rows too long for
-// one cluster): q's max and sum, then per child in row order the residual
-// (c, F) in force when it is tested (one pass over the row each), then the
-// chunk sums of max(p - c q, 0) for the bonus draw.
+// Draft-q phase 1 of one row, by one block (rows too long for one cluster):
+// q's max and sum, then the children in row order, each tested against the
+// residual in force and, when rejected, one pass over the row for the next
+// (c, F); when every child is rejected, the chunk sums of max(p - c q, 0) for
+// the bonus draw.
 template <int NT>
 __device__ void dq_row_block(const VerifyArgs &a, long long row, int b, int node, const float *zr, float M, float S,
                              WalkSmem &w) {
@@ -295,23 +287,41 @@ __device__ void dq_row_block(const VerifyArgs &a, long long row, int b, int node
   const int i = (int)(row - (long long)b * a.N);
   const long long fo = row - i;
   const int nkid = child_list<NT>(a.flat_parent + fo, a.N, i, w.kid, &w.s_nkid);
-  if (nkid == 0) return;
+  if (nkid == 0) {
+    if (t == 0) a.dq[8 * row + 3] = __int_as_float(-1);  // a leaf
+    return;
+  }
   int bad = 0, flag = 0;
   const float *dr = table_row(a.dlog, a.dstride, a.dmap, a.C, b, node, row, bad);
   const float invT = 1.f / a.T, invS = S > 0.f ? 1.f / S : 0.f;
+  for (int k = t; k < nkid; k += NT) {
+    const long long j = fo + w.kid[k];
+    const int x = a.flat_tok[j];
+    const bool ok = x >= 0 && x < a.V;
+    int f2 = 0;
+    w.zc[k] = (ok && zr) ? sanitize_logit(zr[x], f2) : -INFINITY;
+    w.dc[k] = (ok && dr) ? sanitize_logit(dr[x], f2) : -INFINITY;
+    w.uni[k] = a.uniforms[j];
+    w.tokf[k] = ok;
+    if (!ok) bad = 1;
+  }
   auto yd = [&](int v) -> float { return dr ? __fmul_rn(sanitize_logit(dr[v], flag), invT) : -INFINITY; };
   auto yt = [&](int v) -> float { return zr ? __fmul_rn(sanitize_logit(zr[v], flag), invT) : -INFINITY; };
   float lq = -INFINITY;
   for (int v = t; v < a.V; v += NT) lq = fmaxf(lq, yd(v));
-  const float Mq = block_max<NT>(lq, w.redz);
+  const float Mq = block_max<NT>(lq, w.redz);  // its barriers publish the children's values above
   float ls = 0.f;
   if (Mq > -INFINITY)
     for (int v = t; v < a.V; v += NT) ls += exp_fast(yd(v) - Mq);
   const float Sq = block_sum<NT>(ls, w.redz);
   const float invSq = Sq > 0.f ? 1.f / Sq : 0.f;
   float c = 0.f, F = 1.f;
+  int acc = -2;
   for (int k = 0; k < nkid; ++k) {
-    if (t == 0) { a.dq[8 * (fo + w.kid[k]) + 4] = c; a.dq[8 * (fo + w.kid[k]) + 5] = F; }
+    if (dq_accept(w.zc[k], w.dc[k], w.tokf[k] != 0, w.uni[k], invT, M, invS, Mq, invSq, c, F)) {
+      acc = w.kid[k];
+      break;
+    }
     const float c1 = c + F;
     float loc = 0.f;
     for (int v = t; v < a.V; v += NT) loc += dq_excess(dq_weight(yt(v), M, invS), dq_weight(yd(v), Mq, invSq), c1);
@@ -322,17 +332,19 @@ __device__ void dq_row_block(const VerifyArgs &a, long long row, int b, int node
     a.dq[8 * row] = Mq;
     a.dq[8 * row + 1] = Sq;
     a.dq[8 * row + 2] = c;
-    a.dq[8 * row + 3] = F;
+    a.dq[8 * row + 3] = __int_as_float(acc);
   }
-  float *cst = a.part + row * a.nchunk * 2;
-  for (int ch = 0; ch < a.nchunk; ++ch) {
-    float loc = 0.f;
-    for (int e = t; e < kVChunk; e += NT) {
-      const int v = ch * kVChunk + e;
-      if (v < a.V) loc += dq_excess(dq_weight(yt(v), M, invS), dq_weight(yd(v), Mq, invSq), c);
+  if (acc < 0) {
+    float *cst = a.part + row * a.nchunk * 2;
+    for (int ch = 0; ch < a.nchunk; ++ch) {
+      float loc = 0.f;
+      for (int e = t; e < kVChunk; e += NT) {
+        const int v = ch * kVChunk + e;
+        if (v < a.V) loc += dq_excess(dq_weight(yt(v), M, invS), dq_weight(yd(v), Mq, invSq), c);
+      }
+      const float sum = block_sum<NT>(loc, w.redz);
+      if (t == 0) { cst[2 * ch] = M; cst[2 * ch + 1] = sum; }
     }
-    const float sum = block_sum<NT>(loc, w.redz);
-    if (t == 0) { cst[2 * ch] = M; cst[2 * ch + 1] = sum; }
   }
   if (flag) flag_status(a.dev_status, ET_DEV_NONFINITE);
   if (bad && t == 0) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
@@ -369,13 +381,11 @@ __global__ void __launch_bounds__(kVThreads) k_verify(VerifyArgs a) {
     for (int j = 0; j < 4; ++j)
       if (e0 + j < a.V) v[4 * u + j] = sanitize_logit(v[4 * u + j], flag);
   }
-  if (a.mode != ET_ACCEPT_GREEDY) {  // children's logits at this row, from the block holding their token
+  if (a.mode == ET_ACCEPT_STOCH_POINT) {  // children's logits at this row, from the block holding their token
     const int i = row - b * a.N;
     const long long fo = (long long)row - i;
     const int nkid = child_list<kVThreads>(a.flat_parent + fo, a.N, i, w.kid, &w.s_nkid);
-    const float *drow = (a.mode == ET_ACCEPT_STOCH_DRAFTQ && nkid > 0)
-                            ? table_row(a.dlog, a.dstride, a.dmap, a.C, b, node, row, bad) : nullptr;
-    if (nkid > 0) store_child_logits(a, fo, w.kid, nkid, zrow, drow, c0, c0 + kVChunk, c == 0);
+    if (a.mode == ET_ACCEPT_STOCH_POINT && nkid > 0) store_child_logits(a, fo, w.kid, nkid, zrow, c0, c0 + kVChunk, c == 0);
   }
   float *prt = a.part + ((long long)row * a.nchunk + c) * 2;
   if (a.mode == ET_ACCEPT_GREEDY) {
@@ -499,10 +509,23 @@ __global__ void __launch_bounds__(kVClThreads) k_verify_cl(VerifyArgs a) {
   int nkid = 0;
   if (!greedy)  // the children of this row (every block of the cluster finds the same)
     nkid = child_list<kVClThreads>(a.flat_parent + fo, a.N, i, w.kid, &w.s_nkid);
-  const float *drow = (kDraftQ && nkid > 0) ? table_row(a.dlog, a.dstride, a.dmap, a.C, b, node, row, bad) : nullptr;
-  if (nkid > 0) store_child_logits(a, fo, w.kid, nkid, zrow, drow, base, base + kVClSpan, q == 0);
+  if (!kDraftQ && nkid > 0) store_child_logits(a, fo, w.kid, nkid, zrow, base, base + kVClSpan, q == 0);
   if (kDraftQ && nkid > 0) {
     const float invT = 1.f / a.T;
+    const float *drow = table_row(a.dlog, a.dstride, a.dmap, a.C, b, node, row, bad);
+    // every block loads each child's token logits and uniform: the tests below
+    // are evaluated alike in all blocks of the cluster
+    for (int k = t; k < nkid; k += kVClThreads) {
+      const long long j = fo + w.kid[k];
+      const int x = a.flat_tok[j];
+      const bool ok = x >= 0 && x < a.V;
+      int f2 = 0;
+      w.zc[k] = (ok && zrow) ? sanitize_logit(__ldg(zrow + x), f2) : -INFINITY;
+      w.dc[k] = (ok && drow) ? sanitize_logit(__ldg(drow + x), f2) : -INFINITY;
+      w.uni[k] = a.uniforms[j];
+      w.tokf[k] = ok;
+      if (!ok && q == 0) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
+    }
     float d[4 * kVClVec];
     cl_load_span(drow, base, a.vec4d, a.V, d, flag);
     float lm = -INFINITY, lq = -INFINITY;
@@ -555,10 +578,11 @@ __global__ void __launch_bounds__(kVClThreads) k_verify_cl(VerifyArgs a) {
       d[e] = dq_weight(d[e], Mq, invSq);  // q
     }
     float c = 0.f, F = 1.f;  // the residual in force: max(p - c q, 0) / F
-    for (int k = 0; k < nkid; ++k) {  // each child in row order: one rejection more
-      if (q == 0 && t == 0) {
-        a.dq[8 * (fo + w.kid[k]) + 4] = c;
-        a.dq[8 * (fo + w.kid[k]) + 5] = F;
+    int acc = -2;
+    for (int k = 0; k < nkid; ++k) {  // each child in row order; a rejection moves the residual on
+      if (dq_accept(w.zc[k], w.dc[k], w.tokf[k] != 0, w.uni[k], invT, M, invS, Mq, invSq, c, F)) {
+        acc = w.kid[k];
+        break;
       }
       const float c1 = c + F;
       float loc = 0.f;
@@ -581,28 +605,33 @@ __global__ void __launch_bounds__(kVClThreads) k_verify_cl(VerifyArgs a) {
       a.dq[8 * (long long)row] = Mq;
       a.dq[8 * (long long)row + 1] = Sq;
       a.dq[8 * (long long)row + 2] = c;
-      a.dq[8 * (long long)row + 3] = F;
+      a.dq[8 * (long long)row + 3] = __int_as_float(acc);
     }
-    float loc = 0.f;
+    if (acc >= 0) {  // a child is accepted: the walk never draws a bonus token here
+      if (q != 0) return;
+    } else {  // every child rejected: the chunk sums of max(p - c q, 0) for the bonus draw
+      float loc = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4 * kVClVec; ++e) loc += dq_excess(v[e], d[e], c);
-    loc = warp_sum(loc);
-    if (lane == 0) wsum[warp] = loc;
-    __syncthreads();
-    if (t == 0) {  // this chunk's sum of max(p - c q, 0), to the leader
-      float bs = 0.f;
+      for (int e = 0; e < 4 * kVClVec; ++e) loc += dq_excess(v[e], d[e], c);
+      loc = warp_sum(loc);
+      if (lane == 0) wsum[warp] = loc;
+      __syncthreads();
+      if (t == 0) {  // this chunk's sum of max(p - c q, 0), to the leader
+        float bs = 0.f;
 #pragma unroll
-      for (int x = 0; x < NW; ++x) bs += wsum[x];
-      cl_st_f32x2(cl_map(&gms[q], 0), M, bs);
-    }
-    cl_arrive();
-    if (q != 0) return;
-    cl_wait();
-    if (t == 0) {  // chunk weight = sum * exp(M - M): the plain sums
-      float *cst = a.part + (long long)row * a.nchunk * 2;
-      for (int x = 0; x < R; ++x) { cst[2 * x] = gms[x].x; cst[2 * x + 1] = gms[x].y; }
+        for (int x = 0; x < NW; ++x) bs += wsum[x];
+        cl_st_f32x2(cl_map(&gms[q], 0), M, bs);
+      }
+      cl_arrive();
+      if (q != 0) return;
+      cl_wait();
+      if (t == 0) {  // chunk weight = sum * exp(M - M): the plain sums
+        float *cst = a.part + (long long)row * a.nchunk * 2;
+        for (int x = 0; x < R; ++x) { cst[2 * x] = gms[x].x; cst[2 * x + 1] = gms[x].y; }
+      }
     }
   } else {
+    if (kDraftQ && q == 0 && t == 0) a.dq[8 * (long long)row + 3] = __int_as_float(-1);  // a leaf
     if (greedy) {  // (z desc, id asc) as one ascending key: the warp's best is its minimum
       unsigned long long best = ~0ull;
 #pragma unroll

@@ -508,6 +508,57 @@ def test_stoch_draftq_iid_children_lossless():
     assert _chi2_ok(first, p)
 
 
+def test_draftq_residual_closed_form():
+    """The acceptance kernel evaluates the draft-q residual as max(p - c q, 0) / F
+    with (c, F) = (0, 1), then c <- c + F and F <- sum max(p - c q, 0) per
+    rejection (kept when that sum is 0); the rule iterates r <- norm(max(r - q, 0)).
+    The two agree elementwise, and the oracle's bonus token after every child
+    is rejected is the closed form's inverse CDF."""
+    rng = np.random.default_rng(17)
+    for trial in range(20):
+        V = int(rng.integers(2, 40))
+        p = scipy.special.softmax(rng.standard_normal(V) * rng.uniform(0.3, 3.0))
+        q = scipy.special.softmax(rng.standard_normal(V) * rng.uniform(0.3, 3.0))
+        if trial == 0:
+            q = p.copy()  # every excess is 0: r stays p
+        r, c, F = p.copy(), 0.0, 1.0
+        for _ in range(12):
+            d = np.maximum(r - q, 0.0)
+            if d.sum() > 0.0:
+                r = d / d.sum()
+            c1 = c + F
+            F1 = np.maximum(p - c1 * q, 0.0).sum()
+            if F1 > 0.0:
+                c, F = c1, F1
+            assert np.abs(np.maximum(p - c * q, 0.0) / F - r).max() <= 1e-12
+    V, k = 12, 5
+    pz = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    qz = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    p = O.softmax_t(pz, 1.0)
+    q = O.softmax_t(qz, 1.0)
+    c, F = 0.0, 1.0
+    for _ in range(k):
+        F1 = np.maximum(p - (c + F) * q, 0.0).sum()
+        if F1 > 0.0:
+            c, F = c + F, F1
+    w = np.maximum(p - c * q, 0.0)
+    cfg = O.TreeCfg(B=1, V=V, depth=1, topk=k, m=1, n=k)
+    par = np.array([[-1] + [0] * k], np.int32)
+    node = np.arange(-1, k, dtype=np.int32)[None]
+    tok = np.array([[0] + list(rng.choice(V, k, p=q))], np.int32)
+    seen = 0
+    for u0 in np.linspace(0.01, 0.99, 25):
+        us = np.array([[u0] + [1.0] * k], np.float32)  # u = 1 rejects every child
+        res = O.verify_accept(cfg, O.STOCH_DRAFTQ, tok, par, node, np.stack([pz] * (k + 1)), None, uniforms=us,
+                              draft_table=np.stack([qz] * (k + 1)))
+        if res.near_ties:
+            continue
+        want = int(np.nonzero(np.cumsum(w) > float(us[0, 0]) * w.sum())[0][0])
+        assert res.accept_len[0] == 0 and res.tokens[0, 0] == want
+        seen += 1
+    assert seen >= 20
+
+
 def test_stoch_special_cases():
     tok, par, node = _hand_tree()
     cfg = O.TreeCfg(B=1, V=10, depth=3, topk=3, m=3, n=7)
