@@ -369,6 +369,14 @@ def _inverse_cdf(weights: np.ndarray, u: float, total: float) -> Tuple[int, floa
     return t, gap
 
 
+def draftq_residual(r: np.ndarray, q: np.ndarray) -> np.ndarray:
+    """One rejection under the draft-q rule: norm(max(r - q, 0)); when that
+    excess has no mass, r is kept."""
+    res = np.maximum(r - q, 0.0)
+    s = res.sum()
+    return res / s if s > 0.0 else r
+
+
 @dataclasses.dataclass
 class AcceptResult:
     accept_len: np.ndarray   # int32 [B]
@@ -455,10 +463,7 @@ def verify_accept(cfg: TreeCfg, mode: int, flat_tok: np.ndarray, flat_parent: np
                     if u < ratio:
                         nxt = c
                         break
-                    res = np.maximum(r - qd, 0.0)
-                    s = res.sum()
-                    if s > 0.0:
-                        r = res / s
+                    r = draftq_residual(r, qd)
                 if nxt < 0:
                     bonus, gap = _inverse_cdf(r, float(uniforms[b, 0]), float(r.sum()))
                     if gap < TIE_REL_CDF:

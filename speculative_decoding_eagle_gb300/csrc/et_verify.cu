@@ -4,7 +4,9 @@
 //
 // Phase 1 (all blocks): every flat row's target logits are streamed once with
 // 128-bit loads, split over blocks; each block reduces its slice (argmax, or
-// max and sum of exp at temperature T); the last block of a row merges them.
+// max and sum of exp at temperature T) and the row's blocks merge them.  In
+// the draft-q mode a row with children also decides its own acceptance there
+// (p and q of the row, one cluster reduction per rejected child).
 // Phase 2 (the last row-block of a sequence): walk the tree from the root,
 // then draw the bonus token by an inverse CDF over the stopping row.
 #include "et_common.cuh"

@@ -99,6 +99,23 @@ def _static_rank_off_by_one():
     _set(ST, "static_tree", static_tree)
 
 
+def _residual_without_clamp():
+    def draftq_residual(r, q):
+        res = r - q
+        s = np.abs(res).sum()
+        return res / s if s > 0.0 else r
+    _set(T, "draftq_residual", draftq_residual)
+
+
+def _residual_not_renormalised():
+    _set(T, "draftq_residual", lambda r, q: np.maximum(r - q, 0.0))
+
+
+def _inverse_cdf_ignores_mass():
+    orig = T._inverse_cdf
+    _set(T, "_inverse_cdf", lambda weights, u, total: orig(weights, u, 1.0))  # threshold u, not u * mass
+
+
 MUTATIONS = {
     "log_softmax drops the log-sum-exp": _lsm_no_normaliser,
     "top-k ties go to the higher id": _topk_ties_high_id,
@@ -111,6 +128,9 @@ MUTATIONS = {
     "temperature ignored": _softmax_ignores_temperature,
     "KV commit skips the root row": _commit_skips_root,
     "static tree ranks off by one": _static_rank_off_by_one,
+    "draft-q residual drops the clamp": _residual_without_clamp,
+    "draft-q residual not renormalised": _residual_not_renormalised,
+    "inverse CDF ignores the remaining mass": _inverse_cdf_ignores_mass,
 }
 
 
