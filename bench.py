@@ -645,6 +645,56 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_split_sweep(args):
+    """Attention alone at each KV split count: one JSON line per count (a
+    tuning aid; the step's own plan picks the count by default).  Timing as in
+    the step bench: CUDA events around a graph of K launches over input sets
+    that together exceed L2."""
+    import numpy as np
+    import torch
+    from speculative_decoding_eagle_gb300 import binding as E, build_lib, step as S
+    from speculative_decoding_eagle_gb300 import workloads as W
+    build_lib.build()
+    E.load()
+    wl = W.WORKLOADS[args.workload]
+    if args.batch:
+        wl = wl.with_(B=args.batch)
+    if args.prefix:
+        wl = wl.with_(prefix=args.prefix, ragged=False)
+    st0 = S.VerifyStep(wl)
+    cfg = st0.cfg
+    prefix = W.prefix_lengths(wl, cfg.B)
+    abytes = attention_bytes(wl, prefix)
+    R = args.sets or max(2, int(np.ceil(2 * L2_BYTES / abytes)) + 1)
+    sets = [S.to_device(wl, S.host_inputs(wl, st0.C, cfg.B, b0=r * cfg.B)) for r in range(R)]
+    K = max(8, min(200, args.steps))
+    stream = torch.cuda.Stream()
+    for splits in [int(x) for x in args.splits_sweep.split(",")]:
+        st = S.VerifyStep(wl, num_splits=splits, attn_impl=E.ATTN_TCGEN05)
+        st.prepare(sets[0])
+        with torch.cuda.stream(stream):
+            for r in range(R):
+                st.run(sets[r], stream=stream)  # trees and masks of every set
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(K):
+                st.attention(sets[i % R], stream=stream)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        cur = torch.cuda.current_stream()  # a graph replays on the current stream
+        e0.record(cur)
+        g.replay()
+        e1.record(cur)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1000.0 / K
+        print(json.dumps({"workload": wl.name, "batch": cfg.B, "prefix": int(max(prefix)), "splits": splits,
+                          "splits_used": E.et_tree_attention_splits(st.shape), "us_per_launch": round(us, 2),
+                          "GBps": round(abytes / us / 1e3, 1), "launches": K, "input_sets": R}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -660,6 +710,7 @@ def main():
     ap.add_argument("--sets", type=int, default=0)
     ap.add_argument("--eager", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--splits-sweep", default="", help="comma-separated KV split counts: time attention alone at each")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per attention launch from an ncu capture of the same kernel")
     args = ap.parse_args()
@@ -667,6 +718,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.splits_sweep:
+        run_split_sweep(args)
     else:
         run_gpu(args)
 
