@@ -75,15 +75,19 @@ class Clocks:
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, csv_path=""):
         self.proc = None
         self.gpu = gpu_index
+        self.csv_path = csv_path  # where to keep the raw samples ("" = nowhere)
         self.out = None
 
     def __enter__(self):
+        if self.csv_path:
+            try:
+                self.out = open(self.csv_path, "w")
+            except OSError:
+                self.out = None
         try:
-            self.out = open(os.devnull if not os.path.isdir(os.path.join(ROOT, "gpurun_out")) else
-                            os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv"), "w+")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
@@ -321,7 +325,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     cur = torch.cuda.current_stream()
-    with Clocks(local) as clk:
+    with Clocks(local, args.clocks_csv) as clk:
         t_wall = time.perf_counter()
         ev0.record(cur)
         for i in range(args.steps):
@@ -710,6 +714,7 @@ def main():
     ap.add_argument("--sets", type=int, default=0)
     ap.add_argument("--eager", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-csv", default="", help="also write the raw nvidia-smi samples of the timed region here")
     ap.add_argument("--splits-sweep", default="", help="comma-separated KV split counts: time attention alone at each")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per attention launch from an ncu capture of the same kernel")
