@@ -1,0 +1,50 @@
+"""Host-side pieces of bench.py (no GPU): the clocks summary that vets a
+timed run, and the algorithmic byte counts the roofline divides by."""
+import os
+import sys
+
+import pytest
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import bench  # noqa: E402
+from speculative_decoding_eagle_gb300 import workloads as W  # noqa: E402
+
+
+def _clocks(lines):
+    c = bench.Clocks(0)
+    c.lines = lines
+    return c.summary()
+
+
+def test_clocks_summary_median_and_reasons():
+    s = _clocks(["0, 2070, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+                 "0, 1980, 2070, 1100.0, 0x4, Not Active, Not Active, Not Active, Active",
+                 "0, 2070, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active"])
+    assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0 and s["samples"] == 3
+    assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_clocks_summary_flags_thermal_and_skips_garbage():
+    s = _clocks(["garbage", "0, [N/A], 2070, 0, 0x0, Not Active, Not Active, Not Active, Not Active",
+                 "0, 1500, 2070, 1300.0, 0x40, Active, Active, Not Active, Not Active"])
+    assert s["samples"] == 1 and s["sm_mhz"] == 1500.0
+    assert s["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
+
+
+def test_clocks_summary_without_samples():
+    assert _clocks([])["reasons"] == ["unavailable"]
+
+
+def test_clocks_without_nvidia_smi_or_csv(tmp_path):
+    path = tmp_path / "clk.csv"
+    with bench.Clocks(0, str(path)) as c:
+        pass
+    assert "reasons" in c.summary() and path.exists()
+
+
+@pytest.mark.parametrize("name,prefix,want", [("llama2-7b", 1024, 18_776_064), ("llama2-13b", 4096, 86_384_640),
+                                              ("llama2-70b", 8192, 36_540_416)])
+def test_attention_bytes(name, prefix, want):
+    """K/V prefix + tree K/V + Q + O per launch at batch 1."""
+    wl = W.WORKLOADS[name]
+    assert bench.attention_bytes(wl, [prefix]) == want
