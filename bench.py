@@ -233,6 +233,20 @@ def recorded_attention_traffic(workload: str, batch: int, prefix: int):
 # replicas: each rank runs whole steps on its own sequences (no data-path
 # collective); only the timing is reduced, as the maximum over ranks
 # ---------------------------------------------------------------------------
+def step_spread(step_ms):
+    """Median, 10th and 90th percentiles (linear interpolation) of per-step times in ms."""
+    xs = sorted(float(x) for x in step_ms)
+    if not xs:
+        return {"median_ms": None, "p10_ms": None, "p90_ms": None}
+
+    def pct(p):
+        k = (len(xs) - 1) * p / 100.0
+        lo = int(k)
+        hi = min(lo + 1, len(xs) - 1)
+        return xs[lo] + (xs[hi] - xs[lo]) * (k - lo)
+    return {"median_ms": round(pct(50), 5), "p10_ms": round(pct(10), 5), "p90_ms": round(pct(90), 5)}
+
+
 def shard_offsets(rank: int, n_sets: int, batch: int):
     """First sequence index of each of rank `rank`'s input sets: ranks and
     sets cover disjoint, consecutive blocks of `batch` sequences."""
@@ -324,17 +338,34 @@ def run_gpu(args):
         dist.barrier()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    cur = torch.cuda.current_stream()
+    # graphs replay on the current stream; eager steps run on the side stream
+    cur = torch.cuda.current_stream() if graphs else stream
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]  # the end of each step
     with Clocks(local, args.clocks_csv) as clk:
         t_wall = time.perf_counter()
         ev0.record(cur)
         for i in range(args.steps):
             one_step(i)
+            marks[i].record(cur)
         ev1.record(cur)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
     step_ms = reduce_step_ms(ev0.elapsed_time(ev1) / args.steps, world, device="cuda")
     steps_per_s = whole_job_rate(step_ms, world)
+    spread = step_spread([(ev0 if i == 0 else marks[i - 1]).elapsed_time(marks[i]) for i in range(args.steps)])
+
+    # ---- the same step without graphs (every launch from the host) ----
+    eager_ms = None
+    if graphs:
+        ke = max(3, min(50, args.steps))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(ke):
+                st.run(sets[i % R], stream=stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        eager_ms = round(e0.elapsed_time(e1) / ke, 5)
 
     # ---- attention alone: a graph of K launches over the rotating sets ----
     K = max(8, min(200, args.steps))
@@ -374,7 +405,8 @@ def run_gpu(args):
     out = {
         "metric": "tree-verify steps/s (1 GB300, batch 1) with tree-attention HBM GB/s",
         "value": round(steps_per_s, 2), "unit": "steps/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "step_spread": spread,
+        "eager_ms_per_step": eager_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16 attention (fp32 accumulate), fp32 logits" if wl.dtype == "bf16" else "f32",
         "data": "synthetic (seeded Zipf target logits, noisy draft logits, N(0,1) Q/K/V)",
         "config": {"workload": wl.name, "batch": cfg.B, "V": wl.V, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,

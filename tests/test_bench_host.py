@@ -48,3 +48,10 @@ def test_attention_bytes(name, prefix, want):
     """K/V prefix + tree K/V + Q + O per launch at batch 1."""
     wl = W.WORKLOADS[name]
     assert bench.attention_bytes(wl, [prefix]) == want
+
+
+def test_step_spread_percentiles():
+    s = bench.step_spread([0.5, 0.1, 0.4, 0.2, 0.3])  # order does not matter
+    assert s == {"median_ms": 0.3, "p10_ms": 0.14, "p90_ms": 0.46}
+    assert bench.step_spread([0.089] * 7) == {"median_ms": 0.089, "p10_ms": 0.089, "p90_ms": 0.089}
+    assert bench.step_spread([])["median_ms"] is None
