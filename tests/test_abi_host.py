@@ -127,13 +127,23 @@ def test_verify_argument_checks(lib):
     need = E.et_tree_workspace_size(cfg)
     tree = E.TreeC(*([FAKE] * 10))
 
-    def call(mode=E.ET_ACCEPT_GREEDY, uni=None, draft=None, wsb=need):
-        return lib.et_verify_accept(ctypes.byref(cfg.c()), mode, ctypes.byref(tree), FAKE, 1000, None, draft, 1000,
-                                    None, uni, FAKE, FAKE, FAKE, None, FAKE, wsb, None)
+    def call(mode=E.ET_ACCEPT_GREEDY, uni=None, draft=None, wsb=need, target=FAKE, tstride=1000, dstride=1000,
+             ws=FAKE, alen=FAKE, c=cfg):
+        return lib.et_verify_accept(ctypes.byref(c.c()), mode, ctypes.byref(tree), target, tstride, None, draft,
+                                    dstride, None, uni, alen, FAKE, FAKE, None, ws, wsb, None)
     assert call(mode=7) == E.ET_ERR_INVALID_ARG
     assert call(mode=E.ET_ACCEPT_STOCH_POINT) == E.ET_ERR_INVALID_ARG         # no uniforms
     assert call(mode=E.ET_ACCEPT_STOCH_DRAFTQ, uni=FAKE) == E.ET_ERR_INVALID_ARG  # no draft table
+    assert call(mode=E.ET_ACCEPT_STOCH_DRAFTQ, uni=FAKE, draft=FAKE, dstride=999) == E.ET_ERR_INVALID_ARG
+    assert call(tstride=999) == E.ET_ERR_INVALID_ARG                           # rows shorter than V
+    assert call(target=FAKE + 2) == E.ET_ERR_INVALID_ARG                      # fp32 rows need 4-byte alignment
+    assert call(target=None) == E.ET_ERR_INVALID_ARG
+    assert call(alen=None) == E.ET_ERR_INVALID_ARG
     assert call(wsb=need - 1) == E.ET_ERR_WORKSPACE
+    assert call(ws=FAKE + 128) == E.ET_ERR_WORKSPACE                          # 256-byte aligned workspace
+    assert call(ws=None) == E.ET_ERR_WORKSPACE
+    big = E.TreeCfg(B=600, V=1000, depth=3, topk=8, m=8, n=120)               # 600 x 121 flat rows > 65535
+    assert call(c=big, wsb=E.et_tree_workspace_size(big)) == E.ET_ERR_UNSUPPORTED
 
 
 def test_rerank_mask_argument_checks(lib):
