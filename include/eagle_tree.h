@@ -333,6 +333,14 @@ et_status et_tree_attention(const et_attn_shape *shape,
  * path          int32 [B, D+1]: flat rows of the accepted path, root first, -1 padded.
  * tokens        int32 [B, D+1]: accepted draft tokens then the bonus token, -1 padded.
  * ws            et_tree_workspace_size(cfg) bytes (see conventions).
+ *
+ * Errors: ET_ERR_INVALID_ARG for an unknown mode, a missing tree array,
+ * output, uniform table (stochastic modes) or draft table (DRAFTQ), a stride
+ * below V, or target rows that are not 4-byte aligned (16-byte aligned rows
+ * with a stride that is a multiple of 4 are read with 128-bit loads);
+ * ET_ERR_WORKSPACE as in the conventions; ET_ERR_UNSUPPORTED when B * N
+ * exceeds 65535 (one grid row per flat row).  Token indices outside [0, V)
+ * in the tree set ET_DEV_BAD_INDEX and never accept.
  */
 et_status et_verify_accept(const et_tree_cfg *cfg, et_accept_mode mode, const et_tree *tree,
                            const float *target_logits, int64_t target_stride,
