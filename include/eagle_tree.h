@@ -339,8 +339,8 @@ et_status et_tree_attention(const et_attn_shape *shape,
  * below V, or target rows that are not 4-byte aligned (16-byte aligned rows
  * with a stride that is a multiple of 4 are read with 128-bit loads);
  * ET_ERR_WORKSPACE as in the conventions; ET_ERR_UNSUPPORTED when B * N
- * exceeds 65535 (one grid row per flat row).  Token indices outside [0, V)
- * in the tree set ET_DEV_BAD_INDEX and never accept.
+ * exceeds 65535 (one grid row per flat row).  A child whose token lies
+ * outside [0, V) is never accepted (DRAFTQ also sets ET_DEV_BAD_INDEX).
  */
 et_status et_verify_accept(const et_tree_cfg *cfg, et_accept_mode mode, const et_tree *tree,
                            const float *target_logits, int64_t target_stride,
