@@ -47,9 +47,10 @@ Readings where the pages are silent (each one is listed in the design notes):
 * greedy acceptance: argmax (lowest id on ties), children in ascending flat
   index;
 * stochastic acceptance: point-mass proposals for deterministic top-k
-  children (accept child x with probability p(x)/(1-R), R the mass of the
-  siblings already rejected; the bonus token is drawn from p with the
-  rejected tokens removed), or the draft-q variant (accept with
+  children (accept child x with probability r(x)/sum(r), r = p with the
+  tokens of the siblings already rejected removed, i.e. p(x)/(1-R) for
+  distinct tokens; the bonus token is drawn from that residual), or the
+  draft-q variant (accept with
   min(1, r(x)/q(x)), r <- norm(max(r - q, 0)) after a rejection);
   uniforms: slot c is node c's test, slot 0 the bonus draw.
 """
@@ -358,15 +359,34 @@ def softmax_t(z32: np.ndarray, T: float) -> np.ndarray:
 
 def _inverse_cdf(weights: np.ndarray, u: float, total: float) -> Tuple[int, float]:
     """Smallest t with sum_{v<=t} weights[v] > u * total, and the distance of
-    that threshold to the nearest CDF step (relative to total)."""
+    that threshold to the nearest CDF step (relative to total); -1 when no
+    weight is positive."""
+    pos = np.nonzero(weights > 0)[0]
+    if pos.size == 0:
+        return -1, math.inf  # nothing left to draw from
     cdf = np.cumsum(weights)
     thr = u * total
     idx = np.nonzero(cdf > thr)[0]
-    t = int(idx[0]) if idx.size else int(np.nonzero(weights > 0)[0][-1])
+    t = int(idx[0]) if idx.size else int(pos[-1])
     hi = cdf[t]
     lo = cdf[t] - weights[t]
     gap = min(abs(hi - thr), abs(thr - lo)) / max(total, 1e-300)
     return t, gap
+
+
+def point_mass_ratio(r: np.ndarray, x: int) -> float:
+    """min(1, r(x)/q(x)) for the point-mass proposal q at token x, with r the
+    residual kept unnormalised: r(x) / sum(r).  A token outside the row has
+    no mass."""
+    mass = float(r.sum())
+    return float(r[x]) / mass if (0 <= x < r.size and mass > 0.0) else 0.0
+
+
+def point_mass_reject(r: np.ndarray, x: int) -> None:
+    """A rejection of the point-mass proposal at x: max(r - q, 0) removes
+    x's mass (r(x) <= 1); the renormalisation is left to the next ratio."""
+    if 0 <= x < r.size:
+        r[x] = 0.0
 
 
 def draftq_residual(r: np.ndarray, q: np.ndarray) -> np.ndarray:
@@ -429,24 +449,26 @@ def verify_accept(cfg: TreeCfg, mode: int, flat_tok: np.ndarray, flat_parent: np
                         break
                 bonus = a
             elif mode == STOCH_POINT:
-                p = softmax_t(z, cfg.temperature)
-                R = 0.0
-                rej: List[int] = []
+                # r: the residual, kept unnormalised.  A point-mass proposal
+                # at x gives min(1, r(x)/q(x)) = r(x) / sum(r), and after a
+                # rejection norm(max(r - q, 0)) is r with x zeroed (then
+                # renormalised, which the next division by sum(r) does).
+                # For distinct sibling tokens this is p(x) / (1 - R), R the
+                # mass of the siblings already rejected; a token an earlier
+                # sibling already took has no residual mass left.
+                r = softmax_t(z, cfg.temperature)
                 for c in ch[cur]:
                     x = int(flat_tok[b, c])
-                    ratio = p[x] / (1.0 - R) if R < 1.0 else math.inf
+                    ratio = point_mass_ratio(r, x)
                     u = float(uniforms[b, c])
                     if abs(u - ratio) < TIE_REL_ACCEPT * max(1.0, ratio):
                         ties.append((b, "accept", abs(u - ratio)))
                     if u < ratio:
                         nxt = c
                         break
-                    R += p[x]
-                    rej.append(x)
+                    point_mass_reject(r, x)
                 if nxt < 0:
-                    w = p.copy()
-                    w[rej] = 0.0
-                    bonus, gap = _inverse_cdf(w, float(uniforms[b, 0]), 1.0 - R)
+                    bonus, gap = _inverse_cdf(r, float(uniforms[b, 0]), float(r.sum()))
                     if gap < TIE_REL_CDF:
                         ties.append((b, "cdf", gap))
             elif mode == STOCH_DRAFTQ:

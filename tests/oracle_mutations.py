@@ -116,6 +116,14 @@ def _inverse_cdf_ignores_mass():
     _set(T, "_inverse_cdf", lambda weights, u, total: orig(weights, u, 1.0))  # threshold u, not u * mass
 
 
+def _point_mass_keeps_rejected_mass():
+    _set(T, "point_mass_reject", lambda r, x: None)
+
+
+def _point_mass_not_renormalised():
+    _set(T, "point_mass_ratio", lambda r, x: float(r[x]) if 0 <= x < r.size else 0.0)
+
+
 MUTATIONS = {
     "log_softmax drops the log-sum-exp": _lsm_no_normaliser,
     "top-k ties go to the higher id": _topk_ties_high_id,
@@ -131,6 +139,8 @@ MUTATIONS = {
     "draft-q residual drops the clamp": _residual_without_clamp,
     "draft-q residual not renormalised": _residual_not_renormalised,
     "inverse CDF ignores the remaining mass": _inverse_cdf_ignores_mass,
+    "point-mass rejection keeps the token's mass": _point_mass_keeps_rejected_mass,
+    "point-mass ratio not renormalised": _point_mass_not_renormalised,
 }
 
 

@@ -59,3 +59,127 @@ def test_draftq_fp32_decisions_stay_in_the_tie_band(kmin, kmax, squeezes, cases,
         assert _fp32_decision(pz, qz, toks, us, T) == want
         checked += 1
     assert checked >= int(0.95 * cases)
+
+
+# ---------------------------------------------------------------------------
+# point-mass rule
+# ---------------------------------------------------------------------------
+_NINF = f32(-np.inf)
+
+
+def _merge(m1, s1, m2, s2):
+    """(max, sum of exp(y - max)) of two sets, fp32, as the kernel merges them."""
+    m = max(m1, m2)
+    if m == _NINF:
+        return _NINF, f32(0)
+    a = f32(s1 * np.exp(f32(m1 - m), dtype=f32)) if m1 > _NINF else f32(0)
+    b = f32(s2 * np.exp(f32(m2 - m), dtype=f32)) if m2 > _NINF else f32(0)
+    return m, f32(a + b)
+
+
+def _fp32_point_decision(pz, toks, us, T, span=4096):
+    """The kernel's steps: y = z / T; per chunk of `span` tokens the max and
+    sum of exp(y - max) over the tokens that are not children; chunks merged;
+    then from the last child to the first the merged (max, sum) of the rest and
+    the children at or after k (a child whose token an earlier sibling holds
+    counts as nothing); child k's ratio is exp(y_k - max_k) / sum_k."""
+    invT = f32(1.0) / f32(T)
+    y = (pz.astype(f32) * invT).astype(f32)
+    kid = np.zeros(y.size, bool)
+    kid[list(toks)] = True
+    Mr, Sr = _NINF, f32(0)
+    for c0 in range(0, y.size, span):
+        yc = y[c0:c0 + span][~kid[c0:c0 + span]]
+        if yc.size == 0 or yc.max() == _NINF:
+            continue
+        mc = yc.max()
+        sc = np.exp((yc - mc).astype(f32), dtype=f32).sum(dtype=f32)
+        Mr, Sr = _merge(Mr, Sr, mc, sc)
+    first = [x not in toks[:k] for k, x in enumerate(toks)]
+    m, s = Mr, Sr
+    ratio = [f32(0)] * len(toks)
+    for k in range(len(toks) - 1, -1, -1):
+        if first[k]:
+            m, s = _merge(y[toks[k]], f32(1), m, s)
+            ratio[k] = f32(np.exp(f32(y[toks[k]] - m), dtype=f32) / s)
+    for k, u in enumerate(us):
+        if first[k] and u < ratio[k]:
+            return k
+    return -1
+
+
+def _fp32_point_decision_one_minus_r(pz, toks, us, T):
+    """The form p(x) / (1 - R) with R an fp32 running sum of the rejected
+    siblings' p: 1 - R cancels when they hold nearly all the mass."""
+    invT = f32(1.0) / f32(T)
+    y = (pz.astype(f32) * invT).astype(f32)
+    M = y.max()
+    e = np.exp((y - M).astype(f32), dtype=f32)
+    S = e.sum(dtype=f32)
+    R = f32(0)
+    for k, (x, u) in enumerate(zip(toks, us)):
+        px = f32(e[x] / S)
+        if u < (f32(px / f32(1 - R)) if R < 1 else np.inf):
+            return k
+        R = f32(R + px)
+    return -1
+
+
+def _steep_star(rng, V, k, slope, T, squeeze):
+    pz = np.empty(V, np.float32)
+    pz[rng.permutation(V)] = (-slope * np.log(np.arange(1, V + 1)) + rng.standard_normal(V)).astype(np.float32)
+    dz = pz + 0.5 * rng.standard_normal(V)
+    toks = [int(x) for x in np.argsort(-dz, kind="stable")[:k]]  # the draft's top-k, as the dynamic tree keeps
+    us = (1.0 - (1.0 - rng.random(k)) * squeeze).astype(np.float32)
+    return pz, toks, us
+
+
+def test_point_mass_fp32_decisions_stay_in_the_tie_band():
+    """Steep targets (Zipf slope up to 7), T from 0.5 to 1.5 and uniforms near 1
+    reject long runs of children that hold nearly all the mass.  Every decision
+    the oracle does not flag as a near tie agrees with the kernel's
+    cancellation-free form; the 1 - R form, run on the same trees, does not
+    (which shows the cases reach the regime where it fails)."""
+    rng = np.random.default_rng(8)
+    checked = wrong_one_minus_r = long_chains = 0
+    cases = 1500
+    for _ in range(cases):
+        V = int(rng.choice([50, 500, 5000, 32000]))
+        k = int(rng.integers(2, 16))
+        T = float(rng.choice([0.5, 0.7, 1.0, 1.5]))
+        slope = float(rng.uniform(1.2, 7.0))
+        pz, toks, us = _steep_star(rng, V, k, slope, T, float(rng.choice([0.1, 1e-2, 1e-3, 1e-4])))
+        cfg = O.TreeCfg(B=1, V=V, depth=1, topk=k, m=1, n=k, temperature=T)
+        res = O.verify_accept(cfg, O.STOCH_POINT, np.array([[0] + toks], np.int32),
+                              np.array([[-1] + [0] * k], np.int32), np.arange(-1, k, dtype=np.int32)[None],
+                              np.stack([pz] * (k + 1)), None, uniforms=np.array([[0.5] + list(us)], np.float32))
+        if any(what == "accept" for _, what, _ in res.near_ties):
+            continue
+        want = int(res.path[0, 1]) - 1 if res.accept_len[0] > 0 else -1
+        assert _fp32_point_decision(pz, toks, us, T) == want
+        wrong_one_minus_r += _fp32_point_decision_one_minus_r(pz, toks, us, T) != want
+        long_chains += want < 0 or want >= 3
+        checked += 1
+    assert checked >= int(0.95 * cases)
+    assert wrong_one_minus_r >= 10 and long_chains >= cases // 4
+
+
+def test_point_mass_fp32_repeated_tokens_and_chunks():
+    """Repeated sibling tokens count once, and rows spanning several chunks
+    (the 2048-token chunks of rows past one cluster) give the same decisions."""
+    rng = np.random.default_rng(9)
+    for _ in range(300):
+        V = int(rng.choice([3000, 50000]))
+        k = int(rng.integers(2, 10))
+        T = float(rng.choice([0.5, 1.0]))
+        pz, toks, us = _steep_star(rng, V, k, float(rng.uniform(1.2, 5.0)), T, 1e-2)
+        toks = [toks[int(rng.integers(0, j + 1))] if rng.random() < 0.3 else toks[j] for j in range(k)]
+        cfg = O.TreeCfg(B=1, V=V, depth=1, topk=k, m=1, n=k, temperature=T)
+        res = O.verify_accept(cfg, O.STOCH_POINT, np.array([[0] + toks], np.int32),
+                              np.array([[-1] + [0] * k], np.int32), np.arange(-1, k, dtype=np.int32)[None],
+                              np.stack([pz] * (k + 1)), None, uniforms=np.array([[0.5] + list(us)], np.float32))
+        if res.near_ties:
+            continue
+        want = int(res.path[0, 1]) - 1 if res.accept_len[0] > 0 else -1
+        for span in (2048, 4096):
+            assert _fp32_point_decision(pz, toks, us, T, span) == want

@@ -436,76 +436,49 @@ def _stoch_tree(V, rng):
     return np.array([tok], np.int32), np.array([par], np.int32)
 
 
-def test_stoch_point_is_lossless_chi_square():
-    V, trials = 8, 40000
-    rng = np.random.default_rng(123)
-    tok, par = _stoch_tree(V, rng)
-    N = tok.shape[1]
-    logits = (rng.standard_normal((N, V)) * 1.2).astype(np.float32)
-    P = np.stack([scipy.special.softmax(logits[i].astype(np.float64)) for i in range(N)])
-    cfg = O.TreeCfg(B=1, V=V, depth=2, topk=3, m=3, n=N - 1)
-    node = np.arange(-1, N - 1, dtype=np.int32)[None]
-    first = np.zeros(V)
-    second = {c: np.zeros(V) for c in (1, 2, 3)}
-    u_all = rng.random((trials, N)).astype(np.float32)
-    for t in range(trials):
-        r = O.verify_accept(cfg, O.STOCH_POINT, tok, par, node, logits, None, uniforms=u_all[t][None])
-        first[r.tokens[0, 0]] += 1
-        if r.accept_len[0] >= 1:
-            second[int(r.path[0, 1])][r.tokens[0, 1]] += 1
-    assert _chi2_ok(first, P[0])
-    for c in (1, 2, 3):
-        assert second[c].sum() > 1000
-        assert _chi2_ok(second[c], P[c])
+def _star(toks):
+    k = len(toks)
+    return (np.array([[0] + list(toks)], np.int32), np.array([[-1] + [0] * k], np.int32),
+            np.arange(-1, k, dtype=np.int32)[None])
 
 
-def test_stoch_draftq_single_child_is_speculative_sampling():
-    V, trials = 8, 40000
-    rng = np.random.default_rng(7)
-    pz = (rng.standard_normal(V) * 1.5).astype(np.float32)
-    qz = (rng.standard_normal(V) * 1.5).astype(np.float32)
-    p = scipy.special.softmax(pz.astype(np.float64))
-    q = scipy.special.softmax(qz.astype(np.float64))
-    cfg = O.TreeCfg(B=1, V=V, depth=1, topk=1, m=1, n=1)
-    first = np.zeros(V)
-    accepted = 0
-    par = np.array([[-1, 0]], np.int32)
-    node = np.array([[-1, 0]], np.int32)
-    xs = rng.choice(V, trials, p=q)
-    us = rng.random((trials, 2)).astype(np.float32)
-    for t in range(trials):
-        tok = np.array([[0, xs[t]]], np.int32)
-        r = O.verify_accept(cfg, O.STOCH_DRAFTQ, tok, par, node, np.stack([pz, pz]), None,
-                            uniforms=us[t][None], draft_table=np.stack([qz, qz]))
-        first[r.tokens[0, 0]] += 1
-        accepted += int(r.accept_len[0])
-    assert _chi2_ok(first, p)
-    # acceptance rate of speculative sampling = sum_x min(p(x), q(x))
-    rate = np.minimum(p, q).sum()
-    assert abs(accepted / trials - rate) < 4 * math.sqrt(rate * (1 - rate) / trials)
+def test_stoch_point_hand_example():
+    """p = (0.5, 0.3, 0.2), children tokens 0 then 1.  u = 0.6 rejects token 0
+    (ratio 0.5); token 1 then has ratio 0.3 / (1 - 0.5) = 0.6, so u = 0.55
+    accepts it and u = 0.65 rejects it, after which only token 2 is left for
+    the bonus draw, whatever its uniform."""
+    z = np.log(np.array([5.0, 3.0, 2.0])).astype(np.float32)
+    tok, par, node = _star([0, 1])
+    cfg = O.TreeCfg(B=1, V=3, depth=1, topk=2, m=1, n=2)
+    rows = np.stack([z] * 3)
+    r = O.verify_accept(cfg, O.STOCH_POINT, tok, par, node, rows, None,
+                        uniforms=np.array([[0.3, 0.6, 0.55]], np.float32))
+    assert r.accept_len[0] == 1 and list(r.path[0]) == [0, 2] and r.tokens[0, 0] == 1
+    for u0 in (0.01, 0.5, 0.99):
+        r = O.verify_accept(cfg, O.STOCH_POINT, tok, par, node, rows, None,
+                            uniforms=np.array([[u0, 0.6, 0.65]], np.float32))
+        assert r.accept_len[0] == 0 and list(r.tokens[0]) == [2, -1]
+    # u = 0.45 accepts token 0 at once
+    r = O.verify_accept(cfg, O.STOCH_POINT, tok, par, node, rows, None,
+                        uniforms=np.array([[0.3, 0.45, 0.0]], np.float32))
+    assert list(r.path[0]) == [0, 1] and r.tokens[0, 0] == 0
 
 
-def test_stoch_draftq_iid_children_lossless():
-    V, k, trials = 6, 3, 30000
-    rng = np.random.default_rng(99)
-    pz = (rng.standard_normal(V) * 1.3).astype(np.float32)
-    qz = (rng.standard_normal(V) * 1.3).astype(np.float32)
-    p = scipy.special.softmax(pz.astype(np.float64))
-    q = scipy.special.softmax(qz.astype(np.float64))
-    cfg = O.TreeCfg(B=1, V=V, depth=1, topk=k, m=1, n=k)
-    par = np.array([[-1] + [0] * k], np.int32)
-    node = np.arange(-1, k, dtype=np.int32)[None]
-    rows = np.stack([pz] * (k + 1))
-    drows = np.stack([qz] * (k + 1))
-    first = np.zeros(V)
-    xs = rng.choice(V, (trials, k), p=q)
-    us = rng.random((trials, k + 1)).astype(np.float32)
-    for t in range(trials):
-        tok = np.array([[0] + list(xs[t])], np.int32)
-        r = O.verify_accept(cfg, O.STOCH_DRAFTQ, tok, par, node, rows, None, uniforms=us[t][None],
-                            draft_table=drows)
-        first[r.tokens[0, 0]] += 1
-    assert _chi2_ok(first, p)
+def test_stoch_point_repeated_token_has_no_residual_mass():
+    """Once a sibling with token x is rejected, the residual holds no mass at
+    x, so a later sibling with the same token is rejected even with u = 0, and
+    the rejected mass is counted once: the third child (token 1) has ratio
+    0.3 / 0.5."""
+    z = np.log(np.array([5.0, 3.0, 2.0])).astype(np.float32)
+    tok, par, node = _star([0, 0, 1])
+    cfg = O.TreeCfg(B=1, V=3, depth=1, topk=3, m=1, n=3)
+    rows = np.stack([z] * 4)
+    r = O.verify_accept(cfg, O.STOCH_POINT, tok, par, node, rows, None,
+                        uniforms=np.array([[0.5, 0.6, 0.0, 0.59]], np.float32))
+    assert list(r.path[0]) == [0, 3] and r.tokens[0, 0] == 1
+    r = O.verify_accept(cfg, O.STOCH_POINT, tok, par, node, rows, None,
+                        uniforms=np.array([[0.5, 0.6, 0.0, 0.61]], np.float32))
+    assert r.accept_len[0] == 0 and r.tokens[0, 0] == 2
 
 
 def test_draftq_residual_closed_form():
@@ -557,6 +530,25 @@ def test_draftq_residual_closed_form():
         assert res.accept_len[0] == 0 and res.tokens[0, 0] == want
         seen += 1
     assert seen >= 20
+
+
+def test_stoch_draftq_hand_example():
+    """p = (0.5, 0.3, 0.2), q = (0.7, 0.2, 0.1), children tokens 0 then 1.
+    Token 0 has ratio 0.5 / 0.7, so u = 0.8 rejects it; the residual
+    norm(max(p - q, 0)) is (0, 0.5, 0.5), so token 1 has ratio
+    min(1, 0.5 / 0.2) = 1 and is accepted even with u = 0.95."""
+    z = np.log(np.array([0.5, 0.3, 0.2])).astype(np.float32)
+    zq = np.log(np.array([0.7, 0.2, 0.1])).astype(np.float32)
+    tok = np.array([[0, 0, 1]], np.int32)
+    par = np.array([[-1, 0, 0]], np.int32)
+    node = np.arange(-1, 2, dtype=np.int32)[None]
+    cfg = O.TreeCfg(B=1, V=3, depth=1, topk=2, m=1, n=2)
+    r = O.verify_accept(cfg, O.STOCH_DRAFTQ, tok, par, node, np.stack([z] * 3), None,
+                        uniforms=np.array([[0.5, 0.8, 0.95]], np.float32), draft_table=np.stack([zq] * 3))
+    assert list(r.path[0]) == [0, 2] and r.tokens[0, 0] == 1
+    r = O.verify_accept(cfg, O.STOCH_DRAFTQ, tok, par, node, np.stack([z] * 3), None,
+                        uniforms=np.array([[0.5, 0.7, 0.95]], np.float32), draft_table=np.stack([zq] * 3))
+    assert list(r.path[0]) == [0, 1] and r.tokens[0, 0] == 0
 
 
 def test_stoch_special_cases():
@@ -718,3 +710,99 @@ def test_static_tree_sampled_inverse_cdf_by_hand():
     tok2, *_ = O.static_tree_sampled(parent, table, np.array([[0, 1, 2, 3]], np.int32),
                                      np.array([[0, 0.05, 0.5, 0.95]], np.float32), 0.5, np.array([9], np.int32))
     assert tok2.tolist() == [[9, 0, 1, 2]]
+
+
+# ---------------------------------------------------------------------------
+# losslessness of the stochastic walks (chi-square, 2e5 trials each; last in
+# the file so that a cheaper pin stops a mutated run first)
+# ---------------------------------------------------------------------------
+def test_stoch_point_is_lossless_chi_square():
+    V, trials = 8, 200000
+    rng = np.random.default_rng(123)
+    tok, par = _stoch_tree(V, rng)
+    N = tok.shape[1]
+    logits = (rng.standard_normal((N, V)) * 1.2).astype(np.float32)
+    P = np.stack([scipy.special.softmax(logits[i].astype(np.float64)) for i in range(N)])
+    cfg = O.TreeCfg(B=1, V=V, depth=2, topk=3, m=3, n=N - 1)
+    node = np.arange(-1, N - 1, dtype=np.int32)[None]
+    first = np.zeros(V)
+    second = {c: np.zeros(V) for c in (1, 2, 3)}
+    u_all = rng.random((trials, N)).astype(np.float32)
+    for t in range(trials):
+        r = O.verify_accept(cfg, O.STOCH_POINT, tok, par, node, logits, None, uniforms=u_all[t][None])
+        first[r.tokens[0, 0]] += 1
+        if r.accept_len[0] >= 1:
+            second[int(r.path[0, 1])][r.tokens[0, 1]] += 1
+    assert _chi2_ok(first, P[0])
+    for c in (1, 2, 3):
+        assert second[c].sum() > 1000
+        assert _chi2_ok(second[c], P[c])
+
+
+def test_stoch_point_lossless_with_repeated_tokens_chi_square():
+    """Children with repeated tokens (as i.i.d. draws give) keep the first
+    emitted token distributed as p."""
+    V, trials = 6, 200000
+    rng = np.random.default_rng(31)
+    z = (rng.standard_normal(V) * 1.4).astype(np.float32)
+    p = scipy.special.softmax(z.astype(np.float64))
+    top = int(np.argmax(p))
+    toks = [top, (top + 1) % V, top, (top + 1) % V, top]
+    tok, par, node = _star(toks)
+    cfg = O.TreeCfg(B=1, V=V, depth=1, topk=len(toks), m=1, n=len(toks))
+    rows = np.stack([z] * (len(toks) + 1))
+    first = np.zeros(V)
+    us = rng.random((trials, len(toks) + 1)).astype(np.float32)
+    for t in range(trials):
+        r = O.verify_accept(cfg, O.STOCH_POINT, tok, par, node, rows, None, uniforms=us[t][None])
+        first[r.tokens[0, 0]] += 1
+    assert _chi2_ok(first, p)
+
+
+def test_stoch_draftq_single_child_is_speculative_sampling():
+    V, trials = 8, 200000
+    rng = np.random.default_rng(7)
+    pz = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    qz = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    p = scipy.special.softmax(pz.astype(np.float64))
+    q = scipy.special.softmax(qz.astype(np.float64))
+    cfg = O.TreeCfg(B=1, V=V, depth=1, topk=1, m=1, n=1)
+    first = np.zeros(V)
+    accepted = 0
+    par = np.array([[-1, 0]], np.int32)
+    node = np.array([[-1, 0]], np.int32)
+    xs = rng.choice(V, trials, p=q)
+    us = rng.random((trials, 2)).astype(np.float32)
+    for t in range(trials):
+        tok = np.array([[0, xs[t]]], np.int32)
+        r = O.verify_accept(cfg, O.STOCH_DRAFTQ, tok, par, node, np.stack([pz, pz]), None,
+                            uniforms=us[t][None], draft_table=np.stack([qz, qz]))
+        first[r.tokens[0, 0]] += 1
+        accepted += int(r.accept_len[0])
+    assert _chi2_ok(first, p)
+    # acceptance rate of speculative sampling = sum_x min(p(x), q(x))
+    rate = np.minimum(p, q).sum()
+    assert abs(accepted / trials - rate) < 4 * math.sqrt(rate * (1 - rate) / trials)
+
+
+def test_stoch_draftq_iid_children_lossless():
+    V, k, trials = 6, 3, 200000
+    rng = np.random.default_rng(99)
+    pz = (rng.standard_normal(V) * 1.3).astype(np.float32)
+    qz = (rng.standard_normal(V) * 1.3).astype(np.float32)
+    p = scipy.special.softmax(pz.astype(np.float64))
+    q = scipy.special.softmax(qz.astype(np.float64))
+    cfg = O.TreeCfg(B=1, V=V, depth=1, topk=k, m=1, n=k)
+    par = np.array([[-1] + [0] * k], np.int32)
+    node = np.arange(-1, k, dtype=np.int32)[None]
+    rows = np.stack([pz] * (k + 1))
+    drows = np.stack([qz] * (k + 1))
+    first = np.zeros(V)
+    xs = rng.choice(V, (trials, k), p=q)
+    us = rng.random((trials, k + 1)).astype(np.float32)
+    for t in range(trials):
+        tok = np.array([[0] + list(xs[t])], np.int32)
+        r = O.verify_accept(cfg, O.STOCH_DRAFTQ, tok, par, node, rows, None, uniforms=us[t][None],
+                            draft_table=drows)
+        first[r.tokens[0, 0]] += 1
+    assert _chi2_ok(first, p)
