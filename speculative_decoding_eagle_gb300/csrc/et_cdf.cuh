@@ -13,22 +13,25 @@ namespace {
 struct CdfRow {
   int span, nch, V, vec4;  // chunk tokens, chunks, vocabulary, 16-byte aligned row
   float T;                 // temperature
+  float cscale;            // chunk c weighs Sc * exp((Mc - M) * cscale): 1 when the maxima are of z / T,
+                           // 1 / T when they are of the raw logits z
 };
 
 constexpr int kMaxSpan = 4096;                  // chunk tokens (the clustered phase 1)
 constexpr int kMaxSpanWords = kMaxSpan / 32;
 constexpr int kMaxPer = kMaxSpan / 256;         // tokens per thread in the chunk pass
-// Chunk c holds tokens [c·span, (c+1)·span) with statistics (Mc, Sc): its
-// weight is Sc·exp(Mc − M) minus the weights of the rejected tokens it
-// contains.  The rescan weighs token v as wf(zt, zd), zt and zd its sanitised
-// target and draft logits (zd = −inf without a draft row), rejected tokens 0;
-// wf must give the weights the chunk statistics sum.  Sums are fp32 (the
-// weights themselves are fp32 values with ~1e-7 relative error); the threshold
-// inside the crossing chunk is taken relative to the chunk's start.
+// Chunk c holds tokens [c·span, (c+1)·span) with statistics (Mc, Sc) that
+// already leave out the rejected tokens: its weight is Sc·exp((Mc − M)·cscale),
+// a sum of positive terms (nothing is subtracted).  The rescan weighs token v
+// as wf(zt, zd), zt and zd its sanitised target and draft logits (zd = −inf
+// without a draft row), and each of the nrej rejected tokens rej[] as 0; wf
+// must give the weights the chunk statistics sum.  Sums are fp32 (the weights
+// themselves are fp32 values with ~1e-7 relative error); the threshold inside
+// the crossing chunk is taken relative to the chunk's start.
 template <int NT, bool kDraft, typename WF>
 __device__ int chunk_inverse_cdf(const CdfRow &a, const float *zr, const float *dr, int vec4d, const float *cstat,
-                                 float M, float uni, const int *rej, const float *rejw, int nrej, float *redf,
-                                 int *redi, float *tsum, unsigned int *rejbits, WF wf) {
+                                 float M, float uni, const int *rej, int nrej, float *redf, int *redi, float *tsum,
+                                 unsigned int *rejbits, WF wf) {
   const int t = threadIdx.x, lane = t & 31, wp = t >> 5;
   const int span = a.span, nch = a.nch;
   if (t == 0) { redi[0] = 0x7fffffff; redi[1] = -1; }
@@ -39,11 +42,7 @@ __device__ int chunk_inverse_cdf(const CdfRow &a, const float *zr, const float *
       float wc = 0.f;
       if (c < nch) {
         const float mc = ld_cg(cstat + 2 * c), sc = ld_cg(cstat + 2 * c + 1);
-        wc = mc > -INFINITY ? sc * expf(mc - M) : 0.f;
-        const int lo = c * span, hi = lo + span;
-        for (int q = 0; q < nrej; ++q)
-          if (rej[q] >= lo && rej[q] < hi) wc -= rejw[q];
-        wc = fmaxf(wc, 0.f);
+        wc = mc > -INFINITY ? sc * expf((mc - M) * a.cscale) : 0.f;
         tsum[c] = wc;
       }
       total += warp_sum(wc);
@@ -163,17 +162,19 @@ __device__ int chunk_inverse_cdf(const CdfRow &a, const float *zr, const float *
   return r;
 }
 
-// The inverse CDF of the softmax row p at temperature T (rejected children
-// removed) from its chunk statistics (max, sum of exp(z/T − max)).
-template <int NT>
+// The inverse CDF of the softmax row p at temperature T (rejected tokens
+// removed) from its chunk statistics.  kRaw: the statistics are (max of z,
+// sum of exp((z − max)/T)) and M is a raw logit (a.cscale = 1/T); otherwise
+// (max of z/T, sum of exp(z/T − max)) and M is a scaled logit (a.cscale = 1).
+template <int NT, bool kRaw>
 __device__ int bonus_from_chunks(const CdfRow &a, const float *zr, const float *cstat, float M, float uni,
-                                 const int *rej, const float *rejw, int nrej, float *redf, int *redi,
-                                 float *tsum, unsigned int *rejbits) {
+                                 const int *rej, int nrej, float *redf, int *redi, float *tsum,
+                                 unsigned int *rejbits) {
   const float invT = 1.f / a.T;
-  return chunk_inverse_cdf<NT, false>(a, zr, nullptr, 0, cstat, M, uni, rej, rejw, nrej, redf, redi, tsum, rejbits,
-                                      [&](float zt, float) -> float {
-                                        const float y = zt * invT;
-                                        return y > -INFINITY ? exp_fast(y - M) : 0.f;  // as the chunk sums
+  return chunk_inverse_cdf<NT, false>(a, zr, nullptr, 0, cstat, M, uni, rej, nrej, redf, redi, tsum, rejbits,
+                                      [&](float zt, float) -> float {  // as the chunk sums weigh it
+                                        if (!(zt > -INFINITY)) return 0.f;
+                                        return kRaw ? exp_fast((zt - M) * invT) : exp_fast(zt * invT - M);
                                       });
 }
 

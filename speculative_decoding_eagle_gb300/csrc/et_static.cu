@@ -246,9 +246,9 @@ __global__ void __launch_bounds__(kStThreads) k_static_draw(SampledArgs a) {
   const float *cst = a.cst + (fo + p) * a.R * 2;
   float M = -INFINITY;
   for (int x = 0; x < a.R; ++x) M = fmaxf(M, ld_cg(cst + 2 * x));
-  const CdfRow cdf{kStSpan, a.R, a.V, a.vec4, a.T};
-  const int tok = bonus_from_chunks<kStThreads>(cdf, zr, cst, M, a.uniforms[fo + i], nullptr, nullptr, 0, redf, redi,
-                                                tsum, rejbits);
+  const CdfRow cdf{kStSpan, a.R, a.V, a.vec4, a.T, 1.f};  // statistics of z / T
+  const int tok = bonus_from_chunks<kStThreads, false>(cdf, zr, cst, M, a.uniforms[fo + i], nullptr, 0, redf, redi,
+                                                       tsum, rejbits);
   if (threadIdx.x == 0) a.flat_tok[fo + i] = tok;
 }
 

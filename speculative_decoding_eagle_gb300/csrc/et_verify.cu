@@ -36,9 +36,9 @@ struct VerifyArgs {
   int32_t *accept_len, *path, *tokens, *dev_status;
   float *part;        // [B*N][nchunk][2]
   float *rowstat;     // [B*N][2]
-  float *dq;          // [B*N][8] per flat row: draft-q q's max and sum, the residual's c once every child is
-                      // rejected, the accepted child (int bits: row, -1 leaf, -2 all rejected); [6] point-mass:
-                      // the target logit of the row's token in its parent's row
+  float *dq;          // [B*N][8] per flat row: [3] the accepted child (int bits: row, -1 leaf, -2 all
+                      // rejected), both stochastic modes; draft-q also [0..2]: q's max and sum, the residual's
+                      // c once every child is rejected
   unsigned int *row_cnt, *seq_cnt;
   int vec4t, vec4d;       // 16-byte aligned target / draft rows
   int cdf_span, cdf_nch;  // chunk statistics of each row in part: span tokens each, nch chunks
@@ -72,22 +72,79 @@ __device__ __forceinline__ float dq_weight(float y, float M, float inv_sum) {
 }
 __device__ __forceinline__ float dq_excess(float p, float q, float c) { return fmaxf(fmaf(-c, q, p), 0.f); }
 
-// Phase 1 of a row with children (point-mass): the block holding token x_j
-// of each child j in [lo, hi) stores the target logit of x_j at this row into
-// j's record, so the walk reads one value per child; block 0 covers tokens
-// outside [0, V).
-__device__ __forceinline__ void store_child_logits(const VerifyArgs &a, long long fo, const int *kid, int nkid,
-                                                   const float *zrow, int lo, int hi, bool first) {
-  for (int k = threadIdx.x; k < nkid; k += blockDim.x) {
-    const long long j = fo + kid[k];
-    const int x = a.flat_tok[j];
-    const bool ok = x >= 0 && x < a.V;
-    if (ok ? (x >= lo && x < hi) : first) {
-      int f2 = 0;
-      a.dq[8 * j + 6] = (zrow && ok) ? sanitize_logit(__ldg(zrow + x), f2) : -INFINITY;
-      __threadfence();  // device-wide before this block's next barrier (the walk may run in another cluster)
+// ---- point-mass acceptance: every row decided in phase 1 ----
+// A deterministic child x is a point-mass proposal, so its test is
+// u < r(x) / sum(r) with r = p minus the tokens of the siblings rejected
+// before it.  With e_i = exp(z(x_i) / T) (up to a common factor) for each
+// distinct child token and S_rest the row's weight outside every child
+// token, child k's ratio is e_k / (S_rest + sum_{i>=k} e_i): sums of positive
+// terms only, so nothing cancels when the rejected siblings hold almost all
+// of the mass.  The suffix sums run from the last child to the first as
+// (max raw logit, sum of exp((z - max) / T)) pairs merged like a log-sum-exp,
+// so each ratio is formed relative to its own largest term.
+__device__ __forceinline__ void lse_merge(float &m, float &s, float m2, float s2, float invT) {
+  const float M = fmaxf(m, m2);
+  if (M == -INFINITY) { m = M; s = 0.f; return; }
+  s = (m > -INFINITY ? s * expf((m - M) * invT) : 0.f) + (m2 > -INFINITY ? s2 * expf((m2 - M) * invT) : 0.f);
+  m = M;
+}
+
+// One warp decides a row with nkid > 0 children: kid[k] their flat rows in
+// ascending order, zk[k] the raw target logit of each child's token at this
+// row (-inf when the token is outside [0, V) or an earlier sibling holds it:
+// no residual mass), uk[k] their uniforms, (Mr, Sr) the row's tokens outside
+// the children.  Returns the first accepted child's flat row, or -2.
+__device__ int pm_decide(int nkid, const int *kid, const float *zk, const float *uk, float Mr, float Sr, float invT) {
+  const int lane = threadIdx.x & 31;
+  float cm = Mr, cs = Sr;  // the rest plus every child after the current group
+  int acc = -2;
+  for (int g0 = ((nkid - 1) >> 5) << 5; g0 >= 0; g0 -= 32) {
+    const int k = g0 + lane;
+    const float z = k < nkid ? zk[k] : -INFINITY;
+    float m = z, sm = z > -INFINITY ? 1.f : 0.f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {  // suffix merge inside the group: lane gets children k .. g0 + 31
+      const float m2 = __shfl_down_sync(0xffffffffu, m, o), s2 = __shfl_down_sync(0xffffffffu, sm, o);
+      if (lane + o < 32) lse_merge(m, sm, m2, s2, invT);
     }
+    lse_merge(m, sm, cm, cs, invT);
+    const float ratio = (z > -INFINITY && sm > 0.f) ? expf((z - m) * invT) / sm : 0.f;
+    const unsigned int hit = __ballot_sync(0xffffffffu, k < nkid && uk[k] < ratio);
+    if (hit) acc = kid[g0 + __ffs(hit) - 1];  // groups run last to first: the earliest hit wins
+    cm = __shfl_sync(0xffffffffu, m, 0);
+    cs = __shfl_sync(0xffffffffu, sm, 0);
   }
+  return acc;
+}
+
+// The tokens, raw target logits and uniforms of a row's children (by child
+// rank) into shared memory, by the block's threads; a token already held by
+// an earlier sibling, or outside [0, V), gets logit -inf.  The caller
+// synchronises before reading them.
+__device__ void pm_child_inputs(const VerifyArgs &a, long long fo, const int *kid, int nkid, const float *zrow,
+                                int *ktok, float *zk, float *uk) {
+  for (int k = threadIdx.x; k < nkid; k += blockDim.x) ktok[k] = a.flat_tok[fo + kid[k]];
+  __syncthreads();
+  for (int k = threadIdx.x; k < nkid; k += blockDim.x) {
+    const int x = ktok[k];
+    bool ok = zrow && x >= 0 && x < a.V;
+    for (int i = 0; i < k && ok; ++i) ok = ktok[i] != x;
+    int f2 = 0;
+    zk[k] = ok ? sanitize_logit(__ldg(zrow + x), f2) : -INFINITY;
+    uk[k] = a.uniforms[fo + kid[k]];
+  }
+}
+
+// Bitmap of the children's tokens inside [lo, lo + 32 * words) (point-mass
+// rows: their chunk sums leave those tokens out).  Every thread calls it; the
+// bitmap must be zero on entry.
+__device__ __forceinline__ void mark_child_tokens(const VerifyArgs &a, long long fo, const int *kid, int nkid, int lo,
+                                                  int words, unsigned int *bits) {
+  for (int k = threadIdx.x; k < nkid; k += blockDim.x) {
+    const int off = a.flat_tok[fo + kid[k]] - lo;
+    if (off >= 0 && off < 32 * words) atomicOr(&bits[off >> 5], 1u << (off & 31));
+  }
+  __syncthreads();
 }
 
 // Draft-q test of one child from p and q at its token and the residual
@@ -129,24 +186,27 @@ struct WalkSmem {
   int par[kMaxN], tokf[kMaxN], nodef[kMaxN];
   float rs0[kMaxN], rs1[kMaxN];  // per flat row: argmax id (bits) / max, -, / sum
   float qs0[kMaxN], qs1[kMaxN];  // draft-q: max and sum of q at each row
-  float zc[kMaxN];               // target logit of each row's token in its parent's row
+  float zc[kMaxN];               // phase 1: target logit of each child's token (by child rank)
   float dc[kMaxN];               // phase 1, draft-q: draft logit of each child's token (by child rank)
+  int ktok[kMaxN];               // phase 1, point-mass: each child's token (by child rank)
   float cf[kMaxN];               // draft-q: c of the residual once all of a row's children are rejected
-  int acc[kMaxN];                // draft-q: accepted child of each row (-1 leaf, -2 all rejected)
+  int acc[kMaxN];                // accepted child of each row (-1 leaf, -2 all rejected)
   int kid[kMaxN];                // phase 1: the children of the block's row
   int opath[kMaxDepth + 2], otok[kMaxDepth + 2];
-  int rej[kMaxTopk];
-  float rejw[kMaxTopk];  // exp(z/T - M) of each rejected child at the stop row
-  unsigned int rejbits[kMaxSpanWords];  // rejected children inside the chunk being scanned
+  int rej[kMaxN];                // the tokens of the stop row's children (all rejected)
+  unsigned int rejbits[kMaxSpanWords];  // phase 1: children's tokens in the block's span; bonus draw: rejected
+                                        // children inside the chunk being scanned
+  float s_M, s_S;
   float uni[kMaxN];      // this sequence's uniforms
   int s_nrej, s_cur, s_alen, s_kids, s_nkid;
 };
 
 // Phase 2 of acceptance, run by the last row-block of sequence b: everything
-// the walk needs (row statistics, the logits of every child's token in its
-// parent's row, uniforms) is fetched in parallel; one warp walks the kept
-// tree from the root, testing 32 children (ascending flat row) per step; the
-// block then draws the bonus token at the row where the walk stops.
+// the walk needs (row statistics, the decision phase 1 took at each row,
+// uniforms) is fetched in parallel; one warp walks the kept tree from the
+// root (greedy: 32 candidate rows per ballot; stochastic: the accepted child
+// of each row); the block then draws the bonus token at the row where the
+// walk stops.
 template <int NT, bool kDraftQ>
 __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
   const int t = threadIdx.x;
@@ -155,6 +215,7 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
   const long long fo = (long long)b * N;
   const bool greedy = a.mode == ET_ACCEPT_GREEDY, dq = kDraftQ && a.mode == ET_ACCEPT_STOCH_DRAFTQ;
   const float invT = 1.f / a.T;
+  const auto child_of = [&](int ac, int j) { return (ac > j && ac < N) || ac == -2 ? ac : -1; };
   int badp = 0;
   for (int j = t; j < N; j += NT) {
     const int p = a.flat_parent[fo + j], x = a.flat_tok[fo + j];
@@ -169,10 +230,9 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
       w.qs0[j] = lo4.x;
       w.qs1[j] = lo4.y;
       w.cf[j] = lo4.z;
-      const int ac = __float_as_int(lo4.w);
-      w.acc[j] = (ac > j && ac < N) || ac == -2 ? ac : -1;
-    } else if (!greedy) {
-      w.zc[j] = (j > 0 && p >= 0 && p < j) ? ld_cg(a.dq + 8 * (fo + j) + 6) : -INFINITY;
+      w.acc[j] = child_of(__float_as_int(lo4.w), j);
+    } else if (!greedy) {  // point-mass: the decision phase 1 took at the row
+      w.acc[j] = child_of(__float_as_int(ld_cg(a.dq + 8 * (fo + j) + 3)), j);
     }
   }
   __syncthreads();
@@ -192,37 +252,7 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
           if (hit) { nxt = j0 + __ffs(hit) - 1; break; }
         }
         if (nxt < 0 && lane == 0) w.otok[alen] = am;
-      } else if (!dq) {
-        const float M = w.rs0[cur], S = w.rs1[cur];
-        float R = 0.f;
-        for (int j0 = cur + 1; j0 < N && nxt < 0; j0 += 32) {
-          const int j = j0 + lane;
-          const bool child = j < N && par[j] == cur;
-          // p(x) and the uniform of every child at once; R (the mass of the
-          // siblings rejected before a child) as a prefix sum in row order
-          const float wx = child ? expf(w.zc[j] / a.T - M) : 0.f;
-          const float px = (child && S > 0.f) ? wx / S : 0.f;
-          float incl = px;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-          }
-          const float Rj = R + (incl - px);
-          const bool acc = child && w.uni[j] < ((Rj < 1.f) ? px / (1.f - Rj) : INFINITY);
-          const unsigned int kidm = __ballot_sync(0xffffffffu, child);
-          const unsigned int hit = __ballot_sync(0xffffffffu, acc);
-          const unsigned int rejected = hit ? (kidm & ((1u << (__ffs(hit) - 1)) - 1u)) : kidm;
-          if ((rejected >> lane) & 1u) {  // children before the accepted one, in row order
-            const int slot = nrej + __popc(rejected & ((1u << lane) - 1u));
-            if (slot < kMaxTopk) { rej[slot] = tokf[j]; w.rejw[slot] = wx; }
-          }
-          nrej += __popc(rejected);
-          R += __shfl_sync(0xffffffffu, incl, 31);
-          if (hit) nxt = j0 + __ffs(hit) - 1;
-        }
-        if (nrej > kMaxTopk) nrej = kMaxTopk;
-      } else {  // draft-q: phase 1 decided every row
+      } else {  // stochastic: phase 1 decided every row
         const int ac = w.acc[cur];
         nxt = ac >= 0 ? ac : -1;
         kids = ac == -2;
@@ -234,6 +264,15 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
       }
       ++alen;
       cur = nxt;
+    }
+    if (!greedy && !dq && kids) {  // point-mass, every child rejected: the draw leaves out their tokens
+      for (int j0 = cur + 1; j0 < N; j0 += 32) {
+        const int j = j0 + lane;
+        const bool c = j < N && par[j] == cur;
+        const unsigned int m = __ballot_sync(0xffffffffu, c);
+        if (c) rej[nrej + __popc(m & ((1u << lane) - 1u))] = tokf[j];
+        nrej += __popc(m);
+      }
     }
     if (lane == 0) {
       w.s_cur = cur;
@@ -249,20 +288,20 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
     int badz = 0;
     const float *zr = table_row(a.tlog, a.tstride, a.tmap, a.C, b, nodef[cur], fo + cur, badz);
     const float *cst = a.part + (fo + cur) * (long long)a.nchunk * 2;
-    const CdfRow cdf{a.cdf_span, a.cdf_nch, a.V, a.vec4t, a.T};
+    const CdfRow cdf{a.cdf_span, a.cdf_nch, a.V, a.vec4t, a.T, invT};  // chunk maxima are raw logits
     int bonus;
     if (dq && w.s_kids > 0) {  // every child rejected: phase 1 left the chunk sums of max(p - c q, 0)
       const float *dr = table_row(a.dlog, a.dstride, a.dmap, a.C, b, nodef[cur], fo + cur, badz);
       const float M = w.rs0[cur], S = w.rs1[cur], Mq = w.qs0[cur], Sq = w.qs1[cur], c = w.cf[cur];
       const float invS = S > 0.f ? 1.f / S : 0.f, invSq = Sq > 0.f ? 1.f / Sq : 0.f;
-      bonus = chunk_inverse_cdf<NT, true>(cdf, zr, dr, a.vec4d, cst, M, w.uni[0], nullptr, nullptr, 0, w.redz,
-                                          w.redi, w.cdf_tsum, w.rejbits, [&](float zt, float zd) -> float {
+      bonus = chunk_inverse_cdf<NT, true>(cdf, zr, dr, a.vec4d, cst, M, w.uni[0], nullptr, 0, w.redz, w.redi,
+                                          w.cdf_tsum, w.rejbits, [&](float zt, float zd) -> float {
                                             return dq_excess(dq_weight(__fmul_rn(zt, invT), M, invS),
                                                              dq_weight(__fmul_rn(zd, invT), Mq, invSq), c);
                                           });
-    } else {  // point-mass residual (rejected children removed), or a leaf: p itself
-      bonus = bonus_from_chunks<NT>(cdf, zr, cst, w.rs0[cur], w.uni[0], rej, w.rejw, dq ? 0 : w.s_nrej, w.redz,
-                                    w.redi, w.cdf_tsum, w.rejbits);
+    } else {  // point-mass residual (the children's tokens already out of the chunk sums), or a leaf: p
+      bonus = bonus_from_chunks<NT, true>(cdf, zr, cst, w.rs0[cur], w.uni[0], rej, w.s_nrej, w.redz, w.redi,
+                                          w.cdf_tsum, w.rejbits);
     }
     if (t == 0) w.otok[alen] = bonus;
     badp |= badz;
@@ -281,9 +320,9 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
 // q's max and sum, then the children in row order, each tested against the
 // residual in force and, when rejected, one pass over the row for the next
 // (c, F); when every child is rejected, the chunk sums of max(p - c q, 0) for
-// the bonus draw.
+// the bonus draw.  Returns whether the row has children.
 template <int NT>
-__device__ void dq_row_block(const VerifyArgs &a, long long row, int b, int node, const float *zr, float M, float S,
+__device__ bool dq_row_block(const VerifyArgs &a, long long row, int b, int node, const float *zr, float M, float S,
                              WalkSmem &w) {
   const int t = threadIdx.x;
   const int i = (int)(row - (long long)b * a.N);
@@ -291,7 +330,7 @@ __device__ void dq_row_block(const VerifyArgs &a, long long row, int b, int node
   const int nkid = child_list<NT>(a.flat_parent + fo, a.N, i, w.kid, &w.s_nkid);
   if (nkid == 0) {
     if (t == 0) a.dq[8 * row + 3] = __int_as_float(-1);  // a leaf
-    return;
+    return false;
   }
   int bad = 0, flag = 0;
   const float *dr = table_row(a.dlog, a.dstride, a.dmap, a.C, b, node, row, bad);
@@ -350,6 +389,7 @@ __device__ void dq_row_block(const VerifyArgs &a, long long row, int b, int node
   }
   if (flag) flag_status(a.dev_status, ET_DEV_NONFINITE);
   if (bad && t == 0) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
+  return true;
 }
 
 __global__ void __launch_bounds__(kVThreads) k_verify(VerifyArgs a) {
@@ -383,11 +423,21 @@ __global__ void __launch_bounds__(kVThreads) k_verify(VerifyArgs a) {
     for (int j = 0; j < 4; ++j)
       if (e0 + j < a.V) v[4 * u + j] = sanitize_logit(v[4 * u + j], flag);
   }
-  if (a.mode == ET_ACCEPT_STOCH_POINT) {  // children's logits at this row, from the block holding their token
-    const int i = row - b * a.N;
-    const long long fo = (long long)row - i;
-    const int nkid = child_list<kVThreads>(a.flat_parent + fo, a.N, i, w.kid, &w.s_nkid);
-    if (a.mode == ET_ACCEPT_STOCH_POINT && nkid > 0) store_child_logits(a, fo, w.kid, nkid, zrow, c0, c0 + kVChunk, c == 0);
+  const int i = row - b * a.N;
+  const long long fo = (long long)row - i;
+  int nkid = 0;
+  if (a.mode == ET_ACCEPT_STOCH_POINT) {  // the chunk's sums leave out the tokens of the row's children
+    constexpr int kWords = kVChunk / 32;
+    for (int x = t; x < kWords; x += kVThreads) w.rejbits[x] = 0u;
+    nkid = child_list<kVThreads>(a.flat_parent + fo, a.N, i, w.kid, &w.s_nkid);
+    if (nkid > 0) {
+      mark_child_tokens(a, fo, w.kid, nkid, c0, kWords, w.rejbits);
+#pragma unroll
+      for (int j = 0; j < 4 * kVVec; ++j) {
+        const int off = ((j >> 2) * kVThreads + t) * 4 + (j & 3);
+        if ((w.rejbits[off >> 5] >> (off & 31)) & 1u) v[j] = -INFINITY;
+      }
+    }
   }
   float *prt = a.part + ((long long)row * a.nchunk + c) * 2;
   if (a.mode == ET_ACCEPT_GREEDY) {
@@ -400,18 +450,16 @@ __global__ void __launch_bounds__(kVThreads) k_verify(VerifyArgs a) {
     }
     block_best<kVThreads>(bz, bi, redz, redi);
     if (t == 0) { prt[0] = bz; prt[1] = __int_as_float(bi); }
-  } else {
+  } else {  // (max of the raw logits, sum of exp((z - max) / T)) of the chunk
+    const float invT = 1.f / a.T;
     float lm = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < 4 * kVVec; ++j) {
-      v[j] = v[j] / a.T;
-      lm = fmaxf(lm, v[j]);
-    }
+    for (int j = 0; j < 4 * kVVec; ++j) lm = fmaxf(lm, v[j]);
     const float Mc = block_max<kVThreads>(lm, redz);
     float ls = 0.f;
     if (Mc > -INFINITY) {
 #pragma unroll
-      for (int j = 0; j < 4 * kVVec; ++j) ls += v[j] > -INFINITY ? expf(v[j] - Mc) : 0.f;
+      for (int j = 0; j < 4 * kVVec; ++j) ls += v[j] > -INFINITY ? expf((v[j] - Mc) * invT) : 0.f;
     }
     const float Sc = block_sum<kVThreads>(ls, redz);
     if (t == 0) { prt[0] = Mc; prt[1] = Sc; }
@@ -433,12 +481,26 @@ __global__ void __launch_bounds__(kVThreads) k_verify(VerifyArgs a) {
       block_best<kVThreads>(bz, bi, redz, redi);
       if (t == 0) { a.rowstat[2 * row] = __int_as_float(bi); a.rowstat[2 * row + 1] = bz; }
     } else {
+      const float invT = 1.f / a.T;
       float cm = -INFINITY, cs = 0.f;
       if (t < a.nchunk) { cm = ld_cg(rp + 2 * t); cs = ld_cg(rp + 2 * t + 1); }
       const float M = block_max<kVThreads>(cm, redz);
-      const float S = block_sum<kVThreads>((t < a.nchunk && cm > -INFINITY) ? cs * expf(cm - M) : 0.f, redz);
-      if (t == 0) { a.rowstat[2 * row] = M; a.rowstat[2 * row + 1] = S; }
-      if (a.mode == ET_ACCEPT_STOCH_DRAFTQ) dq_row_block<kVThreads>(a, row, b, node, zrow, M, S, w);
+      const float S =
+          block_sum<kVThreads>((t < a.nchunk && cm > -INFINITY) ? cs * expf((cm - M) * invT) : 0.f, redz);
+      if (a.mode == ET_ACCEPT_STOCH_DRAFTQ) {
+        // the residual arithmetic runs on z / T: its maximum is fl(M / T), the sum is the same
+        const bool kids = dq_row_block<kVThreads>(a, row, b, node, zrow, __fmul_rn(M, invT), S, w);
+        if (t == 0) { a.rowstat[2 * row] = kids ? __fmul_rn(M, invT) : M; a.rowstat[2 * row + 1] = S; }
+      } else {
+        if (t == 0) { a.rowstat[2 * row] = M; a.rowstat[2 * row + 1] = S; }
+        int acc = -1;  // a leaf
+        if (nkid > 0) {
+          pm_child_inputs(a, fo, w.kid, nkid, zrow, w.ktok, w.zc, w.uni);
+          __syncthreads();
+          if (t < 32) acc = pm_decide(nkid, w.kid, w.zc, w.uni, M, S, invT);
+        }
+        if (t == 0) a.dq[8 * (long long)row + 3] = __int_as_float(acc);
+      }
     }
   }
   if (!arrive_last(&a.seq_cnt[b], (unsigned)a.N, &sflag)) return;
@@ -509,9 +571,22 @@ __global__ void __launch_bounds__(kVClThreads) k_verify_cl(VerifyArgs a) {
   const bool greedy = a.mode == ET_ACCEPT_GREEDY;
   const long long fo = (long long)row - i;
   int nkid = 0;
-  if (!greedy)  // the children of this row (every block of the cluster finds the same)
+  if (!greedy) {  // the children of this row (every block of the cluster finds the same)
+    if (!kDraftQ)
+      for (int x = t; x < kVClSpan / 32; x += kVClThreads) w.rejbits[x] = 0u;
     nkid = child_list<kVClThreads>(a.flat_parent + fo, a.N, i, w.kid, &w.s_nkid);
-  if (!kDraftQ && nkid > 0) store_child_logits(a, fo, w.kid, nkid, zrow, base, base + kVClSpan, q == 0);
+  }
+  if (!kDraftQ && nkid > 0) {
+    // point-mass: this block's sums leave out the children's tokens, and the
+    // leader fetches the children's logits for the row's decision
+    mark_child_tokens(a, fo, w.kid, nkid, base, kVClSpan / 32, w.rejbits);
+#pragma unroll
+    for (int e = 0; e < 4 * kVClVec; ++e) {
+      const int off = (e >> 2) * (kVClThreads * 4) + t * 4 + (e & 3);
+      if ((w.rejbits[off >> 5] >> (off & 31)) & 1u) v[e] = -INFINITY;
+    }
+    if (q == 0) pm_child_inputs(a, fo, w.kid, nkid, zrow, w.ktok, w.zc, w.uni);
+  }
   if (kDraftQ && nkid > 0) {
     const float invT = 1.f / a.T;
     const float *drow = table_row(a.dlog, a.dstride, a.dmap, a.C, b, node, row, bad);
@@ -646,14 +721,10 @@ __global__ void __launch_bounds__(kVClThreads) k_verify_cl(VerifyArgs a) {
       }
       best = warp_min_u64(best);
       if (lane == 0) wkey[warp] = best;
-    } else {
+    } else {  // (max of the raw logits, sum of exp((z - max) / T)) of this block's slice
       float lm = -INFINITY;
-      const float invT = 1.f / a.T;
 #pragma unroll
-      for (int e = 0; e < 4 * kVClVec; ++e) {
-        v[e] = v[e] * invT;
-        lm = fmaxf(lm, v[e]);
-      }
+      for (int e = 0; e < 4 * kVClVec; ++e) lm = fmaxf(lm, v[e]);
       lm = warp_max(lm);
       if (lane == 0) wmax[warp] = lm;
     }
@@ -667,13 +738,14 @@ __global__ void __launch_bounds__(kVClThreads) k_verify_cl(VerifyArgs a) {
         if (lane == 0) cl_st_u64(cl_map(&gkey[q], 0), kk);
       }
     } else {
+      const float invT = 1.f / a.T;
       float Mq = wmax[0];
 #pragma unroll
       for (int x = 1; x < NW; ++x) Mq = fmaxf(Mq, wmax[x]);
       float ls = 0.f;
       if (Mq > -INFINITY) {
 #pragma unroll
-        for (int e = 0; e < 4 * kVClVec; ++e) ls += exp_fast(v[e] - Mq);
+        for (int e = 0; e < 4 * kVClVec; ++e) ls += exp_fast((v[e] - Mq) * invT);
       }
       ls = warp_sum(ls);
       if (lane == 0) wsum[warp] = ls;
@@ -695,15 +767,24 @@ __global__ void __launch_bounds__(kVClThreads) k_verify_cl(VerifyArgs a) {
         a.rowstat[2 * row] = __int_as_float((int)zid_id(kk));
         a.rowstat[2 * row + 1] = zid_value(kk);
       } else {
+        const float invT = 1.f / a.T;
         float M = -INFINITY;
         for (int x = 0; x < R; ++x) M = fmaxf(M, gms[x].x);
         float S = 0.f;
-        for (int x = 0; x < R; ++x) S += gms[x].x > -INFINITY ? gms[x].y * expf(gms[x].x - M) : 0.f;
+        for (int x = 0; x < R; ++x) S += gms[x].x > -INFINITY ? gms[x].y * expf((gms[x].x - M) * invT) : 0.f;
         a.rowstat[2 * row] = M;
         a.rowstat[2 * row + 1] = S;
         float *cst = a.part + (long long)row * a.nchunk * 2;  // chunk statistics for the bonus draw
         for (int x = 0; x < R; ++x) { cst[2 * x] = gms[x].x; cst[2 * x + 1] = gms[x].y; }
+        w.s_M = M;
+        w.s_S = S;
       }
+    }
+    if (!kDraftQ && !greedy) {  // point-mass: the row's decision, by one warp
+      __syncthreads();
+      int acc = -1;  // a leaf
+      if (nkid > 0 && t < 32) acc = pm_decide(nkid, w.kid, w.zc, w.uni, w.s_M, w.s_S, 1.f / a.T);
+      if (t == 0) a.dq[8 * (long long)row + 3] = __int_as_float(acc);
     }
   }
   if (!arrive_last(&a.seq_cnt[b], (unsigned)a.N, &sflag)) return;

@@ -12,7 +12,8 @@ suites (MT-bench, HumanEval, GSM8K, Alpaca, CNN/DM, Natural Questions) are
 replaced by the recipe below, which mimics a confident draft model:
 
 * target logits of node x: a seeded random permutation ``perm`` of the vocab,
-  ``target[perm[r]] = -1.2 * ln(r + 1) + N(0, 1)`` (Zipf-skewed ranks);
+  ``target[perm[r]] = -s * ln(r + 1) + N(0, 1)`` (Zipf-skewed ranks, slope
+  s = 1.2 unless a test asks for a steeper one);
 * draft logits of node x: ``target + sigma * N(0, 1)``;
 * Q/K/V ~ N(0, 1), rounded to bf16 (round-to-nearest-even) or kept fp32;
 * acceptance uniforms ~ U[0, 1) in fp32;
@@ -57,6 +58,7 @@ class Workload:
     B: int = 1
     temperature: float = 1.0
     ragged: bool = False  # prefixes drawn from U{512..16384}
+    slope: float = 1.2    # Zipf slope of the target logits (steeper: more mass on the top ranks)
 
     @property
     def seed(self) -> int:
@@ -118,7 +120,7 @@ def node_logits(wl: Workload, b: int, seed_id: int) -> Tuple[np.ndarray, np.ndar
     rng = _rng(wl.seed, b, seed_id)
     perm = rng.permutation(wl.V)
     target64 = np.empty(wl.V, dtype=np.float64)
-    target64[perm] = -1.2 * np.log(np.arange(1, wl.V + 1, dtype=np.float64)) + rng.standard_normal(wl.V)
+    target64[perm] = -wl.slope * np.log(np.arange(1, wl.V + 1, dtype=np.float64)) + rng.standard_normal(wl.V)
     draft64 = target64 + wl.sigma * rng.standard_normal(wl.V)
     return target64.astype(np.float32), draft64.astype(np.float32)
 
