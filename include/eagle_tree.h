@@ -8,6 +8,8 @@
  *
  *   for layer = 0 .. depth-1:  [et_lm_head: draft features -> logits]
  *                              et_tree_expand      (expansion phase)
+ *     (or et_tree_build: all layers in one launch, then the rerank and mask,
+ *      when the draft logits of every node are available up front)
  *     (or et_static_tree: a fixed tree shape, EAGLE-1 / Medusa style)
  *   et_tree_rerank                                  (reranking phase, flatten)
  *   et_tree_mask_posids                             (attention mask, positions)
@@ -53,7 +55,7 @@ extern "C" {
 struct CUstream_st;                       /* = cudaStream_t's pointee */
 typedef struct CUstream_st *et_stream_t;
 
-#define ET_ABI_VERSION 1
+#define ET_ABI_VERSION 2
 
 typedef enum {
     ET_OK = 0,
@@ -112,7 +114,7 @@ typedef enum { ET_BF16 = 0, ET_F32 = 1 } et_dtype;
 
 typedef enum {
     ET_ACCEPT_GREEDY = 0,       /* argmax match along the tree */
-    ET_ACCEPT_STOCH_POINT = 1,  /* point-mass proposals: accept child x w.p. p(x)/(1-R) */
+    ET_ACCEPT_STOCH_POINT = 1,  /* point-mass proposals: accept child x w.p. r(x)/sum(r) */
     ET_ACCEPT_STOCH_DRAFTQ = 2  /* draft-q proposals: min(1, r(x)/q(x)), residual update */
 } et_accept_mode;
 
@@ -128,7 +130,17 @@ typedef struct {
     int32_t impl;             /* 0 = auto (tcgen05 for bf16 with d = 128, else mma.sync),
                                  1 = mma.sync tensor-core path, 2 = tcgen05 path
                                  (ET_ERR_UNSUPPORTED unless bf16 and d = 128) */
+    int32_t flags;            /* ET_ATTN_* bits below, 0 = none */
 } et_attn_shape;
+
+/* et_attn_shape.flags: the caller promises that q, k/v_prefix, k/v_tree,
+ * kv_row0 and prefix_len are not written by the kernel launched just before
+ * this call in the same stream (only the mask may come from it, as it does
+ * from et_tree_rerank_mask in a verification step).  The tcgen05 path may
+ * then fetch its first tiles before it waits for that kernel to finish,
+ * which hides their memory latency behind that kernel's tail; the mask, the
+ * outputs and the workspace are touched only after the wait. */
+#define ET_ATTN_INPUTS_READY 1
 
 /* Draft LM head shape (host struct), see et_lm_head. */
 typedef struct {
@@ -220,9 +232,13 @@ et_status et_tree_expand(const et_tree_cfg *cfg, int32_t layer,
  * 4 * B * m_l * ceil(V / 2048) * (2 + 2k) bytes of partials must fit in
  * 4 MiB (e.g. B*m_l <= 2900 at V = 32000, k = 10); larger shapes return
  * ET_ERR_WORKSPACE and launch nothing.
- * Set-up: the first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before capturing a stream into a CUDA graph.
+ * Set-up: the first call in each CUDA context (normally a device's primary
+ * context) looks up the array's device address (cudaGetSymbolAddress) with
+ * that context's device current and keeps it for that context; make that
+ * first call before capturing a stream into a CUDA graph.  A context that
+ * was destroyed (cudaDeviceReset) must not be followed by a new one that the
+ * driver gives the same handle while this library stays loaded: the kept
+ * address would then be stale.
  * Sharing: every call on a device uses the same array and leaves its
  * contents behind; each call clears the counters it needs on `stream`
  * (cudaMemsetAsync) before its kernel.  Two calls whose work can overlap
@@ -269,6 +285,55 @@ et_status et_tree_rerank_mask(const et_tree_cfg *cfg, et_tree *tree, const int32
                               uint64_t *mask, int32_t *posids, int32_t *dev_status, et_stream_t stream);
 
 /*
+ * et_tree_build -- the whole draft tree in one call: D expansion layers, then
+ * the rerank with the attention mask and positions (EAGLE-2 article:
+ * expansion phase layer after layer, reranking phase, attention mask and
+ * position encoding).  Writes exactly what D calls of et_tree_expand (layers
+ * 0..D-1) followed by et_tree_rerank_mask write, for draft logits that are
+ * all available up front (a node-indexed table and row_of_node as in
+ * et_tree_expand, read for the root and every frontier node).
+ *
+ * When V <= 32768 and the B * max_l(m_l) thread-block clusters (one per
+ * sequence and frontier slot, ceil(V / 4096) blocks each) fit on the GPU at
+ * once, the D layers are ONE kernel launch: each cluster expands its
+ * frontier slot in every layer; it waits on the device (a bounded spin on a
+ * per-layer counter) until every row of the previous layer has written its
+ * children, then picks the frontier itself.  The rerank with the mask and
+ * positions follows as a second launch (et_tree_rerank_mask's kernel).
+ * Otherwise it issues the D + 1 launches of the per-layer calls (same
+ * results).  et_tree_build_launches(cfg) says which.
+ *
+ * mask, posids, prefix_len: as in et_tree_rerank_mask; all three null skips
+ *               the mask and positions (then it ends like et_tree_rerank).
+ * ws            et_tree_workspace_size(cfg) bytes (see conventions); the
+ *               one-launch form counts each layer's finished rows in it and
+ *               leaves those counters at zero.
+ * A flag wait that gives up (never expected: all clusters are resident)
+ * sets ET_DEV_TIMEOUT; the tree is then invalid and so are the workspace's
+ * counters (layers may have finished out of order): zero the workspace again
+ * before its next use.
+ */
+et_status et_tree_build(const et_tree_cfg *cfg, const float *logits, int64_t row_stride,
+                        const int32_t *row_of_node, et_tree *tree, const int32_t *prefix_len,
+                        uint64_t *mask, int32_t *posids, int32_t *dev_status,
+                        void *ws, size_t ws_bytes, et_stream_t stream);
+/* Kernel launches et_tree_build makes for cfg on the current device: 2, or D + 1. */
+int32_t et_tree_build_launches(const et_tree_cfg *cfg);
+
+/*
+ * et_set_wait_limit -- a diagnostic, not part of the method.  Sets the bound,
+ * in SM clock cycles, of every device-side wait of the kernels launched
+ * after the call (the mbarrier waits of et_tree_attention's tcgen05 path and
+ * of et_lm_head, the frontier waits of et_tree_build); 0 or a negative value
+ * restores the default of 2^32 cycles (about 2 s).  A wait that runs out
+ * sets ET_DEV_TIMEOUT in dev_status; the kernel lets its copies and MMAs in
+ * flight finish (with the default bound), frees its tensor memory and
+ * returns, and that call's outputs are undefined.  Small values exist to
+ * exercise that path.  Process-wide; returns the previous bound.
+ */
+int64_t et_set_wait_limit(int64_t cycles);
+
+/*
  * et_tree_attention -- attention of the N flattened draft rows over the KV
  * prefix plus their in-tree ancestors (EAGLE-2 article: each token sees only
  * its ancestors; EAGLE blog 1.1: one target forward verifies the draft).
@@ -288,15 +353,18 @@ et_status et_tree_rerank_mask(const et_tree_cfg *cfg, et_tree *tree, const int32
  * lse           nullable fp32 [B, Hq, N]: natural-log log-sum-exp of the
  *               scaled scores of each row.
  * ws            et_tree_attention_workspace_size(shape) bytes, 256-byte
- *               aligned, owned by the caller, no initial contents required
- *               (may be 0/null when that size is 0: the fp32 path or one
- *               split).  Holds the fp32 partial rows and (max, sum) pairs of
- *               the KV splits; the tcgen05 path drops its lines from L2 once
- *               merged.  Calls that run at the same time need separate
- *               workspaces.
+ *               aligned, owned by the caller, zero-filled once before its
+ *               first use like every workspace (may be 0/null when that size
+ *               is 0: the fp32 path or one split).  Holds the fp32 partial
+ *               rows and (max, sum) pairs of the KV splits (and, on the
+ *               mma.sync path, one arrival counter per row tile, which every
+ *               call leaves at zero); the tcgen05 path drops the partial
+ *               rows' lines from L2 once merged.  Calls that run at the same
+ *               time need separate workspaces.
  * Accumulation is fp32; P is rounded to the input dtype before P.V.
- * tcgen05 path: at most 8 splits (one cluster); a bounded wait that expires
- * sets ET_DEV_TIMEOUT in dev_status and leaves that tile's output undefined.
+ * tcgen05 path: at most 8 splits (one thread-block cluster); a bounded wait
+ * that expires sets ET_DEV_TIMEOUT in dev_status and leaves that tile's
+ * output undefined.
  */
 et_status et_tree_attention(const et_attn_shape *shape,
                             const void *q, const void *k_prefix, const void *v_prefix,
@@ -314,11 +382,17 @@ et_status et_tree_attention(const et_attn_shape *shape,
  *  GREEDY: a child is accepted iff its token is the argmax (lowest id on
  *    ties) of the current row's target logits; the bonus token is that
  *    argmax at the row where the walk stops.
- *  STOCH_POINT: p = softmax(target / T); child x is accepted iff
- *    uniforms[b, child] < p(x) / (1 - R), R = p-mass of siblings rejected
- *    so far at this row; bonus = smallest token t whose cumulative residual
- *    mass (rejected tokens removed, ascending token id) exceeds
- *    uniforms[b, 0] * (remaining mass).
+ *  STOCH_POINT: p = softmax(target / T); each child is a point-mass
+ *    proposal, so child x is accepted iff uniforms[b, child] < r(x) / sum(r),
+ *    r = p with the tokens of the siblings rejected so far at this row
+ *    removed (p(x) / (1 - R) for distinct tokens, R their mass; a repeat of a
+ *    rejected token is never accepted); bonus = smallest token t whose
+ *    cumulative residual mass (ascending token id) exceeds
+ *    uniforms[b, 0] * sum(r).  The ratio is evaluated as
+ *    e(x) / (S_rest + sum of e over x and the later distinct siblings), e the
+ *    unnormalised weights and S_rest the row's weight outside every child
+ *    token: sums of positive terms, so it keeps its relative precision when
+ *    the rejected siblings hold almost all of the mass.
  *  STOCH_DRAFTQ: q = softmax(draft row of the current node / T); accept iff
  *    uniforms[b, child] < min(1, r(x) / q(x)), r starting at p and becoming
  *    norm(max(r - q, 0)) after each rejection (kept if that mass is 0);

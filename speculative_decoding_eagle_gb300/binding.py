@@ -24,10 +24,12 @@ ET_DEV_NONFINITE, ET_DEV_BAD_INDEX, ET_DEV_DISCONNECTED, ET_DEV_TIMEOUT = 1, 2, 
 ET_BF16, ET_F32 = 0, 1
 ET_ACCEPT_GREEDY, ET_ACCEPT_STOCH_POINT, ET_ACCEPT_STOCH_DRAFTQ = 0, 1, 2
 ATTN_AUTO, ATTN_MMA_SYNC, ATTN_TCGEN05 = 0, 1, 2
+ET_ATTN_INPUTS_READY = 1
 
 EXPORTED = ("et_num_candidates", "et_layer_expanded", "et_layer_base", "et_tree_workspace_size",
             "et_tree_attention_workspace_size", "et_tree_attention_splits", "et_workspace_init",
             "et_status_string", "et_abi_version", "et_tree_expand", "et_tree_expand_noalloc", "et_tree_rerank", "et_tree_rerank_mask",
+            "et_tree_build", "et_tree_build_launches", "et_set_wait_limit",
             "et_tree_mask_posids", "et_tree_attention", "et_verify_accept", "et_kv_commit", "et_static_tree", "et_lm_head", "et_static_tree_sampled",
             "et_static_tree_workspace_size")
 
@@ -45,7 +47,7 @@ class TreeC(ctypes.Structure):
 class AttnShapeC(ctypes.Structure):
     _fields_ = [("B", c_i32), ("N", c_i32), ("Hq", c_i32), ("Hkv", c_i32), ("d", c_i32), ("dtype", c_i32),
                 ("scale", c_f32), ("max_prefix", c_i32), ("kv_rows", c_i64), ("kv_head_stride", c_i64),
-                ("num_splits", c_i32), ("impl", c_i32)]
+                ("num_splits", c_i32), ("impl", c_i32), ("flags", c_i32)]
 
 
 class LmHeadShapeC(ctypes.Structure):
@@ -95,6 +97,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "et_tree_rerank": (c_i32, [P(TreeCfgC), P(TreeC), c_vp, c_vp]),
         "et_tree_rerank_mask": (c_i32, [P(TreeCfgC), P(TreeC), c_vp, c_vp, c_vp, c_vp, c_vp]),
         "et_tree_mask_posids": (c_i32, [P(TreeCfgC), P(TreeC), c_vp, c_vp, c_vp, c_vp]),
+        "et_tree_build": (c_i32, [P(TreeCfgC), c_vp, c_i64, c_vp, P(TreeC), c_vp, c_vp, c_vp, c_vp, c_vp, c_sz,
+                                  c_vp]),
+        "et_tree_build_launches": (c_i32, [P(TreeCfgC)]),
+        "et_set_wait_limit": (c_i64, [c_i64]),
         "et_tree_attention": (c_i32, [P(AttnShapeC), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                       c_vp, c_vp, c_sz, c_vp]),
         "et_static_tree_workspace_size": (c_sz, [P(StaticCfgC)]),
@@ -288,6 +294,31 @@ def et_tree_rerank_mask(cfg: TreeCfg, tree: TreeBuffers, prefix_len: torch.Tenso
     _check("et_tree_rerank_mask", st)
 
 
+def et_tree_build(cfg: TreeCfg, logits: torch.Tensor, tree: TreeBuffers, ws: torch.Tensor,
+                  row_of_node: Optional[torch.Tensor] = None, prefix_len: Optional[torch.Tensor] = None,
+                  mask: Optional[torch.Tensor] = None, posids: Optional[torch.Tensor] = None,
+                  dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be a [rows, >=V] fp32 table with unit inner stride")
+    if not logits.is_cuda or logits.dtype != torch.float32:
+        raise ValueError("logits must be a CUDA fp32 tensor")
+    st = load().et_tree_build(ctypes.byref(cfg.c()), logits.data_ptr(), logits.stride(0),
+                              _ptr(row_of_node, torch.int32, "row_of_node"), ctypes.byref(tree.c()),
+                              _ptr(prefix_len, torch.int32, "prefix_len"), _ptr(mask, torch.int64, "mask"),
+                              _ptr(posids, torch.int32, "posids"), _ptr(dev_status, torch.int32, "dev_status"),
+                              _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream))
+    _check("et_tree_build", st)
+
+
+def et_tree_build_launches(cfg: TreeCfg) -> int:
+    return int(load().et_tree_build_launches(ctypes.byref(cfg.c())))
+
+
+def et_set_wait_limit(cycles: int) -> int:
+    """Bound (SM cycles) of device waits of later launches; 0 restores the default. Returns the previous bound."""
+    return int(load().et_set_wait_limit(int(cycles)))
+
+
 def et_tree_mask_posids(cfg: TreeCfg, tree: TreeBuffers, prefix_len: torch.Tensor, mask: torch.Tensor,
                         posids: torch.Tensor, stream=None) -> None:
     st = load().et_tree_mask_posids(ctypes.byref(cfg.c()), ctypes.byref(tree.c()),
@@ -310,11 +341,12 @@ class AttnShape:
     kv_head_stride: int = 0
     num_splits: int = 0
     impl: int = ATTN_AUTO
+    flags: int = 0
 
     def c(self) -> AttnShapeC:
         sc = self.scale if self.scale > 0 else self.d ** -0.5
         return AttnShapeC(self.B, self.N, self.Hq, self.Hkv, self.d, self.dtype, sc, self.max_prefix,
-                          self.kv_rows, self.kv_head_stride, self.num_splits, self.impl)
+                          self.kv_rows, self.kv_head_stride, self.num_splits, self.impl, self.flags)
 
 
 def et_tree_attention_workspace_size(shape: AttnShape) -> int:

@@ -459,6 +459,7 @@ static bool attn_shape_ok(const et_attn_shape *s) {
   if (s->dtype != ET_BF16 && s->dtype != ET_F32) return false;
   if (s->max_prefix < 0 || s->kv_rows < 0 || s->kv_head_stride < 0 || s->num_splits < 0) return false;
   if (s->impl < 0 || s->impl > 2) return false;
+  if (s->flags & ~ET_ATTN_INPUTS_READY) return false;
   if (!(s->scale > 0.f)) return false;
   return true;
 }
@@ -562,6 +563,7 @@ extern "C" et_status et_tree_attention(const et_attn_shape *shape, const void *q
     TcLaunch t{};
     t.B = shape->B; t.N = shape->N; t.Hq = shape->Hq; t.Hkv = shape->Hkv; t.G = shape->Hq / shape->Hkv;
     t.MT = plan.MT; t.S = plan.S; t.W = (shape->N + 63) / 64;
+    t.inputs_ready = (shape->flags & ET_ATTN_INPUTS_READY) ? 1 : 0;
     t.scale_log2 = shape->scale * 1.4426950408889634f;
     t.q = q; t.kp = k_prefix; t.vp = v_prefix; t.kt = k_tree; t.vt = v_tree;
     t.kv_row0 = reinterpret_cast<const long long *>(kv_row0);

@@ -22,12 +22,14 @@
 // Two resident blocks per SM keep two independent pipelines in flight.  A
 // 128-row tile packs (token, query head) rows of one KV head, so a GQA group
 // shares every K/V tile.  The KV splits of one tile run as one thread-block
-// cluster: each split writes its partial rows to an L2-resident workspace,
-// one cluster barrier orders them, each split merges a slice of the rows and
-// drops the scratch lines from L2 (measured on GB300, moving the same bytes
-// through distributed shared memory took about four times as long).  Every
-// mbarrier wait is bounded: on expiry the block reports
-// ET_DEV_TIMEOUT, stops, frees its TMEM and exits.
+// cluster: each split writes its partial rows straight from TMEM to an
+// L2-resident workspace, one cluster barrier orders them, each split merges
+// a slice of the rows and drops the scratch lines from L2 (measured on
+// GB300: merging in the last split to finish instead was about twice as
+// slow, one SM reading every partial; moving the rows through distributed
+// shared memory took about four times as long).  Every mbarrier wait is
+// bounded: on expiry the block reports ET_DEV_TIMEOUT, stops, frees its TMEM
+// and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -51,18 +53,29 @@ constexpr uint32_t kOffK = kOffQ + kQBytes;
 constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
 constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
 constexpr uint32_t kOffMisc = kOffBar + 256;
-constexpr uint32_t kSmemBytes = kOffMisc + 256 + 1024;  // + slack for 1024-byte alignment
+// split merge through distributed shared memory (tiles of at most 64 real
+// rows): own (max, sum) pairs, then the pairs received from every split
+constexpr uint32_t kOffMlOwn = kOffMisc + 256;
+constexpr uint32_t kOffMlRecv = kOffMlOwn + kTcRows * 8;
+constexpr int kDsmMaxRows = 64;     // real rows of a tile merged through DSMEM
+constexpr int kDsmMaxSlots = 80;    // S * per for S >= 2, per = ceil(rows / S) rounded up to even (<= 72)
+constexpr uint32_t kMlRecvBytes = kDsmMaxSlots * 8;
+constexpr uint32_t kSmemBytes = kOffMlRecv + kMlRecvBytes + 1024;  // + slack for 1024-byte alignment
+// partial rows: own rows staged in the V stages, received rows in the Q and K space
+constexpr uint32_t kOffStage = kOffV;
+constexpr uint32_t kOffRecv = kOffQ;
+static_assert(kDsmMaxRows * 512 <= kStages * kTileBytes, "own partial rows fit the V stages");
+static_assert(kDsmMaxSlots * 512 <= kOffV, "received rows fit the Q and K space");
 // TMEM columns: S, O accumulator, P (bf16 pairs) double buffer
 constexpr uint32_t kColS = 0, kColO = 64, kColP0 = 192, kColP1 = 224, kTmemCols = 256;
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the row max grows by more than 2^8
 
 // barrier slots
 constexpr int B_KFULL = 0, B_KEMPTY = 2, B_VFULL = 4, B_VEMPTY = 6, B_SFULL = 8, B_SFREE = 9, B_PFULL = 10,
-              B_OFULL = 12, B_QFULL = 13;
+              B_OFULL = 12, B_QFULL = 13, B_DRAIN = 14, B_RECV = 15;
 constexpr int kQWarps = 5;       // warps 3-7 stage Q
 constexpr int kSoftmaxWarps = 4; // warps 4-7: one per TMEM lane quarter
 
-// distributed shared memory (thread block cluster)
 // drop a 128-byte line of merge scratch from L2 without writing it back
 __device__ __forceinline__ void discard_l2_line(const void *p) {
   asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
@@ -91,8 +104,8 @@ __device__ __forceinline__ void split_range_tc(int L, int N, int S, int s, int &
 
 
 // All lanes wait; the warp proceeds only if every lane saw the phase complete.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort, long long limit) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, limit));
 }
 
 __global__ void __launch_bounds__(kThreads, 2)
@@ -111,7 +124,18 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int s = blockIdx.x, g = blockIdx.y / a.MT, mt = blockIdx.y - g * a.MT, b = blockIdx.z;
   const int N = a.N;
 
+  // with inputs_ready the prefix length and start row are inputs: their loads
+  // go out first and overlap the set-up
+  int L_in = 0;
+  long long row0_in = 0;
+  if (a.inputs_ready) {
+    L_in = a.prefix_len[b];
+    row0_in = a.kv_row0 ? a.kv_row0[b] : 0;
+  }
   // ---- set-up that touches no global memory (it overlaps the previous kernel's tail) ----
+  if (warp == 3 && lane < 5) {  // the five tensor maps into the TMA descriptor cache
+    prefetch_tmap(lane == 0 ? &tm_kp : lane == 1 ? &tm_vp : lane == 2 ? &tm_kt : lane == 3 ? &tm_vt : &tm_q);
+  }
   if (t == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bar(B_KFULL + i), 1);
@@ -124,6 +148,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     mbar_init(bar(B_SFREE), kSoftmaxWarps);
     mbar_init(bar(B_OFULL), 1);
     mbar_init(bar(B_QFULL), a.q_tma ? 1 : kQWarps);
+    mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_RECV), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -144,11 +170,16 @@ __global__ void __launch_bounds__(kThreads, 2)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  pdl_wait();     // the previous kernel in the stream has completed (the inputs may come from it)
-  pdl_trigger();  // after the TMEM allocation: a waiting dependent block must not hold the TMEM this block needs
-  const int L = a.prefix_len[b];
+  if (!a.inputs_ready) {
+    pdl_wait();     // the previous kernel in the stream has completed (the inputs may come from it)
+    pdl_trigger();  // after the TMEM allocation: a waiting dependent block must not hold the TMEM this block needs
+  }
+  // with inputs_ready the previous kernel writes none of Q, K/V or the prefix
+  // lengths: the first tiles go out before the wait (only the mask, read by
+  // the softmax, and every output come after it)
+  const int L = a.inputs_ready ? L_in : a.prefix_len[b];
   const long long S_b = a.kv_head_stride > 0 ? a.kv_head_stride : L;
-  const long long row0 = a.kv_row0 ? a.kv_row0[b] : 0;
+  const long long row0 = a.inputs_ready ? row0_in : (a.kv_row0 ? a.kv_row0[b] : 0);
   int t0, t1, nP;
   split_range_tc(L, N, a.S, s, t0, t1, nP);
   const int T = t1 - t0;
@@ -173,13 +204,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
     }
-    if (a.q_tma) {  // rows (token, head in group) of KV head g: one 4-D box per 64 dims
+    if (a.q_tma && T > 0) {  // rows (token, head in group) of KV head g: one 4-D box per 64 dims
       const uint32_t qb = bar(B_QFULL);
       mbar_expect_tx(qb, kQBytes);
       const int tok0 = b * N + mt * (kTcRows / a.G);
       tma_4d(sb + kOffQ, &tm_q, 0, 0, g, tok0, qb);
       tma_4d(sb + kOffQ + kQHalfBytes, &tm_q, 64, 0, g, tok0, qb);
     }
+  }
+  if (a.inputs_ready) {
+    pdl_wait();
+    pdl_trigger();
   }
   if (t == 0 && L > 0 && row0 + (long long)g * S_b + L > a.kv_rows) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
 
@@ -194,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       int issued = T < kStages ? T : kStages;  // the first stages went out at the top
       for (int j = issued; j < T; ++j) {
         const int stage = j % kStages;
-        if (j >= kStages && !mbar_wait(bar(bE + stage), (uint32_t)((j / kStages) - 1) & 1u, abort_flag)) break;
+        if (j >= kStages && !mbar_wait(bar(bE + stage), (uint32_t)((j / kStages) - 1) & 1u, abort_flag, a.wait_cycles)) break;
         const uint32_t fb = bar(bF + stage);
         mbar_expect_tx(fb, kTileBytes);
         const uint32_t dst = base + stage * kTileBytes;
@@ -213,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       // do not leave while copies are in flight (the earlier stages were consumed)
       const int first = issued > kStages ? issued - kStages : 0;
       for (int j = first; j < issued; ++j) mbar_drain(bar(bF + j % kStages), (uint32_t)(j / kStages) & 1u);
+      if (isK && a.q_tma) mbar_drain(bar(B_QFULL), 0);  // the Q tile this thread sent at the top, too
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
@@ -229,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc_commit(bar(B_SFULL));
         if (j + kStages < T) tc_commit(bar(B_KEMPTY + stage));  // K tile consumed once S_j is done
       };
-      bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag) && mbar_wait(bar(B_KFULL + 0), 0, abort_flag);
+      bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, a.wait_cycles) && mbar_wait(bar(B_KFULL + 0), 0, abort_flag, a.wait_cycles);
       if (ok) {
         tc_fence_after();
         issue_s(0);
@@ -237,14 +273,14 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int j = 0; ok && j < T; ++j) {
         // S_{j+1} as soon as the softmax has read S_j out of TMEM
         if (j + 1 < T) {
-          if (!mbar_wait(bar(B_SFREE), (uint32_t)j & 1u, abort_flag)) break;
-          if (!mbar_wait(bar(B_KFULL + (j + 1) % kStages), (uint32_t)((j + 1) / kStages) & 1u, abort_flag)) break;
+          if (!mbar_wait(bar(B_SFREE), (uint32_t)j & 1u, abort_flag, a.wait_cycles)) break;
+          if (!mbar_wait(bar(B_KFULL + (j + 1) % kStages), (uint32_t)((j + 1) / kStages) & 1u, abort_flag, a.wait_cycles)) break;
           tc_fence_after();
           issue_s(j + 1);
         }
         const int stage = j % kStages;
-        if (!mbar_wait(bar(B_PFULL + (j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag)) break;
-        if (!mbar_wait(bar(B_VFULL + stage), (uint32_t)(j / kStages) & 1u, abort_flag)) break;
+        if (!mbar_wait(bar(B_PFULL + (j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag, a.wait_cycles)) break;
+        if (!mbar_wait(bar(B_VFULL + stage), (uint32_t)(j / kStages) & 1u, abort_flag, a.wait_cycles)) break;
         tc_fence_after();
         const uint32_t pcol = tmem + ((j & 1) ? kColP1 : kColP0);
         const uint32_t vbase = sb + kOffV + stage * kTileBytes;
@@ -256,6 +292,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc_commit(bar(B_OFULL));
         if (j + kStages < T) tc_commit(bar(B_VEMPTY + stage));
       }
+      // every MMA this thread issued has finished before TMEM can be freed
+      // (after an expired wait the softmax may not have waited for them)
+      tc_commit(bar(B_DRAIN));
+      mbar_drain(bar(B_DRAIN), 0);
     }
   }
   if (warp >= 3 && !a.q_tma) {
@@ -295,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint32_t raw[64];
     for (int j = 0; j < T; ++j) {
       const int tile = t0 + j;
-      if (!warp_wait(bar(B_SFULL), (uint32_t)j & 1u, abort_flag)) { ok_rows = false; break; }
+      if (!warp_wait(bar(B_SFULL), (uint32_t)j & 1u, abort_flag, a.wait_cycles)) { ok_rows = false; break; }
       tc_fence_after();
       if (active) {
         tmem_ld64(lane_base + kColS, raw);
@@ -327,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // O in TMEM holds sum_{<j} P V relative to m_used: rescale it when the
         // max grew by more than 2^8 (warp-collective TMEM access)
         if (__any_sync(0xffffffffu, grow && j > 0 && m_used > -INFINITY)) {
-          if (!warp_wait(bar(B_OFULL), (uint32_t)(j - 1) & 1u, abort_flag)) { ok_rows = false; break; }
+          if (!warp_wait(bar(B_OFULL), (uint32_t)(j - 1) & 1u, abort_flag, a.wait_cycles)) { ok_rows = false; break; }
           tc_fence_after();
           const float sc = (grow && m_used > -INFINITY) ? ex2(m_used - m_new) : 1.f;
           uint32_t ov[32];
@@ -365,14 +405,17 @@ __global__ void __launch_bounds__(kThreads, 2)
       // whatever the cache holds there cannot reach P.V (0 * NaN)
       if (tile == nP - 1 && (L & (kTcKeys - 1))) {
         const int stage = j % kStages;
-        if (!warp_wait(bar(B_VFULL + stage), (uint32_t)(j / kStages) & 1u, abort_flag)) ok_rows = false;
-        const int first = L & (kTcKeys - 1);
-        unsigned char *vs = sm + kOffV + stage * kTileBytes;
-        for (int x = r; x < (kTcKeys - first) * 16; x += 32 * kSoftmaxWarps) {
-          const int row = first + (x >> 4), c = x & 15;
-          *reinterpret_cast<uint4 *>(vs + (c >> 3) * kHalfBytes + row * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+        if (warp_wait(bar(B_VFULL + stage), (uint32_t)(j / kStages) & 1u, abort_flag, a.wait_cycles)) {
+          const int first = L & (kTcKeys - 1);
+          unsigned char *vs = sm + kOffV + stage * kTileBytes;
+          for (int x = r; x < (kTcKeys - first) * 16; x += 32 * kSoftmaxWarps) {
+            const int row = first + (x >> 4), c = x & 15;
+            *reinterpret_cast<uint4 *>(vs + (c >> 3) * kHalfBytes + row * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_async_smem();
+        } else {
+          ok_rows = false;  // the copy may still be landing: leave the stage alone
         }
-        fence_async_smem();
       }
       tc_fence_before();
       __syncwarp();
@@ -380,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (!__all_sync(0xffffffffu, ok_rows)) { ok_rows = false; break; }
     }
     // the last P.V must have landed before O is read
-    if (ok_rows && T > 0 && !warp_wait(bar(B_OFULL), (uint32_t)(T - 1) & 1u, abort_flag)) ok_rows = false;
+    if (ok_rows && T > 0 && !warp_wait(bar(B_OFULL), (uint32_t)(T - 1) & 1u, abort_flag, a.wait_cycles)) ok_rows = false;
   }
   __syncthreads();
   tc_fence_after();
@@ -390,16 +433,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (smx && !aborted && __any_sync(0xffffffffu, my_tok >= 0) && T > 0) {
       const uint32_t lane_base = tmem + ((uint32_t)(r & ~31) << 16);
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint32_t ov[32];
+      uint32_t ov[64];
 #pragma unroll 1
-      for (int h = 0; h < 4; ++h) {
-        tmem_ld32(lane_base + kColO + 32 * h, ov);
+      for (int h = 0; h < 2; ++h) {  // 64 columns per TMEM load, one wait each
+        tmem_ld64(lane_base + kColO + 64 * h, ov);
         tmem_wait_ld();
         if (my_tok >= 0) {
           __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) +
-                                (((long long)b * N + my_tok) * a.Hq + row_head[r]) * kTcDim + 32 * h;
+                                (((long long)b * N + my_tok) * a.Hq + row_head[r]) * kTcDim + 64 * h;
 #pragma unroll
-          for (int c = 0; c < 32; c += 8) {
+          for (int c = 0; c < 64; c += 8) {
             uint4 v;
             v.x = pack_bf16x2(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
             v.y = pack_bf16x2(__uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv);
@@ -424,53 +467,146 @@ __global__ void __launch_bounds__(kThreads, 2)
     return;
   }
 
-  // ---------------- S splits: partial rows through L2, merged by their owners ----------------
-  // Each split stages its unnormalised fp32 rows in shared memory (the K and
-  // V stages, free now), copies the real rows to the workspace as coalesced
-  // 512-byte row writes and posts (max, sum) per row.  After one cluster
-  // barrier, split s merges rows [s * per, (s + 1) * per) of the tile from
-  // all S partials, then drops those scratch lines from L2 so that they are
-  // never written back to DRAM.
+  // ---------------- S splits of a tile with at most 64 real rows: merged through DSMEM ----------------
+  // Each split stages its unnormalised fp32 rows in its V stages (16-byte
+  // chunk c of row r at c ^ (r & 31): conflict-free from one thread per row)
+  // and its (max, sum) pairs.  After one cluster barrier (every split is done
+  // with its Q, K and V space), split s bulk-copies the rows each owner o
+  // merges, [o * per, (o + 1) * per), into o's Q/K space (slot s), completing
+  // on o's mbarrier; each owner merges its slice from shared memory.  A second
+  // cluster barrier keeps every block resident until the copies out of it
+  // have landed.
   const int S = a.S;
   const int nvalid = min(kTcRows, N * a.G - mt * kTcRows);  // the real rows are a prefix of the tile
+  const bool have = !aborted && T > 0;
+  if (nvalid <= kDsmMaxRows) {
+    const int per = (((nvalid + S - 1) / S) + 1) & ~1;  // even: the pairs' copies stay 16-byte multiples
+    if (smx) {
+      if (have && __any_sync(0xffffffffu, my_tok >= 0)) {
+        const uint32_t lane_base = tmem + ((uint32_t)(r & ~31) << 16);
+        uint32_t ov[64];
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          tmem_ld64(lane_base + kColO + 64 * h, ov);
+          tmem_wait_ld();
+          if (r < nvalid) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const uint32_t dst = sb + kOffStage + (uint32_t)r * 512u + (uint32_t)(((16 * h + c) ^ (r & 31)) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(ov[4 * c]),
+                           "r"(ov[4 * c + 1]), "r"(ov[4 * c + 2]), "r"(ov[4 * c + 3])
+                           : "memory");
+            }
+          }
+        }
+      }
+      reinterpret_cast<float2 *>(sm + kOffMlOwn)[r] =
+          make_float2(have && r < nvalid ? m_used : -INFINITY, have && r < nvalid ? l : 0.f);
+      fence_async_smem();  // the staged rows are read by the bulk copies (async proxy)
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+      __syncwarp();
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+    cluster_sync_all();  // every split has staged its rows and is done with its Q, K and V space
+    const int r0 = s * per, cnt = max(0, min(nvalid, r0 + per) - r0);
+    if (t == 0) {
+      // what arrives here: from every split, its rows of this slice and `per` pairs
+      mbar_expect_tx(bar(B_RECV), (uint32_t)S * ((uint32_t)cnt * 512u + (uint32_t)per * 8u));
+      for (int o = 0; o < S; ++o) {
+        const int o0 = o * per, ocnt = max(0, min(nvalid, o0 + per) - o0);
+        const uint32_t rbar = cl_map(sm + kOffBar + 8 * B_RECV, (uint32_t)o);
+        if (ocnt > 0)
+          bulk_to_peer(cl_map(sm + kOffRecv + (size_t)s * per * 512, (uint32_t)o), sb + kOffStage + (uint32_t)o0 * 512u,
+                       (uint32_t)ocnt * 512u, rbar);
+        bulk_to_peer(cl_map(sm + kOffMlRecv + (size_t)s * per * 8, (uint32_t)o), sb + kOffMlOwn + (uint32_t)o0 * 8u,
+                     (uint32_t)per * 8u, rbar);
+      }
+    }
+    bool got = false;
+    if (!aborted) got = __all_sync(0xffffffffu, mbar_wait(bar(B_RECV), 0, abort_flag, a.wait_cycles));
+    if (!got) mbar_drain(bar(B_RECV), 0);  // the copies into this block land before it may leave
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");  // the copies into this block have landed
+    if (got && !aborted && cnt > 0) {
+      __nv_bfloat16 *O = static_cast<__nv_bfloat16 *>(a.out);
+      const float2 *mlr = reinterpret_cast<const float2 *>(sm + kOffMlRecv);
+      for (int x = t; x < cnt * 32; x += kThreads) {
+        const int lr = x >> 5, chunk = x & 31, rr = r0 + lr;
+        float M = -INFINITY;
+        for (int sp = 0; sp < S; ++sp) M = fmaxf(M, mlr[sp * per + lr].x);
+        float Ls = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sp = 0; sp < S; ++sp) {
+          const float2 ml = mlr[sp * per + lr];
+          if (ml.x > -INFINITY) {  // a split without keys for this row staged no row
+            const float w = exp2f(ml.x - M);
+            Ls = fmaf(ml.y, w, Ls);
+            const float4 p = *reinterpret_cast<const float4 *>(sm + kOffRecv + ((size_t)sp * per + lr) * 512 +
+                                                               ((chunk ^ (rr & 31)) << 4));
+            acc.x = fmaf(w, p.x, acc.x);
+            acc.y = fmaf(w, p.y, acc.y);
+            acc.z = fmaf(w, p.z, acc.z);
+            acc.w = fmaf(w, p.w, acc.w);
+          }
+        }
+        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+        uint2 v;
+        v.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+        v.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2 *>(O + (((long long)b * N + row_tok[rr]) * a.Hq + row_head[rr]) * kTcDim + 4 * chunk) =
+            v;
+        if (chunk == 0 && a.lse)
+          a.lse[((long long)b * a.Hq + row_head[rr]) * N + row_tok[rr]] =
+              Ls > 0.f ? (M + log2f(Ls)) * 0.69314718055994531f : -INFINITY;
+      }
+    }
+    if (!got || aborted) {
+      if (t == 0) flag_status(a.dev_status, ET_DEV_TIMEOUT);
+    }
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");  // no block leaves with copies out of it pending
+    return;
+  }
+
+  // ---------------- S splits, larger tiles: partial rows through L2, merged by their owners ----------------
+  // Each split writes the unnormalised fp32 rows of its real tokens straight
+  // from TMEM to the workspace (one 512-byte row per softmax thread) and
+  // posts (max, sum) per row.  The S splits of a tile form one cluster: after
+  // one cluster barrier, split s merges rows [s * per, (s + 1) * per) of the
+  // tile from all S partials (the pairs and the rows are loaded in one round),
+  // then drops those scratch lines from L2 so that they are never written
+  // back to DRAM.
   const long long tile_id = (long long)blockIdx.z * gridDim.y + blockIdx.y;
   const long long n_tiles = (long long)gridDim.y * gridDim.z;
   float *ws_o = a.ws;                                                                  // [tiles][S][128][128]
   float2 *ws_ml = reinterpret_cast<float2 *>(a.ws + n_tiles * S * kTcRows * kTcDim);  // [tiles][S][128]
-  const bool have = !aborted && T > 0;
   if (smx) {
     if (have && __any_sync(0xffffffffu, my_tok >= 0)) {
       const uint32_t lane_base = tmem + ((uint32_t)(r & ~31) << 16);
-      uint32_t ov[32];
+      float4 *dst = reinterpret_cast<float4 *>(ws_o + ((tile_id * S + s) * kTcRows + r) * kTcDim);
+      uint32_t ov[64];
 #pragma unroll 1
-      for (int h = 0; h < 4; ++h) {
-        tmem_ld32(lane_base + kColO + 32 * h, ov);
+      for (int h = 0; h < 2; ++h) {  // 64 columns per TMEM load, one wait each
+        tmem_ld64(lane_base + kColO + 64 * h, ov);
         tmem_wait_ld();
+        if (my_tok >= 0) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {  // 16-byte chunk j of row r sits at j ^ (r & 31): no bank conflicts
-          const uint32_t dst = sb + kOffK + (uint32_t)r * 512u + (uint32_t)(((8 * h + c) ^ (r & 31)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(ov[4 * c]), "r"(ov[4 * c + 1]),
-                       "r"(ov[4 * c + 2]), "r"(ov[4 * c + 3])
-                       : "memory");
+          for (int c = 0; c < 16; ++c)
+            dst[16 * h + c] = make_float4(__uint_as_float(ov[4 * c]), __uint_as_float(ov[4 * c + 1]),
+                                          __uint_as_float(ov[4 * c + 2]), __uint_as_float(ov[4 * c + 3]));
         }
       }
     }
-    ws_ml[(tile_id * S + s) * kTcRows + r] = make_float2(have ? m_used : -INFINITY, have ? l : 0.f);
+    if (r < nvalid) ws_ml[(tile_id * S + s) * kTcRows + r] = make_float2(have ? m_used : -INFINITY, have ? l : 0.f);
   }
-  static_assert(2 * kStages * kTileBytes >= kTcRows * kTcDim * 4, "staging buffer");
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
-  }
-  if (have) {
-    float4 *dst = reinterpret_cast<float4 *>(ws_o + (tile_id * S + s) * (kTcRows * kTcDim));
-    for (int x = t; x < nvalid * 32; x += kThreads) {
-      const int rr = x >> 5, chunk = x & 31;
-      dst[x] = *reinterpret_cast<const float4 *>(sm + kOffK + rr * 512 + ((chunk ^ (rr & 31)) << 4));
-    }
   }
   cluster_sync_all();  // release / acquire at cluster scope: every split's rows are in L2
   if (aborted) {
@@ -480,55 +616,42 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int per = (nvalid + S - 1) / S;  // the real rows, spread over every split
   const int r0 = s * per, r1 = min(nvalid, r0 + per);
   if (r1 <= r0) return;
-  float *wts = reinterpret_cast<float *>(sm + kOffQ);  // [per][kTcMaxSplits] weight / total
-  if (t < r1 - r0) {
-    float2 ml[kTcMaxSplits];
-#pragma unroll
-    for (int x = 0; x < kTcMaxSplits; ++x)
-      ml[x] = x < S ? __ldcg(ws_ml + (tile_id * S + x) * kTcRows + r0 + t) : make_float2(-INFINITY, 0.f);
-    float M = -INFINITY;
-#pragma unroll
-    for (int x = 0; x < kTcMaxSplits; ++x) M = fmaxf(M, ml[x].x);
-    float Ls = 0.f, w[kTcMaxSplits];
-#pragma unroll
-    for (int x = 0; x < kTcMaxSplits; ++x) {
-      w[x] = ml[x].x > -INFINITY ? exp2f(ml[x].x - M) : 0.f;
-      Ls += ml[x].y * w[x];
-    }
-    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-#pragma unroll
-    for (int x = 0; x < kTcMaxSplits; ++x) wts[t * kTcMaxSplits + x] = w[x] * inv;
-    const int i = row_tok[r0 + t];
-    if (i >= 0 && a.lse)
-      a.lse[((long long)b * a.Hq + row_head[r0 + t]) * N + i] =
-          Ls > 0.f ? (M + log2f(Ls)) * 0.69314718055994531f : -INFINITY;
-  }
-  __syncthreads();
   __nv_bfloat16 *O = static_cast<__nv_bfloat16 *>(a.out);
   const float4 *src = reinterpret_cast<const float4 *>(ws_o + tile_id * S * (kTcRows * kTcDim));
+  const float2 *mlt = ws_ml + tile_id * S * kTcRows;
   for (int x = t; x < (r1 - r0) * 32; x += kThreads) {
-    const int lr = x >> 5, chunk = x & 31, rr = r0 + lr;
+    const int rr = r0 + (x >> 5), chunk = x & 31;
+    float2 ml[kTcMaxSplits];
     float4 p[kTcMaxSplits];
 #pragma unroll
-    for (int sp = 0; sp < kTcMaxSplits; ++sp) {  // every load in flight before the sums
-      p[sp] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (sp < S && wts[lr * kTcMaxSplits + sp] != 0.f) p[sp] = __ldcg(src + (sp * kTcRows + rr) * 32 + chunk);
+    for (int sp = 0; sp < kTcMaxSplits; ++sp) {  // every load in flight before any arithmetic
+      ml[sp] = sp < S ? __ldcg(mlt + sp * kTcRows + rr) : make_float2(-INFINITY, 0.f);
+      p[sp] = sp < S ? __ldcg(src + (sp * kTcRows + rr) * 32 + chunk) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    float M = -INFINITY;
+#pragma unroll
+    for (int sp = 0; sp < kTcMaxSplits; ++sp) M = fmaxf(M, ml[sp].x);
+    float Ls = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int sp = 0; sp < kTcMaxSplits; ++sp) {
-      const float w = sp < S ? wts[lr * kTcMaxSplits + sp] : 0.f;
-      if (w != 0.f) {  // a split without keys for this row wrote no partial row
+      if (ml[sp].x > -INFINITY) {  // a split without keys for this row wrote no partial row
+        const float w = exp2f(ml[sp].x - M);
+        Ls = fmaf(ml[sp].y, w, Ls);
         acc.x = fmaf(w, p[sp].x, acc.x);
         acc.y = fmaf(w, p[sp].y, acc.y);
         acc.z = fmaf(w, p[sp].z, acc.z);
         acc.w = fmaf(w, p[sp].w, acc.w);
       }
     }
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
     uint2 v;
-    v.x = pack_bf16x2(acc.x, acc.y);
-    v.y = pack_bf16x2(acc.z, acc.w);
+    v.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    v.y = pack_bf16x2(acc.z * inv, acc.w * inv);
     *reinterpret_cast<uint2 *>(O + (((long long)b * N + row_tok[rr]) * a.Hq + row_head[rr]) * kTcDim + 4 * chunk) = v;
+    if (chunk == 0 && a.lse)
+      a.lse[((long long)b * a.Hq + row_head[rr]) * N + row_tok[rr]] =
+          Ls > 0.f ? (M + log2f(Ls)) * 0.69314718055994531f : -INFINITY;
   }
   __syncthreads();  // every read of this block's rows has returned
   for (int x = t; x < (r1 - r0) * S * 4; x += kThreads) {
@@ -593,6 +716,7 @@ et_status tc_attention_launch(const TcLaunch &a, cudaStream_t stream) {
   }
   TcLaunch la = a;
   la.q_tma = (a.G <= kTcRows && kTcRows % a.G == 0) ? 1 : 0;
+  la.wait_cycles = et_wait_limit_cycles();
   if (la.q_tma) ok = ok && make_map_q(&m_q, a.q, a.G, a.Hkv, tree_rows);
   else m_q = m_kt;  // not read
   if (!ok) return ET_ERR_INVALID_ARG;

@@ -12,7 +12,7 @@
 namespace et {
 
 struct TcLaunch {
-  int B, N, Hq, Hkv, G, MT, S, W;  // MT row tiles of 128 per KV head, S splits (= cluster size)
+  int B, N, Hq, Hkv, G, MT, S, W;  // MT row tiles of 128 per KV head, S KV splits
   float scale_log2;
   const void *q, *kp, *vp, *kt, *vt;
   const long long *kv_row0;
@@ -24,6 +24,8 @@ struct TcLaunch {
   int *dev_status;
   float *ws;   // S > 1: partial rows [B*Hkv*MT][S][128][128], then (max, sum) [B*Hkv*MT][S][128]
   int q_tma;   // set by the launcher: the Q tile comes by TMA (G divides 128)
+  long long wait_cycles;  // bound of every mbarrier wait (et_set_wait_limit)
+  int inputs_ready;       // ET_ATTN_INPUTS_READY: the first tiles may be fetched before the programmatic wait
 };
 
 constexpr int kTcRows = 128;   // query rows per tile (TMEM lanes)

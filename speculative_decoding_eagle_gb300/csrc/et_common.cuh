@@ -396,6 +396,10 @@ static inline et_status et_launch_status() {
 }
 static inline bool et_aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
+// The bound, in SM clock cycles, of the device waits of the kernels launched
+// from now on (et_set_wait_limit; defined in et_tree.cu).
+__attribute__((visibility("hidden"))) long long et_wait_limit_cycles();
+
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device): the
 // attribute lives in the current device's context, so every device that runs
 // the kernel needs its own call.  Thread-safe.

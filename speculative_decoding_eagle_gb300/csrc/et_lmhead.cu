@@ -37,6 +37,7 @@ struct LmArgs {
   long long ldo;
   float *out;
   int32_t *dev_status;
+  long long wait_cycles;  // bound of every mbarrier wait (et_set_wait_limit)
 };
 
 __global__ void __launch_bounds__(kLmThreads)
@@ -54,6 +55,7 @@ __global__ void __launch_bounds__(kLmThreads)
   auto full = [&](int s) -> uint32_t { return sb + offBar + 8u * (uint32_t)s; };
   auto empty = [&](int s) -> uint32_t { return sb + offBar + 8u * (uint32_t)(S + s); };
   const uint32_t done = sb + offBar + 8u * (uint32_t)(2 * S);
+  const uint32_t drain = sb + offBar + 8u * (uint32_t)(2 * S + 1) + 24u;  // every issued MMA has finished
   const uint32_t tcols = a.Mp <= 32 ? 32u : 64u;
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -65,6 +67,7 @@ __global__ void __launch_bounds__(kLmThreads)
       mbar_init(empty(s), 1);
     }
     mbar_init(done, 1);
+    mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -85,7 +88,7 @@ __global__ void __launch_bounds__(kLmThreads)
     int issued = 0;
     for (int kb = 0; kb < nk; ++kb) {
       const int s = kb % S;
-      if (kb >= S && !mbar_wait(empty(s), (uint32_t)((kb / S) - 1) & 1u, abort_flag)) break;
+      if (kb >= S && !mbar_wait(empty(s), (uint32_t)((kb / S) - 1) & 1u, abort_flag, a.wait_cycles)) break;
       mbar_expect_tx(full(s), kLmABytes + bBytes);
       tma_2d(sb + (uint32_t)s * kLmABytes, &tm_w, kb * kLmK, v0, full(s));
       tma_2d(sb + offB + (uint32_t)s * bBytes, &tm_x, kb * kLmK, 0, full(s));
@@ -99,7 +102,7 @@ __global__ void __launch_bounds__(kLmThreads)
     bool ok = true;
     for (int kb = 0; kb < nk; ++kb) {
       const int s = kb % S;
-      if (!mbar_wait(full(s), (uint32_t)(kb / S) & 1u, abort_flag)) { ok = false; break; }
+      if (!mbar_wait(full(s), (uint32_t)(kb / S) & 1u, abort_flag, a.wait_cycles)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < kLmK / 16; ++kk) {
@@ -110,10 +113,14 @@ __global__ void __launch_bounds__(kLmThreads)
       tc_commit(empty(s));  // the slice is consumed once its MMAs are done
     }
     if (ok) tc_commit(done);
+    // TMEM is freed only after every MMA this thread issued has finished
+    // (after an expired wait the epilogue does not wait for them)
+    tc_commit(drain);
+    mbar_drain(drain, 0);
   }
   __syncwarp();
   // ---------------- epilogue: TMEM lane quarter -> logits rows ----------------
-  const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag));
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag, a.wait_cycles));
   tc_fence_after();
   if (ok) {
     const int v = v0 + 32 * warp + lane;
@@ -172,6 +179,7 @@ extern "C" et_status et_lm_head(const et_lmhead_shape *s, const void *features, 
   a.M = s->M; a.Mp = Mp; a.H = s->H; a.V = s->V; a.stages = stages; a.ldo = s->ldo;
   a.out = logits;
   a.dev_status = dev_status;
+  a.wait_cycles = et_wait_limit_cycles();
   return et_launch(k_lmhead_tc, dim3((s->V + kLmRows - 1) / kLmRows), dim3(kLmThreads), smem, (cudaStream_t)stream,
                    0, m_w, m_x, a);
 }

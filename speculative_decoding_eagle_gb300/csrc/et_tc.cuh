@@ -37,27 +37,44 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait for the phase with this parity; false if it expired or another
-// role already gave up.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+// Bounded wait for the phase with this parity (at most `limit` cycles); false
+// if it expired or another role already gave up.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort, long long limit) {
   if (mbar_try(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kTcWaitCycles) {
+    if (clock64() - t0 > limit) {
       *abort = 1;
       return false;
     }
   }
 }
 
-// Bounded wait that ignores the abort flag: used only to let copies already
-// in flight land before the block leaves.
+// Bounded wait that ignores the abort flag, always with the full bound: used
+// only to let copies and MMAs already in flight finish before the block
+// leaves (or frees its TMEM).
 __device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
   while (!mbar_try(bar, parity) && clock64() - t0 < kTcWaitCycles) {
   }
+}
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
+// this CTA's shared memory to a CTA of the cluster (destination and mbarrier
+// given as shared::cluster addresses); the bytes complete on that mbarrier.
+__device__ __forceinline__ void bulk_to_peer(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                             uint32_t bar_cluster) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst_cluster), "r"(src_cta), "r"(bytes), "r"(bar_cluster)
+               : "memory");
+}
+
+// Fetch a tensor map (a kernel parameter) into the TMA unit's descriptor
+// cache ahead of its first copy.
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"((unsigned long long)map) : "memory");
 }
 
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar) {

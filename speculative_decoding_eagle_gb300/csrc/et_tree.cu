@@ -252,9 +252,8 @@ __global__ void __launch_bounds__(kExpThreads) k_expand(ExpandArgs a) {
 // rerank + flatten
 // ---------------------------------------------------------------------------
 constexpr int kRrThreads = 1024;
-constexpr int kRrPer = kMaxC / kRrThreads;  // 4 candidates per thread
 constexpr int kRrBinBits = 11;
-constexpr int kRrBins = 1 << kRrBinBits;    // two per thread
+constexpr int kRrBins = 1 << kRrBinBits;    // two per thread at 1024 threads
 constexpr int kRrBinCap = 64;               // keys of one bin ranked by counting
 
 struct RerankArgs {
@@ -266,6 +265,19 @@ struct RerankArgs {
   const int32_t *prefix_len;
   uint64_t *mask;
   int32_t *posids;
+};
+
+// Shared memory of one sequence's rerank (and of the fused mask).
+struct RerankSmem {
+  unsigned int hist[kRrBins];
+  unsigned long long red_lo[32], red_hi[32], bin_keys[kRrBinCap];
+  unsigned long long s_lo, s_hi, s_thr;
+  int s_bin;
+  unsigned int s_before, s_nb, s_cnt;
+  short flat_of[kMaxC];
+  unsigned char kept[kMaxC];
+  int tmp[32];
+  int row_par[kMaxN], row_dep[kMaxN];  // fused mask: parent row and depth of each flat row
 };
 
 // Ancestor bitmask of flat row i from its parent rows (parents precede
@@ -284,7 +296,11 @@ __device__ __forceinline__ bool ancestor_bits(const int *par, int i, uint64_t &w
   return true;
 }
 
-__device__ __forceinline__ int block_excl_scan_1024(int v, int *tmp, int &total) {
+// Exclusive prefix sum over the NT threads of a block (NT a multiple of 32,
+// at most 1024); `total` gets the block's sum.
+template <int NT>
+__device__ __forceinline__ int block_excl_scan(int v, int *tmp, int &total) {
+  constexpr int NW = NT / 32;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   int x = v;
 #pragma unroll
@@ -295,7 +311,7 @@ __device__ __forceinline__ int block_excl_scan_1024(int v, int *tmp, int &total)
   if (lane == 31) tmp[w] = x;
   __syncthreads();
   if (w == 0) {
-    int s = tmp[lane];
+    int s = lane < NW ? tmp[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       int y = __shfl_up_sync(0xffffffffu, s, o);
@@ -304,51 +320,27 @@ __device__ __forceinline__ int block_excl_scan_1024(int v, int *tmp, int &total)
     tmp[lane] = s;  // inclusive prefix of warp totals
   }
   __syncthreads();
-  total = tmp[31];
+  total = tmp[NW - 1];
   const int before = w > 0 ? tmp[w - 1] : 0;
+  __syncthreads();  // tmp may be reused by the next call
   return before + x - v;
 }
 
-__global__ void __launch_bounds__(kRrThreads) k_rerank(RerankArgs a) {
-  pdl_wait();     // the previous kernel in the stream has completed
-  pdl_trigger();  // only now may the next kernel launch: at most one waits ahead
-  __shared__ unsigned int hist[kRrBins];
-  __shared__ unsigned long long red_lo[32], red_hi[32], bin_keys[kRrBinCap];
-  __shared__ unsigned long long s_lo, s_hi, s_thr;
-  __shared__ int s_bin;
-  __shared__ unsigned int s_before, s_nb, s_cnt;
-  __shared__ short flat_of[kMaxC];
-  __shared__ unsigned char kept[kMaxC];
-  __shared__ int tmp[32];
-  __shared__ int row_par[kMaxN], row_dep[kMaxN];  // fused mask: parent row and depth of each flat row
+// The n-th smallest of the C rank keys by histogram (keys are unique): a
+// 2048-bin histogram over [min, max] puts it in one bin; that
+// bin's keys are ranked by counting when few, else the bin's range is
+// histogrammed again (each pass narrows the range by 2^11, so six passes
+// reach single keys).  Marks the kept candidates in sm.kept.
+template <int NT>
+__device__ void rerank_select_hist(const RerankArgs &a, const unsigned long long (&rk)[kMaxC / NT], RerankSmem &sm) {
+  constexpr int kPer = kMaxC / NT;
+  constexpr int kHB = kRrBins / NT;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int b = blockIdx.x;
   const int C = a.C;
-
-  unsigned long long rk[kRrPer];
-#pragma unroll
-  for (int q = 0; q < kRrPer; ++q) {
-    const int id = t + q * kRrThreads;
-    rk[q] = id < C ? rank_key(a.tree.cand_key[(long long)b * C + id], id) : ~0ull;
-  }
-  if (t < kMaxN) { row_par[t] = 0; row_dep[t] = 0; }  // rows a broken tree leaves unwritten
-  // the token and parent of this thread's flatten ids, fetched now (they are
-  // needed only after the selection)
-  int pre_tok[kRrPer], pre_par[kRrPer];
-#pragma unroll
-  for (int j = 0; j < kRrPer; ++j) {
-    const int id = kRrPer * t + j;
-    pre_tok[j] = id < C ? a.tree.cand_tok[(long long)b * C + id] : -1;
-    pre_par[j] = id < C ? a.tree.cand_parent[(long long)b * C + id] : -1;
-  }
-  // The n-th smallest rank key (keys are unique): a 2048-bin histogram over
-  // [min, max] puts it in one bin; that bin's keys are ranked by counting
-  // when few, else the bin's range is histogrammed again (each pass narrows
-  // the range by 2^11, so six passes reach single keys).
   unsigned long long mn = ~0ull, mx = 0ull;
 #pragma unroll
-  for (int q = 0; q < kRrPer; ++q) {
-    if (t + q * kRrThreads < C) {
+  for (int q = 0; q < kPer; ++q) {
+    if (t + q * NT < C) {
       mn = rk[q] < mn ? rk[q] : mn;
       mx = rk[q] > mx ? rk[q] : mx;
     }
@@ -359,99 +351,117 @@ __global__ void __launch_bounds__(kRrThreads) k_rerank(RerankArgs a) {
     const unsigned long long y = __shfl_xor_sync(0xffffffffu, mx, o);
     mx = y > mx ? y : mx;
   }
-  if (lane == 0) { red_lo[warp] = mn; red_hi[warp] = mx; }
-  for (int i = t; i < kRrBins; i += kRrThreads) hist[i] = 0u;
-  if (t == 0) s_cnt = 0u;
+  if (lane == 0) { sm.red_lo[warp] = mn; sm.red_hi[warp] = mx; }
+  for (int i = t; i < kRrBins; i += NT) sm.hist[i] = 0u;
+  if (t == 0) sm.s_cnt = 0u;
   __syncthreads();
   if (warp == 0) {
-    mn = warp_min_u64(red_lo[lane]);
-    mx = red_hi[lane];
+    mn = lane < NT / 32 ? sm.red_lo[lane] : ~0ull;
+    mx = lane < NT / 32 ? sm.red_hi[lane] : 0ull;
+    mn = warp_min_u64(mn);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const unsigned long long y = __shfl_xor_sync(0xffffffffu, mx, o);
       mx = y > mx ? y : mx;
     }
-    if (lane == 0) { s_lo = mn; s_hi = mx; s_thr = ~0ull; }
+    if (lane == 0) { sm.s_lo = mn; sm.s_hi = mx; sm.s_thr = ~0ull; }
   }
   __syncthreads();
-  unsigned long long lo = s_lo, hi = s_hi;
+  unsigned long long lo = sm.s_lo, hi = sm.s_hi;
   unsigned int remaining = (unsigned)a.n;  // 1-based rank of the wanted key among keys in [lo, hi]
   for (int pass = 0; pass < 7; ++pass) {
     const unsigned long long range = hi - lo;
     const int bits = range ? 64 - __clzll((long long)range) : 0;
     const int shift = bits > kRrBinBits ? bits - kRrBinBits : 0;
 #pragma unroll
-    for (int q = 0; q < kRrPer; ++q)
-      if (t + q * kRrThreads < C && rk[q] >= lo && rk[q] <= hi) atomicAdd(&hist[(rk[q] - lo) >> shift], 1u);
+    for (int q = 0; q < kPer; ++q)
+      if (t + q * NT < C && rk[q] >= lo && rk[q] <= hi) atomicAdd(&sm.hist[(rk[q] - lo) >> shift], 1u);
     __syncthreads();
-    const unsigned int h0 = hist[2 * t], h1 = hist[2 * t + 1];  // kRrBins = 2 * kRrThreads
+    unsigned int h[kHB], hs = 0;  // this thread's kHB consecutive bins
+#pragma unroll
+    for (int e = 0; e < kHB; ++e) { h[e] = sm.hist[kHB * t + e]; hs += h[e]; }
     int total;
-    const unsigned int excl = (unsigned)block_excl_scan_1024((int)(h0 + h1), tmp, total);
-    if (excl < remaining && remaining <= excl + h0 + h1) {
-      const bool first = excl + h0 >= remaining;
-      s_bin = first ? 2 * t : 2 * t + 1;
-      s_before = first ? excl : excl + h0;
-      s_nb = first ? h0 : h1;
+    const unsigned int excl = (unsigned)block_excl_scan<NT>((int)hs, sm.tmp, total);
+    if (excl < remaining && remaining <= excl + hs) {
+      unsigned int before = excl;
+#pragma unroll
+      for (int e = 0; e < kHB; ++e) {
+        if (before < remaining && remaining <= before + h[e]) {
+          sm.s_bin = kHB * t + e;
+          sm.s_before = before;
+          sm.s_nb = h[e];
+        }
+        before += h[e];
+      }
     }
     __syncthreads();
-    const int B = s_bin;
-    const unsigned int nb = s_nb;
-    remaining -= s_before;
+    const int B = sm.s_bin;
+    const unsigned int nb = sm.s_nb;
+    remaining -= sm.s_before;
     const unsigned long long blo = lo + ((unsigned long long)B << shift);
     const unsigned long long bhi = shift ? (hi - blo < (1ull << shift) - 1 ? hi : blo + ((1ull << shift) - 1)) : blo;
     if (nb <= (unsigned)kRrBinCap) {  // always so for shift == 0 (one key per value)
 #pragma unroll
-      for (int q = 0; q < kRrPer; ++q)
-        if (t + q * kRrThreads < C && rk[q] >= blo && rk[q] <= bhi) bin_keys[atomicAdd(&s_cnt, 1u)] = rk[q];
+      for (int q = 0; q < kPer; ++q)
+        if (t + q * NT < C && rk[q] >= blo && rk[q] <= bhi) sm.bin_keys[atomicAdd(&sm.s_cnt, 1u)] = rk[q];
       __syncthreads();
       if (t < (int)nb) {
-        const unsigned long long mine = bin_keys[t];
+        const unsigned long long mine = sm.bin_keys[t];
         unsigned int r = 0;
-        for (unsigned int j = 0; j < nb; ++j) r += bin_keys[j] < mine ? 1u : 0u;
-        if (r + 1 == remaining) s_thr = mine;
+        for (unsigned int j = 0; j < nb; ++j) r += sm.bin_keys[j] < mine ? 1u : 0u;
+        if (r + 1 == remaining) sm.s_thr = mine;
       }
       __syncthreads();
       break;
     }
     lo = blo;
     hi = bhi;
-    for (int i = t; i < kRrBins; i += kRrThreads) hist[i] = 0u;
+    for (int i = t; i < kRrBins; i += NT) sm.hist[i] = 0u;
     __syncthreads();
   }
-  const unsigned long long thr = s_thr;
+  const unsigned long long thr = sm.s_thr;
 #pragma unroll
-  for (int q = 0; q < kRrPer; ++q) {
-    const int id = t + q * kRrThreads;
-    if (id < C) kept[id] = rk[q] <= thr ? 1 : 0;
+  for (int q = 0; q < kPer; ++q) {
+    const int id = t + q * NT;
+    if (id < C) sm.kept[id] = rk[q] <= thr ? 1 : 0;
   }
   __syncthreads();
-  // flatten: kept ids ascending -> rows 1..n
+}
+
+// Flatten the kept candidates (ids ascending -> rows 1..n) and write the
+// flat arrays; with a.mask set, the ancestor mask and positions as well.
+template <int NT>
+__device__ void flatten_and_mask(const RerankArgs &a, int b, const int (&pre_tok)[kMaxC / NT],
+                                 const int (&pre_par)[kMaxC / NT], RerankSmem &sm) {
+  constexpr int kPer = kMaxC / NT;
+  const int t = threadIdx.x;
+  const int C = a.C;
   int cnt = 0;
 #pragma unroll
-  for (int j = 0; j < kRrPer; ++j) {
-    const int id = kRrPer * t + j;
-    cnt += (id < C && kept[id]) ? 1 : 0;
+  for (int j = 0; j < kPer; ++j) {
+    const int id = kPer * t + j;
+    cnt += (id < C && sm.kept[id]) ? 1 : 0;
   }
   int total;
-  int run = block_excl_scan_1024(cnt, tmp, total);
+  int run = block_excl_scan<NT>(cnt, sm.tmp, total);
 #pragma unroll
-  for (int j = 0; j < kRrPer; ++j) {
-    const int id = kRrPer * t + j;
-    if (id < C) flat_of[id] = kept[id] ? (short)(1 + run++) : (short)-1;
+  for (int j = 0; j < kPer; ++j) {
+    const int id = kPer * t + j;
+    if (id < C) sm.flat_of[id] = sm.kept[id] ? (short)(1 + run++) : (short)-1;
   }
   __syncthreads();
   const long long fo = (long long)b * a.N;
   int bad = 0;
 #pragma unroll
-  for (int j = 0; j < kRrPer; ++j) {
-    const int id = kRrPer * t + j;
-    if (id >= C || !kept[id]) continue;
-    const int row = flat_of[id];
+  for (int j = 0; j < kPer; ++j) {
+    const int id = kPer * t + j;
+    if (id >= C || !sm.kept[id]) continue;
+    const int row = sm.flat_of[id];
     if (row < 1 || row >= a.N) { bad = 1; continue; }  // never write outside the flat arrays
     const int p = pre_par[j];
     int prow = 0;
     if (p >= 0) {
-      prow = (p < C) ? flat_of[p] : -1;
+      prow = (p < C) ? sm.flat_of[p] : -1;
       if (prow < 0) { bad = 1; prow = 0; }
     }
     int depth = 1;
@@ -461,8 +471,8 @@ __global__ void __launch_bounds__(kRrThreads) k_rerank(RerankArgs a) {
     a.tree.flat_tok[fo + row] = pre_tok[j];
     a.tree.flat_parent[fo + row] = prow;
     a.tree.flat_depth[fo + row] = depth;
-    row_par[row] = prow;
-    row_dep[row] = depth;
+    sm.row_par[row] = prow;
+    sm.row_dep[row] = depth;
   }
   if (bad) flag_status(a.dev_status, ET_DEV_DISCONNECTED);
   if (t == 0) {
@@ -470,8 +480,8 @@ __global__ void __launch_bounds__(kRrThreads) k_rerank(RerankArgs a) {
     a.tree.flat_tok[fo] = a.tree.root_tok ? a.tree.root_tok[b] : -1;
     a.tree.flat_parent[fo] = -1;
     a.tree.flat_depth[fo] = 0;
-    row_par[0] = -1;
-    row_dep[0] = 0;
+    sm.row_par[0] = -1;
+    sm.row_dep[0] = 0;
   }
   if (!a.mask) return;
   // ---- fused: ancestor mask + position ids of the rows just written ----
@@ -479,13 +489,52 @@ __global__ void __launch_bounds__(kRrThreads) k_rerank(RerankArgs a) {
   const int N = a.N, W = (N + 63) >> 6;
   if (t < N) {
     uint64_t w0, w1;
-    const bool ok = ancestor_bits(row_par, t, w0, w1);
+    const bool ok = ancestor_bits(sm.row_par, t, w0, w1);
     uint64_t *mrow = a.mask + ((long long)b * N + t) * W;
     mrow[0] = w0;
     if (W > 1) mrow[1] = w1;
-    a.posids[(long long)b * N + t] = a.prefix_len[b] + row_dep[t];
+    a.posids[(long long)b * N + t] = a.prefix_len[b] + sm.row_dep[t];
     if (!ok) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
   }
+}
+
+// Rerank + flatten of sequence b by one block of NT threads (reranking
+// phase of the EAGLE-2 article): keep the n candidates with the smallest
+// rank keys ((key desc, id asc): equal values keep the shallower node, so the
+// kept tree is connected), rows 1..n = kept ids ascending; with a.mask set,
+// the ancestor mask and position ids of the rows just written as well.
+template <int NT>
+__device__ void rerank_sequence(const RerankArgs &a, int b, RerankSmem &sm) {
+  constexpr int kPer = kMaxC / NT;     // candidates per thread
+  const int t = threadIdx.x;
+  const int C = a.C;
+
+  unsigned long long rk[kPer];
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int id = t + q * NT;
+    rk[q] = id < C ? rank_key(ld_cg(a.tree.cand_key + (long long)b * C + id), id) : ~0ull;
+  }
+  if (t < kMaxN) { sm.row_par[t] = 0; sm.row_dep[t] = 0; }  // rows a broken tree leaves unwritten
+  // the token and parent of this thread's flatten ids, fetched now (they are
+  // needed only after the selection)
+  int pre_tok[kPer], pre_par[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int id = kPer * t + j;
+    pre_tok[j] = id < C ? ld_cg(a.tree.cand_tok + (long long)b * C + id) : -1;  // L2: the candidates may have
+    pre_par[j] = id < C ? ld_cg(a.tree.cand_parent + (long long)b * C + id) : -1;  // been written in this launch
+  }
+  rerank_select_hist<NT>(a, rk, sm);
+  // flatten: kept ids ascending -> rows 1..n
+  flatten_and_mask<NT>(a, b, pre_tok, pre_par, sm);
+}
+
+__global__ void __launch_bounds__(kRrThreads) k_rerank(RerankArgs a) {
+  pdl_wait();     // the previous kernel in the stream has completed
+  pdl_trigger();  // only now may the next kernel launch: at most one waits ahead
+  __shared__ RerankSmem sm;
+  rerank_sequence<kRrThreads>(a, blockIdx.x, sm);
 }
 
 // ---------------------------------------------------------------------------
@@ -690,6 +739,217 @@ __global__ void __launch_bounds__(kClThreads) k_expand_cl(ExpandRowArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// The whole draft tree in one launch: the expansion phase layer after layer,
+// then the reranking phase with the attention mask and positions (EAGLE-2
+// article).  One cluster of ceil(V / 4096) CTAs per (sequence, frontier
+// slot) stays resident for all D layers: slot s of sequence b expands the
+// s-th frontier node of every layer that expands more than s nodes (layer 0:
+// the root, in slot 0), with the same per-row work as k_expand_cl.  Each row
+// of a layer arrives on the layer's counter once its children are written.
+// A cluster of the next layer waits (bounded spin) until every row of the
+// previous layer has arrived, then picks the frontier itself -- the top m of
+// the first min(k, m) children of each previous row, as k_expand_cl's last
+// leader does -- fetching the candidates' keys and table rows in one round,
+// and takes its slot's node (slot 0 also writes the frontier array).  The
+// sequence's last row of the final layer re-arms the layer counters; the
+// rerank, mask and positions follow as one more launch (k_rerank, whose 1024
+// threads select faster than one 256-thread block could here).  Every
+// cluster must be resident
+// at once (they wait on one another): the host launches this kernel only
+// when the occupancy calculator says they all fit.  Data written inside the
+// launch (candidates) is read through L2 (ld.cg), not L1, which other SMs'
+// writes do not update.
+// ---------------------------------------------------------------------------
+struct BuildArgs {
+  const float *logits;
+  long long row_stride;
+  const int32_t *row_of_node;
+  int vec4;
+  int B, V, k, m, C, D, slots;  // slots: clusters per sequence (the widest layer's expanded rows)
+  int expanded[kMaxDepth];
+  int base[kMaxDepth + 2];
+  et_tree tree;
+  int32_t *dev_status;
+  unsigned int *layer_cnt;  // [B][kMaxDepth] rows of each layer whose children are written; back to 0 at the end
+  long long wait_cycles;    // bound of a wait for the previous layer (et_set_wait_limit)
+};
+
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+struct BuildPick {
+  unsigned long long fl[kMaxM * kMaxTopk];  // frontier candidates (rank keys)
+  long long rowof[kMaxM * kMaxTopk];        // their table rows
+  int sel[kMaxM];
+  long long s_row;
+  int s_node;
+};
+
+__global__ void __launch_bounds__(kClThreads) k_tree_build(BuildArgs a) {
+  __shared__ ExpandClSmem sh_e;
+  __shared__ BuildPick pk;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int R = gridDim.x;  // CTAs per row = cluster size
+  const int q = (int)cl_rank();
+  const int b = blockIdx.y / a.slots, s = blockIdx.y - b * a.slots;
+  const int k = a.k;
+  unsigned int *cnt = a.layer_cnt + (long long)b * kMaxDepth;
+  cl_arrive_relaxed();  // phase 0: this block has started (waited on before any remote store)
+  pdl_wait();           // the previous kernel in the stream has completed
+  pdl_trigger();        // every block of this grid is resident before a dependent can launch
+
+  for (int layer = 0; layer < a.D; ++layer) {
+    const int m_l = a.expanded[layer];
+    if (s >= m_l) continue;  // this slot has no node to expand in this layer (the whole cluster skips it)
+    const int base_next = a.base[layer + 1];
+    int node = -1, bad = 0;
+    long long row = (long long)b * m_l + s;  // the table row without a row map
+    if (layer > 0) {
+      // every row of the previous layer has written its children
+      const int m_prev = a.expanded[layer - 1];
+      if (t == 0 && ld_acquire_u32(cnt + layer - 1) < (unsigned)m_prev) {
+        const long long t0 = clock64();
+        while (ld_acquire_u32(cnt + layer - 1) < (unsigned)m_prev) {
+          if (clock64() - t0 > a.wait_cycles) {  // never expected: report, go on (outputs invalid)
+            flag_status(a.dev_status, ET_DEV_TIMEOUT);
+            break;
+          }
+        }
+      }
+      __syncthreads();
+      // the frontier: a child at position e of its row has e better siblings,
+      // so only the first m_l of every row can rank below m_l
+      const int base_l = a.base[layer];
+      const int nk = k < m_l ? k : m_l;
+      const int P = m_prev * nk;
+      for (int c = t; c < P; c += kClThreads) {
+        const int rs = c / nk, e = c - rs * nk;
+        const int id = base_l + rs * k + e;
+        pk.fl[c] = rank_key(ld_cg(a.tree.cand_key + (long long)b * a.C + id), id);
+        if (a.row_of_node) pk.rowof[c] = a.row_of_node[(long long)b * (a.C + 1) + id + 1];
+      }
+      __syncthreads();
+      block_select<kClThreads>(pk.fl, P, m_l, [&](int r, unsigned long long key_r) {
+        pk.sel[r] = (int)(key_r & ((1ull << kIdBits) - 1));
+      });
+      __syncthreads();
+      if (t < m_l) {  // slots hold the picked ids in ascending order
+        const int mine = pk.sel[t];
+        int slot = 0;
+        for (int j = 0; j < m_l; ++j) slot += pk.sel[j] < mine ? 1 : 0;
+        if (slot == s) {
+          pk.s_node = mine;
+          const int rs = (mine - base_l) / k, e = (mine - base_l) - rs * k;
+          pk.s_row = a.row_of_node ? pk.rowof[rs * nk + e] : row;
+        }
+        if (s == 0 && q == 0) a.tree.frontier[b * a.m + slot] = mine;
+      } else if (s == 0 && q == 0 && t < a.m) {
+        a.tree.frontier[b * a.m + t] = -1;
+      }
+      __syncthreads();
+      node = pk.s_node;
+      row = pk.s_row;
+      if (node < 0 || node >= a.C) bad = 1;
+    } else if (a.row_of_node) {
+      row = a.row_of_node[(long long)b * (a.C + 1)];  // the root
+    }
+    const float *zrow = nullptr;
+    if (!bad && row >= 0) zrow = a.logits + row * a.row_stride;
+    else bad = 1;
+    const int base = q * kClSpan;
+    int flag = 0;
+    float v[4 * kClVec];
+#pragma unroll
+    for (int u = 0; u < kClVec; ++u) {
+      const int e0 = base + u * kClThreads * 4 + t * 4;
+      if (zrow && a.vec4 && e0 + 3 < a.V) {
+        const float4 f = __ldcs(reinterpret_cast<const float4 *>(zrow + e0));
+        v[4 * u] = f.x; v[4 * u + 1] = f.y; v[4 * u + 2] = f.z; v[4 * u + 3] = f.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[4 * u + j] = (zrow && e0 + j < a.V) ? __ldcs(zrow + e0 + j) : -INFINITY;
+      }
+    }
+    const long long pkey = (q == 0 && node >= 0 && !bad) ? ld_cg(a.tree.cand_key + (long long)b * a.C + node) : 0ll;
+    unsigned long long key[4 * kClVec];
+#pragma unroll
+    for (int u = 0; u < kClVec; ++u) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int e = 4 * u + j, id = base + u * kClThreads * 4 + t * 4 + j;  // ids >= V are padding
+        if (id < a.V) v[e] = sanitize_logit(v[e], flag);
+        key[e] = zid_key(v[e], (unsigned int)id);
+      }
+    }
+    warp_topk_keys<4 * kClVec>(key, k, sh_e.cand[warp], kWarpCand, sh_e.wl + warp * k);
+    if (flag) flag_status(a.dev_status, ET_DEV_NONFINITE);
+    if (bad && q == 0 && t == 0) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
+    __syncthreads();
+    unsigned long long head = sh_e.wl[0];
+#pragma unroll
+    for (int w = 1; w < kClWarps; ++w) head = sh_e.wl[w * k] < head ? sh_e.wl[w * k] : head;
+    const float Mq = zid_value(head);
+    float sum = 0.f;
+    if (Mq > -INFINITY) {
+#pragma unroll
+      for (int e = 0; e < 4 * kClVec; ++e) sum += exp_fast(v[e] - Mq);
+    }
+    sum = warp_sum(sum);
+    if (lane == 0) sh_e.wsum[warp] = sum;
+    cl_wait();  // every block has started, and the leader has finished reading the previous layer
+    const uint32_t gl_remote = cl_map(&sh_e.gl[q * k], 0);
+    block_select<kClThreads>(sh_e.wl, kClWarps * k, k,
+                             [&](int r, unsigned long long key_r) { cl_st_u64(gl_remote + 8u * (uint32_t)r, key_r); });
+    __syncthreads();
+    if (t == 0) {
+      float cs = 0.f;
+#pragma unroll
+      for (int w = 0; w < kClWarps; ++w) cs += sh_e.wsum[w];
+      cl_st_f32x2(cl_map(&sh_e.gms[q], 0), Mq, cs);
+    }
+    cl_arrive();  // release this block's stores
+    cl_wait();    // every block's stores have landed in the leader
+    if (q == 0) {
+      float M = -INFINITY, S = 0.f;
+      {
+        float2 gq[kClMaxCtas];
+#pragma unroll
+        for (int x = 0; x < kClMaxCtas; ++x) {
+          gq[x] = x < R ? sh_e.gms[x] : make_float2(-INFINITY, 0.f);
+          M = fmaxf(M, gq[x].x);
+        }
+#pragma unroll
+        for (int x = 0; x < kClMaxCtas; ++x) S += gq[x].x > -INFINITY ? gq[x].y * expf(gq[x].x - M) : 0.f;
+      }
+      const float logS = (M > -INFINITY) ? logf(S) : 0.f;
+      block_select<kClThreads>(sh_e.gl, R * k, k, [&](int r, unsigned long long key_r) {
+        const float z = zid_value(key_r);
+        const int id = (int)zid_id(key_r);
+        const float lp = (M > -INFINITY && z > -INFINITY) ? (z - M) - logS : -INFINITY;
+        const long long o = (long long)b * a.C + base_next + s * k + r;
+        a.tree.cand_tok[o] = id < a.V ? id : -1;
+        a.tree.cand_parent[o] = node;
+        a.tree.cand_lp[o] = lp;
+        a.tree.cand_key[o] = add_keys(pkey, fixed_key(lp));
+      });
+      __syncthreads();  // every child of this row is written
+      if (t == 0) {
+        __threadfence();
+        const bool last = atomicAdd(cnt + layer, 1u) == (unsigned)(m_l - 1);  // the next layer may count this row
+        // the sequence's last row of the final layer: every wait of this
+        // sequence is over, re-arm the counters for the next call
+        if (last && layer + 1 == a.D)
+          for (int l = 0; l < a.D; ++l) cnt[l] = 0u;
+      }
+    }
+    cl_arrive();  // the leader is done with its shared memory for this layer
+  }
+}
+
 }  // namespace et
 
 using namespace et;
@@ -712,7 +972,8 @@ static TreeWs tree_ws_layout(const et_tree_cfg *cfg) {
   const int nch = nchunk_of(cfg->V);
   const int rows = cfg->B * (cfg->m > N ? cfg->m : N);
   w.rows = rows;
-  w.cnt_bytes = align256(sizeof(unsigned int) * (size_t)(rows + cfg->B));
+  // counters: [rows] per row, [B] per sequence, [B][kMaxDepth] per layer (et_tree_build)
+  w.cnt_bytes = align256(sizeof(unsigned int) * (size_t)(rows + cfg->B + (size_t)cfg->B * kMaxDepth));
   const size_t exp_part = sizeof(float) * (size_t)cfg->B * cfg->m * nch * (2 + 2 * cfg->topk);
   const size_t ver_part = sizeof(float) * (size_t)cfg->B * N * nch * 2;
   w.part_off = w.cnt_bytes;
@@ -837,6 +1098,91 @@ extern "C" et_status et_tree_rerank_mask(const et_tree_cfg *cfg, et_tree *tree, 
   return launch_rerank(cfg, tree, dev_status, prefix_len, mask, posids, stream);
 }
 
+// The whole tree in one launch when every cluster of k_tree_build fits on the
+// GPU at once; otherwise the same work as D expansion launches and the fused
+// rerank launch.
+static int tree_build_fits(int clusters, int R) {
+  static std::mutex mu;
+  static int cached_dev = -1, cached_R = -1, cached_n = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev != cached_dev || R != cached_R) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(R, clusters, 1);
+    lc.blockDim = dim3(kClThreads, 1, 1);
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = (unsigned)R;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    lc.attrs = &attr;
+    lc.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (void *)k_tree_build, &lc) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    cached_dev = dev;
+    cached_R = R;
+    cached_n = n;
+  }
+  return clusters <= cached_n;
+}
+
+extern "C" et_status et_tree_build(const et_tree_cfg *cfg, const float *logits, int64_t row_stride,
+                                   const int32_t *row_of_node, et_tree *tree, const int32_t *prefix_len,
+                                   uint64_t *mask, int32_t *posids, int32_t *dev_status, void *ws, size_t ws_bytes,
+                                   et_stream_t stream) {
+  Geometry g;
+  ET_RETURN_IF(!make_geometry(cfg, &g), ET_ERR_INVALID_ARG);
+  ET_RETURN_IF(!logits || row_stride < cfg->V || !tree_ptrs_ok(tree) || !et_aligned(logits, 4), ET_ERR_INVALID_ARG);
+  ET_RETURN_IF(!tree->flat_node || !tree->flat_tok || !tree->flat_parent || !tree->flat_depth, ET_ERR_INVALID_ARG);
+  ET_RETURN_IF((mask || posids) && (!mask || !posids || !prefix_len || !et_aligned(mask, 8)), ET_ERR_INVALID_ARG);
+  const TreeWs w = tree_ws_layout(cfg);
+  ET_RETURN_IF(!ws || ws_bytes < w.total || !et_aligned(ws, 256), ET_ERR_WORKSPACE);
+  int slots = 1;
+  for (int l = 0; l < cfg->depth; ++l) slots = g.expanded[l] > slots ? g.expanded[l] : slots;
+  const int R = (cfg->V + kClSpan - 1) / kClSpan;
+  const long long clusters = (long long)cfg->B * slots;
+  if (cfg->V <= kClMaxV && clusters <= 65535 && tree_build_fits((int)clusters, R)) {
+    BuildArgs a;
+    a.logits = logits;
+    a.row_stride = row_stride;
+    a.row_of_node = row_of_node;
+    a.vec4 = et_aligned(logits, 16) && (row_stride % 4 == 0);
+    a.B = cfg->B; a.V = cfg->V; a.k = cfg->topk; a.m = cfg->m; a.C = g.C; a.D = cfg->depth; a.slots = slots;
+    for (int l = 0; l < kMaxDepth; ++l) a.expanded[l] = l < cfg->depth ? g.expanded[l] : 0;
+    for (int l = 0; l < kMaxDepth + 2; ++l) a.base[l] = (l <= cfg->depth + 1) ? g.base[l] : 0x7fffffff;
+    a.tree = *tree;
+    a.dev_status = dev_status;
+    unsigned char *base = static_cast<unsigned char *>(ws);
+    a.layer_cnt = reinterpret_cast<unsigned int *>(base) + w.rows + cfg->B;  // the per-layer counters
+    a.wait_cycles = et_wait_limit_cycles();
+    const et_status st = et_launch(k_tree_build, dim3(R, (unsigned)clusters, 1), dim3(kClThreads, 1, 1), 0,
+                                   (cudaStream_t)stream, R, a);
+    if (st != ET_OK) return st;
+    return launch_rerank(cfg, tree, dev_status, prefix_len, mask, posids, stream);
+  }
+  for (int l = 0; l < cfg->depth; ++l) {
+    const et_status st = et_tree_expand(cfg, l, logits, row_stride, row_of_node, tree, dev_status, ws, ws_bytes,
+                                        stream);
+    if (st != ET_OK) return st;
+  }
+  return launch_rerank(cfg, tree, dev_status, prefix_len, mask, posids, stream);
+}
+
+extern "C" int32_t et_tree_build_launches(const et_tree_cfg *cfg) {
+  Geometry g;
+  if (!make_geometry(cfg, &g)) return -1;
+  int slots = 1;
+  for (int l = 0; l < cfg->depth; ++l) slots = g.expanded[l] > slots ? g.expanded[l] : slots;
+  const int R = (cfg->V + kClSpan - 1) / kClSpan;
+  const long long clusters = (long long)cfg->B * slots;
+  if (cfg->V <= kClMaxV && clusters <= 65535 && tree_build_fits((int)clusters, R)) return 2;
+  return cfg->depth + 1;
+}
+
 extern "C" et_status et_tree_mask_posids(const et_tree_cfg *cfg, const et_tree *tree, const int32_t *prefix_len,
                                          uint64_t *mask, int32_t *posids, et_stream_t stream) {
   Geometry g;
@@ -870,9 +1216,24 @@ extern "C" const char *et_status_string(et_status s) {
 extern "C" int32_t et_abi_version(void) { return ET_ABI_VERSION; }
 
 // ---------------------------------------------------------------------------
+// the bound of device waits (a diagnostic: small values make waits expire)
+// ---------------------------------------------------------------------------
+#include <atomic>
+static constexpr long long kDefaultWaitCycles = 1ll << 32;  // ~2 s at 2 GHz
+static std::atomic<long long> g_wait_cycles{kDefaultWaitCycles};
+
+long long et_wait_limit_cycles() { return g_wait_cycles.load(std::memory_order_relaxed); }
+
+extern "C" int64_t et_set_wait_limit(int64_t cycles) {
+  return g_wait_cycles.exchange(cycles > 0 ? (long long)cycles : kDefaultWaitCycles);
+}
+
+// ---------------------------------------------------------------------------
 // et_tree_expand_noalloc: et_tree_expand with its scratch in a static device
 // array, for callers that must not allocate device memory themselves.
 // ---------------------------------------------------------------------------
+#include <cuda.h>
+
 #include <mutex>
 
 namespace et {
@@ -881,25 +1242,52 @@ namespace et {
 constexpr size_t kExpandScratchBytes = 4u << 20;  // 4 MiB
 static __device__ __align__(256) unsigned char g_expand_scratch[kExpandScratchBytes];
 
-constexpr int kMaxDevices = 64;
-static std::mutex g_scratch_mu;
-static void *g_scratch_ptr[kMaxDevices];  // device address of g_expand_scratch, per device
-
-// The array's name is only a host-side stand-in in host code; its device
-// address is looked up once per device, with that device current.
-static et_status expand_scratch(void **out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ET_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+// The array's name is only a host-side stand-in in host code.  Its device
+// address belongs to the module loaded in one CUDA context, so it is looked up
+// (cudaGetSymbolAddress, with that context's device current) the first time a
+// context calls, and kept per context.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+static CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = [] {
     void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_expand_scratch) != cudaSuccess || !p) {
-      cudaGetLastError();
-      return ET_ERR_CUDA;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    cudaGetLastError();
+    return reinterpret_cast<CtxGetCurrentFn>(p);
+  }();
+  return fn;
+}
+
+constexpr int kMaxScratchCtx = 64;
+static std::mutex g_scratch_mu;
+static CUcontext g_scratch_ctx[kMaxScratchCtx];
+static void *g_scratch_ptr[kMaxScratchCtx];
+static int g_scratch_n = 0, g_scratch_next = 0;
+
+static et_status expand_scratch(void **out) {
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  const CtxGetCurrentFn cur = ctx_get_current();
+  CUcontext ctx = nullptr;
+  if (cur && cur(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+  for (int i = 0; ctx && i < g_scratch_n; ++i)
+    if (g_scratch_ctx[i] == ctx) {
+      *out = g_scratch_ptr[i];
+      return ET_OK;
     }
-    g_scratch_ptr[dev] = p;
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_expand_scratch) != cudaSuccess || !p) {
+    cudaGetLastError();
+    return ET_ERR_CUDA;
   }
-  *out = g_scratch_ptr[dev];
+  if (cur && !ctx && cur(&ctx) != CUDA_SUCCESS) ctx = nullptr;  // the look-up made the primary context current
+  if (ctx) {  // remember it (the oldest entry makes room when the table is full)
+    const int slot = g_scratch_n < kMaxScratchCtx ? g_scratch_n++ : (g_scratch_next++ % kMaxScratchCtx);
+    g_scratch_ctx[slot] = ctx;
+    g_scratch_ptr[slot] = p;
+  }
+  *out = p;
   return ET_OK;
 }
 }  // namespace et

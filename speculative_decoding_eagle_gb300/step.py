@@ -90,8 +90,10 @@ class VerifyStep:
     """Buffers and call chain of one verification step for a fixed shape."""
 
     def __init__(self, wl: W.Workload, B: Optional[int] = None, mode: Optional[int] = None, device="cuda",
-                 num_splits: int = 0, max_prefix: Optional[int] = None, attn_impl: int = E.ATTN_AUTO):
+                 num_splits: int = 0, max_prefix: Optional[int] = None, attn_impl: int = E.ATTN_AUTO,
+                 per_layer: bool = False):
         self.wl = wl
+        self.per_layer = per_layer  # the tree by one et_tree_expand launch per layer, then et_tree_rerank_mask
         self.cfg = tree_cfg(wl, B)
         self.B = self.cfg.B
         self.C = E.et_num_candidates(self.cfg)
@@ -124,7 +126,10 @@ class VerifyStep:
         return E.AttnShape(B=self.B, N=self.cfg.N, Hq=self.wl.Hq, Hkv=self.wl.Hkv, d=self.wl.d,
                            dtype=E.ET_BF16 if self.wl.dtype == "bf16" else E.ET_F32, scale=self.wl.d ** -0.5,
                            max_prefix=mp, kv_rows=inp.k_prefix.shape[0], num_splits=self.num_splits,
-                           impl=self.attn_impl)
+                           impl=self.attn_impl,
+                           # Q, K/V and the prefix lengths are step inputs; only the mask comes
+                           # from the kernel before attention
+                           flags=E.ET_ATTN_INPUTS_READY)
 
     def prepare(self, inp: StepInputs) -> None:
         shape = self.attn_shape(inp)
@@ -135,12 +140,18 @@ class VerifyStep:
 
     # the five calls -------------------------------------------------------
     def build_tree(self, inp: StepInputs, stream=None) -> None:
+        """D expansion layers, rerank, mask and positions: one launch (et_tree_build) when its clusters fit."""
         self.tree.root_tok = inp.root_tok
-        for layer in range(self.cfg.depth):
-            E.et_tree_expand(self.cfg, layer, inp.draft, self.tree, self.ws, row_of_node=inp.row_of_node,
-                             dev_status=self.dev_status, stream=stream)
-        E.et_tree_rerank_mask(self.cfg, self.tree, inp.prefix_len, self.mask, self.posids, dev_status=self.dev_status,
-                              stream=stream)
+        if self.per_layer:
+            for layer in range(self.cfg.depth):
+                E.et_tree_expand(self.cfg, layer, inp.draft, self.tree, self.ws, row_of_node=inp.row_of_node,
+                                 dev_status=self.dev_status, stream=stream)
+            E.et_tree_rerank_mask(self.cfg, self.tree, inp.prefix_len, self.mask, self.posids,
+                                  dev_status=self.dev_status, stream=stream)
+        else:
+            E.et_tree_build(self.cfg, inp.draft, self.tree, self.ws, row_of_node=inp.row_of_node,
+                            prefix_len=inp.prefix_len, mask=self.mask, posids=self.posids,
+                            dev_status=self.dev_status, stream=stream)
 
     def attention(self, inp: StepInputs, stream=None) -> None:
         E.et_tree_attention(self.shape, inp.q, inp.k_prefix, inp.v_prefix, inp.kv_row0, inp.prefix_len,
@@ -163,5 +174,7 @@ class VerifyStep:
         self.accept(inp, stream)
 
     def launches(self) -> int:
-        """Kernel launches of one step: D expands, rerank with mask, attention, acceptance."""
-        return self.cfg.depth + 3
+        """Kernel launches of one step: the tree (one launch, or D expands and the rerank with mask),
+        attention, acceptance."""
+        tree = self.cfg.depth + 1 if self.per_layer else E.et_tree_build_launches(self.cfg)
+        return tree + 2
