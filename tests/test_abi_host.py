@@ -24,7 +24,7 @@ def lib():
 def _declared():
     txt = open(os.path.join(ROOT, "include", "eagle_tree.h")).read()
     txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
-    return set(re.findall(r"^\s*(?:et_status|int32_t|size_t|const char \*)\s*(et_\w+)\s*\(", txt, flags=re.M))
+    return set(re.findall(r"^\s*(?:et_status|int32_t|int64_t|size_t|const char \*)\s*(et_\w+)\s*\(", txt, flags=re.M))
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(lib):
     assert names == set(E.EXPORTED)
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.et_abi_version() == 1
+    assert lib.et_abi_version() == 2
 
 
 @pytest.mark.parametrize("D,k,m,n", [(4, 4, 4, 16), (6, 10, 10, 60), (8, 8, 8, 80), (1, 32, 1, 32), (16, 2, 2, 50),
@@ -107,8 +107,8 @@ def test_attention_argument_checks(lib):
     assert sz > 0
     assert call(shape(num_splits=4, impl=1), wsb=sz - 1) == E.ET_ERR_WORKSPACE
     assert lib.et_tree_attention_splits(ctypes.byref(shape(num_splits=4))) == 4
-    # the tcgen05 path: the splits of a tile form one cluster (at most 8) and
-    # merge through the workspace: per split and 128-row tile, fp32 rows and a (max, sum) pair per row
+    # the tcgen05 path: the splits of a tile form one cluster (at most 8) and merge through the
+    # workspace: per split and 128-row tile, fp32 rows and a (max, sum) pair per row
     tc4 = lib.et_tree_attention_workspace_size(ctypes.byref(shape(num_splits=4, impl=2)))
     assert tc4 == 32 * 1 * 4 * 128 * (128 * 4 + 8)
     assert call(shape(num_splits=4, impl=2), ws=None) == E.ET_ERR_WORKSPACE
@@ -120,6 +120,14 @@ def test_attention_argument_checks(lib):
     # workspace: tiles x splits x rows-per-tile x d floats (+ counters and (max, sum) pairs)
     mma = lib.et_tree_attention_workspace_size(ctypes.byref(shape(num_splits=4, impl=1)))
     assert mma >= 32 * 4 * 64 * 128 * 4
+
+
+def test_attention_rejects_unknown_flags(lib):
+    shape = E.AttnShapeC(1, 61, 32, 32, 128, E.ET_BF16, 0.088, 1024, 32 * 1024, 0, 0, 0, 4)
+    assert lib.et_tree_attention_workspace_size(ctypes.byref(shape)) == 0  # not a valid shape
+    assert lib.et_tree_attention_splits(ctypes.byref(shape)) == -1
+    ok = E.AttnShapeC(1, 61, 32, 32, 128, E.ET_BF16, 0.088, 1024, 32 * 1024, 0, 0, 0, E.ET_ATTN_INPUTS_READY)
+    assert lib.et_tree_attention_splits(ctypes.byref(ok)) >= 1
 
 
 def test_verify_argument_checks(lib):
@@ -208,3 +216,29 @@ def test_status_strings(lib):
     for s in range(6):
         assert E.status_string(s)
     assert E.status_string(99) == "unknown status"
+
+
+def test_tree_build_argument_checks(lib):
+    """et_tree_build: host-side rejections; without a GPU nothing launches."""
+    cfg = E.TreeCfgC(1, 32000, 6, 10, 10, 60, 1.0)
+    bad_cfg = E.TreeCfgC(1, 32000, 6, 10, 10, 5000, 1.0)  # n > C
+    tree = E.TreeC(*([FAKE] * 10))
+    ws_sz = lib.et_tree_workspace_size(ctypes.byref(cfg))
+
+    def call(c=cfg, logits=FAKE, stride=32000, t=tree, mask=None, posids=None, prefix=None, ws=FAKE, wsb=ws_sz):
+        return lib.et_tree_build(ctypes.byref(c), logits, stride, None, ctypes.byref(t), prefix, mask, posids, None,
+                                 ws, wsb, None)
+    assert call(c=bad_cfg) == E.ET_ERR_INVALID_ARG
+    assert call(logits=None) == E.ET_ERR_INVALID_ARG
+    assert call(stride=31999) == E.ET_ERR_INVALID_ARG
+    assert call(logits=FAKE + 2) == E.ET_ERR_INVALID_ARG                 # rows must be 4-byte aligned
+    assert call(mask=FAKE) == E.ET_ERR_INVALID_ARG                       # mask without posids / prefix_len
+    assert call(mask=FAKE + 4, posids=FAKE, prefix=FAKE) == E.ET_ERR_INVALID_ARG  # mask not 8-byte aligned
+    assert call(ws=None) == E.ET_ERR_WORKSPACE
+    assert call(wsb=ws_sz - 1) == E.ET_ERR_WORKSPACE
+    assert call(ws=FAKE + 16) == E.ET_ERR_WORKSPACE
+    broken = E.TreeC(*([FAKE] * 6 + [None] + [FAKE] * 3))               # no flat_node array
+    assert call(t=broken) == E.ET_ERR_INVALID_ARG
+    # past one cluster (V > 32768) the call issues the per-layer launches: D + 1 (else 2)
+    assert lib.et_tree_build_launches(ctypes.byref(E.TreeCfgC(1, 50000, 4, 4, 4, 16, 1.0))) == 5
+    assert lib.et_tree_build_launches(ctypes.byref(bad_cfg)) == -1

@@ -265,6 +265,7 @@ ATTN_CASES = [
     (2, 7, 4, 4, 128, [0, 0], "bf16", 0, 0),        # no prefix at all
     (1, 61, 8, 8, 128, [4096], "bf16", 32, 0),      # many splits (8 on the tcgen05 path: one cluster)
     (1, 61, 8, 8, 128, [1000], "bf16", 5, 0),       # odd cluster size
+    (1, 61, 2, 2, 128, [8192], "bf16", 7, 0),       # 7 splits of 129 key tiles
 ]
 
 
@@ -303,6 +304,61 @@ def test_tcgen05_and_mma_paths_agree_at_the_7b_shape():
     a = _attn_case(1, 61, 32, 32, 128, [1024], "bf16", seed=1, impl=E.ATTN_TCGEN05)[0]
     b = _attn_case(1, 61, 32, 32, 128, [1024], "bf16", seed=1, impl=E.ATTN_MMA_SYNC)[0]
     assert np.abs(a - b).max() <= 2 * BF16_MAX_ABS
+
+
+# ---------------------------------------------------------------------------
+# the whole tree in one launch (et_tree_build)
+# ---------------------------------------------------------------------------
+BUILD_CASES = [  # workload, B, n, V, expected launches (None: whatever fits)
+    ("tiny", 4, None, None, 2),
+    ("llama2-7b", 1, None, None, 2),
+    ("llama2-70b", 1, None, None, 2),
+    ("llama2-7b", 3, 100, None, None),
+    ("tiny", 2, None, 50000, 5),  # past one cluster: the per-layer launches
+]
+
+
+@pytest.mark.parametrize("wl_name,B,n,V,launches", BUILD_CASES)
+def test_tree_build_matches_per_layer_path_and_oracle(wl_name, B, n, V, launches):
+    """et_tree_build (all layers in one launch, then the rerank) writes
+    exactly what D et_tree_expand calls and et_tree_rerank_mask write; twice
+    in a row (its per-layer counters must be back at zero for the second
+    call), and equal to the oracle's tree."""
+    wl = W.WORKLOADS[wl_name].with_(B=B)
+    if n is not None:
+        wl = wl.with_(n=n)
+    if V is not None:
+        wl = wl.with_(V=V)
+    one = S.VerifyStep(wl, per_layer=False)
+    ref = S.VerifyStep(wl, per_layer=True)
+    if launches is not None:
+        assert E.et_tree_build_launches(one.cfg) == launches
+    h = S.host_inputs(wl, one.C)
+    inp = S.to_device(wl, h)
+    for st in (one, ref):
+        st.prepare(inp)
+        st.build_tree(inp)
+    torch.cuda.synchronize()
+    first = gpu_tree_np(one.tree)
+    want = gpu_tree_np(ref.tree)
+    for name in want:
+        np.testing.assert_array_equal(first[name], want[name], err_msg=name)
+    np.testing.assert_array_equal(one.mask.cpu().numpy(), ref.mask.cpu().numpy())
+    np.testing.assert_array_equal(one.posids.cpu().numpy(), ref.posids.cpu().numpy())
+    one.tree.flat_node.fill_(-7)
+    one.mask.zero_()
+    one.build_tree(inp)
+    torch.cuda.synchronize()
+    again = gpu_tree_np(one.tree)
+    for name in want:
+        np.testing.assert_array_equal(again[name], want[name], err_msg=name)
+    np.testing.assert_array_equal(one.mask.cpu().numpy(), ref.mask.cpu().numpy())
+    assert int(one.dev_status.item()) == 0
+    ot = O.build_tree(ocfg(one.cfg), h["draft"], h["row_of_node"], h["root_tok"])
+    assert not O.near_tie_selections(ot)
+    for name, o in (("flat_node", ot.flat_node), ("flat_tok", ot.flat_tok), ("flat_parent", ot.flat_parent),
+                    ("flat_depth", ot.flat_depth), ("cand_tok", ot.tok), ("cand_parent", ot.parent)):
+        np.testing.assert_array_equal(again[name], o, err_msg=name)
 
 
 # ---------------------------------------------------------------------------
@@ -373,19 +429,116 @@ def test_draftq_chained_rejections(wl_name, B, V, T, squeeze):
     assert int(st.dev_status.item()) == 0
 
 
+def _rejections(ot, ref, b):
+    """Children the oracle's walk rejected in sequence b: at each row of the
+    accepted path the siblings tried before the accepted one, and every child
+    of the row where it stopped."""
+    ch = {}
+    for j in range(1, ot.flat_parent.shape[1]):
+        ch.setdefault(int(ot.flat_parent[b, j]), []).append(j)
+    a = int(ref.accept_len[b])
+    path = [int(x) for x in ref.path[b, :a + 1]]
+    n = sum(ch.get(path[s], []).index(path[s + 1]) for s in range(a))
+    return n + len(ch.get(path[-1], []))
+
+
+@pytest.mark.parametrize("wl_name,B,V", [("llama2-7b", 4, None), ("tiny", 3, 50000)])
+@pytest.mark.parametrize("slope,T,squeeze", [(7.0, 0.5, 3e-5), (4.0, 1.0, 1e-2), (7.0, 1.5, 1e-4), (2.5, 0.5, 1e-3)])
+def test_point_mass_steep_targets(wl_name, B, V, slope, T, squeeze):
+    """Steep targets, low temperatures and uniforms pushed toward 1 reject long
+    runs of children that hold almost all of a row's mass (the regime where a
+    1 - R form of the ratio cancels in fp32), on both phase-1 layouts: every
+    decision the oracle does not flag as a near tie is bit-exact."""
+    wl = W.WORKLOADS[wl_name].with_(B=B, temperature=T, slope=slope)
+    if V is not None:
+        wl = wl.with_(V=V)
+    cfg = S.tree_cfg(wl)
+    C = E.et_num_candidates(cfg)
+    h = S.host_inputs(wl, C)
+    h["uniforms"] = (1.0 - (1.0 - h["uniforms"].astype(np.float64)) * squeeze).astype(np.float32)
+    ot = O.build_tree(ocfg(cfg), h["draft"], h["row_of_node"], h["root_tok"])
+    ref = O.verify_accept(ocfg(cfg), O.STOCH_POINT, ot.flat_tok, ot.flat_parent, ot.flat_node, h["target"],
+                          h["row_of_node"], uniforms=h["uniforms"])
+    inp = S.to_device(wl, h)
+    st = S.VerifyStep(wl, mode=E.ET_ACCEPT_STOCH_POINT)
+    upload_oracle_tree(ot, st.tree)
+    st.accept(inp)
+    torch.cuda.synchronize()
+    bad_b = {b for b, _, _ in ref.near_ties}
+    longest = 0
+    for b in range(B):
+        if b in bad_b:
+            continue
+        longest = max(longest, _rejections(ot, ref, b))
+        assert st.accept_len[b].item() == ref.accept_len[b]
+        np.testing.assert_array_equal(st.path[b].cpu().numpy(), ref.path[b])
+        np.testing.assert_array_equal(st.tokens[b].cpu().numpy(), ref.tokens[b])
+    assert len(bad_b) < B and longest >= 3  # long rejection chains occurred
+    assert int(st.dev_status.item()) == 0
+
+
+def test_point_mass_repeated_sibling_tokens():
+    """Siblings that repeat a token (a user-built tree): a repeat of a rejected
+    token has no residual mass and is never accepted, and the rejected mass
+    counts once; the oracle's rule, on both phase-1 layouts."""
+    for V in (32000, 50000):
+        wl = W.WORKLOADS["tiny"].with_(B=4, V=V, slope=3.0, temperature=0.7)
+        cfg = S.tree_cfg(wl)
+        C = E.et_num_candidates(cfg)
+        h = S.host_inputs(wl, C)
+        h["uniforms"] = (1.0 - (1.0 - h["uniforms"].astype(np.float64)) * 1e-2).astype(np.float32)
+        ot = O.build_tree(ocfg(cfg), h["draft"], h["row_of_node"], h["root_tok"])
+        tok = ot.flat_tok.copy()
+        for b in range(cfg.B):  # every second child of each row takes its previous sibling's token
+            seen = {}
+            for j in range(1, tok.shape[1]):
+                p = int(ot.flat_parent[b, j])
+                seen[p] = seen.get(p, 0) + 1
+                if seen[p] % 2 == 0:
+                    tok[b, j] = tok[b, j - 1] if int(ot.flat_parent[b, j - 1]) == p else tok[b, j]
+        ot.flat_tok = tok
+        ref = O.verify_accept(ocfg(cfg), O.STOCH_POINT, ot.flat_tok, ot.flat_parent, ot.flat_node, h["target"],
+                              h["row_of_node"], uniforms=h["uniforms"])
+        inp = S.to_device(wl, h)
+        st = S.VerifyStep(wl, mode=E.ET_ACCEPT_STOCH_POINT)
+        upload_oracle_tree(ot, st.tree)
+        st.accept(inp)
+        torch.cuda.synchronize()
+        bad_b = {b for b, _, _ in ref.near_ties}
+        for b in range(cfg.B):
+            if b in bad_b:
+                continue
+            np.testing.assert_array_equal(st.path[b].cpu().numpy(), ref.path[b])
+            np.testing.assert_array_equal(st.tokens[b].cpu().numpy(), ref.tokens[b])
+        assert len(bad_b) < cfg.B
+
+
 # ---------------------------------------------------------------------------
 # the whole step, every configuration
 # ---------------------------------------------------------------------------
-STEP_CASES = [("tiny", None, None), ("tiny", None, E.ET_ACCEPT_STOCH_POINT), ("llama2-7b", None, None),
-              ("llama2-13b", None, None), ("llama2-70b", None, None), ("llama2-70b", None, E.ET_ACCEPT_STOCH_POINT),
-              ("sweep-7b", 4, None)]
+STEP_CASES = [("tiny", None, None, None), ("tiny", None, E.ET_ACCEPT_STOCH_POINT, None),
+              ("llama2-7b", None, None, None), ("llama2-13b", None, None, None), ("llama2-70b", None, None, None),
+              ("llama2-70b", None, E.ET_ACCEPT_STOCH_POINT, None), ("sweep-7b", 4, None, None),
+              # the batched sweep: ragged prefixes of 512..16384 tokens, kept trees of 16, 32 and 100 nodes
+              ("sweep-7b", 16, None, 16), ("sweep-7b", 32, None, 32), ("sweep-7b", 16, None, 100)]
+ATTN_SAMPLE_FROM_B = 16  # from this batch on, attention is checked on sampled sequences
 
 
-@pytest.mark.parametrize("wl_name,B,mode", STEP_CASES)
-def test_full_step_matches_oracle(wl_name, B, mode):
+def _attention_sample(h, B):
+    """Sequences whose attention the oracle recomputes at large batch: the
+    first, the longest and shortest prefix, and one seeded pick."""
+    L = h["prefix_len"]
+    pick = int(np.random.default_rng(B).integers(0, B))
+    return sorted({0, int(np.argmax(L)), int(np.argmin(L)), pick})
+
+
+@pytest.mark.parametrize("wl_name,B,mode,n", STEP_CASES)
+def test_full_step_matches_oracle(wl_name, B, mode, n):
     wl = W.WORKLOADS[wl_name]
     if B is not None:
         wl = wl.with_(B=B)
+    if n is not None:
+        wl = wl.with_(n=n)
     st = S.VerifyStep(wl, mode=mode)
     cfg = st.cfg
     h = S.host_inputs(wl, st.C)
@@ -404,10 +557,17 @@ def test_full_step_matches_oracle(wl_name, B, mode):
     om, op = O.mask_posids(ot.flat_parent, ot.flat_depth, h["prefix_len"])
     np.testing.assert_array_equal(st.mask.cpu().numpy().view(np.uint64), om)
     np.testing.assert_array_equal(st.posids.cpu().numpy(), op)
-    ref, _ = oracle_attention_from_host(wl, h, om, cfg.B)
     got = out_as_float(st.out)
     tol = (BF16_MAX_ABS, BF16_REL_L2) if wl.dtype == "bf16" else (F32_MAX_ABS, F32_REL_L2)
-    assert np.abs(got - ref).max() <= tol[0] and rel_l2(got, ref) <= tol[1]
+    if cfg.B < ATTN_SAMPLE_FROM_B:
+        ref, _ = oracle_attention_from_host(wl, h, om, cfg.B)
+        assert np.abs(got - ref).max() <= tol[0] and rel_l2(got, ref) <= tol[1]
+    else:
+        for b in _attention_sample(h, cfg.B):
+            hb = dict(h, q=h["q"][b:b + 1], k_tree=h["k_tree"][b:b + 1], v_tree=h["v_tree"][b:b + 1],
+                      prefix_len=h["prefix_len"][b:b + 1], kv_row0=h["kv_row0"][b:b + 1])
+            ref, _ = oracle_attention_from_host(wl, hb, om[b:b + 1], 1)
+            assert np.abs(got[b] - ref[0]).max() <= tol[0] and rel_l2(got[b], ref[0]) <= tol[1], b
     acc = O.verify_accept(oc, st.mode, ot.flat_tok, ot.flat_parent, ot.flat_node, h["target"], h["row_of_node"],
                           uniforms=h["uniforms"])
     # a decision within fp32 rounding of its threshold may go either way:

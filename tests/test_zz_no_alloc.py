@@ -55,6 +55,24 @@ def test_noalloc_expand_matches_workspace_expand_two_calls_in_a_row():
         np.testing.assert_array_equal(a, b)
 
 
+def test_noalloc_expand_past_one_cluster_two_calls_in_a_row():
+    """V = 65536 takes the chunked kernel (per-chunk partials and per-row
+    counters in the library's array, laid out for B * m_l rows), not the
+    cluster kernel; two layers in a row must equal the workspace path."""
+    cfg = E.TreeCfg(B=1, V=65536, depth=2, topk=4, m=4, n=8)
+    C = E.et_num_candidates(cfg)
+    rng = np.random.default_rng(2025)
+    table = torch.from_numpy((rng.standard_normal((cfg.B * (C + 1), cfg.V)) * 2).astype(np.float32)).cuda()
+    ref = E.TreeBuffers.allocate(cfg)
+    got = E.TreeBuffers.allocate(cfg)
+    ws = E.new_workspace(E.et_tree_workspace_size(cfg))
+    for layer in range(2):
+        E.et_tree_expand(cfg, layer, table, ref, ws)
+        E.et_tree_expand_noalloc(cfg, layer, table, got)
+        for a, b in zip(_state(ref), _state(got)):
+            np.testing.assert_array_equal(a, b)
+
+
 def test_noalloc_expand_rejects_shapes_beyond_its_scratch():
     # 1000 root rows of a 262144-token vocabulary with k = 32 need ~34 MB of
     # partials: more than the 4 MiB the library keeps, so nothing is launched
