@@ -179,6 +179,79 @@ print(json.dumps({{"steps": done, "seconds": spent, "parts": parts}}))
 """
 
 
+ORACLE_WORKER = r"""
+import json, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+import oracle as O
+from speculative_decoding_eagle_gb300 import workloads as W
+wl = W.WORKLOADS[{name!r}].with_(B=1)
+cfg = O.TreeCfg(B=1, V=wl.V, depth=wl.depth, topk=wl.topk, m=wl.m, n=wl.n, temperature=wl.temperature)
+C = O.num_candidates(cfg)
+b = {worker}
+target, draft, rmap = W.logit_tables(wl, C, batch=range(b, b + 1))
+L = int(W.prefix_lengths(wl, b + 1)[b])
+x = W.qkv(wl, b, L)
+u = W.uniforms(wl, b)[None]
+root = W.root_tokens(wl, b + 1)[b:b + 1]
+q = W.as_float(wl, x["q"])[None].astype(np.float64)
+kp = [W.as_float(wl, x["k_prefix"]).astype(np.float64)]
+vp = [W.as_float(wl, x["v_prefix"]).astype(np.float64)]
+kt = W.as_float(wl, x["k_tree"])[None].astype(np.float64)
+vt = W.as_float(wl, x["v_tree"])[None].astype(np.float64)
+mode = O.GREEDY if "greedy" in wl.accept else O.STOCH_POINT
+start = {start_at}
+while time.time() < start:
+    time.sleep(0.005)
+t0 = time.time()
+done = 0
+while time.time() - t0 < {budget}:
+    tree = O.build_tree(cfg, draft, rmap, root)
+    mask, pos = O.mask_posids(tree.flat_parent, tree.flat_depth, np.array([L]))
+    O.tree_attention(q, kp, vp, kt, vt, mask, wl.d ** -0.5)
+    O.verify_accept(cfg, mode, tree.flat_tok, tree.flat_parent, tree.flat_node, target, rmap, uniforms=u)
+    done += 1
+print(json.dumps({{"steps": done, "t0": t0, "t1": time.time(), "late": t0 - start}}))
+"""
+
+
+def host_cores() -> int:
+    """Cores this process may run on (the box's count is read, not assumed)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_baseline_all_cores(name, budget_s=10.0, lead_s=None):
+    """The oracle on every host core at once: one process per core, one BLAS
+    thread each, each timing full steps of its own sequence from a common
+    wall-clock start; throughput = all completed steps / (last end - start)."""
+    P = host_cores()
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[k] = "1"
+    lead = lead_s if lead_s is not None else 20.0 + 0.5 * P  # input generation before the common start
+    start_at = time.time() + lead
+    procs = [subprocess.Popen([sys.executable, "-c", ORACLE_WORKER.format(root=ROOT, name=name, worker=w,
+                                                                           start_at=start_at, budget=budget_s)],
+                              stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True, env=env)
+             for w in range(P)]
+    res = []
+    for pr in procs:
+        out, err = pr.communicate(timeout=900)
+        if pr.returncode != 0:
+            raise RuntimeError("oracle worker failed:\n" + err[-2000:])
+        res.append(json.loads(out.strip().splitlines()[-1]))
+    steps = sum(r["steps"] for r in res)
+    span = max(r["t1"] for r in res) - start_at
+    late = max(r["late"] for r in res)
+    return {"value": steps / span, "unit": "steps/s", "cores": P, "kind": "oracle",
+            "sample": f"{steps} full steps of the {name} workload (batch 1) on {P} processes, one per core, "
+                      f"one BLAS thread each, {budget_s:.0f} s from a common start; input generation untimed",
+            "seconds": round(span, 3), "late_start_s": round(late, 3)}
+
+
 def oracle_baseline(name, budget_s=15.0, max_steps=80):
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
@@ -389,6 +462,15 @@ def run_gpu(args):
     hbm_peak, bf16_peak, peak_src = _peaks()
     achieved = attn_b / (attn_us * 1e-6) / 1e9
 
+    # ---- attention alone at the other target shapes (batch 1) ----
+    shapes = []
+    if not args.no_attn_shapes:
+        for name, L in ATTN_SHAPES:
+            try:
+                shapes.append(time_attention_shape(name, L, stream, K, hbm_peak, bf16_peak))
+            except Exception as ex:  # report, keep the main line
+                shapes.append({"workload": name, "prefix": L, "error": str(ex)[:300]})
+
     # ---- KV commit of the accepted paths (the step after acceptance), timed alone ----
     commit = time_kv_commit(st, sets[0], wl, cfg, prefix, stream, K)
 
@@ -419,6 +501,7 @@ def run_gpu(args):
                    "cuda_graphs": bool(graphs), "parallelism": f"replicas x{world}"},
         "tree_attention": {"us_per_launch": round(attn_us, 3), "GBps": round(achieved, 1),
                            "pct_of_8TBps": round(100 * achieved / 8000.0, 2), "bytes": attn_b},
+        "tree_attention_shapes": shapes,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4),
                      "traffic": args.traffic if args.traffic is not None else
@@ -433,7 +516,12 @@ def run_gpu(args):
     }
     if rank == 0 and not args.no_cpu_baseline:
         try:
-            out["cpu_baseline"] = oracle_baseline(wl.name)
+            one = oracle_baseline(wl.name)
+            try:
+                allc = oracle_baseline_all_cores(wl.name)
+                out["cpu_baseline"] = dict(allc, one_core=one)
+            except Exception as ex:  # keep the one-core figure
+                out["cpu_baseline"] = dict(one, all_cores_error=str(ex)[:300])
         except Exception as ex:  # report, never hide
             out["cpu_baseline"] = {"error": str(ex)[:300]}
     if world > 1:
@@ -441,6 +529,81 @@ def run_gpu(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+def attention_flops(wl, prefix_lens):
+    """FLOPs one et_tree_attention launch performs as the kernel tiles it: Q K^T
+    and P V of every row over its prefix and the N tree rows (2 x 2 x d each)."""
+    return sum(4 * wl.N * wl.Hq * wl.d * (int(L) + wl.N) for L in prefix_lens)
+
+
+# further attention shapes timed in the same run (batch 1): the two HBM-bound
+# shapes at prefix 4096 and the tensor-core-bound GQA shape
+ATTN_SHAPES = (("llama2-7b", 4096), ("llama2-13b", 4096), ("llama2-70b", 8192))
+
+
+def time_attention_shape(name, prefix, stream, K, hbm_peak, bf16_peak):
+    """et_tree_attention alone at one more shape, batch 1: one tree (from the
+    shape's own seeded draft logits) gives the mask; Q/K/V rotate over sets
+    whose combined size exceeds L2; CUDA events around a graph of K launches."""
+    import dataclasses
+    import numpy as np
+    import torch
+    from speculative_decoding_eagle_gb300 import step as S
+    from speculative_decoding_eagle_gb300 import workloads as W
+    wl = W.WORKLOADS[name].with_(B=1, prefix=prefix, ragged=False)
+    st = S.VerifyStep(wl)
+    base = S.to_device(wl, S.host_inputs(wl, st.C))
+    st.run(base, stream=stream)  # the mask of a real tree
+    stream.synchronize()
+    nb = attention_bytes(wl, [prefix])
+    R = max(2, int(np.ceil(2 * L2_BYTES / nb)) + 1)
+    sets = [base]
+    kind = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    for r in range(1, R):
+        x = W.qkv(wl, r, prefix)
+
+        def up(a):
+            a = np.ascontiguousarray(a)
+            if wl.dtype == "bf16":
+                return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+            return torch.from_numpy(a).cuda()
+        sets.append(dataclasses.replace(base, q=up(x["q"])[None], k_prefix=up(x["k_prefix"].reshape(-1, wl.d)),
+                                        v_prefix=up(x["v_prefix"].reshape(-1, wl.d)), k_tree=up(x["k_tree"])[None],
+                                        v_tree=up(x["v_tree"])[None]))
+    with torch.cuda.stream(stream):
+        for r in range(R):
+            st.attention(sets[r], stream=stream)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(K):
+            st.attention(sets[i % R], stream=stream)
+    g.replay()
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / K
+    gbs = nb / (us * 1e-6) / 1e9
+    fl = attention_flops(wl, [prefix])
+    tfs = fl / (us * 1e-6) / 1e12
+    out = {"workload": name, "batch": 1, "prefix": prefix, "Hq": wl.Hq, "Hkv": wl.Hkv, "N": wl.N,
+           "splits": E_splits(st), "us_per_launch": round(us, 3), "bytes": nb, "GBps": round(gbs, 1),
+           "pct_of_8TBps": round(100.0 * gbs / 8000.0, 2), "frac_hbm": round(gbs / hbm_peak, 4),
+           "flops": fl, "TFLOPs": round(tfs, 1), "frac_bf16": round(tfs / bf16_peak, 4),
+           "bound": "tensor" if fl / nb > 300 else "hbm", "status": int(st.dev_status.item())}
+    del sets, base, g
+    torch.cuda.empty_cache()
+    return out
+
+
+def E_splits(st):
+    from speculative_decoding_eagle_gb300 import binding as E
+    return E.et_tree_attention_splits(st.shape)
 
 
 def time_kv_commit(st, inp, wl, cfg, prefix, stream, K):
@@ -746,6 +909,7 @@ def main():
     ap.add_argument("--sets", type=int, default=0)
     ap.add_argument("--eager", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-attn-shapes", action="store_true", help="skip timing attention at the other target shapes")
     ap.add_argument("--clocks-csv", default="", help="also write the raw nvidia-smi samples of the timed region here")
     ap.add_argument("--splits-sweep", default="", help="comma-separated KV split counts: time attention alone at each")
     ap.add_argument("--traffic", type=float, default=None,
