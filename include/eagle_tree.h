@@ -295,13 +295,16 @@ et_status et_tree_rerank_mask(const et_tree_cfg *cfg, et_tree *tree, const int32
  *
  * When V <= 32768 and the B * max_l(m_l) thread-block clusters (one per
  * sequence and frontier slot, ceil(V / 4096) blocks each) fit on the GPU at
- * once, the D layers are ONE kernel launch: each cluster expands its
- * frontier slot in every layer; it waits on the device (a bounded spin on a
- * per-layer counter) until every row of the previous layer has written its
- * children, then picks the frontier itself.  The rerank with the mask and
- * positions follows as a second launch (et_tree_rerank_mask's kernel).
- * Otherwise it issues the D + 1 launches of the per-layer calls (same
- * results).  et_tree_build_launches(cfg) says which.
+ * once, the tree is ONE kernel launch: each cluster expands its frontier
+ * slot in every layer; it waits on the device (a bounded spin on a per-layer
+ * counter) until every row of the previous layer has written its children,
+ * then picks the frontier itself.  One more cluster per sequence merges
+ * each finished layer into the running top-n and, after the last layer,
+ * writes the flat tree, mask and positions -- when n + max_l(m_l * k) <= 256;
+ * otherwise the rerank follows as a second launch (et_tree_rerank_mask's
+ * kernel).  Past one cluster, or when the clusters do not fit, it issues the
+ * D + 1 launches of the per-layer calls (same results).
+ * et_tree_build_launches(cfg) says which.
  *
  * mask, posids, prefix_len: as in et_tree_rerank_mask; all three null skips
  *               the mask and positions (then it ends like et_tree_rerank).
@@ -317,7 +320,7 @@ et_status et_tree_build(const et_tree_cfg *cfg, const float *logits, int64_t row
                         const int32_t *row_of_node, et_tree *tree, const int32_t *prefix_len,
                         uint64_t *mask, int32_t *posids, int32_t *dev_status,
                         void *ws, size_t ws_bytes, et_stream_t stream);
-/* Kernel launches et_tree_build makes for cfg on the current device: 2, or D + 1. */
+/* Kernel launches et_tree_build makes for cfg on the current device: 1, 2 or D + 1. */
 int32_t et_tree_build_launches(const et_tree_cfg *cfg);
 
 /*
@@ -362,8 +365,9 @@ int64_t et_set_wait_limit(int64_t cycles);
  *               rows' lines from L2 once merged.  Calls that run at the same
  *               time need separate workspaces.
  * Accumulation is fp32; P is rounded to the input dtype before P.V.
- * tcgen05 path: at most 8 splits (one thread-block cluster); a bounded wait
- * that expires sets ET_DEV_TIMEOUT in dev_status and leaves that tile's
+ * tcgen05 path: the splits of a row tile run as one thread-block cluster,
+ * at most 16 (the heuristic picks at most 8, the portable size); a bounded
+ * wait that expires sets ET_DEV_TIMEOUT in dev_status and leaves that tile's
  * output undefined.
  */
 et_status et_tree_attention(const et_attn_shape *shape,

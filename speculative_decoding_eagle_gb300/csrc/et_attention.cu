@@ -501,6 +501,7 @@ static bool make_plan(const et_attn_shape *s, AttnPlan *p) {
       if (S <= 0) {
         S = (int)((17LL * sm_count()) / (10LL * base));
         if (S > cap) S = cap;
+        if (S > 8) S = 8;  // the portable cluster size (larger clusters are an explicit choice)
         if (S < 1) S = 1;
       }
       if (S > kTcMaxSplits) S = kTcMaxSplits;

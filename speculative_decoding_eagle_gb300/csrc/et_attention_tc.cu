@@ -58,7 +58,7 @@ constexpr uint32_t kOffMisc = kOffBar + 256;
 constexpr uint32_t kOffMlOwn = kOffMisc + 256;
 constexpr uint32_t kOffMlRecv = kOffMlOwn + kTcRows * 8;
 constexpr int kDsmMaxRows = 64;     // real rows of a tile merged through DSMEM
-constexpr int kDsmMaxSlots = 80;    // S * per for S >= 2, per = ceil(rows / S) rounded up to even (<= 72)
+constexpr int kDsmMaxSlots = 96;    // S * per for 2 <= S <= 16, per = ceil(rows / S) rounded up to even (<= 90)
 constexpr uint32_t kMlRecvBytes = kDsmMaxSlots * 8;
 constexpr uint32_t kSmemBytes = kOffMlRecv + kMlRecvBytes + 1024;  // + slack for 1024-byte alignment
 // partial rows: own rows staged in the V stages, received rows in the Q and K space
@@ -699,6 +699,20 @@ bool make_map_q(CUtensorMap *m, const void *base, int G, int Hkv, long long toke
 
 cudaError_t set_smem_attr() { return et_smem_attr((const void *)k_attn_tc, (int)kSmemBytes); }
 
+// clusters of more than 8 blocks (the portable limit) need an opt-in per
+// device; thread-safe
+cudaError_t allow_big_clusters() {
+  static std::mutex mu;
+  static int done[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute((const void *)k_attn_tc, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) done[dev] = 1;
+  return e;
+}
+
 }  // namespace
 
 et_status tc_attention_launch(const TcLaunch &a, cudaStream_t stream) {
@@ -721,6 +735,7 @@ et_status tc_attention_launch(const TcLaunch &a, cudaStream_t stream) {
   else m_q = m_kt;  // not read
   if (!ok) return ET_ERR_INVALID_ARG;
   if (set_smem_attr() != cudaSuccess) return ET_ERR_CUDA;
+  if (a.S > 8 && allow_big_clusters() != cudaSuccess) return ET_ERR_CUDA;
   return et_launch(k_attn_tc, dim3(a.S, a.Hkv * a.MT, a.B), dim3(kThreads), kSmemBytes, stream, a.S > 1 ? a.S : 0,
                    m_kp, m_vp, m_kt, m_vt, m_q, la);
 }

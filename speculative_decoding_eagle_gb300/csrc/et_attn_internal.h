@@ -31,7 +31,7 @@ struct TcLaunch {
 constexpr int kTcRows = 128;   // query rows per tile (TMEM lanes)
 constexpr int kTcKeys = 64;    // keys per K/V tile
 constexpr int kTcDim = 128;    // head dim of the tcgen05 path
-constexpr int kTcMaxSplits = 8;  // KV splits of one row tile = one thread-block cluster (portable size)
+constexpr int kTcMaxSplits = 16;  // KV splits of one row tile = one thread-block cluster (past 8: non-portable size)
 
 // workspace bytes of the tcgen05 path: the split merge's partial rows and
 // (max, sum) pairs (0 for one split)

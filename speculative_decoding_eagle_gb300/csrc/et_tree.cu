@@ -773,6 +773,11 @@ struct BuildArgs {
   int32_t *dev_status;
   unsigned int *layer_cnt;  // [B][kMaxDepth] rows of each layer whose children are written; back to 0 at the end
   long long wait_cycles;    // bound of a wait for the previous layer (et_set_wait_limit)
+  int rerank_here;          // one more cluster per sequence reranks the tree inside this launch
+  int n, N;                 // kept nodes, flat rows
+  const int32_t *prefix_len;
+  uint64_t *mask;           // nullable: no mask and positions
+  int32_t *posids;
 };
 
 __device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p) {
@@ -789,18 +794,137 @@ struct BuildPick {
   int s_node;
 };
 
+// The rerank inside k_tree_build, by the leader block of one more cluster per
+// sequence: as each layer completes, its children are merged into the
+// running top-n (top-n of a union = top-n of the running top-n and the new
+// candidates; rank keys are unique, so the result is exact), each key ranked
+// by counting; after the last layer the kept ids, sorted by id, become flat
+// rows 1..n (reranking phase of the EAGLE-2 article), with the mask and the
+// positions.  The merges run beside the layers, off their critical path.
+struct RerankRoleSmem {
+  unsigned long long ks[256];        // running top-n, then the layer's candidates
+  unsigned long long keep[kMaxN];    // the new running top-n, by rank
+  int ids[kMaxN];                    // kept candidate ids
+  short flat_of[kMaxC];              // flat row of each kept id, -1 otherwise
+  int row_par[kMaxN], row_dep[kMaxN];
+};
+
+__device__ void rerank_role(const BuildArgs &a, int b, unsigned int *cnt, RerankRoleSmem &sm) {
+  const int t = threadIdx.x;
+  const int C = a.C, n = a.n, N = a.N;
+  int nk = 0;  // keys in the running top-n
+  for (int layer = 0; layer < a.D; ++layer) {
+    const int m_l = a.expanded[layer], width = m_l * a.k, base_next = a.base[layer + 1];
+    if (t == 0 && ld_acquire_u32(cnt + layer) < (unsigned)m_l) {
+      const long long t0 = clock64();
+      while (ld_acquire_u32(cnt + layer) < (unsigned)m_l) {
+        if (clock64() - t0 > a.wait_cycles) {
+          flag_status(a.dev_status, ET_DEV_TIMEOUT);
+          break;
+        }
+      }
+    }
+    __syncthreads();
+    const int P = nk + width;  // <= 256 (checked by the host)
+    unsigned long long mine = ~0ull;
+    if (t < nk) {
+      mine = sm.keep[t];
+    } else if (t < P) {
+      const int id = base_next + (t - nk);
+      mine = rank_key(ld_cg(a.tree.cand_key + (long long)b * C + id), id);
+    }
+    __syncthreads();  // every running key read before ks is rewritten
+    sm.ks[t] = mine;
+    __syncthreads();
+    if (t < P) {
+      int below = 0;
+      for (int j = 0; j < P; ++j) below += sm.ks[j] < mine ? 1 : 0;
+      if (below < n) sm.keep[below] = mine;  // ranks are unique: the running list stays sorted
+    }
+    nk = P < n ? P : n;
+    __syncthreads();
+  }
+  // kept ids -> flat rows 1..n in ascending id order
+  for (int i = t; i < C; i += kClThreads) sm.flat_of[i] = -1;
+  if (t < kMaxN) { sm.row_par[t] = 0; sm.row_dep[t] = 0; }
+  if (t < nk) sm.ids[t] = (int)(sm.keep[t] & ((1ull << kIdBits) - 1));
+  __syncthreads();
+  int myrow = -1, myid = -1;
+  if (t < nk) {
+    myid = sm.ids[t];
+    int before = 0;
+    for (int j = 0; j < nk; ++j) before += sm.ids[j] < myid ? 1 : 0;
+    myrow = 1 + before;
+    sm.flat_of[myid] = (short)myrow;
+  }
+  __syncthreads();
+  const long long fo = (long long)b * N;
+  int bad = 0;
+  if (t < nk && myrow < N) {
+    const int tok = ld_cg(a.tree.cand_tok + (long long)b * C + myid);
+    const int p = ld_cg(a.tree.cand_parent + (long long)b * C + myid);
+    int prow = 0;
+    if (p >= 0) {
+      prow = p < C ? sm.flat_of[p] : -1;
+      if (prow < 0) { bad = 1; prow = 0; }
+    }
+    int depth = 1;
+    for (int l = 1; l <= a.D; ++l)
+      if (myid >= a.base[l]) depth = l;
+    a.tree.flat_node[fo + myrow] = myid;
+    a.tree.flat_tok[fo + myrow] = tok;
+    a.tree.flat_parent[fo + myrow] = prow;
+    a.tree.flat_depth[fo + myrow] = depth;
+    sm.row_par[myrow] = prow;
+    sm.row_dep[myrow] = depth;
+  }
+  if (bad) flag_status(a.dev_status, ET_DEV_DISCONNECTED);
+  if (t == 0) {
+    a.tree.flat_node[fo] = -1;
+    a.tree.flat_tok[fo] = a.tree.root_tok ? a.tree.root_tok[b] : -1;
+    a.tree.flat_parent[fo] = -1;
+    a.tree.flat_depth[fo] = 0;
+    sm.row_par[0] = -1;
+    sm.row_dep[0] = 0;
+    for (int l = 0; l < a.D; ++l) cnt[l] = 0u;  // every wait of this sequence is over: re-arm for the next call
+  }
+  if (!a.mask) return;
+  __syncthreads();
+  const int W = (N + 63) >> 6;
+  if (t < N) {
+    uint64_t w0, w1;
+    const bool ok = ancestor_bits(sm.row_par, t, w0, w1);
+    uint64_t *mrow = a.mask + ((long long)b * N + t) * W;
+    mrow[0] = w0;
+    if (W > 1) mrow[1] = w1;
+    a.posids[(long long)b * N + t] = a.prefix_len[b] + sm.row_dep[t];
+    if (!ok) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
+  }
+}
+
+union BuildSmem {
+  ExpandClSmem e;
+  RerankRoleSmem r;
+};
+
 __global__ void __launch_bounds__(kClThreads) k_tree_build(BuildArgs a) {
-  __shared__ ExpandClSmem sh_e;
+  __shared__ BuildSmem sh;
   __shared__ BuildPick pk;
+  ExpandClSmem &sh_e = sh.e;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int R = gridDim.x;  // CTAs per row = cluster size
   const int q = (int)cl_rank();
-  const int b = blockIdx.y / a.slots, s = blockIdx.y - b * a.slots;
+  const int per_seq = a.slots + (a.rerank_here ? 1 : 0);
+  const int b = blockIdx.y / per_seq, s = blockIdx.y - b * per_seq;
   const int k = a.k;
   unsigned int *cnt = a.layer_cnt + (long long)b * kMaxDepth;
   cl_arrive_relaxed();  // phase 0: this block has started (waited on before any remote store)
   pdl_wait();           // the previous kernel in the stream has completed
   pdl_trigger();        // every block of this grid is resident before a dependent can launch
+  if (s == a.slots) {   // the rerank cluster: its leader alone works
+    if (q == 0) rerank_role(a, b, cnt, sh.r);
+    return;
+  }
 
   for (int layer = 0; layer < a.D; ++layer) {
     const int m_l = a.expanded[layer];
@@ -940,9 +1064,10 @@ __global__ void __launch_bounds__(kClThreads) k_tree_build(BuildArgs a) {
       if (t == 0) {
         __threadfence();
         const bool last = atomicAdd(cnt + layer, 1u) == (unsigned)(m_l - 1);  // the next layer may count this row
-        // the sequence's last row of the final layer: every wait of this
-        // sequence is over, re-arm the counters for the next call
-        if (last && layer + 1 == a.D)
+        // the sequence's last row of the final layer (when no rerank cluster
+        // follows the layers): every wait of this sequence is over, re-arm
+        // the counters for the next call
+        if (last && layer + 1 == a.D && !a.rerank_here)
           for (int l = 0; l < a.D; ++l) cnt[l] = 0u;
       }
     }
@@ -1141,10 +1266,14 @@ extern "C" et_status et_tree_build(const et_tree_cfg *cfg, const float *logits, 
   ET_RETURN_IF((mask || posids) && (!mask || !posids || !prefix_len || !et_aligned(mask, 8)), ET_ERR_INVALID_ARG);
   const TreeWs w = tree_ws_layout(cfg);
   ET_RETURN_IF(!ws || ws_bytes < w.total || !et_aligned(ws, 256), ET_ERR_WORKSPACE);
-  int slots = 1;
-  for (int l = 0; l < cfg->depth; ++l) slots = g.expanded[l] > slots ? g.expanded[l] : slots;
+  int slots = 1, widest = 0;
+  for (int l = 0; l < cfg->depth; ++l) {
+    slots = g.expanded[l] > slots ? g.expanded[l] : slots;
+    widest = g.expanded[l] * cfg->topk > widest ? g.expanded[l] * cfg->topk : widest;
+  }
   const int R = (cfg->V + kClSpan - 1) / kClSpan;
-  const long long clusters = (long long)cfg->B * slots;
+  const bool rerank_here = cfg->n + widest <= kClThreads;  // every merge ranks at most one key per thread
+  const long long clusters = (long long)cfg->B * (slots + (rerank_here ? 1 : 0));
   if (cfg->V <= kClMaxV && clusters <= 65535 && tree_build_fits((int)clusters, R)) {
     BuildArgs a;
     a.logits = logits;
@@ -1159,9 +1288,15 @@ extern "C" et_status et_tree_build(const et_tree_cfg *cfg, const float *logits, 
     unsigned char *base = static_cast<unsigned char *>(ws);
     a.layer_cnt = reinterpret_cast<unsigned int *>(base) + w.rows + cfg->B;  // the per-layer counters
     a.wait_cycles = et_wait_limit_cycles();
+    a.rerank_here = rerank_here ? 1 : 0;
+    a.n = cfg->n;
+    a.N = cfg->n + 1;
+    a.prefix_len = prefix_len;
+    a.mask = mask;
+    a.posids = posids;
     const et_status st = et_launch(k_tree_build, dim3(R, (unsigned)clusters, 1), dim3(kClThreads, 1, 1), 0,
                                    (cudaStream_t)stream, R, a);
-    if (st != ET_OK) return st;
+    if (st != ET_OK || rerank_here) return st;
     return launch_rerank(cfg, tree, dev_status, prefix_len, mask, posids, stream);
   }
   for (int l = 0; l < cfg->depth; ++l) {
@@ -1175,11 +1310,15 @@ extern "C" et_status et_tree_build(const et_tree_cfg *cfg, const float *logits, 
 extern "C" int32_t et_tree_build_launches(const et_tree_cfg *cfg) {
   Geometry g;
   if (!make_geometry(cfg, &g)) return -1;
-  int slots = 1;
-  for (int l = 0; l < cfg->depth; ++l) slots = g.expanded[l] > slots ? g.expanded[l] : slots;
+  int slots = 1, widest = 0;
+  for (int l = 0; l < cfg->depth; ++l) {
+    slots = g.expanded[l] > slots ? g.expanded[l] : slots;
+    widest = g.expanded[l] * cfg->topk > widest ? g.expanded[l] * cfg->topk : widest;
+  }
   const int R = (cfg->V + kClSpan - 1) / kClSpan;
-  const long long clusters = (long long)cfg->B * slots;
-  if (cfg->V <= kClMaxV && clusters <= 65535 && tree_build_fits((int)clusters, R)) return 2;
+  const bool rerank_here = cfg->n + widest <= kClThreads;
+  const long long clusters = (long long)cfg->B * (slots + (rerank_here ? 1 : 0));
+  if (cfg->V <= kClMaxV && clusters <= 65535 && tree_build_fits((int)clusters, R)) return rerank_here ? 1 : 2;
   return cfg->depth + 1;
 }
 

@@ -107,14 +107,14 @@ def test_attention_argument_checks(lib):
     assert sz > 0
     assert call(shape(num_splits=4, impl=1), wsb=sz - 1) == E.ET_ERR_WORKSPACE
     assert lib.et_tree_attention_splits(ctypes.byref(shape(num_splits=4))) == 4
-    # the tcgen05 path: the splits of a tile form one cluster (at most 8) and merge through the
+    # the tcgen05 path: the splits of a tile form one cluster (at most 16) and merge through the
     # workspace: per split and 128-row tile, fp32 rows and a (max, sum) pair per row
     tc4 = lib.et_tree_attention_workspace_size(ctypes.byref(shape(num_splits=4, impl=2)))
     assert tc4 == 32 * 1 * 4 * 128 * (128 * 4 + 8)
     assert call(shape(num_splits=4, impl=2), ws=None) == E.ET_ERR_WORKSPACE
     assert call(shape(num_splits=4, impl=2), wsb=tc4 - 1) == E.ET_ERR_WORKSPACE
     assert lib.et_tree_attention_workspace_size(ctypes.byref(shape(num_splits=1, impl=2))) == 0
-    assert lib.et_tree_attention_splits(ctypes.byref(shape(num_splits=20, impl=2))) == 8
+    assert lib.et_tree_attention_splits(ctypes.byref(shape(num_splits=20, impl=2))) == 16
     assert lib.et_tree_attention_workspace_size(ctypes.byref(shape(num_splits=1))) == 0
     assert lib.et_tree_attention_splits(ctypes.byref(shape(dtype=E.ET_F32))) == 1
     # workspace: tiles x splits x rows-per-tile x d floats (+ counters and (max, sum) pairs)
@@ -239,6 +239,6 @@ def test_tree_build_argument_checks(lib):
     assert call(ws=FAKE + 16) == E.ET_ERR_WORKSPACE
     broken = E.TreeC(*([FAKE] * 6 + [None] + [FAKE] * 3))               # no flat_node array
     assert call(t=broken) == E.ET_ERR_INVALID_ARG
-    # past one cluster (V > 32768) the call issues the per-layer launches: D + 1 (else 2)
+    # past one cluster (V > 32768) the call issues the per-layer launches: D + 1 (else 1 or 2)
     assert lib.et_tree_build_launches(ctypes.byref(E.TreeCfgC(1, 50000, 4, 4, 4, 16, 1.0))) == 5
     assert lib.et_tree_build_launches(ctypes.byref(bad_cfg)) == -1

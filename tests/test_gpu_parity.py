@@ -263,9 +263,11 @@ ATTN_CASES = [
     (2, 20, 4, 2, 128, [100, 60], "bf16", 2, 128),  # static cache layout (head stride)
     (1, 128, 2, 2, 128, [257], "bf16", 0, 0),       # maximum N
     (2, 7, 4, 4, 128, [0, 0], "bf16", 0, 0),        # no prefix at all
-    (1, 61, 8, 8, 128, [4096], "bf16", 32, 0),      # many splits (8 on the tcgen05 path: one cluster)
+    (1, 61, 8, 8, 128, [4096], "bf16", 32, 0),      # many splits (16 on the tcgen05 path: one cluster)
     (1, 61, 8, 8, 128, [1000], "bf16", 5, 0),       # odd cluster size
     (1, 61, 2, 2, 128, [8192], "bf16", 7, 0),       # 7 splits of 129 key tiles
+    (1, 61, 4, 4, 128, [1024], "bf16", 9, 0),       # 9 splits (a non-portable cluster) of 17 key tiles
+    (2, 81, 16, 2, 128, [3000, 700], "bf16", 12, 0),  # 12 splits, GQA rows merged through L2
 ]
 
 
@@ -309,26 +311,23 @@ def test_tcgen05_and_mma_paths_agree_at_the_7b_shape():
 # ---------------------------------------------------------------------------
 # the whole tree in one launch (et_tree_build)
 # ---------------------------------------------------------------------------
-BUILD_CASES = [  # workload, B, n, V, expected launches (None: whatever fits)
-    ("tiny", 4, None, None, 2),
-    ("llama2-7b", 1, None, None, 2),
-    ("llama2-70b", 1, None, None, 2),
-    ("llama2-7b", 3, 100, None, None),
-    ("tiny", 2, None, 50000, 5),  # past one cluster: the per-layer launches
+BUILD_CASES = [  # workload, B, changed fields, expected launches (None: whatever fits)
+    ("tiny", 4, {}, 1),
+    ("llama2-7b", 1, {}, 1),
+    ("llama2-70b", 1, {}, 1),
+    ("llama2-7b", 3, {"n": 100}, None),
+    ("llama2-7b", 1, {"topk": 16, "m": 16}, 2),  # n + the widest layer > 256: the rerank as a second launch
+    ("tiny", 2, {"V": 50000}, 5),                # past one cluster: the per-layer launches
 ]
 
 
-@pytest.mark.parametrize("wl_name,B,n,V,launches", BUILD_CASES)
-def test_tree_build_matches_per_layer_path_and_oracle(wl_name, B, n, V, launches):
-    """et_tree_build (all layers in one launch, then the rerank) writes
-    exactly what D et_tree_expand calls and et_tree_rerank_mask write; twice
-    in a row (its per-layer counters must be back at zero for the second
-    call), and equal to the oracle's tree."""
-    wl = W.WORKLOADS[wl_name].with_(B=B)
-    if n is not None:
-        wl = wl.with_(n=n)
-    if V is not None:
-        wl = wl.with_(V=V)
+@pytest.mark.parametrize("wl_name,B,changes,launches", BUILD_CASES)
+def test_tree_build_matches_per_layer_path_and_oracle(wl_name, B, changes, launches):
+    """et_tree_build (all layers and the rerank in one launch, or the rerank
+    as a second launch) writes exactly what D et_tree_expand calls and
+    et_tree_rerank_mask write; twice in a row (its per-layer counters must be
+    back at zero for the second call), and equal to the oracle's tree."""
+    wl = W.WORKLOADS[wl_name].with_(B=B, **changes)
     one = S.VerifyStep(wl, per_layer=False)
     ref = S.VerifyStep(wl, per_layer=True)
     if launches is not None:

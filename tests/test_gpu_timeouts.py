@@ -70,7 +70,7 @@ def test_lm_head_wait_runs_out_then_next_call_is_exact():
 def test_tree_build_frontier_wait_runs_out_then_next_call_is_exact():
     wl = W.WORKLOADS["tiny"].with_(B=2)
     one = S.VerifyStep(wl, per_layer=False)
-    if E.et_tree_build_launches(one.cfg) != 2:
+    if E.et_tree_build_launches(one.cfg) not in (1, 2):
         pytest.skip("the clusters of the one-launch layers do not fit here")
     ref = S.VerifyStep(wl, per_layer=True)
     h = S.host_inputs(wl, one.C)
