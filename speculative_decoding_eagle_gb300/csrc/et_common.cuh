@@ -110,13 +110,12 @@ __device__ __forceinline__ double warp_sum_d(double v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
+// every lane gets the warp's smallest 64-bit value (two 32-bit reductions)
 __device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
-    v = w < v ? w : v;
-  }
-  return v;
+  const unsigned int hi = (unsigned int)(v >> 32);
+  const unsigned int mh = __reduce_min_sync(0xffffffffu, hi);
+  const unsigned int ml = __reduce_min_sync(0xffffffffu, hi == mh ? (unsigned int)v : 0xffffffffu);
+  return ((unsigned long long)mh << 32) | ml;
 }
 // warp-wide best (z desc, id asc); every lane gets the winner
 __device__ __forceinline__ void warp_best(float &z, int &id) {
@@ -210,9 +209,9 @@ __device__ __forceinline__ float exp_fast(float x) {
 }
 
 // ---- programmatic dependent launch ----
-// Every kernel of this library is launched with programmatic stream
-// serialization: it may start while the previous kernel in the stream is
-// still running.  pdl_wait() blocks until that kernel has completed and its
+// Every kernel of this library but the persistent tree build is launched with
+// programmatic stream serialization: it may start while the previous kernel
+// in the stream is still running.  pdl_wait() blocks until that kernel has completed and its
 // memory is visible, so it comes before the first global memory access;
 // pdl_trigger() lets the next kernel start launching (it still waits for
 // this one to complete before touching memory).  Triggering only after the
@@ -424,11 +423,12 @@ static inline cudaError_t et_smem_attr(const void *kernel, int bytes) {
   return cudaSuccess;
 }
 
-// Launch with programmatic stream serialization (and, when cluster_x > 0,
-// clusters of cluster_x blocks along x).
+// Launch with programmatic stream serialization (pdl) or as a plain stream-
+// ordered launch, and, when cluster_x > 0, in clusters of cluster_x blocks
+// along x.
 template <typename... KArgs, typename... Args>
-static inline et_status et_launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                                  int cluster_x, Args &&...args) {
+static inline et_status et_launch_ex(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t stream, int cluster_x, Args &&...args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -436,9 +436,11 @@ static inline et_status et_launch(void (*kern)(KArgs...), dim3 grid, dim3 block,
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   int n = 0;
-  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[n].val.programmaticStreamSerializationAllowed = 1;
-  ++n;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
   if (cluster_x > 0) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
     attr[n].val.clusterDim.x = (unsigned)cluster_x;
@@ -453,4 +455,9 @@ static inline et_status et_launch(void (*kern)(KArgs...), dim3 grid, dim3 block,
     return ET_ERR_CUDA;
   }
   return et_launch_status();
+}
+template <typename... KArgs, typename... Args>
+static inline et_status et_launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                  int cluster_x, Args &&...args) {
+  return et_launch_ex(true, kern, grid, block, smem, stream, cluster_x, static_cast<Args &&>(args)...);
 }

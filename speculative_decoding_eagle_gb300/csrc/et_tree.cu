@@ -574,14 +574,14 @@ struct ExpandRowArgs {
 // ---------------------------------------------------------------------------
 // expand, one thread-block cluster per expanded row (V <= 32768): CTA q of the
 // cluster owns logits [4096 q, 4096 q + 4096) (16 per thread).  Each warp
-// finds the exact top-k of its 512 logits; after one block barrier the block
-// selects its top-k from the 8 warp lists (pairwise rank counting over all
-// threads), sums exp(z - block max) and stores both straight into the
-// leader's (rank 0) shared memory; after one cluster barrier the leader
-// selects the row's top-k from the R block lists and writes the children.
-// The last leader of a sequence then picks the next frontier among the
-// first m children of every row.  Spreading a row over up to 8 SMs gives the
-// load 8x the memory parallelism of one block per row.
+// finds the exact top-k of its 512 logits and their (max, sum of exp) and
+// stores both straight into the leader's (rank 0) shared memory; after one
+// cluster barrier the leader's first warp merges the 8R sorted warp lists
+// into the row's top-k, normalises, and writes the children.  The last row
+// of a sequence then picks the next frontier among the first m children of
+// every row.  Spreading a row over up to 8 SMs gives the load 8x the memory
+// parallelism of one block per row; keeping every step after the load inside
+// one warp (no block-wide select) keeps the chain short.
 // ---------------------------------------------------------------------------
 constexpr int kClThreads = 256;
 constexpr int kClWarps = kClThreads / 32;
@@ -589,28 +589,257 @@ constexpr int kClVec = 4;
 constexpr int kClSpan = kClThreads * 4 * kClVec;   // 4096 logits per CTA
 constexpr int kClMaxCtas = 8;
 constexpr int kClMaxV = kClSpan * kClMaxCtas;      // 32768
-constexpr int kWarpCand = 64;                      // keys a warp ranks by counting
+constexpr int kClLists = kClMaxCtas * kClWarps;    // warp lists of one row
 
+// ---- warp-level selection ----
+__device__ __forceinline__ unsigned int f32_ord(float x) {  // ascending with x (no NaN)
+  const unsigned int u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float ord_f32(unsigned int o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+__device__ __forceinline__ float warp_max_f(float x) { return ord_f32(__reduce_max_sync(0xffffffffu, f32_ord(x))); }
+__device__ __forceinline__ float warp_min_f(float x) { return ord_f32(__reduce_min_sync(0xffffffffu, f32_ord(x))); }
+// exclusive prefix sum over the warp of c, 0 <= c < 2^BITS
+template <int BITS>
+__device__ __forceinline__ int warp_excl_prefix(int c) {
+  unsigned int lt;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
+  int pos = 0;
+#pragma unroll
+  for (int bit = 0; bit < BITS; ++bit) pos += __popc(__ballot_sync(0xffffffffu, (c >> bit) & 1) & lt) << bit;
+  return pos;
+}
+// how many of cand[0 .. nc) are below mine (broadcast reads, eight independent per round)
+__device__ __forceinline__ int count_below(const unsigned long long *cand, int nc, unsigned long long mine) {
+  int r = 0, j = 0;
+  for (; j + 8 <= nc; j += 8) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) r += cand[j + u] < mine ? 1 : 0;
+  }
+  for (; j < nc; ++j) r += cand[j] < mine ? 1 : 0;
+  return r;
+}
+// cand[0 .. nc) (nc <= 32, distinct) -> lane r < n returns the r-th smallest, other lanes ~0
+__device__ __forceinline__ unsigned long long warp_rank_small(unsigned long long *cand, int nc, int n) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+  const unsigned long long mine = lane < nc ? cand[lane] : ~0ull;
+  const int r = count_below(cand, nc, mine);
+  __syncwarp();
+  if (lane < nc && r < n) cand[r] = mine;
+  __syncwarp();
+  const unsigned long long out = lane < n ? cand[lane] : ~0ull;
+  __syncwarp();
+  return out;
+}
+
+// The warp's best values at or above tau, at most k of them (value desc,
+// id asc), as ascending (value, id) keys: lane r < n returns the r-th, the
+// other lanes ~0.  v: sanitised values (no NaN), id_of(e): the id of the
+// lane's e-th value (distinct over the warp); k <= 32; cand: 32 keys of warp
+// scratch; n: how many are returned.  Usually none or a few values reach tau: they are ranked by
+// counting; more than 32 (ties, or a warp holding many of the row's best
+// values) take k rounds of a warp argmin, whose k keys all reach tau then.
+template <int NV, typename IdOf>
+__device__ __forceinline__ unsigned long long warp_best_at_least(const float (&v)[NV], IdOf id_of, float tau, int k,
+                                                                 unsigned long long *cand, int &n) {
+  static_assert(NV <= 31, "a lane's count fits 5 bits");
+  const int lane = threadIdx.x & 31;
+  unsigned int msk = 0u;
+#pragma unroll
+  for (int e = 0; e < NV; ++e) msk |= (v[e] >= tau ? 1u : 0u) << e;
+  const int c = __popc(msk);
+  const int nc = (int)__reduce_add_sync(0xffffffffu, (unsigned int)c);
+  if (nc == 0) {
+    n = 0;
+    return ~0ull;
+  }
+  if (nc <= 32) {
+    int pos = warp_excl_prefix<5>(c);
+#pragma unroll
+    for (int e = 0; e < NV; ++e)
+      if ((msk >> e) & 1u) cand[pos++] = zid_key(v[e], id_of(e));
+    n = nc < k ? nc : k;
+    return warp_rank_small(cand, nc, n);
+  }
+  unsigned long long out = ~0ull, lb = ~0ull;
+  unsigned int used = 0u;
+#pragma unroll
+  for (int e = 0; e < NV; ++e) {
+    const unsigned long long x = zid_key(v[e], id_of(e));
+    lb = x < lb ? x : lb;
+  }
+  for (int r = 0; r < k; ++r) {
+    const unsigned long long m = warp_min_u64(lb);
+    if (lane == r) out = m;
+    if (lb == m) {
+      lb = ~0ull;
+#pragma unroll
+      for (int e = 0; e < NV; ++e) {
+        const unsigned long long x = zid_key(v[e], id_of(e));
+        if (x == m) used |= 1u << e;
+        if (!((used >> e) & 1u) && x < lb) lb = x;
+      }
+    }
+  }
+  __syncwarp();
+  n = k;
+  return out;
+}
+
+// Shared memory of one expanding CTA.  Every CTA holds every warp's (max,
+// sum) pair of the row (by layer parity: a pair of the next layer may land
+// while the leader still reads this one); the leader also holds each warp's
+// candidates and their count.
 struct ExpandClSmem {
-  unsigned long long cand[kClWarps][kWarpCand];
-  unsigned long long wl[kClWarps * kMaxTopk];    // warp w's sorted top-k at w * k
-  unsigned long long gl[kClMaxCtas * kMaxTopk];  // leader: CTA q's top-k at q * k
-  float2 gms[kClMaxCtas];                         // leader: (max, sum) of each CTA
-  unsigned long long fl[kMaxM * kMaxTopk];       // last leader: frontier candidates
-  float wsum[kClWarps];
-  int sel[kMaxM];
-  int last;
+  float2 pairs[2][kClLists];                      // (max, sum of exp) of warp w of CTA q at 8 q + w
+  unsigned long long lists[kClLists * kMaxTopk];  // leader: warp (q, w)'s candidates, ascending, at (8 q + w) * k
+  int counts[kClLists];                           // leader: how many
+  unsigned long long cand[kClWarps][32];          // per-warp selection scratch
 };
+
+__device__ __forceinline__ void cl_st_s32(uint32_t addr, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// One row's logits in the CTA's registers: 16 per thread, float4 loads
+// when the row is 16-byte aligned; ids >= V (and a missing row) are -inf.
+__device__ __forceinline__ void load_row_span(const float *zrow, int base, int V, int vec4, float (&v)[4 * kClVec]) {
+  const int t = threadIdx.x;
+#pragma unroll
+  for (int u = 0; u < kClVec; ++u) {
+    const int e0 = base + u * kClThreads * 4 + t * 4;
+    if (zrow && vec4 && e0 + 3 < V) {
+      const float4 f = __ldcs(reinterpret_cast<const float4 *>(zrow + e0));
+      v[4 * u] = f.x; v[4 * u + 1] = f.y; v[4 * u + 2] = f.z; v[4 * u + 3] = f.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[4 * u + j] = (zrow && e0 + j < V) ? __ldcs(zrow + e0 + j) : -INFINITY;
+    }
+  }
+}
+
+// Every warp of every CTA of the row's cluster (EAGLE-2 article, expansion
+// phase: the top-k children of a node by draft confidence).  1: sanitise its
+// 512 logits; their max and sum of exp go to every CTA of the cluster (the
+// caller has completed the previous cluster phase: every block has started,
+// or every block is done with the previous layer).  2: after one cluster barrier
+// every warp takes, from the R x 8 warp maxima, the k-th largest lane
+// maximum (each lane holds two warps' maxima), tau: k distinct values of the
+// row reach it, so only values >= tau can be among the row's top k.  3: each
+// warp sends its best values >= tau (at most k, ascending) to the leader.
+// The caller then arrives on the barrier that releases these stores.
+__device__ __forceinline__ void row_warp_part(float (&v)[4 * kClVec], int base, int V, int k, int par, ExpandClSmem &sh,
+                                              int &flag) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int q = (int)cl_rank(), R = (int)gridDim.x;
+  float best = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < kClVec; ++u) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = 4 * u + j, id = base + u * kClThreads * 4 + t * 4 + j;  // ids >= V are padding (-inf)
+      if (id < V) v[e] = sanitize_logit(v[e], flag);
+      best = fmaxf(best, v[e]);
+    }
+  }
+  const float Mw = warp_max_f(best);
+  float sum = 0.f;
+  if (Mw > -INFINITY) {
+#pragma unroll
+    for (int e = 0; e < 4 * kClVec; ++e) sum += exp_fast(v[e] - Mw);
+  }
+  sum = warp_sum(sum);
+  const int list = q * kClWarps + warp;
+  if (lane < R) cl_st_f32x2(cl_map(&sh.pairs[par][list], (uint32_t)lane), Mw, sum);
+  cl_arrive();
+  cl_wait();  // every warp's pair is in every block
+  const int nl = R * kClWarps;
+  const float lm = fmaxf(lane < nl ? sh.pairs[par][lane].x : -INFINITY, lane + 32 < nl ? sh.pairs[par][lane + 32].x : -INFINITY);
+  int above = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) above += __shfl_sync(0xffffffffu, lm, j) > lm ? 1 : 0;
+  const float tau = warp_min_f(above < k ? lm : INFINITY);
+  int n = 0;
+  const unsigned long long key = warp_best_at_least<4 * kClVec>(
+      v, [&](int e) { return (unsigned int)(base + (e >> 2) * kClThreads * 4 + t * 4 + (e & 3)); }, tau, k,
+      sh.cand[warp], n);
+  if (lane < n) cl_st_u64(cl_map(&sh.lists[list * k + lane], 0), key);
+  if (lane == 0) cl_st_s32(cl_map(&sh.counts[list], 0), n);
+}
+
+// The leader's first warp, once every warp's candidates have landed: the
+// row's normaliser (log-softmax, from the warp pairs) and its top-k children
+// with their path keys (EAGLE-2 article: expansion phase; the value of a
+// path is the product of confidences, here a sum of fixed-point log-probs).
+// The candidates number at least k (every warp among the k holding the
+// largest maxima sends its maximum); a few more usually: ranked by counting.
+// More than 32: k rounds of the smallest list head.  nl: warp lists of the
+// row (8 R).
+__device__ __forceinline__ void row_leader_part(ExpandClSmem &sh, int par, int nl, int k, int V, const et_tree &tree,
+                                                long long o0, int parent, long long pkey) {
+  const int lane = threadIdx.x & 31;
+  const float2 pa = lane < nl ? sh.pairs[par][lane] : make_float2(-INFINITY, 0.f);
+  const float2 pb = lane + 32 < nl ? sh.pairs[par][lane + 32] : make_float2(-INFINITY, 0.f);
+  const float M = warp_max_f(fmaxf(pa.x, pb.x));
+  float part = 0.f;
+  if (M > -INFINITY) {
+    part = (pa.x > -INFINITY ? pa.y * expf(pa.x - M) : 0.f) + (pb.x > -INFINITY ? pb.y * expf(pb.x - M) : 0.f);
+  }
+  const float S = warp_sum(part);
+  const float logS = (M > -INFINITY) ? logf(S) : 0.f;
+  const int la = lane, lb = lane + 32;
+  const int ca = la < nl ? sh.counts[la] : 0, cb = lb < nl ? sh.counts[lb] : 0;
+  const int nc = (int)__reduce_add_sync(0xffffffffu, (unsigned int)(ca + cb));
+  unsigned long long key_r;
+  unsigned long long *cand = sh.cand[0];
+  if (nc <= 32) {
+    int pos = warp_excl_prefix<7>(ca + cb);
+    for (int j = 0; j < ca; ++j) cand[pos++] = sh.lists[la * k + j];
+    for (int j = 0; j < cb; ++j) cand[pos++] = sh.lists[lb * k + j];
+    key_r = warp_rank_small(cand, nc, k);
+  } else {
+    int pa_ = 0, pb_ = 0;
+    unsigned long long ha = ca > 0 ? sh.lists[la * k] : ~0ull, hb = cb > 0 ? sh.lists[lb * k] : ~0ull;
+    key_r = ~0ull;
+    for (int r = 0; r < k; ++r) {
+      const unsigned long long m = warp_min_u64(ha < hb ? ha : hb);
+      if (lane == r) key_r = m;
+      if (ha == m) {
+        ++pa_;
+        ha = pa_ < ca ? sh.lists[la * k + pa_] : ~0ull;
+      } else if (hb == m) {
+        ++pb_;
+        hb = pb_ < cb ? sh.lists[lb * k + pb_] : ~0ull;
+      }
+    }
+  }
+  if (lane < k) {
+    const float z = zid_value(key_r);
+    const int id = (int)zid_id(key_r);
+    const float lp = (M > -INFINITY && z > -INFINITY) ? (z - M) - logS : -INFINITY;
+    const long long o = o0 + lane;
+    tree.cand_tok[o] = id < V ? id : -1;
+    tree.cand_parent[o] = parent;
+    tree.cand_lp[o] = lp;
+    tree.cand_key[o] = add_keys(pkey, fixed_key(lp));
+  }
+}
 
 __global__ void __launch_bounds__(kClThreads) k_expand_cl(ExpandRowArgs a) {
   __shared__ ExpandClSmem sh;
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  __shared__ unsigned long long fl[kMaxM * kMaxTopk];  // the last leader: frontier candidates
+  __shared__ int sel[kMaxM];
+  __shared__ int last;
+  const int t = threadIdx.x, warp = t >> 5;
   const int R = gridDim.x;                 // CTAs per row = cluster size
   const int q = (int)cl_rank();
   const int row = blockIdx.y;
   const int b = row / a.m_l, s = row - b * a.m_l;
   const int k = a.k;
-  cl_arrive_relaxed();  // phase 0: this block has started (waited on before any remote store)
+  cl_arrive_relaxed();  // this block has started (waited on before any remote store)
   pdl_wait();     // the previous kernel in the stream has completed
   pdl_trigger();  // only now may the next kernel launch: at most one waits ahead
 
@@ -628,90 +857,25 @@ __global__ void __launch_bounds__(kClThreads) k_expand_cl(ExpandRowArgs a) {
   }
   const int base = q * kClSpan;
   float v[4 * kClVec];
-#pragma unroll
-  for (int u = 0; u < kClVec; ++u) {
-    const int e0 = base + u * kClThreads * 4 + t * 4;
-    if (zrow && a.vec4 && e0 + 3 < a.V) {
-      const float4 f = __ldcs(reinterpret_cast<const float4 *>(zrow + e0));
-      v[4 * u] = f.x; v[4 * u + 1] = f.y; v[4 * u + 2] = f.z; v[4 * u + 3] = f.w;
-    } else {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) v[4 * u + j] = (zrow && e0 + j < a.V) ? __ldcs(zrow + e0 + j) : -INFINITY;
-    }
-  }
+  load_row_span(zrow, base, a.V, a.vec4, v);
   // the parent's path key, fetched while the logits are in flight
-  const long long pkey = (q == 0 && node >= 0 && !bad) ? ld_cg(a.tree.cand_key + (long long)b * a.C + node) : 0ll;
-  unsigned long long key[4 * kClVec];
-#pragma unroll
-  for (int u = 0; u < kClVec; ++u) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = 4 * u + j, id = base + u * kClThreads * 4 + t * 4 + j;  // ids >= V are padding
-      if (id < a.V) v[e] = sanitize_logit(v[e], flag);
-      key[e] = zid_key(v[e], (unsigned int)id);
-    }
-  }
-  warp_topk_keys<4 * kClVec>(key, k, sh.cand[warp], kWarpCand, sh.wl + warp * k);
+  const long long pkey = (q == 0 && warp == 0 && node >= 0 && !bad) ? ld_cg(a.tree.cand_key + (long long)b * a.C + node)
+                                                                    : 0ll;
+  cl_wait();  // every block of the cluster runs
+  row_warp_part(v, base, a.V, k, 0, sh, flag);
   if (flag) flag_status(a.dev_status, ET_DEV_NONFINITE);
   if (bad && q == 0 && t == 0) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
-  __syncthreads();
-
-  // ---- the block's max (head of the warp lists) and sum of exp ----
-  unsigned long long head = sh.wl[0];
-#pragma unroll
-  for (int w = 1; w < kClWarps; ++w) head = sh.wl[w * k] < head ? sh.wl[w * k] : head;
-  const float Mq = zid_value(head);
-  float sum = 0.f;
-  if (Mq > -INFINITY) {
-#pragma unroll
-    for (int e = 0; e < 4 * kClVec; ++e) sum += exp_fast(v[e] - Mq);
-  }
-  sum = warp_sum(sum);
-  if (lane == 0) sh.wsum[warp] = sum;  // summed in warp order below: deterministic
-
-  // ---- the block's top-k -> the leader's shared memory ----
-  cl_wait();  // phase 0 done: every block of the cluster runs
-  const uint32_t gl_remote = cl_map(&sh.gl[q * k], 0);
-  block_select<kClThreads>(sh.wl, kClWarps * k, k,
-                           [&](int r, unsigned long long key_r) { cl_st_u64(gl_remote + 8u * (uint32_t)r, key_r); });
-  __syncthreads();  // every warp's sum is in
-  if (t == 0) {
-    float cs = 0.f;
-#pragma unroll
-    for (int w = 0; w < kClWarps; ++w) cs += sh.wsum[w];
-    cl_st_f32x2(cl_map(&sh.gms[q], 0), Mq, cs);
-  }
-  cl_arrive();  // phase 1: release this block's stores
+  cl_arrive();  // release the candidates
   if (q != 0) return;
   cl_wait();
 
-  // ---- leader: the row's top-k from the R block lists; write the children ----
-  float M = -INFINITY, S = 0.f;
-  {
-    float2 gq[kClMaxCtas];
-#pragma unroll
-    for (int x = 0; x < kClMaxCtas; ++x) {
-      gq[x] = x < R ? sh.gms[x] : make_float2(-INFINITY, 0.f);
-      M = fmaxf(M, gq[x].x);
-    }
-#pragma unroll
-    for (int x = 0; x < kClMaxCtas; ++x) S += gq[x].x > -INFINITY ? gq[x].y * expf(gq[x].x - M) : 0.f;
-  }
-  const float logS = (M > -INFINITY) ? logf(S) : 0.f;
-  block_select<kClThreads>(sh.gl, R * k, k, [&](int r, unsigned long long key_r) {
-    const float z = zid_value(key_r);
-    const int id = (int)zid_id(key_r);
-    const float lp = (M > -INFINITY && z > -INFINITY) ? (z - M) - logS : -INFINITY;
-    const long long o = (long long)b * a.C + a.base_next + s * k + r;
-    a.tree.cand_tok[o] = id < a.V ? id : -1;
-    a.tree.cand_parent[o] = node;
-    a.tree.cand_lp[o] = lp;
-    a.tree.cand_key[o] = add_keys(pkey, fixed_key(lp));
-  });
+  // ---- the leader's first warp: the row's top-k; write the children ----
+  if (warp == 0)
+    row_leader_part(sh, 0, R * kClWarps, k, a.V, a.tree, (long long)b * a.C + a.base_next + s * k, node, pkey);
   if (a.m_next <= 0) return;  // last layer: no frontier to pick
 
   // ---- the last row of this sequence picks the next frontier ----
-  if (!arrive_last(&a.seq_cnt[b], (unsigned)a.m_l, &sh.last)) return;
+  if (!arrive_last(&a.seq_cnt[b], (unsigned)a.m_l, &last)) return;
   // A child at position e of its row has e better siblings, so only the
   // first m_next of every row can rank below m_next, and among them ranks
   // below m_next are exact.
@@ -720,18 +884,18 @@ __global__ void __launch_bounds__(kClThreads) k_expand_cl(ExpandRowArgs a) {
   for (int c = t; c < P; c += kClThreads) {
     const int rs = c / nk, e = c - rs * nk;
     const int id = a.base_next + rs * k + e;
-    sh.fl[c] = rank_key(ld_cg(a.tree.cand_key + (long long)b * a.C + id), id);
+    fl[c] = rank_key(ld_cg(a.tree.cand_key + (long long)b * a.C + id), id);
   }
   __syncthreads();
-  block_select<kClThreads>(sh.fl, P, a.m_next, [&](int r, unsigned long long key_r) {
-    sh.sel[r] = (int)(key_r & ((1ull << kIdBits) - 1));
+  block_select<kClThreads>(fl, P, a.m_next, [&](int r, unsigned long long key_r) {
+    sel[r] = (int)(key_r & ((1ull << kIdBits) - 1));
   });
   __syncthreads();
   if (t < a.m) {
     if (t < a.m_next) {
       int slot = 0;
-      const int mine = sh.sel[t];
-      for (int j = 0; j < a.m_next; ++j) slot += sh.sel[j] < mine ? 1 : 0;
+      const int mine = sel[t];
+      for (int j = 0; j < a.m_next; ++j) slot += sel[j] < mine ? 1 : 0;
       a.tree.frontier[b * a.m + slot] = mine;
     } else {
       a.tree.frontier[b * a.m + t] = -1;
@@ -788,7 +952,7 @@ __device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p) {
 
 struct BuildPick {
   unsigned long long fl[kMaxM * kMaxTopk];  // frontier candidates (rank keys)
-  long long rowof[kMaxM * kMaxTopk];        // their table rows
+  int rowof[kMaxM * kMaxTopk];              // their table rows
   int sel[kMaxM];
   long long s_row;
   int s_node;
@@ -919,12 +1083,13 @@ __global__ void __launch_bounds__(kClThreads) k_tree_build(BuildArgs a) {
   const int k = a.k;
   unsigned int *cnt = a.layer_cnt + (long long)b * kMaxDepth;
   cl_arrive_relaxed();  // phase 0: this block has started (waited on before any remote store)
-  pdl_wait();           // the previous kernel in the stream has completed
+  pdl_wait();           // returns at once: this kernel is launched stream-ordered (see et_tree_build)
   pdl_trigger();        // every block of this grid is resident before a dependent can launch
   if (s == a.slots) {   // the rerank cluster: its leader alone works
     if (q == 0) rerank_role(a, b, cnt, sh.r);
     return;
   }
+  cl_wait();  // every block of the cluster runs (before any remote store)
 
   for (int layer = 0; layer < a.D; ++layer) {
     const int m_l = a.expanded[layer];
@@ -945,8 +1110,6 @@ __global__ void __launch_bounds__(kClThreads) k_tree_build(BuildArgs a) {
         }
       }
       __syncthreads();
-      // the frontier: a child at position e of its row has e better siblings,
-      // so only the first m_l of every row can rank below m_l
       const int base_l = a.base[layer];
       const int nk = k < m_l ? k : m_l;
       const int P = m_prev * nk;
@@ -987,82 +1150,19 @@ __global__ void __launch_bounds__(kClThreads) k_tree_build(BuildArgs a) {
     const int base = q * kClSpan;
     int flag = 0;
     float v[4 * kClVec];
-#pragma unroll
-    for (int u = 0; u < kClVec; ++u) {
-      const int e0 = base + u * kClThreads * 4 + t * 4;
-      if (zrow && a.vec4 && e0 + 3 < a.V) {
-        const float4 f = __ldcs(reinterpret_cast<const float4 *>(zrow + e0));
-        v[4 * u] = f.x; v[4 * u + 1] = f.y; v[4 * u + 2] = f.z; v[4 * u + 3] = f.w;
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) v[4 * u + j] = (zrow && e0 + j < a.V) ? __ldcs(zrow + e0 + j) : -INFINITY;
-      }
-    }
-    const long long pkey = (q == 0 && node >= 0 && !bad) ? ld_cg(a.tree.cand_key + (long long)b * a.C + node) : 0ll;
-    unsigned long long key[4 * kClVec];
-#pragma unroll
-    for (int u = 0; u < kClVec; ++u) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int e = 4 * u + j, id = base + u * kClThreads * 4 + t * 4 + j;  // ids >= V are padding
-        if (id < a.V) v[e] = sanitize_logit(v[e], flag);
-        key[e] = zid_key(v[e], (unsigned int)id);
-      }
-    }
-    warp_topk_keys<4 * kClVec>(key, k, sh_e.cand[warp], kWarpCand, sh_e.wl + warp * k);
+    load_row_span(zrow, base, a.V, a.vec4, v);
+    const long long pkey = (q == 0 && warp == 0 && node >= 0 && !bad) ? ld_cg(a.tree.cand_key + (long long)b * a.C + node)
+                                                                      : 0ll;
+    row_warp_part(v, base, a.V, k, layer & 1, sh_e, flag);
     if (flag) flag_status(a.dev_status, ET_DEV_NONFINITE);
     if (bad && q == 0 && t == 0) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
-    __syncthreads();
-    unsigned long long head = sh_e.wl[0];
-#pragma unroll
-    for (int w = 1; w < kClWarps; ++w) head = sh_e.wl[w * k] < head ? sh_e.wl[w * k] : head;
-    const float Mq = zid_value(head);
-    float sum = 0.f;
-    if (Mq > -INFINITY) {
-#pragma unroll
-      for (int e = 0; e < 4 * kClVec; ++e) sum += exp_fast(v[e] - Mq);
-    }
-    sum = warp_sum(sum);
-    if (lane == 0) sh_e.wsum[warp] = sum;
-    cl_wait();  // every block has started, and the leader has finished reading the previous layer
-    const uint32_t gl_remote = cl_map(&sh_e.gl[q * k], 0);
-    block_select<kClThreads>(sh_e.wl, kClWarps * k, k,
-                             [&](int r, unsigned long long key_r) { cl_st_u64(gl_remote + 8u * (uint32_t)r, key_r); });
-    __syncthreads();
-    if (t == 0) {
-      float cs = 0.f;
-#pragma unroll
-      for (int w = 0; w < kClWarps; ++w) cs += sh_e.wsum[w];
-      cl_st_f32x2(cl_map(&sh_e.gms[q], 0), Mq, cs);
-    }
-    cl_arrive();  // release this block's stores
-    cl_wait();    // every block's stores have landed in the leader
-    if (q == 0) {
-      float M = -INFINITY, S = 0.f;
-      {
-        float2 gq[kClMaxCtas];
-#pragma unroll
-        for (int x = 0; x < kClMaxCtas; ++x) {
-          gq[x] = x < R ? sh_e.gms[x] : make_float2(-INFINITY, 0.f);
-          M = fmaxf(M, gq[x].x);
-        }
-#pragma unroll
-        for (int x = 0; x < kClMaxCtas; ++x) S += gq[x].x > -INFINITY ? gq[x].y * expf(gq[x].x - M) : 0.f;
-      }
-      const float logS = (M > -INFINITY) ? logf(S) : 0.f;
-      block_select<kClThreads>(sh_e.gl, R * k, k, [&](int r, unsigned long long key_r) {
-        const float z = zid_value(key_r);
-        const int id = (int)zid_id(key_r);
-        const float lp = (M > -INFINITY && z > -INFINITY) ? (z - M) - logS : -INFINITY;
-        const long long o = (long long)b * a.C + base_next + s * k + r;
-        a.tree.cand_tok[o] = id < a.V ? id : -1;
-        a.tree.cand_parent[o] = node;
-        a.tree.cand_lp[o] = lp;
-        a.tree.cand_key[o] = add_keys(pkey, fixed_key(lp));
-      });
-      __syncthreads();  // every child of this row is written
-      if (t == 0) {
-        __threadfence();
+    cl_arrive();  // release the candidates
+    cl_wait();    // every block's candidates have landed in the leader (and every block is done with this layer)
+    if (q == 0 && warp == 0) {
+      row_leader_part(sh_e, layer & 1, R * kClWarps, k, a.V, a.tree, (long long)b * a.C + base_next + s * k, node, pkey);
+      __threadfence();
+      __syncwarp();  // every child of this row is written
+      if (lane == 0) {
         const bool last = atomicAdd(cnt + layer, 1u) == (unsigned)(m_l - 1);  // the next layer may count this row
         // the sequence's last row of the final layer (when no rerank cluster
         // follows the layers): every wait of this sequence is over, re-arm
@@ -1071,7 +1171,6 @@ __global__ void __launch_bounds__(kClThreads) k_tree_build(BuildArgs a) {
           for (int l = 0; l < a.D; ++l) cnt[l] = 0u;
       }
     }
-    cl_arrive();  // the leader is done with its shared memory for this layer
   }
 }
 
@@ -1294,8 +1393,13 @@ extern "C" et_status et_tree_build(const et_tree_cfg *cfg, const float *logits, 
     a.prefix_len = prefix_len;
     a.mask = mask;
     a.posids = posids;
-    const et_status st = et_launch(k_tree_build, dim3(R, (unsigned)clusters, 1), dim3(kClThreads, 1, 1), 0,
-                                   (cudaStream_t)stream, R, a);
+    // A plain stream-ordered launch: as a programmatic dependent, the grid's
+    // clusters were placed while the previous kernel still held the SMs, and
+    // the build ran about 15 us slower behind attention or acceptance on
+    // GB300 (no slowdown behind another tree build or a non-programmatic
+    // kernel).  The kernel still triggers its own dependents early.
+    const et_status st = et_launch_ex(false, k_tree_build, dim3(R, (unsigned)clusters, 1), dim3(kClThreads, 1, 1),
+                                      0, (cudaStream_t)stream, R, a);
     if (st != ET_OK || rerank_here) return st;
     return launch_rerank(cfg, tree, dev_status, prefix_len, mask, posids, stream);
   }
