@@ -22,12 +22,13 @@
 // Two resident blocks per SM keep two independent pipelines in flight.  A
 // 128-row tile packs (token, query head) rows of one KV head, so a GQA group
 // shares every K/V tile.  The KV splits of one tile run as one thread-block
-// cluster: each split writes its partial rows straight from TMEM to an
-// L2-resident workspace, one cluster barrier orders them, each split merges
-// a slice of the rows and drops the scratch lines from L2 (measured on
-// GB300: merging in the last split to finish instead was about twice as
-// slow, one SM reading every partial; moving the rows through distributed
-// shared memory took about four times as long).  Every mbarrier wait is
+// cluster and merge their partial rows among themselves, each split a slice
+// of the rows: a tile of at most 64 real rows (the MHA trees) moves them
+// from TMEM straight into the owners' shared memory (distributed shared
+// memory stores between two cluster barriers); larger tiles write them from
+// TMEM to an L2-resident workspace and drop those lines after the merge
+// (measured on GB300: merging in the last split to finish instead was about
+// twice as slow, one SM reading every partial).  Every mbarrier wait is
 // bounded: on expiry the block reports ET_DEV_TIMEOUT, stops, frees its TMEM
 // and exits.
 #include <cuda.h>
@@ -54,25 +55,23 @@ constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
 constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
 constexpr uint32_t kOffMisc = kOffBar + 256;
 // split merge through distributed shared memory (tiles of at most 64 real
-// rows): own (max, sum) pairs, then the pairs received from every split
-constexpr uint32_t kOffMlOwn = kOffMisc + 256;
-constexpr uint32_t kOffMlRecv = kOffMlOwn + kTcRows * 8;
+// rows): the (max, sum) pairs received from every split; the rows land in
+// the Q and K space
+constexpr uint32_t kOffMlRecv = kOffMisc + 256;
 constexpr int kDsmMaxRows = 64;     // real rows of a tile merged through DSMEM
 constexpr int kDsmMaxSlots = 96;    // S * per for 2 <= S <= 16, per = ceil(rows / S) rounded up to even (<= 90)
-constexpr uint32_t kMlRecvBytes = kDsmMaxSlots * 8;
+constexpr uint32_t kMlRecvBytes = kDsmMaxSlots * 16;  // (max, sum, scale, -) per received row
 constexpr uint32_t kSmemBytes = kOffMlRecv + kMlRecvBytes + 1024;  // + slack for 1024-byte alignment
-// partial rows: own rows staged in the V stages, received rows in the Q and K space
-constexpr uint32_t kOffStage = kOffV;
 constexpr uint32_t kOffRecv = kOffQ;
-static_assert(kDsmMaxRows * 512 <= kStages * kTileBytes, "own partial rows fit the V stages");
-static_assert(kDsmMaxSlots * 512 <= kOffV, "received rows fit the Q and K space");
+constexpr uint32_t kRecvRowBytes = kTcDim * 2;  // a received row: 128 fp16 values scaled into [-1, 1]
+static_assert(kDsmMaxSlots * kRecvRowBytes <= kOffV, "received rows fit the Q and K space");
 // TMEM columns: S, O accumulator, P (bf16 pairs) double buffer
 constexpr uint32_t kColS = 0, kColO = 64, kColP0 = 192, kColP1 = 224, kTmemCols = 256;
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the row max grows by more than 2^8
 
 // barrier slots
 constexpr int B_KFULL = 0, B_KEMPTY = 2, B_VFULL = 4, B_VEMPTY = 6, B_SFULL = 8, B_SFREE = 9, B_PFULL = 10,
-              B_OFULL = 12, B_QFULL = 13, B_DRAIN = 14, B_RECV = 15;
+              B_OFULL = 12, B_QFULL = 13, B_DRAIN = 14;
 constexpr int kQWarps = 5;       // warps 3-7 stage Q
 constexpr int kSoftmaxWarps = 4; // warps 4-7: one per TMEM lane quarter
 
@@ -149,7 +148,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     mbar_init(bar(B_OFULL), 1);
     mbar_init(bar(B_QFULL), a.q_tma ? 1 : kQWarps);
     mbar_init(bar(B_DRAIN), 1);
-    mbar_init(bar(B_RECV), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -468,41 +466,58 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 
   // ---------------- S splits of a tile with at most 64 real rows: merged through DSMEM ----------------
-  // Each split stages its unnormalised fp32 rows in its V stages (16-byte
-  // chunk c of row r at c ^ (r & 31): conflict-free from one thread per row)
-  // and its (max, sum) pairs.  After one cluster barrier (every split is done
-  // with its Q, K and V space), split s bulk-copies the rows each owner o
-  // merges, [o * per, (o + 1) * per), into o's Q/K space (slot s), completing
-  // on o's mbarrier; each owner merges its slice from shared memory.  A second
-  // cluster barrier keeps every block resident until the copies out of it
-  // have landed.
+  // After one cluster barrier (every split is done with its Q, K and V
+  // space), each softmax thread sends its unnormalised row straight from TMEM
+  // to the shared memory of the row's owner o = row / per (slot s of o's Q/K
+  // space) as fp16 scaled by the row's largest magnitude (values in [-1, 1],
+  // error at most 2^-12 of that magnitude), with its (max, sum, scale); the
+  // 16-byte chunk c of row r sits at c ^ (r & 15), conflict-free from one
+  // thread per row and for the merge below.  A second cluster barrier (release / acquire) makes every row
+  // visible to its owner, which merges its slice.  No block writes into
+  // another after that barrier, so each may leave once it has merged.
   const int S = a.S;
   const int nvalid = min(kTcRows, N * a.G - mt * kTcRows);  // the real rows are a prefix of the tile
   const bool have = !aborted && T > 0;
   if (nvalid <= kDsmMaxRows) {
-    const int per = (((nvalid + S - 1) / S) + 1) & ~1;  // even: the pairs' copies stay 16-byte multiples
+    const int per = (((nvalid + S - 1) / S) + 1) & ~1;  // S * per <= kDsmMaxSlots
+    cluster_sync_all();  // every split is done with its Q, K and V space
     if (smx) {
+      const int o = r / per, lr = r - o * per;
+      float amax = 0.f;
       if (have && __any_sync(0xffffffffu, my_tok >= 0)) {
         const uint32_t lane_base = tmem + ((uint32_t)(r & ~31) << 16);
+        const uint32_t dst = r < nvalid ? cl_map(sm + kOffRecv + ((size_t)s * per + lr) * kRecvRowBytes, (uint32_t)o) : 0u;
         uint32_t ov[64];
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {  // the row's largest magnitude (NaN is passed through below)
+          tmem_ld64(lane_base + kColO + 64 * h, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 64; ++c) amax = fmaxf(amax, fabsf(__uint_as_float(ov[c])));
+        }
+        const float inv = amax > 0.f ? 1.f / amax : 0.f;
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
           tmem_ld64(lane_base + kColO + 64 * h, ov);
           tmem_wait_ld();
           if (r < nvalid) {
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const uint32_t dst = sb + kOffStage + (uint32_t)r * 512u + (uint32_t)(((16 * h + c) ^ (r & 31)) << 4);
-              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(ov[4 * c]),
-                           "r"(ov[4 * c + 1]), "r"(ov[4 * c + 2]), "r"(ov[4 * c + 3])
+            for (int c = 0; c < 8; ++c) {
+              uint32_t hv[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                hv[u] = pack_f16x2(__uint_as_float(ov[8 * c + 2 * u]) * inv, __uint_as_float(ov[8 * c + 2 * u + 1]) * inv);
+              asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                               dst + (uint32_t)(((8 * h + c) ^ (r & 15)) << 4)),
+                           "r"(hv[0]), "r"(hv[1]), "r"(hv[2]), "r"(hv[3])
                            : "memory");
             }
           }
         }
       }
-      reinterpret_cast<float2 *>(sm + kOffMlOwn)[r] =
-          make_float2(have && r < nvalid ? m_used : -INFINITY, have && r < nvalid ? l : 0.f);
-      fence_async_smem();  // the staged rows are read by the bulk copies (async proxy)
+      if (r < nvalid)
+        cl_st_f32x4(cl_map(sm + kOffMlRecv + ((size_t)s * per + lr) * 16, (uint32_t)o), have ? m_used : -INFINITY,
+                    have ? l : 0.f, amax, 0.f);
     }
     tc_fence_before();
     __syncthreads();
@@ -511,62 +526,45 @@ __global__ void __launch_bounds__(kThreads, 2)
       __syncwarp();
       asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
-    cluster_sync_all();  // every split has staged its rows and is done with its Q, K and V space
+    cluster_sync_all();  // every split's rows and pairs have landed in their owners
     const int r0 = s * per, cnt = max(0, min(nvalid, r0 + per) - r0);
-    if (t == 0) {
-      // what arrives here: from every split, its rows of this slice and `per` pairs
-      mbar_expect_tx(bar(B_RECV), (uint32_t)S * ((uint32_t)cnt * 512u + (uint32_t)per * 8u));
-      for (int o = 0; o < S; ++o) {
-        const int o0 = o * per, ocnt = max(0, min(nvalid, o0 + per) - o0);
-        const uint32_t rbar = cl_map(sm + kOffBar + 8 * B_RECV, (uint32_t)o);
-        if (ocnt > 0)
-          bulk_to_peer(cl_map(sm + kOffRecv + (size_t)s * per * 512, (uint32_t)o), sb + kOffStage + (uint32_t)o0 * 512u,
-                       (uint32_t)ocnt * 512u, rbar);
-        bulk_to_peer(cl_map(sm + kOffMlRecv + (size_t)s * per * 8, (uint32_t)o), sb + kOffMlOwn + (uint32_t)o0 * 8u,
-                     (uint32_t)per * 8u, rbar);
-      }
-    }
-    bool got = false;
-    if (!aborted) got = __all_sync(0xffffffffu, mbar_wait(bar(B_RECV), 0, abort_flag, a.wait_cycles));
-    if (!got) mbar_drain(bar(B_RECV), 0);  // the copies into this block land before it may leave
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");  // the copies into this block have landed
-    if (got && !aborted && cnt > 0) {
+    if (!aborted && cnt > 0) {
       __nv_bfloat16 *O = static_cast<__nv_bfloat16 *>(a.out);
-      const float2 *mlr = reinterpret_cast<const float2 *>(sm + kOffMlRecv);
+      const float4 *mlr = reinterpret_cast<const float4 *>(sm + kOffMlRecv);
       for (int x = t; x < cnt * 32; x += kThreads) {
-        const int lr = x >> 5, chunk = x & 31, rr = r0 + lr;
+        const int lr = x >> 5, piece = x & 31, rr = r0 + lr;  // piece: 4 of the row's 128 values
         float M = -INFINITY;
         for (int sp = 0; sp < S; ++sp) M = fmaxf(M, mlr[sp * per + lr].x);
         float Ls = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int sp = 0; sp < S; ++sp) {
-          const float2 ml = mlr[sp * per + lr];
-          if (ml.x > -INFINITY) {  // a split without keys for this row staged no row
-            const float w = exp2f(ml.x - M);
+          const float4 ml = mlr[sp * per + lr];
+          if (ml.x > -INFINITY) {  // a split without keys for this row sent no row
+            const float w = ex2(ml.x - M);
             Ls = fmaf(ml.y, w, Ls);
-            const float4 p = *reinterpret_cast<const float4 *>(sm + kOffRecv + ((size_t)sp * per + lr) * 512 +
-                                                               ((chunk ^ (rr & 31)) << 4));
-            acc.x = fmaf(w, p.x, acc.x);
-            acc.y = fmaf(w, p.y, acc.y);
-            acc.z = fmaf(w, p.z, acc.z);
-            acc.w = fmaf(w, p.w, acc.w);
+            const uint2 hp = *reinterpret_cast<const uint2 *>(sm + kOffRecv + ((size_t)sp * per + lr) * kRecvRowBytes +
+                                                              (((piece >> 1) ^ (rr & 15)) << 4) + (piece & 1) * 8);
+            const float ws = w * ml.z;
+            const float2 p01 = __half22float2(*reinterpret_cast<const __half2 *>(&hp.x));
+            const float2 p23 = __half22float2(*reinterpret_cast<const __half2 *>(&hp.y));
+            acc.x = fmaf(ws, p01.x, acc.x);
+            acc.y = fmaf(ws, p01.y, acc.y);
+            acc.z = fmaf(ws, p23.x, acc.z);
+            acc.w = fmaf(ws, p23.y, acc.w);
           }
         }
         const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
         uint2 v;
         v.x = pack_bf16x2(acc.x * inv, acc.y * inv);
         v.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2 *>(O + (((long long)b * N + row_tok[rr]) * a.Hq + row_head[rr]) * kTcDim + 4 * chunk) =
+        *reinterpret_cast<uint2 *>(O + (((long long)b * N + row_tok[rr]) * a.Hq + row_head[rr]) * kTcDim + 4 * piece) =
             v;
-        if (chunk == 0 && a.lse)
+        if (piece == 0 && a.lse)
           a.lse[((long long)b * a.Hq + row_head[rr]) * N + row_tok[rr]] =
-              Ls > 0.f ? (M + log2f(Ls)) * 0.69314718055994531f : -INFINITY;
+              Ls > 0.f ? (M + __log2f(Ls)) * 0.69314718055994531f : -INFINITY;
       }
     }
-    if (!got || aborted) {
-      if (t == 0) flag_status(a.dev_status, ET_DEV_TIMEOUT);
-    }
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");  // no block leaves with copies out of it pending
+    if (aborted && t == 0) flag_status(a.dev_status, ET_DEV_TIMEOUT);
     return;
   }
 
