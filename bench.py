@@ -274,7 +274,7 @@ def oracle_baseline(name, budget_s=15.0, max_steps=80):
 # same build: the summary records a hash of the kernel's sources, and the
 # figure is reported only while the sources still hash the same
 # ---------------------------------------------------------------------------
-ATTN_SOURCES = ("et_attention_tc.cu", "et_attn_internal.h", "et_common.cuh", "et_attention.cu")
+ATTN_SOURCES = ("et_attention_tc.cu", "et_attn_internal.h", "et_common.cuh", "et_tc.cuh", "et_attention.cu")
 
 
 def attention_source_hash() -> str:
@@ -462,6 +462,39 @@ def run_gpu(args):
     hbm_peak, bf16_peak, peak_src = _peaks()
     achieved = attn_b / (attn_us * 1e-6) / 1e9
 
+    # ---- each call of the step alone, graph-timed the same way: which kernel dominates ----
+    def graph_us(call):
+        with torch.cuda.stream(stream):
+            for r in range(R):
+                call(sets[r])
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(K):
+                call(sets[i % R])
+        g.replay()
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(cur)
+        g.replay()
+        a1.record(cur)
+        torch.cuda.synchronize()
+        return a0.elapsed_time(a1) * 1000.0 / K
+
+    tree_us = graph_us(lambda inp: st.build_tree(inp, stream=stream))
+    accept_us = graph_us(lambda inp: st.accept(inp, stream=stream))
+    tree_b = 4 * wl.V * expanded * cfg.B          # one fp32 logits row per expanded node
+    accept_b = 4 * wl.V * cfg.N * cfg.B           # every flat row's target logits
+    parts = [("et_tree_build", tree_us, tree_b, "latency: D dependent layers, each a DRAM round trip, "
+                                                 "two cluster barriers and a cross-cluster handshake"),
+             ("et_tree_attention", attn_us, attn_b, "hbm"),
+             ("et_verify_accept", accept_us, accept_b, "latency: one row per cluster, then the walk")]
+    total_us = sum(p_[1] for p_ in parts)
+    step_kernels = [{"call": n_, "us_alone": round(u_, 3), "share_of_sum": round(u_ / total_us, 3),
+                     "bytes": b_, "GBps": round(b_ / (u_ * 1e-6) / 1e9, 1),
+                     "frac_hbm": round(b_ / (u_ * 1e-6) / 1e9 / hbm_peak, 4), "bound": bd_}
+                    for n_, u_, b_, bd_ in parts]
+
     # ---- attention alone at the other target shapes (batch 1) ----
     shapes = []
     if not args.no_attn_shapes:
@@ -507,6 +540,7 @@ def run_gpu(args):
                      "traffic": args.traffic if args.traffic is not None else
                      recorded_attention_traffic(wl.name, cfg.B, int(prefix.max())),
                      "peak_source": peak_src, "kernel": "et_tree_attention"},
+        "step_kernels": step_kernels,
         "e2e": e2e,
         "kv_commit": commit,
         "static_tree": static,
