@@ -136,10 +136,12 @@ typedef struct {
 /* et_attn_shape.flags: the caller promises that q, k/v_prefix, k/v_tree,
  * kv_row0 and prefix_len are not written by the kernel launched just before
  * this call in the same stream (only the mask may come from it, as it does
- * from et_tree_rerank_mask in a verification step).  The tcgen05 path may
- * then fetch its first tiles before it waits for that kernel to finish,
- * which hides their memory latency behind that kernel's tail; the mask, the
- * outputs and the workspace are touched only after the wait. */
+ * from et_tree_rerank_mask or et_tree_build in a verification step).  The
+ * tcgen05 path then streams Q and the whole unmasked prefix (QK^T, online
+ * softmax and P.V of every prefix tile) without waiting for that kernel: it
+ * waits only before its first tree tile, whose ancestor mask that kernel
+ * writes, and before it writes out, lse or the workspace.  A prefix that
+ * streams while a latency-bound kernel runs costs the step almost nothing. */
 #define ET_ATTN_INPUTS_READY 1
 
 /* Draft LM head shape (host struct), see et_lm_head. */

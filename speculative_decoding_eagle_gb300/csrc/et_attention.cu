@@ -497,9 +497,14 @@ static bool make_plan(const et_attn_shape *s, AttnPlan *p) {
       // the splits of a row tile form one thread-block cluster (<= 8 blocks);
       // two blocks fit per SM: aim at ~1.7 blocks per SM so that the
       // clusters still find room in one wave (measured on GB300: 6 splits for
-      // 40 heads and 5 for 48 row tiles beat both fewer and more)
+      // 40 heads and 5 for 48 row tiles beat both fewer and more), and at
+      // about 4.5 K/V tiles per split: below that the split merge outweighs
+      // the shorter loop (7B heads, prefix 1024, 17 tiles: 11.8 us at 4
+      // splits, 12.4 at 3, 12.8 at 5, 13.3 at 8)
       if (S <= 0) {
         S = (int)((17LL * sm_count()) / (10LL * base));
+        const int by_tiles = (2 * T + 8) / 9;  // ceil(T / 4.5)
+        if (S > by_tiles) S = by_tiles;
         if (S > cap) S = cap;
         if (S > 8) S = 8;  // the portable cluster size (larger clusters are an explicit choice)
         if (S < 1) S = 1;

@@ -173,8 +173,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     pdl_trigger();  // after the TMEM allocation: a waiting dependent block must not hold the TMEM this block needs
   }
   // with inputs_ready the previous kernel writes none of Q, K/V or the prefix
-  // lengths: the first tiles go out before the wait (only the mask, read by
-  // the softmax, and every output come after it)
+  // lengths: the whole prefix streams before the wait; the softmax waits
+  // before the first tree tile (the mask), every thread before the outputs
   const int L = a.inputs_ready ? L_in : a.prefix_len[b];
   const long long S_b = a.kv_head_stride > 0 ? a.kv_head_stride : L;
   const long long row0 = a.inputs_ready ? row0_in : (a.kv_row0 ? a.kv_row0[b] : 0);
@@ -210,10 +210,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       tma_4d(sb + kOffQ + kQHalfBytes, &tm_q, 64, 0, g, tok0, qb);
     }
   }
-  if (a.inputs_ready) {
-    pdl_wait();
-    pdl_trigger();
-  }
+  if (a.inputs_ready) pdl_trigger();  // every block of this grid runs before a dependent can launch
   if (t == 0 && L > 0 && row0 + (long long)g * S_b + L > a.kv_rows) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
 
   if (warp == 0 || warp == 2) {
@@ -324,15 +321,21 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (smx) {
     const bool active = __any_sync(0xffffffffu, my_tok >= 0);  // warp-uniform: any real row here
     unsigned long long mw0 = 0ull, mw1 = 0ull;
-    if (my_tok >= 0) {
-      mw0 = a.mask[((long long)b * N + my_tok) * a.W];
-      if (a.W > 1) mw1 = a.mask[((long long)b * N + my_tok) * a.W + 1];
-    }
+    // the mask comes from the previous kernel: read it after the programmatic
+    // wait, at the top (without inputs_ready) or at the first tree tile
+    const int j_mask = a.inputs_ready ? (nP > t0 ? nP - t0 : 0) : 0;
     const uint32_t lane_base = tmem + ((uint32_t)(r & ~31) << 16);
     const float scale = a.scale_log2;
     uint32_t raw[64];
     for (int j = 0; j < T; ++j) {
       const int tile = t0 + j;
+      if (j == j_mask) {
+        if (a.inputs_ready) pdl_wait();
+        if (my_tok >= 0) {  // in flight while S of this tile completes
+          mw0 = a.mask[((long long)b * N + my_tok) * a.W];
+          if (a.W > 1) mw1 = a.mask[((long long)b * N + my_tok) * a.W + 1];
+        }
+      }
       if (!warp_wait(bar(B_SFULL), (uint32_t)j & 1u, abort_flag, a.wait_cycles)) { ok_rows = false; break; }
       tc_fence_after();
       if (active) {
@@ -425,6 +428,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   __syncthreads();
   tc_fence_after();
+  if (a.inputs_ready) pdl_wait();  // the outputs and the workspace: the previous kernel has completed
   const bool aborted = *abort_flag != 0;
   if (a.S == 1) {
     // ---------------- single split: normalise and write this block's rows ----------------

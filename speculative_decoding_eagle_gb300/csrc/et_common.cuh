@@ -399,28 +399,34 @@ static inline bool et_aligned(const void *p, size_t a) { return ((uintptr_t)p % 
 // from now on (et_set_wait_limit; defined in et_tree.cu).
 __attribute__((visibility("hidden"))) long long et_wait_limit_cycles();
 
-// Raise a kernel's dynamic shared-memory limit once per (kernel, device): the
-// attribute lives in the current device's context, so every device that runs
-// the kernel needs its own call.  Thread-safe.
 #include <mutex>
-static inline cudaError_t et_smem_attr(const void *kernel, int bytes) {
+// Set a kernel attribute once per (kernel, attribute, device): the attribute
+// lives in the current device's context, so every device that runs the
+// kernel needs its own call.  Thread-safe.
+static inline cudaError_t et_func_attr(const void *kernel, cudaFuncAttribute attr, int value) {
   static std::mutex mu;
   static const void *done_fn[64];
+  static int done_attr[64];
   static int done_dev[64];
   static int ndone = 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
   std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < ndone; ++i)
-    if (done_fn[i] == kernel && done_dev[i] == dev) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (done_fn[i] == kernel && done_attr[i] == (int)attr && done_dev[i] == dev) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, attr, value);
   if (e != cudaSuccess) return e;
   if (ndone < 64) {
     done_fn[ndone] = kernel;
+    done_attr[ndone] = (int)attr;
     done_dev[ndone] = dev;
     ++ndone;
   }
   return cudaSuccess;
+}
+// Raise a kernel's dynamic shared-memory limit (once per kernel and device).
+static inline cudaError_t et_smem_attr(const void *kernel, int bytes) {
+  return et_func_attr(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 // Launch with programmatic stream serialization (pdl) or as a plain stream-
