@@ -440,16 +440,19 @@ def run_gpu(args):
         torch.cuda.synchronize()
         eager_ms = round(e0.elapsed_time(e1) / ke, 5)
 
-    # ---- attention alone: a graph of K launches over the rotating sets ----
+    # ---- attention alone (the standalone split plan): a graph of K launches over the rotating sets ----
     K = max(8, min(200, args.steps))
+    sa = S.VerifyStep(wl, mode=mode, num_splits=args.splits, overlap=False,
+                      attn_impl={"auto": E.ATTN_AUTO, "mma": E.ATTN_MMA_SYNC, "tcgen05": E.ATTN_TCGEN05}[args.attn])
+    sa.prepare(sets[0])
     ga = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         for r in range(R):
-            st.attention(sets[r], stream=stream)
+            sa.run(sets[r], stream=stream)  # its own trees and masks
     stream.synchronize()
     with torch.cuda.graph(ga, stream=stream):
         for i in range(K):
-            st.attention(sets[i % R], stream=stream)
+            sa.attention(sets[i % R], stream=stream)
     ga.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -483,6 +486,8 @@ def run_gpu(args):
 
     tree_us = graph_us(lambda inp: st.build_tree(inp, stream=stream))
     accept_us = graph_us(lambda inp: st.accept(inp, stream=stream))
+    # the step's own attention (its split count chosen to stream beside the tree build): what it adds to the tree
+    tree_attn_us = graph_us(lambda inp: (st.build_tree(inp, stream=stream), st.attention(inp, stream=stream)))
     tree_b = 4 * wl.V * expanded * cfg.B          # one fp32 logits row per expanded node
     accept_b = 4 * wl.V * cfg.N * cfg.B           # every flat row's target logits
     parts = [("et_tree_build", tree_us, tree_b, "latency: D dependent layers, each a DRAM round trip, "
@@ -490,10 +495,14 @@ def run_gpu(args):
              ("et_tree_attention", attn_us, attn_b, "hbm"),
              ("et_verify_accept", accept_us, accept_b, "latency: one row per cluster, then the walk")]
     total_us = sum(p_[1] for p_ in parts)
-    step_kernels = [{"call": n_, "us_alone": round(u_, 3), "share_of_sum": round(u_ / total_us, 3),
-                     "bytes": b_, "GBps": round(b_ / (u_ * 1e-6) / 1e9, 1),
-                     "frac_hbm": round(b_ / (u_ * 1e-6) / 1e9 / hbm_peak, 4), "bound": bd_}
-                    for n_, u_, b_, bd_ in parts]
+    step_kernels = {"calls": [{"call": n_, "us_alone": round(u_, 3), "share_of_sum": round(u_ / total_us, 3),
+                               "bytes": b_, "GBps": round(b_ / (u_ * 1e-6) / 1e9, 1),
+                               "frac_hbm": round(b_ / (u_ * 1e-6) / 1e9 / hbm_peak, 4), "bound": bd_}
+                              for n_, u_, b_, bd_ in parts],
+                    "attention_alone_splits": E.et_tree_attention_splits(sa.shape),
+                    "attention_in_step_splits": E.et_tree_attention_splits(st.shape),
+                    "tree_then_attention_us": round(tree_attn_us, 3),
+                    "attention_adds_to_tree_us": round(tree_attn_us - tree_us, 3)}
 
     # ---- attention alone at the other target shapes (batch 1) ----
     shapes = []
@@ -532,7 +541,8 @@ def run_gpu(args):
                    ("fp32 cores" if wl.dtype != "bf16" else ("tcgen05" if wl.d == 128 else "mma.sync")),
                    "l2": f"inputs larger than L2: {R} rotating input sets, {per_step / 1e6:.1f} MB read per step",
                    "cuda_graphs": bool(graphs), "parallelism": f"replicas x{world}"},
-        "tree_attention": {"us_per_launch": round(attn_us, 3), "GBps": round(achieved, 1),
+        "tree_attention": {"us_per_launch": round(attn_us, 3), "splits": E.et_tree_attention_splits(sa.shape),
+                           "GBps": round(achieved, 1),
                            "pct_of_8TBps": round(100 * achieved / 8000.0, 2), "bytes": attn_b},
         "tree_attention_shapes": shapes,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
@@ -586,7 +596,7 @@ def time_attention_shape(name, prefix, stream, K, hbm_peak, bf16_peak):
     from speculative_decoding_eagle_gb300 import step as S
     from speculative_decoding_eagle_gb300 import workloads as W
     wl = W.WORKLOADS[name].with_(B=1, prefix=prefix, ragged=False)
-    st = S.VerifyStep(wl)
+    st = S.VerifyStep(wl, overlap=False)  # the standalone split plan
     base = S.to_device(wl, S.host_inputs(wl, st.C))
     st.run(base, stream=stream)  # the mask of a real tree
     stream.synchronize()
@@ -903,7 +913,7 @@ def run_split_sweep(args):
     K = max(8, min(200, args.steps))
     stream = torch.cuda.Stream()
     for splits in [int(x) for x in args.splits_sweep.split(",")]:
-        st = S.VerifyStep(wl, num_splits=splits, attn_impl=E.ATTN_TCGEN05)
+        st = S.VerifyStep(wl, num_splits=splits, attn_impl=E.ATTN_TCGEN05, overlap=False)
         st.prepare(sets[0])
         with torch.cuda.stream(stream):
             for r in range(R):

@@ -210,7 +210,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       tma_4d(sb + kOffQ + kQHalfBytes, &tm_q, 64, 0, g, tok0, qb);
     }
   }
-  if (a.inputs_ready) pdl_trigger();  // every block of this grid runs before a dependent can launch
   if (t == 0 && L > 0 && row0 + (long long)g * S_b + L > a.kv_rows) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
 
   if (warp == 0 || warp == 2) {
@@ -428,7 +427,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   __syncthreads();
   tc_fence_after();
-  if (a.inputs_ready) pdl_wait();  // the outputs and the workspace: the previous kernel has completed
+  if (a.inputs_ready) {
+    pdl_wait();     // the outputs and the workspace: the previous kernel has completed
+    pdl_trigger();  // only now may the next kernel launch: at most one waits ahead
+  }
   const bool aborted = *abort_flag != 0;
   if (a.S == 1) {
     // ---------------- single split: normalise and write this block's rows ----------------

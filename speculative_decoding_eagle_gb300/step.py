@@ -86,14 +86,40 @@ def to_device(wl: W.Workload, h: Dict[str, np.ndarray], device="cuda") -> StepIn
                       host=h)
 
 
+# Measured on GB300 (7B heads, batch 1): a tcgen05 attention block spends
+# about 1.4 us per 64-key K/V tile; one layer of the one-launch tree build
+# takes about 7 us.
+TILE_US = 1.4
+LAYER_US = 7.0
+
+
+def overlap_splits(tiles: int, depth: int, auto_splits: int, blocks_per_split: int, free_slots: int) -> int:
+    """KV splits for the attention of a step whose tree is built in one launch.
+
+    With ET_ATTN_INPUTS_READY the attention blocks stream their prefix while
+    the latency-bound tree build runs, so a block may take long as long as it
+    ends before the tree does: the fewest splits (at most the standalone
+    plan's) whose blocks each stream within 80% of the tree's expected time
+    and all find room beside the tree's blocks.  Fewer splits leave less to
+    merge after the tree.  Falls back to the standalone plan."""
+    budget = 0.8 * depth * LAYER_US
+    for s in range(1, max(1, auto_splits) + 1):
+        if -(-tiles // s) * TILE_US <= budget and s * blocks_per_split <= free_slots:
+            return s
+    return auto_splits
+
+
 class VerifyStep:
     """Buffers and call chain of one verification step for a fixed shape."""
 
     def __init__(self, wl: W.Workload, B: Optional[int] = None, mode: Optional[int] = None, device="cuda",
                  num_splits: int = 0, max_prefix: Optional[int] = None, attn_impl: int = E.ATTN_AUTO,
-                 per_layer: bool = False):
+                 per_layer: bool = False, overlap: bool = True):
         self.wl = wl
         self.per_layer = per_layer  # the tree by one et_tree_expand launch per layer, then et_tree_rerank_mask
+        # with num_splits = 0: pick the attention's splits for streaming beside the
+        # tree build (overlap_splits), else the standalone plan
+        self.overlap = overlap
         self.cfg = tree_cfg(wl, B)
         self.B = self.cfg.B
         self.C = E.et_num_candidates(self.cfg)
@@ -123,13 +149,30 @@ class VerifyStep:
 
     def attn_shape(self, inp: StepInputs) -> E.AttnShape:
         mp = self.max_prefix if self.max_prefix is not None else int(inp.host["prefix_len"].max())
-        return E.AttnShape(B=self.B, N=self.cfg.N, Hq=self.wl.Hq, Hkv=self.wl.Hkv, d=self.wl.d,
-                           dtype=E.ET_BF16 if self.wl.dtype == "bf16" else E.ET_F32, scale=self.wl.d ** -0.5,
-                           max_prefix=mp, kv_rows=inp.k_prefix.shape[0], num_splits=self.num_splits,
-                           impl=self.attn_impl,
-                           # Q, K/V and the prefix lengths are step inputs; only the mask comes
-                           # from the kernel before attention
-                           flags=E.ET_ATTN_INPUTS_READY)
+        shape = E.AttnShape(B=self.B, N=self.cfg.N, Hq=self.wl.Hq, Hkv=self.wl.Hkv, d=self.wl.d,
+                            dtype=E.ET_BF16 if self.wl.dtype == "bf16" else E.ET_F32, scale=self.wl.d ** -0.5,
+                            max_prefix=mp, kv_rows=inp.k_prefix.shape[0], num_splits=self.num_splits,
+                            impl=self.attn_impl,
+                            # Q, K/V and the prefix lengths are step inputs; only the mask comes
+                            # from the kernel before attention
+                            flags=E.ET_ATTN_INPUTS_READY)
+        if self.num_splits == 0 and self.overlap and not self.per_layer:
+            shape = dataclasses.replace(shape, num_splits=self.step_splits(shape))
+        return shape
+
+    def step_splits(self, shape: E.AttnShape) -> int:
+        """The attention's split count inside the step (see overlap_splits)."""
+        auto = E.et_tree_attention_splits(shape)
+        tc = shape.dtype == E.ET_BF16 and shape.d == 128 and self.attn_impl in (E.ATTN_AUTO, E.ATTN_TCGEN05)
+        if auto <= 0 or not tc or E.et_tree_build_launches(self.cfg) != 1:
+            return max(auto, 0)
+        G = shape.Hq // shape.Hkv
+        MT = -(-(shape.N * G) // 128)
+        tiles = -(-shape.max_prefix // 64) + -(-shape.N // 64)
+        slots = max(E.et_layer_expanded(self.cfg, l) for l in range(self.cfg.depth)) + 1
+        tree_blocks = self.B * slots * -(-self.cfg.V // 4096)
+        sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+        return overlap_splits(tiles, self.cfg.depth, auto, self.B * shape.Hkv * MT, 2 * max(0, sms - tree_blocks))
 
     def prepare(self, inp: StepInputs) -> None:
         shape = self.attn_shape(inp)
