@@ -513,6 +513,15 @@ def run_gpu(args):
             except Exception as ex:  # report, keep the main line
                 shapes.append({"workload": name, "prefix": L, "error": str(ex)[:300]})
 
+    # ---- attention alone at the batched sweep's shape (7B heads, ragged 512-16384 prefixes) ----
+    batched = []
+    if not args.no_attn_shapes:
+        for Bs in (16, 32):
+            try:
+                batched.append(time_attention_batch(Bs, stream, max(4, min(20, K)), hbm_peak))
+            except Exception as ex:  # report, keep the main line
+                batched.append({"workload": "sweep-7b", "batch": Bs, "error": str(ex)[:300]})
+
     # ---- KV commit of the accepted paths (the step after acceptance), timed alone ----
     commit = time_kv_commit(st, sets[0], wl, cfg, prefix, stream, K)
 
@@ -545,6 +554,7 @@ def run_gpu(args):
                            "GBps": round(achieved, 1),
                            "pct_of_8TBps": round(100 * achieved / 8000.0, 2), "bytes": attn_b},
         "tree_attention_shapes": shapes,
+        "tree_attention_batched": batched,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4),
                      "traffic": args.traffic if args.traffic is not None else
@@ -643,6 +653,83 @@ def time_attention_shape(name, prefix, stream, K, hbm_peak, bf16_peak):
     del sets, base, g
     torch.cuda.empty_cache()
     return out
+
+
+def time_attention_batch(B, stream, K, hbm_peak, seed=11, splits=0):
+    """et_tree_attention alone at the batched sweep's shape: B sequences of
+    7B heads (32 x 128, bf16) with ragged prefixes ~ U{512 .. 16384} (the
+    workload's own seeded lengths) and an EAGLE-2-sized tree of n = 60 each.
+    Q/K/V are N(0,1) drawn on the device (the timing needs no oracle); the
+    mask comes from et_tree_mask_posids on a seeded random tree (parent of
+    row i drawn from rows < i).  The standalone split plan; a graph of K
+    launches over inputs far larger than L2."""
+    import numpy as np
+    import torch
+    from speculative_decoding_eagle_gb300 import binding as E
+    from speculative_decoding_eagle_gb300 import workloads as W
+    wl = W.WORKLOADS["sweep-7b"].with_(B=B)
+    cfg = E.TreeCfg(B=B, V=wl.V, depth=wl.depth, topk=wl.topk, m=wl.m, n=wl.n, temperature=1.0)
+    N = cfg.N
+    prefix = W.prefix_lengths(wl, B)
+    kv_row0 = np.concatenate([[0], np.cumsum(wl.Hkv * prefix.astype(np.int64))[:-1]]).astype(np.int64)
+    rows = int(wl.Hkv * prefix.astype(np.int64).sum())
+    gen = torch.Generator(device="cuda").manual_seed(seed)
+    bf = dict(dtype=torch.bfloat16, device="cuda", generator=gen)
+    q = torch.randn((B, N, wl.Hq, wl.d), **bf)
+    kp = torch.randn((rows, wl.d), **bf)
+    vp = torch.randn((rows, wl.d), **bf)
+    kt = torch.randn((B, N, wl.Hkv, wl.d), **bf)
+    vt = torch.randn((B, N, wl.Hkv, wl.d), **bf)
+    rng = np.random.default_rng(seed)
+    par = np.full((B, N), -1, np.int32)
+    dep = np.zeros((B, N), np.int32)
+    for b in range(B):
+        for i in range(1, N):
+            par[b, i] = rng.integers(0, i)
+            dep[b, i] = dep[b, par[b, i]] + 1
+    tree = E.TreeBuffers.allocate(cfg)
+    tree.flat_parent.copy_(torch.from_numpy(par))
+    tree.flat_depth.copy_(torch.from_numpy(dep))
+    plen = torch.from_numpy(prefix).cuda()
+    row0 = torch.from_numpy(kv_row0).cuda()
+    mask = torch.zeros((B, N, (N + 63) // 64), dtype=torch.int64, device="cuda")
+    posids = torch.zeros((B, N), dtype=torch.int32, device="cuda")
+    E.et_tree_mask_posids(cfg, tree, plen, mask, posids)
+    shape = E.AttnShape(B=B, N=N, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d, dtype=E.ET_BF16, scale=wl.d ** -0.5,
+                        max_prefix=int(prefix.max()), kv_rows=rows, num_splits=splits)
+    ws = E.new_workspace(E.et_tree_attention_workspace_size(shape))
+    out = torch.zeros((B, N, wl.Hq, wl.d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((B, wl.Hq, N), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    call = lambda: E.et_tree_attention(shape, q, kp, vp, row0, plen, kt, vt, mask, out, lse=lse, ws=ws,
+                                       dev_status=status, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            call()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(K):
+            call()
+    g.replay()
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / K
+    nbytes = attention_bytes(wl, prefix)
+    gbps = nbytes / (us * 1e-6) / 1e9
+    res = {"workload": "sweep-7b", "batch": B, "prefix_mean": round(float(prefix.mean()), 1),
+           "prefix_min": int(prefix.min()), "prefix_max": int(prefix.max()),
+           "splits": E.et_tree_attention_splits(shape), "us_per_launch": round(us, 3), "bytes": nbytes,
+           "GBps": round(gbps, 1), "pct_of_8TBps": round(100 * gbps / 8000.0, 2),
+           "frac_hbm": round(gbps / hbm_peak, 4), "bound": "hbm", "status": int(status.item())}
+    del q, kp, vp, kt, vt, ws, out
+    torch.cuda.empty_cache()
+    return res
 
 
 def E_splits(st):
@@ -938,6 +1025,21 @@ def run_split_sweep(args):
                           "GBps": round(abytes / us / 1e3, 1), "launches": K, "input_sets": R}), flush=True)
 
 
+def run_attn_batch(args):
+    """Attention alone at the batched sweep's shape (one JSON line); the
+    command the batched attention's ncu summary is captured from."""
+    import torch
+    from speculative_decoding_eagle_gb300 import binding as E
+    from speculative_decoding_eagle_gb300 import build_lib
+    build_lib.build()
+    E.load()
+    torch.cuda.set_device(0)
+    hbm_peak, _, _ = _peaks()
+    res = time_attention_batch(args.attn_batch, torch.cuda.Stream(), max(4, min(20, args.steps)), hbm_peak,
+                               splits=args.splits)
+    print(json.dumps(res))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -958,6 +1060,8 @@ def main():
     ap.add_argument("--splits-sweep", default="", help="comma-separated KV split counts: time attention alone at each")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per attention launch from an ncu capture of the same kernel")
+    ap.add_argument("--attn-batch", type=int, default=0,
+                    help="only time attention alone at the batched sweep's shape with this batch (one JSON line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -965,6 +1069,8 @@ def main():
         run_reference(args)
     elif args.splits_sweep:
         run_split_sweep(args)
+    elif args.attn_batch:
+        run_attn_batch(args)
     else:
         run_gpu(args)
 

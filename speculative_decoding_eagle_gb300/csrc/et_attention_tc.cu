@@ -44,6 +44,7 @@ namespace et {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kLptMaxB = 64;  // batches whose sequences go out longest prefix first
 constexpr int kStages = 2;                           // K ring and V ring, 2 tiles each (two blocks per SM)
 constexpr uint32_t kHalfBytes = kTcKeys * 128;       // 64 rows x 128 B (64 of the 128 dims)
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;      // one K or V tile
@@ -107,6 +108,27 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, limit));
 }
 
+// One warp: the sequence whose prefix is the blockIdx.z-th longest (ties:
+// lower index first) into *seq, its first KV row into *row0.  B <= kLptMaxB.
+__device__ __noinline__ void rank_by_prefix(const int *prefix_len, const long long *kv_row0, int B, int *s_len, int *seq,
+                                            long long *row0) {
+  const int lane = threadIdx.x & 31;
+  for (int j = lane; j < B; j += 32) s_len[j] = prefix_len[j];
+  __syncwarp();
+  for (int c = lane; c < B; c += 32) {
+    const int Lc = s_len[c];
+    int rank = 0;
+    for (int j = 0; j < B; ++j) {
+      const int Lj = s_len[j];
+      rank += (Lj > Lc || (Lj == Lc && j < c)) ? 1 : 0;
+    }
+    if (rank == (int)blockIdx.z) {
+      *seq = c;
+      *row0 = kv_row0 ? kv_row0[c] : 0;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 2)
     k_attn_tc(const __grid_constant__ CUtensorMap tm_kp, const __grid_constant__ CUtensorMap tm_vp,
               const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt,
@@ -120,16 +142,32 @@ __global__ void __launch_bounds__(kThreads, 2)
   auto bar = [&](int i) -> uint32_t { return sb + kOffBar + 8u * (uint32_t)i; };
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int s = blockIdx.x, g = blockIdx.y / a.MT, mt = blockIdx.y - g * a.MT, b = blockIdx.z;
+  const int s = blockIdx.x, g = blockIdx.y / a.MT, mt = blockIdx.y - g * a.MT;
   const int N = a.N;
 
-  // with inputs_ready the prefix length and start row are inputs: their loads
-  // go out first and overlap the set-up
+  // Longest prefix first: blocks go out in grid order (sequence = z slowest),
+  // so block z takes the sequence with the z-th longest prefix (ties: lower
+  // index first) and the ragged batch's longest streams start in the first
+  // wave instead of trailing the last one.  One warp ranks the lengths
+  // (B <= 64; larger batches keep the grid order).
+  __shared__ int s_len[kLptMaxB];
+  __shared__ int s_seq;
+  __shared__ long long s_row0;
+  const bool lpt = a.B > 1 && a.B <= kLptMaxB;
+  // warp 2 ranks; the caller makes s_seq / s_row0 visible with a block barrier
+  auto rank_sequences = [&]() { rank_by_prefix(a.prefix_len, a.kv_row0, a.B, s_len, &s_seq, &s_row0); };
+
+  // with inputs_ready the prefix lengths and start rows are inputs: their
+  // loads go out first and overlap the set-up
   int L_in = 0;
   long long row0_in = 0;
   if (a.inputs_ready) {
-    L_in = a.prefix_len[b];
-    row0_in = a.kv_row0 ? a.kv_row0[b] : 0;
+    if (lpt) {
+      if (warp == 2) rank_sequences();
+    } else {
+      L_in = a.prefix_len[blockIdx.z];
+      row0_in = a.kv_row0 ? a.kv_row0[blockIdx.z] : 0;
+    }
   }
   // ---- set-up that touches no global memory (it overlaps the previous kernel's tail) ----
   if (warp == 3 && lane < 5) {  // the five tensor maps into the TMA descriptor cache
@@ -171,6 +209,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (!a.inputs_ready) {
     pdl_wait();     // the previous kernel in the stream has completed (the inputs may come from it)
     pdl_trigger();  // after the TMEM allocation: a waiting dependent block must not hold the TMEM this block needs
+    if (lpt) {
+      if (warp == 2) rank_sequences();
+      __syncthreads();
+    }
+  }
+  const int b = lpt ? s_seq : (int)blockIdx.z;
+  if (a.inputs_ready && lpt) {
+    L_in = s_len[b];
+    row0_in = s_row0;
   }
   // with inputs_ready the previous kernel writes none of Q, K/V or the prefix
   // lengths: the whole prefix streams before the wait; the softmax waits
