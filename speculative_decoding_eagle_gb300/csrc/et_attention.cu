@@ -503,6 +503,14 @@ static bool make_plan(const et_attn_shape *s, AttnPlan *p) {
       // splits, 12.4 at 3, 12.8 at 5, 13.3 at 8)
       if (S <= 0) {
         S = (int)((17LL * sm_count()) / (10LL * base));
+        // a ragged batch whose blocks go out longest prefix first
+        // (kLptMaxB) runs in several waves: about five blocks per SM keep
+        // the last wave short (7B heads, prefixes 512..16384, measured on
+        // GB300: 4 sequences best at 4 splits, 8 at 2-4, 16 at 2, 32 at 1)
+        if (s->B > 1 && s->B <= kLptMaxB) {
+          const int waves = (int)((5LL * sm_count() + base - 1) / base);
+          if (S < waves) S = waves;
+        }
         const int by_tiles = (2 * T + 8) / 9;  // ceil(T / 4.5)
         if (S > by_tiles) S = by_tiles;
         if (S > cap) S = cap;

@@ -44,7 +44,6 @@ namespace et {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kLptMaxB = 64;  // batches whose sequences go out longest prefix first
 constexpr int kStages = 2;                           // K ring and V ring, 2 tiles each (two blocks per SM)
 constexpr uint32_t kHalfBytes = kTcKeys * 128;       // 64 rows x 128 B (64 of the 128 dims)
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;      // one K or V tile
@@ -129,6 +128,10 @@ __device__ __noinline__ void rank_by_prefix(const int *prefix_len, const long lo
   }
 }
 
+// kLpt: a ragged batch of 2..kLptMaxB sequences goes out longest prefix
+// first; the other instance keeps the grid order (and the registers the
+// remapped index would hold)
+template <bool kLpt>
 __global__ void __launch_bounds__(kThreads, 2)
     k_attn_tc(const __grid_constant__ CUtensorMap tm_kp, const __grid_constant__ CUtensorMap tm_vp,
               const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt,
@@ -153,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ int s_len[kLptMaxB];
   __shared__ int s_seq;
   __shared__ long long s_row0;
-  const bool lpt = a.B > 1 && a.B <= kLptMaxB;
+  constexpr bool lpt = kLpt;
   // warp 2 ranks; the caller makes s_seq / s_row0 visible with a block barrier
   auto rank_sequences = [&]() { rank_by_prefix(a.prefix_len, a.kv_row0, a.B, s_len, &s_seq, &s_row0); };
 
@@ -214,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       __syncthreads();
     }
   }
-  const int b = lpt ? s_seq : (int)blockIdx.z;
+  const int b = lpt ? s_seq : (int)blockIdx.z;  // lpt is a compile-time constant
   if (a.inputs_ready && lpt) {
     L_in = s_len[b];
     row0_in = s_row0;
@@ -748,7 +751,10 @@ bool make_map_q(CUtensorMap *m, const void *base, int G, int Hkv, long long toke
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t set_smem_attr() { return et_smem_attr((const void *)k_attn_tc, (int)kSmemBytes); }
+cudaError_t set_smem_attr() {
+  const cudaError_t e = et_smem_attr((const void *)k_attn_tc<false>, (int)kSmemBytes);
+  return e != cudaSuccess ? e : et_smem_attr((const void *)k_attn_tc<true>, (int)kSmemBytes);
+}
 
 // clusters of more than 8 blocks (the portable limit) need an opt-in per
 // device; thread-safe
@@ -759,7 +765,9 @@ cudaError_t allow_big_clusters() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
   if (done[dev]) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute((const void *)k_attn_tc, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaError_t e = cudaFuncSetAttribute((const void *)k_attn_tc<false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute((const void *)k_attn_tc<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e == cudaSuccess) done[dev] = 1;
   return e;
 }
@@ -787,8 +795,11 @@ et_status tc_attention_launch(const TcLaunch &a, cudaStream_t stream) {
   if (!ok) return ET_ERR_INVALID_ARG;
   if (set_smem_attr() != cudaSuccess) return ET_ERR_CUDA;
   if (a.S > 8 && allow_big_clusters() != cudaSuccess) return ET_ERR_CUDA;
-  return et_launch(k_attn_tc, dim3(a.S, a.Hkv * a.MT, a.B), dim3(kThreads), kSmemBytes, stream, a.S > 1 ? a.S : 0,
-                   m_kp, m_vp, m_kt, m_vt, m_q, la);
+  if (a.B > 1 && a.B <= kLptMaxB)
+    return et_launch(k_attn_tc<true>, dim3(a.S, a.Hkv * a.MT, a.B), dim3(kThreads), kSmemBytes, stream,
+                     a.S > 1 ? a.S : 0, m_kp, m_vp, m_kt, m_vt, m_q, la);
+  return et_launch(k_attn_tc<false>, dim3(a.S, a.Hkv * a.MT, a.B), dim3(kThreads), kSmemBytes, stream,
+                   a.S > 1 ? a.S : 0, m_kp, m_vp, m_kt, m_vt, m_q, la);
 }
 
 }  // namespace et

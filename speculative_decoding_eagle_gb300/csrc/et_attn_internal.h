@@ -32,6 +32,7 @@ constexpr int kTcRows = 128;   // query rows per tile (TMEM lanes)
 constexpr int kTcKeys = 64;    // keys per K/V tile
 constexpr int kTcDim = 128;    // head dim of the tcgen05 path
 constexpr int kTcMaxSplits = 16;  // KV splits of one row tile = one thread-block cluster (past 8: non-portable size)
+constexpr int kLptMaxB = 64;      // batches whose sequences go out longest prefix first (tcgen05 path)
 
 // workspace bytes of the tcgen05 path: the split merge's partial rows and
 // (max, sum) pairs (0 for one split)
