@@ -268,6 +268,8 @@ ATTN_CASES = [
     (1, 61, 2, 2, 128, [8192], "bf16", 7, 0),       # 7 splits of 129 key tiles
     (1, 61, 4, 4, 128, [1024], "bf16", 9, 0),       # 9 splits (a non-portable cluster) of 17 key tiles
     (2, 81, 16, 2, 128, [3000, 700], "bf16", 12, 0),  # 12 splits, GQA rows merged through L2
+    (5, 33, 4, 4, 128, [513, 64, 513, 1000, 64], "bf16", 0, 0),  # ragged batch out longest first, equal lengths
+    (66, 9, 2, 2, 128, [(37 * i) % 301 for i in range(66)], "bf16", 0, 0),  # past 64 sequences: grid order
 ]
 
 
