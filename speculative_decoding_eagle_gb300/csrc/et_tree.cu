@@ -698,6 +698,7 @@ struct ExpandClSmem {
   unsigned long long lists[kClLists * kMaxTopk];  // leader: warp (q, w)'s candidates, ascending, at (8 q + w) * k
   int counts[kClLists];                           // leader: how many
   unsigned long long cand[kClWarps][32];          // per-warp selection scratch
+  float2 norm;                                     // leader: the row's (max, log of the sum of exp)
 };
 
 __device__ __forceinline__ void cl_st_s32(uint32_t addr, int v) {
@@ -770,26 +771,30 @@ __device__ __forceinline__ void row_warp_part(float (&v)[4 * kClVec], int base, 
   if (lane == 0) cl_st_s32(cl_map(&sh.counts[list], 0), n);
 }
 
-// The leader's first warp, once every warp's candidates have landed: the
-// row's normaliser (log-softmax, from the warp pairs) and its top-k children
-// with their path keys (EAGLE-2 article: expansion phase; the value of a
-// path is the product of confidences, here a sum of fixed-point log-probs).
-// The candidates number at least k (every warp among the k holding the
-// largest maxima sends its maximum); a few more usually: ranked by counting.
-// More than 32: k rounds of the smallest list head.  nl: warp lists of the
-// row (8 R).
+// The leader's first two warps, once every warp's candidates have landed:
+// warp 1 forms the row's normaliser (log-softmax, from the warp pairs) while
+// warp 0 selects the row's top-k children, then writes them with their path
+// keys (EAGLE-2 article: expansion phase; the value of a path is the product
+// of confidences, here a sum of fixed-point log-probs).  The candidates
+// number at least k (every warp among the k holding the largest maxima sends
+// its maximum); a few more usually: ranked by counting.  More than 32: k
+// rounds of the smallest list head.  nl: warp lists of the row (8 R).
 __device__ __forceinline__ void row_leader_part(ExpandClSmem &sh, int par, int nl, int k, int V, const et_tree &tree,
                                                 long long o0, int parent, long long pkey) {
   const int lane = threadIdx.x & 31;
-  const float2 pa = lane < nl ? sh.pairs[par][lane] : make_float2(-INFINITY, 0.f);
-  const float2 pb = lane + 32 < nl ? sh.pairs[par][lane + 32] : make_float2(-INFINITY, 0.f);
-  const float M = warp_max_f(fmaxf(pa.x, pb.x));
-  float part = 0.f;
-  if (M > -INFINITY) {
-    part = (pa.x > -INFINITY ? pa.y * expf(pa.x - M) : 0.f) + (pb.x > -INFINITY ? pb.y * expf(pb.x - M) : 0.f);
+  if ((threadIdx.x >> 5) == 1) {
+    const float2 pa = lane < nl ? sh.pairs[par][lane] : make_float2(-INFINITY, 0.f);
+    const float2 pb = lane + 32 < nl ? sh.pairs[par][lane + 32] : make_float2(-INFINITY, 0.f);
+    const float M = warp_max_f(fmaxf(pa.x, pb.x));
+    float part = 0.f;
+    if (M > -INFINITY) {
+      part = (pa.x > -INFINITY ? pa.y * expf(pa.x - M) : 0.f) + (pb.x > -INFINITY ? pb.y * expf(pb.x - M) : 0.f);
+    }
+    const float S = warp_sum(part);
+    if (lane == 0) sh.norm = make_float2(M, (M > -INFINITY) ? logf(S) : 0.f);
+    asm volatile("bar.sync 1, 64;" ::: "memory");  // with warp 0: the normaliser is in
+    return;
   }
-  const float S = warp_sum(part);
-  const float logS = (M > -INFINITY) ? logf(S) : 0.f;
   const int la = lane, lb = lane + 32;
   const int ca = la < nl ? sh.counts[la] : 0, cb = lb < nl ? sh.counts[lb] : 0;
   const int nc = (int)__reduce_add_sync(0xffffffffu, (unsigned int)(ca + cb));
@@ -816,6 +821,8 @@ __device__ __forceinline__ void row_leader_part(ExpandClSmem &sh, int par, int n
       }
     }
   }
+  asm volatile("bar.sync 1, 64;" ::: "memory");  // with warp 1
+  const float M = sh.norm.x, logS = sh.norm.y;
   if (lane < k) {
     const float z = zid_value(key_r);
     const int id = (int)zid_id(key_r);
@@ -869,8 +876,8 @@ __global__ void __launch_bounds__(kClThreads) k_expand_cl(ExpandRowArgs a) {
   if (q != 0) return;
   cl_wait();
 
-  // ---- the leader's first warp: the row's top-k; write the children ----
-  if (warp == 0)
+  // ---- the leader's first two warps: the row's top-k and normaliser; write the children ----
+  if (warp < 2)
     row_leader_part(sh, 0, R * kClWarps, k, a.V, a.tree, (long long)b * a.C + a.base_next + s * k, node, pkey);
   if (a.m_next <= 0) return;  // last layer: no frontier to pick
 
@@ -1158,8 +1165,9 @@ __global__ void __launch_bounds__(kClThreads) k_tree_build(BuildArgs a) {
     if (bad && q == 0 && t == 0) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
     cl_arrive();  // release the candidates
     cl_wait();    // every block's candidates have landed in the leader (and every block is done with this layer)
-    if (q == 0 && warp == 0) {
+    if (q == 0 && warp < 2)
       row_leader_part(sh_e, layer & 1, R * kClWarps, k, a.V, a.tree, (long long)b * a.C + base_next + s * k, node, pkey);
+    if (q == 0 && warp == 0) {
       __threadfence();
       __syncwarp();  // every child of this row is written
       if (lane == 0) {
