@@ -203,10 +203,11 @@ struct WalkSmem {
 
 // Phase 2 of acceptance, run by the last row-block of sequence b: everything
 // the walk needs (row statistics, the decision phase 1 took at each row,
-// uniforms) is fetched in parallel; one warp walks the kept tree from the
-// root (greedy: 32 candidate rows per ballot; stochastic: the accepted child
-// of each row); the block then draws the bonus token at the row where the
-// walk stops.
+// uniforms) is fetched in parallel; greedy: every row's accepted child (its
+// first child whose token is the row's argmax) is found at once by shared-
+// memory atomics; one warp then walks the accepted children from the root
+// (stochastic: the child phase 1 accepted at each row); the block draws the
+// bonus token at the row where the walk stops.
 template <int NT, bool kDraftQ>
 __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
   const int t = threadIdx.x;
@@ -233,10 +234,19 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
       w.acc[j] = child_of(__float_as_int(lo4.w), j);
     } else if (!greedy) {  // point-mass: the decision phase 1 took at the row
       w.acc[j] = child_of(__float_as_int(ld_cg(a.dq + 8 * (fo + j) + 3)), j);
+    } else {
+      w.acc[j] = 0x7fffffff;  // greedy: filled below
     }
   }
   __syncthreads();
-  if (t < 32) {  // one warp walks: 32 candidate rows per ballot
+  if (greedy) {  // every row's accepted child at once: its first child carrying the row's argmax token
+    for (int j = t; j < N; j += NT) {
+      const int p = par[j];
+      if (p >= 0 && p < j && tokf[j] == __float_as_int(w.rs0[p])) atomicMin(&w.acc[p], j);
+    }
+    __syncthreads();
+  }
+  if (t < 32) {  // one warp walks the accepted children
     const int lane = t;
     int cur = 0, alen = 0, nrej = 0, kids = 0;
     if (lane == 0) w.opath[0] = 0;
@@ -246,11 +256,8 @@ __device__ void verify_walk(const VerifyArgs &a, int b, WalkSmem &w) {
       kids = 0;
       if (greedy) {
         const int am = __float_as_int(w.rs0[cur]);
-        for (int j0 = cur + 1; j0 < N; j0 += 32) {  // first row (ascending) that is a child with token am
-          const int j = j0 + lane;
-          const unsigned int hit = __ballot_sync(0xffffffffu, j < N && par[j] == cur && tokf[j] == am);
-          if (hit) { nxt = j0 + __ffs(hit) - 1; break; }
-        }
+        const int ac = w.acc[cur];  // the first row (ascending) that is a child with token am
+        nxt = ac < N ? ac : -1;
         if (nxt < 0 && lane == 0) w.otok[alen] = am;
       } else {  // stochastic: phase 1 decided every row
         const int ac = w.acc[cur];
