@@ -55,3 +55,11 @@ def test_step_spread_percentiles():
     assert s == {"median_ms": 0.3, "p10_ms": 0.14, "p90_ms": 0.46}
     assert bench.step_spread([0.089] * 7) == {"median_ms": 0.089, "p10_ms": 0.089, "p90_ms": 0.089}
     assert bench.step_spread([])["median_ms"] is None
+
+
+def test_recorded_attention_traffic_matches_the_kernel_sources():
+    """The bench reports the attention kernel's DRAM traffic only while the
+    committed ncu summary was taken on the same sources; the headline
+    workload's summary must be current."""
+    assert bench.recorded_attention_traffic("llama2-7b", 1, 1024) is not None
+    assert bench.recorded_attention_traffic("llama2-7b", 1, 999) is None
