@@ -522,6 +522,15 @@ def run_gpu(args):
             except Exception as ex:  # report, keep the main line
                 batched.append({"workload": "sweep-7b", "batch": Bs, "error": str(ex)[:300]})
 
+    # ---- the whole step at the batched sweep's shape ----
+    sweep = []
+    if not args.no_attn_shapes:
+        for Bs in (16, 32):
+            try:
+                sweep.append(time_sweep_step(Bs, stream, max(3, min(10, K)), hbm_peak))
+            except Exception as ex:  # report, keep the main line
+                sweep.append({"workload": "sweep-7b", "batch": Bs, "error": str(ex)[:300]})
+
     # ---- KV commit of the accepted paths (the step after acceptance), timed alone ----
     commit = time_kv_commit(st, sets[0], wl, cfg, prefix, stream, K)
 
@@ -555,6 +564,7 @@ def run_gpu(args):
                            "pct_of_8TBps": round(100 * achieved / 8000.0, 2), "bytes": attn_b},
         "tree_attention_shapes": shapes,
         "tree_attention_batched": batched,
+        "sweep_step": sweep,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4),
                      "traffic": args.traffic if args.traffic is not None else
@@ -728,6 +738,93 @@ def time_attention_batch(B, stream, K, hbm_peak, seed=11, splits=0):
            "GBps": round(gbps, 1), "pct_of_8TBps": round(100 * gbps / 8000.0, 2),
            "frac_hbm": round(gbps / hbm_peak, 4), "bound": "hbm", "status": int(status.item())}
     del q, kp, vp, kt, vt, ws, out
+    torch.cuda.empty_cache()
+    return res
+
+
+def time_sweep_step(B, stream, K, hbm_peak, seed=23):
+    """The whole verification step at the batched sweep's shape: B sequences
+    of 7B heads with ragged prefixes ~ U{512 .. 16384} (the workload's seeded
+    lengths), EAGLE-2 trees of depth 6, top-k 10, m 10, n 60, point-mass
+    stochastic acceptance.  The inputs follow the same recipe as the seeded
+    host generators but are drawn on the device (about 9 GB at B = 32, which
+    the host would take minutes to write): target logits -slope * ln(rank) +
+    N(0, 1) over a random permutation of the vocabulary per node, draft =
+    target + N(0, sigma^2), Q/K/V ~ N(0, 1) in bf16.  One CUDA graph per
+    step, replayed K times over inputs far larger than L2; each call also
+    timed alone."""
+    import numpy as np
+    import torch
+    from speculative_decoding_eagle_gb300 import binding as E
+    from speculative_decoding_eagle_gb300 import step as S
+    from speculative_decoding_eagle_gb300 import workloads as W
+    wl = W.WORKLOADS["sweep-7b"].with_(B=B)
+    st = S.VerifyStep(wl)
+    cfg, C = st.cfg, st.C
+    R, N = C + 1, cfg.N
+    gen = torch.Generator(device="cuda").manual_seed(seed)
+    dev = dict(device="cuda", generator=gen)
+    rows = B * R
+    target = torch.empty((rows, wl.V), dtype=torch.float32, device="cuda")
+    draft = torch.empty_like(target)
+    by_rank = -wl.slope * torch.log(torch.arange(1, wl.V + 1, device="cuda", dtype=torch.float32))
+    for r0 in range(0, rows, 256):
+        r1 = min(rows, r0 + 256)
+        perm = torch.argsort(torch.rand((r1 - r0, wl.V), **dev), dim=1)  # the token at each rank
+        z = by_rank.expand(r1 - r0, -1) + torch.randn((r1 - r0, wl.V), **dev)
+        target[r0:r1].scatter_(1, perm, z)
+        draft[r0:r1] = target[r0:r1] + wl.sigma * torch.randn((r1 - r0, wl.V), **dev)
+        del perm, z
+    prefix = W.prefix_lengths(wl, B)
+    kv_row0 = np.concatenate([[0], np.cumsum(wl.Hkv * prefix.astype(np.int64))[:-1]]).astype(np.int64)
+    kv_rows = int(wl.Hkv * prefix.astype(np.int64).sum())
+    bf = dict(dtype=torch.bfloat16, device="cuda", generator=gen)
+    inp = S.StepInputs(
+        draft=draft, target=target,
+        row_of_node=(torch.arange(B, dtype=torch.int32, device="cuda")[:, None] * R
+                     + torch.arange(R, dtype=torch.int32, device="cuda")[None, :]).contiguous(),
+        root_tok=torch.from_numpy(W.root_tokens(wl, B)).cuda(),
+        prefix_len=torch.from_numpy(prefix).cuda(), kv_row0=torch.from_numpy(kv_row0).cuda(),
+        q=torch.randn((B, N, wl.Hq, wl.d), **bf), k_prefix=torch.randn((kv_rows, wl.d), **bf),
+        v_prefix=torch.randn((kv_rows, wl.d), **bf), k_tree=torch.randn((B, N, wl.Hkv, wl.d), **bf),
+        v_tree=torch.randn((B, N, wl.Hkv, wl.d), **bf),
+        uniforms=torch.rand((B, N), device="cuda", generator=gen), host={"prefix_len": prefix})
+    st.prepare(inp)
+    cur = torch.cuda.current_stream()
+
+    def graph_us(call):
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                call()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            call()
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(cur)
+        for _ in range(K):
+            g.replay()
+        e1.record(cur)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1000.0 / K
+
+    step_us = graph_us(lambda: st.run(inp, stream=stream))
+    tree_us = graph_us(lambda: st.build_tree(inp, stream=stream))
+    attn_us = graph_us(lambda: st.attention(inp, stream=stream))
+    accept_us = graph_us(lambda: st.accept(inp, stream=stream))
+    attn_b = attention_bytes(wl, prefix)
+    res = {"workload": "sweep-7b", "batch": B, "prefix_mean": round(float(prefix.mean()), 1),
+           "accept": "stoch_point", "ms_per_step": round(step_us / 1000.0, 4),
+           "steps_per_s": round(1e6 / step_us, 1), "sequences_per_s": round(B * 1e6 / step_us, 1),
+           "tree_launches": st.launches() - 2, "attention_splits": E.et_tree_attention_splits(st.shape),
+           "calls_alone_us": {"tree": round(tree_us, 2), "attention": round(attn_us, 2),
+                              "accept": round(accept_us, 2)},
+           "attention_GBps": round(attn_b / (attn_us * 1e-6) / 1e9, 1),
+           "attention_pct_of_8TBps": round(100 * attn_b / (attn_us * 1e-6) / 8e12, 2),
+           "inputs": "drawn on the device with the workload's recipe", "status": int(st.dev_status.item())}
+    del inp, target, draft, st
     torch.cuda.empty_cache()
     return res
 
