@@ -798,6 +798,202 @@ __global__ void __launch_bounds__(kVClThreads) k_verify_cl(VerifyArgs a) {
   verify_walk<kVClThreads, kDraftQ>(a, b, w);
 }
 
+// ---------------------------------------------------------------------------
+// Acceptance as one walk per sequence (greedy and point-mass, V <= 32768),
+// for batches large enough that reading every flat row costs more than the
+// walk's dependent steps: one cluster of ceil(V / 4096) CTAs per sequence
+// follows the accepted children from the root, reading only the rows on the
+// path and the row it stops at (at most D + 1 of the N rows).  Each step is
+// the parallel kernel's phase 1 for one row: every CTA reduces its 4096-token
+// slice (greedy: the best (value desc, id asc) key; point-mass: (max raw
+// logit, sum of exp((z - max) / T)) with the children's tokens left out),
+// stores it into every CTA of the cluster (by step parity), and after one
+// cluster barrier every CTA merges the slices in CTA order and decides the
+// row the same way (greedy: the first child carrying the argmax token;
+// point-mass: pm_decide on the same inputs), so the CTAs walk in step.  At
+// the stop row the leader CTA draws the bonus token (greedy: the argmax;
+// point-mass: the chunk inverse CDF of the residual, the slices' statistics
+// being its chunks).
+// ---------------------------------------------------------------------------
+// From this many sequences on, greedy and point-mass acceptance walk each
+// sequence's path in one cluster (measured on GB300 at the 7B shape,
+// point-mass: 32 sequences 182 us reading every row against 25 us walking,
+// 16 sequences 97 against 29 us; at batch 1 the parallel kernel's 8 us beats
+// the walk's dependent steps).
+constexpr int kSeqWalkMinB = 8;
+
+struct SeqWalkSmem {
+  int par[kMaxN], tok[kMaxN], node[kMaxN];
+  int kid[kMaxN];
+  int ktok[kMaxN];
+  float zk[kMaxN], uk[kMaxN];
+  unsigned int rejbits[kMaxSpanWords];
+  unsigned long long wkey[kVClThreads / 32];
+  float wmax[kVClThreads / 32], wsum[kVClThreads / 32];
+  unsigned long long gkey[2][kVClMaxCtas];  // every CTA's best key, by step parity
+  float2 gms[2][kVClMaxCtas];               // every CTA's (max, sum), by step parity
+  int opath[kMaxDepth + 2], otok[kMaxDepth + 2];
+  int rej[kMaxN];
+  float redz[32];
+  int redi[32];
+  float cdf_tsum[kMaxV / kVChunk];
+  int s_nkid, s_acc;
+};
+
+__global__ void __launch_bounds__(kVClThreads) k_verify_seq(VerifyArgs a) {
+  constexpr int NW = kVClThreads / 32;
+  __shared__ SeqWalkSmem w;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int R = gridDim.x;
+  const int q = (int)cl_rank();
+  const int b = blockIdx.y;
+  const int N = a.N;
+  const long long fo = (long long)b * N;
+  const bool greedy = a.mode == ET_ACCEPT_GREEDY;
+  const float invT = 1.f / a.T;
+  cl_arrive_relaxed();  // this block has started (waited on before any remote store)
+  pdl_wait();           // the previous kernel in the stream has completed
+  pdl_trigger();        // only now may the next kernel launch: at most one waits ahead
+  for (int j = t; j < N; j += kVClThreads) {
+    w.par[j] = a.flat_parent[fo + j];
+    w.tok[j] = a.flat_tok[fo + j];
+    w.node[j] = a.flat_node[fo + j];
+  }
+  if (t == 0) w.opath[0] = 0;
+  __syncthreads();
+  cl_wait();
+  const int base = q * kVClSpan;
+  int cur = 0, alen = 0, flag = 0, badp = 0;
+  float M = -INFINITY, S = 0.f;
+  int am = -1, acc = -1, nkid = 0;
+  const float *zrow = nullptr;
+  for (int step = 0; step <= a.D; ++step) {
+    const int par = step & 1;
+    nkid = child_list<kVClThreads>(w.par, N, cur, w.kid, &w.s_nkid);
+    int bad = 0;
+    zrow = table_row(a.tlog, a.tstride, a.tmap, a.C, b, w.node[cur], fo + cur, bad);
+    badp |= bad;
+    float v[4 * kVClVec];
+    cl_load_span(zrow, base, a.vec4t, a.V, v, flag);
+    if (greedy) {
+      unsigned long long best = ~0ull;
+#pragma unroll
+      for (int e = 0; e < 4 * kVClVec; ++e) {
+        const int id = base + (e >> 2) * (kVClThreads * 4) + t * 4 + (e & 3);
+        if (id < a.V) {
+          const unsigned long long kk = zid_key(v[e], (unsigned int)id);
+          best = kk < best ? kk : best;
+        }
+      }
+      best = warp_min_u64(best);
+      if (lane == 0) w.wkey[warp] = best;
+      __syncthreads();
+      if (warp == 0) {
+        const unsigned long long kk = warp_min_u64(w.wkey[lane & (NW - 1)]);
+        if (lane < R) cl_st_u64(cl_map(&w.gkey[par][q], (uint32_t)lane), kk);
+      }
+    } else {
+      // the children's tokens leave this block's sums (the residual after every child is rejected)
+      for (int x = t; x < kVClSpan / 32; x += kVClThreads) w.rejbits[x] = 0u;
+      __syncthreads();
+      if (nkid > 0) {
+        mark_child_tokens(a, fo, w.kid, nkid, base, kVClSpan / 32, w.rejbits);
+#pragma unroll
+        for (int e = 0; e < 4 * kVClVec; ++e) {
+          const int off = (e >> 2) * (kVClThreads * 4) + t * 4 + (e & 3);
+          if ((w.rejbits[off >> 5] >> (off & 31)) & 1u) v[e] = -INFINITY;
+        }
+        pm_child_inputs(a, fo, w.kid, nkid, zrow, w.ktok, w.zk, w.uk);  // every CTA: the same inputs
+      }
+      float lm = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < 4 * kVClVec; ++e) lm = fmaxf(lm, v[e]);
+      lm = warp_max(lm);
+      if (lane == 0) w.wmax[warp] = lm;
+      __syncthreads();
+      float Mq = w.wmax[0];
+#pragma unroll
+      for (int x = 1; x < NW; ++x) Mq = fmaxf(Mq, w.wmax[x]);
+      float ls = 0.f;
+      if (Mq > -INFINITY) {
+#pragma unroll
+        for (int e = 0; e < 4 * kVClVec; ++e) ls += exp_fast((v[e] - Mq) * invT);
+      }
+      ls = warp_sum(ls);
+      if (lane == 0) w.wsum[warp] = ls;
+      __syncthreads();
+      if (t < R) {  // this block's pair into every block of the cluster
+        float Sq = 0.f;
+#pragma unroll
+        for (int x = 0; x < NW; ++x) Sq += w.wsum[x];
+        cl_st_f32x2(cl_map(&w.gms[par][q], (uint32_t)t), Mq, Sq);
+      }
+    }
+    cl_arrive();  // release this block's stores
+    cl_wait();    // every block's statistic is in every block
+    int nxt = -1;
+    if (greedy) {
+      unsigned long long kk = w.gkey[par][0];
+      for (int x = 1; x < R; ++x) kk = w.gkey[par][x] < kk ? w.gkey[par][x] : kk;
+      am = (int)zid_id(kk);
+      for (int k = 0; k < nkid && nxt < 0; ++k)
+        if (w.tok[w.kid[k]] == am) nxt = w.kid[k];  // the first child (row order) with the argmax token
+    } else {
+      M = -INFINITY;
+      for (int x = 0; x < R; ++x) M = fmaxf(M, w.gms[par][x].x);
+      S = 0.f;
+      for (int x = 0; x < R; ++x)  // the same order in every block: the same M and S
+        S += w.gms[par][x].x > -INFINITY ? w.gms[par][x].y * expf((w.gms[par][x].x - M) * invT) : 0.f;
+      if (warp == 0) {
+        const int d = nkid > 0 ? pm_decide(nkid, w.kid, w.zk, w.uk, M, S, invT) : -1;
+        if (lane == 0) w.s_acc = d;
+      }
+      __syncthreads();
+      acc = w.s_acc;
+      nxt = acc >= 0 ? acc : -1;
+    }
+    if (nxt < 0 || alen >= a.D) break;
+    if (q == 0 && t == 0) {
+      w.otok[alen] = w.tok[nxt];
+      w.opath[alen + 1] = nxt;
+    }
+    ++alen;
+    cur = nxt;
+    __syncthreads();  // the step's shared arrays are rewritten by the next
+  }
+  if (flag) flag_status(a.dev_status, ET_DEV_NONFINITE);
+  if (q != 0) return;
+  // ---- the leader: the bonus token at the stop row, then the outputs ----
+  if (greedy) {
+    if (t == 0) w.otok[alen] = am;
+  } else {
+    const int nrej = acc == -2 ? nkid : 0;  // every child of the stop row rejected: their tokens are out of the draw
+    for (int k = t; k < nrej; k += kVClThreads) w.rej[k] = w.tok[w.kid[k]];
+    __syncthreads();
+    // the stop row's chunk statistics, into the workspace the draw reads them
+    // from (through L2, as the parallel kernel's are)
+    const int last = alen;  // the walk stopped in step alen (one step per accepted child, then the stop row)
+    float *cst = a.part + (fo + cur) * (long long)a.nchunk * 2;
+    for (int x = t; x < R; x += kVClThreads) {
+      cst[2 * x] = w.gms[last & 1][x].x;
+      cst[2 * x + 1] = w.gms[last & 1][x].y;
+    }
+    __syncthreads();
+    const CdfRow cdf{kVClSpan, R, a.V, a.vec4t, a.T, invT};  // chunk maxima are raw logits
+    const int bonus = bonus_from_chunks<kVClThreads, true>(cdf, zrow, cst, M, a.uniforms[fo], w.rej, nrej, w.redz,
+                                                          w.redi, w.cdf_tsum, w.rejbits);
+    if (t == 0) w.otok[alen] = bonus;
+  }
+  __syncthreads();
+  const long long po = (long long)b * (a.D + 1);
+  for (int j = t; j <= a.D; j += kVClThreads) {
+    a.path[po + j] = j <= alen ? w.opath[j] : -1;
+    a.tokens[po + j] = j <= alen ? w.otok[j] : -1;
+  }
+  if (t == 0) a.accept_len[b] = alen;
+  if (badp && t == 0) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
+}
+
 }  // namespace et
 
 using namespace et;
@@ -847,6 +1043,8 @@ extern "C" et_status et_verify_accept(const et_tree_cfg *cfg, et_accept_mode mod
     a.cdf_nch = R;
     if (mode == ET_ACCEPT_STOCH_DRAFTQ)
       return et_launch(k_verify_cl<true>, dim3(R, cfg->B * N, 1), dim3(kVClThreads), 0, (cudaStream_t)stream, R, a);
+    if (cfg->B >= kSeqWalkMinB)  // the walk reads at most D + 1 of the N rows per sequence
+      return et_launch(k_verify_seq, dim3(R, cfg->B, 1), dim3(kVClThreads), 0, (cudaStream_t)stream, R, a);
     return et_launch(k_verify_cl<false>, dim3(R, cfg->B * N, 1), dim3(kVClThreads), 0, (cudaStream_t)stream, R, a);
   }
   a.cdf_span = kVChunk;

@@ -366,7 +366,9 @@ def test_tree_build_matches_per_layer_path_and_oracle(wl_name, B, changes, launc
 # acceptance, given the oracle's flat tree
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("mode", [E.ET_ACCEPT_GREEDY, E.ET_ACCEPT_STOCH_POINT, E.ET_ACCEPT_STOCH_DRAFTQ])
-@pytest.mark.parametrize("wl_name,B,V", [("tiny", 4, None), ("llama2-7b", 2, None), ("tiny", 3, 50000)])
+@pytest.mark.parametrize("wl_name,B,V", [("tiny", 4, None), ("llama2-7b", 2, None), ("tiny", 3, 50000),
+                                          # 8 or more sequences: greedy and point-mass walk each path in one cluster
+                                          ("tiny", 8, None), ("llama2-7b", 9, None)])
 def test_verify_matches_oracle(mode, wl_name, B, V):
     """V = 50000 is past one cluster (32768 tokens): one block per 2048-token chunk, merged by the last."""
     wl = W.WORKLOADS[wl_name].with_(B=B, temperature=0.7 if mode == E.ET_ACCEPT_STOCH_DRAFTQ else 1.0)
@@ -443,7 +445,7 @@ def _rejections(ot, ref, b):
     return n + len(ch.get(path[-1], []))
 
 
-@pytest.mark.parametrize("wl_name,B,V", [("llama2-7b", 4, None), ("tiny", 3, 50000)])
+@pytest.mark.parametrize("wl_name,B,V", [("llama2-7b", 4, None), ("tiny", 3, 50000), ("llama2-7b", 8, None)])
 @pytest.mark.parametrize("slope,T,squeeze", [(7.0, 0.5, 3e-5), (4.0, 1.0, 1e-2), (7.0, 1.5, 1e-4), (2.5, 0.5, 1e-3)])
 def test_point_mass_steep_targets(wl_name, B, V, slope, T, squeeze):
     """Steep targets, low temperatures and uniforms pushed toward 1 reject long
