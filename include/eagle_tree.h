@@ -210,6 +210,11 @@ int32_t et_abi_version(void);
  *             the root, 1 + id = candidate id).  Null: rows are in expansion
  *             order, row = b * m_l + slot (what a draft model writes).
  * ws          et_tree_workspace_size(cfg) bytes (see conventions).
+ * Kernels: V <= 32768 takes one thread-block cluster of ceil(V / 4096)
+ * blocks per row when the layer has fewer than 64 rows (B * m_l), else one
+ * 1024-thread block per row (et_set_expand_kernel overrides the choice: the
+ * same children and frontier, log-probs equal up to the order of the softmax
+ * sum); larger V takes a chunked kernel.
  */
 et_status et_tree_expand(const et_tree_cfg *cfg, int32_t layer,
                          const float *logits, int64_t row_stride, const int32_t *row_of_node,
@@ -337,6 +342,23 @@ int32_t et_tree_build_launches(const et_tree_cfg *cfg);
  * exercise that path.  Process-wide; returns the previous bound.
  */
 int64_t et_set_wait_limit(int64_t cycles);
+
+/*
+ * et_set_expand_kernel -- a tuning and test switch, not part of the method.
+ * Chooses the kernel of every later expansion launch with V <= 32768
+ * (et_tree_expand, et_tree_expand_noalloc and et_tree_build's per-layer
+ * form; the one-launch et_tree_build is unaffected): ET_EXPAND_AUTO (the
+ * default: by the layer's row count), ET_EXPAND_CLUSTER (one cluster of
+ * ceil(V / 4096) blocks per row) or ET_EXPAND_BLOCK (one 1024-thread block
+ * per row).  Both select the same children and frontier; their log-probs
+ * agree up to the summation order of the softmax normaliser.
+ * Process-wide; returns the previous choice, or -1 (and changes nothing)
+ * for any other value.
+ */
+#define ET_EXPAND_AUTO    0
+#define ET_EXPAND_CLUSTER 1
+#define ET_EXPAND_BLOCK   2
+int32_t et_set_expand_kernel(int32_t which);
 
 /*
  * et_tree_attention -- attention of the N flattened draft rows over the KV

@@ -25,11 +25,12 @@ ET_BF16, ET_F32 = 0, 1
 ET_ACCEPT_GREEDY, ET_ACCEPT_STOCH_POINT, ET_ACCEPT_STOCH_DRAFTQ = 0, 1, 2
 ATTN_AUTO, ATTN_MMA_SYNC, ATTN_TCGEN05 = 0, 1, 2
 ET_ATTN_INPUTS_READY = 1
+ET_EXPAND_AUTO, ET_EXPAND_CLUSTER, ET_EXPAND_BLOCK = 0, 1, 2
 
 EXPORTED = ("et_num_candidates", "et_layer_expanded", "et_layer_base", "et_tree_workspace_size",
             "et_tree_attention_workspace_size", "et_tree_attention_splits", "et_workspace_init",
             "et_status_string", "et_abi_version", "et_tree_expand", "et_tree_expand_noalloc", "et_tree_rerank", "et_tree_rerank_mask",
-            "et_tree_build", "et_tree_build_launches", "et_set_wait_limit",
+            "et_tree_build", "et_tree_build_launches", "et_set_wait_limit", "et_set_expand_kernel",
             "et_tree_mask_posids", "et_tree_attention", "et_verify_accept", "et_kv_commit", "et_static_tree", "et_lm_head", "et_static_tree_sampled",
             "et_static_tree_workspace_size")
 
@@ -101,6 +102,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                   c_vp]),
         "et_tree_build_launches": (c_i32, [P(TreeCfgC)]),
         "et_set_wait_limit": (c_i64, [c_i64]),
+        "et_set_expand_kernel": (c_i32, [c_i32]),
         "et_tree_attention": (c_i32, [P(AttnShapeC), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                       c_vp, c_vp, c_sz, c_vp]),
         "et_static_tree_workspace_size": (c_sz, [P(StaticCfgC)]),
@@ -317,6 +319,14 @@ def et_tree_build_launches(cfg: TreeCfg) -> int:
 def et_set_wait_limit(cycles: int) -> int:
     """Bound (SM cycles) of device waits of later launches; 0 restores the default. Returns the previous bound."""
     return int(load().et_set_wait_limit(int(cycles)))
+
+
+def et_set_expand_kernel(which: int) -> int:
+    """Kernel of later expansion launches with V <= 32768 (ET_EXPAND_*); returns the previous choice."""
+    prev = int(load().et_set_expand_kernel(int(which)))
+    if prev < 0:
+        raise ValueError(f"unknown expansion kernel {which}")
+    return prev
 
 
 def et_tree_mask_posids(cfg: TreeCfg, tree: TreeBuffers, prefix_len: torch.Tensor, mask: torch.Tensor,

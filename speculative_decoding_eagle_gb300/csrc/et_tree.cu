@@ -4,6 +4,8 @@
 // acceleration: EAGLE-2 lets an RTX 3060 generate faster than an A100"):
 // expansion phase, reranking phase, attention-mask example and the
 // position-encoding sentence.
+#include <atomic>
+
 #include "et_common.cuh"
 
 namespace et {
@@ -635,6 +637,43 @@ __device__ __forceinline__ unsigned long long warp_rank_small(unsigned long long
   return out;
 }
 
+// The warp's (max, sum of exp(z - max)) over its lanes' NV logits each,
+// with the lane's own maximum in lane_max (EAGLE-2 article, expansion phase:
+// the softmax normaliser of a node's draft distribution).  NaN counts as -inf
+// and +inf as FLT_MAX (flag set); padding must already be -inf.  The common
+// case costs a max and an exponential a value: fmaxf skips NaN, and a NaN or
+// +inf leaves a NaN in the lane's sum (inf - inf), so only a warp whose sum
+// turned NaN, or whose maximum is -inf (nothing to show a NaN), sanitises
+// its values and starts again.
+template <int NV>
+__device__ __forceinline__ float2 warp_row_stats(float (&v)[NV], float &lane_max, int &flag) {
+  float m = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < NV; ++e) m = fmaxf(m, v[e]);
+  float Mw = warp_max_f(m);
+  float sum = 0.f;
+  if (Mw > -INFINITY) {
+#pragma unroll
+    for (int e = 0; e < NV; ++e) sum += exp_fast(v[e] - Mw);
+  }
+  if (__any_sync(0xffffffffu, sum != sum || Mw == -INFINITY)) {
+    m = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < NV; ++e) {
+      v[e] = sanitize_logit(v[e], flag);
+      m = fmaxf(m, v[e]);
+    }
+    Mw = warp_max_f(m);
+    sum = 0.f;
+    if (Mw > -INFINITY) {
+#pragma unroll
+      for (int e = 0; e < NV; ++e) sum += exp_fast(v[e] - Mw);
+    }
+  }
+  lane_max = m;
+  return make_float2(Mw, warp_sum(sum));
+}
+
 // The warp's best values at or above tau, at most k of them (value desc,
 // id asc), as ascending (value, id) keys: lane r < n returns the r-th, the
 // other lanes ~0.  v: sanitised values (no NaN), id_of(e): the id of the
@@ -643,10 +682,15 @@ __device__ __forceinline__ unsigned long long warp_rank_small(unsigned long long
 // counting; more than 32 (ties, or a warp holding many of the row's best
 // values) take k rounds of a warp argmin, whose k keys all reach tau then.
 template <int NV, typename IdOf>
-__device__ __forceinline__ unsigned long long warp_best_at_least(const float (&v)[NV], IdOf id_of, float tau, int k,
-                                                                 unsigned long long *cand, int &n) {
-  static_assert(NV <= 31, "a lane's count fits 5 bits");
+__device__ __forceinline__ unsigned long long warp_best_at_least(const float (&v)[NV], float lane_max, IdOf id_of,
+                                                                 float tau, int k, unsigned long long *cand, int &n) {
+  static_assert(NV <= 32, "a lane's values fit one 32-bit mask");
+  constexpr int kCountBits = NV < 32 ? 5 : 6;  // a lane's count, 0 .. NV
   const int lane = threadIdx.x & 31;
+  if (!__any_sync(0xffffffffu, lane_max >= tau)) {  // most warps of a row
+    n = 0;
+    return ~0ull;
+  }
   unsigned int msk = 0u;
 #pragma unroll
   for (int e = 0; e < NV; ++e) msk |= (v[e] >= tau ? 1u : 0u) << e;
@@ -657,10 +701,12 @@ __device__ __forceinline__ unsigned long long warp_best_at_least(const float (&v
     return ~0ull;
   }
   if (nc <= 32) {
-    int pos = warp_excl_prefix<5>(c);
+    int pos = warp_excl_prefix<kCountBits>(c);
+    if (c) {
 #pragma unroll
-    for (int e = 0; e < NV; ++e)
-      if ((msk >> e) & 1u) cand[pos++] = zid_key(v[e], id_of(e));
+      for (int e = 0; e < NV; ++e)
+        if ((msk >> e) & 1u) cand[pos++] = zid_key(v[e], id_of(e));
+    }
     n = nc < k ? nc : k;
     return warp_rank_small(cand, nc, n);
   }
@@ -736,25 +782,10 @@ __device__ __forceinline__ void row_warp_part(float (&v)[4 * kClVec], int base, 
                                               int &flag) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int q = (int)cl_rank(), R = (int)gridDim.x;
-  float best = -INFINITY;
-#pragma unroll
-  for (int u = 0; u < kClVec; ++u) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = 4 * u + j, id = base + u * kClThreads * 4 + t * 4 + j;  // ids >= V are padding (-inf)
-      if (id < V) v[e] = sanitize_logit(v[e], flag);
-      best = fmaxf(best, v[e]);
-    }
-  }
-  const float Mw = warp_max_f(best);
-  float sum = 0.f;
-  if (Mw > -INFINITY) {
-#pragma unroll
-    for (int e = 0; e < 4 * kClVec; ++e) sum += exp_fast(v[e] - Mw);
-  }
-  sum = warp_sum(sum);
+  float lane_max;
+  const float2 st = warp_row_stats(v, lane_max, flag);  // ids >= V are padding (-inf)
   const int list = q * kClWarps + warp;
-  if (lane < R) cl_st_f32x2(cl_map(&sh.pairs[par][list], (uint32_t)lane), Mw, sum);
+  if (lane < R) cl_st_f32x2(cl_map(&sh.pairs[par][list], (uint32_t)lane), st.x, st.y);
   cl_arrive();
   cl_wait();  // every warp's pair is in every block
   const int nl = R * kClWarps;
@@ -765,8 +796,8 @@ __device__ __forceinline__ void row_warp_part(float (&v)[4 * kClVec], int base, 
   const float tau = warp_min_f(above < k ? lm : INFINITY);
   int n = 0;
   const unsigned long long key = warp_best_at_least<4 * kClVec>(
-      v, [&](int e) { return (unsigned int)(base + (e >> 2) * kClThreads * 4 + t * 4 + (e & 3)); }, tau, k,
-      sh.cand[warp], n);
+      v, lane_max, [&](int e) { return (unsigned int)(base + (e >> 2) * kClThreads * 4 + t * 4 + (e & 3)); }, tau,
+      k, sh.cand[warp], n);
   if (lane < n) cl_st_u64(cl_map(&sh.lists[list * k + lane], 0), key);
   if (lane == 0) cl_st_s32(cl_map(&sh.counts[list], 0), n);
 }
@@ -779,50 +810,51 @@ __device__ __forceinline__ void row_warp_part(float (&v)[4 * kClVec], int base, 
 // number at least k (every warp among the k holding the largest maxima sends
 // its maximum); a few more usually: ranked by counting.  More than 32: k
 // rounds of the smallest list head.  nl: warp lists of the row (8 R).
-__device__ __forceinline__ void row_leader_part(ExpandClSmem &sh, int par, int nl, int k, int V, const et_tree &tree,
-                                                long long o0, int parent, long long pkey) {
+__device__ __forceinline__ void row_leader_part(const float2 *pairs, const unsigned long long *lists,
+                                                const int *counts, unsigned long long *cand, float2 *norm, int nl,
+                                                int k, int V, const et_tree &tree, long long o0, int parent,
+                                                long long pkey) {
   const int lane = threadIdx.x & 31;
   if ((threadIdx.x >> 5) == 1) {
-    const float2 pa = lane < nl ? sh.pairs[par][lane] : make_float2(-INFINITY, 0.f);
-    const float2 pb = lane + 32 < nl ? sh.pairs[par][lane + 32] : make_float2(-INFINITY, 0.f);
+    const float2 pa = lane < nl ? pairs[lane] : make_float2(-INFINITY, 0.f);
+    const float2 pb = lane + 32 < nl ? pairs[lane + 32] : make_float2(-INFINITY, 0.f);
     const float M = warp_max_f(fmaxf(pa.x, pb.x));
     float part = 0.f;
     if (M > -INFINITY) {
       part = (pa.x > -INFINITY ? pa.y * expf(pa.x - M) : 0.f) + (pb.x > -INFINITY ? pb.y * expf(pb.x - M) : 0.f);
     }
     const float S = warp_sum(part);
-    if (lane == 0) sh.norm = make_float2(M, (M > -INFINITY) ? logf(S) : 0.f);
+    if (lane == 0) *norm = make_float2(M, (M > -INFINITY) ? logf(S) : 0.f);
     asm volatile("bar.sync 1, 64;" ::: "memory");  // with warp 0: the normaliser is in
     return;
   }
   const int la = lane, lb = lane + 32;
-  const int ca = la < nl ? sh.counts[la] : 0, cb = lb < nl ? sh.counts[lb] : 0;
+  const int ca = la < nl ? counts[la] : 0, cb = lb < nl ? counts[lb] : 0;
   const int nc = (int)__reduce_add_sync(0xffffffffu, (unsigned int)(ca + cb));
   unsigned long long key_r;
-  unsigned long long *cand = sh.cand[0];
   if (nc <= 32) {
     int pos = warp_excl_prefix<7>(ca + cb);
-    for (int j = 0; j < ca; ++j) cand[pos++] = sh.lists[la * k + j];
-    for (int j = 0; j < cb; ++j) cand[pos++] = sh.lists[lb * k + j];
+    for (int j = 0; j < ca; ++j) cand[pos++] = lists[la * k + j];
+    for (int j = 0; j < cb; ++j) cand[pos++] = lists[lb * k + j];
     key_r = warp_rank_small(cand, nc, k);
   } else {
     int pa_ = 0, pb_ = 0;
-    unsigned long long ha = ca > 0 ? sh.lists[la * k] : ~0ull, hb = cb > 0 ? sh.lists[lb * k] : ~0ull;
+    unsigned long long ha = ca > 0 ? lists[la * k] : ~0ull, hb = cb > 0 ? lists[lb * k] : ~0ull;
     key_r = ~0ull;
     for (int r = 0; r < k; ++r) {
       const unsigned long long m = warp_min_u64(ha < hb ? ha : hb);
       if (lane == r) key_r = m;
       if (ha == m) {
         ++pa_;
-        ha = pa_ < ca ? sh.lists[la * k + pa_] : ~0ull;
+        ha = pa_ < ca ? lists[la * k + pa_] : ~0ull;
       } else if (hb == m) {
         ++pb_;
-        hb = pb_ < cb ? sh.lists[lb * k + pb_] : ~0ull;
+        hb = pb_ < cb ? lists[lb * k + pb_] : ~0ull;
       }
     }
   }
   asm volatile("bar.sync 1, 64;" ::: "memory");  // with warp 1
-  const float M = sh.norm.x, logS = sh.norm.y;
+  const float M = norm->x, logS = norm->y;
   if (lane < k) {
     const float z = zid_value(key_r);
     const int id = (int)zid_id(key_r);
@@ -832,6 +864,40 @@ __device__ __forceinline__ void row_leader_part(ExpandClSmem &sh, int par, int n
     tree.cand_parent[o] = parent;
     tree.cand_lp[o] = lp;
     tree.cand_key[o] = add_keys(pkey, fixed_key(lp));
+  }
+}
+
+// The last row of sequence b to finish a layer picks the next layer's
+// frontier: the m_next best children of the layer by rank key (EAGLE-2
+// article, expansion phase: the top-m nodes by path value expand next),
+// written in ascending id order, the unused slots -1.  A child at position e
+// of its row has e better siblings, so only the first m_next of every row can
+// rank below m_next, and among them ranks below m_next are exact.  Every
+// thread of the block takes part.
+template <int NT>
+__device__ __forceinline__ void pick_next_frontier(const ExpandRowArgs &a, int b, unsigned long long *fl, int *sel) {
+  const int t = threadIdx.x;
+  const int nk = a.k < a.m_next ? a.k : a.m_next;
+  const int P = a.m_l * nk;  // <= 1024
+  for (int c = t; c < P; c += NT) {
+    const int rs = c / nk, e = c - rs * nk;
+    const int id = a.base_next + rs * a.k + e;
+    fl[c] = rank_key(ld_cg(a.tree.cand_key + (long long)b * a.C + id), id);
+  }
+  __syncthreads();
+  block_select<NT>(fl, P, a.m_next, [&](int r, unsigned long long key_r) {
+    sel[r] = (int)(key_r & ((1ull << kIdBits) - 1));
+  });
+  __syncthreads();
+  if (t < a.m) {
+    if (t < a.m_next) {
+      int slot = 0;
+      const int mine = sel[t];
+      for (int j = 0; j < a.m_next; ++j) slot += sel[j] < mine ? 1 : 0;
+      a.tree.frontier[b * a.m + slot] = mine;
+    } else {
+      a.tree.frontier[b * a.m + t] = -1;
+    }
   }
 }
 
@@ -878,36 +944,109 @@ __global__ void __launch_bounds__(kClThreads) k_expand_cl(ExpandRowArgs a) {
 
   // ---- the leader's first two warps: the row's top-k and normaliser; write the children ----
   if (warp < 2)
-    row_leader_part(sh, 0, R * kClWarps, k, a.V, a.tree, (long long)b * a.C + a.base_next + s * k, node, pkey);
+    row_leader_part(sh.pairs[0], sh.lists, sh.counts, sh.cand[0], &sh.norm, R * kClWarps, k, a.V, a.tree,
+                    (long long)b * a.C + a.base_next + s * k, node, pkey);
   if (a.m_next <= 0) return;  // last layer: no frontier to pick
 
   // ---- the last row of this sequence picks the next frontier ----
   if (!arrive_last(&a.seq_cnt[b], (unsigned)a.m_l, &last)) return;
-  // A child at position e of its row has e better siblings, so only the
-  // first m_next of every row can rank below m_next, and among them ranks
-  // below m_next are exact.
-  const int nk = k < a.m_next ? k : a.m_next;
-  const int P = a.m_l * nk;  // <= 1024
-  for (int c = t; c < P; c += kClThreads) {
-    const int rs = c / nk, e = c - rs * nk;
-    const int id = a.base_next + rs * k + e;
-    fl[c] = rank_key(ld_cg(a.tree.cand_key + (long long)b * a.C + id), id);
+  pick_next_frontier<kClThreads>(a, b, fl, sel);
+}
+
+// ---------------------------------------------------------------------------
+// expand, one 1024-thread block per expanded row (V <= 32768), for layers of
+// many rows.  The cluster kernel needs 8 blocks of 64 registers a thread per
+// row, so only 4 of its blocks fit an SM and a layer of a few hundred rows
+// runs in several waves of that kernel's latency chain (load, cluster
+// barrier, threshold, cluster barrier, leader).  Here one block holds the
+// whole row in registers (32 logits a thread, the same 128-bit loads) and
+// every exchange is a block barrier: each of the 32 warps forms its (max,
+// sum of exp) and, after one barrier, the k-th largest warp maximum, tau;
+// it sends its best values >= tau (at most k) to shared lists; after a
+// second barrier warps 0 and 1 select and normalise exactly as the cluster
+// leader does.  The children and the frontier are those of k_expand_cl; the
+// log-probs may differ in the last bits (the sum of exp is taken in another
+// order).
+// ---------------------------------------------------------------------------
+constexpr int kWdThreads = 1024;
+constexpr int kWdWarps = kWdThreads / 32;
+constexpr int kWdVec = 8;  // float4 loads a thread: 32 logits
+static_assert(kWdThreads * 4 * kWdVec == kClMaxV, "one block spans the widest row of the cluster kernel");
+
+struct ExpandWdSmem {
+  float2 pairs[kWdWarps];                          // (max, sum of exp) of warp w
+  unsigned long long lists[kWdWarps * kMaxTopk];  // warp w's candidates, ascending, at w * k
+  int counts[kWdWarps];                            // how many
+  unsigned long long cand[kWdWarps][32];           // per-warp selection scratch
+  unsigned long long fl[kMaxM * kMaxTopk];         // the sequence's last row: frontier candidates
+  int sel[kMaxM];
+  float2 norm;                                     // the row's (max, log of the sum of exp)
+  int last;
+};
+
+__global__ void __launch_bounds__(kWdThreads) k_expand_wd(ExpandRowArgs a) {
+  __shared__ ExpandWdSmem sh;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int row = blockIdx.x;
+  const int b = row / a.m_l, s = row - b * a.m_l;
+  const int k = a.k;
+  pdl_wait();     // the previous kernel in the stream has completed
+  pdl_trigger();  // only now may the next kernel launch: at most one waits ahead
+
+  int flag = 0, bad = 0;
+  int node = -1;
+  if (a.layer > 0) {
+    node = a.tree.frontier[b * a.m + s];
+    if (node < 0 || node >= a.C) bad = 1;
   }
-  __syncthreads();
-  block_select<kClThreads>(fl, P, a.m_next, [&](int r, unsigned long long key_r) {
-    sel[r] = (int)(key_r & ((1ull << kIdBits) - 1));
-  });
-  __syncthreads();
-  if (t < a.m) {
-    if (t < a.m_next) {
-      int slot = 0;
-      const int mine = sel[t];
-      for (int j = 0; j < a.m_next; ++j) slot += sel[j] < mine ? 1 : 0;
-      a.tree.frontier[b * a.m + slot] = mine;
+  const float *zrow = nullptr;
+  if (!bad) {
+    long long r = a.row_of_node ? (long long)a.row_of_node[(long long)b * (a.C + 1) + node + 1] : (long long)row;
+    if (r < 0) bad = 1;
+    else zrow = a.logits + r * a.row_stride;
+  }
+  // thread t holds logits 4096 u + 4 t + j, u < 8, j < 4; ids >= V (and a missing row) are -inf
+  float v[4 * kWdVec];
+#pragma unroll
+  for (int u = 0; u < kWdVec; ++u) {
+    const int e0 = u * kWdThreads * 4 + t * 4;
+    if (zrow && a.vec4 && e0 + 3 < a.V) {
+      const float4 f = __ldcs(reinterpret_cast<const float4 *>(zrow + e0));
+      v[4 * u] = f.x; v[4 * u + 1] = f.y; v[4 * u + 2] = f.z; v[4 * u + 3] = f.w;
     } else {
-      a.tree.frontier[b * a.m + t] = -1;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[4 * u + j] = (zrow && e0 + j < a.V) ? __ldcs(zrow + e0 + j) : -INFINITY;
     }
   }
+  // the parent's path key, fetched while the logits are in flight
+  const long long pkey = (warp == 0 && node >= 0 && !bad) ? ld_cg(a.tree.cand_key + (long long)b * a.C + node) : 0ll;
+
+  float lane_max;
+  const float2 st = warp_row_stats(v, lane_max, flag);
+  if (lane == 0) sh.pairs[warp] = st;
+  __syncthreads();
+  // tau: the k-th largest warp maximum (lane j holds warp j's); k distinct
+  // values of the row reach it, so only values >= tau can be in the top k
+  const float lm = sh.pairs[lane].x;
+  int above = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) above += __shfl_sync(0xffffffffu, lm, j) > lm ? 1 : 0;
+  const float tau = warp_min_f(above < k ? lm : INFINITY);
+  int n = 0;
+  const unsigned long long key = warp_best_at_least<4 * kWdVec>(
+      v, lane_max, [&](int e) { return (unsigned int)((e >> 2) * kWdThreads * 4 + t * 4 + (e & 3)); }, tau, k,
+      sh.cand[warp], n);
+  if (lane < n) sh.lists[warp * k + lane] = key;
+  if (lane == 0) sh.counts[warp] = n;
+  if (flag) flag_status(a.dev_status, ET_DEV_NONFINITE);
+  if (bad && t == 0) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
+  __syncthreads();
+  if (warp < 2)
+    row_leader_part(sh.pairs, sh.lists, sh.counts, sh.cand[0], &sh.norm, kWdWarps, k, a.V, a.tree,
+                    (long long)b * a.C + a.base_next + s * k, node, pkey);
+  if (a.m_next <= 0) return;  // last layer: no frontier to pick
+  if (!arrive_last(&a.seq_cnt[b], (unsigned)a.m_l, &sh.last)) return;
+  pick_next_frontier<kWdThreads>(a, b, sh.fl, sh.sel);
 }
 
 // ---------------------------------------------------------------------------
@@ -1166,7 +1305,8 @@ __global__ void __launch_bounds__(kClThreads) k_tree_build(BuildArgs a) {
     cl_arrive();  // release the candidates
     cl_wait();    // every block's candidates have landed in the leader (and every block is done with this layer)
     if (q == 0 && warp < 2)
-      row_leader_part(sh_e, layer & 1, R * kClWarps, k, a.V, a.tree, (long long)b * a.C + base_next + s * k, node, pkey);
+      row_leader_part(sh_e.pairs[layer & 1], sh_e.lists, sh_e.counts, sh_e.cand[0], &sh_e.norm, R * kClWarps, k, a.V,
+                      a.tree, (long long)b * a.C + base_next + s * k, node, pkey);
     if (q == 0 && warp == 0) {
       __threadfence();
       __syncwarp();  // every child of this row is written
@@ -1252,15 +1392,31 @@ extern "C" int32_t et_layer_base(const et_tree_cfg *cfg, int32_t layer) {
 }
 
 // one block per expanded row; same arguments as the chunked kernel
+// Which kernel expands a layer when V <= 32768 (et_set_expand_kernel): the
+// cluster kernel spreads a row over ceil(V / 4096) SMs, which shortens each
+// row's load when the layer has few rows; one block per row saves the
+// cluster barriers and runs more rows at once when it has many.
+static std::atomic<int> g_expand_kernel{ET_EXPAND_AUTO};
+constexpr int kWdMinRows = 64;  // auto: one block per row from this many rows of a layer
+
 static et_status launch_expand_row(const ExpandArgs &c, cudaStream_t stream) {
   ExpandRowArgs a;
   a.logits = c.logits; a.row_stride = c.row_stride; a.row_of_node = c.row_of_node; a.vec4 = c.vec4;
   a.B = c.B; a.V = c.V; a.k = c.k; a.m = c.m; a.C = c.C; a.layer = c.layer; a.m_l = c.m_l;
   a.base_next = c.base_next; a.m_next = c.m_next;
   a.tree = c.tree; a.dev_status = c.dev_status; a.seq_cnt = c.seq_cnt;
+  const int rows = c.B * c.m_l;
+  const int which = g_expand_kernel.load(std::memory_order_relaxed);
+  if (which == ET_EXPAND_BLOCK || (which == ET_EXPAND_AUTO && rows >= kWdMinRows))
+    return et_launch(k_expand_wd, dim3(rows, 1, 1), dim3(kWdThreads, 1, 1), 0, stream, 0, a);
   // one cluster of ceil(V / 4096) CTAs per expanded row
   const int R = (c.V + kClSpan - 1) / kClSpan;
-  return et_launch(k_expand_cl, dim3(R, c.B * c.m_l, 1), dim3(kClThreads, 1, 1), 0, stream, R, a);
+  return et_launch(k_expand_cl, dim3(R, rows, 1), dim3(kClThreads, 1, 1), 0, stream, R, a);
+}
+
+extern "C" int32_t et_set_expand_kernel(int32_t which) {
+  if (which != ET_EXPAND_AUTO && which != ET_EXPAND_CLUSTER && which != ET_EXPAND_BLOCK) return -1;
+  return g_expand_kernel.exchange(which);
 }
 
 static bool tree_ptrs_ok(const et_tree *t) {
@@ -1469,7 +1625,6 @@ extern "C" int32_t et_abi_version(void) { return ET_ABI_VERSION; }
 // ---------------------------------------------------------------------------
 // the bound of device waits (a diagnostic: small values make waits expire)
 // ---------------------------------------------------------------------------
-#include <atomic>
 static constexpr long long kDefaultWaitCycles = 1ll << 32;  // ~2 s at 2 GHz
 static std::atomic<long long> g_wait_cycles{kDefaultWaitCycles};
 

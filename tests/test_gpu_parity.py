@@ -30,6 +30,15 @@ def _lib():
     E.load()
 
 
+@pytest.fixture(params=["cluster", "block"])
+def expand_kernel(request):
+    """Runs the test once with each expansion kernel (a cluster per row, one block per row)."""
+    which = E.ET_EXPAND_CLUSTER if request.param == "cluster" else E.ET_EXPAND_BLOCK
+    prev = E.et_set_expand_kernel(which)
+    yield request.param
+    E.et_set_expand_kernel(prev)
+
+
 def _random_table(rows, V, seed, scale=2.0, ties=False):
     rng = np.random.default_rng(seed)
     if ties:
@@ -52,11 +61,12 @@ EXPAND_CASES = [
     (2, 300, 3, 32, 32, 100, True, 0),         # k = m = 32, many tied logits
     (1, 5000, 4, 1, 1, 4, False, 0),           # chain tree (k = 1)
     (4, 2048, 3, 3, 8, 12, False, 0),          # m > layer width
+    (9, 32000, 3, 10, 8, 40, False, 0),        # 72 rows a layer: the automatic choice is one block per row
 ]
 
 
 @pytest.mark.parametrize("B,V,D,k,m,n,ties,pad", EXPAND_CASES)
-def test_expand_each_layer_matches_oracle(B, V, D, k, m, n, ties, pad):
+def test_expand_each_layer_matches_oracle(B, V, D, k, m, n, ties, pad, expand_kernel):
     cfg = E.TreeCfg(B=B, V=V, depth=D, topk=k, m=m, n=n)
     C = E.et_num_candidates(cfg)
     assert C == O.num_candidates(ocfg(cfg))
@@ -79,7 +89,7 @@ def test_expand_each_layer_matches_oracle(B, V, D, k, m, n, ties, pad):
     assert int(status.item()) == 0
 
 
-def test_expand_slot_ordered_rows_and_nonfinite():
+def test_expand_slot_ordered_rows_and_nonfinite(expand_kernel):
     """Rows given in expansion order (no row map), with NaN / +-inf logits."""
     B, V = 2, 3000
     cfg = E.TreeCfg(B=B, V=V, depth=2, topk=5, m=3, n=8)
@@ -104,7 +114,7 @@ def test_expand_slot_ordered_rows_and_nonfinite():
     assert C == 5 + 15
 
 
-def test_expand_all_neg_inf_row():
+def test_expand_all_neg_inf_row(expand_kernel):
     cfg = E.TreeCfg(B=1, V=100, depth=1, topk=3, m=1, n=3)
     tb = E.TreeBuffers.allocate(cfg)
     ws = E.new_workspace(E.et_tree_workspace_size(cfg))
@@ -116,7 +126,7 @@ def test_expand_all_neg_inf_row():
 
 
 @pytest.mark.parametrize("k", [10, 32])
-def test_expand_constant_row_takes_lowest_ids(k):
+def test_expand_constant_row_takes_lowest_ids(k, expand_kernel):
     # every logit equal: the top-k by (value desc, id asc) are ids 0..k-1, each
     # with log-prob -ln V (k = 32 makes every warp rank more tied keys than it
     # counts directly, so the exact argmin rounds decide)
