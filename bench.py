@@ -742,6 +742,77 @@ def time_attention_batch(B, stream, K, hbm_peak, seed=11, splits=0):
     return res
 
 
+def sweep_logit_tables(wl, rows, gen, with_target=True):
+    """Target and draft logit tables of `rows` nodes drawn on the device with
+    the workload's recipe: target -slope * ln(rank) + N(0, 1) over a random
+    permutation of the vocabulary per node, draft = target + N(0, sigma^2)."""
+    import torch
+    dev = dict(device="cuda", generator=gen)
+    target = torch.empty((rows, wl.V), dtype=torch.float32, device="cuda")
+    draft = torch.empty_like(target)
+    by_rank = -wl.slope * torch.log(torch.arange(1, wl.V + 1, device="cuda", dtype=torch.float32))
+    for r0 in range(0, rows, 256):
+        r1 = min(rows, r0 + 256)
+        perm = torch.argsort(torch.rand((r1 - r0, wl.V), **dev), dim=1)  # the token at each rank
+        z = by_rank.expand(r1 - r0, -1) + torch.randn((r1 - r0, wl.V), **dev)
+        target[r0:r1].scatter_(1, perm, z)
+        draft[r0:r1] = target[r0:r1] + wl.sigma * torch.randn((r1 - r0, wl.V), **dev)
+        del perm, z
+    if not with_target:
+        del target
+        return None, draft
+    return target, draft
+
+
+def time_tree_batch(B, stream, K, hbm_peak, seed=23):
+    """et_tree_build alone at the batched sweep's shape (B sequences, V =
+    32000, depth 6, top-k 10, m 10, n 60; draft logits drawn on the device
+    as in the sweep step, about 2 GB at B = 32): a graph of one build
+    replayed K times.  The algorithmic bytes are the expanded rows' logits
+    (B * sum of m_l rows of V fp32) -- the rerank reads a few KB."""
+    import torch
+    from speculative_decoding_eagle_gb300 import binding as E
+    from speculative_decoding_eagle_gb300 import step as S
+    from speculative_decoding_eagle_gb300 import workloads as W
+    wl = W.WORKLOADS["sweep-7b"].with_(B=B)
+    st = S.VerifyStep(wl)
+    cfg, R = st.cfg, st.C + 1
+    gen = torch.Generator(device="cuda").manual_seed(seed)
+    _, draft = sweep_logit_tables(wl, B * R, gen, with_target=False)
+    row_of_node = (torch.arange(B, dtype=torch.int32, device="cuda")[:, None] * R
+                   + torch.arange(R, dtype=torch.int32, device="cuda")[None, :]).contiguous()
+    prefix = torch.from_numpy(W.prefix_lengths(wl, B)).cuda()
+    st.tree.root_tok = torch.from_numpy(W.root_tokens(wl, B)).cuda()
+    call = lambda: E.et_tree_build(cfg, draft, st.tree, st.ws, row_of_node=row_of_node, prefix_len=prefix,
+                                   mask=st.mask, posids=st.posids, dev_status=st.dev_status, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            call()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        call()
+    g.replay()
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    for _ in range(K):
+        g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / K
+    rows = B * sum(E.et_layer_expanded(cfg, l) for l in range(cfg.depth))
+    tb = rows * wl.V * 4
+    res = {"workload": "sweep-7b", "batch": B, "us_per_tree": round(us, 2), "launches": E.et_tree_build_launches(cfg),
+           "rows_expanded": rows, "logit_bytes": tb, "GBps": round(tb / (us * 1e-6) / 1e9, 1),
+           "frac_of_measured_hbm": round(tb / (us * 1e-6) / 1e9 / hbm_peak, 4), "replays": K,
+           "status": int(st.dev_status.item())}
+    del draft, st
+    torch.cuda.empty_cache()
+    return res
+
+
 def time_sweep_step(B, stream, K, hbm_peak, seed=23):
     """The whole verification step at the batched sweep's shape: B sequences
     of 7B heads with ragged prefixes ~ U{512 .. 16384} (the workload's seeded
@@ -763,18 +834,7 @@ def time_sweep_step(B, stream, K, hbm_peak, seed=23):
     cfg, C = st.cfg, st.C
     R, N = C + 1, cfg.N
     gen = torch.Generator(device="cuda").manual_seed(seed)
-    dev = dict(device="cuda", generator=gen)
-    rows = B * R
-    target = torch.empty((rows, wl.V), dtype=torch.float32, device="cuda")
-    draft = torch.empty_like(target)
-    by_rank = -wl.slope * torch.log(torch.arange(1, wl.V + 1, device="cuda", dtype=torch.float32))
-    for r0 in range(0, rows, 256):
-        r1 = min(rows, r0 + 256)
-        perm = torch.argsort(torch.rand((r1 - r0, wl.V), **dev), dim=1)  # the token at each rank
-        z = by_rank.expand(r1 - r0, -1) + torch.randn((r1 - r0, wl.V), **dev)
-        target[r0:r1].scatter_(1, perm, z)
-        draft[r0:r1] = target[r0:r1] + wl.sigma * torch.randn((r1 - r0, wl.V), **dev)
-        del perm, z
+    target, draft = sweep_logit_tables(wl, B * R, gen)
     prefix = W.prefix_lengths(wl, B)
     kv_row0 = np.concatenate([[0], np.cumsum(wl.Hkv * prefix.astype(np.int64))[:-1]]).astype(np.int64)
     kv_rows = int(wl.Hkv * prefix.astype(np.int64).sum())
@@ -1137,6 +1197,23 @@ def run_attn_batch(args):
     print(json.dumps(res))
 
 
+def run_tree_batch(args):
+    """The tree build alone at the batched sweep's shape (one JSON line); the
+    command the batched expansion's ncu summary is captured from."""
+    import torch
+    from speculative_decoding_eagle_gb300 import binding as E
+    from speculative_decoding_eagle_gb300 import build_lib
+    build_lib.build()
+    E.load()
+    torch.cuda.set_device(0)
+    hbm_peak, _, _ = _peaks()
+    E.et_set_expand_kernel({"auto": E.ET_EXPAND_AUTO, "cluster": E.ET_EXPAND_CLUSTER,
+                            "block": E.ET_EXPAND_BLOCK}[args.expand_kernel])
+    res = time_tree_batch(args.tree_batch, torch.cuda.Stream(), max(4, min(50, args.steps)), hbm_peak)
+    res["expand_kernel"] = args.expand_kernel
+    print(json.dumps(res))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1159,6 +1236,10 @@ def main():
                     help="dram bytes per attention launch from an ncu capture of the same kernel")
     ap.add_argument("--attn-batch", type=int, default=0,
                     help="only time attention alone at the batched sweep's shape with this batch (one JSON line)")
+    ap.add_argument("--tree-batch", type=int, default=0,
+                    help="only time the tree build alone at the batched sweep's shape with this batch (one JSON line)")
+    ap.add_argument("--expand-kernel", default="auto", choices=["auto", "cluster", "block"],
+                    help="expansion kernel of per-layer launches (et_set_expand_kernel)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -1168,6 +1249,8 @@ def main():
         run_split_sweep(args)
     elif args.attn_batch:
         run_attn_batch(args)
+    elif args.tree_batch:
+        run_tree_batch(args)
     else:
         run_gpu(args)
 
