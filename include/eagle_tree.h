@@ -309,8 +309,14 @@ et_status et_tree_rerank_mask(const et_tree_cfg *cfg, et_tree *tree, const int32
  * each finished layer into the running top-n and, after the last layer,
  * writes the flat tree, mask and positions -- when n + max_l(m_l * k) <= 256;
  * otherwise the rerank follows as a second launch (et_tree_rerank_mask's
- * kernel).  Past one cluster, or when the clusters do not fit, it issues the
- * D + 1 launches of the per-layer calls (same results).
+ * kernel).  When the clusters do not all fit (larger batches), it is still
+ * one launch, of a work-queue form: persistent 1024-thread blocks take one
+ * expanded row at a time from a counter, in layer order; a row of layer l
+ * waits (bounded spin) only until its own sequence's layer-l frontier is
+ * written, so different sequences' layers overlap; the last row of a
+ * sequence's layer picks the next frontier, and the last row of its final
+ * layer reranks the sequence and writes its mask and positions.  V > 32768
+ * issues the D + 1 launches of the per-layer calls (same results).
  * et_tree_build_launches(cfg) says which.
  *
  * mask, posids, prefix_len: as in et_tree_rerank_mask; all three null skips
@@ -318,16 +324,17 @@ et_status et_tree_rerank_mask(const et_tree_cfg *cfg, et_tree *tree, const int32
  * ws            et_tree_workspace_size(cfg) bytes (see conventions); the
  *               one-launch form counts each layer's finished rows in it and
  *               leaves those counters at zero.
- * A flag wait that gives up (never expected: all clusters are resident)
- * sets ET_DEV_TIMEOUT; the tree is then invalid and so are the workspace's
- * counters (layers may have finished out of order): zero the workspace again
- * before its next use.
+ * A flag wait that gives up (never expected: all clusters are resident, and
+ * in the work-queue form a row waits only on rows that running blocks took
+ * before it) sets ET_DEV_TIMEOUT; the tree is then invalid and so are the
+ * workspace's counters (layers may have finished out of order): zero the
+ * workspace again before its next use.
  */
 et_status et_tree_build(const et_tree_cfg *cfg, const float *logits, int64_t row_stride,
                         const int32_t *row_of_node, et_tree *tree, const int32_t *prefix_len,
                         uint64_t *mask, int32_t *posids, int32_t *dev_status,
                         void *ws, size_t ws_bytes, et_stream_t stream);
-/* Kernel launches et_tree_build makes for cfg on the current device: 1, 2 or D + 1. */
+/* Kernel launches et_tree_build makes for cfg on the current device: 1, 2 (the rerank apart) or D + 1 (V > 32768). */
 int32_t et_tree_build_launches(const et_tree_cfg *cfg);
 
 /*
@@ -345,15 +352,19 @@ int64_t et_set_wait_limit(int64_t cycles);
 
 /*
  * et_set_expand_kernel -- a tuning and test switch, not part of the method.
- * Chooses the kernel of every later expansion launch with V <= 32768
- * (et_tree_expand, et_tree_expand_noalloc and et_tree_build's per-layer
- * form; the one-launch et_tree_build is unaffected): ET_EXPAND_AUTO (the
- * default: by the layer's row count), ET_EXPAND_CLUSTER (one cluster of
- * ceil(V / 4096) blocks per row) or ET_EXPAND_BLOCK (one 1024-thread block
- * per row).  Both select the same children and frontier; their log-probs
- * agree up to the summation order of the softmax normaliser.
- * Process-wide; returns the previous choice, or -1 (and changes nothing)
- * for any other value.
+ * Chooses the row code of every later expansion with V <= 32768:
+ *   ET_EXPAND_AUTO (the default): et_tree_expand by the layer's row count;
+ *     et_tree_build in one cluster launch when its clusters fit, else in the
+ *     work-queue form;
+ *   ET_EXPAND_CLUSTER: one cluster of ceil(V / 4096) blocks per row;
+ *     et_tree_build in one cluster launch when its clusters fit, else as the
+ *     D + 1 per-layer launches;
+ *   ET_EXPAND_BLOCK: one 1024-thread block per row; et_tree_build always in
+ *     the work-queue form.
+ * (et_tree_expand_noalloc follows et_tree_expand.)  Every choice selects the
+ * same children, frontier and kept tree; log-probs agree up to the
+ * summation order of the softmax normaliser.  Process-wide; returns the
+ * previous choice, or -1 (and changes nothing) for any other value.
  */
 #define ET_EXPAND_AUTO    0
 #define ET_EXPAND_CLUSTER 1

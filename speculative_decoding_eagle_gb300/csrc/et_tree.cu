@@ -875,28 +875,29 @@ __device__ __forceinline__ void row_leader_part(const float2 *pairs, const unsig
 // rank below m_next, and among them ranks below m_next are exact.  Every
 // thread of the block takes part.
 template <int NT>
-__device__ __forceinline__ void pick_next_frontier(const ExpandRowArgs &a, int b, unsigned long long *fl, int *sel) {
+__device__ __forceinline__ void pick_next_frontier(const et_tree &tree, int b, int C, int k, int m, int m_l,
+                                                   int m_next, int base_next, unsigned long long *fl, int *sel) {
   const int t = threadIdx.x;
-  const int nk = a.k < a.m_next ? a.k : a.m_next;
-  const int P = a.m_l * nk;  // <= 1024
+  const int nk = k < m_next ? k : m_next;
+  const int P = m_l * nk;  // <= 1024
   for (int c = t; c < P; c += NT) {
     const int rs = c / nk, e = c - rs * nk;
-    const int id = a.base_next + rs * a.k + e;
-    fl[c] = rank_key(ld_cg(a.tree.cand_key + (long long)b * a.C + id), id);
+    const int id = base_next + rs * k + e;
+    fl[c] = rank_key(ld_cg(tree.cand_key + (long long)b * C + id), id);
   }
   __syncthreads();
-  block_select<NT>(fl, P, a.m_next, [&](int r, unsigned long long key_r) {
+  block_select<NT>(fl, P, m_next, [&](int r, unsigned long long key_r) {
     sel[r] = (int)(key_r & ((1ull << kIdBits) - 1));
   });
   __syncthreads();
-  if (t < a.m) {
-    if (t < a.m_next) {
+  if (t < m) {
+    if (t < m_next) {
       int slot = 0;
       const int mine = sel[t];
-      for (int j = 0; j < a.m_next; ++j) slot += sel[j] < mine ? 1 : 0;
-      a.tree.frontier[b * a.m + slot] = mine;
+      for (int j = 0; j < m_next; ++j) slot += sel[j] < mine ? 1 : 0;
+      tree.frontier[b * m + slot] = mine;
     } else {
-      a.tree.frontier[b * a.m + t] = -1;
+      tree.frontier[b * m + t] = -1;
     }
   }
 }
@@ -950,7 +951,7 @@ __global__ void __launch_bounds__(kClThreads) k_expand_cl(ExpandRowArgs a) {
 
   // ---- the last row of this sequence picks the next frontier ----
   if (!arrive_last(&a.seq_cnt[b], (unsigned)a.m_l, &last)) return;
-  pick_next_frontier<kClThreads>(a, b, fl, sel);
+  pick_next_frontier<kClThreads>(a.tree, b, a.C, a.k, a.m, a.m_l, a.m_next, a.base_next, fl, sel);
 }
 
 // ---------------------------------------------------------------------------
@@ -984,43 +985,32 @@ struct ExpandWdSmem {
   int last;
 };
 
-__global__ void __launch_bounds__(kWdThreads) k_expand_wd(ExpandRowArgs a) {
-  __shared__ ExpandWdSmem sh;
+// One row of the expansion by a whole 1024-thread block (every thread calls
+// it): the row's logits into registers, the warp statistics, the threshold,
+// each warp's candidates, then warps 0 and 1 write the k children at o0..
+// (parent `parent`, path keys from *pkey_src, 0 when null).  zrow null: a
+// missing row, all -inf.  Ends with the children written by warp 0 (no
+// barrier after them).
+__device__ __forceinline__ void wide_row(const float *zrow, int V, int vec4, int k, const et_tree &tree, long long o0,
+                                         int parent, const int64_t *pkey_src, int32_t *dev_status,
+                                         ExpandWdSmem &sh) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int row = blockIdx.x;
-  const int b = row / a.m_l, s = row - b * a.m_l;
-  const int k = a.k;
-  pdl_wait();     // the previous kernel in the stream has completed
-  pdl_trigger();  // only now may the next kernel launch: at most one waits ahead
-
-  int flag = 0, bad = 0;
-  int node = -1;
-  if (a.layer > 0) {
-    node = a.tree.frontier[b * a.m + s];
-    if (node < 0 || node >= a.C) bad = 1;
-  }
-  const float *zrow = nullptr;
-  if (!bad) {
-    long long r = a.row_of_node ? (long long)a.row_of_node[(long long)b * (a.C + 1) + node + 1] : (long long)row;
-    if (r < 0) bad = 1;
-    else zrow = a.logits + r * a.row_stride;
-  }
   // thread t holds logits 4096 u + 4 t + j, u < 8, j < 4; ids >= V (and a missing row) are -inf
   float v[4 * kWdVec];
 #pragma unroll
   for (int u = 0; u < kWdVec; ++u) {
     const int e0 = u * kWdThreads * 4 + t * 4;
-    if (zrow && a.vec4 && e0 + 3 < a.V) {
+    if (zrow && vec4 && e0 + 3 < V) {
       const float4 f = __ldcs(reinterpret_cast<const float4 *>(zrow + e0));
       v[4 * u] = f.x; v[4 * u + 1] = f.y; v[4 * u + 2] = f.z; v[4 * u + 3] = f.w;
     } else {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) v[4 * u + j] = (zrow && e0 + j < a.V) ? __ldcs(zrow + e0 + j) : -INFINITY;
+      for (int j = 0; j < 4; ++j) v[4 * u + j] = (zrow && e0 + j < V) ? __ldcs(zrow + e0 + j) : -INFINITY;
     }
   }
   // the parent's path key, fetched while the logits are in flight
-  const long long pkey = (warp == 0 && node >= 0 && !bad) ? ld_cg(a.tree.cand_key + (long long)b * a.C + node) : 0ll;
-
+  const long long pkey = (warp == 0 && pkey_src) ? ld_cg(pkey_src) : 0ll;
+  int flag = 0;
   float lane_max;
   const float2 st = warp_row_stats(v, lane_max, flag);
   if (lane == 0) sh.pairs[warp] = st;
@@ -1038,15 +1028,37 @@ __global__ void __launch_bounds__(kWdThreads) k_expand_wd(ExpandRowArgs a) {
       sh.cand[warp], n);
   if (lane < n) sh.lists[warp * k + lane] = key;
   if (lane == 0) sh.counts[warp] = n;
-  if (flag) flag_status(a.dev_status, ET_DEV_NONFINITE);
-  if (bad && t == 0) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
+  if (flag) flag_status(dev_status, ET_DEV_NONFINITE);
   __syncthreads();
-  if (warp < 2)
-    row_leader_part(sh.pairs, sh.lists, sh.counts, sh.cand[0], &sh.norm, kWdWarps, k, a.V, a.tree,
-                    (long long)b * a.C + a.base_next + s * k, node, pkey);
+  if (warp < 2) row_leader_part(sh.pairs, sh.lists, sh.counts, sh.cand[0], &sh.norm, kWdWarps, k, V, tree, o0, parent, pkey);
+}
+
+__global__ void __launch_bounds__(kWdThreads) k_expand_wd(ExpandRowArgs a) {
+  __shared__ ExpandWdSmem sh;
+  const int t = threadIdx.x;
+  const int row = blockIdx.x;
+  const int b = row / a.m_l, s = row - b * a.m_l;
+  pdl_wait();     // the previous kernel in the stream has completed
+  pdl_trigger();  // only now may the next kernel launch: at most one waits ahead
+
+  int bad = 0;
+  int node = -1;
+  if (a.layer > 0) {
+    node = a.tree.frontier[b * a.m + s];
+    if (node < 0 || node >= a.C) bad = 1;
+  }
+  const float *zrow = nullptr;
+  if (!bad) {
+    long long r = a.row_of_node ? (long long)a.row_of_node[(long long)b * (a.C + 1) + node + 1] : (long long)row;
+    if (r < 0) bad = 1;
+    else zrow = a.logits + r * a.row_stride;
+  }
+  wide_row(zrow, a.V, a.vec4, a.k, a.tree, (long long)b * a.C + a.base_next + s * a.k, node,
+           (node >= 0 && !bad) ? a.tree.cand_key + (long long)b * a.C + node : nullptr, a.dev_status, sh);
+  if (bad && t == 0) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
   if (a.m_next <= 0) return;  // last layer: no frontier to pick
   if (!arrive_last(&a.seq_cnt[b], (unsigned)a.m_l, &sh.last)) return;
-  pick_next_frontier<kWdThreads>(a, b, sh.fl, sh.sel);
+  pick_next_frontier<kWdThreads>(a.tree, b, a.C, a.k, a.m, a.m_l, a.m_next, a.base_next, sh.fl, sh.sel);
 }
 
 // ---------------------------------------------------------------------------
@@ -1322,6 +1334,120 @@ __global__ void __launch_bounds__(kClThreads) k_tree_build(BuildArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// The whole draft tree in one launch for batches whose clusters do not all
+// fit k_tree_build (EAGLE-2 article: expansion layer after layer, then the
+// reranking phase with the attention mask and positions).  Persistent
+// 1024-thread blocks take work items from a counter: one item per expanded
+// row, in layer-major order (layer, then sequence, then frontier slot), each
+// expanded as k_expand_wd expands a row.  An item of layer l > 0 waits
+// (bounded spin) only for its own sequence's layer-l frontier, so the layers
+// of different sequences overlap and no layer waits for a whole-grid
+// boundary.  The last row of a sequence's layer (arrival counter) picks the
+// next frontier and publishes it with a release flag; the last row of its
+// final layer reranks the sequence in the same block (the rerank kernel's
+// code, 1024 threads) and clears the sequence's flags.  No deadlock
+// whatever the residency: an item waits only on items of earlier layers,
+// which blocks that are already running took before it.  The last block to
+// run out of items re-arms the item counter.
+// ---------------------------------------------------------------------------
+struct FlowArgs {
+  const float *logits;
+  long long row_stride;
+  const int32_t *row_of_node;
+  int vec4;
+  int V, k, m, C, D;
+  int expanded[kMaxDepth];
+  int base[kMaxDepth + 2];
+  int item0[kMaxDepth + 1];  // first item of each layer; item0[D] = the number of items
+  et_tree tree;
+  int32_t *dev_status;
+  unsigned int *layer_cnt;   // [B][kMaxDepth] rows of a layer whose children are written (the last re-arms it)
+  unsigned int *ready;       // [B][kMaxDepth] 1 once the layer's frontier is written (cleared by the rerank)
+  unsigned int *work;        // [2] next item, blocks out of items (both back to 0 at the end)
+  long long wait_cycles;     // bound of a wait for a frontier (et_set_wait_limit)
+  RerankArgs rr;             // the rerank, mask and positions of each sequence
+};
+
+union FlowSmem {
+  ExpandWdSmem e;
+  RerankSmem r;
+};
+
+__device__ __forceinline__ void st_release_u32(unsigned int *p, unsigned int v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(kWdThreads) k_tree_flow(FlowArgs a) {
+  __shared__ FlowSmem sh;
+  __shared__ int s_item, s_last;  // outside the union: read after the barriers that end a phase
+  const int t = threadIdx.x;
+  pdl_wait();     // returns at once: this kernel is launched stream-ordered (see et_tree_build)
+  pdl_trigger();  // every block of this grid is resident before a dependent can launch
+  const int total = a.item0[a.D];
+  for (;;) {
+    if (t == 0) s_item = (int)atomicAdd(a.work, 1u);
+    __syncthreads();
+    const int i = s_item;
+    if (i >= total) break;
+    int l = 0;
+    while (l + 1 < a.D && i >= a.item0[l + 1]) ++l;
+    const int m_l = a.expanded[l];
+    const int j = i - a.item0[l], b = j / m_l, s = j - b * m_l;
+    unsigned int *cnt = a.layer_cnt + (long long)b * kMaxDepth;
+    unsigned int *rdy = a.ready + (long long)b * kMaxDepth;
+    int node = -1, bad = 0;
+    if (l > 0) {
+      // this sequence's frontier of layer l is written
+      if (t == 0 && ld_acquire_u32(rdy + l) == 0u) {
+        const long long t0 = clock64();
+        while (ld_acquire_u32(rdy + l) == 0u) {
+          if (clock64() - t0 > a.wait_cycles) {  // never expected: report, go on (outputs invalid)
+            flag_status(a.dev_status, ET_DEV_TIMEOUT);
+            break;
+          }
+        }
+      }
+      __syncthreads();
+      node = ld_cg(a.tree.frontier + b * a.m + s);  // written in this launch: read through L2
+      if (node < 0 || node >= a.C) bad = 1;
+    }
+    const float *zrow = nullptr;
+    if (!bad) {
+      const long long r = a.row_of_node ? (long long)a.row_of_node[(long long)b * (a.C + 1) + node + 1]
+                                        : (long long)b * m_l + s;
+      if (r < 0) bad = 1;
+      else zrow = a.logits + r * a.row_stride;
+    }
+    wide_row(zrow, a.V, a.vec4, a.k, a.tree, (long long)b * a.C + a.base[l + 1] + s * a.k, node,
+             (node >= 0 && !bad) ? a.tree.cand_key + (long long)b * a.C + node : nullptr, a.dev_status, sh.e);
+    if (bad && t == 0) flag_status(a.dev_status, ET_DEV_BAD_INDEX);
+    if (arrive_last(cnt + l, (unsigned)m_l, &s_last)) {
+      if (l + 1 < a.D) {
+        pick_next_frontier<kWdThreads>(a.tree, b, a.C, a.k, a.m, m_l, a.expanded[l + 1], a.base[l + 1], sh.e.fl,
+                                       sh.e.sel);
+        __syncthreads();  // every frontier slot is written
+        if (t == 0) {
+          __threadfence();
+          st_release_u32(rdy + l + 1, 1u);
+        }
+      } else {
+        // every item of this sequence is done: rerank it, then clear its flags
+        rerank_sequence<kWdThreads>(a.rr, b, sh.r);
+        if (t < a.D) rdy[t] = 0u;
+      }
+    }
+    __syncthreads();  // s_item and the shared memory are free for the next item
+  }
+  if (t == 0) {
+    __threadfence();
+    if (atomicAdd(a.work + 1, 1u) == gridDim.x - 1) {  // every block is out of items
+      a.work[0] = 0u;
+      a.work[1] = 0u;
+    }
+  }
+}
+
 }  // namespace et
 
 using namespace et;
@@ -1344,8 +1470,9 @@ static TreeWs tree_ws_layout(const et_tree_cfg *cfg) {
   const int nch = nchunk_of(cfg->V);
   const int rows = cfg->B * (cfg->m > N ? cfg->m : N);
   w.rows = rows;
-  // counters: [rows] per row, [B] per sequence, [B][kMaxDepth] per layer (et_tree_build)
-  w.cnt_bytes = align256(sizeof(unsigned int) * (size_t)(rows + cfg->B + (size_t)cfg->B * kMaxDepth));
+  // counters: [rows] per row, [B] per sequence, [B][kMaxDepth] per layer and [B][kMaxDepth]
+  // frontier flags (et_tree_build), 2 item counters (et_tree_build's work-queue form)
+  w.cnt_bytes = align256(sizeof(unsigned int) * (size_t)(rows + cfg->B + 2 * (size_t)cfg->B * kMaxDepth + 2));
   const size_t exp_part = sizeof(float) * (size_t)cfg->B * cfg->m * nch * (2 + 2 * cfg->topk);
   const size_t ver_part = sizeof(float) * (size_t)cfg->B * N * nch * 2;
   w.part_off = w.cnt_bytes;
@@ -1456,13 +1583,8 @@ extern "C" et_status et_tree_expand(const et_tree_cfg *cfg, int32_t layer, const
   return et_launch(k_expand, grid, dim3(kExpThreads), smem, (cudaStream_t)stream, 0, a);
 }
 
-static et_status launch_rerank(const et_tree_cfg *cfg, et_tree *tree, int32_t *dev_status, const int32_t *prefix_len,
-                               uint64_t *mask, int32_t *posids, et_stream_t stream) {
-  Geometry g;
-  ET_RETURN_IF(!make_geometry(cfg, &g), ET_ERR_INVALID_ARG);
-  ET_RETURN_IF(!tree || !tree->cand_tok || !tree->cand_parent || !tree->cand_key || !tree->flat_node ||
-                   !tree->flat_tok || !tree->flat_parent || !tree->flat_depth,
-               ET_ERR_INVALID_ARG);
+static RerankArgs rerank_args(const et_tree_cfg *cfg, const Geometry &g, const et_tree *tree, int32_t *dev_status,
+                              const int32_t *prefix_len, uint64_t *mask, int32_t *posids) {
   RerankArgs a;
   a.B = cfg->B; a.C = g.C; a.n = cfg->n; a.N = cfg->n + 1; a.depth = cfg->depth;
   for (int l = 0; l < kMaxDepth + 2; ++l) a.base[l] = (l <= cfg->depth + 1) ? g.base[l] : 0x7fffffff;
@@ -1472,6 +1594,17 @@ static et_status launch_rerank(const et_tree_cfg *cfg, et_tree *tree, int32_t *d
   a.prefix_len = prefix_len;
   a.mask = mask;
   a.posids = posids;
+  return a;
+}
+
+static et_status launch_rerank(const et_tree_cfg *cfg, et_tree *tree, int32_t *dev_status, const int32_t *prefix_len,
+                               uint64_t *mask, int32_t *posids, et_stream_t stream) {
+  Geometry g;
+  ET_RETURN_IF(!make_geometry(cfg, &g), ET_ERR_INVALID_ARG);
+  ET_RETURN_IF(!tree || !tree->cand_tok || !tree->cand_parent || !tree->cand_key || !tree->flat_node ||
+                   !tree->flat_tok || !tree->flat_parent || !tree->flat_depth,
+               ET_ERR_INVALID_ARG);
+  const RerankArgs a = rerank_args(cfg, g, tree, dev_status, prefix_len, mask, posids);
   return et_launch(k_rerank, dim3(cfg->B), dim3(kRrThreads), 0, (cudaStream_t)stream, 0, a);
 }
 
@@ -1518,6 +1651,27 @@ static int tree_build_fits(int clusters, int R) {
   return clusters <= cached_n;
 }
 
+// Blocks of k_tree_flow that the current device holds at once (cached per device).
+static long long flow_blocks() {
+  static std::mutex mu;
+  static int cached_dev = -1;
+  static long long cached_n = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev != cached_dev) {
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_tree_flow, kWdThreads, 0) != cudaSuccess) {
+      cudaGetLastError();
+      return 1;
+    }
+    cached_dev = dev;
+    cached_n = (long long)sms * (per_sm > 0 ? per_sm : 1);
+  }
+  return cached_n;
+}
+
 extern "C" et_status et_tree_build(const et_tree_cfg *cfg, const float *logits, int64_t row_stride,
                                    const int32_t *row_of_node, et_tree *tree, const int32_t *prefix_len,
                                    uint64_t *mask, int32_t *posids, int32_t *dev_status, void *ws, size_t ws_bytes,
@@ -1537,7 +1691,8 @@ extern "C" et_status et_tree_build(const et_tree_cfg *cfg, const float *logits, 
   const int R = (cfg->V + kClSpan - 1) / kClSpan;
   const bool rerank_here = cfg->n + widest <= kClThreads;  // every merge ranks at most one key per thread
   const long long clusters = (long long)cfg->B * (slots + (rerank_here ? 1 : 0));
-  if (cfg->V <= kClMaxV && clusters <= 65535 && tree_build_fits((int)clusters, R)) {
+  const int which = g_expand_kernel.load(std::memory_order_relaxed);
+  if (cfg->V <= kClMaxV && which != ET_EXPAND_BLOCK && clusters <= 65535 && tree_build_fits((int)clusters, R)) {
     BuildArgs a;
     a.logits = logits;
     a.row_stride = row_stride;
@@ -1567,6 +1722,35 @@ extern "C" et_status et_tree_build(const et_tree_cfg *cfg, const float *logits, 
     if (st != ET_OK || rerank_here) return st;
     return launch_rerank(cfg, tree, dev_status, prefix_len, mask, posids, stream);
   }
+  if (cfg->V <= kClMaxV && which != ET_EXPAND_CLUSTER) {  // the clusters do not all fit: the work-queue form
+    static_assert(kWdThreads == kRrThreads, "the flow blocks run the rerank's code");
+    FlowArgs a;
+    a.logits = logits;
+    a.row_stride = row_stride;
+    a.row_of_node = row_of_node;
+    a.vec4 = et_aligned(logits, 16) && (row_stride % 4 == 0);
+    a.V = cfg->V; a.k = cfg->topk; a.m = cfg->m; a.C = g.C; a.D = cfg->depth;
+    long long items = 0;
+    for (int l = 0; l <= kMaxDepth; ++l) {
+      a.item0[l] = (int)items;
+      if (l < cfg->depth) items += (long long)cfg->B * g.expanded[l];
+    }
+    ET_RETURN_IF(items > 0x7fffffffll - 4 * 1024 * 1024, ET_ERR_UNSUPPORTED);
+    for (int l = 0; l < kMaxDepth; ++l) a.expanded[l] = l < cfg->depth ? g.expanded[l] : 0;
+    for (int l = 0; l < kMaxDepth + 2; ++l) a.base[l] = (l <= cfg->depth + 1) ? g.base[l] : 0x7fffffff;
+    a.tree = *tree;
+    a.dev_status = dev_status;
+    unsigned int *counters = reinterpret_cast<unsigned int *>(ws);
+    a.layer_cnt = counters + w.rows + cfg->B;
+    a.ready = a.layer_cnt + (size_t)cfg->B * kMaxDepth;
+    a.work = a.ready + (size_t)cfg->B * kMaxDepth;
+    a.wait_cycles = et_wait_limit_cycles();
+    a.rr = rerank_args(cfg, g, tree, dev_status, prefix_len, mask, posids);
+    // one block per SM can hold (64 registers x 1024 threads); more would only queue
+    const int grid = (int)(items < flow_blocks() ? items : flow_blocks());
+    // stream-ordered, as k_tree_build (blocks spin on flags that other blocks set)
+    return et_launch_ex(false, k_tree_flow, dim3(grid, 1, 1), dim3(kWdThreads, 1, 1), 0, (cudaStream_t)stream, 0, a);
+  }
   for (int l = 0; l < cfg->depth; ++l) {
     const et_status st = et_tree_expand(cfg, l, logits, row_stride, row_of_node, tree, dev_status, ws, ws_bytes,
                                         stream);
@@ -1586,7 +1770,10 @@ extern "C" int32_t et_tree_build_launches(const et_tree_cfg *cfg) {
   const int R = (cfg->V + kClSpan - 1) / kClSpan;
   const bool rerank_here = cfg->n + widest <= kClThreads;
   const long long clusters = (long long)cfg->B * (slots + (rerank_here ? 1 : 0));
-  if (cfg->V <= kClMaxV && clusters <= 65535 && tree_build_fits((int)clusters, R)) return rerank_here ? 1 : 2;
+  const int which = g_expand_kernel.load(std::memory_order_relaxed);
+  if (cfg->V <= kClMaxV && which != ET_EXPAND_BLOCK && clusters <= 65535 && tree_build_fits((int)clusters, R))
+    return rerank_here ? 1 : 2;
+  if (cfg->V <= kClMaxV && which != ET_EXPAND_CLUSTER) return 1;  // the work-queue form
   return cfg->depth + 1;
 }
 

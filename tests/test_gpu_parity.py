@@ -333,6 +333,33 @@ BUILD_CASES = [  # workload, B, changed fields, expected launches (None: whateve
 ]
 
 
+# forms of et_tree_build chosen by et_tree_expand's row code: (expansion kernel, cases)
+FORM_CASES = [
+    # the work-queue form (one block per row, layers of different sequences overlapping, rerank inside)
+    (E.ET_EXPAND_BLOCK, "tiny", 4, {}, 1),
+    (E.ET_EXPAND_BLOCK, "llama2-7b", 1, {}, 1),
+    (E.ET_EXPAND_BLOCK, "llama2-7b", 3, {"n": 100}, 1),
+    (E.ET_EXPAND_BLOCK, "llama2-7b", 1, {"topk": 16, "m": 16}, 1),  # n + the widest layer > 256: still inside
+    (E.ET_EXPAND_BLOCK, "llama2-70b", 1, {}, 1),
+    (E.ET_EXPAND_BLOCK, "llama2-7b", 9, {}, 1),
+    (E.ET_EXPAND_BLOCK, "tiny", 2, {"V": 50000}, 5),  # past one cluster: the per-layer launches
+    # the cluster row code where the one-launch clusters do not fit: the per-layer launches
+    (E.ET_EXPAND_CLUSTER, "llama2-7b", 9, {}, None),
+]
+
+
+@pytest.mark.parametrize("kernel,wl_name,B,changes,launches", FORM_CASES)
+def test_tree_build_forms_match_per_layer_path_and_oracle(kernel, wl_name, B, changes, launches):
+    """et_tree_build with the expansion row code forced: the work-queue form
+    (one block per row) against the per-layer launches of the same row code,
+    bit for bit, twice in a row, and the oracle."""
+    prev = E.et_set_expand_kernel(kernel)
+    try:
+        test_tree_build_matches_per_layer_path_and_oracle(wl_name, B, changes, launches)
+    finally:
+        E.et_set_expand_kernel(prev)
+
+
 @pytest.mark.parametrize("wl_name,B,changes,launches", BUILD_CASES)
 def test_tree_build_matches_per_layer_path_and_oracle(wl_name, B, changes, launches):
     """et_tree_build (all layers and the rerank in one launch, or the rerank

@@ -67,7 +67,15 @@ def test_lm_head_wait_runs_out_then_next_call_is_exact():
     assert np.all(np.abs(out.cpu().numpy() - ref) <= bound)
 
 
-def test_tree_build_frontier_wait_runs_out_then_next_call_is_exact():
+@pytest.fixture(params=["cluster", "block"])
+def build_form(request):
+    """et_tree_build in its cluster form (every cluster resident) and in its work-queue form."""
+    prev = E.et_set_expand_kernel(E.ET_EXPAND_CLUSTER if request.param == "cluster" else E.ET_EXPAND_BLOCK)
+    yield request.param
+    E.et_set_expand_kernel(prev)
+
+
+def test_tree_build_frontier_wait_runs_out_then_next_call_is_exact(build_form):
     wl = W.WORKLOADS["tiny"].with_(B=2)
     one = S.VerifyStep(wl, per_layer=False)
     if E.et_tree_build_launches(one.cfg) not in (1, 2):
