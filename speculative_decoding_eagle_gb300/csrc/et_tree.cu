@@ -876,7 +876,9 @@ __device__ __forceinline__ void row_leader_part(const float2 *pairs, const unsig
 // thread of the block takes part.
 template <int NT>
 __device__ __forceinline__ void pick_next_frontier(const et_tree &tree, int b, int C, int k, int m, int m_l,
-                                                   int m_next, int base_next, unsigned long long *fl, int *sel) {
+                                                   int m_next, int base_next, unsigned long long *fl, int *sel,
+                                                   const int32_t *rmap = nullptr, int *rowof = nullptr,
+                                                   int *frow = nullptr) {
   const int t = threadIdx.x;
   const int nk = k < m_next ? k : m_next;
   const int P = m_l * nk;  // <= 1024
@@ -884,6 +886,7 @@ __device__ __forceinline__ void pick_next_frontier(const et_tree &tree, int b, i
     const int rs = c / nk, e = c - rs * nk;
     const int id = base_next + rs * k + e;
     fl[c] = rank_key(ld_cg(tree.cand_key + (long long)b * C + id), id);
+    if (rmap) rowof[c] = rmap[(long long)b * (C + 1) + id + 1];  // the table row, in the same round
   }
   __syncthreads();
   block_select<NT>(fl, P, m_next, [&](int r, unsigned long long key_r) {
@@ -896,6 +899,10 @@ __device__ __forceinline__ void pick_next_frontier(const et_tree &tree, int b, i
       const int mine = sel[t];
       for (int j = 0; j < m_next; ++j) slot += sel[j] < mine ? 1 : 0;
       tree.frontier[b * m + slot] = mine;
+      if (rmap) {
+        const int rs = (mine - base_next) / k, e = (mine - base_next) - rs * k;
+        frow[b * kMaxM + slot] = rowof[rs * nk + e];
+      }
     } else {
       tree.frontier[b * m + t] = -1;
     }
@@ -980,6 +987,7 @@ struct ExpandWdSmem {
   int counts[kWdWarps];                            // how many
   unsigned long long cand[kWdWarps][32];           // per-warp selection scratch
   unsigned long long fl[kMaxM * kMaxTopk];         // the sequence's last row: frontier candidates
+  int rowof[kMaxM * kMaxTopk];                     // their table rows (the work-queue build)
   int sel[kMaxM];
   float2 norm;                                     // the row's (max, log of the sum of exp)
   int last;
@@ -1365,6 +1373,7 @@ struct FlowArgs {
   unsigned int *layer_cnt;   // [B][kMaxDepth] rows of a layer whose children are written (the last re-arms it)
   unsigned int *ready;       // [B][kMaxDepth] 1 once the layer's frontier is written (cleared by the rerank)
   unsigned int *work;        // [2] next item, blocks out of items (both back to 0 at the end)
+  int *frow;                 // [B][kMaxM] table row of each frontier slot (with row_of_node)
   long long wait_cycles;     // bound of a wait for a frontier (et_set_wait_limit)
   RerankArgs rr;             // the rerank, mask and positions of each sequence
 };
@@ -1409,13 +1418,18 @@ __global__ void __launch_bounds__(kWdThreads) k_tree_flow(FlowArgs a) {
         }
       }
       __syncthreads();
-      node = ld_cg(a.tree.frontier + b * a.m + s);  // written in this launch: read through L2
+    }
+    // the node and its table row (written in this launch by the picker: read through L2, in one round)
+    long long r = (long long)b * m_l + s;
+    if (l > 0) {
+      node = ld_cg(a.tree.frontier + b * a.m + s);
+      if (a.row_of_node) r = ld_cg(a.frow + b * kMaxM + s);
       if (node < 0 || node >= a.C) bad = 1;
+    } else if (a.row_of_node) {
+      r = a.row_of_node[(long long)b * (a.C + 1)];  // the root
     }
     const float *zrow = nullptr;
     if (!bad) {
-      const long long r = a.row_of_node ? (long long)a.row_of_node[(long long)b * (a.C + 1) + node + 1]
-                                        : (long long)b * m_l + s;
       if (r < 0) bad = 1;
       else zrow = a.logits + r * a.row_stride;
     }
@@ -1425,7 +1439,7 @@ __global__ void __launch_bounds__(kWdThreads) k_tree_flow(FlowArgs a) {
     if (arrive_last(cnt + l, (unsigned)m_l, &s_last)) {
       if (l + 1 < a.D) {
         pick_next_frontier<kWdThreads>(a.tree, b, a.C, a.k, a.m, m_l, a.expanded[l + 1], a.base[l + 1], sh.e.fl,
-                                       sh.e.sel);
+                                       sh.e.sel, a.row_of_node, sh.e.rowof, a.frow);
         __syncthreads();  // every frontier slot is written
         if (t == 0) {
           __threadfence();
@@ -1471,8 +1485,10 @@ static TreeWs tree_ws_layout(const et_tree_cfg *cfg) {
   const int rows = cfg->B * (cfg->m > N ? cfg->m : N);
   w.rows = rows;
   // counters: [rows] per row, [B] per sequence, [B][kMaxDepth] per layer and [B][kMaxDepth]
-  // frontier flags (et_tree_build), 2 item counters (et_tree_build's work-queue form)
-  w.cnt_bytes = align256(sizeof(unsigned int) * (size_t)(rows + cfg->B + 2 * (size_t)cfg->B * kMaxDepth + 2));
+  // frontier flags (et_tree_build), 2 item counters and [B][kMaxM] frontier table rows
+  // (et_tree_build's work-queue form)
+  w.cnt_bytes = align256(sizeof(unsigned int) *
+                         (size_t)(rows + cfg->B + 2 * (size_t)cfg->B * kMaxDepth + 2 + (size_t)cfg->B * kMaxM));
   const size_t exp_part = sizeof(float) * (size_t)cfg->B * cfg->m * nch * (2 + 2 * cfg->topk);
   const size_t ver_part = sizeof(float) * (size_t)cfg->B * N * nch * 2;
   w.part_off = w.cnt_bytes;
@@ -1744,6 +1760,7 @@ extern "C" et_status et_tree_build(const et_tree_cfg *cfg, const float *logits, 
     a.layer_cnt = counters + w.rows + cfg->B;
     a.ready = a.layer_cnt + (size_t)cfg->B * kMaxDepth;
     a.work = a.ready + (size_t)cfg->B * kMaxDepth;
+    a.frow = reinterpret_cast<int *>(a.work + 2);
     a.wait_cycles = et_wait_limit_cycles();
     a.rr = rerank_args(cfg, g, tree, dev_status, prefix_len, mask, posids);
     // one block per SM can hold (64 registers x 1024 threads); more would only queue
