@@ -764,18 +764,20 @@ def sweep_logit_tables(wl, rows, gen, with_target=True):
     return target, draft
 
 
-def time_tree_batch(B, stream, K, hbm_peak, seed=23):
+def time_tree_batch(B, stream, K, hbm_peak, seed=23, per_layer=False):
     """et_tree_build alone at the batched sweep's shape (B sequences, V =
     32000, depth 6, top-k 10, m 10, n 60; draft logits drawn on the device
     as in the sweep step, about 2 GB at B = 32): a graph of one build
-    replayed K times.  The algorithmic bytes are the expanded rows' logits
-    (B * sum of m_l rows of V fp32) -- the rerank reads a few KB."""
+    replayed K times (per_layer: D et_tree_expand launches and
+    et_tree_rerank_mask instead).  The algorithmic bytes are the expanded
+    rows' logits (B * sum of m_l rows of V fp32) -- the rerank reads a few
+    KB."""
     import torch
     from speculative_decoding_eagle_gb300 import binding as E
     from speculative_decoding_eagle_gb300 import step as S
     from speculative_decoding_eagle_gb300 import workloads as W
     wl = W.WORKLOADS["sweep-7b"].with_(B=B)
-    st = S.VerifyStep(wl)
+    st = S.VerifyStep(wl, per_layer=per_layer)
     cfg, R = st.cfg, st.C + 1
     gen = torch.Generator(device="cuda").manual_seed(seed)
     _, draft = sweep_logit_tables(wl, B * R, gen, with_target=False)
@@ -783,8 +785,10 @@ def time_tree_batch(B, stream, K, hbm_peak, seed=23):
                    + torch.arange(R, dtype=torch.int32, device="cuda")[None, :]).contiguous()
     prefix = torch.from_numpy(W.prefix_lengths(wl, B)).cuda()
     st.tree.root_tok = torch.from_numpy(W.root_tokens(wl, B)).cuda()
-    call = lambda: E.et_tree_build(cfg, draft, st.tree, st.ws, row_of_node=row_of_node, prefix_len=prefix,
-                                   mask=st.mask, posids=st.posids, dev_status=st.dev_status, stream=stream)
+    inp = S.StepInputs(draft=draft, target=None, row_of_node=row_of_node, root_tok=st.tree.root_tok,
+                       prefix_len=prefix, kv_row0=None, q=None, k_prefix=None, v_prefix=None, k_tree=None,
+                       v_tree=None, uniforms=None, host={})
+    call = lambda: st.build_tree(inp, stream=stream)
     with torch.cuda.stream(stream):
         for _ in range(3):
             call()
@@ -804,7 +808,7 @@ def time_tree_batch(B, stream, K, hbm_peak, seed=23):
     us = e0.elapsed_time(e1) * 1000.0 / K
     rows = B * sum(E.et_layer_expanded(cfg, l) for l in range(cfg.depth))
     tb = rows * wl.V * 4
-    res = {"workload": "sweep-7b", "batch": B, "us_per_tree": round(us, 2), "launches": E.et_tree_build_launches(cfg),
+    res = {"workload": "sweep-7b", "batch": B, "us_per_tree": round(us, 2), "launches": st.launches() - 2,
            "rows_expanded": rows, "logit_bytes": tb, "GBps": round(tb / (us * 1e-6) / 1e9, 1),
            "frac_of_measured_hbm": round(tb / (us * 1e-6) / 1e9 / hbm_peak, 4), "replays": K,
            "status": int(st.dev_status.item())}
@@ -1209,8 +1213,10 @@ def run_tree_batch(args):
     hbm_peak, _, _ = _peaks()
     E.et_set_expand_kernel({"auto": E.ET_EXPAND_AUTO, "cluster": E.ET_EXPAND_CLUSTER,
                             "block": E.ET_EXPAND_BLOCK}[args.expand_kernel])
-    res = time_tree_batch(args.tree_batch, torch.cuda.Stream(), max(4, min(50, args.steps)), hbm_peak)
+    res = time_tree_batch(args.tree_batch, torch.cuda.Stream(), max(4, min(50, args.steps)), hbm_peak,
+                          per_layer=args.per_layer)
     res["expand_kernel"] = args.expand_kernel
+    res["per_layer"] = bool(args.per_layer)
     print(json.dumps(res))
 
 
@@ -1239,7 +1245,9 @@ def main():
     ap.add_argument("--tree-batch", type=int, default=0,
                     help="only time the tree build alone at the batched sweep's shape with this batch (one JSON line)")
     ap.add_argument("--expand-kernel", default="auto", choices=["auto", "cluster", "block"],
-                    help="expansion kernel of per-layer launches (et_set_expand_kernel)")
+                    help="expansion row code (et_set_expand_kernel)")
+    ap.add_argument("--per-layer", action="store_true",
+                    help="with --tree-batch: the tree as D et_tree_expand launches and the rerank")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
