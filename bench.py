@@ -817,6 +817,58 @@ def time_tree_batch(B, stream, K, hbm_peak, seed=23, per_layer=False):
     return res
 
 
+def time_accept_batch(B, stream, K, hbm_peak, seed=23):
+    """et_verify_accept alone (point-mass) at the batched sweep's shape: the
+    tree is built once from the sweep's device-drawn draft logits, then a
+    graph of one acceptance call is replayed K times over the target table.
+    The algorithmic bytes are the logit rows on the accepted paths plus the
+    stop rows (at most D + 1 rows of V fp32 per sequence)."""
+    import torch
+    from speculative_decoding_eagle_gb300 import binding as E
+    from speculative_decoding_eagle_gb300 import step as S
+    from speculative_decoding_eagle_gb300 import workloads as W
+    wl = W.WORKLOADS["sweep-7b"].with_(B=B)
+    st = S.VerifyStep(wl)
+    cfg, R, N = st.cfg, st.C + 1, st.cfg.N
+    gen = torch.Generator(device="cuda").manual_seed(seed)
+    target, draft = sweep_logit_tables(wl, B * R, gen)
+    row_of_node = (torch.arange(B, dtype=torch.int32, device="cuda")[:, None] * R
+                   + torch.arange(R, dtype=torch.int32, device="cuda")[None, :]).contiguous()
+    prefix = torch.from_numpy(W.prefix_lengths(wl, B)).cuda()
+    inp = S.StepInputs(draft=draft, target=target, row_of_node=row_of_node,
+                       root_tok=torch.from_numpy(W.root_tokens(wl, B)).cuda(), prefix_len=prefix, kv_row0=None,
+                       q=None, k_prefix=None, v_prefix=None, k_tree=None, v_tree=None,
+                       uniforms=torch.rand((B, N), device="cuda", generator=gen), host={})
+    st.build_tree(inp, stream=stream)
+    call = lambda: st.accept(inp, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            call()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        call()
+    g.replay()
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    for _ in range(K):
+        g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / K
+    acc = st.accept_len.cpu()
+    rows = int((acc + 1).clamp(max=wl.depth + 1).sum())  # the path rows and each stop row
+    pb = rows * wl.V * 4
+    res = {"workload": "sweep-7b", "batch": B, "accept": "stoch_point", "us_per_call": round(us, 2),
+           "mean_accept_len": round(float(acc.float().mean()), 3), "rows_on_paths": rows, "path_bytes": pb,
+           "GBps": round(pb / (us * 1e-6) / 1e9, 1), "replays": K, "status": int(st.dev_status.item())}
+    del inp, target, draft, st
+    torch.cuda.empty_cache()
+    return res
+
+
 def time_sweep_step(B, stream, K, hbm_peak, seed=23):
     """The whole verification step at the batched sweep's shape: B sequences
     of 7B heads with ragged prefixes ~ U{512 .. 16384} (the workload's seeded
@@ -1220,6 +1272,19 @@ def run_tree_batch(args):
     print(json.dumps(res))
 
 
+def run_accept_batch(args):
+    """Acceptance alone at the batched sweep's shape (one JSON line); the
+    command the batched acceptance's ncu summary is captured from."""
+    import torch
+    from speculative_decoding_eagle_gb300 import binding as E
+    from speculative_decoding_eagle_gb300 import build_lib
+    build_lib.build()
+    E.load()
+    torch.cuda.set_device(0)
+    hbm_peak, _, _ = _peaks()
+    print(json.dumps(time_accept_batch(args.accept_batch, torch.cuda.Stream(), max(4, min(50, args.steps)), hbm_peak)))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1246,6 +1311,8 @@ def main():
                     help="only time the tree build alone at the batched sweep's shape with this batch (one JSON line)")
     ap.add_argument("--expand-kernel", default="auto", choices=["auto", "cluster", "block"],
                     help="expansion row code (et_set_expand_kernel)")
+    ap.add_argument("--accept-batch", type=int, default=0,
+                    help="only time the acceptance alone at the batched sweep's shape with this batch (one JSON line)")
     ap.add_argument("--per-layer", action="store_true",
                     help="with --tree-batch: the tree as D et_tree_expand launches and the rerank")
     args = ap.parse_args()
@@ -1259,6 +1326,8 @@ def main():
         run_attn_batch(args)
     elif args.tree_batch:
         run_tree_batch(args)
+    elif args.accept_batch:
+        run_accept_batch(args)
     else:
         run_gpu(args)
 
