@@ -1635,9 +1635,10 @@ extern "C" et_status et_tree_rerank_mask(const et_tree_cfg *cfg, et_tree *tree, 
   return launch_rerank(cfg, tree, dev_status, prefix_len, mask, posids, stream);
 }
 
-// The whole tree in one launch when every cluster of k_tree_build fits on the
-// GPU at once; otherwise the same work as D expansion launches and the fused
-// rerank launch.
+// The whole tree in one cluster launch (k_tree_build) when every one of its
+// clusters fits on the GPU at once; otherwise in one work-queue launch
+// (k_tree_flow), or, past one cluster (V > 32768), as D expansion launches
+// and the fused rerank launch.
 static int tree_build_fits(int clusters, int R) {
   static std::mutex mu;
   static int cached_dev = -1, cached_R = -1, cached_n = 0;

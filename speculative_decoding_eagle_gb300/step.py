@@ -170,6 +170,7 @@ class VerifyStep:
         MT = -(-(shape.N * G) // 128)
         tiles = -(-shape.max_prefix // 64) + -(-shape.N // 64)
         slots = max(E.et_layer_expanded(self.cfg, l) for l in range(self.cfg.depth)) + 1
+        # the cluster build's blocks; when they do not all fit, the work-queue build holds every SM
         tree_blocks = self.B * slots * -(-self.cfg.V // 4096)
         sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
         return overlap_splits(tiles, self.cfg.depth, auto, self.B * shape.Hkv * MT, 2 * max(0, sms - tree_blocks))
@@ -183,7 +184,8 @@ class VerifyStep:
 
     # the five calls -------------------------------------------------------
     def build_tree(self, inp: StepInputs, stream=None) -> None:
-        """D expansion layers, rerank, mask and positions: one launch (et_tree_build) when its clusters fit."""
+        """D expansion layers, rerank, mask and positions: one launch of et_tree_build (V <= 32768), or the
+        per-layer calls when ``per_layer``."""
         self.tree.root_tok = inp.root_tok
         if self.per_layer:
             for layer in range(self.cfg.depth):
