@@ -541,7 +541,8 @@ def run_gpu(args):
     lm_head = time_lm_head(wl, cfg, stream, K, hbm_peak)
 
     # ---- end to end through the public API with host buffers ----
-    e2e = run_e2e(args, st, sets, wl, stream)
+    e2e = run_e2e(args, st, sets, wl, stream, host_tables=True)
+    e2e["whole_copy"] = run_e2e(args, st, sets, wl, stream, host_tables=False)
 
     launches = st.launches() * args.steps
     out = {
@@ -1102,25 +1103,40 @@ def time_static_tree(wl, cfg, inp, stream, K):
             "GBps": round(nbytes / (us * 1e-6) / 1e9, 1), "sampled_us": round(us_s, 3), "bound": "latency at batch 1"}
 
 
-def run_e2e(args, st, sets, wl, stream):
-    """Steps through the public API with the inputs in pinned host memory:
-    every step copies all of its inputs host -> device and reads its result
-    (accept_len, path, tokens) device -> host.  Double-buffered like a serving
-    loop: step i+1's inputs upload on a copy stream while step i computes,
-    and the host waits for step i-2 (whose buffers it reuses) before issuing
-    step i."""
+def run_e2e(args, st, sets, wl, stream, host_tables=True):
+    """Steps through the public API with the inputs in pinned host memory,
+    each step reading its result (accept_len, path, tokens) device -> host.
+    Double-buffered like a serving loop: step i+1's copies run on a copy
+    stream while step i computes, and the host waits for step i-2 (whose
+    buffers it reuses) before issuing step i.
+
+    host_tables: the draft and target logit tables (one row per candidate
+    node, 131 MB at the 7B shape) stay in pinned host memory and the tree
+    build and the acceptance read only the rows they use over the host link
+    (NVLink-C2C on Grace-Blackwell); everything else is copied each step.
+    Otherwise every input is copied whole."""
+    import dataclasses
     import torch
+    from speculative_decoding_eagle_gb300 import binding as E
     names = ("draft", "target", "row_of_node", "root_tok", "prefix_len", "kv_row0", "q", "k_prefix", "v_prefix",
              "k_tree", "v_tree", "uniforms")
+    tables = ("draft", "target") if host_tables else ()
+    copied_names = tuple(n for n in names if n not in tables)
     nbuf = 2
     R = min(len(sets), 2)
     host = [{n: getattr(sets[r], n).cpu().pin_memory() for n in names} for r in range(R)]
     dev = [sets[0], sets[1] if len(sets) > 1 else sets[0]]
     if dev[1] is dev[0]:
         nbuf = 1
+    # the inputs a step is given: device buffers, with the tables left in host memory
+    step_in = [[dataclasses.replace(dev[k], **{n: host[r][n] for n in tables}) for r in range(R)]
+               for k in range(2)]
     outs = [st.accept_len, st.path, st.tokens]
     host_out = [[t.cpu().pin_memory() for t in outs] for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in host[0].values())
+    h2d = sum(host[0][n].numel() * host[0][n].element_size() for n in copied_names)
+    cfg = st.cfg
+    expanded_rows = cfg.B * sum(E.et_layer_expanded(cfg, l) for l in range(cfg.depth))
+    path_rows = [0]  # target rows the acceptance walks read, summed over the consumed steps
     d2h = sum(t.numel() * t.element_size() for t in host_out[0])
     K = max(3, min(20, args.steps))
     copy_stream = torch.cuda.Stream()
@@ -1132,23 +1148,26 @@ def run_e2e(args, st, sets, wl, stream):
         k = i % nbuf
         if issued[k]:
             done[k].synchronize()  # step i-2 finished: its device inputs and host result buffer are free
-            _ = int(host_out[k][0][0])  # the host consumes that step's result
+            path_rows[0] += int(host_out[k][0].sum()) + cfg.B  # the host consumes that step's result
         with torch.cuda.stream(copy_stream):
-            for n in names:
+            for n in copied_names:
                 getattr(dev[k], n).copy_(host[i % R][n], non_blocking=True)
             copied[k].record(copy_stream)
         with torch.cuda.stream(stream):
             stream.wait_event(copied[k])
-            st.run(dev[k], stream=stream)
+            st.run(step_in[k][i % R], stream=stream)
             for d, hh in zip(outs, host_out[k]):
                 hh.copy_(d, non_blocking=True)
             done[k].record(stream)
         issued[k] = True
 
-    for i in range(2):
+    # warm-up: with the tables in host memory, one untimed pass of K steps (the GPU's first reads of
+    # freshly pinned pages run about twice as slow until their translations are cached)
+    for i in range(K if host_tables else 2):
         one(i)
     torch.cuda.synchronize()
     issued[:] = [False, False]
+    path_rows[0] = 0
     t0 = time.perf_counter()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(copy_stream)
@@ -1158,10 +1177,23 @@ def run_e2e(args, st, sets, wl, stream):
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     ms = max(e0.elapsed_time(e1), wall * 1000.0) / K
-    return {"value": round(1000.0 / ms, 2), "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 4), "steps": K,
-            "h2d_GBps": round(h2d / (ms * 1e-3) / 1e9, 1),
-            "pipeline": "inputs of step i+1 upload while step i computes (two device input sets)"}
+    consumed = K - min(K, nbuf)  # steps whose result the loop read back before the last ones
+    table_bytes = 0
+    if host_tables and consumed > 0:
+        # every expanded draft row; the target rows on the walked paths (8 or more sequences) or every flat row
+        target_rows = path_rows[0] / consumed if cfg.B >= 8 else cfg.B * cfg.N
+        table_bytes = int((expanded_rows + target_rows) * wl.V * 4)
+    out = {"value": round(1000.0 / ms, 2), "unit": "steps/s", "h2d_bytes_per_step": int(h2d + table_bytes),
+           "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 4), "steps": K,
+           "h2d_GBps": round((h2d + table_bytes) / (ms * 1e-3) / 1e9, 1)}
+    if host_tables:
+        out["copied_bytes_per_step"] = int(h2d)
+        out["table_rows_read_bytes_per_step"] = int(table_bytes)
+        out["pipeline"] = ("logit tables stay in pinned host memory, the kernels read the rows they use over the "
+                           "host link; the other inputs of step i+1 copy while step i computes (two device sets)")
+    else:
+        out["pipeline"] = "every input of step i+1 copies while step i computes (two device input sets)"
+    return out
 
 
 def run_reference(args):

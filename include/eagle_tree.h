@@ -203,7 +203,14 @@ int32_t et_abi_version(void);
  * If layer + 1 < D, the frontier of layer + 1 is then the top-m_{l+1} new
  * nodes by (key desc, id asc), written in ascending id order.
  *
- * logits      fp32 table; row r starts at logits + r * row_stride.
+ * logits      fp32 table; row r starts at logits + r * row_stride.  Device
+ *             memory, or page-locked host memory that the GPU addresses
+ *             (cudaHostAlloc / cudaHostRegister): the kernels then read only
+ *             the rows they expand, over the host link (NVLink-C2C on
+ *             Grace-Blackwell), and the node-indexed table never has to be
+ *             copied whole.  Pageable host memory returns ET_ERR_INVALID_ARG
+ *             and launches nothing (cudaPointerGetAttributes decides, on the
+ *             host, before the launch).
  * row_stride  elements between rows (>= V).  With 16-byte aligned `logits`
  *             and row_stride % 4 == 0 the rows are read with 128-bit loads.
  * row_of_node nullable int32 [B, C + 1]: table row of each node (index 0 =
@@ -441,6 +448,12 @@ et_status et_tree_attention(const et_attn_shape *shape,
  *               nullable int32 [B, C+1] (index 1 + node, 0 = root); null:
  *               row = b * N + flat row (the target forward's output order).
  * draft_logits  (DRAFTQ only) same convention with draft_row_of_node.
+ *               Both tables: device memory or page-locked host memory, as the
+ *               logits of et_tree_expand (only the rows the kernels use are
+ *               read).  Greedy and point-mass acceptance walk each sequence's
+ *               accepted path, reading at most D + 1 target rows, when B >= 8;
+ *               otherwise every flat row is read at once (fewer dependent
+ *               reads at small batch).
  * uniforms      fp32 [B, N] in [0, 1) (stochastic modes; nullable for GREEDY).
  * accept_len    int32 [B]: accepted draft tokens (0..D).
  * path          int32 [B, D+1]: flat rows of the accepted path, root first, -1 padded.

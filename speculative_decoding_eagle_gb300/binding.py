@@ -147,6 +147,16 @@ def _ptr(t: Optional[torch.Tensor], dtype=None, what: str = "tensor") -> Optiona
     return t.data_ptr()
 
 
+def _table(t: torch.Tensor, what: str) -> int:
+    """A logit table: fp32 [rows, >=V] with unit inner stride, in device memory or in page-locked host memory
+    (the library reads the rows it needs over the host link)."""
+    if t.dim() != 2 or t.stride(1) != 1 or t.dtype != torch.float32:
+        raise ValueError(f"{what} must be an fp32 [rows, >=V] table with unit inner stride")
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{what} must be a CUDA tensor or a pinned host tensor")
+    return t.data_ptr()
+
+
 def _stream(stream: Optional[torch.cuda.Stream]) -> int:
     s = stream if stream is not None else torch.cuda.current_stream()
     return s.cuda_stream
@@ -249,11 +259,8 @@ def new_workspace(nbytes: int, device="cuda") -> torch.Tensor:
 def et_tree_expand(cfg: TreeCfg, layer: int, logits: torch.Tensor, tree: TreeBuffers, ws: torch.Tensor,
                    row_of_node: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None,
                    stream=None) -> None:
-    if logits.dim() != 2 or logits.stride(1) != 1:
-        raise ValueError("logits must be a [rows, >=V] fp32 table with unit inner stride")
-    if not logits.is_cuda or logits.dtype != torch.float32:
-        raise ValueError("logits must be a CUDA fp32 tensor")
-    st = load().et_tree_expand(ctypes.byref(cfg.c()), layer, logits.data_ptr(), logits.stride(0),
+    lp = _table(logits, "logits")
+    st = load().et_tree_expand(ctypes.byref(cfg.c()), layer, lp, logits.stride(0),
                                _ptr(row_of_node, torch.int32, "row_of_node"), ctypes.byref(tree.c()),
                                _ptr(dev_status, torch.int32, "dev_status"), _ptr(ws, None, "ws"),
                                ws.numel() * ws.element_size(), _stream(stream))
@@ -271,11 +278,8 @@ def et_tree_expand_noalloc(cfg: TreeCfg, layer: int, logits: torch.Tensor, tree:
     4 MiB array the library keeps on each device.  Calls on one device share
     it, so they must not overlap on the GPU.
     """
-    if logits.dim() != 2 or logits.stride(1) != 1:
-        raise ValueError("logits must be a [rows, >=V] fp32 table with unit inner stride")
-    if not logits.is_cuda or logits.dtype != torch.float32:
-        raise ValueError("logits must be a CUDA fp32 tensor")
-    st = load().et_tree_expand_noalloc(ctypes.byref(cfg.c()), layer, logits.data_ptr(), logits.stride(0),
+    lp = _table(logits, "logits")
+    st = load().et_tree_expand_noalloc(ctypes.byref(cfg.c()), layer, lp, logits.stride(0),
                                        _ptr(row_of_node, torch.int32, "row_of_node"), ctypes.byref(tree.c()),
                                        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
     _check("et_tree_expand_noalloc", st)
@@ -300,11 +304,8 @@ def et_tree_build(cfg: TreeCfg, logits: torch.Tensor, tree: TreeBuffers, ws: tor
                   row_of_node: Optional[torch.Tensor] = None, prefix_len: Optional[torch.Tensor] = None,
                   mask: Optional[torch.Tensor] = None, posids: Optional[torch.Tensor] = None,
                   dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
-    if logits.dim() != 2 or logits.stride(1) != 1:
-        raise ValueError("logits must be a [rows, >=V] fp32 table with unit inner stride")
-    if not logits.is_cuda or logits.dtype != torch.float32:
-        raise ValueError("logits must be a CUDA fp32 tensor")
-    st = load().et_tree_build(ctypes.byref(cfg.c()), logits.data_ptr(), logits.stride(0),
+    lp = _table(logits, "logits")
+    st = load().et_tree_build(ctypes.byref(cfg.c()), lp, logits.stride(0),
                               _ptr(row_of_node, torch.int32, "row_of_node"), ctypes.byref(tree.c()),
                               _ptr(prefix_len, torch.int32, "prefix_len"), _ptr(mask, torch.int64, "mask"),
                               _ptr(posids, torch.int32, "posids"), _ptr(dev_status, torch.int32, "dev_status"),
@@ -383,13 +384,12 @@ def et_verify_accept(cfg: TreeCfg, mode: int, tree: TreeBuffers, target_logits: 
                      accept_len: torch.Tensor, path: torch.Tensor, tokens: torch.Tensor, ws: torch.Tensor,
                      target_row_of_node=None, draft_logits=None, draft_row_of_node=None, uniforms=None,
                      dev_status=None, stream=None) -> None:
-    for name, t in (("target_logits", target_logits), ("draft_logits", draft_logits)):
-        if t is not None and (t.dim() != 2 or t.stride(1) != 1 or t.dtype != torch.float32 or not t.is_cuda):
-            raise ValueError(f"{name} must be a CUDA fp32 [rows, >=V] table with unit inner stride")
+    tp = _table(target_logits, "target_logits")
+    dp = None if draft_logits is None else _table(draft_logits, "draft_logits")
     st = load().et_verify_accept(
-        ctypes.byref(cfg.c()), mode, ctypes.byref(tree.c()), target_logits.data_ptr(), target_logits.stride(0),
+        ctypes.byref(cfg.c()), mode, ctypes.byref(tree.c()), tp, target_logits.stride(0),
         _ptr(target_row_of_node, torch.int32, "target_row_of_node"),
-        None if draft_logits is None else draft_logits.data_ptr(),
+        dp,
         0 if draft_logits is None else draft_logits.stride(0),
         _ptr(draft_row_of_node, torch.int32, "draft_row_of_node"), _ptr(uniforms, torch.float32, "uniforms"),
         _ptr(accept_len, torch.int32, "accept_len"), _ptr(path, torch.int32, "path"),

@@ -1507,6 +1507,36 @@ extern "C" size_t et_tree_workspace_size(const et_tree_cfg *cfg) {
 }
 
 // used by et_verify.cu; not part of the ABI
+// A logit table may sit in device memory or in page-locked host memory that
+// the device addresses (the kernels then read only the rows they need over
+// the host link: NVLink-C2C on Grace-Blackwell).  Writes the address the
+// kernels use into *dev; returns 0, launching nothing, for memory the device
+// cannot address (pageable host memory) or a pointer the runtime does not know;
+// 1 for device (or managed) memory, 2 for page-locked host memory.
+extern "C" __attribute__((visibility("hidden"))) int et_internal_table_ptr(const void *p, const void **dev) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) {
+    *dev = p;
+    return 1;
+  }
+  if (at.type == cudaMemoryTypeHost && at.devicePointer) {
+    *dev = at.devicePointer;
+    return 2;
+  }
+  return 0;
+}
+
+static bool table_ptr(const float *p, const float **dev) {
+  const void *d = nullptr;
+  if (!et_internal_table_ptr(p, &d)) return false;
+  *dev = static_cast<const float *>(d);
+  return true;
+}
+
 extern "C" __attribute__((visibility("hidden"))) size_t et_internal_tree_ws(const et_tree_cfg *cfg, size_t *cnt_bytes, size_t *part_off,
                                       size_t *rowstat_off, size_t *dq_off) {
   TreeWs w = tree_ws_layout(cfg);
@@ -1578,6 +1608,7 @@ extern "C" et_status et_tree_expand(const et_tree_cfg *cfg, int32_t layer, const
   ET_RETURN_IF(!ws || ws_bytes < w.total || !et_aligned(ws, 256), ET_ERR_WORKSPACE);
   const int m_l = g.expanded[layer];
   ET_RETURN_IF((long long)cfg->B * m_l > 65535, ET_ERR_UNSUPPORTED);
+  ET_RETURN_IF(!table_ptr(logits, &logits), ET_ERR_INVALID_ARG);  // device, or page-locked host memory
   ExpandArgs a;
   a.logits = logits;
   a.row_stride = row_stride;
@@ -1700,6 +1731,8 @@ extern "C" et_status et_tree_build(const et_tree_cfg *cfg, const float *logits, 
   ET_RETURN_IF((mask || posids) && (!mask || !posids || !prefix_len || !et_aligned(mask, 8)), ET_ERR_INVALID_ARG);
   const TreeWs w = tree_ws_layout(cfg);
   ET_RETURN_IF(!ws || ws_bytes < w.total || !et_aligned(ws, 256), ET_ERR_WORKSPACE);
+  const float *const logits_in = logits;  // the per-layer form resolves the table itself
+  ET_RETURN_IF(!table_ptr(logits, &logits), ET_ERR_INVALID_ARG);  // device, or page-locked host memory
   int slots = 1, widest = 0;
   for (int l = 0; l < cfg->depth; ++l) {
     slots = g.expanded[l] > slots ? g.expanded[l] : slots;
@@ -1770,7 +1803,7 @@ extern "C" et_status et_tree_build(const et_tree_cfg *cfg, const float *logits, 
     return et_launch_ex(false, k_tree_flow, dim3(grid, 1, 1), dim3(kWdThreads, 1, 1), 0, (cudaStream_t)stream, 0, a);
   }
   for (int l = 0; l < cfg->depth; ++l) {
-    const et_status st = et_tree_expand(cfg, l, logits, row_stride, row_of_node, tree, dev_status, ws, ws_bytes,
+    const et_status st = et_tree_expand(cfg, l, logits_in, row_stride, row_of_node, tree, dev_status, ws, ws_bytes,
                                         stream);
     if (st != ET_OK) return st;
   }
@@ -1919,6 +1952,7 @@ extern "C" et_status et_tree_expand_noalloc(const et_tree_cfg *cfg, int32_t laye
   const size_t cnt_bytes = align256(sizeof(unsigned int) * (size_t)(rows + cfg->B));
   const size_t need = cnt_bytes + sizeof(float) * (size_t)rows * nchunk * (2 + 2 * cfg->topk);
   ET_RETURN_IF(need > kExpandScratchBytes, ET_ERR_WORKSPACE);  // beyond the static scratch
+  ET_RETURN_IF(!table_ptr(logits, &logits), ET_ERR_INVALID_ARG);  // device, or page-locked host memory
   void *scratch = nullptr;
   const et_status s = expand_scratch(&scratch);
   if (s != ET_OK) return s;

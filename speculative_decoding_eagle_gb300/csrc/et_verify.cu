@@ -12,6 +12,7 @@
 #include "et_common.cuh"
 #include "et_cdf.cuh"
 
+extern "C" __attribute__((visibility("hidden"))) int et_internal_table_ptr(const void *p, const void **dev);
 extern "C" __attribute__((visibility("hidden"))) size_t et_internal_tree_ws(const et_tree_cfg *cfg, size_t *cnt_bytes, size_t *part_off,
                                       size_t *rowstat_off, size_t *dq_off);
 
@@ -1018,6 +1019,15 @@ extern "C" et_status et_verify_accept(const et_tree_cfg *cfg, et_accept_mode mod
   ET_RETURN_IF(!ws || ws_bytes < need || !et_aligned(ws, 256), ET_ERR_WORKSPACE);
   const int N = cfg->n + 1;
   ET_RETURN_IF((long long)cfg->B * N > 65535, ET_ERR_UNSUPPORTED);
+  {  // the logit tables: device, or page-locked host memory (rows read over the host link)
+    const void *d = nullptr;
+    ET_RETURN_IF(!et_internal_table_ptr(target_logits, &d), ET_ERR_INVALID_ARG);
+    target_logits = static_cast<const float *>(d);
+    if (draft_logits) {
+      ET_RETURN_IF(!et_internal_table_ptr(draft_logits, &d), ET_ERR_INVALID_ARG);
+      draft_logits = static_cast<const float *>(d);
+    }
+  }
   VerifyArgs a;
   a.mode = (int)mode;
   a.B = cfg->B; a.V = cfg->V; a.N = N; a.C = g.C; a.D = cfg->depth;
@@ -1043,7 +1053,11 @@ extern "C" et_status et_verify_accept(const et_tree_cfg *cfg, et_accept_mode mod
     a.cdf_nch = R;
     if (mode == ET_ACCEPT_STOCH_DRAFTQ)
       return et_launch(k_verify_cl<true>, dim3(R, cfg->B * N, 1), dim3(kVClThreads), 0, (cudaStream_t)stream, R, a);
-    if (cfg->B >= kSeqWalkMinB)  // the walk reads at most D + 1 of the N rows per sequence
+    // The walk reads at most D + 1 of the N rows per sequence, one after the
+    // other.  With a target table in host memory it was measured slower in a
+    // serving loop (its dependent reads queue behind the next step's copies on
+    // the host link), so small batches read every row in one round either way.
+    if (cfg->B >= kSeqWalkMinB)
       return et_launch(k_verify_seq, dim3(R, cfg->B, 1), dim3(kVClThreads), 0, (cudaStream_t)stream, R, a);
     return et_launch(k_verify_cl<false>, dim3(R, cfg->B * N, 1), dim3(kVClThreads), 0, (cudaStream_t)stream, R, a);
   }
