@@ -242,3 +242,26 @@ def test_tree_build_argument_checks(lib):
     # past one cluster (V > 32768) the call issues the per-layer launches: D + 1 (else 1 or 2)
     assert lib.et_tree_build_launches(ctypes.byref(E.TreeCfgC(1, 50000, 4, 4, 4, 16, 1.0))) == 5
     assert lib.et_tree_build_launches(ctypes.byref(bad_cfg)) == -1
+
+
+def test_expand_kernel_switch_round_trips_and_refuses_unknown_values(lib):
+    """et_set_expand_kernel is host state only: it returns the previous choice, and -1 (changing nothing)
+    for a value that names no kernel.  et_tree_build_launches follows it for V > 32768 (always the
+    per-layer launches) without touching a device."""
+    prev = lib.et_set_expand_kernel(E.ET_EXPAND_CLUSTER)
+    try:
+        assert prev in (E.ET_EXPAND_AUTO, E.ET_EXPAND_CLUSTER, E.ET_EXPAND_BLOCK)
+        assert lib.et_set_expand_kernel(E.ET_EXPAND_BLOCK) == E.ET_EXPAND_CLUSTER
+        assert lib.et_set_expand_kernel(7) == -1
+        assert lib.et_set_expand_kernel(-1) == -1
+        assert lib.et_set_expand_kernel(E.ET_EXPAND_AUTO) == E.ET_EXPAND_BLOCK  # unchanged by the refusals
+        wide = E.TreeCfgC(1, 50000, 4, 4, 4, 16, 1.0)
+        for which in (E.ET_EXPAND_AUTO, E.ET_EXPAND_CLUSTER, E.ET_EXPAND_BLOCK):
+            lib.et_set_expand_kernel(which)
+            assert lib.et_tree_build_launches(ctypes.byref(wide)) == 5
+        lib.et_set_expand_kernel(E.ET_EXPAND_BLOCK)  # one block per row: always the one work-queue launch
+        assert lib.et_tree_build_launches(ctypes.byref(E.TreeCfgC(3, 1000, 4, 4, 4, 16, 1.0))) == 1
+    finally:
+        lib.et_set_expand_kernel(prev)
+    with pytest.raises(ValueError):
+        E.et_set_expand_kernel(9)
