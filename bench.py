@@ -511,6 +511,7 @@ def run_gpu(args):
             try:
                 shapes.append(time_attention_shape(name, L, stream, K, hbm_peak, bf16_peak))
             except Exception as ex:  # report, keep the main line
+                print(f"attention at {name}, prefix {L}: {ex!r}", file=sys.stderr, flush=True)
                 shapes.append({"workload": name, "prefix": L, "error": str(ex)[:300]})
 
     # ---- attention alone at the batched sweep's shape (7B heads, ragged 512-16384 prefixes) ----
@@ -520,6 +521,7 @@ def run_gpu(args):
             try:
                 batched.append(time_attention_batch(Bs, stream, max(4, min(20, K)), hbm_peak))
             except Exception as ex:  # report, keep the main line
+                print(f"batched attention, batch {Bs}: {ex!r}", file=sys.stderr, flush=True)
                 batched.append({"workload": "sweep-7b", "batch": Bs, "error": str(ex)[:300]})
 
     # ---- the whole step at the batched sweep's shape ----
@@ -529,6 +531,7 @@ def run_gpu(args):
             try:
                 sweep.append(time_sweep_step(Bs, stream, max(3, min(10, K)), hbm_peak))
             except Exception as ex:  # report, keep the main line
+                print(f"sweep step, batch {Bs}: {ex!r}", file=sys.stderr, flush=True)
                 sweep.append({"workload": "sweep-7b", "batch": Bs, "error": str(ex)[:300]})
 
     # ---- KV commit of the accepted paths (the step after acceptance), timed alone ----
