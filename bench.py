@@ -504,35 +504,12 @@ def run_gpu(args):
                     "tree_then_attention_us": round(tree_attn_us, 3),
                     "attention_adds_to_tree_us": round(tree_attn_us - tree_us, 3)}
 
-    # ---- attention alone at the other target shapes (batch 1) ----
-    shapes = []
-    if not args.no_attn_shapes:
-        for name, L in ATTN_SHAPES:
-            try:
-                shapes.append(time_attention_shape(name, L, stream, K, hbm_peak, bf16_peak))
-            except Exception as ex:  # report, keep the main line
-                print(f"attention at {name}, prefix {L}: {ex!r}", file=sys.stderr, flush=True)
-                shapes.append({"workload": name, "prefix": L, "error": str(ex)[:300]})
-
-    # ---- attention alone at the batched sweep's shape (7B heads, ragged 512-16384 prefixes) ----
-    batched = []
-    if not args.no_attn_shapes:
-        for Bs in (16, 32):
-            try:
-                batched.append(time_attention_batch(Bs, stream, max(4, min(20, K)), hbm_peak))
-            except Exception as ex:  # report, keep the main line
-                print(f"batched attention, batch {Bs}: {ex!r}", file=sys.stderr, flush=True)
-                batched.append({"workload": "sweep-7b", "batch": Bs, "error": str(ex)[:300]})
-
-    # ---- the whole step at the batched sweep's shape ----
-    sweep = []
-    if not args.no_attn_shapes:
-        for Bs in (16, 32):
-            try:
-                sweep.append(time_sweep_step(Bs, stream, max(3, min(10, K)), hbm_peak))
-            except Exception as ex:  # report, keep the main line
-                print(f"sweep step, batch {Bs}: {ex!r}", file=sys.stderr, flush=True)
-                sweep.append({"workload": "sweep-7b", "batch": Bs, "error": str(ex)[:300]})
+    # ---- attention alone at the other target shapes, at the batched sweep's shape, and the
+    # batched sweep's whole step: in a child process, so that a failure there cannot end this one ----
+    shapes, batched, sweep = [], [], []
+    if not args.no_attn_shapes and local == 0:  # the child runs on device 0: the first rank's GPU
+        ex = run_extras_child(args)
+        shapes, batched, sweep = ex["tree_attention_shapes"], ex["tree_attention_batched"], ex["sweep_step"]
 
     # ---- KV commit of the accepted paths (the step after acceptance), timed alone ----
     commit = time_kv_commit(st, sets[0], wl, cfg, prefix, stream, K)
@@ -1273,6 +1250,65 @@ def run_split_sweep(args):
                           "GBps": round(abytes / us / 1e3, 1), "launches": K, "input_sets": R}), flush=True)
 
 
+def extras_sections(args, K, hbm_peak, bf16_peak):
+    """The bench line's secondary measurements (each guarded: an error is
+    reported in its entry): attention alone at the other target shapes, at
+    the batched sweep's shape, and the batched sweep's whole step."""
+    import torch
+    stream = torch.cuda.Stream()
+    shapes, batched, sweep = [], [], []
+    for name, L in ATTN_SHAPES:
+        try:
+            shapes.append(time_attention_shape(name, L, stream, K, hbm_peak, bf16_peak))
+        except Exception as ex:  # report, keep the rest
+            print(f"attention at {name}, prefix {L}: {ex!r}", file=sys.stderr, flush=True)
+            shapes.append({"workload": name, "prefix": L, "error": str(ex)[:300]})
+    for Bs in (16, 32):
+        try:
+            batched.append(time_attention_batch(Bs, stream, max(4, min(20, K)), hbm_peak))
+        except Exception as ex:  # report, keep the rest
+            print(f"batched attention, batch {Bs}: {ex!r}", file=sys.stderr, flush=True)
+            batched.append({"workload": "sweep-7b", "batch": Bs, "error": str(ex)[:300]})
+    for Bs in (16, 32):
+        try:
+            sweep.append(time_sweep_step(Bs, stream, max(3, min(10, K)), hbm_peak))
+        except Exception as ex:  # report, keep the rest
+            print(f"sweep step, batch {Bs}: {ex!r}", file=sys.stderr, flush=True)
+            sweep.append({"workload": "sweep-7b", "batch": Bs, "error": str(ex)[:300]})
+    return {"tree_attention_shapes": shapes, "tree_attention_batched": batched, "sweep_step": sweep}
+
+
+def run_extras(args):
+    """--extras: the secondary sections alone, one JSON line (the child process of the main bench)."""
+    import torch
+    from speculative_decoding_eagle_gb300 import binding as E
+    from speculative_decoding_eagle_gb300 import build_lib
+    build_lib.build()
+    E.load()
+    torch.cuda.set_device(0)
+    hbm_peak, bf16_peak, _ = _peaks()
+    print(json.dumps(extras_sections(args, max(8, min(200, args.steps)), hbm_peak, bf16_peak)), flush=True)
+
+
+def run_extras_child(args):
+    """Runs --extras in a child process on the same GPU and returns its sections; a child that fails
+    leaves an error entry in each section instead of ending the bench."""
+    cmd = [sys.executable, os.path.abspath(__file__), "--extras", "--steps", str(args.steps)]
+    env = dict(os.environ)
+    try:
+        p = subprocess.run(cmd, capture_output=True, text=True, timeout=1200, env=env)
+        lines = [ln for ln in p.stdout.splitlines() if ln.startswith("{")]
+        if p.returncode == 0 and lines:
+            sys.stderr.write(p.stderr[-2000:])
+            return json.loads(lines[-1])
+        err = f"child exited {p.returncode}: {p.stderr.strip()[-300:]}"
+    except Exception as ex:
+        err = f"child failed: {ex!r}"[:300]
+    print(err, file=sys.stderr, flush=True)
+    return {"tree_attention_shapes": [{"error": err}], "tree_attention_batched": [{"error": err}],
+            "sweep_step": [{"error": err}]}
+
+
 def run_attn_batch(args):
     """Attention alone at the batched sweep's shape (one JSON line); the
     command the batched attention's ncu summary is captured from."""
@@ -1346,6 +1382,8 @@ def main():
                     help="only time the tree build alone at the batched sweep's shape with this batch (one JSON line)")
     ap.add_argument("--expand-kernel", default="auto", choices=["auto", "cluster", "block"],
                     help="expansion row code (et_set_expand_kernel)")
+    ap.add_argument("--extras", action="store_true",
+                    help="only the secondary sections (other attention shapes, batched attention, sweep steps)")
     ap.add_argument("--accept-batch", type=int, default=0,
                     help="only time the acceptance alone at the batched sweep's shape with this batch (one JSON line)")
     ap.add_argument("--per-layer", action="store_true",
@@ -1363,6 +1401,8 @@ def main():
         run_tree_batch(args)
     elif args.accept_batch:
         run_accept_batch(args)
+    elif args.extras:
+        run_extras(args)
     else:
         run_gpu(args)
 
