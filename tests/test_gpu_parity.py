@@ -360,6 +360,45 @@ def test_tree_build_forms_match_per_layer_path_and_oracle(kernel, wl_name, B, ch
         E.et_set_expand_kernel(prev)
 
 
+@pytest.mark.parametrize("kernel", [E.ET_EXPAND_CLUSTER, E.ET_EXPAND_BLOCK])
+def test_tree_build_nonfinite_logits_both_forms(kernel):
+    """NaN (counted as -inf), +inf (counted as FLT_MAX) and -inf logits in
+    the draft rows, including a whole -inf row: both build forms write what
+    the per-layer launches of the same row code write, bit for bit, and flag
+    ET_DEV_NONFINITE."""
+    prev = E.et_set_expand_kernel(kernel)
+    try:
+        wl = W.WORKLOADS["llama2-7b"].with_(B=3)
+        one = S.VerifyStep(wl, per_layer=False)
+        ref = S.VerifyStep(wl, per_layer=True)
+        h = S.host_inputs(wl, one.C)
+        C = one.C
+        d = h["draft"].copy()
+        rng = np.random.default_rng(7)
+        for b in range(wl.B):
+            for node in range(-1, C, 37):  # the root and every 37th candidate's row
+                row = h["row_of_node"][b, node + 1]
+                cols = rng.integers(0, wl.V, 6)
+                d[row, cols[:2]] = np.nan
+                d[row, cols[2]] = np.inf
+                d[row, cols[3:]] = -np.inf
+            d[h["row_of_node"][b, 5], :] = -np.inf  # a whole row of -inf (a child of the root)
+        h = dict(h, draft=d)
+        inp = S.to_device(wl, h)
+        for st in (one, ref):
+            st.prepare(inp)
+            st.build_tree(inp)
+        torch.cuda.synchronize()
+        got, want = gpu_tree_np(one.tree), gpu_tree_np(ref.tree)
+        for name in want:
+            np.testing.assert_array_equal(got[name], want[name], err_msg=name)
+        np.testing.assert_array_equal(one.mask.cpu().numpy(), ref.mask.cpu().numpy())
+        assert int(one.dev_status.item()) & E.ET_DEV_NONFINITE
+        assert int(ref.dev_status.item()) & E.ET_DEV_NONFINITE
+    finally:
+        E.et_set_expand_kernel(prev)
+
+
 @pytest.mark.parametrize("wl_name,B,changes,launches", BUILD_CASES)
 def test_tree_build_matches_per_layer_path_and_oracle(wl_name, B, changes, launches):
     """et_tree_build (all layers and the rerank in one launch, or the rerank
