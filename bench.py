@@ -1193,7 +1193,11 @@ def run_reference(args):
     out = {"impl": "reference", "metric": "tree-verify steps/s (1 GB300, batch 1) with tree-attention HBM GB/s",
            "value": round(v, 4), "unit": "steps/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(1000.0 / v, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-           "dtype": "f64", "data": "synthetic (seeded)", "config": {"workload": wl.name, "batch": 1},
+           "dtype": "f64", "data": "synthetic (seeded)",
+           "config": {"workload": wl.name, "batch": 1, "V": wl.V, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+                      "prefix": int(wl.prefix), "depth": wl.depth, "topk": wl.topk, "m": wl.m, "n": wl.n,
+                      "accept": "greedy" if "greedy" in wl.accept else "stoch_point",
+                      "parallelism": f"replicas x{world}"},
            "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": base["sample"] if base else "",
                             "value": round(v, 4)},
            "e2e": {"value": round(v, 4), "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
