@@ -489,7 +489,14 @@ def run_gpu(args):
     # the step's own attention (its split count chosen to stream beside the tree build): what it adds to the tree
     tree_attn_us = graph_us(lambda inp: (st.build_tree(inp, stream=stream), st.attention(inp, stream=stream)))
     tree_b = 4 * wl.V * expanded * cfg.B          # one fp32 logits row per expanded node
-    accept_b = 4 * wl.V * cfg.N * cfg.B           # every flat row's target logits
+    accept_b = 4 * wl.V * cfg.N * cfg.B           # every flat row's target logits (what the kernel reads)
+    # the acceptance's algorithmic minimum: the rows on the accepted paths and each stop row
+    path_rows = []
+    for r in range(R):
+        st.accept(sets[r], stream=stream)
+        stream.synchronize()
+        path_rows.append(int((st.accept_len.cpu() + 1).clamp(max=wl.depth + 1).sum()))
+    accept_path_b = int(round(4 * wl.V * sum(path_rows) / len(path_rows)))
     parts = [("et_tree_build", tree_us, tree_b, "latency: D dependent layers, each a DRAM round trip, "
                                                  "two cluster barriers and a cross-cluster handshake"),
              ("et_tree_attention", attn_us, attn_b, "hbm"),
@@ -499,6 +506,8 @@ def run_gpu(args):
                                "bytes": b_, "GBps": round(b_ / (u_ * 1e-6) / 1e9, 1),
                                "frac_hbm": round(b_ / (u_ * 1e-6) / 1e9 / hbm_peak, 4), "bound": bd_}
                               for n_, u_, b_, bd_ in parts],
+                    # bytes the acceptance moves (every flat row) and its algorithmic minimum (the path rows)
+                    "accept_moved_bytes": accept_b, "accept_algorithmic_bytes": accept_path_b,
                     "attention_alone_splits": E.et_tree_attention_splits(sa.shape),
                     "attention_in_step_splits": E.et_tree_attention_splits(st.shape),
                     "tree_then_attention_us": round(tree_attn_us, 3),
