@@ -859,7 +859,7 @@ def time_accept_batch(B, stream, K, hbm_peak, seed=23):
     return res
 
 
-def time_sweep_step(B, stream, K, hbm_peak, seed=23):
+def time_sweep_step(B, stream, K, hbm_peak, seed=23, n=None):
     """The whole verification step at the batched sweep's shape: B sequences
     of 7B heads with ragged prefixes ~ U{512 .. 16384} (the workload's seeded
     lengths), EAGLE-2 trees of depth 6, top-k 10, m 10, n 60, point-mass
@@ -876,6 +876,8 @@ def time_sweep_step(B, stream, K, hbm_peak, seed=23):
     from speculative_decoding_eagle_gb300 import step as S
     from speculative_decoding_eagle_gb300 import workloads as W
     wl = W.WORKLOADS["sweep-7b"].with_(B=B)
+    if n is not None:
+        wl = wl.with_(n=n)
     st = S.VerifyStep(wl)
     cfg, C = st.cfg, st.C
     R, N = C + 1, cfg.N
@@ -921,7 +923,7 @@ def time_sweep_step(B, stream, K, hbm_peak, seed=23):
     attn_us = graph_us(lambda: st.attention(inp, stream=stream))
     accept_us = graph_us(lambda: st.accept(inp, stream=stream))
     attn_b = attention_bytes(wl, prefix)
-    res = {"workload": "sweep-7b", "batch": B, "prefix_mean": round(float(prefix.mean()), 1),
+    res = {"workload": "sweep-7b", "batch": B, "n": cfg.n, "prefix_mean": round(float(prefix.mean()), 1),
            "accept": "stoch_point", "ms_per_step": round(step_us / 1000.0, 4),
            "steps_per_s": round(1e6 / step_us, 1), "sequences_per_s": round(B * 1e6 / step_us, 1),
            "tree_launches": st.launches() - 2, "attention_splits": E.et_tree_attention_splits(st.shape),
@@ -1282,12 +1284,13 @@ def extras_sections(args, K, hbm_peak, bf16_peak):
         except Exception as ex:  # report, keep the rest
             print(f"batched attention, batch {Bs}: {ex!r}", file=sys.stderr, flush=True)
             batched.append({"workload": "sweep-7b", "batch": Bs, "error": str(ex)[:300]})
-    for Bs in (16, 32):
+    # the sweep's grid: batches at the kept-tree size n = 60, then other sizes at batch 32
+    for Bs, n in ((16, 60), (32, 60), (1, 60), (4, 60), (32, 16), (32, 32), (32, 100)):
         try:
-            sweep.append(time_sweep_step(Bs, stream, max(3, min(10, K)), hbm_peak))
+            sweep.append(time_sweep_step(Bs, stream, max(3, min(10, K)), hbm_peak, n=n))
         except Exception as ex:  # report, keep the rest
-            print(f"sweep step, batch {Bs}: {ex!r}", file=sys.stderr, flush=True)
-            sweep.append({"workload": "sweep-7b", "batch": Bs, "error": str(ex)[:300]})
+            print(f"sweep step, batch {Bs}, n {n}: {ex!r}", file=sys.stderr, flush=True)
+            sweep.append({"workload": "sweep-7b", "batch": Bs, "n": n, "error": str(ex)[:300]})
     return {"tree_attention_shapes": shapes, "tree_attention_batched": batched, "sweep_step": sweep}
 
 
