@@ -1284,8 +1284,8 @@ def extras_sections(args, K, hbm_peak, bf16_peak):
         except Exception as ex:  # report, keep the rest
             print(f"batched attention, batch {Bs}: {ex!r}", file=sys.stderr, flush=True)
             batched.append({"workload": "sweep-7b", "batch": Bs, "error": str(ex)[:300]})
-    # the sweep's grid: batches at the kept-tree size n = 60, then other sizes at batch 16
-    for Bs, n in ((1, 60), (4, 60), (16, 60), (32, 60), (16, 16), (16, 32), (16, 100)):
+    # the sweep's grid: batches at the kept-tree size n = 60 and other sizes at batch 16; batch 32 last
+    for Bs, n in ((1, 60), (4, 60), (16, 60), (16, 16), (16, 32), (16, 100), (32, 60)):
         try:
             sweep.append(time_sweep_step(Bs, stream, max(3, min(10, K)), hbm_peak, n=n))
         except Exception as ex:  # report, keep the rest
