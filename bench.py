@@ -1359,6 +1359,20 @@ def run_tree_batch(args):
     print(json.dumps(res))
 
 
+def run_sweep_batch(args):
+    """The batched sweep's whole step at one batch (and --sweep-n kept-tree size), one JSON line; the
+    command the sweep step's launch list is captured from."""
+    import torch
+    from speculative_decoding_eagle_gb300 import binding as E
+    from speculative_decoding_eagle_gb300 import build_lib
+    build_lib.build()
+    E.load()
+    torch.cuda.set_device(0)
+    hbm_peak, _, _ = _peaks()
+    print(json.dumps(time_sweep_step(args.sweep_batch, torch.cuda.Stream(), max(3, min(10, args.steps)), hbm_peak,
+                                     n=args.sweep_n or None)))
+
+
 def run_accept_batch(args):
     """Acceptance alone at the batched sweep's shape (one JSON line); the
     command the batched acceptance's ncu summary is captured from."""
@@ -1400,6 +1414,9 @@ def main():
                     help="expansion row code (et_set_expand_kernel)")
     ap.add_argument("--extras", action="store_true",
                     help="only the secondary sections (other attention shapes, batched attention, sweep steps)")
+    ap.add_argument("--sweep-batch", type=int, default=0,
+                    help="only the batched sweep's whole step at this batch (one JSON line)")
+    ap.add_argument("--sweep-n", type=int, default=0, help="with --sweep-batch: the kept-tree size n")
     ap.add_argument("--accept-batch", type=int, default=0,
                     help="only time the acceptance alone at the batched sweep's shape with this batch (one JSON line)")
     ap.add_argument("--per-layer", action="store_true",
@@ -1417,6 +1434,8 @@ def main():
         run_tree_batch(args)
     elif args.accept_batch:
         run_accept_batch(args)
+    elif args.sweep_batch:
+        run_sweep_batch(args)
     elif args.extras:
         run_extras(args)
     else:
