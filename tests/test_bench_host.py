@@ -63,3 +63,32 @@ def test_recorded_attention_traffic_matches_the_kernel_sources():
     workload's summary must be current."""
     assert bench.recorded_attention_traffic("llama2-7b", 1, 1024) is not None
     assert bench.recorded_attention_traffic("llama2-7b", 1, 999) is None
+
+
+def test_extras_child_failure_becomes_error_entries(monkeypatch):
+    """The default bench runs its secondary sections in a child process; a child that fails (here: a command
+    that exits non-zero at once) must leave an error entry in each section, not end the bench."""
+    import types
+
+    def fake_run(cmd, capture_output, text, timeout, env):
+        assert "--extras" in cmd
+        return types.SimpleNamespace(returncode=3, stdout="", stderr="CUDA error: unspecified launch failure")
+
+    monkeypatch.setattr(bench.subprocess, "run", fake_run)
+    ex = bench.run_extras_child(types.SimpleNamespace(steps=10))
+    for key in ("tree_attention_shapes", "tree_attention_batched", "sweep_step"):
+        assert ex[key] and "error" in ex[key][0] and "exited 3" in ex[key][0]["error"]
+
+
+def test_extras_child_result_is_merged(monkeypatch):
+    import json
+    import types
+    line = json.dumps({"tree_attention_shapes": [{"us_per_launch": 1.0}], "tree_attention_batched": [],
+                       "sweep_step": [{"batch": 32}]})
+
+    def fake_run(cmd, capture_output, text, timeout, env):
+        return types.SimpleNamespace(returncode=0, stdout="noise\n" + line + "\n", stderr="")
+
+    monkeypatch.setattr(bench.subprocess, "run", fake_run)
+    ex = bench.run_extras_child(types.SimpleNamespace(steps=10))
+    assert ex["tree_attention_shapes"] == [{"us_per_launch": 1.0}] and ex["sweep_step"] == [{"batch": 32}]
