@@ -1134,6 +1134,7 @@ struct BuildPick {
 struct RerankRoleSmem {
   unsigned long long ks[256];        // running top-n, then the layer's candidates
   unsigned long long keep[kMaxN];    // the new running top-n, by rank
+  int keep_tok[kMaxN], keep_par[kMaxN];  // their tokens and parents (carried, so the flatten loads nothing)
   int ids[kMaxN];                    // kept candidate ids
   short flat_of[kMaxC];              // flat row of each kept id, -1 otherwise
   int row_par[kMaxN], row_dep[kMaxN];
@@ -1157,19 +1158,35 @@ __device__ void rerank_role(const BuildArgs &a, int b, unsigned int *cnt, Rerank
     __syncthreads();
     const int P = nk + width;  // <= 256 (checked by the host)
     unsigned long long mine = ~0ull;
+    int mtok = -1, mpar = -1;
     if (t < nk) {
       mine = sm.keep[t];
-    } else if (t < P) {
+      mtok = sm.keep_tok[t];
+      mpar = sm.keep_par[t];
+    } else if (t < P) {  // the key, token and parent in one round
       const int id = base_next + (t - nk);
-      mine = rank_key(ld_cg(a.tree.cand_key + (long long)b * C + id), id);
+      const long long o = (long long)b * C + id;
+      mine = rank_key(ld_cg(a.tree.cand_key + o), id);
+      mtok = ld_cg(a.tree.cand_tok + o);
+      mpar = ld_cg(a.tree.cand_parent + o);
     }
     __syncthreads();  // every running key read before ks is rewritten
     sm.ks[t] = mine;
     __syncthreads();
     if (t < P) {
-      int below = 0;
-      for (int j = 0; j < P; ++j) below += sm.ks[j] < mine ? 1 : 0;
-      if (below < n) sm.keep[below] = mine;  // ranks are unique: the running list stays sorted
+      int c4[4] = {0, 0, 0, 0};  // independent counters: short dependency chains
+      int j = 0;
+      for (; j + 4 <= P; j += 4) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) c4[u] += sm.ks[j + u] < mine ? 1 : 0;
+      }
+      for (; j < P; ++j) c4[0] += sm.ks[j] < mine ? 1 : 0;
+      const int below = (c4[0] + c4[1]) + (c4[2] + c4[3]);
+      if (below < n) {  // ranks are unique: the running list stays sorted
+        sm.keep[below] = mine;
+        sm.keep_tok[below] = mtok;
+        sm.keep_par[below] = mpar;
+      }
     }
     nk = P < n ? P : n;
     __syncthreads();
@@ -1182,17 +1199,22 @@ __device__ void rerank_role(const BuildArgs &a, int b, unsigned int *cnt, Rerank
   int myrow = -1, myid = -1;
   if (t < nk) {
     myid = sm.ids[t];
-    int before = 0;
-    for (int j = 0; j < nk; ++j) before += sm.ids[j] < myid ? 1 : 0;
-    myrow = 1 + before;
+    int c4[4] = {0, 0, 0, 0};
+    int j = 0;
+    for (; j + 4 <= nk; j += 4) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) c4[u] += sm.ids[j + u] < myid ? 1 : 0;
+    }
+    for (; j < nk; ++j) c4[0] += sm.ids[j] < myid ? 1 : 0;
+    myrow = 1 + (c4[0] + c4[1]) + (c4[2] + c4[3]);
     sm.flat_of[myid] = (short)myrow;
   }
   __syncthreads();
   const long long fo = (long long)b * N;
   int bad = 0;
   if (t < nk && myrow < N) {
-    const int tok = ld_cg(a.tree.cand_tok + (long long)b * C + myid);
-    const int p = ld_cg(a.tree.cand_parent + (long long)b * C + myid);
+    const int tok = sm.keep_tok[t];  // the merges carried them with the key
+    const int p = sm.keep_par[t];
     int prow = 0;
     if (p >= 0) {
       prow = p < C ? sm.flat_of[p] : -1;
