@@ -86,6 +86,13 @@ __device__ __forceinline__ void cluster_sync_all() {
 constexpr uint32_t kIdescQK = idesc_bf16(kTcRows, kTcKeys, false);
 constexpr uint32_t kIdescPV = idesc_bf16(kTcRows, kTcDim, true);
 
+// 32 lanes x 32 bits x 16 columns (the narrow form of the TMEM loads in et_tc.cuh)
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                 "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+               : "r"(taddr));
+}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -402,10 +409,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int c = 0; c < 64; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(raw[c]));
         } else {
-          const unsigned long long w = tile < nP ? 0ull : ((tile - nP) == 0 ? mw0 : mw1);
+          // keep bits: the first lim keys of the partial prefix tile (0 < lim < 64), else the row's mask word
+          const unsigned long long w = tile < nP ? (1ull << lim) - 1ull : ((tile - nP) == 0 ? mw0 : mw1);
+          const uint32_t w_lo = (uint32_t)w, w_hi = (uint32_t)(w >> 32);
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
-            const bool keep = tile < nP ? (c < lim) : (((w >> c) & 1ull) != 0ull);
+            const bool keep = ((c < 32 ? w_lo : w_hi) & (1u << (c & 31))) != 0u;
             const float v = keep ? __uint_as_float(raw[c]) : -INFINITY;
             raw[c] = __float_as_uint(v);
             mx[c & 3] = fmaxf(mx[c & 3], v);
@@ -420,15 +429,15 @@ __global__ void __launch_bounds__(kThreads, 2)
           if (!warp_wait(bar(B_OFULL), (uint32_t)(j - 1) & 1u, abort_flag, a.wait_cycles)) { ok_rows = false; break; }
           tc_fence_after();
           const float sc = (grow && m_used > -INFINITY) ? ex2(m_used - m_new) : 1.f;
-          uint32_t ov[32];
+          uint32_t ov[16];  // 16 columns at a time: with S's 64 values live, wider chunks spill registers
 #pragma unroll
-          for (int part = 0; part < 4; ++part) {
-            const uint32_t oa = lane_base + kColO + 32 * part;
-            tmem_ld32(oa, ov);
+          for (int part = 0; part < kTcDim / 16; ++part) {
+            const uint32_t oa = lane_base + kColO + 16 * part;
+            tmem_ld16(oa, ov);
             tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * sc);
-            tmem_st32(oa, ov);
+            for (int c = 0; c < 16; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * sc);
+            tmem_st16(oa, ov);
           }
           tmem_wait_st();
           l *= sc;

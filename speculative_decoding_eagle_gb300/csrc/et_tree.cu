@@ -603,6 +603,14 @@ __device__ __forceinline__ float ord_f32(unsigned int o) {
 }
 __device__ __forceinline__ float warp_max_f(float x) { return ord_f32(__reduce_max_sync(0xffffffffu, f32_ord(x))); }
 __device__ __forceinline__ float warp_min_f(float x) { return ord_f32(__reduce_min_sync(0xffffffffu, f32_ord(x))); }
+// How many lanes of the warp hold a larger value than this lane's x (four
+// independent counters: a short dependency chain).
+__device__ __forceinline__ int lanes_above(float x) {
+  int c4[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int j = 0; j < 32; ++j) c4[j & 3] += __shfl_sync(0xffffffffu, x, j) > x ? 1 : 0;
+  return (c4[0] + c4[1]) + (c4[2] + c4[3]);
+}
 // exclusive prefix sum over the warp of c, 0 <= c < 2^BITS
 template <int BITS>
 __device__ __forceinline__ int warp_excl_prefix(int c) {
@@ -790,9 +798,7 @@ __device__ __forceinline__ void row_warp_part(float (&v)[4 * kClVec], int base, 
   cl_wait();  // every warp's pair is in every block
   const int nl = R * kClWarps;
   const float lm = fmaxf(lane < nl ? sh.pairs[par][lane].x : -INFINITY, lane + 32 < nl ? sh.pairs[par][lane + 32].x : -INFINITY);
-  int above = 0;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) above += __shfl_sync(0xffffffffu, lm, j) > lm ? 1 : 0;
+  const int above = lanes_above(lm);
   const float tau = warp_min_f(above < k ? lm : INFINITY);
   int n = 0;
   const unsigned long long key = warp_best_at_least<4 * kClVec>(
@@ -1026,9 +1032,7 @@ __device__ __forceinline__ void wide_row(const float *zrow, int V, int vec4, int
   // tau: the k-th largest warp maximum (lane j holds warp j's); k distinct
   // values of the row reach it, so only values >= tau can be in the top k
   const float lm = sh.pairs[lane].x;
-  int above = 0;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) above += __shfl_sync(0xffffffffu, lm, j) > lm ? 1 : 0;
+  const int above = lanes_above(lm);
   const float tau = warp_min_f(above < k ? lm : INFINITY);
   int n = 0;
   const unsigned long long key = warp_best_at_least<4 * kWdVec>(
