@@ -498,9 +498,9 @@ static bool make_plan(const et_attn_shape *s, AttnPlan *p) {
       // two blocks fit per SM: aim at ~1.7 blocks per SM so that the
       // clusters still find room in one wave (measured on GB300: 6 splits for
       // 40 heads and 5 for 48 row tiles beat both fewer and more), and at
-      // about 4.5 K/V tiles per split: below that the split merge outweighs
-      // the shorter loop (7B heads, prefix 1024, 17 tiles: 11.8 us at 4
-      // splits, 12.4 at 3, 12.8 at 5, 13.3 at 8)
+      // about 3 K/V tiles per split: below that the split merge outweighs
+      // the shorter loop (7B heads, prefix 1024, 17 tiles: 10.45 us at 6
+      // splits, 10.8 at 4 and 5, 11.6 at 3)
       if (S <= 0) {
         S = (int)((17LL * sm_count()) / (10LL * base));
         // a ragged batch whose blocks go out longest prefix first
@@ -511,7 +511,7 @@ static bool make_plan(const et_attn_shape *s, AttnPlan *p) {
           const int waves = (int)((5LL * sm_count() + base - 1) / base);
           if (S < waves) S = waves;
         }
-        const int by_tiles = (2 * T + 8) / 9;  // ceil(T / 4.5)
+        const int by_tiles = (T + 2) / 3;  // ceil(T / 3)
         if (S > by_tiles) S = by_tiles;
         if (S > cap) S = cap;
         if (S > 8) S = 8;  // the portable cluster size (larger clusters are an explicit choice)
