@@ -265,3 +265,19 @@ def test_expand_kernel_switch_round_trips_and_refuses_unknown_values(lib):
         lib.et_set_expand_kernel(prev)
     with pytest.raises(ValueError):
         E.et_set_expand_kernel(9)
+
+
+def test_attention_split_plan_short_prefixes(lib):
+    """The tcgen05 plan gives each split about three K/V tiles at short
+    prefixes (fewer and the split merge outweighs the shorter loop), and at
+    long prefixes the SM count and the portable cluster size bound it."""
+    def splits(**kw):
+        s = dict(B=1, N=61, Hq=32, Hkv=32, d=128, dtype=E.ET_BF16, scale=0.088, max_prefix=1024,
+                 kv_rows=32 * 1024, kv_head_stride=0, num_splits=0, impl=2)
+        s.update(kw)
+        return lib.et_tree_attention_splits(ctypes.byref(E.AttnShapeC(*s.values())))
+    assert splits() == 6                                         # 16 prefix tiles + 1 tree tile: ceil(17 / 3)
+    assert splits(max_prefix=512, kv_rows=32 * 512) == 3         # 9 tiles
+    assert splits(max_prefix=128, kv_rows=32 * 128) == 1         # 3 tiles: at least two a split
+    assert 6 <= splits(max_prefix=4096, kv_rows=32 * 4096) <= 8  # 65 tiles: the SM count and cluster size bound it
+    assert splits(num_splits=5) == 5                             # an explicit count is kept
